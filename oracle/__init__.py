@@ -1,0 +1,272 @@
+"""CPU oracle of the fused optimizer step -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may import
+this package.  It wraps ``oracle.c`` (plain single-threaded C, compiled with gcc and
+``-ffp-contract=off``) through ctypes and numpy; it shares no code with the CUDA library.
+
+Parity status of each function (pins live in ``tests/test_oracle_*.py``):
+  kahan_split / kahan_merge      pinned: exhaustive 2^32 round trip, IEEE bit-pattern fixtures
+  round_bf16                     pinned: torch's round-to-nearest-even bf16 cast
+  encode/decode (u16 codec)      pinned: exhaustive 65536-code round trip, half-step bound,
+                                 monotonicity, hand-derived fixtures (tie to even)
+  nadam_scalars / nadam_step     pinned: Adam step-1 = -lr sign(g), NAdam step-1 closed form,
+                                 torch.optim.Adam/AdamW/NAdam trajectories, zero grad, decay-only
+  factored_step                  pinned: torch.optim.Adafactor special case, rank-1 g^2 gives
+                                 u = sign(g), 1-D step-1 sign, clipped RMS == clip, zero grad
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+_CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-Wall"]
+
+_lock = threading.Lock()
+_lib = None
+
+SMALL_NUMEL = 4096
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into oracle/_build/liboracle.so (gcc); returns the path."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", *_CFLAGS, "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class NadamScalars(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_float) for n in
+                ("lr", "b1", "omb1", "b2", "omb2", "eps", "lr_wd", "c_m", "c_g", "k2")] + \
+               [("decoupled_wd", ctypes.c_int32)]
+
+
+class Scale(ctypes.Structure):
+    _fields_ = [("s_m", ctypes.c_float), ("s_v", ctypes.c_float),
+                ("a_m", ctypes.c_float), ("a_v", ctypes.c_float)]
+
+
+class FactoredScalars(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_float) for n in
+                ("b2t", "alpha", "eps1", "eps2", "clip", "lr_eff", "nwdlr")] + \
+               [("mode", ctypes.c_int32)]
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I64 = ctypes.c_int64
+        F = ctypes.c_float
+        I32 = ctypes.c_int32
+        sig = {
+            "orc_kahan_split": (None, [P, P, P, I64]),
+            "orc_kahan_merge": (None, [P, P, P, I64]),
+            "orc_round_bf16": (None, [P, P, I64]),
+            "orc_inv_scale_m": (F, [F]),
+            "orc_inv_scale_v": (F, [F]),
+            "orc_encode_m": (ctypes.c_uint16, [F, F]),
+            "orc_decode_m": (F, [ctypes.c_uint16, F]),
+            "orc_encode_v": (ctypes.c_uint16, [F, F]),
+            "orc_decode_v": (F, [ctypes.c_uint16, F]),
+            "orc_state_pack": (None, [P, P, P, I64, I32]),
+            "orc_state_unpack": (None, [P, F, P, I64, I32]),
+            "orc_nadam_scalars": (None, [I64, F, F, F, F, F, I32, I32, F,
+                                         ctypes.POINTER(ctypes.c_double), ctypes.POINTER(NadamScalars)]),
+            "orc_grad_absmax": (F, [P, I64]),
+            "orc_nadam_step_tensor": (None, [P, P, P, P, P, I64, ctypes.POINTER(Scale),
+                                             ctypes.POINTER(NadamScalars)]),
+            "orc_nadam_step_fp32": (None, [P, P, P, P, I64, ctypes.POINTER(NadamScalars)]),
+            "orc_factored_scalars": (None, [I64, F, F, F, F, F, F, F, F, I32,
+                                            ctypes.POINTER(FactoredScalars)]),
+            "orc_factored_step_tensor": (F, [P, P, P, I64, I64, I64, P, P,
+                                             ctypes.POINTER(FactoredScalars)]),
+            "orc_factored_step_vector": (F, [P, P, P, I64, P, ctypes.POINTER(FactoredScalars)]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _p(a: np.ndarray | None):
+    if a is None:
+        return None
+    assert a.flags.c_contiguous, "oracle buffers must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u16(a):
+    a = np.ascontiguousarray(a)
+    assert a.dtype == np.uint16
+    return a
+
+
+# ---------------------------------------------------------------- Kahan split / merge, bf16
+def kahan_split(x: np.ndarray):
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    hi = np.empty(x.shape, np.uint16)
+    lo = np.empty(x.shape, np.uint16)
+    _load().orc_kahan_split(_p(x), _p(hi), _p(lo), x.size)
+    return hi, lo
+
+
+def kahan_merge(hi: np.ndarray, lo: np.ndarray) -> np.ndarray:
+    hi, lo = _u16(hi), _u16(lo)
+    out = np.empty(hi.shape, np.float32)
+    _load().orc_kahan_merge(_p(hi), _p(lo), _p(out), hi.size)
+    return out
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, np.uint16)
+    _load().orc_round_bf16(_p(x), _p(out), x.size)
+    return out
+
+
+# ---------------------------------------------------------------- u16 codec
+def inv_scale_m(s: float) -> float:
+    return _load().orc_inv_scale_m(s)
+
+
+def inv_scale_v(s: float) -> float:
+    return _load().orc_inv_scale_v(s)
+
+
+def encode_m(m: float, inv: float) -> int:
+    return _load().orc_encode_m(m, inv)
+
+
+def decode_m(c: int, s: float) -> float:
+    return _load().orc_decode_m(c, s)
+
+
+def encode_v(sv: float, rs: float) -> int:
+    return _load().orc_encode_v(sv, rs)
+
+
+def decode_v(c: int, s: float) -> float:
+    return _load().orc_decode_v(c, s)
+
+
+def state_pack(x: np.ndarray, is_signed: bool):
+    """fp32 moments -> (u16 codes, scale); scale = max |x| (signed) or max x."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    codes = np.empty(x.shape, np.uint16)
+    scale = np.zeros(1, np.float32)
+    _load().orc_state_pack(_p(x), _p(codes), _p(scale), x.size, int(is_signed))
+    return codes, float(scale[0])
+
+
+def state_unpack(codes: np.ndarray, scale: float, is_signed: bool) -> np.ndarray:
+    codes = _u16(codes)
+    out = np.empty(codes.shape, np.float32)
+    _load().orc_state_unpack(_p(codes), scale, _p(out), codes.size, int(is_signed))
+    return out
+
+
+# ---------------------------------------------------------------- NAdam / Adam
+class NadamState:
+    """Oracle state of one group: per-tensor scale records plus the NAdam mu product."""
+
+    def __init__(self, n_tensors: int):
+        self.scales = (Scale * n_tensors)()
+        self.mu_product = ctypes.c_double(1.0)
+
+    def scale(self, i):
+        s = self.scales[i]
+        return s.s_m, s.s_v, s.a_m, s.a_v
+
+
+def nadam_scalars(t, lr, beta1, beta2, eps, wd, decoupled_wd, nesterov, psi, mu_product):
+    """Returns (NadamScalars, new mu_product)."""
+    k = NadamScalars()
+    mp = ctypes.c_double(mu_product)
+    _load().orc_nadam_scalars(int(t), lr, beta1, beta2, eps, wd, int(decoupled_wd), int(nesterov),
+                              psi, ctypes.byref(mp), ctypes.byref(k))
+    return k, mp.value
+
+
+def grad_absmax(g: np.ndarray) -> float:
+    g = _u16(g)
+    return _load().orc_grad_absmax(_p(g), g.size)
+
+
+def nadam_step_tensor(hi, lo, m, v, g, scale: Scale, k: NadamScalars):
+    """In place on numpy buffers: hi/lo uint16 (lo may be None), m/v uint16 codes or float32."""
+    n = hi.size
+    _load().orc_nadam_step_tensor(_p(hi), _p(lo), _p(m), _p(v), _p(_u16(g)), n,
+                                  ctypes.byref(scale), ctypes.byref(k))
+
+
+def nadam_step_fp32(w, m, v, g, k: NadamScalars):
+    _load().orc_nadam_step_fp32(_p(w), _p(m), _p(v), _p(_u16(g)), w.size, ctypes.byref(k))
+
+
+def nadam_group_step(tensors, grads, state: NadamState, t, hp):
+    """One step of a group.  tensors: list of dicts with hi, lo, m, v numpy arrays (in place);
+    grads: list of uint16 arrays; hp: dict lr, beta1, beta2, eps, weight_decay, wd_mode,
+    nesterov, momentum_decay."""
+    k, state.mu_product.value = nadam_scalars(
+        t, hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"],
+        hp["wd_mode"] == 1, hp["nesterov"], hp["momentum_decay"], state.mu_product.value)
+    for i, (tt, g) in enumerate(zip(tensors, grads)):
+        nadam_step_tensor(tt["hi"], tt.get("lo"), tt["m"], tt["v"], g, state.scales[i], k)
+    return k
+
+
+# ---------------------------------------------------------------- factored
+def factored_scalars(t, lr, beta2, decay_rate, eps1, eps2, d, clip, wd, mode):
+    k = FactoredScalars()
+    _load().orc_factored_scalars(int(t), lr, beta2, decay_rate, eps1, eps2, d, clip, wd, int(mode),
+                                 ctypes.byref(k))
+    return k
+
+
+def factored_step_tensor(hi, lo, g, B, R, C, row, col, k: FactoredScalars) -> float:
+    return _load().orc_factored_step_tensor(_p(hi), _p(lo), _p(_u16(g)), B, R, C, _p(row), _p(col),
+                                            ctypes.byref(k))
+
+
+def factored_step_vector(hi, lo, g, V, k: FactoredScalars) -> float:
+    return _load().orc_factored_step_vector(_p(hi), _p(lo), _p(_u16(g)), hi.size, _p(V),
+                                            ctypes.byref(k))
+
+
+def factored_dims(shape):
+    """(factored, B, R, C) for a tensor shape: factored over the last two dims iff ndim >= 2."""
+    shape = tuple(int(s) for s in shape)
+    if len(shape) < 2:
+        return False, 1, 1, int(np.prod(shape)) if shape else 1
+    B = int(np.prod(shape[:-2])) if len(shape) > 2 else 1
+    return True, B, shape[-2], shape[-1]
+
+
+def factored_group_step(tensors, grads, t, hp):
+    """tensors: list of dicts with hi, lo, shape and state 'row','col' (factored) or 'V'."""
+    k = factored_scalars(t, hp["lr"], hp["beta2"], hp["decay_rate"], hp["eps1"], hp["eps2"],
+                         hp["d"], hp["clip_threshold"], hp["weight_decay"], hp["mode"])
+    dens = []
+    for tt, g in zip(tensors, grads):
+        fac, B, R, C = factored_dims(tt["shape"])
+        if fac:
+            dens.append(factored_step_tensor(tt["hi"], tt.get("lo"), g, B, R, C, tt["row"], tt["col"], k))
+        else:
+            dens.append(factored_step_vector(tt["hi"], tt.get("lo"), g, tt["V"], k))
+    return k, dens

@@ -1,0 +1,468 @@
+/*
+ * oracle.c -- plain, slow, single-threaded CPU oracle of the fused optimizer step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or call this file:
+ * only the tests, the smoke check and the benchmark's CPU-baseline leg use it.  It shares no
+ * code, header, table or constant generator with the CUDA library.
+ *
+ * Arithmetic.  The pages fix fp32 for the update: the master weight is an f32 value that is
+ * restored bit-identically from its bf16 upper half and the 16 low bits ("Kahan summation for
+ * Adafactor-optimized Flux FFT", sd-scripts PR #2159, first comment), and the printed fused
+ * Adafactor step casts grad and weight to float32 before updating ("Fused backward pass" commit,
+ * library/adafactor_fused.py, adafactor_step_param).  So every per-element operation below is a
+ * single IEEE fp32 operation rounded to nearest-even, in the order written, with no contraction
+ * (build with -ffp-contract=off).  Means over rows, columns and tensors are summed in double and
+ * rounded once to fp32.  Per-step host scalars are computed in double and rounded once.
+ *
+ * Readings of the pages that this file fixes (each one is listed with its reason in the design
+ * notes of the repository):
+ *   R1  Kahan split = truncation: hi = upper 16 bits of the f32 pattern, lo = lower 16 bits.
+ *   R2  NAdam = Dozat's Nesterov Adam with the momentum schedule mu_t = b1 (1 - 0.5*0.96^(t psi)).
+ *   R3  u16 codec for exp_avg: code = 32768 + sgn(m) rint(32767 sqrt(|m|/S)); decode
+ *       m = S t|t|, t = (code-32768)/32767.  For exp_avg_sq: code = rint(65535 (v/S)^(1/4)),
+ *       computed as sqrt(sqrt(v) / sqrt(S)); decode v = S z^4, z = code/65535.
+ *   R4  Per-tensor scale for step t: S_m = b1 A_m(t-1) + (1-b1) G(t), S_v = b2 A_v(t-1) +
+ *       (1-b2) G(t)^2, with A the max over the tensor of the pre-encode moments at t-1 and
+ *       G(t) = max |g(t)|.
+ *   R5  Tensors of 4096 or fewer elements keep fp32 moments (no codec).
+ *   R6  Factored second moment: means of g^2+eps1 over the last dim (rows) and the second-to-last
+ *       dim (columns); V^ = R C / mean(R); update clipped by max(1, RMS/clip).
+ *
+ * Parity pins (tests/test_oracle_*.py) tie this file to what the pages and mathematics fix:
+ * exhaustive split/merge round trip, IEEE bit patterns, exhaustive codec round trip, Adam
+ * step-1 = lr sign(g), NAdam step-1 closed form, torch.optim.{Adam,AdamW,NAdam,Adafactor}
+ * special cases, rank-1 factored case, zero-gradient and decay-only closed forms.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#include <float.h>
+
+#define ORC_SMALL_NUMEL 4096
+
+/* ----------------------------------------------------------------------------------------
+ * bit helpers
+ * -------------------------------------------------------------------------------------- */
+static float f_of(uint32_t b) { float f; memcpy(&f, &b, 4); return f; }
+static uint32_t b_of(float f) { uint32_t b; memcpy(&b, &f, 4); return b; }
+static float bf16_to_f32(uint16_t h) { return f_of((uint32_t)h << 16); }
+
+/* ----------------------------------------------------------------------------------------
+ * R1: Kahan split / merge.  The bf16 weight is the upper half of the f32 master and the
+ * residual is the 16 low bits that bf16 drops, so merge(split(x)) == x for every pattern.
+ * -------------------------------------------------------------------------------------- */
+void orc_kahan_split(const float* x, uint16_t* hi, uint16_t* lo, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        uint32_t b = b_of(x[i]);
+        hi[i] = (uint16_t)(b >> 16);
+        lo[i] = (uint16_t)(b & 0xFFFFu);
+    }
+}
+
+void orc_kahan_merge(const uint16_t* hi, const uint16_t* lo, float* x, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        x[i] = f_of(((uint32_t)hi[i] << 16) | (uint32_t)lo[i]);
+}
+
+/* Round-to-nearest-even f32 -> bf16 (the store used when no residual is kept).  Ties go to the
+ * even upper half; NaN stays NaN (quiet bit set), infinities stay infinities. */
+static uint16_t rne_bf16(float x)
+{
+    uint32_t b = b_of(x);
+    if ((b & 0x7F800000u) == 0x7F800000u && (b & 0x007FFFFFu) != 0)
+        return (uint16_t)((b >> 16) | 0x0040u);
+    uint32_t up = b >> 16, rem = b & 0xFFFFu;
+    if (rem > 0x8000u || (rem == 0x8000u && (up & 1u)))
+        up += 1u;
+    return (uint16_t)up;
+}
+
+void orc_round_bf16(const float* x, uint16_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = rne_bf16(x[i]);
+}
+
+/* ----------------------------------------------------------------------------------------
+ * R3: u16 companded codec ("I scale the exp_avg[_sq] structures and store them in
+ * scaled/biased uint16 format ... apply a pow() function", sd-scripts PR #2187, second post).
+ * Scale S per tensor; the encoder takes the reciprocal inv = 1/S (exp_avg) or rs = 1/sqrt(S)
+ * (exp_avg_sq), computed once per tensor.
+ * -------------------------------------------------------------------------------------- */
+float orc_inv_scale_m(float s)
+{
+    if (!(s > 0.0f)) return 0.0f;
+    return fminf(1.0f / s, FLT_MAX);
+}
+
+float orc_inv_scale_v(float s)
+{
+    if (!(s > 0.0f)) return 0.0f;
+    return 1.0f / sqrtf(s);
+}
+
+uint16_t orc_encode_m(float m, float inv)
+{
+    float a = fabsf(m) * inv;
+    float y = sqrtf(a);
+    float k = rintf(fminf(y * 32767.0f, 32767.0f));
+    uint32_t kk = (uint32_t)k;
+    return (uint16_t)(signbit(m) ? 32768u - kk : 32768u + kk);
+}
+
+float orc_decode_m(uint16_t c, float s)
+{
+    float t = (float)((int32_t)c - 32768) * (1.0f / 32767.0f);
+    float p = t * fabsf(t);
+    return p * s;
+}
+
+/* sv is sqrt(v); the update needs that root anyway, so the codec reuses it. */
+uint16_t orc_encode_v(float sv, float rs)
+{
+    float y = sqrtf(sv * rs);
+    float k = rintf(fminf(y * 65535.0f, 65535.0f));
+    return (uint16_t)(uint32_t)k;
+}
+
+float orc_decode_v(uint16_t c, float s)
+{
+    float z = (float)c * (1.0f / 65535.0f);
+    float z2 = z * z;
+    return (z2 * z2) * s;
+}
+
+/* Stand-alone pack: S = max over the buffer (|x| for exp_avg, x for exp_avg_sq), then encode. */
+void orc_state_pack(const float* x, uint16_t* codes, float* scale, int64_t n, int32_t is_signed)
+{
+    uint32_t mx = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        uint32_t b = b_of(x[i]) & 0x7FFFFFFFu;
+        if (b > mx) mx = b;
+    }
+    float s = f_of(mx);
+    *scale = s;
+    if (is_signed) {
+        float inv = orc_inv_scale_m(s);
+        for (int64_t i = 0; i < n; ++i) codes[i] = orc_encode_m(x[i], inv);
+    } else {
+        float rs = orc_inv_scale_v(s);
+        for (int64_t i = 0; i < n; ++i) codes[i] = orc_encode_v(sqrtf(x[i]), rs);
+    }
+}
+
+void orc_state_unpack(const uint16_t* codes, float scale, float* x, int64_t n, int32_t is_signed)
+{
+    for (int64_t i = 0; i < n; ++i)
+        x[i] = is_signed ? orc_decode_m(codes[i], scale) : orc_decode_v(codes[i], scale);
+}
+
+/* ----------------------------------------------------------------------------------------
+ * R2: per-step host scalars of Adam / NAdam, double then one rounding to fp32.
+ *   Adam:  c_m = 1/(1-b1^t), c_g = 0
+ *   NAdam: mu_t = b1 (1 - 0.5*0.96^(t psi)), P_t = P_{t-1} mu_t,
+ *          c_g = (1-mu_t)/(1-P_t), c_m = mu_{t+1}/(1 - P_t mu_{t+1})
+ *   both:  k2 = 1/sqrt(1-b2^t)
+ * The pages name "Nesterov Momentum (i.e. NAdamW)" (sd-scripts PR #2187, first post) without
+ * printing a formula; this is Dozat's NAdam with the usual momentum-decay schedule.
+ * -------------------------------------------------------------------------------------- */
+typedef struct {
+    float lr, b1, omb1, b2, omb2, eps, lr_wd, c_m, c_g, k2;
+    int32_t decoupled_wd;
+} orc_nadam_scalars_t;
+
+void orc_nadam_scalars(int64_t t, float lr, float beta1, float beta2, float eps, float wd,
+                       int32_t decoupled_wd, int32_t nesterov, float psi, double* mu_product,
+                       orc_nadam_scalars_t* k)
+{
+    double b1 = beta1, b2 = beta2, td = (double)t;
+    k->lr = lr;
+    k->b1 = beta1;
+    k->omb1 = (float)(1.0 - b1);
+    k->b2 = beta2;
+    k->omb2 = (float)(1.0 - b2);
+    k->eps = eps;
+    k->lr_wd = (float)((double)lr * (double)wd);
+    k->decoupled_wd = decoupled_wd;
+    k->k2 = (float)(1.0 / sqrt(1.0 - pow(b2, td)));
+    if (nesterov) {
+        double mu = b1 * (1.0 - 0.5 * pow(0.96, td * (double)psi));
+        double mu_next = b1 * (1.0 - 0.5 * pow(0.96, (td + 1.0) * (double)psi));
+        double prod = *mu_product * mu;
+        *mu_product = prod;
+        k->c_g = (float)((1.0 - mu) / (1.0 - prod));
+        k->c_m = (float)(mu_next / (1.0 - prod * mu_next));
+    } else {
+        k->c_m = (float)(1.0 / (1.0 - pow(b1, td)));
+        k->c_g = 0.0f;
+    }
+}
+
+/* Per-tensor scale record.  s_m, s_v: scales the stored codes were encoded with (decode slot);
+ * a_m, a_v: max |m| and max v of the fp32 moments before encoding, at the last step. */
+typedef struct { float s_m, s_v, a_m, a_v; } orc_scale_t;
+
+/* G = max |g| over the tensor, taken on the bf16 magnitude bits (equal to the float max for
+ * every non-NaN input; a NaN magnitude compares above infinity). */
+float orc_grad_absmax(const uint16_t* g, int64_t n)
+{
+    uint32_t mx = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        uint32_t b = g[i] & 0x7FFFu;
+        if (b > mx) mx = b;
+    }
+    return bf16_to_f32((uint16_t)mx);
+}
+
+/* ----------------------------------------------------------------------------------------
+ * One NAdam(W)/Adam step of one tensor with the Kahan residual and companded states.
+ *   hi : bf16 weight bits (in/out);  lo : residual bits (in/out), or NULL for a plain RNE store
+ *   m, v : uint16 codes if n > 4096, else fp32 (R5)
+ *   g  : bf16 gradient bits
+ * Order per element (moments first, then decoupled decay, then the update -- the printed
+ * Adafactor step decays the weight before subtracting the update):
+ *   w  = merge(hi, lo);  g = f32(g)
+ *   m  = b1 m0 + (1-b1) g;    v = b2 v0 + (1-b2) (g g)
+ *   w  = w - (lr wd) w                                  (decoupled decay only)
+ *   sv = sqrt(v);  den = sv k2 + eps;  num = c_m m + c_g g
+ *   w  = w - lr (num / den);  (hi, lo) = split(w)
+ * The update uses the fp32 moments just computed; quantisation happens only between steps
+ * ("it can only be used for storage rather than operations", PR #2187, third post).
+ * -------------------------------------------------------------------------------------- */
+void orc_nadam_step_tensor(uint16_t* hi, uint16_t* lo, void* m, void* v, const uint16_t* g,
+                           int64_t n, orc_scale_t* sc, const orc_nadam_scalars_t* k)
+{
+    int small = n <= ORC_SMALL_NUMEL;
+    float s_m = 0.0f, s_v = 0.0f, inv_m = 0.0f, rs_v = 0.0f;
+    if (!small) {
+        float G = orc_grad_absmax(g, n);
+        s_m = k->b1 * sc->a_m + k->omb1 * G;
+        s_v = k->b2 * sc->a_v + k->omb2 * (G * G);
+        inv_m = orc_inv_scale_m(s_m);
+        rs_v = orc_inv_scale_v(s_v);
+    }
+    uint32_t am = 0, av = 0;
+    uint16_t* mc = (uint16_t*)m;
+    uint16_t* vc = (uint16_t*)v;
+    float* mf = (float*)m;
+    float* vf = (float*)v;
+    for (int64_t i = 0; i < n; ++i) {
+        float w = lo ? f_of(((uint32_t)hi[i] << 16) | lo[i]) : bf16_to_f32(hi[i]);
+        float gg = bf16_to_f32(g[i]);
+        float m0 = small ? mf[i] : orc_decode_m(mc[i], sc->s_m);
+        float v0 = small ? vf[i] : orc_decode_v(vc[i], sc->s_v);
+        float mm = k->b1 * m0 + k->omb1 * gg;
+        float vv = k->b2 * v0 + k->omb2 * (gg * gg);
+        if (k->decoupled_wd)
+            w = w - k->lr_wd * w;
+        float sv = sqrtf(vv);
+        float den = sv * k->k2 + k->eps;
+        float num = k->c_m * mm + k->c_g * gg;
+        w = w - k->lr * (num / den);
+        if (lo) {
+            uint32_t b = b_of(w);
+            hi[i] = (uint16_t)(b >> 16);
+            lo[i] = (uint16_t)(b & 0xFFFFu);
+        } else {
+            hi[i] = rne_bf16(w);
+        }
+        if (small) {
+            mf[i] = mm;
+            vf[i] = vv;
+        } else {
+            mc[i] = orc_encode_m(mm, inv_m);
+            vc[i] = orc_encode_v(sv, rs_v);
+            uint32_t bm = b_of(mm) & 0x7FFFFFFFu, bv = b_of(vv) & 0x7FFFFFFFu;
+            if (bm > am) am = bm;
+            if (bv > av) av = bv;
+        }
+    }
+    if (!small) {
+        sc->s_m = s_m;
+        sc->s_v = s_v;
+        sc->a_m = f_of(am);
+        sc->a_v = f_of(av);
+    }
+}
+
+/* Same step with a plain fp32 master weight and fp32 moments (no Kahan split, no codec):
+ * the textbook optimizer the Kahan path must reproduce bit for bit given equal moments. */
+void orc_nadam_step_fp32(float* w, float* m, float* v, const uint16_t* g, int64_t n,
+                         const orc_nadam_scalars_t* k)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        float ww = w[i];
+        float gg = bf16_to_f32(g[i]);
+        float mm = k->b1 * m[i] + k->omb1 * gg;
+        float vv = k->b2 * v[i] + k->omb2 * (gg * gg);
+        if (k->decoupled_wd)
+            ww = ww - k->lr_wd * ww;
+        float den = sqrtf(vv) * k->k2 + k->eps;
+        float num = k->c_m * mm + k->c_g * gg;
+        w[i] = ww - k->lr * (num / den);
+        m[i] = mm;
+        v[i] = vv;
+    }
+}
+
+/* ----------------------------------------------------------------------------------------
+ * R6: factored second moment (Adafactor; Prodigy's factored variant), beta1 = 0, no exp_avg.
+ * Follows the printed fused Adafactor step ("Fused backward pass" commit,
+ * library/adafactor_fused.py, adafactor_step_param) with a fixed learning rate, and the eps2
+ * placement of prodigy PR #25 ("more VRAM savings: no first moment and factored second
+ * moment", the comment that moves eps2 out of the d^2 scaling).
+ *
+ * mode 0 (Adafactor): b2t = 1 - t^decay_rate, q = g g + eps1,
+ *                     R = b2t R + (1-b2t) mean_j q, C = b2t C + (1-b2t) mean_i q
+ * mode 1 (Prodigy):   q = g g, R = b2 R + d^2 (1-b2) mean_j q + eps2, C likewise
+ * V^_ij = R_i C_j / mean_i(R);  u_ij = (rsqrt(R_i / mean R) rsqrt(C_j)) g_ij
+ * 1-D:   V = b2t V + (1-b2t) q (mode 1: + eps2);  u = rsqrt(V) g
+ * then   u = (u / max(1, RMS(u)/clip)) lr_eff;  w = w + w (-wd lr_eff);  w = w - u;  split.
+ * lr_eff = lr in mode 0 and d lr in mode 1.
+ * -------------------------------------------------------------------------------------- */
+typedef struct {
+    float b2t, alpha, eps1, eps2, clip, lr_eff, nwdlr;
+    int32_t mode;
+} orc_factored_scalars_t;
+
+void orc_factored_scalars(int64_t t, float lr, float beta2, float decay_rate, float eps1,
+                          float eps2, float d, float clip, float wd, int32_t mode,
+                          orc_factored_scalars_t* k)
+{
+    double td = (double)t;
+    k->mode = mode;
+    k->clip = clip;
+    k->eps1 = eps1;
+    k->eps2 = eps2;
+    if (mode == 0) {
+        double beta2t = 1.0 - pow(td, (double)decay_rate);
+        k->b2t = (float)beta2t;
+        k->alpha = (float)(1.0 - beta2t);
+        k->lr_eff = lr;
+    } else {
+        k->b2t = beta2;
+        k->alpha = (float)((double)d * (double)d * (1.0 - (double)beta2));
+        k->lr_eff = (float)((double)d * (double)lr);
+    }
+    k->nwdlr = (float)(-(double)wd * (double)k->lr_eff);
+}
+
+static float rsqrt_rn(float x) { return 1.0f / sqrtf(x); }
+
+/* Update of the weight given the final (unscaled) update u and the clip divisor. */
+static void apply_update(uint16_t* hi, uint16_t* lo, int64_t i, float u, float den,
+                         const orc_factored_scalars_t* k)
+{
+    float w = lo ? f_of(((uint32_t)hi[i] << 16) | lo[i]) : bf16_to_f32(hi[i]);
+    float uu = (u / den) * k->lr_eff;
+    if (k->nwdlr != 0.0f)
+        w = w + w * k->nwdlr;
+    w = w - uu;
+    if (lo) {
+        uint32_t b = b_of(w);
+        hi[i] = (uint16_t)(b >> 16);
+        lo[i] = (uint16_t)(b & 0xFFFFu);
+    } else {
+        hi[i] = rne_bf16(w);
+    }
+}
+
+static float clip_divisor(double ss, int64_t n, float clip)
+{
+    float ss32 = (float)ss;
+    float ms = ss32 / (float)n;
+    float rms = sqrtf(ms);
+    return fmaxf(1.0f, rms / clip);
+}
+
+/* Factored tensor viewed as B matrices of R rows x C columns (the last two dims), row-major.
+ * row[B*R], col[B*C] fp32 state (in/out).  Returns the clip divisor used (for tests). */
+float orc_factored_step_tensor(uint16_t* hi, uint16_t* lo, const uint16_t* g, int64_t B,
+                               int64_t R, int64_t C, float* row, float* col,
+                               const orc_factored_scalars_t* k)
+{
+    int64_t n = B * R * C;
+    /* 1. EMA of row and column means of q */
+    for (int64_t b = 0; b < B; ++b) {
+        const uint16_t* gb = g + b * R * C;
+        for (int64_t i = 0; i < R; ++i) {
+            double s = 0.0;
+            for (int64_t j = 0; j < C; ++j) {
+                float gg = bf16_to_f32(gb[i * C + j]);
+                float q = k->mode == 0 ? gg * gg + k->eps1 : gg * gg;
+                s += (double)q;
+            }
+            float r = (float)(s / (double)C);
+            float nr = k->b2t * row[b * R + i] + k->alpha * r;
+            if (k->mode == 1) nr = nr + k->eps2;
+            row[b * R + i] = nr;
+        }
+        for (int64_t j = 0; j < C; ++j) {
+            double s = 0.0;
+            for (int64_t i = 0; i < R; ++i) {
+                float gg = bf16_to_f32(gb[i * C + j]);
+                float q = k->mode == 0 ? gg * gg + k->eps1 : gg * gg;
+                s += (double)q;
+            }
+            float c = (float)(s / (double)R);
+            float nc = k->b2t * col[b * C + j] + k->alpha * c;
+            if (k->mode == 1) nc = nc + k->eps2;
+            col[b * C + j] = nc;
+        }
+    }
+    /* 2. u = rsqrt(R_i / mean R) rsqrt(C_j) g and its sum of squares */
+    double ss = 0.0;
+    for (int64_t b = 0; b < B; ++b) {
+        double rs = 0.0;
+        for (int64_t i = 0; i < R; ++i) rs += (double)row[b * R + i];
+        float rbar = (float)(rs / (double)R);
+        for (int64_t i = 0; i < R; ++i) {
+            float rr = rsqrt_rn(row[b * R + i] / rbar);
+            for (int64_t j = 0; j < C; ++j) {
+                float cc = rsqrt_rn(col[b * C + j]);
+                float u = (rr * cc) * bf16_to_f32(g[(b * R + i) * C + j]);
+                ss += (double)u * (double)u;
+            }
+        }
+    }
+    float den = clip_divisor(ss, n, k->clip);
+    /* 3. clip, lr, decay, subtract, split */
+    for (int64_t b = 0; b < B; ++b) {
+        double rs = 0.0;
+        for (int64_t i = 0; i < R; ++i) rs += (double)row[b * R + i];
+        float rbar = (float)(rs / (double)R);
+        for (int64_t i = 0; i < R; ++i) {
+            float rr = rsqrt_rn(row[b * R + i] / rbar);
+            for (int64_t j = 0; j < C; ++j) {
+                float cc = rsqrt_rn(col[b * C + j]);
+                int64_t e = (b * R + i) * C + j;
+                float u = (rr * cc) * bf16_to_f32(g[e]);
+                apply_update(hi, lo, e, u, den, k);
+            }
+        }
+    }
+    return den;
+}
+
+/* Non-factored (1-D) tensor: full fp32 second moment V[n] (in/out). */
+float orc_factored_step_vector(uint16_t* hi, uint16_t* lo, const uint16_t* g, int64_t n,
+                               float* V, const orc_factored_scalars_t* k)
+{
+    double ss = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        float gg = bf16_to_f32(g[i]);
+        float q = k->mode == 0 ? gg * gg + k->eps1 : gg * gg;
+        float nv = k->b2t * V[i] + k->alpha * q;
+        if (k->mode == 1) nv = nv + k->eps2;
+        V[i] = nv;
+        float u = rsqrt_rn(nv) * gg;
+        ss += (double)u * (double)u;
+    }
+    float den = clip_divisor(ss, n, k->clip);
+    for (int64_t i = 0; i < n; ++i) {
+        float u = rsqrt_rn(V[i]) * bf16_to_f32(g[i]);
+        apply_update(hi, lo, i, u, den, k);
+    }
+    return den;
+}

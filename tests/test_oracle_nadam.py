@@ -1,0 +1,194 @@
+"""Pins of the oracle's NAdam(W)/Adam step with the Kahan residual and the u16 states.
+
+The pages recommend NAdam (Nesterov momentum) and its W variant with decoupled weight decay,
+without printing a formula ("Amazing Flux FFT quality on a 5090", sd-scripts PR #2187, first
+post).  The oracle takes Dozat's NAdam with the momentum-decay schedule; these tests pin it to
+closed forms and to torch.optim's Adam, AdamW and NAdam (library routines), using tensors of
+4096 or fewer elements, which keep fp32 moments (same post, "4096 or fewer elements").
+"""
+import numpy as np
+import pytest
+import torch
+
+HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, wd_mode=0, nesterov=1,
+          momentum_decay=0.004)
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().astype(np.uint16)
+
+
+def bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def make_tensor(orc, w0: np.ndarray, small: bool):
+    hi, lo = orc.kahan_split(w0.astype(np.float32))
+    n = w0.size
+    if small:
+        return dict(hi=hi, lo=lo, m=np.zeros(n, np.float32), v=np.zeros(n, np.float32))
+    return dict(hi=hi, lo=lo, m=np.full(n, 32768, np.uint16), v=np.zeros(n, np.uint16))
+
+
+def run_oracle(orc, w0, grads, hp, small=True):
+    t = make_tensor(orc, w0, small)
+    st = orc.NadamState(1)
+    for step, g in enumerate(grads, start=1):
+        orc.nadam_group_step([t], [g], st, step, hp)
+    return orc.kahan_merge(t["hi"], t["lo"]), t, st
+
+
+@pytest.mark.parametrize("n", [1000, 50_000])
+def test_adam_step1_is_lr_sign(orc, n):
+    """Adam at t=1 with eps=0: m/sqrt(v) after bias correction is sign(g), so w1 - w0 = -lr sign(g)."""
+    rng = np.random.default_rng(10)
+    g = bf16_bits(rng.standard_normal(n) * 1e-3)
+    g[bits_to_f32(g) == 0] = bf16_bits(np.array([1e-3]))[0]
+    hp = dict(HP, eps=0.0, nesterov=0, lr=3.5e-6)
+    w1, _, _ = run_oracle(orc, np.zeros(n, np.float32), [g], hp, small=n <= 4096)
+    lr = np.float32(hp["lr"])
+    ulp = np.spacing(lr)
+    assert np.all(np.abs(w1.astype(np.float64) + float(lr) * np.sign(bits_to_f32(g))) <= 4 * ulp)
+
+
+def test_nadam_step1_closed_form(orc):
+    rng = np.random.default_rng(11)
+    n = 3000
+    g = bf16_bits(rng.standard_normal(n) * 1e-3)
+    w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    hp = dict(HP, lr=1e-2)
+    w1, _, _ = run_oracle(orc, w0, [g], hp)
+    b1, b2, psi, eps = 0.9, 0.999, 0.004, 1e-8
+    mu1 = b1 * (1 - 0.5 * 0.96 ** (1 * psi))
+    mu2 = b1 * (1 - 0.5 * 0.96 ** (2 * psi))
+    gd = bits_to_f32(g).astype(np.float64)
+    # m1 = (1-b1) g, v1 = (1-b2) g^2; NAdam's bias-corrected Nesterov numerator at t=1
+    num = (1 - mu1) / (1 - mu1) * gd + mu2 / (1 - mu1 * mu2) * (1 - b1) * gd
+    den = np.abs(gd) * np.sqrt(1 - b2) / np.sqrt(1 - b2) + eps
+    expect = -hp["lr"] * num / den
+    got = w1.astype(np.float64) - w0
+    tol = 2e-6 * np.abs(expect) + 2 * np.spacing(np.abs(w0)).astype(np.float64)
+    assert np.all(np.abs(got - expect) <= tol)
+
+
+def _torch_traj(opt_cls, w0, grads, **kw):
+    p = torch.nn.Parameter(torch.from_numpy(w0.copy()))
+    opt = opt_cls([p], **kw)
+    for g in grads:
+        p.grad = torch.from_numpy(bits_to_f32(g).copy())
+        opt.step()
+    return p.detach().numpy()
+
+
+@pytest.mark.parametrize("variant", ["adam", "adamw", "nadam", "nadamw"])
+def test_matches_torch_optim(orc, variant):
+    """fp32 moments + Kahan (an exact fp32 master) reproduce torch.optim within fp32 rounding."""
+    rng = np.random.default_rng(12)
+    n, steps = 4096, 10
+    w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    grads = [bf16_bits(rng.standard_normal(n) * 1e-3) for _ in range(steps)]
+    wd = 0.1 if variant.endswith("w") else 0.0
+    hp = dict(HP, lr=1e-3, weight_decay=wd, wd_mode=1 if wd else 0, nesterov=variant.startswith("n"))
+    ours, _, _ = run_oracle(orc, w0, grads, hp)
+    if variant == "adam":
+        ref = _torch_traj(torch.optim.Adam, w0, grads, lr=1e-3, betas=(0.9, 0.999), eps=1e-8)
+    elif variant == "adamw":
+        ref = _torch_traj(torch.optim.AdamW, w0, grads, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=wd)
+    else:
+        ref = _torch_traj(torch.optim.NAdam, w0, grads, lr=1e-3, betas=(0.9, 0.999), eps=1e-8,
+                          momentum_decay=0.004, weight_decay=wd, decoupled_weight_decay=bool(wd))
+    d_ours = ours.astype(np.float64) - w0
+    d_ref = ref.astype(np.float64) - w0
+    # rounding-order differences are a few ulps of each step's update (size ~lr) plus the
+    # weight's own rounding; the net displacement can be small through cancellation
+    tol = 1e-6 * hp["lr"] * steps + 4 * np.spacing(np.abs(w0)).astype(np.float64)
+    if wd:
+        # torch multiplies by fp32(1 - lr wd), whose rounding (up to 2^-25 near 1) is a large
+        # relative error of the decay itself; the oracle subtracts fp32(lr wd) * w instead
+        tol = tol + steps * np.abs(w0).astype(np.float64) * 2.0 ** -24
+    assert np.all(np.abs(d_ours - d_ref) <= tol), np.max(np.abs(d_ours - d_ref) - tol)
+
+
+def test_kahan_equals_fp32_master(orc):
+    """Given equal moments the Kahan pair (hi, lo) is exactly the fp32 master of a plain step."""
+    rng = np.random.default_rng(13)
+    n = 4000
+    w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    grads = [bf16_bits(rng.standard_normal(n) * 1e-3) for _ in range(6)]
+    hp = dict(HP, lr=3.5e-6, weight_decay=0.01, wd_mode=1)
+    ours, _, _ = run_oracle(orc, w0, grads, hp)
+    w = w0.copy()
+    m = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    mp = 1.0
+    for t, g in enumerate(grads, start=1):
+        k, mp = orc.nadam_scalars(t, hp["lr"], 0.9, 0.999, 1e-8, 0.01, True, True, 0.004, mp)
+        orc.nadam_step_fp32(w, m, v, g, k)
+    assert np.array_equal(ours.view(np.uint32), w.view(np.uint32))
+
+
+def test_low_bits_accumulate_sub_bf16_updates(orc):
+    """Updates far below one bf16 step still move the live bf16 weight through the residual."""
+    n = 5000
+    w0 = np.full(n, 1.0, np.float32)
+    g = bf16_bits(np.full(n, 1e-3))
+    hp = dict(HP, eps=0.0, nesterov=0, lr=2.0 ** -12)   # 1/32 of a bf16 step at 1.0
+    t = make_tensor(orc, w0, small=False)
+    st = orc.NadamState(1)
+    for step in range(1, 65):
+        orc.nadam_group_step([t], [g], st, step, hp)
+    w = orc.kahan_merge(t["hi"], t["lo"])
+    assert np.all(bits_to_f32(t["hi"]) < 1.0)          # the bf16 weight moved
+    assert np.all(np.abs(w - (1.0 - 64 * 2.0 ** -12)) < 2e-3 * 64 * 2.0 ** -12)
+    t2 = dict(hi=bf16_bits(w0), lo=None, m=np.full(n, 32768, np.uint16), v=np.zeros(n, np.uint16))
+    st2 = orc.NadamState(1)
+    for step in range(1, 65):
+        orc.nadam_group_step([t2], [g], st2, step, hp)
+    assert np.all(bits_to_f32(t2["hi"]) == 1.0)         # without the residual the update is lost
+
+
+def test_zero_grad_and_decay_only(orc):
+    rng = np.random.default_rng(14)
+    for n in (2048, 10000):
+        w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+        z = np.zeros(n, np.uint16)
+        w, _, _ = run_oracle(orc, w0, [z] * 5, dict(HP), small=n <= 4096)
+        assert np.array_equal(w, w0)
+        lr, wd, T = 1e-2, 0.1, 7
+        w, _, _ = run_oracle(orc, w0, [z] * T, dict(HP, lr=lr, weight_decay=wd, wd_mode=1), small=n <= 4096)
+        expect = w0.astype(np.float64) * (1 - np.float64(np.float32(lr * wd))) ** T
+        assert np.all(np.abs(w - expect) <= T * np.spacing(np.abs(w0)))
+
+
+def test_u16_states_track_fp32_states(orc):
+    """Above 4096 elements the moments are u16-companded; the trajectory stays within the codec's
+    error of the fp32-moment trajectory (a loose property check, not an exact pin)."""
+    rng = np.random.default_rng(15)
+    n, steps = 8192, 10
+    w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    grads = [bf16_bits(rng.standard_normal(n) * 1e-3) for _ in range(steps)]
+    hp = dict(HP, lr=1e-3)
+    w_u16, t, st = run_oracle(orc, w0, grads, hp, small=False)
+    ref = _torch_traj(torch.optim.NAdam, w0, grads, lr=1e-3, betas=(0.9, 0.999), eps=1e-8,
+                      momentum_decay=0.004)
+    d_u16 = w_u16.astype(np.float64) - w0
+    d_ref = ref.astype(np.float64) - w0
+    rel = np.abs(d_u16 - d_ref).sum() / np.abs(d_ref).sum()
+    assert rel < 0.02
+    s_m, s_v, a_m, a_v = st.scale(0)
+    assert 0 < a_m <= s_m * 1.0001 and 0 < a_v <= s_v * 1.0001
+
+
+def test_scale_is_a_bound(orc):
+    """S_m(t) = b1 A_m(t-1) + (1-b1) G(t) bounds every |m(t)|, so codes rarely saturate."""
+    rng = np.random.default_rng(16)
+    n = 20000
+    t = make_tensor(orc, (rng.standard_normal(n) * 0.02).astype(np.float32), small=False)
+    st = orc.NadamState(1)
+    for step in range(1, 6):
+        g = bf16_bits(rng.standard_normal(n) * 1e-3 * step)
+        orc.nadam_group_step([t], [g], st, step, dict(HP))
+        s_m, s_v, a_m, a_v = st.scale(0)
+        assert a_m <= s_m * (1 + 1e-4) and a_v <= s_v * (1 + 1e-4)
+        sat = np.mean((t["m"] == 1) | (t["m"] == 65535))
+        assert sat < 0.01
