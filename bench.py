@@ -1,0 +1,426 @@
+#!/usr/bin/env python
+"""Throughput of the fused optimizer step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload flux19]
+
+One step = one pass of the whole hot path over the workload: for the flux19 workload, the 19
+group calls (one per Flux-like double-stream block, ~170M parameters each) of the fused
+NAdamW + Kahan + u16-moment step, each a gradient-max pre-pass and the update kernel.  Inputs
+(bf16 weights, residuals, moment codes, one set of bf16 gradients) are resident in HBM before
+the timed region; together they are ~32 GB, far larger than L2, so no L2 flush is needed.
+
+The JSON line reports params updated/s (whole job, all ranks), the step's HBM GB/s at the
+algorithmic 18 bytes per parameter, a roofline record for the dominant kernel timed live with
+CUDA events, the oracle's CPU throughput on a bounded sample, and an end-to-end figure through
+the public API with the gradients copied in from pinned host memory and the weights copied back
+every step.  With N > 1 (torchrun), every rank steps its own copy of the workload (weak scaling,
+no collective on the data path) and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "params updated/s and achieved HBM GB/s (% of GB300 roofline) per optimizer step"
+BYTES_PER_PARAM_U16 = 18      # read w, res, g, m, v; write w, res, m, v (2 bytes each)
+BYTES_PER_PARAM_F32 = 26      # fp32 moments: m, v 4 bytes each way
+PREPASS_BYTES_PER_PARAM = 2   # gradient-max pre-pass re-reads g
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["memory_lean_optimizer_gb300/csrc/nadam.cu", "memory_lean_optimizer_gb300/csrc/common.cuh"]
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=5)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="flux19")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    return p.parse_args()
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            for key in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+                if key in d and d[key]:
+                    return float(d[key]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_per_launch(params_per_launch):
+    """DRAM bytes per launch of the update kernel from the committed ncu summary, scaled to the
+    launch's parameter count; None when absent or taken on different kernel source."""
+    path = os.path.join(ROOT, "profiles", "k_nadam_step_traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("kernel_source_sha") != kernel_hash():
+            return None
+        return d["dram_bytes_per_param"] * params_per_launch
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- workload setup
+def build_groups(cfg, device, rank):
+    import torch
+    from memory_lean_optimizer_gb300 import engine, workloads as W
+    groups, grads, params = [], [], 0
+    tid = 0
+    for shapes in cfg["groups"]:
+        masters, gs = [], []
+        for s in shapes:
+            masters.append(W.master_weights(s, cfg["seed"] + 1000 * rank, tid, device=device))
+            gs.append(W.grad_bf16(s, cfg["seed"] + 1000 * rank, tid, 1, cfg["g_std"], device=device,
+                                  zero_frac=cfg["zero_frac"]))
+            params += W.numel(s)
+            tid += 1
+        groups.append(engine.NadamGroup.from_masters(masters))
+        del masters
+        grads.append(gs)
+    torch.cuda.synchronize()
+    return groups, grads, params
+
+
+def bytes_alg(shapes):
+    from memory_lean_optimizer_gb300 import workloads as W
+    tot = 0
+    for s in shapes:
+        n = W.numel(s)
+        tot += n * (BYTES_PER_PARAM_F32 if n <= 4096 else BYTES_PER_PARAM_U16)
+    return tot
+
+
+def cpu_baseline(cfg, target_s):
+    """The oracle, as it stands (single-threaded C), on a bounded sample of the workload: the
+    tensors of the first groups, stepped until about target_s seconds of CPU time."""
+    import oracle
+    from memory_lean_optimizer_gb300 import workloads as W
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    oracle.build()
+    shapes = [s for grp in cfg["groups"] for s in grp]
+    done_params, spent, steps_done = 0, 0.0, 0
+    sample = []
+    tid = 0
+    while spent < target_s and tid < len(shapes):
+        s = shapes[tid]
+        x = W.master_weights(s, cfg["seed"], tid).numpy().reshape(-1)
+        hi, lo = oracle.kahan_split(x)
+        n = x.size
+        if n <= 4096:
+            import numpy as np
+            m, v = np.zeros(n, np.float32), np.zeros(n, np.float32)
+        else:
+            import numpy as np
+            m, v = np.full(n, 32768, np.uint16), np.zeros(n, np.uint16)
+        st = oracle.NadamState(1)
+        t = dict(hi=hi, lo=lo, m=m, v=v)
+        for step in (1, 2):
+            g = W.bits16(W.grad_bf16(s, cfg["seed"], tid, step, cfg["g_std"], zero_frac=cfg["zero_frac"])).reshape(-1)
+            t0 = time.perf_counter()
+            oracle.nadam_group_step([t], [g], st, step, cfg["hp"])
+            spent += time.perf_counter() - t0
+            done_params += n
+            steps_done += 1
+        sample.append(tuple(s))
+        tid += 1
+    return {"value": done_params / spent, "unit": "params/s", "cores": 1, "kind": "oracle",
+            "sample": f"{len(sample)} tensors of the workload ({sum(W.numel(s) for s in sample)} params) x 2 steps, "
+                      f"{spent:.1f} s single-threaded C"}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, cfg):
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return 0
+    import oracle
+    from memory_lean_optimizer_gb300 import workloads as W
+    import numpy as np
+    oracle.build()
+    shapes = [s for grp in cfg["groups"] for s in grp]
+    # each step: the oracle over a bounded sample (the workload's first tensor), sized so that
+    # --steps K --warmup W ends within a few minutes
+    s = shapes[0]
+    x = W.master_weights(s, cfg["seed"], 0).numpy().reshape(-1)
+    n = x.size
+    hi, lo = oracle.kahan_split(x)
+    t = dict(hi=hi, lo=lo, m=np.full(n, 32768, np.uint16) if n > 4096 else np.zeros(n, np.float32),
+             v=np.zeros(n, np.uint16) if n > 4096 else np.zeros(n, np.float32))
+    st = oracle.NadamState(1)
+    g = W.bits16(W.grad_bf16(s, cfg["seed"], 0, 1, cfg["g_std"])).reshape(-1)
+    step = 0
+    for _ in range(args.warmup):
+        step += 1
+        oracle.nadam_group_step([t], [g], st, step, cfg["hp"])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step += 1
+        oracle.nadam_group_step([t], [g], st, step, cfg["hp"])
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    line = {"metric": METRIC, "value": value, "unit": "params/s", "impl": "reference", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": args.workload, "sample_params_per_step": n},
+            "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
+                             "sample": f"one {s} tensor per step (single-threaded C oracle)"},
+            "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, cfg):
+    import torch
+    import torch.distributed as dist
+    from memory_lean_optimizer_gb300 import build, lmopt
+
+    world, rank, local = dist_info()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    build.build()
+    lmopt.load()
+
+    groups, grads, params = build_groups(cfg, device, rank)
+    hp = cfg["hp"]
+    stream = torch.cuda.current_stream()
+
+    def one_step(events=None):
+        for gi, (grp, gs) in enumerate(zip(groups, grads)):
+            if events is not None:
+                e0, em, e1 = events[gi]
+                e0.record(stream)
+                lmopt.optim_group_set_profile_event(grp.handle, em.cuda_event)
+            grp.step(gs, hp, stream)
+            if events is not None:
+                e1.record(stream)
+                lmopt.optim_group_set_profile_event(grp.handle, None)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+
+    launches_per_step = sum(2 if any(W_numel(s) > 4096 for s in shapes) else 1 for shapes in cfg["groups"])
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in groups] for _ in range(args.steps)]
+    for per_step in ev:               # materialise the event handles the library records into
+        for trio in per_step:
+            for e in trio:
+                e.record(stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    start.record(stream)
+    for k in range(args.steps):
+        one_step(ev[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    elapsed = start.elapsed_time(end) / 1e3
+    if world > 1:
+        t = torch.tensor([elapsed], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+
+    # live per-kernel timing of the update kernel (between the library's mid event and the end)
+    k2_ms, k1_ms = [], []
+    for k in range(args.steps):
+        for gi in range(len(groups)):
+            e0, em, e1 = ev[k][gi]
+            k1_ms.append(e0.elapsed_time(em))
+            k2_ms.append(em.elapsed_time(e1))
+    group_bytes = [bytes_alg(shapes) for shapes in cfg["groups"]]
+    group_params = [sum(W_numel(s) for s in shapes) for shapes in cfg["groups"]]
+    k2_bytes_total = sum(group_bytes) * args.steps
+    k2_time_total = sum(k2_ms) / 1e3
+    k2_gbs = k2_bytes_total / k2_time_total / 1e9
+    peak, peak_src = peaks()
+    params_per_launch = sum(group_params) / len(group_params)
+    traffic = traffic_per_launch(params_per_launch)
+
+    step_s = elapsed / args.steps
+    value = world * params * args.steps / elapsed
+    result = {
+        "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * step_s, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "params_per_gpu": params, "groups": len(groups),
+                   "tensors": sum(len(s) for s in cfg["groups"]), "optimizer": "NAdamW+Kahan, u16 moments",
+                   "lr": hp["lr"], "weight_decay": hp["weight_decay"], "grads": "one resident set reused each step",
+                   "l2": "inputs ~32 GB per GPU, far above the 129 MB L2: no flush needed",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_gbs_step": sum(group_bytes) / step_s / 1e9,
+        "hbm_gbs_step_as_run": (sum(group_bytes) + PREPASS_BYTES_PER_PARAM * params) / step_s / 1e9,
+        "roofline": {"bound": "hbm", "kernel": "k_nadam_step", "achieved": k2_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": k2_gbs / peak, "traffic": traffic, "peak_source": peak_src,
+                     "bytes_per_param": BYTES_PER_PARAM_U16,
+                     "launch_ms_mean": 1e3 * k2_time_total / len(k2_ms),
+                     "prepass_ms_mean": statistics.mean(k1_ms)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = e2e_run(args, groups, grads, hp, params, stream, world, device)
+    for grp in groups:
+        grp.close()
+    del groups, grads
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    return 0
+
+
+def e2e_run(args, groups, grads, hp, params, stream, world, device):
+    """Same metric through the public API, host buffers: each step copies every group's bf16
+    gradients from pinned host memory to the device, steps the group, and copies the updated bf16
+    weights back to pinned host memory; all copies are inside the timed region."""
+    import torch
+    import torch.distributed as dist
+    host_g = [[g.to("cpu").pin_memory() for g in gs] for gs in grads]
+    host_w = [[torch.empty(w.shape, dtype=w.dtype, pin_memory=True) for w in grp.weights] for grp in groups]
+    steps = max(1, min(args.steps, 3))
+
+    def one():
+        for grp, gs, hg, hw in zip(groups, grads, host_g, host_w):
+            for d, h in zip(gs, hg):
+                d.copy_(h, non_blocking=True)
+            grp.step(gs, hp, stream)
+            for h, w in zip(hw, grp.weights):
+                h.copy_(w, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([dt], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dt = float(t.item())
+    nbytes = 2 * params
+    return {"value": world * params * steps / dt, "unit": "params/s", "h2d_bytes_per_step": nbytes,
+            "d2h_bytes_per_step": nbytes, "steps": steps}
+
+
+def W_numel(shape):
+    n = 1
+    for s in shape:
+        n *= int(s)
+    return n
+
+
+def main():
+    args = parse()
+    from memory_lean_optimizer_gb300 import workloads as W
+    cfg = W.config(args.workload)
+    if cfg["kind"] != "nadam":
+        raise SystemExit(f"workload {args.workload} is not a NAdam workload")
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

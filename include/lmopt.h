@@ -1,0 +1,171 @@
+/*
+ * lmopt.h -- C ABI of the GB300 fused optimizer-step engine (liblmopt.so).
+ *
+ * The engine performs the per-parameter optimizer step of memory-lean full fine-tuning:
+ * a group of parameters is registered once, then "step this group" is called each time the
+ * group's gradients are complete -- the granularity of the fused backward pass and of
+ * optimizer groups ("Fused backward pass" commit, README, "Fused optimizer" and "Optimizer
+ * groups" items).
+ *
+ * Conventions
+ *  - Every function returns int: OPTIM_OK (0) or a negative OPTIM_E* code.  On error,
+ *    optim_last_error() returns a thread-local message.  A failing call validates everything
+ *    before its first launch, so weights and states are left untouched.
+ *  - Device buffers are owned by the caller.  The library owns its group handle and the small
+ *    device tables behind it (tensor table, chunk table, per-tensor scales), freed by
+ *    optim_group_destroy.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).  All work is
+ *    enqueued asynchronously on it; only optim_group_create, optim_query_* and optim_set_*
+ *    synchronise.  Calls on one group must be ordered by the caller (one stream, or events).
+ *  - bf16 and uint16 buffers are arrays of 16-bit words and must be 2-byte aligned; fp32 buffers
+ *    4-byte aligned.  16-byte alignment of every buffer of a tensor enables 128-bit accesses;
+ *    other alignments take a slower element-by-element path with identical results.
+ *  - All arithmetic is IEEE fp32, every operation rounded to nearest-even, no contraction; the
+ *    results are deterministic run to run.
+ */
+#ifndef LMOPT_H
+#define LMOPT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    OPTIM_OK = 0,
+    OPTIM_EINVAL = -1,     /* bad argument (NULL pointer, size, shape, hyper-parameter, step) */
+    OPTIM_ECUDA = -2,      /* a CUDA runtime call or launch failed */
+    OPTIM_ENOMEM = -3,     /* device or pinned host allocation failed */
+    OPTIM_EALIGN = -4,     /* a buffer is not aligned to its element size */
+    OPTIM_ETIMEOUT = -5,   /* a bounded host wait on a stream event ran out */
+    OPTIM_ENONFINITE = -6, /* reserved for callers that turn a nonzero non-finite count into an error */
+    OPTIM_ESTATE = -7      /* call not valid in the group's current state */
+};
+
+/* Tensors of this many elements or fewer keep fp32 moments instead of u16 codes ("any tensors
+ * that have 4096 or fewer elements ... are just stored ... in f32 format", "Amazing Flux FFT
+ * quality on a 5090", sd-scripts PR #2187, second post). */
+#define OPTIM_SMALL_NUMEL 4096
+
+typedef struct optim_group optim_group_t;
+
+/* One parameter tensor of a group.
+ *   w_bf16  : device, numel bf16 weights (the upper 16 bits of the fp32 master), in/out
+ *   res_u16 : device, numel uint16 Kahan residuals (the 16 low bits bf16 drops), in/out, or
+ *             NULL: no residual, the weight is stored round-to-nearest-even
+ *   m, v    : kind NADAM: exp_avg / exp_avg_sq -- numel uint16 codes if numel > 4096, else
+ *             numel fp32 values.
+ *             kind FACTORED: ndim >= 2: m = row state fp32 [prod(shape[:-1])], v = column state
+ *             fp32 [prod(shape[:-2]) * shape[-1]]; ndim == 1: m unused (NULL), v = full fp32
+ *             second moment [numel].
+ *   numel   : element count (0 allowed: the tensor is skipped)
+ *   ndim, shape : logical shape, 1 <= ndim <= 4, product == numel (FACTORED groups factor the
+ *             last two dims; NADAM groups ignore the shape).
+ * All buffers must stay valid and unmoved for the life of the group. */
+typedef struct {
+    void* w_bf16;
+    void* res_u16;
+    void* m;
+    void* v;
+    int64_t numel;
+    int32_t ndim;
+    int32_t reserved;
+    int64_t shape[4];
+} optim_tensor_desc_t;
+
+enum { OPTIM_KIND_NADAM = 0, OPTIM_KIND_FACTORED = 1 };
+
+/* Adam / NAdam(W) hyper-parameters ("(N)AdamW / Adan with fused backwards pass & CPU
+ * offloading", sd-scripts PR #2187, first post: NAdamOffload, AdamOffload, NAdamWOffload).
+ *   wd_mode  : 0 none, 1 decoupled (the "W" variants: w -= lr*wd*w before the update)
+ *   nesterov : 0 Adam, 1 NAdam (Dozat's momentum schedule mu_t = beta1 (1 - 0.5*0.96^(t*psi)))
+ *   momentum_decay : psi, 0.004 by default */
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay;
+    int32_t wd_mode;
+    int32_t nesterov;
+    float momentum_decay;
+} optim_nadam_hparams_t;
+
+/* Factored second-moment hyper-parameters (beta1 = 0: no exp_avg is read or written).
+ *   mode 0 Adafactor ("Fused backward pass" commit, library/adafactor_fused.py,
+ *          adafactor_step_param): beta2_t = 1 - t^decay_rate, eps1 added to g^2 before the means.
+ *   mode 1 Prodigy ("more VRAM savings: no first moment and factored second moment",
+ *          prodigy PR #25): constant beta2, EMAs weighted by d^2 (1-beta2), eps2 added after the
+ *          EMA; the step size is d*lr with d fixed (no d-adaptation).
+ *   clip_threshold : update clipping, u /= max(1, RMS(u)/clip_threshold)
+ *   weight_decay   : decoupled, w += w * (-wd * lr_eff) before the update */
+typedef struct {
+    float lr, beta2, decay_rate, eps1, eps2, d, clip_threshold, weight_decay;
+    int32_t mode;
+} optim_factored_hparams_t;
+
+/* Registers `n` tensors as one group (n >= 1) and allocates the group's device tables
+ * (tensor table, chunk table, per-tensor scale records).  Synchronises (one upload).
+ * All scale records start at zero; the u16 m codes must start at 32768 and v codes at 0 (the
+ * zero point), fp32 moments and factored states at 0. */
+int optim_group_create(const optim_tensor_desc_t* tensors, int32_t n, int32_t kind,
+                       optim_group_t** out);
+int optim_group_destroy(optim_group_t* group);
+
+/* One fused NAdam(W)/Adam step of every tensor of a NADAM group, in one pass per element:
+ * rebuild the fp32 master from (w_bf16, res_u16), decode m and v, update the moments, apply
+ * decoupled decay and the bias-corrected (Nesterov) update, split the master back into
+ * (w_bf16, res_u16), re-encode m and v, and reduce the per-tensor maxima that bound the next
+ * step's scales.  Before it, a pre-pass reduces max|g| per u16 tensor.
+ * ("Kahan summation for Adafactor-optimized Flux FFT", sd-scripts PR #2159, first comment:
+ * the 16 clipped low bits restore the bit-identical f32; PR #2187, second post: scaled,
+ * biased, pow()-companded uint16 moments.)
+ *   grads_bf16 : host array of n device pointers, one bf16 gradient per tensor, same order as at
+ *                create (may change from call to call; unchanged pointers cost no upload)
+ *   step       : 1 on the first call, then previous + 1; anything else is OPTIM_EINVAL
+ * Two enqueued kernels (one if every tensor has 4096 or fewer elements). */
+int optim_step_nadam_kahan(optim_group_t* group, const void* const* grads_bf16, int64_t step,
+                           const optim_nadam_hparams_t* hp, void* stream);
+
+/* One factored-second-moment step (Adafactor / Prodigy with beta1 = 0) of a FACTORED group:
+ * row and column EMAs of g^2 over the last two dims, rank-1 reconstruction
+ * V_ij = R_i C_j / mean(R), update u = g / sqrt(V), RMS clipping, decoupled decay, Kahan split.
+ * 1-D tensors keep a full second moment.  Arguments as optim_step_nadam_kahan. */
+int optim_step_factored(optim_group_t* group, const void* const* grads_bf16, int64_t step,
+                        const optim_factored_hparams_t* hp, void* stream);
+
+/* Encodes n fp32 moments into u16 codes with the engine's codec.  scale (device, 1 float) is
+ * written with max|src| (is_signed = 1, exp_avg) or max src (is_signed = 0, exp_avg_sq); codes
+ * are 32768 + sgn(x) rint(32767 sqrt(|x|/S)) or rint(65535 (x/S)^(1/4)).  Two kernels. */
+int state_pack_u16(const float* src, uint16_t* codes, float* scale, int64_t n, int32_t is_signed,
+                   void* stream);
+/* Decodes n u16 codes with the device scale: S t|t|, t = (c-32768)/32767, or S z^4, z = c/65535. */
+int state_unpack_u16(const uint16_t* codes, const float* scale, float* dst, int64_t n,
+                     int32_t is_signed, void* stream);
+
+/* fp32 <-> (bf16 upper half, uint16 lower half), bit-exact both ways.  hi/lo/src/dst device. */
+int optim_kahan_split(const float* src, uint16_t* hi, uint16_t* lo, int64_t n, void* stream);
+int optim_kahan_merge(const uint16_t* hi, const uint16_t* lo, float* dst, int64_t n, void* stream);
+
+/* Per-tensor scale records after the last completed step, 4 floats per tensor in group order:
+ * S_m, S_v (scales the stored codes were encoded with), A_m, A_v (max |m| and max v before
+ * encoding).  host_out holds 4*n floats.  Synchronises the group's last stream. */
+int optim_query_scales(optim_group_t* group, float* host_out);
+/* Restores scale records (same layout) before the next step, e.g. on checkpoint resume. */
+int optim_set_scales(optim_group_t* group, const float* host_in);
+/* Step counter and NAdam momentum product (the product of mu_1..mu_t, kept in double). */
+int optim_group_get_step(optim_group_t* group, int64_t* step, double* mu_product);
+int optim_group_set_step(optim_group_t* group, int64_t step, double mu_product);
+/* Number of updated weights that came out non-finite, summed over all steps so far. */
+int optim_query_nonfinite(optim_group_t* group, uint64_t* count);
+
+/* Profiling hook: when `event` (a cudaEvent_t passed as void*) is not NULL, the next step calls
+ * of this group record it on their stream between the pre-pass (gradient max, or the factored
+ * statistics passes) and the update kernel, so that a caller can time the two phases with its
+ * own events around the call.  NULL turns it off. */
+int optim_group_set_profile_event(optim_group_t* group, void* event);
+
+const char* optim_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LMOPT_H */

@@ -1,0 +1,144 @@
+// common.cuh -- device helpers and tables shared by the engine's kernels (sm_103a).
+//
+// Every floating-point operation on the state path is an explicit round-to-nearest intrinsic
+// (__fmul_rn, __fadd_rn, __fsqrt_rn, __fdiv_rn), which the compiler never fuses into FMA; the
+// library is also built with --fmad=false.  The results are therefore the IEEE fp32 results of
+// the operation order written here, on every run.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <float.h>
+#include <stdint.h>
+
+#include "../../include/lmopt.h"
+
+namespace lmo {
+
+constexpr int kThreads = 256;          // threads per CTA of the streaming kernels
+constexpr int64_t kChunk = 16384;      // elements per CTA (u16-state tensors); multiple of 8
+constexpr int64_t kSmall = OPTIM_SMALL_NUMEL;
+
+// Flags of a tensor record.
+constexpr int32_t kFlagSmall = 1;      // fp32 moments (numel <= 4096)
+constexpr int32_t kFlagRes = 2;        // has a Kahan residual
+
+// One parameter tensor, as the kernels see it.  48 bytes.
+struct TensorRec {
+    uint16_t* w;
+    uint16_t* res;
+    void* m;
+    void* v;
+    int64_t numel;
+    int32_t flags;
+    int32_t pad;
+};
+
+// Per-tensor scale record of the u16 codec, double-buffered by step parity p:
+// slot p is written by the step with parity p and read (as "previous") by the next step.
+//   s_m, s_v : scales the codes were encoded with
+//   a_m, a_v : max |m|, max v before encoding (fp32 bit patterns, atomicMax'ed)
+//   g        : max |g| of the step's gradient (fp32 bit pattern of the bf16 magnitude)
+struct ScaleRec {
+    float s_m[2];
+    float s_v[2];
+    uint32_t a_m[2];
+    uint32_t a_v[2];
+    uint32_t g[2];
+    uint32_t pad[6];
+};
+static_assert(sizeof(ScaleRec) == 64, "ScaleRec layout");
+
+// One CTA's work item: elements [index*kChunk, min(numel, (index+1)*kChunk)) of a tensor.
+struct Chunk {
+    int32_t tensor;
+    int32_t index;
+};
+
+__device__ __forceinline__ float bf16_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
+
+// Round-to-nearest-even fp32 -> bf16 bits (store used when no residual is kept); NaN keeps
+// its payload's upper bits with the quiet bit set.
+__device__ __forceinline__ uint32_t rne_bf16(float x) {
+    uint32_t b = __float_as_uint(x);
+    if ((b & 0x7F800000u) == 0x7F800000u && (b & 0x007FFFFFu) != 0u) return (b >> 16) | 0x0040u;
+    uint32_t up = b >> 16, rem = b & 0xFFFFu;
+    up += (rem > 0x8000u || (rem == 0x8000u && (up & 1u))) ? 1u : 0u;
+    return up & 0xFFFFu;
+}
+
+// ---- u16 companded codec (exp_avg: exponent 1/2, bias 32768; exp_avg_sq: exponent 1/4) ----
+__device__ __forceinline__ float inv_scale_m(float s) {
+    return s > 0.0f ? fminf(__fdiv_rn(1.0f, s), FLT_MAX) : 0.0f;
+}
+__device__ __forceinline__ float inv_scale_v(float s) {
+    return s > 0.0f ? __fdiv_rn(1.0f, __fsqrt_rn(s)) : 0.0f;
+}
+__device__ __forceinline__ float dec_m(uint32_t c, float s) {
+    float t = __fmul_rn(__int2float_rn((int)c - 32768), 1.0f / 32767.0f);
+    return __fmul_rn(__fmul_rn(t, fabsf(t)), s);
+}
+__device__ __forceinline__ float dec_v(uint32_t c, float s) {
+    float z = __fmul_rn(__uint2float_rn(c), 1.0f / 65535.0f);
+    float z2 = __fmul_rn(z, z);
+    return __fmul_rn(__fmul_rn(z2, z2), s);
+}
+__device__ __forceinline__ uint32_t enc_m(float m, float inv) {
+    float y = __fsqrt_rn(__fmul_rn(fabsf(m), inv));
+    uint32_t k = __float2uint_rn(fminf(__fmul_rn(y, 32767.0f), 32767.0f));
+    return (__float_as_uint(m) >> 31) ? 32768u - k : 32768u + k;
+}
+// sv = sqrt(v), shared with the update's denominator.
+__device__ __forceinline__ uint32_t enc_v(float sv, float rs) {
+    float y = __fsqrt_rn(__fmul_rn(sv, rs));
+    return __float2uint_rn(fminf(__fmul_rn(y, 65535.0f), 65535.0f));
+}
+
+// ---- block reductions (kThreads threads) ----
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = max(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+    return x;
+}
+__device__ __forceinline__ uint32_t warp_sum_u32(uint32_t x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+    return x;
+}
+__device__ __forceinline__ float warp_sum_f32(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = __fadd_rn(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+    return x;
+}
+
+// Max over the block of up to three values; result valid in thread 0.
+template <int N>
+__device__ __forceinline__ void block_max_u32(uint32_t (&v)[N], uint32_t* smem /* N*32 */) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = warp_max_u32(v[i]);
+    if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) smem[i * 32 + warp] = v[i];
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = blockDim.x >> 5;
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            uint32_t x = lane < nw ? smem[i * 32 + lane] : 0u;
+            v[i] = warp_max_u32(x);
+        }
+    }
+}
+
+// Streaming 128-bit loads and stores: data touched once per step, evict first.
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(uint4* p, uint4 v) { __stcs(p, v); }
+__device__ __forceinline__ float4 ld_stream(const float4* p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(float4* p, float4 v) { __stcs(p, v); }
+
+__device__ __forceinline__ bool aligned16(const void* p) {
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0u;
+}
+
+}  // namespace lmo

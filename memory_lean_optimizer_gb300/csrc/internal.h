@@ -1,0 +1,50 @@
+// internal.h -- host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "common.cuh"
+
+namespace lmo {
+
+// Records the thread-local error message and returns `code`.
+int set_error(int code, const char* fmt, ...);
+// OPTIM_OK if e == cudaSuccess, else records "<what>: <cuda message>" and returns OPTIM_ECUDA.
+int check_cuda(cudaError_t e, const char* what);
+// Streaming-multiprocessor count of the current device (cached per device).
+int sm_count();
+// Grid for a grid-stride elementwise kernel over `units` work units of kThreads each.
+unsigned grid_for(int64_t units);
+
+inline bool is_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ---- launchers (each returns OPTIM_OK or OPTIM_ECUDA after checking the launch) ----
+int launch_kahan_split(const float* src, uint16_t* hi, uint16_t* lo, int64_t n, cudaStream_t s);
+int launch_kahan_merge(const uint16_t* hi, const uint16_t* lo, float* dst, int64_t n, cudaStream_t s);
+int launch_state_pack(const float* src, uint16_t* codes, float* scale, int64_t n, int is_signed,
+                      cudaStream_t s);
+int launch_state_unpack(const uint16_t* codes, const float* scale, float* dst, int64_t n,
+                        int is_signed, cudaStream_t s);
+
+// Per-step scalars of the NAdam/Adam kernel (host-computed: double, then one rounding).
+struct NadamScalars {
+    float lr, b1, omb1, b2, omb2, eps, lr_wd, c_m, c_g, k2;
+    int32_t decoupled;
+    int32_t parity;
+};
+
+struct NadamLaunch {
+    const TensorRec* tensors;
+    const uint16_t* const* grads;
+    ScaleRec* scales;
+    const Chunk* chunks;
+    unsigned long long* nonfinite;
+    int32_t n_chunks_large;   // chunks of u16-state tensors come first
+    int32_t n_chunks_total;
+};
+int launch_nadam_step(const NadamLaunch& L, const NadamScalars& k, cudaStream_t s, cudaEvent_t mid);
+
+}  // namespace lmo

@@ -1,0 +1,326 @@
+// nadam.cu -- multi-tensor fused NAdam(W)/Adam step with Kahan residual and u16 moments.
+//
+// Two kernels per group call, each one CTA per chunk of the group's chunk table:
+//  K1 k_grad_absmax : G = max|g| per u16-state tensor (the bound the encoder's scale needs before
+//                     the step's moments exist); also clears the slots the step will accumulate.
+//  K2 k_nadam_step  : per element, in one pass: merge (w_bf16, res) -> fp32 master, decode m, v,
+//                     moment EMAs, decoupled decay, bias-corrected (Nesterov) update, split,
+//                     re-encode, and the per-tensor maxima that bound the next step's scales.
+// Sources: "Kahan summation for Adafactor-optimized Flux FFT" (sd-scripts PR #2159, first
+// comment: the 16 clipped low bits restore the bit-identical f32); "Amazing Flux FFT quality on
+// a 5090" (sd-scripts PR #2187: NAdam(W) first post, u16 scaled/biased/pow()-companded moments
+// and the 4096-element fp32 rule second post, moments used only as storage third post).
+//
+// Per element the order of operations is:
+//   w  = f32(hi<<16 | lo);  g = f32(g_bf16<<16)
+//   m  = b1*m0 + (1-b1)*g;  v = b2*v0 + (1-b2)*(g*g)
+//   w  = w - (lr*wd)*w                                   (decoupled decay only)
+//   sv = sqrt(v);  den = sv*k2 + eps;  num = c_m*m + c_g*g;  w = w - lr*(num/den)
+//   (hi, lo) = split(w);  codes = enc_m(m, 1/S_m), enc_v(sv, 1/sqrt(S_v))
+// with S_m = b1*A_m(prev) + (1-b1)*G, S_v = b2*A_v(prev) + (1-b2)*G*G per tensor.
+//
+// Memory: 18 bytes per u16-state element per step (read w, res, g, m, v; write w, res, m, v),
+// 26 bytes per fp32-state element, plus 2 bytes of K1's gradient read.  All accesses are
+// 128-bit and coalesced when a tensor's buffers are 16-byte aligned.
+#include "internal.h"
+
+namespace lmo {
+namespace {
+
+struct Prm {
+    float lr, b1, omb1, b2, omb2, eps, lr_wd, c_m, c_g, k2;
+    int32_t decoupled;
+};
+
+// ------------------------------------------------------------------------------------ K1
+__global__ void __launch_bounds__(kThreads) k_grad_absmax(NadamLaunch L, int parity) {
+    __shared__ uint32_t red[32];
+    const Chunk c = L.chunks[blockIdx.x];
+    const int64_t numel = L.tensors[c.tensor].numel;
+    const uint16_t* __restrict__ g = L.grads[c.tensor];
+    ScaleRec* sr = L.scales + c.tensor;
+    const int p = parity, q = parity ^ 1;
+    if (c.index == 0 && threadIdx.x == 0) {
+        sr->a_m[p] = 0u;   // this step's maxima accumulate here
+        sr->a_v[p] = 0u;
+        sr->g[q] = 0u;     // next step's gradient max accumulates here
+    }
+    const int64_t start = (int64_t)c.index * kChunk;
+    const int64_t end = min(numel, start + kChunk);
+    uint32_t mx = 0u;
+    int64_t done = start;
+    if (aligned16(g)) {
+        const int64_t nv = (end - start) >> 3;
+        const uint4* gv = reinterpret_cast<const uint4*>(g + start);
+        int64_t i = threadIdx.x;
+        for (; i + 3 * kThreads < nv; i += 4 * kThreads) {
+            uint4 x0 = __ldcg(gv + i), x1 = __ldcg(gv + i + kThreads);
+            uint4 x2 = __ldcg(gv + i + 2 * kThreads), x3 = __ldcg(gv + i + 3 * kThreads);
+            mx = __vmaxu2(mx, __vmaxu2(x0.x & 0x7FFF7FFFu, x0.y & 0x7FFF7FFFu));
+            mx = __vmaxu2(mx, __vmaxu2(x0.z & 0x7FFF7FFFu, x0.w & 0x7FFF7FFFu));
+            mx = __vmaxu2(mx, __vmaxu2(x1.x & 0x7FFF7FFFu, x1.y & 0x7FFF7FFFu));
+            mx = __vmaxu2(mx, __vmaxu2(x1.z & 0x7FFF7FFFu, x1.w & 0x7FFF7FFFu));
+            mx = __vmaxu2(mx, __vmaxu2(x2.x & 0x7FFF7FFFu, x2.y & 0x7FFF7FFFu));
+            mx = __vmaxu2(mx, __vmaxu2(x2.z & 0x7FFF7FFFu, x2.w & 0x7FFF7FFFu));
+            mx = __vmaxu2(mx, __vmaxu2(x3.x & 0x7FFF7FFFu, x3.y & 0x7FFF7FFFu));
+            mx = __vmaxu2(mx, __vmaxu2(x3.z & 0x7FFF7FFFu, x3.w & 0x7FFF7FFFu));
+        }
+        for (; i < nv; i += kThreads) {
+            uint4 x = __ldcg(gv + i);
+            mx = __vmaxu2(mx, __vmaxu2(x.x & 0x7FFF7FFFu, x.y & 0x7FFF7FFFu));
+            mx = __vmaxu2(mx, __vmaxu2(x.z & 0x7FFF7FFFu, x.w & 0x7FFF7FFFu));
+        }
+        mx = max(mx & 0xFFFFu, mx >> 16);
+        done = start + (nv << 3);
+    }
+    for (int64_t i = done + threadIdx.x; i < end; i += kThreads) mx = max(mx, (uint32_t)(g[i] & 0x7FFFu));
+    uint32_t v[1] = {mx};
+    block_max_u32<1>(v, red);
+    if (threadIdx.x == 0 && v[0] != 0u) atomicMax(&sr->g[p], v[0] << 16);
+}
+
+// ------------------------------------------------------------------------------------ K2
+// One element.  hi/lo/g are 16-bit words; m0/v0 the decoded (or fp32) moments; outputs in place.
+__device__ __forceinline__ void elem(const Prm& k, uint32_t& hi, uint32_t& lo, bool has_res,
+                                     uint32_t gb, float& m, float& v, float& sv, uint32_t& nonfin) {
+    float w = has_res ? __uint_as_float((hi << 16) | lo) : bf16_to_f32(hi);
+    const float g = bf16_to_f32(gb);
+    m = __fadd_rn(__fmul_rn(k.b1, m), __fmul_rn(k.omb1, g));
+    v = __fadd_rn(__fmul_rn(k.b2, v), __fmul_rn(k.omb2, __fmul_rn(g, g)));
+    if (k.decoupled) w = __fsub_rn(w, __fmul_rn(k.lr_wd, w));
+    sv = __fsqrt_rn(v);
+    const float den = __fadd_rn(__fmul_rn(sv, k.k2), k.eps);
+    const float num = __fadd_rn(__fmul_rn(k.c_m, m), __fmul_rn(k.c_g, g));
+    w = __fsub_rn(w, __fmul_rn(k.lr, __fdiv_rn(num, den)));
+    const uint32_t b = __float_as_uint(w);
+    if (has_res) {
+        hi = b >> 16;
+        lo = b & 0xFFFFu;
+    } else {
+        hi = rne_bf16(w);
+    }
+    nonfin += ((b & 0x7F800000u) == 0x7F800000u) ? 1u : 0u;
+}
+
+struct Codec {
+    float s_m_dec, s_v_dec, inv_m, rs_v;
+};
+
+// Eight u16-state elements packed in 128-bit words.
+__device__ __forceinline__ void step8_u16(const Prm& k, const Codec& cd, bool has_res, uint4& W,
+                                          uint4& R, const uint4& G, uint4& M, uint4& V,
+                                          uint32_t& am, uint32_t& av, uint32_t& nonfin) {
+    uint32_t* w32 = reinterpret_cast<uint32_t*>(&W);
+    uint32_t* r32 = reinterpret_cast<uint32_t*>(&R);
+    const uint32_t* g32 = reinterpret_cast<const uint32_t*>(&G);
+    uint32_t* m32 = reinterpret_cast<uint32_t*>(&M);
+    uint32_t* v32 = reinterpret_cast<uint32_t*>(&V);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t ow = 0, orr = 0, om = 0, ov = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int sh = 16 * h;
+            uint32_t hi = (w32[j] >> sh) & 0xFFFFu, lo = (r32[j] >> sh) & 0xFFFFu;
+            const uint32_t gb = (g32[j] >> sh) & 0xFFFFu;
+            float m = dec_m((m32[j] >> sh) & 0xFFFFu, cd.s_m_dec);
+            float v = dec_v((v32[j] >> sh) & 0xFFFFu, cd.s_v_dec);
+            float sv;
+            elem(k, hi, lo, has_res, gb, m, v, sv, nonfin);
+            ow |= hi << sh;
+            orr |= lo << sh;
+            om |= enc_m(m, cd.inv_m) << sh;
+            ov |= enc_v(sv, cd.rs_v) << sh;
+            am = max(am, __float_as_uint(m) & 0x7FFFFFFFu);
+            av = max(av, __float_as_uint(v) & 0x7FFFFFFFu);
+        }
+        w32[j] = ow;
+        r32[j] = orr;
+        m32[j] = om;
+        v32[j] = ov;
+    }
+}
+
+// Eight fp32-state elements (numel <= 4096): m, v as two float4 each.
+__device__ __forceinline__ void step8_f32(const Prm& k, bool has_res, uint4& W, uint4& R,
+                                          const uint4& G, float4 (&M)[2], float4 (&V)[2],
+                                          uint32_t& nonfin) {
+    uint32_t* w32 = reinterpret_cast<uint32_t*>(&W);
+    uint32_t* r32 = reinterpret_cast<uint32_t*>(&R);
+    const uint32_t* g32 = reinterpret_cast<const uint32_t*>(&G);
+    float* mf = reinterpret_cast<float*>(&M[0]);
+    float* vf = reinterpret_cast<float*>(&V[0]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t ow = 0, orr = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int sh = 16 * h;
+            uint32_t hi = (w32[j] >> sh) & 0xFFFFu, lo = (r32[j] >> sh) & 0xFFFFu;
+            float sv;
+            elem(k, hi, lo, has_res, (g32[j] >> sh) & 0xFFFFu, mf[2 * j + h], vf[2 * j + h], sv, nonfin);
+            ow |= hi << sh;
+            orr |= lo << sh;
+        }
+        w32[j] = ow;
+        r32[j] = orr;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) k_nadam_step(NadamLaunch L, Prm k, int parity) {
+    __shared__ uint32_t red[3 * 32];
+    const Chunk c = L.chunks[blockIdx.x];
+    const TensorRec t = L.tensors[c.tensor];
+    const uint16_t* __restrict__ g = L.grads[c.tensor];
+    const int p = parity, q = parity ^ 1;
+    const bool small = (t.flags & kFlagSmall) != 0;
+    const bool has_res = (t.flags & kFlagRes) != 0;
+    const int64_t start = (int64_t)c.index * kChunk;
+    const int64_t end = min(t.numel, start + kChunk);
+
+    Codec cd = {0.f, 0.f, 0.f, 0.f};
+    ScaleRec* sr = L.scales + c.tensor;
+    if (!small) {
+        const float a_m = __uint_as_float(sr->a_m[q]), a_v = __uint_as_float(sr->a_v[q]);
+        const float G = __uint_as_float(sr->g[p]);
+        const float s_m = __fadd_rn(__fmul_rn(k.b1, a_m), __fmul_rn(k.omb1, G));
+        const float s_v = __fadd_rn(__fmul_rn(k.b2, a_v), __fmul_rn(k.omb2, __fmul_rn(G, G)));
+        cd.s_m_dec = sr->s_m[q];
+        cd.s_v_dec = sr->s_v[q];
+        cd.inv_m = inv_scale_m(s_m);
+        cd.rs_v = inv_scale_v(s_v);
+        if (c.index == 0 && threadIdx.x == 0) {
+            sr->s_m[p] = s_m;
+            sr->s_v[p] = s_v;
+        }
+    }
+
+    uint32_t am = 0u, av = 0u, nonfin = 0u;
+    uint16_t* __restrict__ w = t.w;
+    uint16_t* __restrict__ res = t.res;
+    const bool vec = aligned16(w) && (!has_res || aligned16(res)) && aligned16(t.m) &&
+                     aligned16(t.v) && aligned16(g);
+    int64_t done = start;
+    if (vec) {
+        const int64_t nv = (end - start) >> 3;
+        uint4* wv = reinterpret_cast<uint4*>(w + start);
+        uint4* rv = has_res ? reinterpret_cast<uint4*>(res + start) : nullptr;
+        const uint4* gv = reinterpret_cast<const uint4*>(g + start);
+        if (!small) {
+            uint4* mv = reinterpret_cast<uint4*>(static_cast<uint16_t*>(t.m) + start);
+            uint4* vv = reinterpret_cast<uint4*>(static_cast<uint16_t*>(t.v) + start);
+            int64_t i = threadIdx.x;
+            // two independent 8-element groups per iteration: ten 128-bit loads in flight
+            for (; i + kThreads < nv; i += 2 * kThreads) {
+                const int64_t i1 = i + kThreads;
+                uint4 W0 = ld_stream(wv + i), W1 = ld_stream(wv + i1);
+                uint4 R0 = has_res ? ld_stream(rv + i) : make_uint4(0, 0, 0, 0);
+                uint4 R1 = has_res ? ld_stream(rv + i1) : make_uint4(0, 0, 0, 0);
+                uint4 G0 = ld_stream(gv + i), G1 = ld_stream(gv + i1);
+                uint4 M0 = ld_stream(mv + i), M1 = ld_stream(mv + i1);
+                uint4 V0 = ld_stream(vv + i), V1 = ld_stream(vv + i1);
+                step8_u16(k, cd, has_res, W0, R0, G0, M0, V0, am, av, nonfin);
+                st_stream(wv + i, W0);
+                if (has_res) st_stream(rv + i, R0);
+                st_stream(mv + i, M0);
+                st_stream(vv + i, V0);
+                step8_u16(k, cd, has_res, W1, R1, G1, M1, V1, am, av, nonfin);
+                st_stream(wv + i1, W1);
+                if (has_res) st_stream(rv + i1, R1);
+                st_stream(mv + i1, M1);
+                st_stream(vv + i1, V1);
+            }
+            for (; i < nv; i += kThreads) {
+                uint4 W0 = ld_stream(wv + i);
+                uint4 R0 = has_res ? ld_stream(rv + i) : make_uint4(0, 0, 0, 0);
+                uint4 G0 = ld_stream(gv + i), M0 = ld_stream(mv + i), V0 = ld_stream(vv + i);
+                step8_u16(k, cd, has_res, W0, R0, G0, M0, V0, am, av, nonfin);
+                st_stream(wv + i, W0);
+                if (has_res) st_stream(rv + i, R0);
+                st_stream(mv + i, M0);
+                st_stream(vv + i, V0);
+            }
+        } else {
+            float4* mv = reinterpret_cast<float4*>(static_cast<float*>(t.m) + start);
+            float4* vv = reinterpret_cast<float4*>(static_cast<float*>(t.v) + start);
+            for (int64_t i = threadIdx.x; i < nv; i += kThreads) {
+                uint4 W0 = ld_stream(wv + i);
+                uint4 R0 = has_res ? ld_stream(rv + i) : make_uint4(0, 0, 0, 0);
+                uint4 G0 = ld_stream(gv + i);
+                float4 M[2] = {ld_stream(mv + 2 * i), ld_stream(mv + 2 * i + 1)};
+                float4 V[2] = {ld_stream(vv + 2 * i), ld_stream(vv + 2 * i + 1)};
+                step8_f32(k, has_res, W0, R0, G0, M, V, nonfin);
+                st_stream(wv + i, W0);
+                if (has_res) st_stream(rv + i, R0);
+                st_stream(mv + 2 * i, M[0]);
+                st_stream(mv + 2 * i + 1, M[1]);
+                st_stream(vv + 2 * i, V[0]);
+                st_stream(vv + 2 * i + 1, V[1]);
+            }
+        }
+        done = start + (nv << 3);
+    }
+    // element-by-element: ragged tail, or the whole chunk when a buffer is not 16-byte aligned
+    for (int64_t i = done + threadIdx.x; i < end; i += kThreads) {
+        uint32_t hi = w[i], lo = has_res ? res[i] : 0u;
+        float m, v, sv;
+        if (small) {
+            m = static_cast<float*>(t.m)[i];
+            v = static_cast<float*>(t.v)[i];
+        } else {
+            m = dec_m(static_cast<uint16_t*>(t.m)[i], cd.s_m_dec);
+            v = dec_v(static_cast<uint16_t*>(t.v)[i], cd.s_v_dec);
+        }
+        elem(k, hi, lo, has_res, g[i], m, v, sv, nonfin);
+        w[i] = (uint16_t)hi;
+        if (has_res) res[i] = (uint16_t)lo;
+        if (small) {
+            static_cast<float*>(t.m)[i] = m;
+            static_cast<float*>(t.v)[i] = v;
+        } else {
+            static_cast<uint16_t*>(t.m)[i] = (uint16_t)enc_m(m, cd.inv_m);
+            static_cast<uint16_t*>(t.v)[i] = (uint16_t)enc_v(sv, cd.rs_v);
+            am = max(am, __float_as_uint(m) & 0x7FFFFFFFu);
+            av = max(av, __float_as_uint(v) & 0x7FFFFFFFu);
+        }
+    }
+
+    // per-tensor maxima for the next step's scales, and the non-finite count
+    uint32_t r[2] = {am, av};
+    nonfin = warp_sum_u32(nonfin);
+    block_max_u32<2>(r, red);
+    __shared__ uint32_t nf[32];
+    if ((threadIdx.x & 31) == 0) nf[threadIdx.x >> 5] = nonfin;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t tot = 0;
+        for (int wi = 0; wi < kThreads / 32; ++wi) tot += nf[wi];
+        if (!small) {
+            if (r[0]) atomicMax(&sr->a_m[p], r[0]);
+            if (r[1]) atomicMax(&sr->a_v[p], r[1]);
+        }
+        if (tot) atomicAdd(L.nonfinite, (unsigned long long)tot);
+    }
+}
+
+}  // namespace
+
+int launch_nadam_step(const NadamLaunch& L, const NadamScalars& s, cudaStream_t stream, cudaEvent_t mid) {
+    Prm k{s.lr, s.b1, s.omb1, s.b2, s.omb2, s.eps, s.lr_wd, s.c_m, s.c_g, s.k2, s.decoupled};
+    if (L.n_chunks_large > 0) {
+        k_grad_absmax<<<L.n_chunks_large, kThreads, 0, stream>>>(L, s.parity);
+        int rc = check_cuda(cudaGetLastError(), "grad absmax launch");
+        if (rc) return rc;
+    }
+    if (mid) {
+        int rc = check_cuda(cudaEventRecord(mid, stream), "profile event");
+        if (rc) return rc;
+    }
+    if (L.n_chunks_total > 0) {
+        k_nadam_step<<<L.n_chunks_total, kThreads, 0, stream>>>(L, k, s.parity);
+        return check_cuda(cudaGetLastError(), "nadam step launch");
+    }
+    return OPTIM_OK;
+}
+
+}  // namespace lmo

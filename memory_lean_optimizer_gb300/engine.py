@@ -1,0 +1,202 @@
+"""Torch-facing parameter groups over liblmopt.so.
+
+PyTorch provides device memory and streams only: every step, split, merge, pack and unpack is a
+library kernel called through the C ABI (``lmopt``).  A group owns the optimizer state of its
+tensors (Kahan residuals, moments or factored statistics) as torch tensors, registers them once
+with ``optim_group_create`` and then steps them with one library call per group -- the
+granularity of the fused backward pass and of optimizer groups ("Fused backward pass" commit,
+README: per-parameter hook, optimizer groups of 4-10).
+"""
+from __future__ import annotations
+
+from typing import Sequence
+
+import torch
+
+from . import lmopt
+
+SMALL = lmopt.SMALL_NUMEL
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _u16_empty(n: int, device, fill: int | None = None) -> torch.Tensor:
+    """A uint16 buffer held as int16 storage (bit pattern only)."""
+    t = torch.empty(n, dtype=torch.int16, device=device)
+    if fill is not None:
+        t.fill_(fill - 65536 if fill >= 32768 else fill)
+    return t
+
+
+def kahan_split(master: torch.Tensor, hi: torch.Tensor | None = None, lo: torch.Tensor | None = None, stream=None):
+    """fp32 master -> (bf16 weight, int16-stored residual) via the library kernel."""
+    assert master.dtype == torch.float32 and master.is_cuda and master.is_contiguous()
+    if hi is None:
+        hi = torch.empty(master.shape, dtype=torch.bfloat16, device=master.device)
+    if lo is None:
+        lo = _u16_empty(master.numel(), master.device)
+    lmopt.optim_kahan_split(master.data_ptr(), hi.data_ptr(), lo.data_ptr(), master.numel(), _stream_ptr(stream))
+    return hi, lo
+
+
+def kahan_merge(hi: torch.Tensor, lo: torch.Tensor, out: torch.Tensor | None = None, stream=None):
+    if out is None:
+        out = torch.empty(hi.shape, dtype=torch.float32, device=hi.device)
+    lmopt.optim_kahan_merge(hi.data_ptr(), lo.data_ptr(), out.data_ptr(), hi.numel(), _stream_ptr(stream))
+    return out
+
+
+def state_pack(x: torch.Tensor, is_signed: bool, stream=None):
+    codes = _u16_empty(x.numel(), x.device)
+    scale = torch.empty(1, dtype=torch.float32, device=x.device)
+    lmopt.state_pack_u16(x.data_ptr(), codes.data_ptr(), scale.data_ptr(), x.numel(), is_signed, _stream_ptr(stream))
+    return codes, scale
+
+
+def state_unpack(codes: torch.Tensor, scale: torch.Tensor, is_signed: bool, stream=None):
+    out = torch.empty(codes.numel(), dtype=torch.float32, device=codes.device)
+    lmopt.state_unpack_u16(codes.data_ptr(), scale.data_ptr(), out.data_ptr(), codes.numel(), is_signed,
+                           _stream_ptr(stream))
+    return out
+
+
+def _desc(w, res, m, v, shape) -> lmopt.TensorDesc:
+    d = lmopt.TensorDesc()
+    d.w_bf16 = w.data_ptr() if w.numel() else None
+    d.res_u16 = res.data_ptr() if (res is not None and res.numel()) else None
+    d.m = m.data_ptr() if (m is not None and m.numel()) else None
+    d.v = v.data_ptr() if (v is not None and v.numel()) else None
+    d.numel = w.numel()
+    shape = tuple(shape) if len(shape) else (w.numel(),)
+    d.ndim = len(shape)
+    for i, s in enumerate(shape):
+        d.shape[i] = int(s)
+    return d
+
+
+class _Group:
+    kind = -1
+
+    def __init__(self):
+        self.handle = None
+        self.step_count = 0
+
+    def close(self):
+        if self.handle:
+            lmopt.optim_group_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _grad_ptrs(self, grads):
+        assert len(grads) == len(self.weights)
+        ptrs = []
+        for g, w in zip(grads, self.weights):
+            assert g.dtype == torch.bfloat16 and g.is_contiguous() and g.numel() == w.numel()
+            ptrs.append(g.data_ptr() if g.numel() else None)
+        return ptrs
+
+
+class NadamGroup(_Group):
+    """Kahan + u16-moment NAdam(W)/Adam state for a list of bf16 weights (one library group)."""
+
+    kind = lmopt.OPTIM_KIND_NADAM
+
+    def __init__(self, weights: Sequence[torch.Tensor], residuals: Sequence[torch.Tensor] | None = None,
+                 kahan: bool = True):
+        super().__init__()
+        self.weights = list(weights)
+        for w in self.weights:
+            assert w.dtype == torch.bfloat16 and w.is_cuda and w.is_contiguous()
+        dev = self.weights[0].device
+        if residuals is None:
+            residuals = [_u16_empty(w.numel(), dev, 0) if kahan else None for w in self.weights]
+        self.res = list(residuals)
+        self.m, self.v = [], []
+        for w in self.weights:
+            n = w.numel()
+            if n <= SMALL:
+                self.m.append(torch.zeros(n, dtype=torch.float32, device=dev))
+                self.v.append(torch.zeros(n, dtype=torch.float32, device=dev))
+            else:
+                self.m.append(_u16_empty(n, dev, 32768))
+                self.v.append(_u16_empty(n, dev, 0))
+        descs = [_desc(w, r, m, v, w.shape) for w, r, m, v in zip(self.weights, self.res, self.m, self.v)]
+        self.handle = lmopt.optim_group_create(descs, self.kind)
+
+    @classmethod
+    def from_masters(cls, masters: Sequence[torch.Tensor], stream=None):
+        ws, rs = [], []
+        for x in masters:
+            hi, lo = kahan_split(x.contiguous(), stream=stream)
+            ws.append(hi)
+            rs.append(lo)
+        return cls(ws, rs)
+
+    def step(self, grads: Sequence[torch.Tensor], hp: dict, stream=None):
+        h = lmopt.NadamHparams(lr=hp["lr"], beta1=hp["beta1"], beta2=hp["beta2"], eps=hp["eps"],
+                               weight_decay=hp.get("weight_decay", 0.0), wd_mode=hp.get("wd_mode", 0),
+                               nesterov=hp.get("nesterov", 1), momentum_decay=hp.get("momentum_decay", 0.004))
+        lmopt.optim_step_nadam_kahan(self.handle, self._grad_ptrs(grads), self.step_count + 1, h, _stream_ptr(stream))
+        self.step_count += 1
+
+    def masters(self):
+        return [kahan_merge(w, r) for w, r in zip(self.weights, self.res)]
+
+    def scales(self):
+        return lmopt.optim_query_scales(self.handle, len(self.weights))
+
+
+class FactoredGroup(_Group):
+    """Adafactor / Prodigy factored-second-moment state (beta1 = 0, no exp_avg)."""
+
+    kind = lmopt.OPTIM_KIND_FACTORED
+
+    def __init__(self, weights: Sequence[torch.Tensor], residuals: Sequence[torch.Tensor] | None = None,
+                 kahan: bool = True):
+        super().__init__()
+        self.weights = list(weights)
+        dev = self.weights[0].device
+        if residuals is None:
+            residuals = [_u16_empty(w.numel(), dev, 0) if kahan else None for w in self.weights]
+        self.res = list(residuals)
+        self.row, self.col = [], []
+        for w in self.weights:
+            shape = tuple(w.shape)
+            if len(shape) >= 2:
+                lead = int(torch.tensor(shape[:-2]).prod().item()) if len(shape) > 2 else 1
+                self.row.append(torch.zeros(lead * shape[-2], dtype=torch.float32, device=dev))
+                self.col.append(torch.zeros(lead * shape[-1], dtype=torch.float32, device=dev))
+            else:
+                self.row.append(None)
+                self.col.append(torch.zeros(w.numel(), dtype=torch.float32, device=dev))
+        descs = [_desc(w, r, m, v, w.shape) for w, r, m, v in zip(self.weights, self.res, self.row, self.col)]
+        self.handle = lmopt.optim_group_create(descs, self.kind)
+
+    @classmethod
+    def from_masters(cls, masters: Sequence[torch.Tensor], stream=None):
+        ws, rs = [], []
+        for x in masters:
+            hi, lo = kahan_split(x.contiguous(), stream=stream)
+            ws.append(hi)
+            rs.append(lo)
+        return cls(ws, rs)
+
+    def step(self, grads: Sequence[torch.Tensor], hp: dict, stream=None):
+        h = lmopt.FactoredHparams(lr=hp["lr"], beta2=hp.get("beta2", 0.999), decay_rate=hp.get("decay_rate", -0.8),
+                                  eps1=hp.get("eps1", 1e-30), eps2=hp.get("eps2", 1e-30), d=hp.get("d", 1.0),
+                                  clip_threshold=hp.get("clip_threshold", 1.0),
+                                  weight_decay=hp.get("weight_decay", 0.0), mode=hp.get("mode", 0))
+        lmopt.optim_step_factored(self.handle, self._grad_ptrs(grads), self.step_count + 1, h, _stream_ptr(stream))
+        self.step_count += 1
+
+    def masters(self):
+        return [kahan_merge(w, r) for w, r in zip(self.weights, self.res)]

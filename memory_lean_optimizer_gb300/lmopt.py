@@ -1,0 +1,190 @@
+"""Thin ctypes binding of liblmopt.so (include/lmopt.h): argument marshalling only.
+
+Every function here has the name of its C entry point and takes plain integers for device
+pointers (``tensor.data_ptr()``) and streams (``torch.cuda.Stream.cuda_stream``); all work runs in
+the library's CUDA kernels.  The library must have been built (``memory_lean_optimizer_gb300.build``):
+there is no fallback, and a missing library raises at first use.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "liblmopt.so")
+
+OPTIM_OK = 0
+OPTIM_EINVAL = -1
+OPTIM_ECUDA = -2
+OPTIM_ENOMEM = -3
+OPTIM_EALIGN = -4
+OPTIM_ETIMEOUT = -5
+OPTIM_ENONFINITE = -6
+OPTIM_ESTATE = -7
+OPTIM_KIND_NADAM = 0
+OPTIM_KIND_FACTORED = 1
+SMALL_NUMEL = 4096
+
+ERROR_NAMES = {OPTIM_EINVAL: "EINVAL", OPTIM_ECUDA: "ECUDA", OPTIM_ENOMEM: "ENOMEM", OPTIM_EALIGN: "EALIGN",
+               OPTIM_ETIMEOUT: "ETIMEOUT", OPTIM_ENONFINITE: "ENONFINITE", OPTIM_ESTATE: "ESTATE"}
+
+EXPORTED = (
+    "optim_group_create", "optim_group_destroy", "optim_step_nadam_kahan", "optim_step_factored",
+    "state_pack_u16", "state_unpack_u16", "optim_kahan_split", "optim_kahan_merge",
+    "optim_query_scales", "optim_set_scales", "optim_group_get_step", "optim_group_set_step",
+    "optim_query_nonfinite", "optim_group_set_profile_event", "optim_last_error",
+)
+
+
+class LmoptError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{ERROR_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+class TensorDesc(ctypes.Structure):
+    _fields_ = [("w_bf16", ctypes.c_void_p), ("res_u16", ctypes.c_void_p), ("m", ctypes.c_void_p),
+                ("v", ctypes.c_void_p), ("numel", ctypes.c_int64), ("ndim", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("shape", ctypes.c_int64 * 4)]
+
+
+class NadamHparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("wd_mode", ctypes.c_int32),
+                ("nesterov", ctypes.c_int32), ("momentum_decay", ctypes.c_float)]
+
+
+class FactoredHparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta2", ctypes.c_float), ("decay_rate", ctypes.c_float),
+                ("eps1", ctypes.c_float), ("eps2", ctypes.c_float), ("d", ctypes.c_float),
+                ("clip_threshold", ctypes.c_float), ("weight_decay", ctypes.c_float), ("mode", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Loads liblmopt.so (once) and declares its signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with `python -m memory_lean_optimizer_gb300.build` "
+                               "(the engine has no CPU fallback)")
+        lib = ctypes.CDLL(path)
+        P, I32, I64, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+        sig = {
+            "optim_group_create": [ctypes.POINTER(TensorDesc), I32, I32, ctypes.POINTER(P)],
+            "optim_group_destroy": [P],
+            "optim_step_nadam_kahan": [P, P, I64, ctypes.POINTER(NadamHparams), P],
+            "optim_step_factored": [P, P, I64, ctypes.POINTER(FactoredHparams), P],
+            "state_pack_u16": [P, P, P, I64, I32, P],
+            "state_unpack_u16": [P, P, P, I64, I32, P],
+            "optim_kahan_split": [P, P, P, I64, P],
+            "optim_kahan_merge": [P, P, P, I64, P],
+            "optim_query_scales": [P, P],
+            "optim_set_scales": [P, P],
+            "optim_group_get_step": [P, ctypes.POINTER(I64), ctypes.POINTER(ctypes.c_double)],
+            "optim_group_set_step": [P, I64, ctypes.c_double],
+            "optim_query_nonfinite": [P, ctypes.POINTER(ctypes.c_uint64)],
+            "optim_group_set_profile_event": [P, P],
+        }
+        for name, args in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        lib.optim_last_error.argtypes = []
+        lib.optim_last_error.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def last_error() -> str:
+    return load().optim_last_error().decode()
+
+
+def check(rc: int) -> int:
+    if rc != OPTIM_OK:
+        raise LmoptError(rc, last_error())
+    return rc
+
+
+def _ptr_array(ptrs):
+    arr = (ctypes.c_void_p * max(1, len(ptrs)))()
+    for i, p in enumerate(ptrs):
+        arr[i] = p
+    return arr
+
+
+# ------------------------------------------------------------------ raw entry points (same names)
+def optim_group_create(descs, kind: int) -> int:
+    """descs: sequence of TensorDesc; returns the opaque handle as an int."""
+    arr = (TensorDesc * len(descs))(*descs)
+    out = ctypes.c_void_p()
+    check(load().optim_group_create(arr, len(descs), kind, ctypes.byref(out)))
+    return out.value
+
+
+def optim_group_destroy(handle: int) -> None:
+    check(load().optim_group_destroy(handle))
+
+
+def optim_step_nadam_kahan(handle: int, grad_ptrs, step: int, hp: NadamHparams, stream: int = 0) -> None:
+    check(load().optim_step_nadam_kahan(handle, _ptr_array(grad_ptrs), step, ctypes.byref(hp), stream))
+
+
+def optim_step_factored(handle: int, grad_ptrs, step: int, hp: FactoredHparams, stream: int = 0) -> None:
+    check(load().optim_step_factored(handle, _ptr_array(grad_ptrs), step, ctypes.byref(hp), stream))
+
+
+def state_pack_u16(src: int, codes: int, scale: int, n: int, is_signed: bool, stream: int = 0) -> None:
+    check(load().state_pack_u16(src, codes, scale, n, int(is_signed), stream))
+
+
+def state_unpack_u16(codes: int, scale: int, dst: int, n: int, is_signed: bool, stream: int = 0) -> None:
+    check(load().state_unpack_u16(codes, scale, dst, n, int(is_signed), stream))
+
+
+def optim_kahan_split(src: int, hi: int, lo: int, n: int, stream: int = 0) -> None:
+    check(load().optim_kahan_split(src, hi, lo, n, stream))
+
+
+def optim_kahan_merge(hi: int, lo: int, dst: int, n: int, stream: int = 0) -> None:
+    check(load().optim_kahan_merge(hi, lo, dst, n, stream))
+
+
+def optim_query_scales(handle: int, n: int):
+    """Returns a list of (S_m, S_v, A_m, A_v) per tensor after the last completed step."""
+    buf = (ctypes.c_float * (4 * n))()
+    check(load().optim_query_scales(handle, buf))
+    return [tuple(buf[4 * i:4 * i + 4]) for i in range(n)]
+
+
+def optim_set_scales(handle: int, records) -> None:
+    flat = [float(x) for r in records for x in r]
+    buf = (ctypes.c_float * len(flat))(*flat)
+    check(load().optim_set_scales(handle, buf))
+
+
+def optim_group_get_step(handle: int):
+    step, mp = ctypes.c_int64(), ctypes.c_double()
+    check(load().optim_group_get_step(handle, ctypes.byref(step), ctypes.byref(mp)))
+    return step.value, mp.value
+
+
+def optim_group_set_step(handle: int, step: int, mu_product: float) -> None:
+    check(load().optim_group_set_step(handle, step, mu_product))
+
+
+def optim_group_set_profile_event(handle: int, event: int | None) -> None:
+    """event: a cudaEvent_t as int (torch.cuda.Event.cuda_event), or None to turn the hook off."""
+    check(load().optim_group_set_profile_event(handle, event))
+
+
+def optim_query_nonfinite(handle: int) -> int:
+    c = ctypes.c_uint64()
+    check(load().optim_query_nonfinite(handle, ctypes.byref(c)))
+    return c.value

@@ -1,0 +1,189 @@
+"""GPU parity of the fused multi-tensor NAdam(W)/Adam + Kahan + u16-moment step against the oracle,
+through the C ABI.  Weights, residuals and moment codes must be bit-identical to the oracle's
+after every step; per-tensor scale records equal."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import OracleNadam, alloc_offset, assert_nadam_equal, cuda_bits
+from memory_lean_optimizer_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+HP = dict(W.NADAM_HP)
+
+
+@pytest.fixture(scope="module")
+def eng():
+    from memory_lean_optimizer_gb300 import build, engine
+    build.build()
+    return engine
+
+
+def run_parity(orc, eng, shapes, steps, hp, seed=0, g_std=1e-3, zero_frac=0.0, kahan=True, check_every=True):
+    masters = [W.master_weights(s, seed, i) for i, s in enumerate(shapes)]
+    ora = OracleNadam(orc, [m.numpy() for m in masters], kahan=kahan)
+    if kahan:
+        grp = eng.NadamGroup.from_masters([m.cuda() for m in masters])
+    else:
+        grp = eng.NadamGroup([m.cuda().to(torch.bfloat16) for m in masters], kahan=False)
+    for t in range(1, steps + 1):
+        grads = [W.grad_bf16(s, seed, i, t, g_std, zero_frac=zero_frac) for i, s in enumerate(shapes)]
+        ora.step([W.bits16(g).reshape(-1) for g in grads], hp)
+        grp.step([g.cuda() for g in grads], hp)
+        if check_every or t == steps:
+            torch.cuda.synchronize()
+            assert_nadam_equal(ora, grp, f"step {t}")
+            got = grp.scales()
+            for i, (a, b) in enumerate(zip(got, ora.scales())):
+                if W.numel(shapes[i]) > 4096:
+                    assert a == pytest.approx(b, rel=0, abs=0), (i, a, b)
+    return ora, grp
+
+
+def test_one_1024x1024_ten_steps(orc, eng):
+    """The 1024x1024 single-tensor workload, NAdam, lr 3.5e-6, 10 steps, seed 0."""
+    run_parity(orc, eng, [(1024, 1024)], 10, HP, g_std=1e-3)
+
+
+@pytest.mark.parametrize("variant", ["adam", "nadam", "nadamw", "adamw"])
+def test_ragged_group_all_paths(orc, eng, variant):
+    """Sizes around every boundary: fp32-state (<=4096) and u16 tensors, ragged tails, several
+    chunks, sizes not multiple of 8."""
+    sizes = [1, 7, 8, 63, 64, 4095, 4096, 4097, 16383, 16384, 16385, 50001, 131075, 1 << 18]
+    hp = dict(HP, lr=1e-4, nesterov=variant.startswith("n"),
+              weight_decay=0.05 if variant.endswith("w") else 0.0, wd_mode=1 if variant.endswith("w") else 0)
+    run_parity(orc, eng, [(n,) for n in sizes], 4, hp, seed=3, zero_frac=0.01)
+
+
+def test_no_residual_store(orc, eng):
+    """res = NULL: the weight is stored round-to-nearest-even, as the oracle's bf16 store."""
+    sizes = [100, 5000, 40000]
+    run_parity(orc, eng, [(n,) for n in sizes], 3, dict(HP, lr=1e-3), seed=4, kahan=False)
+
+
+def test_misaligned_buffers_take_scalar_path(orc, eng):
+    """Buffers 2-byte (not 16-byte) aligned go element by element and give identical bits."""
+    from memory_lean_optimizer_gb300 import lmopt
+    sizes = [3000, 20001, 70000]
+    seed = 5
+    masters = [W.master_weights((n,), seed, i) for i, n in enumerate(sizes)]
+    ora = OracleNadam(orc, [m.numpy() for m in masters])
+    keep, descs, ws, rs, ms, vs = [], [], [], [], [], []
+    for i, n in enumerate(sizes):
+        hi, lo = orc.kahan_split(masters[i].numpy())
+        b1, w = alloc_offset(n, torch.int16, 1)
+        b2, r = alloc_offset(n, torch.int16, 3)
+        w.copy_(torch.from_numpy(hi.view(np.int16)))
+        r.copy_(torch.from_numpy(lo.view(np.int16)))
+        if n <= 4096:
+            b3, m = alloc_offset(n, torch.float32, 1)
+            b4, v = alloc_offset(n, torch.float32, 1)
+        else:
+            b3, m = alloc_offset(n, torch.int16, 5, fill=-32768)
+            b4, v = alloc_offset(n, torch.int16, 7)
+        keep += [b1, b2, b3, b4]
+        d = lmopt.TensorDesc(w_bf16=w.data_ptr(), res_u16=r.data_ptr(), m=m.data_ptr(), v=v.data_ptr(),
+                             numel=n, ndim=1)
+        d.shape[0] = n
+        descs.append(d)
+        ws.append(w), rs.append(r), ms.append(m), vs.append(v)
+    h = lmopt.optim_group_create(descs, lmopt.OPTIM_KIND_NADAM)
+    hp = dict(HP, lr=1e-3)
+    H = lmopt.NadamHparams(lr=hp["lr"], beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, wd_mode=0,
+                           nesterov=1, momentum_decay=0.004)
+    try:
+        for t in range(1, 4):
+            grads = [W.grad_bf16((n,), seed, i, t, 1e-3) for i, n in enumerate(sizes)]
+            ora.step([W.bits16(g) for g in grads], hp)
+            gbufs = []
+            for g in grads:
+                b, gg = alloc_offset(g.numel(), torch.int16, 1)
+                gg.copy_(g.view(torch.int16))
+                gbufs += [b, gg]
+            lmopt.optim_step_nadam_kahan(h, [gbufs[2 * i + 1].data_ptr() for i in range(len(sizes))], t, H, 0)
+            torch.cuda.synchronize()
+            for i, ot in enumerate(ora.t):
+                assert np.array_equal(cuda_bits(ws[i]), ot["hi"])
+                assert np.array_equal(cuda_bits(rs[i]), ot["lo"])
+                if sizes[i] > 4096:
+                    assert np.array_equal(cuda_bits(ms[i]), ot["m"])
+                    assert np.array_equal(cuda_bits(vs[i]), ot["v"])
+                else:
+                    assert np.array_equal(ms[i].cpu().numpy(), ot["m"])
+    finally:
+        lmopt.optim_group_destroy(h)
+
+
+def test_ragged_log_uniform_small(orc, eng):
+    """A reduced ragged workload: 400 tensors, sizes round(2^U(6,18)), 1% exact-zero grads."""
+    sizes = W.ragged_sizes(400, seed=1, hi_exp=18.0)
+    run_parity(orc, eng, [(n,) for n in sizes], 3, HP, seed=1, zero_frac=0.01, check_every=False)
+
+
+def test_checkpoint_resume_bit_identical(orc, eng):
+    """k steps, save (codes, residuals, scales, step, mu product), restore into a new group,
+    N-k more steps == N uninterrupted steps."""
+    from memory_lean_optimizer_gb300 import lmopt
+    shapes = [(5000,), (70000,), (300,)]
+    seed = 6
+    masters = [W.master_weights(s, seed, i) for i, s in enumerate(shapes)]
+    grads = {t: [W.grad_bf16(s, seed, i, t, 1e-3) for i, s in enumerate(shapes)] for t in range(1, 6)}
+    a = eng.NadamGroup.from_masters([m.cuda() for m in masters])
+    for t in range(1, 6):
+        a.step([g.cuda() for g in grads[t]], HP)
+    b = eng.NadamGroup.from_masters([m.cuda() for m in masters])
+    for t in range(1, 4):
+        b.step([g.cuda() for g in grads[t]], HP)
+    recs = b.scales()
+    step, mp = lmopt.optim_group_get_step(b.handle)
+    c = eng.NadamGroup([w.clone() for w in b.weights], [r.clone() for r in b.res])
+    for i in range(len(shapes)):
+        c.m[i].copy_(b.m[i])
+        c.v[i].copy_(b.v[i])
+    lmopt.optim_set_scales(c.handle, recs)
+    lmopt.optim_group_set_step(c.handle, step, mp)
+    c.step_count = step
+    for t in range(4, 6):
+        c.step([g.cuda() for g in grads[t]], HP)
+    torch.cuda.synchronize()
+    for i in range(len(shapes)):
+        assert torch.equal(a.weights[i].view(torch.int16), c.weights[i].view(torch.int16))
+        assert torch.equal(a.res[i], c.res[i])
+        assert torch.equal(a.m[i].view(torch.int32) if a.m[i].dtype == torch.float32 else a.m[i],
+                           c.m[i].view(torch.int32) if c.m[i].dtype == torch.float32 else c.m[i])
+
+
+def test_nonfinite_counter_and_step_validation(eng):
+    from memory_lean_optimizer_gb300 import lmopt
+    n = 10000
+    grp = eng.NadamGroup.from_masters([torch.randn(n, device="cuda") * 0.02])
+    g = torch.randn(n, device="cuda").mul_(1e-3).to(torch.bfloat16)
+    grp.step([g], HP)
+    assert lmopt.optim_query_nonfinite(grp.handle) == 0
+    g[:17] = float("inf")
+    grp.step([g], HP)
+    assert lmopt.optim_query_nonfinite(grp.handle) > 0
+    with pytest.raises(lmopt.LmoptError) as e:
+        lmopt.optim_step_nadam_kahan(grp.handle, [g.data_ptr()], 7, lmopt.NadamHparams(lr=1e-3, beta1=0.9, beta2=0.999), 0)
+    assert e.value.code == lmopt.OPTIM_EINVAL
+    bad = lmopt.NadamHparams(lr=1e-3, beta1=0.9, beta2=1.0, eps=1e-8)
+    with pytest.raises(lmopt.LmoptError):
+        lmopt.optim_step_nadam_kahan(grp.handle, [g.data_ptr()], 3, bad, 0)
+    with pytest.raises(lmopt.LmoptError) as e:
+        lmopt.optim_step_nadam_kahan(grp.handle, [g.data_ptr() + 1], 3, lmopt.NadamHparams(lr=1e-3, beta1=0.9, beta2=0.999), 0)
+    assert e.value.code == lmopt.OPTIM_EALIGN
+
+
+def test_deterministic_two_runs(eng):
+    shapes = [(200_000,), (3000,)]
+    outs = []
+    for _ in range(2):
+        masters = [W.master_weights(s, 9, i, device="cuda") for i, s in enumerate(shapes)]
+        grp = eng.NadamGroup.from_masters(masters)
+        for t in range(1, 4):
+            grp.step([W.grad_bf16(s, 9, i, t, 1e-3, device="cuda") for i, s in enumerate(shapes)], HP)
+        outs.append([x.clone() for x in grp.masters()] + [grp.m[0].clone(), grp.v[0].clone()])
+    for a, b in zip(*outs):
+        assert torch.equal(a.view(torch.int32) if a.dtype == torch.float32 else a,
+                           b.view(torch.int32) if b.dtype == torch.float32 else b)
