@@ -1,14 +1,596 @@
-// factored.cu -- factored second-moment step (placeholder until the kernels land).
+// factored.cu -- factored second-moment step (Adafactor / Prodigy, beta1 = 0, no exp_avg).
+//
+// Follows the printed fused Adafactor step ("Fused backward pass" commit,
+// library/adafactor_fused.py, adafactor_step_param) with a fixed learning rate and the eps2
+// placement of prodigy PR #25 ("more VRAM savings: no first moment and factored second moment"):
+//   q = g*g + eps1 (Adafactor) | g*g (Prodigy)
+//   R = b2t*R + alpha*mean_j(q) (+eps2),  C = b2t*C + alpha*mean_i(q) (+eps2)
+//   u_ij = (rsqrt(R_i / mean(R)) * rsqrt(C_j)) * g_ij        (1-D: u = rsqrt(V) * g)
+//   u = (u / max(1, RMS(u)/clip)) * lr_eff;  w = w + w*(-wd*lr_eff);  w = w - u;  Kahan split
+// Factoring is over the last two dims; leading dims are a batch of matrices.
+//
+// Tensor classes and their kernels:
+//   wide  (ndim >= 2, rows*cols > 16): 64x256 tiles, 256 threads (8 warps x 8 rows, lane = 8 cols)
+//   tiny  (ndim >= 2, rows*cols <= 16, e.g. 3x3 conv kernels): one thread per matrix
+//   vector (ndim == 1): one thread per element, full fp32 second moment
+// Per wave of tensors (waves keep the wave's gradients, read three times, within L2):
+//   1. k_stats  : wide tiles -> row/column partial sums of q;  tiny/vector -> state EMA, u, sum u^2
+//   2. k_final  : wide matrices -> R, C EMAs, mean(R), rsqrt factors per row and column
+//   3. k_rms    : wide tiles -> sum u^2 per tile
+//   4. k_apply  : every element -> clip, lr, decay, subtract, split
+// The clip divisor of a tensor is computed by the last CTA to finish its partial sums (threadfence
+// and counter), summing the partials in a fixed order.  Every reduction is in a fixed order, so
+// results are deterministic; sums are fp32 trees, with compensated (Neumaier) sums across partials.
+#include <algorithm>
+#include <vector>
+
 #include "factored.h"
 
 namespace lmo {
-struct FactoredPlan { int unused; };
-int factored_plan_build(FactoredPlan*& plan, const std::vector<optim_tensor_desc_t>&) {
+
+namespace {
+
+constexpr int kTR = 64;      // rows per wide tile
+constexpr int kTC = 256;     // columns per wide tile
+constexpr int kTinyPerCta = kThreads;
+constexpr int kVecPerCta = kThreads * 8;
+constexpr int64_t kWaveGradBytes = 40ll << 20;   // gradient bytes per wave (L2-resident target)
+
+enum : int32_t { kWide = 0, kTiny = 1, kVec = 2 };
+enum : int32_t { kFinRows = 0, kFinCols = 1 };
+
+struct FTensor {
+    uint16_t* w;
+    uint16_t* res;
+    float* row;     // R state [B*R] (wide, tiny)
+    float* col;     // C state [B*C] (wide, tiny) or V [numel] (vector)
+    int64_t numel;
+    int64_t B, R, C;
+    int32_t cls;
+    int32_t ncb;    // column blocks (wide)
+    int32_t nbands; // row bands (wide)
+    int32_t ss_cnt;
+    int64_t rowpart_off, colpart_off, rr_off, cc_off, ss_off;
+};
+
+struct Item {        // one CTA of k_stats / k_rms / k_apply / k_final
+    int32_t tensor;
+    int32_t cls;     // kWide / kTiny / kVec (k_final: kFinRows / kFinCols)
+    int32_t x;       // wide: matrix; tiny: first matrix; vector: chunk; final: matrix
+    int32_t band;    // wide: row band
+    int32_t cb;      // wide / final cols: column block
+    int32_t part;    // index of this CTA's sum-of-squares partial within its tensor
+};
+
+struct Dev {
+    const FTensor* tensors;
+    const uint16_t* const* grads;
+    float* rowpart;
+    float* colpart;
+    float* rr;
+    float* cc;
+    float* ss;
+    float* den;
+    unsigned* counter;
+};
+
+struct K {
+    float b2t, alpha, eps1, eps2, clip, lr_eff, nwdlr;
+    int32_t mode;
+};
+
+__device__ __forceinline__ float qval(float g, const K& k) {
+    float gg = __fmul_rn(g, g);
+    return k.mode == 0 ? __fadd_rn(gg, k.eps1) : gg;
+}
+__device__ __forceinline__ float ema(float s, float x, const K& k) {
+    float r = __fadd_rn(__fmul_rn(k.b2t, s), __fmul_rn(k.alpha, x));
+    return k.mode == 1 ? __fadd_rn(r, k.eps2) : r;
+}
+__device__ __forceinline__ float rsqrt_rn(float x) { return __fdiv_rn(1.0f, __fsqrt_rn(x)); }
+// Columns of a lane's 8-column group that lie inside the matrix (0..8).
+__device__ __forceinline__ int cols_in(int64_t remaining) {
+    return remaining <= 0 ? 0 : (remaining >= 8 ? 8 : (int)remaining);
+}
+
+// Neumaier-compensated accumulation.
+struct Comp {
+    float s = 0.f, c = 0.f;
+    __device__ __forceinline__ void add(float x) {
+        float t = __fadd_rn(s, x);
+        if (fabsf(s) >= fabsf(x)) c = __fadd_rn(c, __fadd_rn(__fsub_rn(s, t), x));
+        else c = __fadd_rn(c, __fadd_rn(__fsub_rn(x, t), s));
+        s = t;
+    }
+    __device__ __forceinline__ float value() const { return __fadd_rn(s, c); }
+};
+
+// Block-wide fp32 sum in a fixed tree; result valid in every thread.
+__device__ float block_sum(float x, float* sm /* 32 floats */) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    x = warp_sum_f32(x);
+    __syncthreads();
+    if (lane == 0) sm[warp] = x;
+    __syncthreads();
+    float y = lane < (int)(blockDim.x >> 5) ? sm[lane] : 0.f;
+    y = warp_sum_f32(y);
+    return y;
+}
+
+__device__ __forceinline__ void apply_elem(uint32_t& hi, uint32_t& lo, bool has_res, float u, float den, const K& k) {
+    float w = has_res ? __uint_as_float((hi << 16) | lo) : bf16_to_f32(hi);
+    const float uu = den == 1.0f ? __fmul_rn(u, k.lr_eff) : __fmul_rn(__fdiv_rn(u, den), k.lr_eff);
+    if (k.nwdlr != 0.0f) w = __fadd_rn(w, __fmul_rn(w, k.nwdlr));
+    w = __fsub_rn(w, uu);
+    const uint32_t b = __float_as_uint(w);
+    if (has_res) {
+        hi = b >> 16;
+        lo = b & 0xFFFFu;
+    } else {
+        hi = rne_bf16(w);
+    }
+}
+
+// Clip divisor from the tensor's fp32 sum of squares.
+__device__ __forceinline__ float clip_den(float ss, int64_t n, float clip) {
+    const float ms = __fdiv_rn(ss, (float)n);
+    return fmaxf(1.0f, __fdiv_rn(__fsqrt_rn(ms), clip));
+}
+
+// Writes this CTA's partial; the last CTA of the tensor sums all partials (fixed order) and
+// writes the clip divisor.  Must be called by every thread of the CTA.
+__device__ void finish_ss(const Dev& D, const FTensor& t, int tensor, int part, float block_total,
+                          const K& k, float* sm) {
+    __shared__ bool last;
+    if (threadIdx.x == 0) {
+        D.ss[t.ss_off + part] = block_total;
+        __threadfence();
+        const unsigned prev = atomicAdd(&D.counter[tensor], 1u);
+        last = prev == (unsigned)t.ss_cnt - 1u;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    Comp acc;
+    for (int i = threadIdx.x; i < t.ss_cnt; i += blockDim.x) acc.add(__ldcg(D.ss + t.ss_off + i));
+    const float tot = block_sum(acc.value(), sm);
+    if (threadIdx.x == 0) {
+        D.den[tensor] = clip_den(tot, t.numel, k.clip);
+        D.counter[tensor] = 0u;
+    }
+}
+
+// Loads 8 consecutive bf16 words (columns col0..col0+7 of one row) into w[8]; columns past
+// `ncols` read as 0.  vec: 16-byte aligned fast path.
+__device__ __forceinline__ void load8(const uint16_t* p, int ncols, bool vec, uint32_t (&v)[8]) {
+    if (vec && ncols == 8) {
+        uint4 x = __ldcg(reinterpret_cast<const uint4*>(p));
+        v[0] = x.x & 0xFFFFu; v[1] = x.x >> 16; v[2] = x.y & 0xFFFFu; v[3] = x.y >> 16;
+        v[4] = x.z & 0xFFFFu; v[5] = x.z >> 16; v[6] = x.w & 0xFFFFu; v[7] = x.w >> 16;
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = j < ncols ? p[j] : 0u;
+    }
+}
+
+// ------------------------------------------------------------------------------------ stats
+__global__ void __launch_bounds__(kThreads) k_stats(Dev D, const Item* items, K k) {
+    __shared__ float sm[32];
+    __shared__ float cols[8][kTC + 1];
+    const Item it = items[blockIdx.x];
+    const FTensor t = D.tensors[it.tensor];
+    const uint16_t* __restrict__ g = D.grads[it.tensor];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+    if (it.cls == kWide) {
+        const int64_t b = it.x;
+        const int64_t col0 = (int64_t)it.cb * kTC + lane * 8;
+        const int ncols = cols_in(t.C - col0);
+        const bool vec = aligned16(g) && (t.C % 8 == 0);
+        float cacc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int kk = 0; kk < kTR / 8; ++kk) {
+            const int64_t row = (int64_t)it.band * kTR + warp + 8 * kk;
+            if (row >= t.R) break;
+            uint32_t v[8];
+            load8(g + (b * t.R + row) * t.C + col0, ncols, vec, v);
+            float rs = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (j < ncols) {
+                    const float q = qval(bf16_to_f32(v[j]), k);
+                    rs = __fadd_rn(rs, q);
+                    cacc[j] = __fadd_rn(cacc[j], q);
+                }
+            }
+            rs = warp_sum_f32(rs);
+            if (lane == 0) D.rowpart[t.rowpart_off + (b * t.R + row) * t.ncb + it.cb] = rs;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) cols[warp][lane * 8 + j] = cacc[j];
+        __syncthreads();
+        const int c = threadIdx.x;
+        const float s = __fadd_rn(__fadd_rn(__fadd_rn(cols[0][c], cols[1][c]), __fadd_rn(cols[2][c], cols[3][c])),
+                                  __fadd_rn(__fadd_rn(cols[4][c], cols[5][c]), __fadd_rn(cols[6][c], cols[7][c])));
+        const int64_t col = (int64_t)it.cb * kTC + c;
+        if (col < t.C) D.colpart[t.colpart_off + (b * t.nbands + it.band) * t.C + col] = s;
+        return;
+    }
+
+    float acc = 0.f;
+    if (it.cls == kTiny) {
+        const int64_t mat = (int64_t)it.x + threadIdx.x;
+        if (mat < t.B) {
+            const int r = (int)t.R, c = (int)t.C;
+            const uint16_t* gm = g + mat * r * c;
+            float q[16], rsum[16], csum[16];
+            for (int e = 0; e < r * c; ++e) q[e] = qval(bf16_to_f32(gm[e]), k);
+            for (int i = 0; i < r; ++i) {
+                float s = 0.f;
+                for (int j = 0; j < c; ++j) s = __fadd_rn(s, q[i * c + j]);
+                rsum[i] = s;
+            }
+            for (int j = 0; j < c; ++j) {
+                float s = 0.f;
+                for (int i = 0; i < r; ++i) s = __fadd_rn(s, q[i * c + j]);
+                csum[j] = s;
+            }
+            float* Rs = t.row + mat * r;
+            float* Cs = t.col + mat * c;
+            float rtot = 0.f;
+            for (int i = 0; i < r; ++i) {
+                const float nr = ema(Rs[i], __fdiv_rn(rsum[i], (float)c), k);
+                Rs[i] = nr;
+                rsum[i] = nr;
+                rtot = __fadd_rn(rtot, nr);
+            }
+            for (int j = 0; j < c; ++j) {
+                const float nc = ema(Cs[j], __fdiv_rn(csum[j], (float)r), k);
+                Cs[j] = nc;
+                csum[j] = rsqrt_rn(nc);
+            }
+            const float rbar = __fdiv_rn(rtot, (float)r);
+            for (int i = 0; i < r; ++i) {
+                const float rr = rsqrt_rn(__fdiv_rn(rsum[i], rbar));
+                for (int j = 0; j < c; ++j) {
+                    const float u = __fmul_rn(__fmul_rn(rr, csum[j]), bf16_to_f32(gm[i * c + j]));
+                    acc = __fadd_rn(acc, __fmul_rn(u, u));
+                }
+            }
+        }
+    } else {  // kVec
+        const int64_t e0 = (int64_t)it.x * kVecPerCta;
+        const int64_t e1 = (t.numel < e0 + kVecPerCta ? t.numel : e0 + kVecPerCta);
+        for (int64_t e = e0 + threadIdx.x; e < e1; e += kThreads) {
+            const float gg = bf16_to_f32(g[e]);
+            const float nv = ema(t.col[e], qval(gg, k), k);
+            t.col[e] = nv;
+            const float u = __fmul_rn(rsqrt_rn(nv), gg);
+            acc = __fadd_rn(acc, __fmul_rn(u, u));
+        }
+    }
+    const float tot = block_sum(acc, sm);
+    finish_ss(D, t, it.tensor, it.part, tot, k, sm);
+}
+
+// ------------------------------------------------------------------------------------ finalize
+__global__ void __launch_bounds__(kThreads) k_final(Dev D, const Item* items, K k) {
+    __shared__ float sm[32];
+    const Item it = items[blockIdx.x];
+    const FTensor t = D.tensors[it.tensor];
+    const int64_t b = it.x;
+    if (it.cls == kFinRows) {
+        Comp acc;
+        const float fc = (float)t.C;
+        for (int64_t i = threadIdx.x; i < t.R; i += kThreads) {
+            const float* rp = D.rowpart + t.rowpart_off + (b * t.R + i) * t.ncb;
+            Comp s;
+            for (int cb = 0; cb < t.ncb; ++cb) s.add(rp[cb]);
+            const float nr = ema(t.row[b * t.R + i], __fdiv_rn(s.value(), fc), k);
+            t.row[b * t.R + i] = nr;
+            acc.add(nr);
+        }
+        const float tot = block_sum(acc.value(), sm);
+        const float rbar = __fdiv_rn(tot, (float)t.R);
+        for (int64_t i = threadIdx.x; i < t.R; i += kThreads)
+            D.rr[t.rr_off + b * t.R + i] = rsqrt_rn(__fdiv_rn(t.row[b * t.R + i], rbar));
+    } else {
+        const int64_t j = (int64_t)it.cb * kTC + threadIdx.x;
+        if (j < t.C) {
+            Comp s;
+            const float* cp = D.colpart + t.colpart_off + b * t.nbands * t.C + j;
+            for (int band = 0; band < t.nbands; ++band) s.add(cp[(int64_t)band * t.C]);
+            const float nc = ema(t.col[b * t.C + j], __fdiv_rn(s.value(), (float)t.R), k);
+            t.col[b * t.C + j] = nc;
+            D.cc[t.cc_off + b * t.C + j] = rsqrt_rn(nc);
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------ rms
+__global__ void __launch_bounds__(kThreads) k_rms(Dev D, const Item* items, K k) {
+    __shared__ float sm[32];
+    const Item it = items[blockIdx.x];
+    const FTensor t = D.tensors[it.tensor];
+    const uint16_t* __restrict__ g = D.grads[it.tensor];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t b = it.x;
+    const int64_t col0 = (int64_t)it.cb * kTC + lane * 8;
+    const int ncols = cols_in(t.C - col0);
+    const bool vec = aligned16(g) && (t.C % 8 == 0);
+    float ccv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ccv[j] = j < ncols ? D.cc[t.cc_off + b * t.C + col0 + j] : 0.f;
+    float acc = 0.f;
+    for (int kk = 0; kk < kTR / 8; ++kk) {
+        const int64_t row = (int64_t)it.band * kTR + warp + 8 * kk;
+        if (row >= t.R) break;
+        const float rr = D.rr[t.rr_off + b * t.R + row];
+        uint32_t v[8];
+        load8(g + (b * t.R + row) * t.C + col0, ncols, vec, v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j < ncols) {
+                const float u = __fmul_rn(__fmul_rn(rr, ccv[j]), bf16_to_f32(v[j]));
+                acc = __fadd_rn(acc, __fmul_rn(u, u));
+            }
+        }
+    }
+    const float tot = block_sum(acc, sm);
+    finish_ss(D, t, it.tensor, it.part, tot, k, sm);
+}
+
+// ------------------------------------------------------------------------------------ apply
+__global__ void __launch_bounds__(kThreads) k_apply(Dev D, const Item* items, K k) {
+    const Item it = items[blockIdx.x];
+    const FTensor t = D.tensors[it.tensor];
+    const uint16_t* __restrict__ g = D.grads[it.tensor];
+    const float den = D.den[it.tensor];
+    const bool has_res = t.res != nullptr;
+
+    if (it.cls == kWide) {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        const int64_t b = it.x;
+        const int64_t col0 = (int64_t)it.cb * kTC + lane * 8;
+        const int ncols = cols_in(t.C - col0);
+        const bool vec = aligned16(g) && aligned16(t.w) && (!has_res || aligned16(t.res)) && (t.C % 8 == 0);
+        float ccv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ccv[j] = j < ncols ? D.cc[t.cc_off + b * t.C + col0 + j] : 0.f;
+        for (int kk = 0; kk < kTR / 8; ++kk) {
+            const int64_t row = (int64_t)it.band * kTR + warp + 8 * kk;
+            if (row >= t.R) break;
+            const float rr = D.rr[t.rr_off + b * t.R + row];
+            const int64_t off = (b * t.R + row) * t.C + col0;
+            if (vec && ncols == 8) {
+                const uint4 G = __ldcg(reinterpret_cast<const uint4*>(g + off));
+                uint4 Wv = ld_stream(reinterpret_cast<const uint4*>(t.w + off));
+                uint4 Rv = has_res ? ld_stream(reinterpret_cast<const uint4*>(t.res + off)) : make_uint4(0, 0, 0, 0);
+                const uint32_t* g32 = reinterpret_cast<const uint32_t*>(&G);
+                uint32_t* w32 = reinterpret_cast<uint32_t*>(&Wv);
+                uint32_t* r32 = reinterpret_cast<uint32_t*>(&Rv);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t ow = 0, orr = 0;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int sh = 16 * h;
+                        uint32_t hi = (w32[q] >> sh) & 0xFFFFu, lo = (r32[q] >> sh) & 0xFFFFu;
+                        const float u = __fmul_rn(__fmul_rn(rr, ccv[2 * q + h]), bf16_to_f32((g32[q] >> sh) & 0xFFFFu));
+                        apply_elem(hi, lo, has_res, u, den, k);
+                        ow |= hi << sh;
+                        orr |= lo << sh;
+                    }
+                    w32[q] = ow;
+                    r32[q] = orr;
+                }
+                st_stream(reinterpret_cast<uint4*>(t.w + off), Wv);
+                if (has_res) st_stream(reinterpret_cast<uint4*>(t.res + off), Rv);
+            } else {
+                for (int j = 0; j < ncols; ++j) {
+                    uint32_t hi = t.w[off + j], lo = has_res ? t.res[off + j] : 0u;
+                    const float u = __fmul_rn(__fmul_rn(rr, ccv[j]), bf16_to_f32(g[off + j]));
+                    apply_elem(hi, lo, has_res, u, den, k);
+                    t.w[off + j] = (uint16_t)hi;
+                    if (has_res) t.res[off + j] = (uint16_t)lo;
+                }
+            }
+        }
+        return;
+    }
+    if (it.cls == kTiny) {
+        const int64_t mat = (int64_t)it.x + threadIdx.x;
+        if (mat >= t.B) return;
+        const int r = (int)t.R, c = (int)t.C;
+        const float* Rs = t.row + mat * r;
+        const float* Cs = t.col + mat * c;
+        float rtot = 0.f;
+        for (int i = 0; i < r; ++i) rtot = __fadd_rn(rtot, Rs[i]);
+        const float rbar = __fdiv_rn(rtot, (float)r);
+        float ccv[16];
+        for (int j = 0; j < c; ++j) ccv[j] = rsqrt_rn(Cs[j]);
+        const int64_t base = mat * r * c;
+        for (int i = 0; i < r; ++i) {
+            const float rr = rsqrt_rn(__fdiv_rn(Rs[i], rbar));
+            for (int j = 0; j < c; ++j) {
+                const int64_t e = base + i * c + j;
+                uint32_t hi = t.w[e], lo = has_res ? t.res[e] : 0u;
+                const float u = __fmul_rn(__fmul_rn(rr, ccv[j]), bf16_to_f32(g[e]));
+                apply_elem(hi, lo, has_res, u, den, k);
+                t.w[e] = (uint16_t)hi;
+                if (has_res) t.res[e] = (uint16_t)lo;
+            }
+        }
+        return;
+    }
+    const int64_t e0 = (int64_t)it.x * kVecPerCta;
+    const int64_t e1 = (t.numel < e0 + kVecPerCta ? t.numel : e0 + kVecPerCta);
+    for (int64_t e = e0 + threadIdx.x; e < e1; e += kThreads) {
+        uint32_t hi = t.w[e], lo = has_res ? t.res[e] : 0u;
+        const float u = __fmul_rn(rsqrt_rn(t.col[e]), bf16_to_f32(g[e]));
+        apply_elem(hi, lo, has_res, u, den, k);
+        t.w[e] = (uint16_t)hi;
+        if (has_res) t.res[e] = (uint16_t)lo;
+    }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------------------------ host plan
+struct Wave {
+    int32_t item_off, n_wide, n_total;   // items: wide tiles first, then tiny and vector CTAs
+    int32_t fin_off, n_fin;
+};
+
+struct FactoredPlan {
+    Dev dev{};
+    FTensor* d_tensors = nullptr;
+    Item* d_items = nullptr;
+    Item* d_fin = nullptr;
+    std::vector<Wave> waves;
+    std::vector<void*> allocs;
+};
+
+template <class T>
+static int alloc_dev(FactoredPlan* p, T** out, size_t count, const char* what) {
+    const size_t bytes = std::max<size_t>(count, 1) * sizeof(T);
+    if (cudaMalloc(reinterpret_cast<void**>(out), bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return set_error(OPTIM_ENOMEM, "cudaMalloc(%zu) for %s failed", bytes, what);
+    }
+    p->allocs.push_back(*out);
+    return check_cuda(cudaMemset(*out, 0, bytes), what);
+}
+
+int factored_plan_build(FactoredPlan*& plan, const std::vector<optim_tensor_desc_t>& desc) {
+    plan = new FactoredPlan();
+    FactoredPlan* p = plan;
+    const int32_t n = (int32_t)desc.size();
+    std::vector<FTensor> ts(n);
+    int64_t rowpart = 0, colpart = 0, rr = 0, cc = 0, ss = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        const optim_tensor_desc_t& d = desc[i];
+        FTensor& t = ts[i];
+        t = FTensor{};
+        t.w = static_cast<uint16_t*>(d.w_bf16);
+        t.res = static_cast<uint16_t*>(d.res_u16);
+        t.numel = d.numel;
+        if (d.ndim >= 2) {
+            t.R = d.shape[d.ndim - 2];
+            t.C = d.shape[d.ndim - 1];
+            t.B = 1;
+            for (int k = 0; k < d.ndim - 2; ++k) t.B *= d.shape[k];
+            t.row = static_cast<float*>(d.m);
+            t.col = static_cast<float*>(d.v);
+            t.cls = (t.R * t.C <= 16) ? kTiny : kWide;
+        } else {
+            t.B = 1;
+            t.R = 1;
+            t.C = d.numel;
+            t.col = static_cast<float*>(d.v);
+            t.cls = kVec;
+        }
+        if (d.numel == 0) continue;
+        if (t.cls == kWide) {
+            t.ncb = (int32_t)((t.C + kTC - 1) / kTC);
+            t.nbands = (int32_t)((t.R + kTR - 1) / kTR);
+            t.rowpart_off = rowpart;
+            rowpart += t.B * t.R * t.ncb;
+            t.colpart_off = colpart;
+            colpart += t.B * t.nbands * t.C;
+            t.rr_off = rr;
+            rr += t.B * t.R;
+            t.cc_off = cc;
+            cc += t.B * t.C;
+            t.ss_cnt = (int32_t)(t.B * t.nbands * t.ncb);
+        } else if (t.cls == kTiny) {
+            t.ss_cnt = (int32_t)((t.B + kTinyPerCta - 1) / kTinyPerCta);
+        } else {
+            t.ss_cnt = (int32_t)((t.numel + kVecPerCta - 1) / kVecPerCta);
+        }
+        t.ss_off = ss;
+        ss += t.ss_cnt;
+    }
+    // waves: consecutive tensors until the wave's gradient bytes reach the L2-resident target
+    std::vector<Item> items, fin;
+    int32_t i = 0;
+    while (i < n) {
+        int64_t bytes = 0;
+        int32_t j = i;
+        while (j < n && (j == i || bytes + 2 * ts[j].numel <= kWaveGradBytes)) bytes += 2 * ts[j++].numel;
+        Wave wv{};
+        wv.item_off = (int32_t)items.size();
+        wv.fin_off = (int32_t)fin.size();
+        for (int32_t q = i; q < j; ++q) {
+            const FTensor& t = ts[q];
+            if (t.numel == 0 || t.cls != kWide) continue;
+            int32_t part = 0;
+            for (int64_t b = 0; b < t.B; ++b) {
+                for (int32_t band = 0; band < t.nbands; ++band)
+                    for (int32_t cb = 0; cb < t.ncb; ++cb) items.push_back(Item{q, kWide, (int32_t)b, band, cb, part++});
+                fin.push_back(Item{q, kFinRows, (int32_t)b, 0, 0, 0});
+                for (int32_t cb = 0; cb < t.ncb; ++cb) fin.push_back(Item{q, kFinCols, (int32_t)b, 0, cb, 0});
+            }
+        }
+        wv.n_wide = (int32_t)items.size() - wv.item_off;
+        for (int32_t q = i; q < j; ++q) {
+            const FTensor& t = ts[q];
+            if (t.numel == 0 || t.cls == kWide) continue;
+            for (int32_t part = 0; part < t.ss_cnt; ++part) {
+                const int32_t x = t.cls == kTiny ? part * kTinyPerCta : part;
+                items.push_back(Item{q, t.cls, x, 0, 0, part});
+            }
+        }
+        wv.n_total = (int32_t)items.size() - wv.item_off;
+        wv.n_fin = (int32_t)fin.size() - wv.fin_off;
+        p->waves.push_back(wv);
+        i = j;
+    }
+    int rc = OPTIM_OK;
+    Dev& D = p->dev;
+    if (!rc) rc = alloc_dev(p, &p->d_tensors, ts.size(), "factored tensor table");
+    if (!rc) rc = check_cuda(cudaMemcpy(p->d_tensors, ts.data(), ts.size() * sizeof(FTensor), cudaMemcpyHostToDevice), "upload");
+    if (!rc) rc = alloc_dev(p, &p->d_items, items.size(), "factored work items");
+    if (!rc && !items.empty()) rc = check_cuda(cudaMemcpy(p->d_items, items.data(), items.size() * sizeof(Item), cudaMemcpyHostToDevice), "upload");
+    if (!rc) rc = alloc_dev(p, &p->d_fin, fin.size(), "factored finalize items");
+    if (!rc && !fin.empty()) rc = check_cuda(cudaMemcpy(p->d_fin, fin.data(), fin.size() * sizeof(Item), cudaMemcpyHostToDevice), "upload");
+    if (!rc) rc = alloc_dev(p, &D.rowpart, (size_t)rowpart, "row partial sums");
+    if (!rc) rc = alloc_dev(p, &D.colpart, (size_t)colpart, "column partial sums");
+    if (!rc) rc = alloc_dev(p, &D.rr, (size_t)rr, "row factors");
+    if (!rc) rc = alloc_dev(p, &D.cc, (size_t)cc, "column factors");
+    if (!rc) rc = alloc_dev(p, &D.ss, (size_t)ss, "sum-of-squares partials");
+    if (!rc) rc = alloc_dev(p, &D.den, (size_t)n, "clip divisors");
+    if (!rc) rc = alloc_dev(p, &D.counter, (size_t)n, "partial counters");
+    D.tensors = p->d_tensors;
+    return rc;
+}
+
+void factored_plan_free(FactoredPlan*& plan) {
+    if (!plan) return;
+    for (void* a : plan->allocs) cudaFree(a);
+    delete plan;
     plan = nullptr;
-    return set_error(OPTIM_EINVAL, "factored groups are not available in this build");
 }
-void factored_plan_free(FactoredPlan*& plan) { delete plan; plan = nullptr; }
-int launch_factored_step(const FactoredPlan*, const uint16_t* const*, const FactoredScalars&, cudaStream_t, cudaEvent_t) {
-    return set_error(OPTIM_EINVAL, "factored groups are not available in this build");
+
+int launch_factored_step(const FactoredPlan* p, const uint16_t* const* d_grads, const FactoredScalars& s,
+                         cudaStream_t stream, cudaEvent_t mid) {
+    K k{s.b2t, s.alpha, s.eps1, s.eps2, s.clip, s.lr_eff, s.nwdlr, s.mode};
+    Dev D = p->dev;
+    D.grads = d_grads;
+    for (size_t w = 0; w < p->waves.size(); ++w) {
+        const Wave& wv = p->waves[w];
+        const Item* items = p->d_items + wv.item_off;
+        if (wv.n_total > 0) k_stats<<<wv.n_total, kThreads, 0, stream>>>(D, items, k);
+        if (wv.n_fin > 0) k_final<<<wv.n_fin, kThreads, 0, stream>>>(D, p->d_fin + wv.fin_off, k);
+        if (wv.n_wide > 0) k_rms<<<wv.n_wide, kThreads, 0, stream>>>(D, items, k);
+        if (mid && w + 1 == p->waves.size()) {
+            int rc = check_cuda(cudaEventRecord(mid, stream), "profile event");
+            if (rc) return rc;
+        }
+        if (wv.n_total > 0) k_apply<<<wv.n_total, kThreads, 0, stream>>>(D, items, k);
+        int rc = check_cuda(cudaGetLastError(), "factored step launch");
+        if (rc) return rc;
+    }
+    return OPTIM_OK;
 }
+
 }  // namespace lmo

@@ -1,0 +1,97 @@
+"""Fused backward pass: step each parameter group from autograd's post-accumulate-grad hooks.
+
+The pages' mechanism: instead of backward-then-step over all gradients, each parameter's
+gradient is applied as soon as it is accumulated (``Tensor.register_post_accumulate_grad_hook``),
+and optimizer groups step a group of parameters once all of the group's gradients exist, after
+which the gradients are dropped ("Fused backward pass" commit, README: "Fused optimizer" and
+"Optimizer groups" items).  Here each group is one library group, so one C-ABI call (two kernel
+launches) steps every tensor of the group.  Gradient accumulation is not supported, as on the
+pages.
+"""
+from __future__ import annotations
+
+from typing import Callable, Sequence
+
+import torch
+
+
+def split_groups(params: Sequence[torch.Tensor], n_groups: int) -> list[list[int]]:
+    """Contiguous split of the parameter list into n_groups groups of roughly equal element count
+    (parameters keep their order, which is roughly the reverse of gradient arrival)."""
+    n_groups = max(1, min(n_groups, len(params)))
+    total = sum(p.numel() for p in params)
+    groups, cur, acc = [], [], 0
+    for i, p in enumerate(params):
+        cur.append(i)
+        acc += p.numel()
+        remaining_groups = n_groups - len(groups) - 1
+        remaining_params = len(params) - i - 1
+        if remaining_groups > 0 and (acc >= total * (len(groups) + 1) / n_groups or remaining_params == remaining_groups):
+            groups.append(cur)
+            cur = []
+    if cur:
+        groups.append(cur)
+    return groups
+
+
+class FusedStepper:
+    """Registers post-accumulate-grad hooks on `params` and steps each group when its last
+    gradient arrives.
+
+    make_group(list_of_params) -> object with .step(grads, hp, stream) (e.g. engine.NadamGroup
+    over the parameters' bf16 storage).  After a group steps, its parameters' .grad are set to
+    None so that gradient memory is released during the backward pass.
+    """
+
+    def __init__(self, params: Sequence[torch.Tensor], n_groups: int, hp: dict,
+                 make_group: Callable[[list], object], on_step: Callable | None = None):
+        self.params = list(params)
+        self.hp = hp
+        self.index = split_groups(self.params, n_groups)
+        self.groups = [make_group([self.params[i] for i in idx]) for idx in self.index]
+        self.group_of = {}
+        for gi, idx in enumerate(self.index):
+            for i in idx:
+                self.group_of[id(self.params[i])] = gi
+        self.pending = [len(idx) for idx in self.index]
+        self.on_step = on_step
+        self.steps_taken = [0] * len(self.groups)
+        self.handles = [p.register_post_accumulate_grad_hook(self._hook) for p in self.params]
+
+    def _hook(self, p: torch.Tensor):
+        gi = self.group_of[id(p)]
+        self.pending[gi] -= 1
+        if self.pending[gi] > 0:
+            return
+        idx = self.index[gi]
+        grads = [self.params[i].grad for i in idx]
+        if self.on_step is not None:
+            self.on_step(gi, grads)
+        self.groups[gi].step(grads, self.hp, None)
+        self.steps_taken[gi] += 1
+        for i in idx:
+            self.params[i].grad = None
+        self.pending[gi] = len(idx)
+
+    def remove(self):
+        for h in self.handles:
+            h.remove()
+        self.handles = []
+
+
+def attach_fused_nadam(params: Sequence[torch.nn.Parameter], n_groups: int, hp: dict, on_step=None) -> FusedStepper:
+    """bf16 parameters stepped in place by the fused NAdam+Kahan engine (the parameter's bf16
+    storage is the live weight; residuals and u16 moments are allocated per group)."""
+    from .engine import NadamGroup
+
+    def make(ps):
+        return NadamGroup([p.data for p in ps])
+    return FusedStepper(params, n_groups, hp, make, on_step)
+
+
+def attach_fused_factored(params: Sequence[torch.nn.Parameter], n_groups: int, hp: dict, on_step=None) -> FusedStepper:
+    from .engine import FactoredGroup
+
+    def make(ps):
+        return FactoredGroup([p.data for p in ps])
+    return FusedStepper(params, n_groups, hp, make, on_step)

@@ -1,0 +1,153 @@
+"""GPU parity of the factored second-moment step (Adafactor / Prodigy, beta1 = 0) against the
+oracle, through the C ABI.
+
+The oracle sums rows, columns and squares in double; the kernels use fp32 trees (and compensated
+sums across tiles), so R, C and the clip divisor agree to a few fp32 roundings, not bit for bit.
+Tolerances, derived from that:
+  R, C states      : 2e-6 relative  (at most ~20 fp32 roundings of positive terms: 20 * 2^-24)
+  fp32 masters     : |w - w_ref| <= 1e-6 |w_ref| + 1e-6 * lr * steps  (the update is ~lr per step;
+                     a 1e-6-relative difference in it, plus one rounding of w)
+"""
+import numpy as np
+import pytest
+import torch
+
+from memory_lean_optimizer_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+HP = dict(lr=1e-3, beta2=0.999, decay_rate=-0.8, eps1=1e-30, eps2=1e-30, d=1.0, clip_threshold=1.0,
+          weight_decay=0.0, mode=0)
+
+
+@pytest.fixture(scope="module")
+def eng():
+    from memory_lean_optimizer_gb300 import build, engine
+    build.build()
+    return engine
+
+
+class OracleFactored:
+    def __init__(self, orc, masters, shapes, kahan=True):
+        self.orc = orc
+        self.t = []
+        for x, s in zip(masters, shapes):
+            x = np.ascontiguousarray(x, np.float32).reshape(-1)
+            hi, lo = orc.kahan_split(x) if kahan else (orc.round_bf16(x), None)
+            fac, B, R, C = orc.factored_dims(s)
+            d = dict(hi=hi, lo=lo, shape=s)
+            if fac:
+                d["row"] = np.zeros(B * R, np.float32)
+                d["col"] = np.zeros(B * C, np.float32)
+            else:
+                d["V"] = np.zeros(x.size, np.float32)
+            self.t.append(d)
+        self.steps = 0
+
+    def step(self, grads, hp):
+        self.steps += 1
+        self.orc.factored_group_step(self.t, grads, self.steps, hp)
+
+
+def compare(ora, grp, hp, steps, kahan=True):
+    masters = grp.masters() if kahan else None
+    for i, ot in enumerate(ora.t):
+        if ot["hi"].size == 0:
+            continue
+        if kahan:
+            ref = ora.orc.kahan_merge(ot["hi"], ot["lo"]).astype(np.float64)
+            got = masters[i].cpu().numpy().reshape(-1).astype(np.float64)
+            tol = 1e-6 * np.abs(ref) + 1e-6 * hp["lr"] * hp.get("d", 1.0) * steps
+            bad = np.abs(got - ref) > tol
+            assert not bad.any(), f"tensor {i} {ot['shape']}: {bad.sum()} masters out of tolerance, " \
+                                  f"max excess {np.max(np.abs(got - ref) - tol):.3e}"
+        else:
+            ref = (ot["hi"].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            got = grp.weights[i].float().cpu().numpy().reshape(-1).astype(np.float64)
+            step = np.abs(ref) * 2.0 ** -7 + 1e-30
+            assert np.all(np.abs(got - ref) <= step), f"tensor {i}: bf16 weights differ by more than one step"
+            assert np.mean(got != ref) < 1e-3
+        if "row" in ot:
+            for name, st in (("row", grp.row[i]), ("col", grp.col[i])):
+                r = ot[name].astype(np.float64)
+                gv = st.cpu().numpy().astype(np.float64)
+                assert np.all(np.abs(gv - r) <= 2e-6 * np.abs(r) + 1e-37), f"tensor {i}: {name} state differs"
+        else:
+            r = ot["V"].astype(np.float64)
+            gv = grp.col[i].cpu().numpy().astype(np.float64)
+            assert np.all(np.abs(gv - r) <= 2e-6 * np.abs(r) + 1e-37), f"tensor {i}: V state differs"
+
+
+def run_parity(orc, eng, shapes, steps, hp, seed=0, g_std=1e-3, kahan=True, scale_rows=False):
+    masters = [W.master_weights(s, seed, i) for i, s in enumerate(shapes)]
+    ora = OracleFactored(orc, [m.numpy() for m in masters], shapes, kahan=kahan)
+    if kahan:
+        grp = eng.FactoredGroup.from_masters([m.cuda() for m in masters])
+    else:
+        grp = eng.FactoredGroup([m.cuda().to(torch.bfloat16) for m in masters], kahan=False)
+    for t in range(1, steps + 1):
+        grads = []
+        for i, s in enumerate(shapes):
+            g = W.grad_bf16(s, seed, i, t, g_std)
+            if scale_rows and len(s) >= 2:      # uneven row/column scales exercise clipping
+                g = (g.float() * torch.linspace(0.1, 3.0, s[-1])).to(torch.bfloat16)
+            grads.append(g)
+        ora.step([W.bits16(g).reshape(-1) for g in grads], hp)
+        grp.step([g.cuda() for g in grads], hp)
+    torch.cuda.synchronize()
+    compare(ora, grp, hp, steps, kahan=kahan)
+    return ora, grp
+
+
+SHAPES = [(64, 80), (300, 257), (1000, 640), (3, 40, 72), (1, 300), (300, 1), (4, 6, 3, 3), (32, 16, 3, 3),
+          (2, 2), (1280,), (77,), (5000,)]
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_mixed_shapes(orc, eng, mode):
+    hp = dict(HP, mode=mode, beta2=0.99)
+    run_parity(orc, eng, SHAPES, 4, hp, seed=1, scale_rows=True)
+
+
+def test_weight_decay_and_clip_threshold(orc, eng):
+    hp = dict(HP, weight_decay=0.05, clip_threshold=0.5)
+    run_parity(orc, eng, SHAPES[:8], 3, hp, seed=2)
+
+
+def test_sdxl_like_shapes_reduced(orc, eng):
+    """The SDXL-like tensor kinds at their real sizes: a 10240x1280 and a 1280x5120 linear, a
+    1280x1280 3x3 conv, 2048-wide linears and 1-D norms/biases."""
+    shapes = [(10240, 1280), (1280, 5120), (1280, 2048), (640, 640), (1280, 1280, 3, 3), (320, 320, 3, 3),
+              (1280,), (640,)]
+    hp = dict(HP, lr=2e-6, eps1=1e-30)
+    run_parity(orc, eng, shapes, 2, hp, seed=3, g_std=1e-4)
+
+
+def test_no_residual(orc, eng):
+    run_parity(orc, eng, [(96, 130), (8, 8, 3, 3), (500,)], 3, dict(HP), seed=4, kahan=False)
+
+
+def test_rank1_sign_on_gpu(eng):
+    """Rank-1 g^2 with eps1 = 0: every step moves w by exactly -lr sign(g) (to a few ulps)."""
+    rng = np.random.default_rng(5)
+    R, C = 96, 72
+    a = rng.choice([-2.0, -1.0, -0.5, 0.5, 1.0, 2.0], size=(R, 1))
+    b = rng.choice([-4.0, -1.0, -0.25, 0.25, 1.0, 4.0], size=(1, C))
+    g32 = torch.from_numpy((a * b).astype(np.float32))
+    lr = 2.0 ** -10
+    grp = eng.FactoredGroup.from_masters([torch.zeros(R, C, device="cuda")])
+    for t in range(1, 4):
+        grp.step([g32.to(torch.bfloat16).cuda()], dict(HP, lr=lr, eps1=0.0))
+    w = grp.masters()[0].cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(w + 3 * lr * np.sign(g32.numpy())) <= 3 * 8 * np.spacing(np.float32(lr)))
+
+
+def test_factored_validation(eng):
+    from memory_lean_optimizer_gb300 import lmopt
+    grp = eng.FactoredGroup.from_masters([torch.zeros(16, 16, device="cuda")])
+    g = torch.zeros(16, 16, dtype=torch.bfloat16, device="cuda")
+    bad = lmopt.FactoredHparams(lr=1e-3, clip_threshold=0.0)
+    with pytest.raises(lmopt.LmoptError):
+        lmopt.optim_step_factored(grp.handle, [g.data_ptr()], 1, bad, 0)
+    with pytest.raises(lmopt.LmoptError):
+        lmopt.optim_step_nadam_kahan(grp.handle, [g.data_ptr()], 1, lmopt.NadamHparams(lr=1e-3, beta1=0.9, beta2=0.99), 0)
