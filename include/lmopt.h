@@ -154,8 +154,34 @@ int optim_set_scales(optim_group_t* group, const float* host_in);
 /* Step counter and NAdam momentum product (the product of mu_1..mu_t, kept in double). */
 int optim_group_get_step(optim_group_t* group, int64_t* step, double* mu_product);
 int optim_group_set_step(optim_group_t* group, int64_t step, double mu_product);
-/* Number of updated weights that came out non-finite, summed over all steps so far. */
+/* Non-finite detection: the number of (step, chunk) pairs in which an updated weight came out
+ * NaN or infinite, summed over all steps so far (a chunk is up to 16384 elements of one tensor). */
 int optim_query_nonfinite(optim_group_t* group, uint64_t* count);
+
+/* ---- pinned-host offload of the states between steps --------------------------------------
+ * The pages keep the moments and Kahan residuals in CPU memory between steps and move each
+ * parameter group's states in for its update and back out afterwards ("Amazing Flux FFT quality
+ * on a 5090", sd-scripts PR #2187, first post; "Kahan summation for Adafactor-optimized Flux
+ * FFT", sd-scripts PR #2159, PR description).  An engine owns n_slots device staging slots of
+ * slot_bytes each and two copy streams (H2D, D2H).  A NADAM group attached to it keeps res_u16,
+ * m and v in PINNED HOST memory (the pointers of its descriptors); weights, gradients and the
+ * per-tensor scale records stay on the device.  optim_step_nadam_kahan on such a group
+ * prefetches if needed, makes the caller's stream wait (device-side) for the copy-in, runs the
+ * update on the staging slot and enqueues the copy-out; the host never blocks.  Calling
+ * optim_offload_prefetch for the next group before stepping the current one overlaps the copies
+ * with the kernels.  At most n_slots - 1 groups may be prefetched ahead of the one being stepped
+ * (else OPTIM_ESTATE).  Host states are valid again after optim_offload_sync. */
+typedef struct optim_offload optim_offload_t;
+int optim_offload_create(size_t slot_bytes, int32_t n_slots, optim_offload_t** out);
+/* Waits (bounded) for the engine's copies, then frees it; OPTIM_ESTATE while groups are attached. */
+int optim_offload_destroy(optim_offload_t* engine);
+/* Binds a NADAM group (before its first offloaded step); OPTIM_EINVAL if a state buffer is not
+ * pinned host memory or the group does not fit in one slot. Destroying the group unbinds it. */
+int optim_group_attach_offload(optim_group_t* group, optim_offload_t* engine);
+/* Enqueues the copy-in of the group's states into the next staging slot. */
+int optim_offload_prefetch(optim_group_t* group);
+/* Bounded wait for every enqueued copy; returns the bytes copied in each direction so far. */
+int optim_offload_sync(optim_offload_t* engine, uint64_t* bytes_h2d, uint64_t* bytes_d2h);
 
 /* Profiling hook: when `event` (a cudaEvent_t passed as void*) is not NULL, the next step calls
  * of this group record it on their stream between the pre-pass (gradient max, or the factored

@@ -8,8 +8,7 @@
 #include <thread>
 #include <vector>
 
-#include "factored.h"
-#include "internal.h"
+#include "group.h"
 
 namespace lmo {
 
@@ -48,7 +47,7 @@ unsigned grid_for(int64_t units) {
 }
 
 // Bounded host wait: polls the event until it completes or `timeout_s` passes.
-static int wait_event(cudaEvent_t ev, double timeout_s, const char* what) {
+int wait_event(cudaEvent_t ev, double timeout_s, const char* what) {
     auto t0 = std::chrono::steady_clock::now();
     for (;;) {
         cudaError_t e = cudaEventQuery(ev);
@@ -60,43 +59,14 @@ static int wait_event(cudaEvent_t ev, double timeout_s, const char* what) {
     }
 }
 
-constexpr double kWaitTimeout = 120.0;
 
 }  // namespace lmo
 
 using namespace lmo;
 
-struct optim_group {
-    int32_t kind = 0;
-    int device = 0;
-    int32_t n = 0;
-    std::vector<optim_tensor_desc_t> desc;
-    // device tables
-    TensorRec* d_tensors = nullptr;
-    const uint16_t** d_grads = nullptr;
-    ScaleRec* d_scales = nullptr;
-    Chunk* d_chunks = nullptr;
-    unsigned long long* d_nonfinite = nullptr;
-    int32_t n_chunks_large = 0;
-    int32_t n_chunks_total = 0;
-    FactoredPlan* fplan = nullptr;
-    // gradient pointers: host copy of the last upload, two pinned staging slots
-    std::vector<const void*> cur_grads;
-    bool grads_valid = false;
-    const void** h_stage[2] = {nullptr, nullptr};
-    cudaEvent_t stage_ev[2] = {nullptr, nullptr};
-    int stage_slot = 0;
-    cudaEvent_t sync_ev = nullptr;
-    // step bookkeeping
-    int64_t last_step = 0;
-    double mu_product = 1.0;
-    int next_parity = 0;
-    cudaStream_t last_stream = nullptr;
-    cudaEvent_t profile_ev = nullptr;
-};
-
 static void group_free(optim_group* g) {
     if (!g) return;
+    offload_unbind(g);
     for (int s = 0; s < 2; ++s) {
         if (g->stage_ev[s]) {
             cudaEventSynchronize(g->stage_ev[s]);
@@ -315,7 +285,12 @@ int optim_step_nadam_kahan(optim_group_t* g, const void* const* grads, int64_t s
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     rc = upload_grads(g, grads, s);
     if (rc) return rc;
-    NadamLaunch L{g->d_tensors, g->d_grads, g->d_scales, g->d_chunks, g->d_nonfinite,
+    const TensorRec* table = g->d_tensors;
+    if (g->offload) {
+        rc = offload_step_begin(g, s, &table);
+        if (rc) return rc;
+    }
+    NadamLaunch L{table, g->d_grads, g->d_scales, g->d_chunks, g->d_nonfinite,
                   g->n_chunks_large, g->n_chunks_total};
     rc = launch_nadam_step(L, k, s, g->profile_ev);
     if (rc) return rc;
@@ -323,6 +298,7 @@ int optim_step_nadam_kahan(optim_group_t* g, const void* const* grads, int64_t s
     g->mu_product = mu_product;
     g->next_parity ^= 1;
     g->last_stream = s;
+    if (g->offload) return offload_step_end(g, s);
     return OPTIM_OK;
 }
 

@@ -92,11 +92,11 @@ __global__ void __launch_bounds__(kThreads) k_encode(const float* __restrict__ s
                                                      uint16_t* __restrict__ codes, int64_t n,
                                                      const float* scale, int is_signed) {
     const float s = *scale;
-    const float inv = is_signed ? inv_scale_m(s) : inv_scale_v(s);
+    const CodecK c = codec_consts(s, s);
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
         float x = src[i];
-        codes[i] = (uint16_t)(is_signed ? enc_m(x, inv) : enc_v(__fsqrt_rn(x), inv));
+        codes[i] = (uint16_t)(is_signed ? enc_m(x, c.rm) : enc_v(__fsqrt_rn(x), c.rv));
     }
 }
 
@@ -104,9 +104,10 @@ __global__ void __launch_bounds__(kThreads) k_decode(const uint16_t* __restrict_
                                                      float* __restrict__ dst, int64_t n,
                                                      const float* scale, int is_signed) {
     const float s = *scale;
+    const CodecK c = codec_consts(s, s);
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
-        dst[i] = is_signed ? dec_m(codes[i], s) : dec_v(codes[i], s);
+        dst[i] = is_signed ? dec_m(codes[i], c.qm) : dec_v(codes[i], c.qv);
 }
 
 }  // namespace

@@ -1,9 +1,10 @@
 // common.cuh -- device helpers and tables shared by the engine's kernels (sm_103a).
 //
 // Every floating-point operation on the state path is an explicit round-to-nearest intrinsic
-// (__fmul_rn, __fadd_rn, __fsqrt_rn, __fdiv_rn), which the compiler never fuses into FMA; the
-// library is also built with --fmad=false.  The results are therefore the IEEE fp32 results of
-// the operation order written here, on every run.
+// (__fmul_rn, __fadd_rn, __fsqrt_rn, __fdiv_rn, and __fmaf_rn where a fused multiply-add with
+// one rounding is meant), which the compiler never fuses or reorders; the library is also built
+// with --fmad=false.  The results are therefore the IEEE fp32 results of the operation order
+// written here, on every run.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -66,32 +67,63 @@ __device__ __forceinline__ uint32_t rne_bf16(float x) {
     return up & 0xFFFFu;
 }
 
-// ---- u16 companded codec (exp_avg: exponent 1/2, bias 32768; exp_avg_sq: exponent 1/4) ----
-__device__ __forceinline__ float inv_scale_m(float s) {
-    return s > 0.0f ? fminf(__fdiv_rn(1.0f, s), FLT_MAX) : 0.0f;
+// ---- u16 companded codec --------------------------------------------------------------
+// Curve: exp_avg code = 32768 + sgn(m) rint(32767 (|m|/S)^(1/2)); exp_avg_sq code =
+// rint(65535 (v/S)^(1/4)).  Scale and code step are folded into four per-tensor constants:
+//   qm = sqrt(S_m)/32767, rm = 1/qm^2   (decode m = t|t|, t = (c-32768) qm; encode sqrt(|m| rm))
+//   qv = S_v^(1/4)/65535, rv = 1/qv^2   (decode v = (z z)(z z), z = c qv; encode sqrt(sqrt(v) rv))
+struct CodecK {
+    float qm, rm, qv, rv;
+};
+__device__ __forceinline__ CodecK codec_consts(float s_m, float s_v) {
+    CodecK c;
+    c.qm = __fmul_rn(__fsqrt_rn(s_m), 1.0f / 32767.0f);
+    c.rm = s_m > 0.0f ? fminf(__fdiv_rn(1.0f, __fmul_rn(c.qm, c.qm)), FLT_MAX) : 0.0f;
+    c.qv = __fmul_rn(__fsqrt_rn(__fsqrt_rn(s_v)), 1.0f / 65535.0f);
+    c.rv = s_v > 0.0f ? fminf(__fdiv_rn(1.0f, __fmul_rn(c.qv, c.qv)), FLT_MAX) : 0.0f;
+    return c;
 }
-__device__ __forceinline__ float inv_scale_v(float s) {
-    return s > 0.0f ? __fdiv_rn(1.0f, __fsqrt_rn(s)) : 0.0f;
+
+// Exact int -> float of a 16-bit field without the conversion unit: the field is placed in the
+// mantissa of 2^23 and 2^23 is subtracted.  sel: 0x7610 for the low half of `word`, 0x7632 for
+// the high half.
+template <unsigned kSel>
+__device__ __forceinline__ float u16_field_to_f32(uint32_t word, float minus) {
+    return __fadd_rn(__uint_as_float(__byte_perm(word, 0x4B000000u, kSel)), minus);
 }
-__device__ __forceinline__ float dec_m(uint32_t c, float s) {
-    float t = __fmul_rn(__int2float_rn((int)c - 32768), 1.0f / 32767.0f);
-    return __fmul_rn(__fmul_rn(t, fabsf(t)), s);
+// Decoded moments of the code in the low (kSel 0x7610) or high (0x7632) half of a word.
+template <unsigned kSel>
+__device__ __forceinline__ float dec_m_field(uint32_t word, float qm) {
+    const float t = __fmul_rn(u16_field_to_f32<kSel>(word, -8421376.0f), qm);   // c - 32768
+    return __fmul_rn(t, fabsf(t));
 }
-__device__ __forceinline__ float dec_v(uint32_t c, float s) {
-    float z = __fmul_rn(__uint2float_rn(c), 1.0f / 65535.0f);
-    float z2 = __fmul_rn(z, z);
-    return __fmul_rn(__fmul_rn(z2, z2), s);
+template <unsigned kSel>
+__device__ __forceinline__ float dec_v_field(uint32_t word, float qv) {
+    const float z = __fmul_rn(u16_field_to_f32<kSel>(word, -8388608.0f), qv);
+    const float z2 = __fmul_rn(z, z);
+    return __fmul_rn(z2, z2);
 }
-__device__ __forceinline__ uint32_t enc_m(float m, float inv) {
-    float y = __fsqrt_rn(__fmul_rn(fabsf(m), inv));
-    uint32_t k = __float2uint_rn(fminf(__fmul_rn(y, 32767.0f), 32767.0f));
-    return (__float_as_uint(m) >> 31) ? 32768u - k : 32768u + k;
+__device__ __forceinline__ float dec_m(uint32_t c, float qm) { return dec_m_field<0x7610>(c, qm); }
+__device__ __forceinline__ float dec_v(uint32_t c, float qv) { return dec_v_field<0x7610>(c, qv); }
+
+// Encoders return a float whose low 16 bits are the code: adding 1.5*2^23 (+32768 for the
+// biased exp_avg code) rounds the clamped root to the nearest integer, ties to even, exactly as
+// rint, and leaves it in the low mantissa bits.
+__device__ __forceinline__ uint32_t enc_m_bits(float m, float rm) {
+    const float y = fminf(__fsqrt_rn(__fmul_rn(fabsf(m), rm)), 32767.0f);
+    return __float_as_uint(__fadd_rn(12615680.0f, copysignf(y, m)));
 }
 // sv = sqrt(v), shared with the update's denominator.
-__device__ __forceinline__ uint32_t enc_v(float sv, float rs) {
-    float y = __fsqrt_rn(__fmul_rn(sv, rs));
-    return __float2uint_rn(fminf(__fmul_rn(y, 65535.0f), 65535.0f));
+__device__ __forceinline__ uint32_t enc_v_bits(float sv, float rv) {
+    const float y = fminf(__fsqrt_rn(__fmul_rn(sv, rv)), 65535.0f);
+    return __float_as_uint(__fadd_rn(12582912.0f, y));
 }
+__device__ __forceinline__ uint32_t enc_m(float m, float rm) { return enc_m_bits(m, rm) & 0xFFFFu; }
+__device__ __forceinline__ uint32_t enc_v(float sv, float rv) { return enc_v_bits(sv, rv) & 0xFFFFu; }
+
+// Packs the low 16 bits of two words (element 0 low, element 1 high) / the high 16 bits.
+__device__ __forceinline__ uint32_t pack_lo16(uint32_t e0, uint32_t e1) { return __byte_perm(e0, e1, 0x5410); }
+__device__ __forceinline__ uint32_t pack_hi16(uint32_t e0, uint32_t e1) { return __byte_perm(e0, e1, 0x7632); }
 
 // ---- block reductions (kThreads threads) ----
 __device__ __forceinline__ uint32_t warp_max_u32(uint32_t x) {

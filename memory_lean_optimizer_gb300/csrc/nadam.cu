@@ -11,13 +11,13 @@
 // a 5090" (sd-scripts PR #2187: NAdam(W) first post, u16 scaled/biased/pow()-companded moments
 // and the 4096-element fp32 rule second post, moments used only as storage third post).
 //
-// Per element the order of operations is:
+// Per element the order of operations is (fma = one rounding):
 //   w  = f32(hi<<16 | lo);  g = f32(g_bf16<<16)
-//   m  = b1*m0 + (1-b1)*g;  v = b2*v0 + (1-b2)*(g*g)
-//   w  = w - (lr*wd)*w                                   (decoupled decay only)
-//   sv = sqrt(v);  den = sv*k2 + eps;  num = c_m*m + c_g*g;  w = w - lr*(num/den)
-//   (hi, lo) = split(w);  codes = enc_m(m, 1/S_m), enc_v(sv, 1/sqrt(S_v))
-// with S_m = b1*A_m(prev) + (1-b1)*G, S_v = b2*A_v(prev) + (1-b2)*G*G per tensor.
+//   m  = fma(b1, m0, (1-b1)*g);  v = fma(b2, v0, (1-b2)*(g*g))
+//   w  = fma(-(lr*wd), w, w)                              (decoupled decay only)
+//   sv = sqrt(v);  den = fma(sv, k2, eps);  num = fma(c_m, m, c_g*g);  w = fma(-lr, num/den, w)
+//   (hi, lo) = split(w);  codes = enc_m(m), enc_v(sv) with the per-tensor codec constants
+// with S_m = fma(b1, A_m(prev), (1-b1)*G), S_v = fma(b2, A_v(prev), (1-b2)*G*G) per tensor.
 //
 // Memory: 18 bytes per u16-state element per step (read w, res, g, m, v; write w, res, m, v),
 // 26 bytes per fp32-state element, plus 2 bytes of K1's gradient read.  All accesses are
@@ -80,91 +80,82 @@ __global__ void __launch_bounds__(kThreads) k_grad_absmax(NadamLaunch L, int par
 }
 
 // ------------------------------------------------------------------------------------ K2
-// One element.  hi/lo/g are 16-bit words; m0/v0 the decoded (or fp32) moments; outputs in place.
-__device__ __forceinline__ void elem(const Prm& k, uint32_t& hi, uint32_t& lo, bool has_res,
-                                     uint32_t gb, float& m, float& v, float& sv, uint32_t& nonfin) {
-    float w = has_res ? __uint_as_float((hi << 16) | lo) : bf16_to_f32(hi);
-    const float g = bf16_to_f32(gb);
-    m = __fadd_rn(__fmul_rn(k.b1, m), __fmul_rn(k.omb1, g));
-    v = __fadd_rn(__fmul_rn(k.b2, v), __fmul_rn(k.omb2, __fmul_rn(g, g)));
-    if (k.decoupled) w = __fsub_rn(w, __fmul_rn(k.lr_wd, w));
+// One element: w, g fp32; m, v in: decoded (or fp32) moments, out: new moments; sv = sqrt(v).
+__device__ __forceinline__ float elem(const Prm& k, float w, float g, float& m, float& v, float& sv) {
+    m = __fmaf_rn(k.b1, m, __fmul_rn(k.omb1, g));
+    v = __fmaf_rn(k.b2, v, __fmul_rn(k.omb2, __fmul_rn(g, g)));
+    if (k.decoupled) w = __fmaf_rn(-k.lr_wd, w, w);
     sv = __fsqrt_rn(v);
-    const float den = __fadd_rn(__fmul_rn(sv, k.k2), k.eps);
-    const float num = __fadd_rn(__fmul_rn(k.c_m, m), __fmul_rn(k.c_g, g));
-    w = __fsub_rn(w, __fmul_rn(k.lr, __fdiv_rn(num, den)));
-    const uint32_t b = __float_as_uint(w);
+    const float den = __fmaf_rn(sv, k.k2, k.eps);
+    const float num = __fmaf_rn(k.c_m, m, __fmul_rn(k.c_g, g));
+    return __fmaf_rn(-k.lr, __fdiv_rn(num, den), w);
+}
+
+// Weight words in/out for two elements packed in 32-bit words W (bf16 weights) and R (residuals).
+__device__ __forceinline__ void unpack_w(uint32_t W, uint32_t R, bool has_res, float& w0, float& w1) {
+    w0 = __uint_as_float(has_res ? __byte_perm(R, W, 0x5410) : (W << 16));
+    w1 = __uint_as_float(has_res ? __byte_perm(R, W, 0x7632) : (W & 0xFFFF0000u));
+}
+__device__ __forceinline__ void pack_w(float w0, float w1, bool has_res, uint32_t& W, uint32_t& R) {
+    const uint32_t b0 = __float_as_uint(w0), b1 = __float_as_uint(w1);
     if (has_res) {
-        hi = b >> 16;
-        lo = b & 0xFFFFu;
+        W = pack_hi16(b0, b1);
+        R = pack_lo16(b0, b1);
     } else {
-        hi = rne_bf16(w);
+        W = pack_lo16(rne_bf16(w0), rne_bf16(w1));
     }
-    nonfin += ((b & 0x7F800000u) == 0x7F800000u) ? 1u : 0u;
 }
 
 struct Codec {
-    float s_m_dec, s_v_dec, inv_m, rs_v;
+    CodecK dec, enc;
 };
 
-// Eight u16-state elements packed in 128-bit words.
-__device__ __forceinline__ void step8_u16(const Prm& k, const Codec& cd, bool has_res, uint4& W,
-                                          uint4& R, const uint4& G, uint4& M, uint4& V,
-                                          uint32_t& am, uint32_t& av, uint32_t& nonfin) {
-    uint32_t* w32 = reinterpret_cast<uint32_t*>(&W);
-    uint32_t* r32 = reinterpret_cast<uint32_t*>(&R);
-    const uint32_t* g32 = reinterpret_cast<const uint32_t*>(&G);
-    uint32_t* m32 = reinterpret_cast<uint32_t*>(&M);
-    uint32_t* v32 = reinterpret_cast<uint32_t*>(&V);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        uint32_t ow = 0, orr = 0, om = 0, ov = 0;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int sh = 16 * h;
-            uint32_t hi = (w32[j] >> sh) & 0xFFFFu, lo = (r32[j] >> sh) & 0xFFFFu;
-            const uint32_t gb = (g32[j] >> sh) & 0xFFFFu;
-            float m = dec_m((m32[j] >> sh) & 0xFFFFu, cd.s_m_dec);
-            float v = dec_v((v32[j] >> sh) & 0xFFFFu, cd.s_v_dec);
-            float sv;
-            elem(k, hi, lo, has_res, gb, m, v, sv, nonfin);
-            ow |= hi << sh;
-            orr |= lo << sh;
-            om |= enc_m(m, cd.inv_m) << sh;
-            ov |= enc_v(sv, cd.rs_v) << sh;
-            am = max(am, __float_as_uint(m) & 0x7FFFFFFFu);
-            av = max(av, __float_as_uint(v) & 0x7FFFFFFFu);
-        }
-        w32[j] = ow;
-        r32[j] = orr;
-        m32[j] = om;
-        v32[j] = ov;
-    }
+// Two u16-state elements.  am/av: running max |m|, max v (NaN skipped); nf: running max of the
+// bf16 weight magnitudes (>= 0x7F80 in either half means a non-finite weight).
+__device__ __forceinline__ void step2_u16(const Prm& k, const Codec& cd, bool has_res, uint32_t& W,
+                                          uint32_t& R, uint32_t G, uint32_t& M, uint32_t& V, float& am,
+                                          float& av, uint32_t& nf) {
+    float w0, w1;
+    unpack_w(W, R, has_res, w0, w1);
+    float m0 = dec_m_field<0x7610>(M, cd.dec.qm), m1 = dec_m_field<0x7632>(M, cd.dec.qm);
+    float v0 = dec_v_field<0x7610>(V, cd.dec.qv), v1 = dec_v_field<0x7632>(V, cd.dec.qv);
+    float s0, s1;
+    w0 = elem(k, w0, __uint_as_float(G << 16), m0, v0, s0);
+    w1 = elem(k, w1, __uint_as_float(G & 0xFFFF0000u), m1, v1, s1);
+    pack_w(w0, w1, has_res, W, R);
+    M = pack_lo16(enc_m_bits(m0, cd.enc.rm), enc_m_bits(m1, cd.enc.rm));
+    V = pack_lo16(enc_v_bits(s0, cd.enc.rv), enc_v_bits(s1, cd.enc.rv));
+    am = fmaxf(am, fmaxf(fabsf(m0), fabsf(m1)));
+    av = fmaxf(av, fmaxf(v0, v1));
+    nf = __vmaxu2(nf, W & 0x7FFF7FFFu);
 }
 
-// Eight fp32-state elements (numel <= 4096): m, v as two float4 each.
-__device__ __forceinline__ void step8_f32(const Prm& k, bool has_res, uint4& W, uint4& R,
-                                          const uint4& G, float4 (&M)[2], float4 (&V)[2],
-                                          uint32_t& nonfin) {
-    uint32_t* w32 = reinterpret_cast<uint32_t*>(&W);
-    uint32_t* r32 = reinterpret_cast<uint32_t*>(&R);
-    const uint32_t* g32 = reinterpret_cast<const uint32_t*>(&G);
-    float* mf = reinterpret_cast<float*>(&M[0]);
-    float* vf = reinterpret_cast<float*>(&V[0]);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        uint32_t ow = 0, orr = 0;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int sh = 16 * h;
-            uint32_t hi = (w32[j] >> sh) & 0xFFFFu, lo = (r32[j] >> sh) & 0xFFFFu;
-            float sv;
-            elem(k, hi, lo, has_res, (g32[j] >> sh) & 0xFFFFu, mf[2 * j + h], vf[2 * j + h], sv, nonfin);
-            ow |= hi << sh;
-            orr |= lo << sh;
-        }
-        w32[j] = ow;
-        r32[j] = orr;
-    }
+// Two fp32-state elements (numel <= 4096).
+__device__ __forceinline__ void step2_f32(const Prm& k, bool has_res, uint32_t& W, uint32_t& R, uint32_t G,
+                                          float& m0, float& m1, float& v0, float& v1, uint32_t& nf) {
+    float w0, w1, s0, s1;
+    unpack_w(W, R, has_res, w0, w1);
+    w0 = elem(k, w0, __uint_as_float(G << 16), m0, v0, s0);
+    w1 = elem(k, w1, __uint_as_float(G & 0xFFFF0000u), m1, v1, s1);
+    pack_w(w0, w1, has_res, W, R);
+    nf = __vmaxu2(nf, W & 0x7FFF7FFFu);
+}
+
+__device__ __forceinline__ void step8_u16(const Prm& k, const Codec& cd, bool has_res, uint4& W, uint4& R,
+                                          const uint4& G, uint4& M, uint4& V, float& am, float& av,
+                                          uint32_t& nf) {
+    step2_u16(k, cd, has_res, W.x, R.x, G.x, M.x, V.x, am, av, nf);
+    step2_u16(k, cd, has_res, W.y, R.y, G.y, M.y, V.y, am, av, nf);
+    step2_u16(k, cd, has_res, W.z, R.z, G.z, M.z, V.z, am, av, nf);
+    step2_u16(k, cd, has_res, W.w, R.w, G.w, M.w, V.w, am, av, nf);
+}
+
+__device__ __forceinline__ void step8_f32(const Prm& k, bool has_res, uint4& W, uint4& R, const uint4& G,
+                                          float4 (&M)[2], float4 (&V)[2], uint32_t& nf) {
+    step2_f32(k, has_res, W.x, R.x, G.x, M[0].x, M[0].y, V[0].x, V[0].y, nf);
+    step2_f32(k, has_res, W.y, R.y, G.y, M[0].z, M[0].w, V[0].z, V[0].w, nf);
+    step2_f32(k, has_res, W.z, R.z, G.z, M[1].x, M[1].y, V[1].x, V[1].y, nf);
+    step2_f32(k, has_res, W.w, R.w, G.w, M[1].z, M[1].w, V[1].z, V[1].w, nf);
 }
 
 __global__ void __launch_bounds__(kThreads) k_nadam_step(NadamLaunch L, Prm k, int parity) {
@@ -178,24 +169,23 @@ __global__ void __launch_bounds__(kThreads) k_nadam_step(NadamLaunch L, Prm k, i
     const int64_t start = (int64_t)c.index * kChunk;
     const int64_t end = min(t.numel, start + kChunk);
 
-    Codec cd = {0.f, 0.f, 0.f, 0.f};
+    Codec cd{};
     ScaleRec* sr = L.scales + c.tensor;
     if (!small) {
         const float a_m = __uint_as_float(sr->a_m[q]), a_v = __uint_as_float(sr->a_v[q]);
         const float G = __uint_as_float(sr->g[p]);
-        const float s_m = __fadd_rn(__fmul_rn(k.b1, a_m), __fmul_rn(k.omb1, G));
-        const float s_v = __fadd_rn(__fmul_rn(k.b2, a_v), __fmul_rn(k.omb2, __fmul_rn(G, G)));
-        cd.s_m_dec = sr->s_m[q];
-        cd.s_v_dec = sr->s_v[q];
-        cd.inv_m = inv_scale_m(s_m);
-        cd.rs_v = inv_scale_v(s_v);
+        const float s_m = __fmaf_rn(k.b1, a_m, __fmul_rn(k.omb1, G));
+        const float s_v = __fmaf_rn(k.b2, a_v, __fmul_rn(k.omb2, __fmul_rn(G, G)));
+        cd.dec = codec_consts(sr->s_m[q], sr->s_v[q]);
+        cd.enc = codec_consts(s_m, s_v);
         if (c.index == 0 && threadIdx.x == 0) {
             sr->s_m[p] = s_m;
             sr->s_v[p] = s_v;
         }
     }
 
-    uint32_t am = 0u, av = 0u, nonfin = 0u;
+    float am = 0.f, av = 0.f;
+    uint32_t nf = 0u;
     uint16_t* __restrict__ w = t.w;
     uint16_t* __restrict__ res = t.res;
     const bool vec = aligned16(w) && (!has_res || aligned16(res)) && aligned16(t.m) &&
@@ -219,12 +209,12 @@ __global__ void __launch_bounds__(kThreads) k_nadam_step(NadamLaunch L, Prm k, i
                 uint4 G0 = ld_stream(gv + i), G1 = ld_stream(gv + i1);
                 uint4 M0 = ld_stream(mv + i), M1 = ld_stream(mv + i1);
                 uint4 V0 = ld_stream(vv + i), V1 = ld_stream(vv + i1);
-                step8_u16(k, cd, has_res, W0, R0, G0, M0, V0, am, av, nonfin);
+                step8_u16(k, cd, has_res, W0, R0, G0, M0, V0, am, av, nf);
                 st_stream(wv + i, W0);
                 if (has_res) st_stream(rv + i, R0);
                 st_stream(mv + i, M0);
                 st_stream(vv + i, V0);
-                step8_u16(k, cd, has_res, W1, R1, G1, M1, V1, am, av, nonfin);
+                step8_u16(k, cd, has_res, W1, R1, G1, M1, V1, am, av, nf);
                 st_stream(wv + i1, W1);
                 if (has_res) st_stream(rv + i1, R1);
                 st_stream(mv + i1, M1);
@@ -234,7 +224,7 @@ __global__ void __launch_bounds__(kThreads) k_nadam_step(NadamLaunch L, Prm k, i
                 uint4 W0 = ld_stream(wv + i);
                 uint4 R0 = has_res ? ld_stream(rv + i) : make_uint4(0, 0, 0, 0);
                 uint4 G0 = ld_stream(gv + i), M0 = ld_stream(mv + i), V0 = ld_stream(vv + i);
-                step8_u16(k, cd, has_res, W0, R0, G0, M0, V0, am, av, nonfin);
+                step8_u16(k, cd, has_res, W0, R0, G0, M0, V0, am, av, nf);
                 st_stream(wv + i, W0);
                 if (has_res) st_stream(rv + i, R0);
                 st_stream(mv + i, M0);
@@ -249,7 +239,7 @@ __global__ void __launch_bounds__(kThreads) k_nadam_step(NadamLaunch L, Prm k, i
                 uint4 G0 = ld_stream(gv + i);
                 float4 M[2] = {ld_stream(mv + 2 * i), ld_stream(mv + 2 * i + 1)};
                 float4 V[2] = {ld_stream(vv + 2 * i), ld_stream(vv + 2 * i + 1)};
-                step8_f32(k, has_res, W0, R0, G0, M, V, nonfin);
+                step8_f32(k, has_res, W0, R0, G0, M, V, nf);
                 st_stream(wv + i, W0);
                 if (has_res) st_stream(rv + i, R0);
                 st_stream(mv + 2 * i, M[0]);
@@ -262,44 +252,41 @@ __global__ void __launch_bounds__(kThreads) k_nadam_step(NadamLaunch L, Prm k, i
     }
     // element-by-element: ragged tail, or the whole chunk when a buffer is not 16-byte aligned
     for (int64_t i = done + threadIdx.x; i < end; i += kThreads) {
-        uint32_t hi = w[i], lo = has_res ? res[i] : 0u;
+        const float w0 = has_res ? __uint_as_float(((uint32_t)w[i] << 16) | res[i]) : bf16_to_f32(w[i]);
         float m, v, sv;
         if (small) {
             m = static_cast<float*>(t.m)[i];
             v = static_cast<float*>(t.v)[i];
         } else {
-            m = dec_m(static_cast<uint16_t*>(t.m)[i], cd.s_m_dec);
-            v = dec_v(static_cast<uint16_t*>(t.v)[i], cd.s_v_dec);
+            m = dec_m(static_cast<uint16_t*>(t.m)[i], cd.dec.qm);
+            v = dec_v(static_cast<uint16_t*>(t.v)[i], cd.dec.qv);
         }
-        elem(k, hi, lo, has_res, g[i], m, v, sv, nonfin);
+        const float w1 = elem(k, w0, bf16_to_f32(g[i]), m, v, sv);
+        const uint32_t b = __float_as_uint(w1);
+        const uint32_t hi = has_res ? (b >> 16) : rne_bf16(w1);
         w[i] = (uint16_t)hi;
-        if (has_res) res[i] = (uint16_t)lo;
+        if (has_res) res[i] = (uint16_t)(b & 0xFFFFu);
+        nf = max(nf, hi & 0x7FFFu);
         if (small) {
             static_cast<float*>(t.m)[i] = m;
             static_cast<float*>(t.v)[i] = v;
         } else {
-            static_cast<uint16_t*>(t.m)[i] = (uint16_t)enc_m(m, cd.inv_m);
-            static_cast<uint16_t*>(t.v)[i] = (uint16_t)enc_v(sv, cd.rs_v);
-            am = max(am, __float_as_uint(m) & 0x7FFFFFFFu);
-            av = max(av, __float_as_uint(v) & 0x7FFFFFFFu);
+            static_cast<uint16_t*>(t.m)[i] = (uint16_t)enc_m(m, cd.enc.rm);
+            static_cast<uint16_t*>(t.v)[i] = (uint16_t)enc_v(sv, cd.enc.rv);
+            am = fmaxf(am, fabsf(m));
+            av = fmaxf(av, v);
         }
     }
 
-    // per-tensor maxima for the next step's scales, and the non-finite count
-    uint32_t r[2] = {am, av};
-    nonfin = warp_sum_u32(nonfin);
-    block_max_u32<2>(r, red);
-    __shared__ uint32_t nf[32];
-    if ((threadIdx.x & 31) == 0) nf[threadIdx.x >> 5] = nonfin;
-    __syncthreads();
+    // per-tensor maxima for the next step's scales; one count per chunk with a non-finite weight
+    uint32_t r[3] = {__float_as_uint(am), __float_as_uint(av), (max(nf & 0xFFFFu, nf >> 16) >= 0x7F80u) ? 1u : 0u};
+    block_max_u32<3>(r, red);
     if (threadIdx.x == 0) {
-        uint32_t tot = 0;
-        for (int wi = 0; wi < kThreads / 32; ++wi) tot += nf[wi];
         if (!small) {
             if (r[0]) atomicMax(&sr->a_m[p], r[0]);
             if (r[1]) atomicMax(&sr->a_v[p], r[1]);
         }
-        if (tot) atomicAdd(L.nonfinite, (unsigned long long)tot);
+        if (r[2]) atomicAdd(L.nonfinite, 1ull);
     }
 }
 

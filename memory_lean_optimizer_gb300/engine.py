@@ -105,41 +105,90 @@ class _Group:
         return ptrs
 
 
+def _round256(x: int) -> int:
+    return (x + 255) & ~255
+
+
+def offload_slot_bytes(numels: Sequence[int], kahan: bool = True) -> int:
+    """Staging bytes one offloaded NADAM group of tensors with these sizes needs in a slot."""
+    tot = 0
+    for n in numels:
+        sm = (4 if n <= SMALL else 2) * n
+        tot += (_round256(2 * n) if kahan else 0) + 2 * _round256(sm)
+    return tot
+
+
+class OffloadEngine:
+    """Device staging ring + copy streams for groups whose states live in pinned host memory."""
+
+    def __init__(self, slot_bytes: int, n_slots: int = 3):
+        self.handle = lmopt.optim_offload_create(int(slot_bytes), int(n_slots))
+
+    def sync(self):
+        return lmopt.optim_offload_sync(self.handle)
+
+    def close(self):
+        if self.handle:
+            lmopt.optim_offload_destroy(self.handle)
+            self.handle = None
+
+
+def _state_buffer(n: int, dtype, device, pinned: bool, fill: int = 0) -> torch.Tensor:
+    if pinned:
+        t = torch.empty(n, dtype=dtype, pin_memory=True)
+        t.fill_(fill - 65536 if (dtype == torch.int16 and fill >= 32768) else fill)
+        return t
+    if dtype == torch.int16:
+        return _u16_empty(n, device, fill)
+    return torch.full((n,), float(fill), dtype=dtype, device=device)
+
+
 class NadamGroup(_Group):
-    """Kahan + u16-moment NAdam(W)/Adam state for a list of bf16 weights (one library group)."""
+    """Kahan + u16-moment NAdam(W)/Adam state for a list of bf16 weights (one library group).
+    With `offload`, residuals and moments live in pinned host memory and move through the
+    engine's staging slots around each step."""
 
     kind = lmopt.OPTIM_KIND_NADAM
 
     def __init__(self, weights: Sequence[torch.Tensor], residuals: Sequence[torch.Tensor] | None = None,
-                 kahan: bool = True):
+                 kahan: bool = True, offload: OffloadEngine | None = None):
         super().__init__()
         self.weights = list(weights)
         for w in self.weights:
             assert w.dtype == torch.bfloat16 and w.is_cuda and w.is_contiguous()
         dev = self.weights[0].device
+        pinned = offload is not None
         if residuals is None:
-            residuals = [_u16_empty(w.numel(), dev, 0) if kahan else None for w in self.weights]
+            residuals = [_state_buffer(w.numel(), torch.int16, dev, pinned) if kahan else None for w in self.weights]
+        elif pinned:
+            residuals = [r.cpu().pin_memory() if r is not None else None for r in residuals]
         self.res = list(residuals)
         self.m, self.v = [], []
         for w in self.weights:
             n = w.numel()
             if n <= SMALL:
-                self.m.append(torch.zeros(n, dtype=torch.float32, device=dev))
-                self.v.append(torch.zeros(n, dtype=torch.float32, device=dev))
+                self.m.append(_state_buffer(n, torch.float32, dev, pinned))
+                self.v.append(_state_buffer(n, torch.float32, dev, pinned))
             else:
-                self.m.append(_u16_empty(n, dev, 32768))
-                self.v.append(_u16_empty(n, dev, 0))
+                self.m.append(_state_buffer(n, torch.int16, dev, pinned, 32768))
+                self.v.append(_state_buffer(n, torch.int16, dev, pinned, 0))
         descs = [_desc(w, r, m, v, w.shape) for w, r, m, v in zip(self.weights, self.res, self.m, self.v)]
         self.handle = lmopt.optim_group_create(descs, self.kind)
+        self.offload = offload
+        if offload is not None:
+            lmopt.optim_group_attach_offload(self.handle, offload.handle)
+
+    def prefetch(self):
+        lmopt.optim_offload_prefetch(self.handle)
 
     @classmethod
-    def from_masters(cls, masters: Sequence[torch.Tensor], stream=None):
+    def from_masters(cls, masters: Sequence[torch.Tensor], stream=None, offload: OffloadEngine | None = None):
         ws, rs = [], []
         for x in masters:
             hi, lo = kahan_split(x.contiguous(), stream=stream)
             ws.append(hi)
             rs.append(lo)
-        return cls(ws, rs)
+        return cls(ws, rs, offload=offload)
 
     def step(self, grads: Sequence[torch.Tensor], hp: dict, stream=None):
         h = lmopt.NadamHparams(lr=hp["lr"], beta1=hp["beta1"], beta2=hp["beta2"], eps=hp["eps"],
@@ -149,7 +198,7 @@ class NadamGroup(_Group):
         self.step_count += 1
 
     def masters(self):
-        return [kahan_merge(w, r) for w, r in zip(self.weights, self.res)]
+        return [kahan_merge(w, r.to(w.device)) for w, r in zip(self.weights, self.res)]
 
     def scales(self):
         return lmopt.optim_query_scales(self.handle, len(self.weights))

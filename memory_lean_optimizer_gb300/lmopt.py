@@ -34,6 +34,8 @@ EXPORTED = (
     "state_pack_u16", "state_unpack_u16", "optim_kahan_split", "optim_kahan_merge",
     "optim_query_scales", "optim_set_scales", "optim_group_get_step", "optim_group_set_step",
     "optim_query_nonfinite", "optim_group_set_profile_event", "optim_last_error",
+    "optim_offload_create", "optim_offload_destroy", "optim_group_attach_offload",
+    "optim_offload_prefetch", "optim_offload_sync",
 )
 
 
@@ -91,6 +93,11 @@ def load(path: str = LIB_PATH):
             "optim_group_set_step": [P, I64, ctypes.c_double],
             "optim_query_nonfinite": [P, ctypes.POINTER(ctypes.c_uint64)],
             "optim_group_set_profile_event": [P, P],
+            "optim_offload_create": [ctypes.c_size_t, I32, ctypes.POINTER(P)],
+            "optim_offload_destroy": [P],
+            "optim_group_attach_offload": [P, P],
+            "optim_offload_prefetch": [P],
+            "optim_offload_sync": [P, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -188,3 +195,28 @@ def optim_query_nonfinite(handle: int) -> int:
     c = ctypes.c_uint64()
     check(load().optim_query_nonfinite(handle, ctypes.byref(c)))
     return c.value
+
+
+def optim_offload_create(slot_bytes: int, n_slots: int) -> int:
+    out = ctypes.c_void_p()
+    check(load().optim_offload_create(slot_bytes, n_slots, ctypes.byref(out)))
+    return out.value
+
+
+def optim_offload_destroy(engine: int) -> None:
+    check(load().optim_offload_destroy(engine))
+
+
+def optim_group_attach_offload(handle: int, engine: int) -> None:
+    check(load().optim_group_attach_offload(handle, engine))
+
+
+def optim_offload_prefetch(handle: int) -> None:
+    check(load().optim_offload_prefetch(handle))
+
+
+def optim_offload_sync(engine: int):
+    """Returns (bytes copied host->device, bytes copied device->host) so far."""
+    a, b = ctypes.c_uint64(), ctypes.c_uint64()
+    check(load().optim_offload_sync(engine, ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value

@@ -56,6 +56,10 @@ class Scale(ctypes.Structure):
                 ("a_m", ctypes.c_float), ("a_v", ctypes.c_float)]
 
 
+class CodecConsts(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_float) for n in ("qm", "rm", "qv", "rv")]
+
+
 class FactoredScalars(ctypes.Structure):
     _fields_ = [(n, ctypes.c_float) for n in
                 ("b2t", "alpha", "eps1", "eps2", "clip", "lr_eff", "nwdlr")] + \
@@ -76,8 +80,7 @@ def _load():
             "orc_kahan_split": (None, [P, P, P, I64]),
             "orc_kahan_merge": (None, [P, P, P, I64]),
             "orc_round_bf16": (None, [P, P, I64]),
-            "orc_inv_scale_m": (F, [F]),
-            "orc_inv_scale_v": (F, [F]),
+            "orc_codec_consts": (None, [F, F, ctypes.POINTER(CodecConsts)]),
             "orc_encode_m": (ctypes.c_uint16, [F, F]),
             "orc_decode_m": (F, [ctypes.c_uint16, F]),
             "orc_encode_v": (ctypes.c_uint16, [F, F]),
@@ -141,28 +144,28 @@ def round_bf16(x: np.ndarray) -> np.ndarray:
 
 
 # ---------------------------------------------------------------- u16 codec
-def inv_scale_m(s: float) -> float:
-    return _load().orc_inv_scale_m(s)
+def codec_consts(s_m: float, s_v: float) -> CodecConsts:
+    """Per-tensor codec constants (qm, rm, qv, rv) from the scales S_m, S_v."""
+    c = CodecConsts()
+    _load().orc_codec_consts(s_m, s_v, ctypes.byref(c))
+    return c
 
 
-def inv_scale_v(s: float) -> float:
-    return _load().orc_inv_scale_v(s)
+def encode_m(m: float, rm: float) -> int:
+    return _load().orc_encode_m(m, rm)
 
 
-def encode_m(m: float, inv: float) -> int:
-    return _load().orc_encode_m(m, inv)
+def decode_m(c: int, qm: float) -> float:
+    return _load().orc_decode_m(c, qm)
 
 
-def decode_m(c: int, s: float) -> float:
-    return _load().orc_decode_m(c, s)
+def encode_v(sv: float, rv: float) -> int:
+    """sv = sqrt(v)."""
+    return _load().orc_encode_v(sv, rv)
 
 
-def encode_v(sv: float, rs: float) -> int:
-    return _load().orc_encode_v(sv, rs)
-
-
-def decode_v(c: int, s: float) -> float:
-    return _load().orc_decode_v(c, s)
+def decode_v(c: int, qv: float) -> float:
+    return _load().orc_decode_v(c, qv)
 
 
 def state_pack(x: np.ndarray, is_signed: bool):

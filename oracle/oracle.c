@@ -10,17 +10,20 @@
  * Adafactor-optimized Flux FFT", sd-scripts PR #2159, first comment), and the printed fused
  * Adafactor step casts grad and weight to float32 before updating ("Fused backward pass" commit,
  * library/adafactor_fused.py, adafactor_step_param).  So every per-element operation below is a
- * single IEEE fp32 operation rounded to nearest-even, in the order written, with no contraction
- * (build with -ffp-contract=off).  Means over rows, columns and tensors are summed in double and
- * rounded once to fp32.  Per-step host scalars are computed in double and rounded once.
+ * single IEEE fp32 operation rounded to nearest-even, in the order written: a*b+c written as
+ * fmaf() is one fused rounding (C99 fmaf is exact), everything else rounds per operation and
+ * nothing is contracted implicitly (build with -ffp-contract=off).  Means over rows, columns
+ * and tensors are summed in double and rounded once to fp32.  Per-step host scalars are
+ * computed in double and rounded once.
  *
  * Readings of the pages that this file fixes (each one is listed with its reason in the design
  * notes of the repository):
  *   R1  Kahan split = truncation: hi = upper 16 bits of the f32 pattern, lo = lower 16 bits.
  *   R2  NAdam = Dozat's Nesterov Adam with the momentum schedule mu_t = b1 (1 - 0.5*0.96^(t psi)).
  *   R3  u16 codec for exp_avg: code = 32768 + sgn(m) rint(32767 sqrt(|m|/S)); decode
- *       m = S t|t|, t = (code-32768)/32767.  For exp_avg_sq: code = rint(65535 (v/S)^(1/4)),
- *       computed as sqrt(sqrt(v) / sqrt(S)); decode v = S z^4, z = code/65535.
+ *       m = S t|t|, t = (code-32768)/32767.  For exp_avg_sq: code = rint(65535 (v/S)^(1/4));
+ *       decode v = S z^4, z = code/65535.  Scale and code step are folded into per-tensor
+ *       constants (orc_codec_consts).
  *   R4  Per-tensor scale for step t: S_m = b1 A_m(t-1) + (1-b1) G(t), S_v = b2 A_v(t-1) +
  *       (1-b2) G(t)^2, with A the max over the tensor of the pre-encode moments at t-1 and
  *       G(t) = max |g(t)|.
@@ -87,50 +90,54 @@ void orc_round_bf16(const float* x, uint16_t* out, int64_t n)
 /* ----------------------------------------------------------------------------------------
  * R3: u16 companded codec ("I scale the exp_avg[_sq] structures and store them in
  * scaled/biased uint16 format ... apply a pow() function", sd-scripts PR #2187, second post).
- * Scale S per tensor; the encoder takes the reciprocal inv = 1/S (exp_avg) or rs = 1/sqrt(S)
- * (exp_avg_sq), computed once per tensor.
+ * Curve: exp_avg code = 32768 + sgn(m) rint(32767 (|m|/S)^(1/2)), exp_avg_sq code =
+ * rint(65535 (v/S)^(1/4)).  The code step and the scale are folded into per-tensor constants,
+ * computed once per tensor from S:
+ *   qm = sqrt(S) * (1/32767)      decode  m = t |t|,  t = (code - 32768) qm
+ *   rm = 1 / (qm qm)              encode  k = rint(min(sqrt(|m| rm), 32767))
+ *   qv = sqrt(sqrt(S)) * (1/65535) decode v = (z z)(z z), z = code qv
+ *   rv = 1 / (qv qv)              encode  k = rint(min(sqrt(sqrt(v) rv), 65535))
+ * (rm, rv: 0 when S = 0, at most FLT_MAX otherwise).  Each written operation is one fp32
+ * rounding; sqrt is IEEE-correct; rint rounds half to even.
  * -------------------------------------------------------------------------------------- */
-float orc_inv_scale_m(float s)
+typedef struct { float qm, rm, qv, rv; } orc_codec_t;
+
+void orc_codec_consts(float s_m, float s_v, orc_codec_t* c)
 {
-    if (!(s > 0.0f)) return 0.0f;
-    return fminf(1.0f / s, FLT_MAX);
+    c->qm = sqrtf(s_m) * (1.0f / 32767.0f);
+    c->rm = (s_m > 0.0f) ? fminf(1.0f / (c->qm * c->qm), FLT_MAX) : 0.0f;
+    c->qv = sqrtf(sqrtf(s_v)) * (1.0f / 65535.0f);
+    c->rv = (s_v > 0.0f) ? fminf(1.0f / (c->qv * c->qv), FLT_MAX) : 0.0f;
 }
 
-float orc_inv_scale_v(float s)
+uint16_t orc_encode_m(float m, float rm)
 {
-    if (!(s > 0.0f)) return 0.0f;
-    return 1.0f / sqrtf(s);
-}
-
-uint16_t orc_encode_m(float m, float inv)
-{
-    float a = fabsf(m) * inv;
+    float a = fabsf(m) * rm;
     float y = sqrtf(a);
-    float k = rintf(fminf(y * 32767.0f, 32767.0f));
+    float k = rintf(fminf(y, 32767.0f));
     uint32_t kk = (uint32_t)k;
     return (uint16_t)(signbit(m) ? 32768u - kk : 32768u + kk);
 }
 
-float orc_decode_m(uint16_t c, float s)
+float orc_decode_m(uint16_t c, float qm)
 {
-    float t = (float)((int32_t)c - 32768) * (1.0f / 32767.0f);
-    float p = t * fabsf(t);
-    return p * s;
+    float t = (float)((int32_t)c - 32768) * qm;
+    return t * fabsf(t);
 }
 
 /* sv is sqrt(v); the update needs that root anyway, so the codec reuses it. */
-uint16_t orc_encode_v(float sv, float rs)
+uint16_t orc_encode_v(float sv, float rv)
 {
-    float y = sqrtf(sv * rs);
-    float k = rintf(fminf(y * 65535.0f, 65535.0f));
+    float y = sqrtf(sv * rv);
+    float k = rintf(fminf(y, 65535.0f));
     return (uint16_t)(uint32_t)k;
 }
 
-float orc_decode_v(uint16_t c, float s)
+float orc_decode_v(uint16_t c, float qv)
 {
-    float z = (float)c * (1.0f / 65535.0f);
+    float z = (float)c * qv;
     float z2 = z * z;
-    return (z2 * z2) * s;
+    return z2 * z2;
 }
 
 /* Stand-alone pack: S = max over the buffer (|x| for exp_avg, x for exp_avg_sq), then encode. */
@@ -143,19 +150,18 @@ void orc_state_pack(const float* x, uint16_t* codes, float* scale, int64_t n, in
     }
     float s = f_of(mx);
     *scale = s;
-    if (is_signed) {
-        float inv = orc_inv_scale_m(s);
-        for (int64_t i = 0; i < n; ++i) codes[i] = orc_encode_m(x[i], inv);
-    } else {
-        float rs = orc_inv_scale_v(s);
-        for (int64_t i = 0; i < n; ++i) codes[i] = orc_encode_v(sqrtf(x[i]), rs);
-    }
+    orc_codec_t c;
+    orc_codec_consts(s, s, &c);
+    for (int64_t i = 0; i < n; ++i)
+        codes[i] = is_signed ? orc_encode_m(x[i], c.rm) : orc_encode_v(sqrtf(x[i]), c.rv);
 }
 
 void orc_state_unpack(const uint16_t* codes, float scale, float* x, int64_t n, int32_t is_signed)
 {
+    orc_codec_t c;
+    orc_codec_consts(scale, scale, &c);
     for (int64_t i = 0; i < n; ++i)
-        x[i] = is_signed ? orc_decode_m(codes[i], scale) : orc_decode_v(codes[i], scale);
+        x[i] = is_signed ? orc_decode_m(codes[i], c.qm) : orc_decode_v(codes[i], c.qv);
 }
 
 /* ----------------------------------------------------------------------------------------
@@ -204,7 +210,8 @@ void orc_nadam_scalars(int64_t t, float lr, float beta1, float beta2, float eps,
 typedef struct { float s_m, s_v, a_m, a_v; } orc_scale_t;
 
 /* G = max |g| over the tensor, taken on the bf16 magnitude bits (equal to the float max for
- * every non-NaN input; a NaN magnitude compares above infinity). */
+ * every non-NaN input; a NaN magnitude compares above infinity, so a NaN gradient makes the
+ * tensor's scale NaN and is reported by the non-finite count). */
 float orc_grad_absmax(const uint16_t* g, int64_t n)
 {
     uint32_t mx = 0;
@@ -221,28 +228,43 @@ float orc_grad_absmax(const uint16_t* g, int64_t n)
  *   m, v : uint16 codes if n > 4096, else fp32 (R5)
  *   g  : bf16 gradient bits
  * Order per element (moments first, then decoupled decay, then the update -- the printed
- * Adafactor step decays the weight before subtracting the update):
+ * Adafactor step decays the weight before subtracting the update); fma() is one rounding:
  *   w  = merge(hi, lo);  g = f32(g)
- *   m  = b1 m0 + (1-b1) g;    v = b2 v0 + (1-b2) (g g)
- *   w  = w - (lr wd) w                                  (decoupled decay only)
- *   sv = sqrt(v);  den = sv k2 + eps;  num = c_m m + c_g g
- *   w  = w - lr (num / den);  (hi, lo) = split(w)
+ *   m  = fma(b1, m0, (1-b1) g);   v = fma(b2, v0, (1-b2) (g g))
+ *   w  = fma(-(lr wd), w, w)                            (decoupled decay only)
+ *   sv = sqrt(v);  den = fma(sv, k2, eps);  num = fma(c_m, m, c_g g)
+ *   w  = fma(-lr, num / den, w);  (hi, lo) = split(w)
  * The update uses the fp32 moments just computed; quantisation happens only between steps
  * ("it can only be used for storage rather than operations", PR #2187, third post).
+ * The scale maxima A_m = max |m|, A_v = max v skip NaN (fmax semantics).
  * -------------------------------------------------------------------------------------- */
+static float nadam_elem(float w, float gg, float* mm, float* vv, float* sv,
+                        const orc_nadam_scalars_t* k)
+{
+    *mm = fmaf(k->b1, *mm, k->omb1 * gg);
+    *vv = fmaf(k->b2, *vv, k->omb2 * (gg * gg));
+    if (k->decoupled_wd)
+        w = fmaf(-k->lr_wd, w, w);
+    *sv = sqrtf(*vv);
+    float den = fmaf(*sv, k->k2, k->eps);
+    float num = fmaf(k->c_m, *mm, k->c_g * gg);
+    return fmaf(-k->lr, num / den, w);
+}
+
 void orc_nadam_step_tensor(uint16_t* hi, uint16_t* lo, void* m, void* v, const uint16_t* g,
                            int64_t n, orc_scale_t* sc, const orc_nadam_scalars_t* k)
 {
     int small = n <= ORC_SMALL_NUMEL;
-    float s_m = 0.0f, s_v = 0.0f, inv_m = 0.0f, rs_v = 0.0f;
+    float s_m = 0.0f, s_v = 0.0f;
+    orc_codec_t dec, enc;
     if (!small) {
         float G = orc_grad_absmax(g, n);
-        s_m = k->b1 * sc->a_m + k->omb1 * G;
-        s_v = k->b2 * sc->a_v + k->omb2 * (G * G);
-        inv_m = orc_inv_scale_m(s_m);
-        rs_v = orc_inv_scale_v(s_v);
+        s_m = fmaf(k->b1, sc->a_m, k->omb1 * G);
+        s_v = fmaf(k->b2, sc->a_v, k->omb2 * (G * G));
+        orc_codec_consts(sc->s_m, sc->s_v, &dec);
+        orc_codec_consts(s_m, s_v, &enc);
     }
-    uint32_t am = 0, av = 0;
+    float am = 0.0f, av = 0.0f;
     uint16_t* mc = (uint16_t*)m;
     uint16_t* vc = (uint16_t*)v;
     float* mf = (float*)m;
@@ -250,16 +272,10 @@ void orc_nadam_step_tensor(uint16_t* hi, uint16_t* lo, void* m, void* v, const u
     for (int64_t i = 0; i < n; ++i) {
         float w = lo ? f_of(((uint32_t)hi[i] << 16) | lo[i]) : bf16_to_f32(hi[i]);
         float gg = bf16_to_f32(g[i]);
-        float m0 = small ? mf[i] : orc_decode_m(mc[i], sc->s_m);
-        float v0 = small ? vf[i] : orc_decode_v(vc[i], sc->s_v);
-        float mm = k->b1 * m0 + k->omb1 * gg;
-        float vv = k->b2 * v0 + k->omb2 * (gg * gg);
-        if (k->decoupled_wd)
-            w = w - k->lr_wd * w;
-        float sv = sqrtf(vv);
-        float den = sv * k->k2 + k->eps;
-        float num = k->c_m * mm + k->c_g * gg;
-        w = w - k->lr * (num / den);
+        float mm = small ? mf[i] : orc_decode_m(mc[i], dec.qm);
+        float vv = small ? vf[i] : orc_decode_v(vc[i], dec.qv);
+        float sv;
+        w = nadam_elem(w, gg, &mm, &vv, &sv, k);
         if (lo) {
             uint32_t b = b_of(w);
             hi[i] = (uint16_t)(b >> 16);
@@ -271,18 +287,17 @@ void orc_nadam_step_tensor(uint16_t* hi, uint16_t* lo, void* m, void* v, const u
             mf[i] = mm;
             vf[i] = vv;
         } else {
-            mc[i] = orc_encode_m(mm, inv_m);
-            vc[i] = orc_encode_v(sv, rs_v);
-            uint32_t bm = b_of(mm) & 0x7FFFFFFFu, bv = b_of(vv) & 0x7FFFFFFFu;
-            if (bm > am) am = bm;
-            if (bv > av) av = bv;
+            mc[i] = orc_encode_m(mm, enc.rm);
+            vc[i] = orc_encode_v(sv, enc.rv);
+            am = fmaxf(am, fabsf(mm));
+            av = fmaxf(av, vv);
         }
     }
     if (!small) {
         sc->s_m = s_m;
         sc->s_v = s_v;
-        sc->a_m = f_of(am);
-        sc->a_v = f_of(av);
+        sc->a_m = am;
+        sc->a_v = av;
     }
 }
 
@@ -292,17 +307,8 @@ void orc_nadam_step_fp32(float* w, float* m, float* v, const uint16_t* g, int64_
                          const orc_nadam_scalars_t* k)
 {
     for (int64_t i = 0; i < n; ++i) {
-        float ww = w[i];
-        float gg = bf16_to_f32(g[i]);
-        float mm = k->b1 * m[i] + k->omb1 * gg;
-        float vv = k->b2 * v[i] + k->omb2 * (gg * gg);
-        if (k->decoupled_wd)
-            ww = ww - k->lr_wd * ww;
-        float den = sqrtf(vv) * k->k2 + k->eps;
-        float num = k->c_m * mm + k->c_g * gg;
-        w[i] = ww - k->lr * (num / den);
-        m[i] = mm;
-        v[i] = vv;
+        float sv;
+        w[i] = nadam_elem(w[i], bf16_to_f32(g[i]), &m[i], &v[i], &sv, k);
     }
 }
 

@@ -21,10 +21,11 @@ def test_hand_worked_codes(orc):
     assert len(rows) >= 20
     for kind, s, x, code in rows:
         s, x, code = np.float32(s), np.float32(x), int(code)
+        c = orc.codec_consts(float(s), float(s))
         if kind == "m":
-            got = orc.encode_m(float(x), orc.inv_scale_m(float(s)))
+            got = orc.encode_m(float(x), c.rm)
         else:
-            got = orc.encode_v(float(np.sqrt(np.float32(x))), orc.inv_scale_v(float(s)))
+            got = orc.encode_v(float(np.sqrt(np.float32(x))), c.rv)
         assert got == code, (kind, s, x, got, code)
 
 
@@ -32,14 +33,17 @@ def test_hand_worked_codes(orc):
 def test_roundtrip_every_code(orc, s):
     """encode(decode(c)) == c for all 65535 exp_avg codes and all 65536 exp_avg_sq codes."""
     s = float(np.float32(s))
-    inv, rs = orc.inv_scale_m(s), orc.inv_scale_v(s)
+    k = orc.codec_consts(s, s)
     codes = np.arange(65536, dtype=np.uint16)
     mdec = orc.state_unpack(codes, s, True)
     vdec = orc.state_unpack(codes, s, False)
     for c in range(1, 65536):
-        assert orc.encode_m(float(mdec[c]), inv) == c
+        assert orc.encode_m(float(mdec[c]), k.rm) == c
     for c in range(65536):
-        assert orc.encode_v(float(np.sqrt(vdec[c])), rs) == c
+        assert orc.encode_v(float(np.sqrt(vdec[c])), k.rv) == c
+    # the decoded end points are the scale itself (to a few ulps) and zero
+    assert abs(mdec[65535] - s) <= 4 * np.spacing(np.float32(s)) and mdec[32768] == 0.0
+    assert abs(vdec[65535] - s) <= 8 * np.spacing(np.float32(s)) and vdec[0] == 0.0
 
 
 def test_half_step_bound_and_monotone(orc):
