@@ -158,7 +158,7 @@ __device__ __forceinline__ void step8_f32(const Prm& k, bool has_res, uint4& W, 
     step2_f32(k, has_res, W.w, R.w, G.w, M[1].z, M[1].w, V[1].z, V[1].w, nf);
 }
 
-__global__ void __launch_bounds__(kThreads) k_nadam_step(NadamLaunch L, Prm k, int parity) {
+__global__ void __launch_bounds__(kThreads, 4) k_nadam_step(NadamLaunch L, Prm k, int parity) {
     __shared__ uint32_t red[3 * 32];
     const Chunk c = L.chunks[blockIdx.x];
     const TensorRec t = L.tensors[c.tensor];

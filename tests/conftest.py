@@ -11,6 +11,7 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: CPU test that takes tens of seconds")
+    config.addinivalue_line("markers", "full: GPU parity at full workload size (tens of GB, about a minute each)")
 
 
 @pytest.fixture(scope="session")
