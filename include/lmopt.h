@@ -114,15 +114,14 @@ int optim_group_destroy(optim_group_t* group);
  * rebuild the fp32 master from (w_bf16, res_u16), decode m and v, update the moments, apply
  * decoupled decay and the bias-corrected (Nesterov) update, split the master back into
  * (w_bf16, res_u16), re-encode m and v, and reduce the per-tensor maxima that bound the next
- * step's scales.  A gradient-max pass per u16 tensor (needed for the encoder's scale) runs in the
- * same persistent kernel, overlapped with the updates of the previous tensor.
+ * step's scales.  Before it, a pre-pass reduces max|g| per u16 tensor.
  * ("Kahan summation for Adafactor-optimized Flux FFT", sd-scripts PR #2159, first comment:
  * the 16 clipped low bits restore the bit-identical f32; PR #2187, second post: scaled,
  * biased, pow()-companded uint16 moments.)
  *   grads_bf16 : host array of n device pointers, one bf16 gradient per tensor, same order as at
  *                create (may change from call to call; unchanged pointers cost no upload)
  *   step       : 1 on the first call, then previous + 1; anything else is OPTIM_EINVAL
- * One enqueued kernel. */
+ * Two enqueued kernels (one if every tensor has 4096 or fewer elements). */
 int optim_step_nadam_kahan(optim_group_t* group, const void* const* grads_bf16, int64_t step,
                            const optim_nadam_hparams_t* hp, void* stream);
 
@@ -183,10 +182,6 @@ int optim_group_attach_offload(optim_group_t* group, optim_offload_t* engine);
 int optim_offload_prefetch(optim_group_t* group);
 /* Bounded wait for every enqueued copy; returns the bytes copied in each direction so far. */
 int optim_offload_sync(optim_offload_t* engine, uint64_t* bytes_h2d, uint64_t* bytes_d2h);
-
-/* OPTIM_OK, or OPTIM_ETIMEOUT if a bounded in-kernel wait of any step of this group so far gave
- * up (the group's states are then not valid).  Synchronises the group's last stream. */
-int optim_group_status(optim_group_t* group);
 
 /* Profiling hook: when `event` (a cudaEvent_t passed as void*) is not NULL, the next step calls
  * of this group record it on their stream between the pre-pass (gradient max, or the factored

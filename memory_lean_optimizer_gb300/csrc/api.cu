@@ -78,8 +78,7 @@ static void group_free(optim_group* g) {
     cudaFree(g->d_tensors);
     cudaFree(g->d_grads);
     cudaFree(g->d_scales);
-    cudaFree(g->d_tasks);
-    cudaFree(g->d_sync);
+    cudaFree(g->d_chunks);
     cudaFree(g->d_nonfinite);
     factored_plan_free(g->fplan);
     delete g;
@@ -186,6 +185,7 @@ int optim_group_create(const optim_tensor_desc_t* tensors, int32_t n, int32_t ki
     int rc = check_cuda(cudaGetDevice(&g->device), "cudaGetDevice");
     if (!rc) {
         std::vector<TensorRec> recs(n);
+        std::vector<Chunk> chunks;
         for (int32_t i = 0; i < n; ++i) {
             const optim_tensor_desc_t& d = tensors[i];
             TensorRec& r = recs[i];
@@ -195,20 +195,23 @@ int optim_group_create(const optim_tensor_desc_t* tensors, int32_t n, int32_t ki
             r.v = d.v;
             r.numel = d.numel;
             r.flags = (d.numel <= kSmall ? kFlagSmall : 0) | (d.res_u16 ? kFlagRes : 0);
-            r.n_max_tasks = 0;
+            r.pad = 0;
         }
-        std::vector<Task> tasks;
         if (kind == OPTIM_KIND_NADAM) {
-            tasks = build_nadam_tasks(recs);
-            if (tasks.size() > (size_t)INT32_MAX) rc = set_error(OPTIM_EINVAL, "group too large");
-            g->n_tasks = (int32_t)tasks.size();
+            for (int pass = 0; pass < 2; ++pass) {   // u16-state tensors first, then fp32-state
+                for (int32_t i = 0; i < n; ++i) {
+                    const int64_t ne = tensors[i].numel;
+                    if (ne == 0 || (pass == 0) != (ne > kSmall)) continue;
+                    const int64_t nc = (ne + kChunk - 1) / kChunk;
+                    for (int64_t c = 0; c < nc; ++c) chunks.push_back(Chunk{i, (int32_t)c});
+                }
+                if (pass == 0) g->n_chunks_large = (int32_t)chunks.size();
+            }
+            if (chunks.size() > (size_t)INT32_MAX) rc = set_error(OPTIM_EINVAL, "group too large");
+            g->n_chunks_total = (int32_t)chunks.size();
         }
-        g->h_recs = recs;
         if (!rc) rc = dev_upload(&g->d_tensors, recs, "tensor table");
-        if (!rc) rc = dev_upload(&g->d_tasks, tasks, "task table");
-        if (!rc)
-            rc = dev_upload(&g->d_sync, std::vector<unsigned>(sizeof(NadamSync) / sizeof(unsigned) + 2 * (size_t)n, 0u),
-                            "synchronisation words");
+        if (!rc) rc = dev_upload(&g->d_chunks, chunks, "chunk table");
         if (!rc) rc = dev_upload(&g->d_scales, std::vector<ScaleRec>(n, ScaleRec{}), "scale table");
         if (!rc) rc = dev_upload(&g->d_nonfinite, std::vector<unsigned long long>(1, 0ull), "counter");
         if (!rc) rc = dev_upload(&g->d_grads, std::vector<const uint16_t*>(n, nullptr), "gradient table");
@@ -287,7 +290,8 @@ int optim_step_nadam_kahan(optim_group_t* g, const void* const* grads, int64_t s
         rc = offload_step_begin(g, s, &table);
         if (rc) return rc;
     }
-    NadamLaunch L{table, g->d_grads, g->d_scales, g->d_tasks, g->d_sync, g->d_nonfinite, g->n, g->n_tasks};
+    NadamLaunch L{table, g->d_grads, g->d_scales, g->d_chunks, g->d_nonfinite,
+                  g->n_chunks_large, g->n_chunks_total};
     rc = launch_nadam_step(L, k, s, g->profile_ev);
     if (rc) return rc;
     g->last_step = step;
@@ -420,18 +424,6 @@ int optim_query_nonfinite(optim_group_t* g, uint64_t* count) {
     unsigned long long c = 0;
     rc = check_cuda(cudaMemcpy(&c, g->d_nonfinite, sizeof c, cudaMemcpyDeviceToHost), "counter download");
     *count = c;
-    return rc;
-}
-
-int optim_group_status(optim_group_t* g) {
-    if (!g) return set_error(OPTIM_EINVAL, "group is NULL");
-    int rc = check_device(g);
-    if (!rc) rc = sync_group(g);
-    if (rc || !g->d_sync) return rc;
-    NadamSync h{};
-    rc = check_cuda(cudaMemcpy(&h, g->d_sync, sizeof h, cudaMemcpyDeviceToHost), "status download");
-    if (!rc && (h.error & 1u))
-        return set_error(OPTIM_ETIMEOUT, "a step's bounded in-kernel wait gave up; its results are not valid");
     return rc;
 }
 

@@ -31,7 +31,7 @@ struct TensorRec {
     void* v;
     int64_t numel;
     int32_t flags;
-    int32_t n_max_tasks;   // gradient-max tasks of this tensor (its update tasks wait for all of them)
+    int32_t pad;
 };
 
 // Per-tensor scale record of the u16 codec, double-buffered by step parity p:
@@ -53,17 +53,6 @@ static_assert(sizeof(ScaleRec) == 64, "ScaleRec layout");
 struct Chunk {
     int32_t tensor;
     int32_t index;
-};
-
-// One task of the fused NAdam kernel's queue: gradient max over chunks [chunk0, chunk0+nchunks)
-// of a tensor (kTaskMax), or the update of one chunk (kTaskStep).
-constexpr int32_t kTaskMax = 0;
-constexpr int32_t kTaskStep = 1;
-struct Task {
-    int32_t tensor;
-    int32_t kind;
-    int32_t chunk0;
-    int32_t nchunks;
 };
 
 __device__ __forceinline__ float bf16_to_f32(uint32_t h) { return __uint_as_float(h << 16); }

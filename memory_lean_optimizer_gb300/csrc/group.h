@@ -22,11 +22,10 @@ struct optim_group {
     lmo::TensorRec* d_tensors = nullptr;
     const uint16_t** d_grads = nullptr;
     lmo::ScaleRec* d_scales = nullptr;
-    lmo::Task* d_tasks = nullptr;          // NADAM task queue (fixed order, built at create)
-    unsigned* d_sync = nullptr;            // queue heads, error word, completion counters
+    lmo::Chunk* d_chunks = nullptr;
     unsigned long long* d_nonfinite = nullptr;
-    int32_t n_tasks = 0;
-    std::vector<lmo::TensorRec> h_recs;    // host copy of the tensor table
+    int32_t n_chunks_large = 0;
+    int32_t n_chunks_total = 0;
     lmo::FactoredPlan* fplan = nullptr;
     // gradient pointers: host copy of the last upload, two pinned staging slots
     std::vector<const void*> cur_grads;

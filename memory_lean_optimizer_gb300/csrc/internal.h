@@ -36,29 +36,15 @@ struct NadamScalars {
     int32_t parity;
 };
 
-// Device synchronisation words of a NADAM group: task-queue heads and per-tensor completion
-// counters of the gradient-max tasks, both double-buffered by step parity, and an error word.
-struct NadamSync {
-    unsigned queue[2];
-    unsigned error;      // bit 0: a bounded wait gave up (the step's results are not valid)
-    unsigned pad;
-    // followed by done[2][n_tensors]
-};
-
 struct NadamLaunch {
     const TensorRec* tensors;
     const uint16_t* const* grads;
     ScaleRec* scales;
-    const Task* tasks;
-    unsigned* sync;                // NadamSync header + done counters
+    const Chunk* chunks;
     unsigned long long* nonfinite;
-    int32_t n_tensors;
-    int32_t n_tasks;
+    int32_t n_chunks_large;   // chunks of u16-state tensors come first
+    int32_t n_chunks_total;
 };
-// Task order of a group: max tasks of the first u16-state tensor, update tasks of the fp32-state
-// tensors, then for each u16-state tensor i: max tasks of tensor i+1 followed by the update
-// tasks of tensor i.  n_max_tasks of each record is filled in.
-std::vector<Task> build_nadam_tasks(std::vector<TensorRec>& recs);
 int launch_nadam_step(const NadamLaunch& L, const NadamScalars& k, cudaStream_t s, cudaEvent_t mid);
 
 }  // namespace lmo

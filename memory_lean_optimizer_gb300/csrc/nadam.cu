@@ -1,13 +1,11 @@
 // nadam.cu -- multi-tensor fused NAdam(W)/Adam step with Kahan residual and u16 moments.
 //
-// One persistent kernel per group call (k_nadam_fused), whose CTAs take tasks from a queue:
-//  max tasks  : G = max|g| per u16-state tensor (the bound the encoder's scale needs before the
-//               step's moments exist); the first also clears the slots the step accumulates into.
-//  step tasks : per element, in one pass: merge (w_bf16, res) -> fp32 master, decode m, v,
-//               moment EMAs, decoupled decay, bias-corrected (Nesterov) update, split,
-//               re-encode, and the per-tensor maxima that bound the next step's scales.
-// The max tasks of tensor i+1 are queued before the step tasks of tensor i, so the gradient
-// pre-pass overlaps the (ALU-heavy) updates and the gradient is re-read from L2 where it fits.
+// Two kernels per group call, each one CTA per chunk of the group's chunk table:
+//  K1 k_grad_absmax : G = max|g| per u16-state tensor (the bound the encoder's scale needs before
+//                     the step's moments exist); also clears the slots the step will accumulate.
+//  K2 k_nadam_step  : per element, in one pass: merge (w_bf16, res) -> fp32 master, decode m, v,
+//                     moment EMAs, decoupled decay, bias-corrected (Nesterov) update, split,
+//                     re-encode, and the per-tensor maxima that bound the next step's scales.
 // Sources: "Kahan summation for Adafactor-optimized Flux FFT" (sd-scripts PR #2159, first
 // comment: the 16 clipped low bits restore the bit-identical f32); "Amazing Flux FFT quality on
 // a 5090" (sd-scripts PR #2187: NAdam(W) first post, u16 scaled/biased/pow()-companded moments
@@ -24,8 +22,6 @@
 // Memory: 18 bytes per u16-state element per step (read w, res, g, m, v; write w, res, m, v),
 // 26 bytes per fp32-state element, plus 2 bytes of K1's gradient read.  All accesses are
 // 128-bit and coalesced when a tensor's buffers are 16-byte aligned.
-#include <algorithm>
-
 #include "internal.h"
 
 namespace lmo {
@@ -35,6 +31,53 @@ struct Prm {
     float lr, b1, omb1, b2, omb2, eps, lr_wd, c_m, c_g, k2;
     int32_t decoupled;
 };
+
+// ------------------------------------------------------------------------------------ K1
+__global__ void __launch_bounds__(kThreads) k_grad_absmax(NadamLaunch L, int parity) {
+    __shared__ uint32_t red[32];
+    const Chunk c = L.chunks[blockIdx.x];
+    const int64_t numel = L.tensors[c.tensor].numel;
+    const uint16_t* __restrict__ g = L.grads[c.tensor];
+    ScaleRec* sr = L.scales + c.tensor;
+    const int p = parity, q = parity ^ 1;
+    if (c.index == 0 && threadIdx.x == 0) {
+        sr->a_m[p] = 0u;   // this step's maxima accumulate here
+        sr->a_v[p] = 0u;
+        sr->g[q] = 0u;     // next step's gradient max accumulates here
+    }
+    const int64_t start = (int64_t)c.index * kChunk;
+    const int64_t end = min(numel, start + kChunk);
+    uint32_t mx = 0u;
+    int64_t done = start;
+    if (aligned16(g)) {
+        const int64_t nv = (end - start) >> 3;
+        const uint4* gv = reinterpret_cast<const uint4*>(g + start);
+        int64_t i = threadIdx.x;
+        for (; i + 3 * kThreads < nv; i += 4 * kThreads) {
+            uint4 x0 = __ldcg(gv + i), x1 = __ldcg(gv + i + kThreads);
+            uint4 x2 = __ldcg(gv + i + 2 * kThreads), x3 = __ldcg(gv + i + 3 * kThreads);
+            mx = __vmaxu2(mx, __vmaxu2(x0.x & 0x7FFF7FFFu, x0.y & 0x7FFF7FFFu));
+            mx = __vmaxu2(mx, __vmaxu2(x0.z & 0x7FFF7FFFu, x0.w & 0x7FFF7FFFu));
+            mx = __vmaxu2(mx, __vmaxu2(x1.x & 0x7FFF7FFFu, x1.y & 0x7FFF7FFFu));
+            mx = __vmaxu2(mx, __vmaxu2(x1.z & 0x7FFF7FFFu, x1.w & 0x7FFF7FFFu));
+            mx = __vmaxu2(mx, __vmaxu2(x2.x & 0x7FFF7FFFu, x2.y & 0x7FFF7FFFu));
+            mx = __vmaxu2(mx, __vmaxu2(x2.z & 0x7FFF7FFFu, x2.w & 0x7FFF7FFFu));
+            mx = __vmaxu2(mx, __vmaxu2(x3.x & 0x7FFF7FFFu, x3.y & 0x7FFF7FFFu));
+            mx = __vmaxu2(mx, __vmaxu2(x3.z & 0x7FFF7FFFu, x3.w & 0x7FFF7FFFu));
+        }
+        for (; i < nv; i += kThreads) {
+            uint4 x = __ldcg(gv + i);
+            mx = __vmaxu2(mx, __vmaxu2(x.x & 0x7FFF7FFFu, x.y & 0x7FFF7FFFu));
+            mx = __vmaxu2(mx, __vmaxu2(x.z & 0x7FFF7FFFu, x.w & 0x7FFF7FFFu));
+        }
+        mx = max(mx & 0xFFFFu, mx >> 16);
+        done = start + (nv << 3);
+    }
+    for (int64_t i = done + threadIdx.x; i < end; i += kThreads) mx = max(mx, (uint32_t)(g[i] & 0x7FFFu));
+    uint32_t v[1] = {mx};
+    block_max_u32<1>(v, red);
+    if (threadIdx.x == 0 && v[0] != 0u) atomicMax(&sr->g[p], v[0] << 16);
+}
 
 // ------------------------------------------------------------------------------------ K2
 // One element: w, g fp32; m, v in: decoded (or fp32) moments, out: new moments; sv = sqrt(v).
@@ -115,115 +158,27 @@ __device__ __forceinline__ void step8_f32(const Prm& k, bool has_res, uint4& W, 
     step2_f32(k, has_res, W.w, R.w, G.w, M[1].z, M[1].w, V[1].z, V[1].w, nf);
 }
 
-constexpr int kMaxChunksPerTask = 4;           // chunks per gradient-max task
-constexpr unsigned kSpinLimit = 1u << 24;         // bounded wait: ~2 s of 128 ns naps
-
-__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ uint64_t policy_evict_last() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-// Gradient load that asks L2 to keep the line: the update task re-reads it shortly after.
-__device__ __forceinline__ uint4 ld_keep(const uint4* p, uint64_t pol) {
-    uint4 v;
-    asm volatile("ld.global.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p), "l"(pol));
-    return v;
-}
-
-// Gradient-max task: G[p] = max |g| over the task's chunks; the first task of a tensor also
-// clears the slots this step accumulates into.  Publishes completion on done[p][tensor].
-__device__ void task_max(const NadamLaunch& L, const Task& tk, int p, unsigned* done_p, unsigned* done_q,
-                         uint64_t pol, uint32_t* red) {
-    const int q = p ^ 1;
-    const int64_t numel = L.tensors[tk.tensor].numel;
-    const uint16_t* __restrict__ g = L.grads[tk.tensor];
-    ScaleRec* sr = L.scales + tk.tensor;
-    const int64_t start = (int64_t)tk.chunk0 * kChunk;
-    const int64_t end = min(numel, (int64_t)(tk.chunk0 + tk.nchunks) * kChunk);
-    uint32_t mx = 0u;
-    int64_t done = start;
-    if (aligned16(g)) {
-        const int64_t nv = (end - start) >> 3;
-        const uint4* gv = reinterpret_cast<const uint4*>(g + start);
-        int64_t i = threadIdx.x;
-        for (; i + 3 * kThreads < nv; i += 4 * kThreads) {
-            uint4 x0 = ld_keep(gv + i, pol), x1 = ld_keep(gv + i + kThreads, pol);
-            uint4 x2 = ld_keep(gv + i + 2 * kThreads, pol), x3 = ld_keep(gv + i + 3 * kThreads, pol);
-            mx = __vmaxu2(mx, __vmaxu2(x0.x & 0x7FFF7FFFu, x0.y & 0x7FFF7FFFu));
-            mx = __vmaxu2(mx, __vmaxu2(x0.z & 0x7FFF7FFFu, x0.w & 0x7FFF7FFFu));
-            mx = __vmaxu2(mx, __vmaxu2(x1.x & 0x7FFF7FFFu, x1.y & 0x7FFF7FFFu));
-            mx = __vmaxu2(mx, __vmaxu2(x1.z & 0x7FFF7FFFu, x1.w & 0x7FFF7FFFu));
-            mx = __vmaxu2(mx, __vmaxu2(x2.x & 0x7FFF7FFFu, x2.y & 0x7FFF7FFFu));
-            mx = __vmaxu2(mx, __vmaxu2(x2.z & 0x7FFF7FFFu, x2.w & 0x7FFF7FFFu));
-            mx = __vmaxu2(mx, __vmaxu2(x3.x & 0x7FFF7FFFu, x3.y & 0x7FFF7FFFu));
-            mx = __vmaxu2(mx, __vmaxu2(x3.z & 0x7FFF7FFFu, x3.w & 0x7FFF7FFFu));
-        }
-        for (; i < nv; i += kThreads) {
-            uint4 x = ld_keep(gv + i, pol);
-            mx = __vmaxu2(mx, __vmaxu2(x.x & 0x7FFF7FFFu, x.y & 0x7FFF7FFFu));
-            mx = __vmaxu2(mx, __vmaxu2(x.z & 0x7FFF7FFFu, x.w & 0x7FFF7FFFu));
-        }
-        mx = max(mx & 0xFFFFu, mx >> 16);
-        done = start + (nv << 3);
-    }
-    for (int64_t i = done + threadIdx.x; i < end; i += kThreads) mx = max(mx, (uint32_t)(g[i] & 0x7FFFu));
-    uint32_t v[1] = {mx};
-    block_max_u32<1>(v, red);
-    if (threadIdx.x == 0) {
-        if (tk.chunk0 == 0) {
-            sr->a_m[p] = 0u;        // this step's moment maxima accumulate here
-            sr->a_v[p] = 0u;
-            sr->g[q] = 0u;          // next step's gradient maximum accumulates here
-            done_q[tk.tensor] = 0u; // next step's completion counter
-        }
-        if (v[0]) atomicMax(&sr->g[p], v[0] << 16);
-        __threadfence();
-        atomicAdd(&done_p[tk.tensor], 1u);
-    }
-}
-
-// Update task: one chunk of one tensor (see the operation order at the top of this file).
-__device__ void task_step(const NadamLaunch& L, const Prm& k, const Task& tk, int p, const unsigned* done_p,
-                          unsigned* error, uint32_t* red, int* ok) {
-    const int q = p ^ 1;
-    const TensorRec t = L.tensors[tk.tensor];
-    const uint16_t* __restrict__ g = L.grads[tk.tensor];
+__global__ void __launch_bounds__(kThreads, 4) k_nadam_step(NadamLaunch L, Prm k, int parity) {
+    __shared__ uint32_t red[3 * 32];
+    const Chunk c = L.chunks[blockIdx.x];
+    const TensorRec t = L.tensors[c.tensor];
+    const uint16_t* __restrict__ g = L.grads[c.tensor];
+    const int p = parity, q = parity ^ 1;
     const bool small = (t.flags & kFlagSmall) != 0;
     const bool has_res = (t.flags & kFlagRes) != 0;
-    const int64_t start = (int64_t)tk.chunk0 * kChunk;
+    const int64_t start = (int64_t)c.index * kChunk;
     const int64_t end = min(t.numel, start + kChunk);
 
     Codec cd{};
-    ScaleRec* sr = L.scales + tk.tensor;
+    ScaleRec* sr = L.scales + c.tensor;
     if (!small) {
-        // wait (bounded) until every gradient-max task of this tensor has published
-        if (threadIdx.x == 0) {
-            unsigned spins = 0;
-            *ok = 1;
-            while (ld_acquire(done_p + tk.tensor) < (unsigned)t.n_max_tasks) {
-                if (++spins > kSpinLimit) {
-                    atomicOr(error, 1u);
-                    *ok = 0;
-                    break;
-                }
-                __nanosleep(128);
-            }
-        }
-        __syncthreads();
-        if (!*ok) return;
-        const float a_m = __uint_as_float(__ldcg(&sr->a_m[q])), a_v = __uint_as_float(__ldcg(&sr->a_v[q]));
-        const float G = __uint_as_float(__ldcg(&sr->g[p]));
+        const float a_m = __uint_as_float(sr->a_m[q]), a_v = __uint_as_float(sr->a_v[q]);
+        const float G = __uint_as_float(sr->g[p]);
         const float s_m = __fmaf_rn(k.b1, a_m, __fmul_rn(k.omb1, G));
         const float s_v = __fmaf_rn(k.b2, a_v, __fmul_rn(k.omb2, __fmul_rn(G, G)));
-        cd.dec = codec_consts(__ldcg(&sr->s_m[q]), __ldcg(&sr->s_v[q]));
+        cd.dec = codec_consts(sr->s_m[q], sr->s_v[q]);
         cd.enc = codec_consts(s_m, s_v);
-        if (tk.chunk0 == 0 && threadIdx.x == 0) {
+        if (c.index == 0 && threadIdx.x == 0) {
             sr->s_m[p] = s_m;
             sr->s_v[p] = s_v;
         }
@@ -335,89 +290,24 @@ __device__ void task_step(const NadamLaunch& L, const Prm& k, const Task& tk, in
     }
 }
 
-// Persistent kernel: CTAs take tasks from the group's queue in list order until it runs dry.
-// Because a tensor's gradient-max tasks precede its update tasks in the list and never wait,
-// every wait ends (no residency assumption is needed).
-__global__ void __launch_bounds__(kThreads, 4) k_nadam_fused(NadamLaunch L, Prm k, int parity) {
-    __shared__ uint32_t red[3 * 32];
-    __shared__ int s_task[2];
-    __shared__ int s_ok;
-    NadamSync* hdr = reinterpret_cast<NadamSync*>(L.sync);
-    unsigned* done_base = L.sync + sizeof(NadamSync) / sizeof(unsigned);
-    unsigned* done_p = done_base + (size_t)parity * L.n_tensors;
-    unsigned* done_q = done_base + (size_t)(parity ^ 1) * L.n_tensors;
-    const uint64_t pol = policy_evict_last();
-    if (threadIdx.x == 0) {
-        if (blockIdx.x == 0) hdr->queue[parity ^ 1] = 0u;   // the next step's queue head
-        s_task[0] = (int)atomicAdd(&hdr->queue[parity], 1u);
-    }
-    __syncthreads();
-    int cur = 0;
-    for (;;) {
-        const int ti = s_task[cur];
-        if (ti >= L.n_tasks) break;
-        if (threadIdx.x == 0) s_task[cur ^ 1] = (int)atomicAdd(&hdr->queue[parity], 1u);
-        const Task tk = L.tasks[ti];
-        if (tk.kind == kTaskMax) task_max(L, tk, parity, done_p, done_q, pol, red);
-        else task_step(L, k, tk, parity, done_p, &hdr->error, red, &s_ok);
-        __syncthreads();
-        cur ^= 1;
-    }
-}
-
 }  // namespace
 
 int launch_nadam_step(const NadamLaunch& L, const NadamScalars& s, cudaStream_t stream, cudaEvent_t mid) {
     Prm k{s.lr, s.b1, s.omb1, s.b2, s.omb2, s.eps, s.lr_wd, s.c_m, s.c_g, s.k2, s.decoupled};
+    if (L.n_chunks_large > 0) {
+        k_grad_absmax<<<L.n_chunks_large, kThreads, 0, stream>>>(L, s.parity);
+        int rc = check_cuda(cudaGetLastError(), "grad absmax launch");
+        if (rc) return rc;
+    }
     if (mid) {
         int rc = check_cuda(cudaEventRecord(mid, stream), "profile event");
         if (rc) return rc;
     }
-    if (L.n_tasks == 0) return OPTIM_OK;
-    static int per_sm[256] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 256) dev = 0;
-    if (per_sm[dev] == 0) {
-        int nb = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, k_nadam_fused, kThreads, 0) != cudaSuccess || nb < 1) {
-            cudaGetLastError();
-            nb = 1;
-        }
-        per_sm[dev] = nb;
+    if (L.n_chunks_total > 0) {
+        k_nadam_step<<<L.n_chunks_total, kThreads, 0, stream>>>(L, k, s.parity);
+        return check_cuda(cudaGetLastError(), "nadam step launch");
     }
-    const int64_t cap = (int64_t)per_sm[dev] * sm_count();
-    const unsigned grid = (unsigned)(L.n_tasks < cap ? L.n_tasks : cap);
-    k_nadam_fused<<<grid, kThreads, 0, stream>>>(L, k, s.parity);
-    return check_cuda(cudaGetLastError(), "fused nadam launch");
-}
-
-std::vector<Task> build_nadam_tasks(std::vector<TensorRec>& recs) {
-    std::vector<int32_t> large, small;
-    for (int32_t i = 0; i < (int32_t)recs.size(); ++i) {
-        recs[i].n_max_tasks = 0;
-        if (recs[i].numel == 0) continue;
-        (recs[i].numel > kSmall ? large : small).push_back(i);
-    }
-    std::vector<Task> tasks;
-    auto add_max = [&](int32_t i) {
-        const int32_t nc = (int32_t)((recs[i].numel + kChunk - 1) / kChunk);
-        for (int32_t c = 0; c < nc; c += kMaxChunksPerTask) {
-            tasks.push_back(Task{i, kTaskMax, c, std::min<int32_t>(kMaxChunksPerTask, nc - c)});
-            recs[i].n_max_tasks++;
-        }
-    };
-    auto add_steps = [&](int32_t i) {
-        const int32_t nc = (int32_t)((recs[i].numel + kChunk - 1) / kChunk);
-        for (int32_t c = 0; c < nc; ++c) tasks.push_back(Task{i, kTaskStep, c, 1});
-    };
-    if (!large.empty()) add_max(large[0]);
-    for (int32_t i : small) add_steps(i);
-    for (size_t j = 0; j < large.size(); ++j) {
-        if (j + 1 < large.size()) add_max(large[j + 1]);
-        add_steps(large[j]);
-    }
-    return tasks;
+    return OPTIM_OK;
 }
 
 }  // namespace lmo

@@ -9,7 +9,7 @@
 // copy-out of group k-1 overlap the update kernels of group k:
 //
 //   prefetch(g):  h2d  waits slot.d2h_done   -> H2D copies -> record slot.h2d_done
-//   step(g):      comp waits slot.h2d_done   -> fused step kernel on the slot's tensor table
+//   step(g):      comp waits slot.h2d_done   -> K1, K2 on the slot's tensor table
 //                                            -> record slot.comp_done
 //                 d2h  waits slot.comp_done  -> D2H copies -> record slot.d2h_done
 //
@@ -246,7 +246,7 @@ int optim_group_attach_offload(optim_group_t* g, optim_offload_t* e) {
             r.v = e->slots[s].base + b->off_v[i];
             r.numel = d.numel;
             r.flags = (d.numel <= kSmall ? kFlagSmall : 0) | (d.res_u16 ? kFlagRes : 0);
-            r.n_max_tasks = g->h_recs[i].n_max_tasks;
+            r.pad = 0;
         }
     }
     int rc = OPTIM_OK;

@@ -35,7 +35,7 @@ EXPORTED = (
     "optim_query_scales", "optim_set_scales", "optim_group_get_step", "optim_group_set_step",
     "optim_query_nonfinite", "optim_group_set_profile_event", "optim_last_error",
     "optim_offload_create", "optim_offload_destroy", "optim_group_attach_offload",
-    "optim_offload_prefetch", "optim_offload_sync", "optim_group_status",
+    "optim_offload_prefetch", "optim_offload_sync",
 )
 
 
@@ -93,7 +93,6 @@ def load(path: str = LIB_PATH):
             "optim_group_set_step": [P, I64, ctypes.c_double],
             "optim_query_nonfinite": [P, ctypes.POINTER(ctypes.c_uint64)],
             "optim_group_set_profile_event": [P, P],
-            "optim_group_status": [P],
             "optim_offload_create": [ctypes.c_size_t, I32, ctypes.POINTER(P)],
             "optim_offload_destroy": [P],
             "optim_group_attach_offload": [P, P],
@@ -185,11 +184,6 @@ def optim_group_get_step(handle: int):
 
 def optim_group_set_step(handle: int, step: int, mu_product: float) -> None:
     check(load().optim_group_set_step(handle, step, mu_product))
-
-
-def optim_group_status(handle: int) -> None:
-    """Raises LmoptError(ETIMEOUT) if a bounded in-kernel wait of any step so far gave up."""
-    check(load().optim_group_status(handle))
 
 
 def optim_group_set_profile_event(handle: int, event: int | None) -> None:
