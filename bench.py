@@ -34,6 +34,7 @@ sys.path.insert(0, ROOT)
 METRIC = "params updated/s and achieved HBM GB/s (% of GB300 roofline) per optimizer step"
 BYTES_PER_PARAM_U16 = 18      # read w, res, g, m, v; write w, res, m, v (2 bytes each)
 BYTES_PER_PARAM_F32 = 26      # fp32 moments: m, v 4 bytes each way
+BYTES_PER_PARAM_F24 = 22      # f24 moments: m, v 3 bytes each way
 PREPASS_BYTES_PER_PARAM = 2   # gradient-max pre-pass re-reads g
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["memory_lean_optimizer_gb300/csrc/nadam.cu", "memory_lean_optimizer_gb300/csrc/common.cuh"]
@@ -46,6 +47,9 @@ def parse():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="flux19")
+    p.add_argument("--states", default="u16", choices=["u16", "f24"], help="moment storage of NAdam workloads")
+    p.add_argument("--rounding", default="kahan", choices=["kahan", "sr"],
+                   help="kahan: bf16 weight + u16 residual; sr: no residual, stochastic rounding")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
@@ -146,7 +150,7 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- workload setup
-def build_groups(cfg, device, rank):
+def build_groups(cfg, device, rank, states="u16", rounding="kahan"):
     import torch
     from memory_lean_optimizer_gb300 import engine, workloads as W
     groups, grads, params = [], [], 0
@@ -159,19 +163,23 @@ def build_groups(cfg, device, rank):
                                   zero_frac=cfg["zero_frac"]))
             params += W.numel(s)
             tid += 1
-        groups.append(engine.NadamGroup.from_masters(masters))
+        if rounding == "sr":
+            groups.append(engine.NadamGroup([x.to(torch.bfloat16) for x in masters], kahan=False, states=states))
+        else:
+            groups.append(engine.NadamGroup.from_masters(masters, states=states))
         del masters
         grads.append(gs)
     torch.cuda.synchronize()
     return groups, grads, params
 
 
-def bytes_alg(shapes):
+def bytes_alg(shapes, states="u16", rounding="kahan"):
     from memory_lean_optimizer_gb300 import workloads as W
     tot = 0
     for s in shapes:
         n = W.numel(s)
-        tot += n * (BYTES_PER_PARAM_F32 if n <= 4096 else BYTES_PER_PARAM_U16)
+        per = BYTES_PER_PARAM_F32 if n <= 4096 else (BYTES_PER_PARAM_F24 if states == "f24" else BYTES_PER_PARAM_U16)
+        tot += n * (per - (4 if rounding == "sr" else 0))     # no residual read or written
     return tot
 
 
@@ -268,8 +276,8 @@ def run_ours(args, cfg):
     build.build()
     lmopt.load()
 
-    groups, grads, params = build_groups(cfg, device, rank)
-    hp = cfg["hp"]
+    groups, grads, params = build_groups(cfg, device, rank, args.states, args.rounding)
+    hp = dict(cfg["hp"], stochastic_rounding=int(args.rounding == "sr"), seed=12345)
     stream = torch.cuda.current_stream()
 
     def one_step(events=None):
@@ -287,7 +295,8 @@ def run_ours(args, cfg):
         one_step()
     torch.cuda.synchronize()
 
-    launches_per_step = sum(2 if any(W_numel(s) > 4096 for s in shapes) else 1 for shapes in cfg["groups"])
+    launches_per_step = sum(2 if (args.states == "u16" and any(W_numel(s) > 4096 for s in shapes)) else 1
+                            for shapes in cfg["groups"])
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
             torch.cuda.Event(enable_timing=True)) for _ in groups] for _ in range(args.steps)]
     for per_step in ev:               # materialise the event handles the library records into
@@ -321,7 +330,7 @@ def run_ours(args, cfg):
             e0, em, e1 = ev[k][gi]
             k1_ms.append(e0.elapsed_time(em))
             k2_ms.append(em.elapsed_time(e1))
-    group_bytes = [bytes_alg(shapes) for shapes in cfg["groups"]]
+    group_bytes = [bytes_alg(shapes, args.states, args.rounding) for shapes in cfg["groups"]]
     group_params = [sum(W_numel(s) for s in shapes) for shapes in cfg["groups"]]
     k2_bytes_total = sum(group_bytes) * args.steps
     k2_time_total = sum(k2_ms) / 1e3
@@ -337,15 +346,20 @@ def run_ours(args, cfg):
         "warmup": args.warmup, "ms_per_step": 1e3 * step_s, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, "params_per_gpu": params, "groups": len(groups),
-                   "tensors": sum(len(s) for s in cfg["groups"]), "optimizer": "NAdamW+Kahan, u16 moments",
+                   "tensors": sum(len(s) for s in cfg["groups"]), "optimizer": f"NAdamW+{'Kahan' if args.rounding == 'kahan' else 'stochastic rounding'}, {args.states} moments",
                    "lr": hp["lr"], "weight_decay": hp["weight_decay"], "grads": "one resident set reused each step",
                    "l2": "inputs ~32 GB per GPU, far above the 129 MB L2: no flush needed",
                    "parallelism": f"replicas x{world}"},
         "hbm_gbs_step": sum(group_bytes) / step_s / 1e9,
-        "hbm_gbs_step_as_run": (sum(group_bytes) + PREPASS_BYTES_PER_PARAM * params) / step_s / 1e9,
-        "roofline": {"bound": "hbm", "kernel": "k_nadam_step", "achieved": k2_gbs, "peak": peak, "unit": "GB/s",
-                     "frac": k2_gbs / peak, "traffic": traffic, "peak_source": peak_src,
-                     "bytes_per_param": BYTES_PER_PARAM_U16,
+        "hbm_gbs_step_as_run": (sum(group_bytes) + (PREPASS_BYTES_PER_PARAM * params if args.states == "u16" else 0)) / step_s / 1e9,
+        "roofline": {"bound": "hbm", "kernel": ("k_nadam_f24" if args.states == "f24" else "k_nadam_step")
+                     + ("<sr>" if args.rounding == "sr" else ""),
+                     "achieved": k2_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": k2_gbs / peak,
+                     "traffic": traffic if (args.states == "u16" and args.rounding == "kahan") else None,
+                     "peak_source": peak_src,
+                     "bytes_per_param": (BYTES_PER_PARAM_F24 if args.states == "f24" else BYTES_PER_PARAM_U16)
+                     - (4 if args.rounding == "sr" else 0),
                      "launch_ms_mean": 1e3 * k2_time_total / len(k2_ms),
                      "prepass_ms_mean": statistics.mean(k1_ms)},
         "gpu_launches": launches_per_step * args.steps,
@@ -371,20 +385,38 @@ def run_ours(args, cfg):
 def e2e_run(args, groups, grads, hp, params, stream, world, device):
     """Same metric through the public API, host buffers: each step copies every group's bf16
     gradients from pinned host memory to the device, steps the group, and copies the updated bf16
-    weights back to pinned host memory; all copies are inside the timed region."""
+    weights back to pinned host memory; all copies are inside the timed region.  Copies run on
+    their own streams, ordered per group by events, so group k+1's copy-in and group k-1's
+    copy-out overlap group k's kernels."""
     import torch
     import torch.distributed as dist
     host_g = [[g.to("cpu").pin_memory() for g in gs] for gs in grads]
     host_w = [[torch.empty(w.shape, dtype=w.dtype, pin_memory=True) for w in grp.weights] for grp in groups]
     steps = max(1, min(args.steps, 3))
+    cin, cout = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+    n = len(groups)
+    done = [torch.cuda.Event() for _ in range(n)]      # group k's step finished (its buffers are free)
+    for e in done:
+        e.record(stream)
 
     def one():
-        for grp, gs, hg, hw in zip(groups, grads, host_g, host_w):
-            for d, h in zip(gs, hg):
-                d.copy_(h, non_blocking=True)
-            grp.step(gs, hp, stream)
-            for h, w in zip(hw, grp.weights):
-                h.copy_(w, non_blocking=True)
+        ins = []
+        for k in range(n):
+            cin.wait_event(done[k])                    # previous step no longer reads these gradients
+            with torch.cuda.stream(cin):
+                for d, h in zip(grads[k], host_g[k]):
+                    d.copy_(h, non_blocking=True)
+            e = torch.cuda.Event()
+            e.record(cin)
+            ins.append(e)
+        for k in range(n):
+            stream.wait_event(ins[k])
+            groups[k].step(grads[k], hp, stream)
+            done[k].record(stream)
+            cout.wait_event(done[k])
+            with torch.cuda.stream(cout):
+                for h, w in zip(host_w[k], groups[k].weights):
+                    h.copy_(w, non_blocking=True)
 
     one()
     torch.cuda.synchronize()
@@ -401,7 +433,8 @@ def e2e_run(args, groups, grads, hp, params, stream, world, device):
         dt = float(t.item())
     nbytes = 2 * params
     return {"value": world * params * steps / dt, "unit": "params/s", "h2d_bytes_per_step": nbytes,
-            "d2h_bytes_per_step": nbytes, "steps": steps}
+            "d2h_bytes_per_step": nbytes, "steps": steps,
+            "link_gbs": 2 * nbytes * steps / dt / 1e9}
 
 
 def run_offload(args, cfg):

@@ -75,18 +75,35 @@ typedef struct {
     int64_t shape[4];
 } optim_tensor_desc_t;
 
-enum { OPTIM_KIND_NADAM = 0, OPTIM_KIND_FACTORED = 1 };
+/* Group kinds.  NADAM_F24 is NADAM with f24 moment storage: the upper three bytes of each fp32
+ * moment ("f24 is the upper three bytes [of f32] - i.e. with 8 more bits of mantissa", "Amazing
+ * Flux FFT quality on a 5090", sd-scripts PR #2187, third post), truncated.  Its m and v buffers
+ * (numel > 4096) hold 3*numel bytes: numel uint16 upper words, then numel bytes of bits 8..15;
+ * 16-byte aligned planes (numel a multiple of 8) take the 128-bit path.  No scale records and no
+ * gradient pre-pass are involved; tensors of 4096 or fewer elements keep fp32 moments. */
+enum { OPTIM_KIND_NADAM = 0, OPTIM_KIND_FACTORED = 1, OPTIM_KIND_NADAM_F24 = 2, OPTIM_KIND_ADAN = 3 };
+/* ADAN groups: m -> fp32 [3*numel] (planes m, v, n), v -> uint16 [numel] (previous bf16 gradient),
+ * all zero at creation. */
 
 /* Adam / NAdam(W) hyper-parameters ("(N)AdamW / Adan with fused backwards pass & CPU
  * offloading", sd-scripts PR #2187, first post: NAdamOffload, AdamOffload, NAdamWOffload).
  *   wd_mode  : 0 none, 1 decoupled (the "W" variants: w -= lr*wd*w before the update)
  *   nesterov : 0 Adam, 1 NAdam (Dozat's momentum schedule mu_t = beta1 (1 - 0.5*0.96^(t*psi)))
- *   momentum_decay : psi, 0.004 by default */
+ *   momentum_decay : psi, 0.004 by default
+ *   stochastic_rounding : 1 = tensors WITHOUT a residual store the new weight stochastically
+ *             rounded to bf16 instead of round-to-nearest (sd-scripts' default alternative to
+ *             Kahan summation, "Kahan summation for Adafactor-optimized Flux FFT", PR #2159, PR
+ *             description): 16 random bits are added below the kept half.  The bits come from
+ *             Philox4x64-10 with key (seed, tensor index in the group) and counter (element / 16,
+ *             step, 0, 0), element i taking 16-bit lane i mod 16; results are reproducible.
+ *   seed     : key of the stochastic rounding */
 typedef struct {
     float lr, beta1, beta2, eps, weight_decay;
     int32_t wd_mode;
     int32_t nesterov;
     float momentum_decay;
+    int32_t stochastic_rounding;
+    uint64_t seed;
 } optim_nadam_hparams_t;
 
 /* Factored second-moment hyper-parameters (beta1 = 0: no exp_avg is read or written).
@@ -110,7 +127,7 @@ int optim_group_create(const optim_tensor_desc_t* tensors, int32_t n, int32_t ki
                        optim_group_t** out);
 int optim_group_destroy(optim_group_t* group);
 
-/* One fused NAdam(W)/Adam step of every tensor of a NADAM group, in one pass per element:
+/* One fused NAdam(W)/Adam step of every tensor of a NADAM or NADAM_F24 group, in one pass per element:
  * rebuild the fp32 master from (w_bf16, res_u16), decode m and v, update the moments, apply
  * decoupled decay and the bias-corrected (Nesterov) update, split the master back into
  * (w_bf16, res_u16), re-encode m and v, and reduce the per-tensor maxima that bound the next
@@ -131,6 +148,23 @@ int optim_step_nadam_kahan(optim_group_t* group, const void* const* grads_bf16, 
  * 1-D tensors keep a full second moment.  Arguments as optim_step_nadam_kahan. */
 int optim_step_factored(optim_group_t* group, const void* const* grads_bf16, int64_t step,
                         const optim_factored_hparams_t* hp, void* stream);
+
+/* Adan hyper-parameters (Algorithm 1 of the Adan paper linked by "Amazing Flux FFT quality on a
+ * 5090", sd-scripts PR #2187, fourth post; beta weights the new term, as in the paper).
+ * stochastic_rounding / seed as in optim_nadam_hparams_t (tensors without a residual). */
+typedef struct {
+    float lr, beta1, beta2, beta3, eps, weight_decay;
+    int32_t stochastic_rounding;
+    int32_t reserved;
+    uint64_t seed;
+} optim_adan_hparams_t;
+
+/* One fused Adan step of an ADAN group: d = g - g_prev, m, v, n EMAs, w = (w - lr (m + (1-b2) v) /
+ * (sqrt(n) + eps)) / (1 + lr wd), Kahan split (or stochastic / nearest rounding), g_prev = g.
+ * Step 1 starts from m = g, v = 0, n = g^2 and step 2 sets v = d.  Arguments as
+ * optim_step_nadam_kahan; one enqueued kernel. */
+int optim_step_adan(optim_group_t* group, const void* const* grads_bf16, int64_t step,
+                    const optim_adan_hparams_t* hp, void* stream);
 
 /* Encodes n fp32 moments into u16 codes with the engine's codec.  scale (device, 1 float) is
  * written with max|src| (is_signed = 1, exp_avg) or max src (is_signed = 0, exp_avg_sq); codes

@@ -108,11 +108,15 @@ static int validate_desc(const optim_tensor_desc_t& d, int32_t i, int32_t kind) 
     if (!d.w_bf16) return set_error(OPTIM_EINVAL, "tensor %d: w_bf16 is NULL", i);
     if (!is_aligned(d.w_bf16, 2) || (d.res_u16 && !is_aligned(d.res_u16, 2)))
         return set_error(OPTIM_EALIGN, "tensor %d: weight/residual not 2-byte aligned", i);
-    if (kind == OPTIM_KIND_NADAM) {
+    if (kind == OPTIM_KIND_NADAM || kind == OPTIM_KIND_NADAM_F24) {
         if (!d.m || !d.v) return set_error(OPTIM_EINVAL, "tensor %d: m or v is NULL", i);
         size_t a = d.numel <= kSmall ? 4 : 2;
         if (!is_aligned(d.m, a) || !is_aligned(d.v, a))
             return set_error(OPTIM_EALIGN, "tensor %d: m/v not %zu-byte aligned", i, a);
+    } else if (kind == OPTIM_KIND_ADAN) {
+        if (!d.m || !d.v) return set_error(OPTIM_EINVAL, "tensor %d: Adan state or previous gradient is NULL", i);
+        if (!is_aligned(d.m, 4) || !is_aligned(d.v, 2))
+            return set_error(OPTIM_EALIGN, "tensor %d: Adan buffers not aligned", i);
     } else {
         if (!d.v || (d.ndim >= 2 && !d.m)) return set_error(OPTIM_EINVAL, "tensor %d: factored state is NULL", i);
         if (!is_aligned(d.v, 4) || (d.m && !is_aligned(d.m, 4)))
@@ -171,7 +175,8 @@ int optim_group_create(const optim_tensor_desc_t* tensors, int32_t n, int32_t ki
     if (!out) return set_error(OPTIM_EINVAL, "out is NULL");
     *out = nullptr;
     if (!tensors || n < 1) return set_error(OPTIM_EINVAL, "need n >= 1 tensors");
-    if (kind != OPTIM_KIND_NADAM && kind != OPTIM_KIND_FACTORED)
+    if (kind != OPTIM_KIND_NADAM && kind != OPTIM_KIND_FACTORED && kind != OPTIM_KIND_NADAM_F24 &&
+        kind != OPTIM_KIND_ADAN)
         return set_error(OPTIM_EINVAL, "unknown group kind %d", kind);
     for (int32_t i = 0; i < n; ++i) {
         int rc = validate_desc(tensors[i], i, kind);
@@ -197,7 +202,7 @@ int optim_group_create(const optim_tensor_desc_t* tensors, int32_t n, int32_t ki
             r.flags = (d.numel <= kSmall ? kFlagSmall : 0) | (d.res_u16 ? kFlagRes : 0);
             r.pad = 0;
         }
-        if (kind == OPTIM_KIND_NADAM) {
+        if (kind == OPTIM_KIND_NADAM || kind == OPTIM_KIND_NADAM_F24 || kind == OPTIM_KIND_ADAN) {
             for (int pass = 0; pass < 2; ++pass) {   // u16-state tensors first, then fp32-state
                 for (int32_t i = 0; i < n; ++i) {
                     const int64_t ne = tensors[i].numel;
@@ -243,14 +248,16 @@ int optim_group_destroy(optim_group_t* g) {
 int optim_step_nadam_kahan(optim_group_t* g, const void* const* grads, int64_t step,
                            const optim_nadam_hparams_t* hp, void* stream) {
     if (!g || !hp) return set_error(OPTIM_EINVAL, "group or hparams is NULL");
-    if (g->kind != OPTIM_KIND_NADAM) return set_error(OPTIM_EINVAL, "not a NADAM group");
+    if (g->kind != OPTIM_KIND_NADAM && g->kind != OPTIM_KIND_NADAM_F24)
+        return set_error(OPTIM_EINVAL, "not a NADAM group");
     if (step != g->last_step + 1)
         return set_error(OPTIM_EINVAL, "step %lld but the group expects %lld", (long long)step,
                          (long long)(g->last_step + 1));
     if (!finite_nonneg(hp->lr) || !(hp->beta1 >= 0.0f && hp->beta1 < 1.0f) ||
         !(hp->beta2 >= 0.0f && hp->beta2 < 1.0f) || !finite_nonneg(hp->eps) ||
         !finite_nonneg(hp->weight_decay) || !finite_nonneg(hp->momentum_decay) ||
-        (hp->wd_mode != 0 && hp->wd_mode != 1) || (hp->nesterov != 0 && hp->nesterov != 1))
+        (hp->wd_mode != 0 && hp->wd_mode != 1) || (hp->nesterov != 0 && hp->nesterov != 1) ||
+        (hp->stochastic_rounding != 0 && hp->stochastic_rounding != 1))
         return set_error(OPTIM_EINVAL, "invalid NAdam hyper-parameters (wd_mode must be 0 or 1)");
     int rc = check_device(g);
     if (!rc) rc = validate_grads(g, grads);
@@ -281,6 +288,9 @@ int optim_step_nadam_kahan(optim_group_t* g, const void* const* grads, int64_t s
         k.c_g = 0.0f;
     }
     k.parity = g->next_parity;
+    k.sr = hp->stochastic_rounding;
+    k.seed = hp->seed;
+    k.step = (uint64_t)step;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     rc = upload_grads(g, grads, s);
@@ -291,7 +301,7 @@ int optim_step_nadam_kahan(optim_group_t* g, const void* const* grads, int64_t s
         if (rc) return rc;
     }
     NadamLaunch L{table, g->d_grads, g->d_scales, g->d_chunks, g->d_nonfinite,
-                  g->n_chunks_large, g->n_chunks_total};
+                  g->n_chunks_large, g->n_chunks_total, g->kind == OPTIM_KIND_NADAM_F24};
     rc = launch_nadam_step(L, k, s, g->profile_ev);
     if (rc) return rc;
     g->last_step = step;
@@ -299,6 +309,46 @@ int optim_step_nadam_kahan(optim_group_t* g, const void* const* grads, int64_t s
     g->next_parity ^= 1;
     g->last_stream = s;
     if (g->offload) return offload_step_end(g, s);
+    return OPTIM_OK;
+}
+
+int optim_step_adan(optim_group_t* g, const void* const* grads, int64_t step, const optim_adan_hparams_t* hp,
+                    void* stream) {
+    if (!g || !hp) return set_error(OPTIM_EINVAL, "group or hparams is NULL");
+    if (g->kind != OPTIM_KIND_ADAN) return set_error(OPTIM_EINVAL, "not an ADAN group");
+    if (step != g->last_step + 1)
+        return set_error(OPTIM_EINVAL, "step %lld but the group expects %lld", (long long)step,
+                         (long long)(g->last_step + 1));
+    auto unit = [](float x) { return x >= 0.0f && x <= 1.0f; };
+    if (!finite_nonneg(hp->lr) || !unit(hp->beta1) || !unit(hp->beta2) || !unit(hp->beta3) ||
+        !finite_nonneg(hp->eps) || !finite_nonneg(hp->weight_decay) ||
+        (hp->stochastic_rounding != 0 && hp->stochastic_rounding != 1))
+        return set_error(OPTIM_EINVAL, "invalid Adan hyper-parameters");
+    int rc = check_device(g);
+    if (!rc) rc = validate_grads(g, grads);
+    if (rc) return rc;
+    AdanScalars k{};
+    k.lr = hp->lr;
+    k.b1 = hp->beta1;
+    k.omb1 = (float)(1.0 - (double)hp->beta1);
+    k.b2 = hp->beta2;
+    k.omb2 = (float)(1.0 - (double)hp->beta2);
+    k.b3 = hp->beta3;
+    k.omb3 = (float)(1.0 - (double)hp->beta3);
+    k.eps = hp->eps;
+    k.inv_decay = (float)(1.0 / (1.0 + (double)hp->lr * (double)hp->weight_decay));
+    k.sr = hp->stochastic_rounding;
+    k.step = step;
+    k.seed = hp->seed;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    rc = upload_grads(g, grads, s);
+    if (rc) return rc;
+    NadamLaunch L{g->d_tensors, g->d_grads, g->d_scales, g->d_chunks, g->d_nonfinite, g->n_chunks_large,
+                  g->n_chunks_total, 0};
+    rc = launch_adan_step(L, k, s);
+    if (rc) return rc;
+    g->last_step = step;
+    g->last_stream = s;
     return OPTIM_OK;
 }
 

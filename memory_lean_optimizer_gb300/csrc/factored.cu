@@ -15,7 +15,8 @@
 //   vector (ndim == 1): one thread per element, full fp32 second moment
 // Per wave of tensors (waves keep the wave's gradients, read three times, within L2):
 //   1. k_stats  : wide tiles -> row/column partial sums of q;  tiny/vector -> state EMA, u, sum u^2
-//   2. k_final  : wide matrices -> R, C EMAs, mean(R), rsqrt factors per row and column
+//   2. k_final  : wide matrices -> R EMA over 256-row blocks (mean(R) by the last block of a
+//                 matrix), C EMA over 64-column blocks, rsqrt factor per column
 //   3. k_rms    : wide tiles -> sum u^2 per tile
 //   4. k_apply  : every element -> clip, lr, decay, subtract, split
 // The clip divisor of a tensor is computed by the last CTA to finish its partial sums (threadfence
@@ -32,9 +33,11 @@ namespace {
 
 constexpr int kTR = 64;      // rows per wide tile
 constexpr int kTC = 256;     // columns per wide tile
+constexpr int kFinRowsPerItem = 256;   // rows per finalize row block (one per thread)
+constexpr int kFinColsPerItem = 64;    // columns per finalize column block (4 band groups)
 constexpr int kTinyPerCta = kThreads;
 constexpr int kVecPerCta = kThreads * 8;
-constexpr int64_t kWaveGradBytes = 40ll << 20;   // gradient bytes per wave (L2-resident target)
+constexpr int64_t kWaveGradBytes = 64ll << 20;   // gradient bytes per wave (L2-resident target)
 
 enum : int32_t { kWide = 0, kTiny = 1, kVec = 2 };
 enum : int32_t { kFinRows = 0, kFinCols = 1 };
@@ -50,7 +53,11 @@ struct FTensor {
     int32_t ncb;    // column blocks (wide)
     int32_t nbands; // row bands (wide)
     int32_t ss_cnt;
-    int64_t rowpart_off, colpart_off, rr_off, cc_off, ss_off;
+    int32_t n_rowitems;  // finalize row blocks per matrix (wide)
+    int32_t pad;
+    int64_t rowpart_off, colpart_off, cc_off, ss_off;
+    int64_t mat_off;     // first matrix index of this tensor (mean(R) and its counter)
+    int64_t rbarpart_off;
 };
 
 struct Item {        // one CTA of k_stats / k_rms / k_apply / k_final
@@ -58,7 +65,7 @@ struct Item {        // one CTA of k_stats / k_rms / k_apply / k_final
     int32_t cls;     // kWide / kTiny / kVec (k_final: kFinRows / kFinCols)
     int32_t x;       // wide: matrix; tiny: first matrix; vector: chunk; final: matrix
     int32_t band;    // wide: row band
-    int32_t cb;      // wide / final cols: column block
+    int32_t cb;      // wide: 256-column block; final: row block / 64-column block
     int32_t part;    // index of this CTA's sum-of-squares partial within its tensor
 };
 
@@ -67,11 +74,13 @@ struct Dev {
     const uint16_t* const* grads;
     float* rowpart;
     float* colpart;
-    float* rr;
     float* cc;
+    float* rbar;        // mean(R) per matrix
+    float* rbarpart;    // per finalize row block
     float* ss;
     float* den;
-    unsigned* counter;
+    unsigned* counter;  // per tensor (sum of squares)
+    unsigned* rcounter; // per matrix (mean of R)
 };
 
 struct K {
@@ -173,10 +182,127 @@ __device__ __forceinline__ void load8(const uint16_t* p, int ncols, bool vec, ui
     }
 }
 
+// Copies n 16-bit words from global memory to shared memory, 128 bits at a time when aligned.
+__device__ __forceinline__ void stage_u16(uint16_t* dst, const uint16_t* src, int n) {
+    if (aligned16(src) && (n & 7) == 0) {
+        for (int i = threadIdx.x; i < (n >> 3); i += blockDim.x)
+            reinterpret_cast<uint4*>(dst)[i] = __ldcg(reinterpret_cast<const uint4*>(src) + i);
+    } else {
+        for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = src[i];
+    }
+}
+__device__ __forceinline__ void unstage_u16(uint16_t* dst, const uint16_t* src, int n) {
+    if (aligned16(dst) && (n & 7) == 0) {
+        for (int i = threadIdx.x; i < (n >> 3); i += blockDim.x)
+            st_stream(reinterpret_cast<uint4*>(dst) + i, reinterpret_cast<const uint4*>(src)[i]);
+    } else {
+        for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = src[i];
+    }
+}
+
+// One small matrix (rows*cols <= 16) of a tiny-class tensor: R, C EMAs (written back), mean(R),
+// and the matrix's sum of squared updates.  The fixed-size form keeps everything in registers.
+template <int RR, int CC>
+__device__ __forceinline__ float tiny_stats(const uint16_t* gm, float* Rs, float* Cs, const K& k) {
+    float q[RR * CC], rsum[RR], cfac[CC];
+#pragma unroll
+    for (int e = 0; e < RR * CC; ++e) q[e] = qval(bf16_to_f32(gm[e]), k);
+    float rtot = 0.f;
+#pragma unroll
+    for (int i = 0; i < RR; ++i) {
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < CC; ++j) s = __fadd_rn(s, q[i * CC + j]);
+        const float nr = ema(Rs[i], __fdiv_rn(s, (float)CC), k);
+        Rs[i] = nr;
+        rsum[i] = nr;
+        rtot = __fadd_rn(rtot, nr);
+    }
+#pragma unroll
+    for (int j = 0; j < CC; ++j) {
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < RR; ++i) s = __fadd_rn(s, q[i * CC + j]);
+        const float nc = ema(Cs[j], __fdiv_rn(s, (float)RR), k);
+        Cs[j] = nc;
+        cfac[j] = rsqrt_rn(nc);
+    }
+    const float rbar = __fdiv_rn(rtot, (float)RR);
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < RR; ++i) {
+        const float rr = rsqrt_rn(__fdiv_rn(rsum[i], rbar));
+#pragma unroll
+        for (int j = 0; j < CC; ++j) {
+            const float u = __fmul_rn(__fmul_rn(rr, cfac[j]), bf16_to_f32(gm[i * CC + j]));
+            acc = __fadd_rn(acc, __fmul_rn(u, u));
+        }
+    }
+    return acc;
+}
+__device__ float tiny_stats_any(const uint16_t* gm, float* Rs, float* Cs, int r, int c, const K& k) {
+    float q[16], rsum[16], csum[16];
+    for (int e = 0; e < r * c; ++e) q[e] = qval(bf16_to_f32(gm[e]), k);
+    float rtot = 0.f;
+    for (int i = 0; i < r; ++i) {
+        float s = 0.f;
+        for (int j = 0; j < c; ++j) s = __fadd_rn(s, q[i * c + j]);
+        const float nr = ema(Rs[i], __fdiv_rn(s, (float)c), k);
+        Rs[i] = nr;
+        rsum[i] = nr;
+        rtot = __fadd_rn(rtot, nr);
+    }
+    for (int j = 0; j < c; ++j) {
+        float s = 0.f;
+        for (int i = 0; i < r; ++i) s = __fadd_rn(s, q[i * c + j]);
+        const float nc = ema(Cs[j], __fdiv_rn(s, (float)r), k);
+        Cs[j] = nc;
+        csum[j] = rsqrt_rn(nc);
+    }
+    const float rbar = __fdiv_rn(rtot, (float)r);
+    float acc = 0.f;
+    for (int i = 0; i < r; ++i) {
+        const float rr = rsqrt_rn(__fdiv_rn(rsum[i], rbar));
+        for (int j = 0; j < c; ++j) {
+            const float u = __fmul_rn(__fmul_rn(rr, csum[j]), bf16_to_f32(gm[i * c + j]));
+            acc = __fadd_rn(acc, __fmul_rn(u, u));
+        }
+    }
+    return acc;
+}
+
+// Apply step of one small matrix on staged words (w, res, g in shared memory).
+template <int RR, int CC>
+__device__ __forceinline__ void tiny_apply(uint16_t* wm, uint16_t* rm, const uint16_t* gm, const float* Rs,
+                                           const float* Cs, bool has_res, float den, const K& k) {
+    float rtot = 0.f, rv[RR], cfac[CC];
+#pragma unroll
+    for (int i = 0; i < RR; ++i) {
+        rv[i] = Rs[i];
+        rtot = __fadd_rn(rtot, rv[i]);
+    }
+    const float rbar = __fdiv_rn(rtot, (float)RR);
+#pragma unroll
+    for (int j = 0; j < CC; ++j) cfac[j] = rsqrt_rn(Cs[j]);
+#pragma unroll
+    for (int i = 0; i < RR; ++i) {
+        const float rr = rsqrt_rn(__fdiv_rn(rv[i], rbar));
+#pragma unroll
+        for (int j = 0; j < CC; ++j) {
+            const int e = i * CC + j;
+            uint32_t hi = wm[e], lo = has_res ? rm[e] : 0u;
+            apply_elem(hi, lo, has_res, __fmul_rn(__fmul_rn(rr, cfac[j]), bf16_to_f32(gm[e])), den, k);
+            wm[e] = (uint16_t)hi;
+            if (has_res) rm[e] = (uint16_t)lo;
+        }
+    }
+}
+
 // ------------------------------------------------------------------------------------ stats
 __global__ void __launch_bounds__(kThreads) k_stats(Dev D, const Item* items, K k) {
     __shared__ float sm[32];
     __shared__ float cols[8][kTC + 1];
+    __shared__ __align__(16) uint16_t tile_g[kTinyPerCta * 16];
     const Item it = items[blockIdx.x];
     const FTensor t = D.tensors[it.tensor];
     const uint16_t* __restrict__ g = D.grads[it.tensor];
@@ -186,24 +312,50 @@ __global__ void __launch_bounds__(kThreads) k_stats(Dev D, const Item* items, K 
         const int64_t b = it.x;
         const int64_t col0 = (int64_t)it.cb * kTC + lane * 8;
         const int ncols = cols_in(t.C - col0);
-        const bool vec = aligned16(g) && (t.C % 8 == 0);
+        const bool vec = aligned16(g) && (t.C % 8 == 0) && ncols == 8;
+        const int64_t row0 = (int64_t)it.band * kTR + warp;
         float cacc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int kk = 0; kk < kTR / 8; ++kk) {
-            const int64_t row = (int64_t)it.band * kTR + warp + 8 * kk;
-            if (row >= t.R) break;
-            uint32_t v[8];
-            load8(g + (b * t.R + row) * t.C + col0, ncols, vec, v);
-            float rs = 0.f;
+        if (vec) {
+            // all eight rows' loads issued before any use (memory-level parallelism)
+            uint4 x[kTR / 8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (j < ncols) {
-                    const float q = qval(bf16_to_f32(v[j]), k);
-                    rs = __fadd_rn(rs, q);
-                    cacc[j] = __fadd_rn(cacc[j], q);
-                }
+            for (int kk = 0; kk < kTR / 8; ++kk) {
+                const int64_t row = row0 + 8 * kk;
+                x[kk] = row < t.R ? __ldcg(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0))
+                                  : make_uint4(0, 0, 0, 0);
             }
-            rs = warp_sum_f32(rs);
-            if (lane == 0) D.rowpart[t.rowpart_off + (b * t.R + row) * t.ncb + it.cb] = rs;
+#pragma unroll
+            for (int kk = 0; kk < kTR / 8; ++kk) {
+                const int64_t row = row0 + 8 * kk;
+                const uint32_t wd[4] = {x[kk].x, x[kk].y, x[kk].z, x[kk].w};
+                float rs = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float q = qval(__uint_as_float((j & 1) ? (wd[j >> 1] & 0xFFFF0000u) : (wd[j >> 1] << 16)), k);
+                    rs = __fadd_rn(rs, q);
+                    if (row < t.R) cacc[j] = __fadd_rn(cacc[j], q);
+                }
+                rs = warp_sum_f32(rs);
+                if (lane == 0 && row < t.R) D.rowpart[t.rowpart_off + (b * t.R + row) * t.ncb + it.cb] = rs;
+            }
+        } else {
+            for (int kk = 0; kk < kTR / 8; ++kk) {
+                const int64_t row = row0 + 8 * kk;
+                if (row >= t.R) break;
+                uint32_t v[8];
+                load8(g + (b * t.R + row) * t.C + col0, ncols, false, v);
+                float rs = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (j < ncols) {
+                        const float q = qval(bf16_to_f32(v[j]), k);
+                        rs = __fadd_rn(rs, q);
+                        cacc[j] = __fadd_rn(cacc[j], q);
+                    }
+                }
+                rs = warp_sum_f32(rs);
+                if (lane == 0) D.rowpart[t.rowpart_off + (b * t.R + row) * t.ncb + it.cb] = rs;
+            }
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j) cols[warp][lane * 8 + j] = cacc[j];
@@ -218,44 +370,16 @@ __global__ void __launch_bounds__(kThreads) k_stats(Dev D, const Item* items, K 
 
     float acc = 0.f;
     if (it.cls == kTiny) {
-        const int64_t mat = (int64_t)it.x + threadIdx.x;
-        if (mat < t.B) {
-            const int r = (int)t.R, c = (int)t.C;
-            const uint16_t* gm = g + mat * r * c;
-            float q[16], rsum[16], csum[16];
-            for (int e = 0; e < r * c; ++e) q[e] = qval(bf16_to_f32(gm[e]), k);
-            for (int i = 0; i < r; ++i) {
-                float s = 0.f;
-                for (int j = 0; j < c; ++j) s = __fadd_rn(s, q[i * c + j]);
-                rsum[i] = s;
-            }
-            for (int j = 0; j < c; ++j) {
-                float s = 0.f;
-                for (int i = 0; i < r; ++i) s = __fadd_rn(s, q[i * c + j]);
-                csum[j] = s;
-            }
-            float* Rs = t.row + mat * r;
-            float* Cs = t.col + mat * c;
-            float rtot = 0.f;
-            for (int i = 0; i < r; ++i) {
-                const float nr = ema(Rs[i], __fdiv_rn(rsum[i], (float)c), k);
-                Rs[i] = nr;
-                rsum[i] = nr;
-                rtot = __fadd_rn(rtot, nr);
-            }
-            for (int j = 0; j < c; ++j) {
-                const float nc = ema(Cs[j], __fdiv_rn(csum[j], (float)r), k);
-                Cs[j] = nc;
-                csum[j] = rsqrt_rn(nc);
-            }
-            const float rbar = __fdiv_rn(rtot, (float)r);
-            for (int i = 0; i < r; ++i) {
-                const float rr = rsqrt_rn(__fdiv_rn(rsum[i], rbar));
-                for (int j = 0; j < c; ++j) {
-                    const float u = __fmul_rn(__fmul_rn(rr, csum[j]), bf16_to_f32(gm[i * c + j]));
-                    acc = __fadd_rn(acc, __fmul_rn(u, u));
-                }
-            }
+        const int r = (int)t.R, c = (int)t.C, rc = r * c;
+        const int64_t m0 = it.x;
+        const int nm = (int)(t.B - m0 < kTinyPerCta ? t.B - m0 : kTinyPerCta);
+        stage_u16(tile_g, g + m0 * rc, nm * rc);
+        __syncthreads();
+        if ((int)threadIdx.x < nm) {
+            const uint16_t* gm = tile_g + threadIdx.x * rc;
+            float* Rs = t.row + (m0 + threadIdx.x) * r;
+            float* Cs = t.col + (m0 + threadIdx.x) * c;
+            acc = (r == 3 && c == 3) ? tiny_stats<3, 3>(gm, Rs, Cs, k) : tiny_stats_any(gm, Rs, Cs, r, c, k);
         }
     } else {  // kVec
         const int64_t e0 = (int64_t)it.x * kVecPerCta;
@@ -275,31 +399,54 @@ __global__ void __launch_bounds__(kThreads) k_stats(Dev D, const Item* items, K 
 // ------------------------------------------------------------------------------------ finalize
 __global__ void __launch_bounds__(kThreads) k_final(Dev D, const Item* items, K k) {
     __shared__ float sm[32];
+    __shared__ float part[4][kFinColsPerItem];
+    __shared__ bool last;
     const Item it = items[blockIdx.x];
     const FTensor t = D.tensors[it.tensor];
     const int64_t b = it.x;
     if (it.cls == kFinRows) {
-        Comp acc;
-        const float fc = (float)t.C;
-        for (int64_t i = threadIdx.x; i < t.R; i += kThreads) {
+        // R EMA of 256 rows (one per thread), their sum, and mean(R) by the matrix's last block
+        const int64_t i = (int64_t)it.cb * kFinRowsPerItem + threadIdx.x;
+        float nr = 0.f;
+        if (i < t.R) {
             const float* rp = D.rowpart + t.rowpart_off + (b * t.R + i) * t.ncb;
             Comp s;
             for (int cb = 0; cb < t.ncb; ++cb) s.add(rp[cb]);
-            const float nr = ema(t.row[b * t.R + i], __fdiv_rn(s.value(), fc), k);
+            nr = ema(t.row[b * t.R + i], __fdiv_rn(s.value(), (float)t.C), k);
             t.row[b * t.R + i] = nr;
-            acc.add(nr);
         }
-        const float tot = block_sum(acc.value(), sm);
-        const float rbar = __fdiv_rn(tot, (float)t.R);
-        for (int64_t i = threadIdx.x; i < t.R; i += kThreads)
-            D.rr[t.rr_off + b * t.R + i] = rsqrt_rn(__fdiv_rn(t.row[b * t.R + i], rbar));
+        const float tot = block_sum(nr, sm);
+        const int64_t mat = t.mat_off + b;
+        if (threadIdx.x == 0) {
+            D.rbarpart[t.rbarpart_off + b * t.n_rowitems + it.cb] = tot;
+            __threadfence();
+            last = atomicAdd(&D.rcounter[mat], 1u) == (unsigned)t.n_rowitems - 1u;
+        }
+        __syncthreads();
+        if (!last) return;
+        __threadfence();
+        Comp acc;
+        for (int r = threadIdx.x; r < t.n_rowitems; r += kThreads)
+            acc.add(__ldcg(D.rbarpart + t.rbarpart_off + b * t.n_rowitems + r));
+        const float all = block_sum(acc.value(), sm);
+        if (threadIdx.x == 0) {
+            D.rbar[mat] = __fdiv_rn(all, (float)t.R);
+            D.rcounter[mat] = 0u;
+        }
     } else {
-        const int64_t j = (int64_t)it.cb * kTC + threadIdx.x;
+        // C EMA of 64 columns: 4 groups of 64 threads split the row bands, combined in order
+        const int cl = threadIdx.x & (kFinColsPerItem - 1), grp = threadIdx.x / kFinColsPerItem;
+        const int64_t j = (int64_t)it.cb * kFinColsPerItem + cl;
+        Comp s;
         if (j < t.C) {
-            Comp s;
             const float* cp = D.colpart + t.colpart_off + b * t.nbands * t.C + j;
-            for (int band = 0; band < t.nbands; ++band) s.add(cp[(int64_t)band * t.C]);
-            const float nc = ema(t.col[b * t.C + j], __fdiv_rn(s.value(), (float)t.R), k);
+            for (int band = grp; band < t.nbands; band += 4) s.add(cp[(int64_t)band * t.C]);
+        }
+        part[grp][cl] = s.value();
+        __syncthreads();
+        if (grp == 0 && j < t.C) {
+            const float c = __fadd_rn(__fadd_rn(part[0][cl], part[1][cl]), __fadd_rn(part[2][cl], part[3][cl]));
+            const float nc = ema(t.col[b * t.C + j], __fdiv_rn(c, (float)t.R), k);
             t.col[b * t.C + j] = nc;
             D.cc[t.cc_off + b * t.C + j] = rsqrt_rn(nc);
         }
@@ -316,22 +463,47 @@ __global__ void __launch_bounds__(kThreads) k_rms(Dev D, const Item* items, K k)
     const int64_t b = it.x;
     const int64_t col0 = (int64_t)it.cb * kTC + lane * 8;
     const int ncols = cols_in(t.C - col0);
-    const bool vec = aligned16(g) && (t.C % 8 == 0);
+    const bool vec = aligned16(g) && (t.C % 8 == 0) && ncols == 8;
+    const float rbar = D.rbar[t.mat_off + b];
+    const int64_t row0 = (int64_t)it.band * kTR + warp;
     float ccv[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) ccv[j] = j < ncols ? D.cc[t.cc_off + b * t.C + col0 + j] : 0.f;
     float acc = 0.f;
-    for (int kk = 0; kk < kTR / 8; ++kk) {
-        const int64_t row = (int64_t)it.band * kTR + warp + 8 * kk;
-        if (row >= t.R) break;
-        const float rr = D.rr[t.rr_off + b * t.R + row];
-        uint32_t v[8];
-        load8(g + (b * t.R + row) * t.C + col0, ncols, vec, v);
+    if (vec) {
+        uint4 x[kTR / 8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (j < ncols) {
-                const float u = __fmul_rn(__fmul_rn(rr, ccv[j]), bf16_to_f32(v[j]));
+        for (int kk = 0; kk < kTR / 8; ++kk) {
+            const int64_t row = row0 + 8 * kk;
+            x[kk] = row < t.R ? __ldcg(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0))
+                              : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kTR / 8; ++kk) {
+            const int64_t row = row0 + 8 * kk;
+            if (row >= t.R) break;
+            const float rr = rsqrt_rn(__fdiv_rn(t.row[b * t.R + row], rbar));
+            const uint32_t wd[4] = {x[kk].x, x[kk].y, x[kk].z, x[kk].w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float gv = __uint_as_float((j & 1) ? (wd[j >> 1] & 0xFFFF0000u) : (wd[j >> 1] << 16));
+                const float u = __fmul_rn(__fmul_rn(rr, ccv[j]), gv);
                 acc = __fadd_rn(acc, __fmul_rn(u, u));
+            }
+        }
+    } else {
+        for (int kk = 0; kk < kTR / 8; ++kk) {
+            const int64_t row = row0 + 8 * kk;
+            if (row >= t.R) break;
+            const float rr = rsqrt_rn(__fdiv_rn(t.row[b * t.R + row], rbar));
+            uint32_t v[8];
+            load8(g + (b * t.R + row) * t.C + col0, ncols, false, v);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (j < ncols) {
+                    const float u = __fmul_rn(__fmul_rn(rr, ccv[j]), bf16_to_f32(v[j]));
+                    acc = __fadd_rn(acc, __fmul_rn(u, u));
+                }
             }
         }
     }
@@ -341,6 +513,9 @@ __global__ void __launch_bounds__(kThreads) k_rms(Dev D, const Item* items, K k)
 
 // ------------------------------------------------------------------------------------ apply
 __global__ void __launch_bounds__(kThreads) k_apply(Dev D, const Item* items, K k) {
+    __shared__ __align__(16) uint16_t tile_g[kTinyPerCta * 9];
+    __shared__ __align__(16) uint16_t tile_w[kTinyPerCta * 9];
+    __shared__ __align__(16) uint16_t tile_r[kTinyPerCta * 9];
     const Item it = items[blockIdx.x];
     const FTensor t = D.tensors[it.tensor];
     const uint16_t* __restrict__ g = D.grads[it.tensor];
@@ -356,10 +531,12 @@ __global__ void __launch_bounds__(kThreads) k_apply(Dev D, const Item* items, K 
         float ccv[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) ccv[j] = j < ncols ? D.cc[t.cc_off + b * t.C + col0 + j] : 0.f;
+        const float rbar = D.rbar[t.mat_off + b];
+#pragma unroll 2
         for (int kk = 0; kk < kTR / 8; ++kk) {
             const int64_t row = (int64_t)it.band * kTR + warp + 8 * kk;
             if (row >= t.R) break;
-            const float rr = D.rr[t.rr_off + b * t.R + row];
+            const float rr = rsqrt_rn(__fdiv_rn(t.row[b * t.R + row], rbar));
             const int64_t off = (b * t.R + row) * t.C + col0;
             if (vec && ncols == 8) {
                 const uint4 G = __ldcg(reinterpret_cast<const uint4*>(g + off));
@@ -398,9 +575,24 @@ __global__ void __launch_bounds__(kThreads) k_apply(Dev D, const Item* items, K 
         return;
     }
     if (it.cls == kTiny) {
-        const int64_t mat = (int64_t)it.x + threadIdx.x;
+        const int r = (int)t.R, c = (int)t.C, rc = r * c;
+        const int64_t m0 = it.x;
+        const int nm = (int)(t.B - m0 < kTinyPerCta ? t.B - m0 : kTinyPerCta);
+        if (r == 3 && c == 3) {
+            stage_u16(tile_g, g + m0 * rc, nm * rc);
+            stage_u16(tile_w, t.w + m0 * rc, nm * rc);
+            if (has_res) stage_u16(tile_r, t.res + m0 * rc, nm * rc);
+            __syncthreads();
+            if ((int)threadIdx.x < nm)
+                tiny_apply<3, 3>(tile_w + threadIdx.x * rc, tile_r + threadIdx.x * rc, tile_g + threadIdx.x * rc,
+                                 t.row + (m0 + threadIdx.x) * r, t.col + (m0 + threadIdx.x) * c, has_res, den, k);
+            __syncthreads();
+            unstage_u16(t.w + m0 * rc, tile_w, nm * rc);
+            if (has_res) unstage_u16(t.res + m0 * rc, tile_r, nm * rc);
+            return;
+        }
+        const int64_t mat = m0 + threadIdx.x;
         if (mat >= t.B) return;
-        const int r = (int)t.R, c = (int)t.C;
         const float* Rs = t.row + mat * r;
         const float* Cs = t.col + mat * c;
         float rtot = 0.f;
@@ -461,16 +653,21 @@ static int alloc_dev(FactoredPlan* p, T** out, size_t count, const char* what) {
     return check_cuda(cudaMemset(*out, 0, bytes), what);
 }
 
-int factored_plan_build(FactoredPlan*& plan, const std::vector<optim_tensor_desc_t>& desc) {
-    plan = new FactoredPlan();
-    FactoredPlan* p = plan;
+// Host-side layout of a factored plan: tensor records, work items and the sizes (in elements)
+// of every scratch array.  Shared by the allocating plan below.
+struct PlanLayout {
+    std::vector<FTensor> ts;
+    std::vector<Item> items, fin;
+    std::vector<Wave> waves;
+    int64_t rowpart = 0, colpart = 0, cc = 0, ss = 0, mats = 0, rbarpart = 0;
+};
+
+static void plan_layout(const std::vector<optim_tensor_desc_t>& desc, PlanLayout& L) {
     const int32_t n = (int32_t)desc.size();
-    std::vector<FTensor> ts(n);
-    int64_t rowpart = 0, colpart = 0, rr = 0, cc = 0, ss = 0;
+    L.ts.assign(n, FTensor{});
     for (int32_t i = 0; i < n; ++i) {
         const optim_tensor_desc_t& d = desc[i];
-        FTensor& t = ts[i];
-        t = FTensor{};
+        FTensor& t = L.ts[i];
         t.w = static_cast<uint16_t*>(d.w_bf16);
         t.res = static_cast<uint16_t*>(d.res_u16);
         t.numel = d.numel;
@@ -493,73 +690,87 @@ int factored_plan_build(FactoredPlan*& plan, const std::vector<optim_tensor_desc
         if (t.cls == kWide) {
             t.ncb = (int32_t)((t.C + kTC - 1) / kTC);
             t.nbands = (int32_t)((t.R + kTR - 1) / kTR);
-            t.rowpart_off = rowpart;
-            rowpart += t.B * t.R * t.ncb;
-            t.colpart_off = colpart;
-            colpart += t.B * t.nbands * t.C;
-            t.rr_off = rr;
-            rr += t.B * t.R;
-            t.cc_off = cc;
-            cc += t.B * t.C;
+            t.n_rowitems = (int32_t)((t.R + kFinRowsPerItem - 1) / kFinRowsPerItem);
+            t.rowpart_off = L.rowpart;
+            L.rowpart += t.B * t.R * t.ncb;
+            t.colpart_off = L.colpart;
+            L.colpart += t.B * t.nbands * t.C;
+            t.cc_off = L.cc;
+            L.cc += t.B * t.C;
+            t.mat_off = L.mats;
+            L.mats += t.B;
+            t.rbarpart_off = L.rbarpart;
+            L.rbarpart += t.B * t.n_rowitems;
             t.ss_cnt = (int32_t)(t.B * t.nbands * t.ncb);
         } else if (t.cls == kTiny) {
             t.ss_cnt = (int32_t)((t.B + kTinyPerCta - 1) / kTinyPerCta);
         } else {
             t.ss_cnt = (int32_t)((t.numel + kVecPerCta - 1) / kVecPerCta);
         }
-        t.ss_off = ss;
-        ss += t.ss_cnt;
+        t.ss_off = L.ss;
+        L.ss += t.ss_cnt;
     }
     // waves: consecutive tensors until the wave's gradient bytes reach the L2-resident target
-    std::vector<Item> items, fin;
     int32_t i = 0;
     while (i < n) {
         int64_t bytes = 0;
         int32_t j = i;
-        while (j < n && (j == i || bytes + 2 * ts[j].numel <= kWaveGradBytes)) bytes += 2 * ts[j++].numel;
+        while (j < n && (j == i || bytes + 2 * L.ts[j].numel <= kWaveGradBytes)) bytes += 2 * L.ts[j++].numel;
         Wave wv{};
-        wv.item_off = (int32_t)items.size();
-        wv.fin_off = (int32_t)fin.size();
+        wv.item_off = (int32_t)L.items.size();
+        wv.fin_off = (int32_t)L.fin.size();
         for (int32_t q = i; q < j; ++q) {
-            const FTensor& t = ts[q];
+            const FTensor& t = L.ts[q];
             if (t.numel == 0 || t.cls != kWide) continue;
             int32_t part = 0;
             for (int64_t b = 0; b < t.B; ++b) {
                 for (int32_t band = 0; band < t.nbands; ++band)
-                    for (int32_t cb = 0; cb < t.ncb; ++cb) items.push_back(Item{q, kWide, (int32_t)b, band, cb, part++});
-                fin.push_back(Item{q, kFinRows, (int32_t)b, 0, 0, 0});
-                for (int32_t cb = 0; cb < t.ncb; ++cb) fin.push_back(Item{q, kFinCols, (int32_t)b, 0, cb, 0});
+                    for (int32_t cb = 0; cb < t.ncb; ++cb) L.items.push_back(Item{q, kWide, (int32_t)b, band, cb, part++});
+                for (int32_t rb = 0; rb < t.n_rowitems; ++rb) L.fin.push_back(Item{q, kFinRows, (int32_t)b, 0, rb, 0});
+                const int32_t ncol = (int32_t)((t.C + kFinColsPerItem - 1) / kFinColsPerItem);
+                for (int32_t cb = 0; cb < ncol; ++cb) L.fin.push_back(Item{q, kFinCols, (int32_t)b, 0, cb, 0});
             }
         }
-        wv.n_wide = (int32_t)items.size() - wv.item_off;
+        wv.n_wide = (int32_t)L.items.size() - wv.item_off;
         for (int32_t q = i; q < j; ++q) {
-            const FTensor& t = ts[q];
+            const FTensor& t = L.ts[q];
             if (t.numel == 0 || t.cls == kWide) continue;
             for (int32_t part = 0; part < t.ss_cnt; ++part) {
                 const int32_t x = t.cls == kTiny ? part * kTinyPerCta : part;
-                items.push_back(Item{q, t.cls, x, 0, 0, part});
+                L.items.push_back(Item{q, t.cls, x, 0, 0, part});
             }
         }
-        wv.n_total = (int32_t)items.size() - wv.item_off;
-        wv.n_fin = (int32_t)fin.size() - wv.fin_off;
-        p->waves.push_back(wv);
+        wv.n_total = (int32_t)L.items.size() - wv.item_off;
+        wv.n_fin = (int32_t)L.fin.size() - wv.fin_off;
+        L.waves.push_back(wv);
         i = j;
     }
+}
+
+int factored_plan_build(FactoredPlan*& plan, const std::vector<optim_tensor_desc_t>& desc) {
+    plan = new FactoredPlan();
+    FactoredPlan* p = plan;
+    PlanLayout L;
+    plan_layout(desc, L);
+    p->waves = L.waves;
+    const size_t n = desc.size();
     int rc = OPTIM_OK;
     Dev& D = p->dev;
-    if (!rc) rc = alloc_dev(p, &p->d_tensors, ts.size(), "factored tensor table");
-    if (!rc) rc = check_cuda(cudaMemcpy(p->d_tensors, ts.data(), ts.size() * sizeof(FTensor), cudaMemcpyHostToDevice), "upload");
-    if (!rc) rc = alloc_dev(p, &p->d_items, items.size(), "factored work items");
-    if (!rc && !items.empty()) rc = check_cuda(cudaMemcpy(p->d_items, items.data(), items.size() * sizeof(Item), cudaMemcpyHostToDevice), "upload");
-    if (!rc) rc = alloc_dev(p, &p->d_fin, fin.size(), "factored finalize items");
-    if (!rc && !fin.empty()) rc = check_cuda(cudaMemcpy(p->d_fin, fin.data(), fin.size() * sizeof(Item), cudaMemcpyHostToDevice), "upload");
-    if (!rc) rc = alloc_dev(p, &D.rowpart, (size_t)rowpart, "row partial sums");
-    if (!rc) rc = alloc_dev(p, &D.colpart, (size_t)colpart, "column partial sums");
-    if (!rc) rc = alloc_dev(p, &D.rr, (size_t)rr, "row factors");
-    if (!rc) rc = alloc_dev(p, &D.cc, (size_t)cc, "column factors");
-    if (!rc) rc = alloc_dev(p, &D.ss, (size_t)ss, "sum-of-squares partials");
-    if (!rc) rc = alloc_dev(p, &D.den, (size_t)n, "clip divisors");
-    if (!rc) rc = alloc_dev(p, &D.counter, (size_t)n, "partial counters");
+    if (!rc) rc = alloc_dev(p, &p->d_tensors, L.ts.size(), "factored tensor table");
+    if (!rc) rc = check_cuda(cudaMemcpy(p->d_tensors, L.ts.data(), L.ts.size() * sizeof(FTensor), cudaMemcpyHostToDevice), "upload");
+    if (!rc) rc = alloc_dev(p, &p->d_items, L.items.size(), "factored work items");
+    if (!rc && !L.items.empty()) rc = check_cuda(cudaMemcpy(p->d_items, L.items.data(), L.items.size() * sizeof(Item), cudaMemcpyHostToDevice), "upload");
+    if (!rc) rc = alloc_dev(p, &p->d_fin, L.fin.size(), "factored finalize items");
+    if (!rc && !L.fin.empty()) rc = check_cuda(cudaMemcpy(p->d_fin, L.fin.data(), L.fin.size() * sizeof(Item), cudaMemcpyHostToDevice), "upload");
+    if (!rc) rc = alloc_dev(p, &D.rowpart, (size_t)L.rowpart, "row partial sums");
+    if (!rc) rc = alloc_dev(p, &D.colpart, (size_t)L.colpart, "column partial sums");
+    if (!rc) rc = alloc_dev(p, &D.cc, (size_t)L.cc, "column factors");
+    if (!rc) rc = alloc_dev(p, &D.rbar, (size_t)L.mats, "row means");
+    if (!rc) rc = alloc_dev(p, &D.rbarpart, (size_t)L.rbarpart, "row-mean partials");
+    if (!rc) rc = alloc_dev(p, &D.rcounter, (size_t)L.mats, "row-mean counters");
+    if (!rc) rc = alloc_dev(p, &D.ss, (size_t)L.ss, "sum-of-squares partials");
+    if (!rc) rc = alloc_dev(p, &D.den, n, "clip divisors");
+    if (!rc) rc = alloc_dev(p, &D.counter, n, "partial counters");
     D.tensors = p->d_tensors;
     return rc;
 }
@@ -594,3 +805,4 @@ int launch_factored_step(const FactoredPlan* p, const uint16_t* const* d_grads, 
 }
 
 }  // namespace lmo
+

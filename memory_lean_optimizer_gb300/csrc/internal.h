@@ -34,6 +34,9 @@ struct NadamScalars {
     float lr, b1, omb1, b2, omb2, eps, lr_wd, c_m, c_g, k2;
     int32_t decoupled;
     int32_t parity;
+    int32_t sr;        // stochastic rounding for tensors without a residual
+    uint64_t seed;
+    uint64_t step;
 };
 
 struct NadamLaunch {
@@ -44,7 +47,17 @@ struct NadamLaunch {
     unsigned long long* nonfinite;
     int32_t n_chunks_large;   // chunks of u16-state tensors come first
     int32_t n_chunks_total;
+    int32_t f24;              // moments stored as f24 planes instead of u16 codes
 };
 int launch_nadam_step(const NadamLaunch& L, const NadamScalars& k, cudaStream_t s, cudaEvent_t mid);
+
+// Per-step scalars of the Adan kernel.
+struct AdanScalars {
+    float lr, b1, omb1, b2, omb2, b3, omb3, eps, inv_decay;
+    int32_t sr;
+    int64_t step;
+    uint64_t seed;
+};
+int launch_adan_step(const NadamLaunch& L, const AdanScalars& k, cudaStream_t s);
 
 }  // namespace lmo

@@ -30,7 +30,54 @@ namespace {
 struct Prm {
     float lr, b1, omb1, b2, omb2, eps, lr_wd, c_m, c_g, k2;
     int32_t decoupled;
+    int32_t sr;           // stochastic rounding of tensors without a residual
+    uint64_t seed;
+    uint64_t step;
 };
+
+// Philox4x64-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
+// SC 2011): ten rounds of two 64x64->128 multiplies with Weyl-sequence key bumps.
+__device__ __forceinline__ void philox4x64_10(uint64_t& c0, uint64_t& c1, uint64_t& c2, uint64_t& c3,
+                                              uint64_t k0, uint64_t k1) {
+    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint64_t hi0 = __umul64hi(M0, c0), lo0 = M0 * c0;
+        const uint64_t hi1 = __umul64hi(M1, c2), lo1 = M1 * c2;
+        const uint64_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+        k0 += W0;
+        k1 += W1;
+    }
+}
+// Random 16-bit lanes for 8 consecutive elements starting at element i0 (i0 % 8 == 0) of
+// tensor `tensor`: key (seed, tensor), counter (i0 / 16, step, 0, 0); lanes low to high.
+__device__ __forceinline__ void sr_lanes8(const Prm& k, uint32_t tensor, int64_t i0, uint32_t (&r)[4]) {
+    uint64_t c0 = (uint64_t)i0 >> 4, c1 = k.step, c2 = 0, c3 = 0;
+    philox4x64_10(c0, c1, c2, c3, k.seed, tensor);
+    const uint64_t a = (i0 & 8) ? c2 : c0, b = (i0 & 8) ? c3 : c1;
+    r[0] = (uint32_t)a;          // lanes 0,1 (low half = first element)
+    r[1] = (uint32_t)(a >> 32);  // lanes 2,3
+    r[2] = (uint32_t)b;
+    r[3] = (uint32_t)(b >> 32);
+}
+__device__ __forceinline__ uint32_t sr_lane1(const Prm& k, uint32_t tensor, int64_t i) {
+    uint64_t c0 = (uint64_t)i >> 4, c1 = k.step, c2 = 0, c3 = 0;
+    philox4x64_10(c0, c1, c2, c3, k.seed, tensor);
+    const int lane = (int)(i & 15);
+    const uint64_t wsel = lane < 4 ? c0 : (lane < 8 ? c1 : (lane < 12 ? c2 : c3));
+    return (uint32_t)(wsel >> (16 * (lane & 3))) & 0xFFFFu;
+}
+// Stochastic rounding to bf16 bits: add 16 random bits below the kept half (inf/NaN kept).
+__device__ __forceinline__ uint32_t sr_bf16(float x, uint32_t r16) {
+    const uint32_t b = __float_as_uint(x);
+    if ((b & 0x7F800000u) == 0x7F800000u) return b >> 16;
+    return (b + r16) >> 16;
+}
 
 // ------------------------------------------------------------------------------------ K1
 __global__ void __launch_bounds__(kThreads) k_grad_absmax(NadamLaunch L, int parity) {
@@ -96,11 +143,15 @@ __device__ __forceinline__ void unpack_w(uint32_t W, uint32_t R, bool has_res, f
     w0 = __uint_as_float(has_res ? __byte_perm(R, W, 0x5410) : (W << 16));
     w1 = __uint_as_float(has_res ? __byte_perm(R, W, 0x7632) : (W & 0xFFFF0000u));
 }
-__device__ __forceinline__ void pack_w(float w0, float w1, bool has_res, uint32_t& W, uint32_t& R) {
+// rnd: two random 16-bit lanes (low half for w0) when stochastic rounding applies, else unused.
+__device__ __forceinline__ void pack_w(float w0, float w1, bool has_res, bool sr, uint32_t rnd, uint32_t& W,
+                                       uint32_t& R) {
     const uint32_t b0 = __float_as_uint(w0), b1 = __float_as_uint(w1);
     if (has_res) {
         W = pack_hi16(b0, b1);
         R = pack_lo16(b0, b1);
+    } else if (sr) {
+        W = pack_lo16(sr_bf16(w0, rnd & 0xFFFFu), sr_bf16(w1, rnd >> 16));
     } else {
         W = pack_lo16(rne_bf16(w0), rne_bf16(w1));
     }
@@ -112,9 +163,9 @@ struct Codec {
 
 // Two u16-state elements.  am/av: running max |m|, max v (NaN skipped); nf: running max of the
 // bf16 weight magnitudes (>= 0x7F80 in either half means a non-finite weight).
-__device__ __forceinline__ void step2_u16(const Prm& k, const Codec& cd, bool has_res, uint32_t& W,
-                                          uint32_t& R, uint32_t G, uint32_t& M, uint32_t& V, float& am,
-                                          float& av, uint32_t& nf) {
+__device__ __forceinline__ void step2_u16(const Prm& k, const Codec& cd, bool has_res, bool sr, uint32_t rnd,
+                                          uint32_t& W, uint32_t& R, uint32_t G, uint32_t& M, uint32_t& V,
+                                          float& am, float& av, uint32_t& nf) {
     float w0, w1;
     unpack_w(W, R, has_res, w0, w1);
     float m0 = dec_m_field<0x7610>(M, cd.dec.qm), m1 = dec_m_field<0x7632>(M, cd.dec.qm);
@@ -122,7 +173,7 @@ __device__ __forceinline__ void step2_u16(const Prm& k, const Codec& cd, bool ha
     float s0, s1;
     w0 = elem(k, w0, __uint_as_float(G << 16), m0, v0, s0);
     w1 = elem(k, w1, __uint_as_float(G & 0xFFFF0000u), m1, v1, s1);
-    pack_w(w0, w1, has_res, W, R);
+    pack_w(w0, w1, has_res, sr, rnd, W, R);
     M = pack_lo16(enc_m_bits(m0, cd.enc.rm), enc_m_bits(m1, cd.enc.rm));
     V = pack_lo16(enc_v_bits(s0, cd.enc.rv), enc_v_bits(s1, cd.enc.rv));
     am = fmaxf(am, fmaxf(fabsf(m0), fabsf(m1)));
@@ -131,33 +182,45 @@ __device__ __forceinline__ void step2_u16(const Prm& k, const Codec& cd, bool ha
 }
 
 // Two fp32-state elements (numel <= 4096).
-__device__ __forceinline__ void step2_f32(const Prm& k, bool has_res, uint32_t& W, uint32_t& R, uint32_t G,
-                                          float& m0, float& m1, float& v0, float& v1, uint32_t& nf) {
+__device__ __forceinline__ void step2_f32(const Prm& k, bool has_res, bool sr, uint32_t rnd, uint32_t& W,
+                                          uint32_t& R, uint32_t G, float& m0, float& m1, float& v0, float& v1,
+                                          uint32_t& nf) {
     float w0, w1, s0, s1;
     unpack_w(W, R, has_res, w0, w1);
     w0 = elem(k, w0, __uint_as_float(G << 16), m0, v0, s0);
     w1 = elem(k, w1, __uint_as_float(G & 0xFFFF0000u), m1, v1, s1);
-    pack_w(w0, w1, has_res, W, R);
+    pack_w(w0, w1, has_res, sr, rnd, W, R);
     nf = __vmaxu2(nf, W & 0x7FFF7FFFu);
 }
 
-__device__ __forceinline__ void step8_u16(const Prm& k, const Codec& cd, bool has_res, uint4& W, uint4& R,
-                                          const uint4& G, uint4& M, uint4& V, float& am, float& av,
-                                          uint32_t& nf) {
-    step2_u16(k, cd, has_res, W.x, R.x, G.x, M.x, V.x, am, av, nf);
-    step2_u16(k, cd, has_res, W.y, R.y, G.y, M.y, V.y, am, av, nf);
-    step2_u16(k, cd, has_res, W.z, R.z, G.z, M.z, V.z, am, av, nf);
-    step2_u16(k, cd, has_res, W.w, R.w, G.w, M.w, V.w, am, av, nf);
+// i0: index of the first of the 8 elements (for the stochastic-rounding lanes).  kSR: the
+// stochastic-rounding variant (compiled separately so the residual path carries none of it).
+template <bool kSR>
+__device__ __forceinline__ void step8_u16(const Prm& k, const Codec& cd, bool has_res, uint32_t tensor,
+                                          int64_t i0, uint4& W, uint4& R, const uint4& G, uint4& M, uint4& V,
+                                          float& am, float& av, uint32_t& nf) {
+    const bool sr = kSR && !has_res;
+    uint32_t r[4] = {0u, 0u, 0u, 0u};
+    if (sr) sr_lanes8(k, tensor, i0, r);
+    step2_u16(k, cd, has_res, sr, r[0], W.x, R.x, G.x, M.x, V.x, am, av, nf);
+    step2_u16(k, cd, has_res, sr, r[1], W.y, R.y, G.y, M.y, V.y, am, av, nf);
+    step2_u16(k, cd, has_res, sr, r[2], W.z, R.z, G.z, M.z, V.z, am, av, nf);
+    step2_u16(k, cd, has_res, sr, r[3], W.w, R.w, G.w, M.w, V.w, am, av, nf);
 }
 
-__device__ __forceinline__ void step8_f32(const Prm& k, bool has_res, uint4& W, uint4& R, const uint4& G,
-                                          float4 (&M)[2], float4 (&V)[2], uint32_t& nf) {
-    step2_f32(k, has_res, W.x, R.x, G.x, M[0].x, M[0].y, V[0].x, V[0].y, nf);
-    step2_f32(k, has_res, W.y, R.y, G.y, M[0].z, M[0].w, V[0].z, V[0].w, nf);
-    step2_f32(k, has_res, W.z, R.z, G.z, M[1].x, M[1].y, V[1].x, V[1].y, nf);
-    step2_f32(k, has_res, W.w, R.w, G.w, M[1].z, M[1].w, V[1].z, V[1].w, nf);
+template <bool kSR>
+__device__ __forceinline__ void step8_f32(const Prm& k, bool has_res, uint32_t tensor, int64_t i0, uint4& W,
+                                          uint4& R, const uint4& G, float4 (&M)[2], float4 (&V)[2], uint32_t& nf) {
+    const bool sr = kSR && !has_res;
+    uint32_t r[4] = {0u, 0u, 0u, 0u};
+    if (sr) sr_lanes8(k, tensor, i0, r);
+    step2_f32(k, has_res, sr, r[0], W.x, R.x, G.x, M[0].x, M[0].y, V[0].x, V[0].y, nf);
+    step2_f32(k, has_res, sr, r[1], W.y, R.y, G.y, M[0].z, M[0].w, V[0].z, V[0].w, nf);
+    step2_f32(k, has_res, sr, r[2], W.z, R.z, G.z, M[1].x, M[1].y, V[1].x, V[1].y, nf);
+    step2_f32(k, has_res, sr, r[3], W.w, R.w, G.w, M[1].z, M[1].w, V[1].z, V[1].w, nf);
 }
 
+template <bool kSR>
 __global__ void __launch_bounds__(kThreads, 4) k_nadam_step(NadamLaunch L, Prm k, int parity) {
     __shared__ uint32_t red[3 * 32];
     const Chunk c = L.chunks[blockIdx.x];
@@ -209,12 +272,12 @@ __global__ void __launch_bounds__(kThreads, 4) k_nadam_step(NadamLaunch L, Prm k
                 uint4 G0 = ld_stream(gv + i), G1 = ld_stream(gv + i1);
                 uint4 M0 = ld_stream(mv + i), M1 = ld_stream(mv + i1);
                 uint4 V0 = ld_stream(vv + i), V1 = ld_stream(vv + i1);
-                step8_u16(k, cd, has_res, W0, R0, G0, M0, V0, am, av, nf);
+                step8_u16<kSR>(k, cd, has_res, c.tensor, start + 8 * i, W0, R0, G0, M0, V0, am, av, nf);
                 st_stream(wv + i, W0);
                 if (has_res) st_stream(rv + i, R0);
                 st_stream(mv + i, M0);
                 st_stream(vv + i, V0);
-                step8_u16(k, cd, has_res, W1, R1, G1, M1, V1, am, av, nf);
+                step8_u16<kSR>(k, cd, has_res, c.tensor, start + 8 * i1, W1, R1, G1, M1, V1, am, av, nf);
                 st_stream(wv + i1, W1);
                 if (has_res) st_stream(rv + i1, R1);
                 st_stream(mv + i1, M1);
@@ -224,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_nadam_step(NadamLaunch L, Prm k
                 uint4 W0 = ld_stream(wv + i);
                 uint4 R0 = has_res ? ld_stream(rv + i) : make_uint4(0, 0, 0, 0);
                 uint4 G0 = ld_stream(gv + i), M0 = ld_stream(mv + i), V0 = ld_stream(vv + i);
-                step8_u16(k, cd, has_res, W0, R0, G0, M0, V0, am, av, nf);
+                step8_u16<kSR>(k, cd, has_res, c.tensor, start + 8 * i, W0, R0, G0, M0, V0, am, av, nf);
                 st_stream(wv + i, W0);
                 if (has_res) st_stream(rv + i, R0);
                 st_stream(mv + i, M0);
@@ -239,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_nadam_step(NadamLaunch L, Prm k
                 uint4 G0 = ld_stream(gv + i);
                 float4 M[2] = {ld_stream(mv + 2 * i), ld_stream(mv + 2 * i + 1)};
                 float4 V[2] = {ld_stream(vv + 2 * i), ld_stream(vv + 2 * i + 1)};
-                step8_f32(k, has_res, W0, R0, G0, M, V, nf);
+                step8_f32<kSR>(k, has_res, c.tensor, start + 8 * i, W0, R0, G0, M, V, nf);
                 st_stream(wv + i, W0);
                 if (has_res) st_stream(rv + i, R0);
                 st_stream(mv + 2 * i, M[0]);
@@ -263,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_nadam_step(NadamLaunch L, Prm k
         }
         const float w1 = elem(k, w0, bf16_to_f32(g[i]), m, v, sv);
         const uint32_t b = __float_as_uint(w1);
-        const uint32_t hi = has_res ? (b >> 16) : rne_bf16(w1);
+        const uint32_t hi = has_res ? (b >> 16) : (kSR ? sr_bf16(w1, sr_lane1(k, c.tensor, i)) : rne_bf16(w1));
         w[i] = (uint16_t)hi;
         if (has_res) res[i] = (uint16_t)(b & 0xFFFFu);
         nf = max(nf, hi & 0x7FFFu);
@@ -290,10 +353,151 @@ __global__ void __launch_bounds__(kThreads, 4) k_nadam_step(NadamLaunch L, Prm k
     }
 }
 
+// ------------------------------------------------------------------------------------ f24
+// f24 moments: the upper 24 bits of the fp32 moment ("f24 is the upper three bytes [of f32]",
+// sd-scripts PR #2187, third post), stored as a plane of n upper 16-bit words followed by a
+// plane of n bytes (bits 8..15).  Storage only: the update runs on the decoded fp32 values, and
+// no scale (hence no gradient pre-pass) is needed.  22 bytes per element per step.
+__device__ __forceinline__ float f24_value(uint32_t hi16, uint32_t lo8) { return __uint_as_float((hi16 << 16) | (lo8 << 8)); }
+
+// Bits 8..15 of four fp32 patterns, packed into one word (element 0 in the low byte).
+__device__ __forceinline__ uint32_t pack_byte1(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+    return __byte_perm(__byte_perm(b0, b1, 0x0051), __byte_perm(b2, b3, 0x0051), 0x5410);
+}
+
+template <bool kSR>
+__device__ __forceinline__ void step8_f24(const Prm& k, bool has_res, uint32_t tensor, int64_t i0, uint4& W, uint4& R,
+                                          const uint4& G, uint4& MH, uint2& ML, uint4& VH, uint2& VL, uint32_t& nf) {
+    const bool sr = kSR && !has_res;
+    uint32_t rnd[4] = {0u, 0u, 0u, 0u};
+    if (sr) sr_lanes8(k, tensor, i0, rnd);
+    uint32_t* w32 = reinterpret_cast<uint32_t*>(&W);
+    uint32_t* r32 = reinterpret_cast<uint32_t*>(&R);
+    const uint32_t* g32 = reinterpret_cast<const uint32_t*>(&G);
+    uint32_t* mh = reinterpret_cast<uint32_t*>(&MH);
+    uint32_t* vh = reinterpret_cast<uint32_t*>(&VH);
+    const uint32_t ml[2] = {ML.x, ML.y}, vl[2] = {VL.x, VL.y};
+    uint32_t mb[8], vb[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float w0, w1, s0, s1;
+        unpack_w(w32[j], r32[j], has_res, w0, w1);
+        const uint32_t lm = ml[j >> 1] >> (16 * (j & 1)), lv = vl[j >> 1] >> (16 * (j & 1));
+        float m0 = f24_value(mh[j] & 0xFFFFu, lm & 0xFFu), m1 = f24_value(mh[j] >> 16, (lm >> 8) & 0xFFu);
+        float v0 = f24_value(vh[j] & 0xFFFFu, lv & 0xFFu), v1 = f24_value(vh[j] >> 16, (lv >> 8) & 0xFFu);
+        w0 = elem(k, w0, __uint_as_float(g32[j] << 16), m0, v0, s0);
+        w1 = elem(k, w1, __uint_as_float(g32[j] & 0xFFFF0000u), m1, v1, s1);
+        pack_w(w0, w1, has_res, sr, rnd[j], w32[j], r32[j]);
+        nf = __vmaxu2(nf, w32[j] & 0x7FFF7FFFu);
+        mb[2 * j] = __float_as_uint(m0);
+        mb[2 * j + 1] = __float_as_uint(m1);
+        vb[2 * j] = __float_as_uint(v0);
+        vb[2 * j + 1] = __float_as_uint(v1);
+        mh[j] = pack_hi16(mb[2 * j], mb[2 * j + 1]);
+        vh[j] = pack_hi16(vb[2 * j], vb[2 * j + 1]);
+    }
+    ML.x = pack_byte1(mb[0], mb[1], mb[2], mb[3]);
+    ML.y = pack_byte1(mb[4], mb[5], mb[6], mb[7]);
+    VL.x = pack_byte1(vb[0], vb[1], vb[2], vb[3]);
+    VL.y = pack_byte1(vb[4], vb[5], vb[6], vb[7]);
+}
+
+template <bool kSR>
+__global__ void __launch_bounds__(kThreads, 4) k_nadam_f24(NadamLaunch L, Prm k) {
+    __shared__ uint32_t red[32];
+    const Chunk c = L.chunks[blockIdx.x];
+    const TensorRec t = L.tensors[c.tensor];
+    const uint16_t* __restrict__ g = L.grads[c.tensor];
+    const bool small = (t.flags & kFlagSmall) != 0;
+    const bool has_res = (t.flags & kFlagRes) != 0;
+    const int64_t n = t.numel;
+    const int64_t start = (int64_t)c.index * kChunk;
+    const int64_t end = min(n, start + kChunk);
+    uint32_t nf = 0u;
+    uint16_t* __restrict__ w = t.w;
+    uint16_t* __restrict__ res = t.res;
+    int64_t done = start;
+    if (!small) {
+        uint16_t* mhi = static_cast<uint16_t*>(t.m);
+        uint16_t* vhi = static_cast<uint16_t*>(t.v);
+        uint8_t* mlo = reinterpret_cast<uint8_t*>(mhi + n);
+        uint8_t* vlo = reinterpret_cast<uint8_t*>(vhi + n);
+        const bool vec = aligned16(w) && (!has_res || aligned16(res)) && aligned16(g) && aligned16(mhi) &&
+                         aligned16(vhi) && ((reinterpret_cast<uintptr_t>(mlo) | reinterpret_cast<uintptr_t>(vlo)) & 7u) == 0u;
+        if (vec) {
+            const int64_t nv = (end - start) >> 3;
+            uint4* wv = reinterpret_cast<uint4*>(w + start);
+            uint4* rv = has_res ? reinterpret_cast<uint4*>(res + start) : nullptr;
+            const uint4* gv = reinterpret_cast<const uint4*>(g + start);
+            uint4* mhv = reinterpret_cast<uint4*>(mhi + start);
+            uint4* vhv = reinterpret_cast<uint4*>(vhi + start);
+            uint2* mlv = reinterpret_cast<uint2*>(mlo + start);
+            uint2* vlv = reinterpret_cast<uint2*>(vlo + start);
+            for (int64_t i = threadIdx.x; i < nv; i += kThreads) {
+                uint4 W0 = ld_stream(wv + i);
+                uint4 R0 = has_res ? ld_stream(rv + i) : make_uint4(0, 0, 0, 0);
+                uint4 G0 = ld_stream(gv + i), MH = ld_stream(mhv + i), VH = ld_stream(vhv + i);
+                uint2 ML = __ldcs(mlv + i), VL = __ldcs(vlv + i);
+                step8_f24<kSR>(k, has_res, c.tensor, start + 8 * i, W0, R0, G0, MH, ML, VH, VL, nf);
+                st_stream(wv + i, W0);
+                if (has_res) st_stream(rv + i, R0);
+                st_stream(mhv + i, MH);
+                st_stream(vhv + i, VH);
+                __stcs(mlv + i, ML);
+                __stcs(vlv + i, VL);
+            }
+            done = start + (nv << 3);
+        }
+        for (int64_t i = done + threadIdx.x; i < end; i += kThreads) {
+            const float w0 = has_res ? __uint_as_float(((uint32_t)w[i] << 16) | res[i]) : bf16_to_f32(w[i]);
+            float m = f24_value(mhi[i], mlo[i]), v = f24_value(vhi[i], vlo[i]), sv;
+            const float w1 = elem(k, w0, bf16_to_f32(g[i]), m, v, sv);
+            const uint32_t b = __float_as_uint(w1);
+            const uint32_t hi = has_res ? (b >> 16) : (kSR ? sr_bf16(w1, sr_lane1(k, c.tensor, i)) : rne_bf16(w1));
+            w[i] = (uint16_t)hi;
+            if (has_res) res[i] = (uint16_t)(b & 0xFFFFu);
+            nf = max(nf, hi & 0x7FFFu);
+            const uint32_t mb = __float_as_uint(m), vb = __float_as_uint(v);
+            mhi[i] = (uint16_t)(mb >> 16);
+            vhi[i] = (uint16_t)(vb >> 16);
+            mlo[i] = (uint8_t)(mb >> 8);
+            vlo[i] = (uint8_t)(vb >> 8);
+        }
+    } else {
+        float* mf = static_cast<float*>(t.m);
+        float* vf = static_cast<float*>(t.v);
+        for (int64_t i = start + threadIdx.x; i < end; i += kThreads) {
+            const float w0 = has_res ? __uint_as_float(((uint32_t)w[i] << 16) | res[i]) : bf16_to_f32(w[i]);
+            float m = mf[i], v = vf[i], sv;
+            const float w1 = elem(k, w0, bf16_to_f32(g[i]), m, v, sv);
+            const uint32_t b = __float_as_uint(w1);
+            const uint32_t hi = has_res ? (b >> 16) : (kSR ? sr_bf16(w1, sr_lane1(k, c.tensor, i)) : rne_bf16(w1));
+            w[i] = (uint16_t)hi;
+            if (has_res) res[i] = (uint16_t)(b & 0xFFFFu);
+            nf = max(nf, hi & 0x7FFFu);
+            mf[i] = m;
+            vf[i] = v;
+        }
+    }
+    uint32_t r[1] = {(max(nf & 0xFFFFu, nf >> 16) >= 0x7F80u) ? 1u : 0u};
+    block_max_u32<1>(r, red);
+    if (threadIdx.x == 0 && r[0]) atomicAdd(L.nonfinite, 1ull);
+}
+
 }  // namespace
 
 int launch_nadam_step(const NadamLaunch& L, const NadamScalars& s, cudaStream_t stream, cudaEvent_t mid) {
-    Prm k{s.lr, s.b1, s.omb1, s.b2, s.omb2, s.eps, s.lr_wd, s.c_m, s.c_g, s.k2, s.decoupled};
+    Prm k{s.lr, s.b1, s.omb1, s.b2, s.omb2, s.eps, s.lr_wd, s.c_m, s.c_g, s.k2, s.decoupled, s.sr, s.seed, s.step};
+    if (L.f24) {
+        if (mid) {
+            int rc = check_cuda(cudaEventRecord(mid, stream), "profile event");
+            if (rc) return rc;
+        }
+        if (L.n_chunks_total == 0) return OPTIM_OK;
+        if (k.sr) k_nadam_f24<true><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k);
+        else k_nadam_f24<false><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k);
+        return check_cuda(cudaGetLastError(), "nadam f24 step launch");
+    }
     if (L.n_chunks_large > 0) {
         k_grad_absmax<<<L.n_chunks_large, kThreads, 0, stream>>>(L, s.parity);
         int rc = check_cuda(cudaGetLastError(), "grad absmax launch");
@@ -304,7 +508,8 @@ int launch_nadam_step(const NadamLaunch& L, const NadamScalars& s, cudaStream_t 
         if (rc) return rc;
     }
     if (L.n_chunks_total > 0) {
-        k_nadam_step<<<L.n_chunks_total, kThreads, 0, stream>>>(L, k, s.parity);
+        if (k.sr) k_nadam_step<true><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k, s.parity);
+        else k_nadam_step<false><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k, s.parity);
         return check_cuda(cudaGetLastError(), "nadam step launch");
     }
     return OPTIM_OK;

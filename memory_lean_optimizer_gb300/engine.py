@@ -151,13 +151,15 @@ class NadamGroup(_Group):
     kind = lmopt.OPTIM_KIND_NADAM
 
     def __init__(self, weights: Sequence[torch.Tensor], residuals: Sequence[torch.Tensor] | None = None,
-                 kahan: bool = True, offload: OffloadEngine | None = None):
+                 kahan: bool = True, offload: OffloadEngine | None = None, states: str = "u16"):
         super().__init__()
         self.weights = list(weights)
         for w in self.weights:
             assert w.dtype == torch.bfloat16 and w.is_cuda and w.is_contiguous()
         dev = self.weights[0].device
         pinned = offload is not None
+        assert states in ("u16", "f24") and not (pinned and states == "f24")
+        self.kind = lmopt.OPTIM_KIND_NADAM_F24 if states == "f24" else lmopt.OPTIM_KIND_NADAM
         if residuals is None:
             residuals = [_state_buffer(w.numel(), torch.int16, dev, pinned) if kahan else None for w in self.weights]
         elif pinned:
@@ -169,6 +171,9 @@ class NadamGroup(_Group):
             if n <= SMALL:
                 self.m.append(_state_buffer(n, torch.float32, dev, pinned))
                 self.v.append(_state_buffer(n, torch.float32, dev, pinned))
+            elif states == "f24":       # n upper 16-bit words, then n low bytes, all zero
+                self.m.append(torch.zeros(3 * n, dtype=torch.uint8, device=dev))
+                self.v.append(torch.zeros(3 * n, dtype=torch.uint8, device=dev))
             else:
                 self.m.append(_state_buffer(n, torch.int16, dev, pinned, 32768))
                 self.v.append(_state_buffer(n, torch.int16, dev, pinned, 0))
@@ -182,18 +187,20 @@ class NadamGroup(_Group):
         lmopt.optim_offload_prefetch(self.handle)
 
     @classmethod
-    def from_masters(cls, masters: Sequence[torch.Tensor], stream=None, offload: OffloadEngine | None = None):
+    def from_masters(cls, masters: Sequence[torch.Tensor], stream=None, offload: OffloadEngine | None = None,
+                     states: str = "u16"):
         ws, rs = [], []
         for x in masters:
             hi, lo = kahan_split(x.contiguous(), stream=stream)
             ws.append(hi)
             rs.append(lo)
-        return cls(ws, rs, offload=offload)
+        return cls(ws, rs, offload=offload, states=states)
 
     def step(self, grads: Sequence[torch.Tensor], hp: dict, stream=None):
         h = lmopt.NadamHparams(lr=hp["lr"], beta1=hp["beta1"], beta2=hp["beta2"], eps=hp["eps"],
                                weight_decay=hp.get("weight_decay", 0.0), wd_mode=hp.get("wd_mode", 0),
-                               nesterov=hp.get("nesterov", 1), momentum_decay=hp.get("momentum_decay", 0.004))
+                               nesterov=hp.get("nesterov", 1), momentum_decay=hp.get("momentum_decay", 0.004),
+                               stochastic_rounding=hp.get("stochastic_rounding", 0), seed=hp.get("seed", 0))
         lmopt.optim_step_nadam_kahan(self.handle, self._grad_ptrs(grads), self.step_count + 1, h, _stream_ptr(stream))
         self.step_count += 1
 
@@ -245,6 +252,45 @@ class FactoredGroup(_Group):
                                   clip_threshold=hp.get("clip_threshold", 1.0),
                                   weight_decay=hp.get("weight_decay", 0.0), mode=hp.get("mode", 0))
         lmopt.optim_step_factored(self.handle, self._grad_ptrs(grads), self.step_count + 1, h, _stream_ptr(stream))
+        self.step_count += 1
+
+    def masters(self):
+        return [kahan_merge(w, r) for w, r in zip(self.weights, self.res)]
+
+
+class AdanGroup(_Group):
+    """Adan state (fp32 m, v, n planes and the previous bf16 gradient) for a list of bf16 weights."""
+
+    kind = lmopt.OPTIM_KIND_ADAN
+
+    def __init__(self, weights: Sequence[torch.Tensor], residuals: Sequence[torch.Tensor] | None = None,
+                 kahan: bool = True):
+        super().__init__()
+        self.weights = list(weights)
+        dev = self.weights[0].device
+        if residuals is None:
+            residuals = [_u16_empty(w.numel(), dev, 0) if kahan else None for w in self.weights]
+        self.res = list(residuals)
+        self.mvn = [torch.zeros(3 * w.numel(), dtype=torch.float32, device=dev) for w in self.weights]
+        self.gprev = [torch.zeros(w.numel(), dtype=torch.int16, device=dev) for w in self.weights]
+        descs = [_desc(w, r, m, v, w.shape) for w, r, m, v in zip(self.weights, self.res, self.mvn, self.gprev)]
+        self.handle = lmopt.optim_group_create(descs, self.kind)
+
+    @classmethod
+    def from_masters(cls, masters: Sequence[torch.Tensor], stream=None):
+        ws, rs = [], []
+        for x in masters:
+            hi, lo = kahan_split(x.contiguous(), stream=stream)
+            ws.append(hi)
+            rs.append(lo)
+        return cls(ws, rs)
+
+    def step(self, grads: Sequence[torch.Tensor], hp: dict, stream=None):
+        h = lmopt.AdanHparams(lr=hp["lr"], beta1=hp.get("beta1", 0.02), beta2=hp.get("beta2", 0.08),
+                              beta3=hp.get("beta3", 0.01), eps=hp.get("eps", 1e-8),
+                              weight_decay=hp.get("weight_decay", 0.0),
+                              stochastic_rounding=hp.get("stochastic_rounding", 0), seed=hp.get("seed", 0))
+        lmopt.optim_step_adan(self.handle, self._grad_ptrs(grads), self.step_count + 1, h, _stream_ptr(stream))
         self.step_count += 1
 
     def masters(self):

@@ -24,6 +24,8 @@ OPTIM_ENONFINITE = -6
 OPTIM_ESTATE = -7
 OPTIM_KIND_NADAM = 0
 OPTIM_KIND_FACTORED = 1
+OPTIM_KIND_NADAM_F24 = 2
+OPTIM_KIND_ADAN = 3
 SMALL_NUMEL = 4096
 
 ERROR_NAMES = {OPTIM_EINVAL: "EINVAL", OPTIM_ECUDA: "ECUDA", OPTIM_ENOMEM: "ENOMEM", OPTIM_EALIGN: "EALIGN",
@@ -34,6 +36,7 @@ EXPORTED = (
     "state_pack_u16", "state_unpack_u16", "optim_kahan_split", "optim_kahan_merge",
     "optim_query_scales", "optim_set_scales", "optim_group_get_step", "optim_group_set_step",
     "optim_query_nonfinite", "optim_group_set_profile_event", "optim_last_error",
+    "optim_step_adan",
     "optim_offload_create", "optim_offload_destroy", "optim_group_attach_offload",
     "optim_offload_prefetch", "optim_offload_sync",
 )
@@ -54,7 +57,14 @@ class TensorDesc(ctypes.Structure):
 class NadamHparams(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
                 ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("wd_mode", ctypes.c_int32),
-                ("nesterov", ctypes.c_int32), ("momentum_decay", ctypes.c_float)]
+                ("nesterov", ctypes.c_int32), ("momentum_decay", ctypes.c_float),
+                ("stochastic_rounding", ctypes.c_int32), ("seed", ctypes.c_uint64)]
+
+
+class AdanHparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("beta3", ctypes.c_float), ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float),
+                ("stochastic_rounding", ctypes.c_int32), ("reserved", ctypes.c_int32), ("seed", ctypes.c_uint64)]
 
 
 class FactoredHparams(ctypes.Structure):
@@ -83,6 +93,7 @@ def load(path: str = LIB_PATH):
             "optim_group_destroy": [P],
             "optim_step_nadam_kahan": [P, P, I64, ctypes.POINTER(NadamHparams), P],
             "optim_step_factored": [P, P, I64, ctypes.POINTER(FactoredHparams), P],
+            "optim_step_adan": [P, P, I64, ctypes.POINTER(AdanHparams), P],
             "state_pack_u16": [P, P, P, I64, I32, P],
             "state_unpack_u16": [P, P, P, I64, I32, P],
             "optim_kahan_split": [P, P, P, I64, P],
@@ -145,6 +156,10 @@ def optim_step_nadam_kahan(handle: int, grad_ptrs, step: int, hp: NadamHparams, 
 
 def optim_step_factored(handle: int, grad_ptrs, step: int, hp: FactoredHparams, stream: int = 0) -> None:
     check(load().optim_step_factored(handle, _ptr_array(grad_ptrs), step, ctypes.byref(hp), stream))
+
+
+def optim_step_adan(handle: int, grad_ptrs, step: int, hp: AdanHparams, stream: int = 0) -> None:
+    check(load().optim_step_adan(handle, _ptr_array(grad_ptrs), step, ctypes.byref(hp), stream))
 
 
 def state_pack_u16(src: int, codes: int, scale: int, n: int, is_signed: bool, stream: int = 0) -> None:

@@ -110,6 +110,10 @@ def config(name: str):
                     hp=dict(lr=2e-6, beta2=0.999, decay_rate=-0.8, eps1=1e-30, eps2=1e-30, d=1.0,
                             clip_threshold=1.0, weight_decay=0.0, mode=0),
                     steps=5, g_std=1e-4, zero_frac=0.0, seed=0)
+    if name == "sdxl_like_4":   # the first 4 groups of sdxl_like: the factored profiling case
+        c = config("sdxl_like")
+        c["groups"] = c["groups"][:4]
+        return c
     if name == "flux35":
         return dict(kind="nadam", groups=flux_shapes(35), hp=dict(NADAM_HP), steps=3, g_std=1e-4,
                     zero_frac=0.0, seed=0)

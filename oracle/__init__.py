@@ -60,6 +60,10 @@ class CodecConsts(ctypes.Structure):
     _fields_ = [(n, ctypes.c_float) for n in ("qm", "rm", "qv", "rv")]
 
 
+class AdanScalars(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_float) for n in ("lr", "b1", "omb1", "b2", "omb2", "b3", "omb3", "eps", "inv_decay")]
+
+
 class FactoredScalars(ctypes.Structure):
     _fields_ = [(n, ctypes.c_float) for n in
                 ("b2t", "alpha", "eps1", "eps2", "clip", "lr_eff", "nwdlr")] + \
@@ -93,6 +97,16 @@ def _load():
             "orc_nadam_step_tensor": (None, [P, P, P, P, P, I64, ctypes.POINTER(Scale),
                                              ctypes.POINTER(NadamScalars)]),
             "orc_nadam_step_fp32": (None, [P, P, P, P, I64, ctypes.POINTER(NadamScalars)]),
+            "orc_nadam_step_tensor_f24": (None, [P, P, P, P, P, I64, ctypes.POINTER(NadamScalars), I32,
+                                                 ctypes.c_uint64, ctypes.c_uint32, I64]),
+            "orc_philox4x64_10": (None, [P, P, P]),
+            "orc_adan_scalars": (None, [F, F, F, F, F, F, ctypes.POINTER(AdanScalars)]),
+            "orc_adan_step_tensor": (None, [P, P, P, P, P, I64, I64, ctypes.POINTER(AdanScalars), I32,
+                                            ctypes.c_uint64, ctypes.c_uint32]),
+            "orc_sr_bits": (ctypes.c_uint32, [ctypes.c_uint64, ctypes.c_uint32, I64, I64]),
+            "orc_stochastic_round": (None, [P, P, I64, ctypes.c_uint64, ctypes.c_uint32, I64]),
+            "orc_nadam_step_tensor_sr": (None, [P, P, P, P, I64, ctypes.POINTER(Scale), ctypes.POINTER(NadamScalars),
+                                                ctypes.c_uint64, ctypes.c_uint32, I64]),
             "orc_factored_scalars": (None, [I64, F, F, F, F, F, F, F, F, I32,
                                             ctypes.POINTER(FactoredScalars)]),
             "orc_factored_step_tensor": (F, [P, P, P, I64, I64, I64, P, P,
@@ -216,6 +230,65 @@ def nadam_step_tensor(hi, lo, m, v, g, scale: Scale, k: NadamScalars):
     n = hi.size
     _load().orc_nadam_step_tensor(_p(hi), _p(lo), _p(m), _p(v), _p(_u16(g)), n,
                                   ctypes.byref(scale), ctypes.byref(k))
+
+
+def nadam_step_tensor_f24(hi, lo, m, v, g, k: NadamScalars, sr=False, seed=0, tensor=0, step=0):
+    """f24 moments: m, v are uint8 buffers of 3n bytes (n uint16 upper words, then n low bytes),
+    or float32 arrays when n <= 4096.  sr (lo None): stochastic rounding of the weight."""
+    _load().orc_nadam_step_tensor_f24(_p(hi), _p(lo), _p(m), _p(v), _p(_u16(g)), hi.size, ctypes.byref(k),
+                                      int(sr), seed, tensor, step)
+
+
+def philox4x64_10(ctr, key):
+    c = np.ascontiguousarray(ctr, np.uint64)
+    k = np.ascontiguousarray(key, np.uint64)
+    out = np.zeros(4, np.uint64)
+    _load().orc_philox4x64_10(_p(c), _p(k), _p(out))
+    return out
+
+
+def sr_bits(seed, tensor, step, i) -> int:
+    return _load().orc_sr_bits(seed, tensor, step, i)
+
+
+def stochastic_round(x: np.ndarray, seed: int, tensor: int, step: int) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, np.uint16)
+    _load().orc_stochastic_round(_p(x), _p(out), x.size, seed, tensor, step)
+    return out
+
+
+def nadam_step_tensor_sr(hi, m, v, g, scale: Scale, k: NadamScalars, seed: int, tensor: int, step: int):
+    _load().orc_nadam_step_tensor_sr(_p(hi), _p(m), _p(v), _p(_u16(g)), hi.size, ctypes.byref(scale),
+                                     ctypes.byref(k), seed, tensor, step)
+
+
+def adan_scalars(lr, b1, b2, b3, eps, wd) -> AdanScalars:
+    k = AdanScalars()
+    _load().orc_adan_scalars(lr, b1, b2, b3, eps, wd, ctypes.byref(k))
+    return k
+
+
+def adan_step_tensor(hi, lo, mnv, gprev, g, step, k: AdanScalars, sr=False, seed=0, tensor=0):
+    """In place: hi/lo uint16 (lo may be None), mnv float32 [3n] (m, v, n planes), gprev uint16."""
+    _load().orc_adan_step_tensor(_p(hi), _p(lo), _p(mnv), _p(gprev), _p(_u16(g)), hi.size, int(step),
+                                 ctypes.byref(k), int(sr), seed, tensor)
+
+
+def f24_split(x: np.ndarray) -> np.ndarray:
+    """fp32 values -> 3n-byte f24 buffer (upper 16 bits plane, then bits 8..15 plane)."""
+    b = np.ascontiguousarray(x, np.float32).view(np.uint32).reshape(-1)
+    out = np.empty(3 * b.size, np.uint8)
+    out[:2 * b.size].view(np.uint16)[:] = (b >> 16).astype(np.uint16)
+    out[2 * b.size:] = ((b >> 8) & 0xFF).astype(np.uint8)
+    return out
+
+
+def f24_merge(buf: np.ndarray) -> np.ndarray:
+    n = buf.size // 3
+    hi = buf[:2 * n].view(np.uint16).astype(np.uint32)
+    lo = buf[2 * n:].astype(np.uint32)
+    return ((hi << 16) | (lo << 8)).view(np.float32)
 
 
 def nadam_step_fp32(w, m, v, g, k: NadamScalars):

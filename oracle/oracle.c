@@ -43,6 +43,9 @@
 
 #define ORC_SMALL_NUMEL 4096
 
+uint32_t orc_sr_bits(uint64_t seed, uint32_t tensor, int64_t step, int64_t i);
+static uint16_t sr_bf16(float x, uint32_t r16);
+
 /* ----------------------------------------------------------------------------------------
  * bit helpers
  * -------------------------------------------------------------------------------------- */
@@ -298,6 +301,239 @@ void orc_nadam_step_tensor(uint16_t* hi, uint16_t* lo, void* m, void* v, const u
         sc->s_v = s_v;
         sc->a_m = am;
         sc->a_v = av;
+    }
+}
+
+/* ----------------------------------------------------------------------------------------
+ * f24 moment storage ("f24 is the upper three bytes [of f32] - i.e. with 8 more bits of
+ * mantissa ... it can only be used for storage rather than operations", sd-scripts PR #2187,
+ * third post).  Reading: the stored value is the f32 pattern truncated to its upper 24 bits
+ * (like the Kahan split); decode appends a zero byte.  Layout per moment buffer of n elements:
+ * n uint16 words of the upper 16 bits, then n bytes of bits 8..15.  No scale is needed, so no
+ * gradient maximum either.  Tensors of 4096 or fewer elements keep fp32 moments as before.
+ * -------------------------------------------------------------------------------------- */
+static float f24_load(const uint8_t* buf, int64_t n, int64_t i)
+{
+    const uint16_t* hi = (const uint16_t*)buf;
+    const uint8_t* lo = buf + 2 * n;
+    return f_of(((uint32_t)hi[i] << 16) | ((uint32_t)lo[i] << 8));
+}
+
+static void f24_store(uint8_t* buf, int64_t n, int64_t i, float x)
+{
+    uint16_t* hi = (uint16_t*)buf;
+    uint8_t* lo = buf + 2 * n;
+    uint32_t b = b_of(x);
+    hi[i] = (uint16_t)(b >> 16);
+    lo[i] = (uint8_t)((b >> 8) & 0xFFu);
+}
+
+/* sr != 0 (and lo == NULL): the new weight is stochastically rounded (see orc_sr_bits below). */
+void orc_nadam_step_tensor_f24(uint16_t* hi, uint16_t* lo, void* m, void* v, const uint16_t* g,
+                               int64_t n, const orc_nadam_scalars_t* k, int32_t sr, uint64_t seed,
+                               uint32_t tensor, int64_t step)
+{
+    int small = n <= ORC_SMALL_NUMEL;
+    for (int64_t i = 0; i < n; ++i) {
+        float w = lo ? f_of(((uint32_t)hi[i] << 16) | lo[i]) : bf16_to_f32(hi[i]);
+        float gg = bf16_to_f32(g[i]);
+        float mm = small ? ((float*)m)[i] : f24_load((const uint8_t*)m, n, i);
+        float vv = small ? ((float*)v)[i] : f24_load((const uint8_t*)v, n, i);
+        float sv;
+        w = nadam_elem(w, gg, &mm, &vv, &sv, k);
+        if (lo) {
+            uint32_t b = b_of(w);
+            hi[i] = (uint16_t)(b >> 16);
+            lo[i] = (uint16_t)(b & 0xFFFFu);
+        } else if (sr) {
+            hi[i] = sr_bf16(w, orc_sr_bits(seed, tensor, step, i));
+        } else {
+            hi[i] = rne_bf16(w);
+        }
+        if (small) {
+            ((float*)m)[i] = mm;
+            ((float*)v)[i] = vv;
+        } else {
+            f24_store((uint8_t*)m, n, i, mm);
+            f24_store((uint8_t*)v, n, i, vv);
+        }
+    }
+}
+
+/* ----------------------------------------------------------------------------------------
+ * Stochastic rounding of the fp32 master to bf16, in place of the Kahan residual ("stochastic
+ * rounding ... randomly moving the value either up or down to the next rounded bfloat16 value,
+ * depending on the distance", "Kahan summation for Adafactor-optimized Flux FFT", sd-scripts
+ * PR #2159, PR description).  Reading: add 16 uniform random bits to the f32 pattern and keep
+ * the upper half, which rounds the magnitude up with probability (low 16 bits)/65536.
+ * Random bits: Philox4x64-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as
+ * 1, 2, 3", SC 2011), key (seed, tensor index), counter (element index / 16, step, 0, 0); element
+ * i takes 16-bit lane i mod 16 of the 256-bit block (lanes low to high within each 64-bit word).
+ * -------------------------------------------------------------------------------------- */
+static void mulhilo64(uint64_t a, uint64_t b, uint64_t* hi, uint64_t* lo)
+{
+    unsigned __int128 p = (unsigned __int128)a * (unsigned __int128)b;
+    *hi = (uint64_t)(p >> 64);
+    *lo = (uint64_t)p;
+}
+
+void orc_philox4x64_10(const uint64_t ctr_in[4], const uint64_t key_in[2], uint64_t out[4])
+{
+    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+    uint64_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint64_t k0 = key_in[0], k1 = key_in[1];
+    for (int r = 0; r < 10; ++r) {
+        uint64_t hi0, lo0, hi1, lo1;
+        mulhilo64(M0, c0, &hi0, &lo0);
+        mulhilo64(M1, c2, &hi1, &lo1);
+        uint64_t n0 = hi1 ^ c1 ^ k0, n1 = lo1, n2 = hi0 ^ c3 ^ k1, n3 = lo0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+        k0 += W0;
+        k1 += W1;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+uint32_t orc_sr_bits(uint64_t seed, uint32_t tensor, int64_t step, int64_t i)
+{
+    uint64_t ctr[4] = {(uint64_t)i >> 4, (uint64_t)step, 0, 0}, key[2] = {seed, tensor}, out[4];
+    orc_philox4x64_10(ctr, key, out);
+    int lane = (int)(i & 15);
+    return (uint32_t)((out[lane >> 2] >> (16 * (lane & 3))) & 0xFFFFu);
+}
+
+static uint16_t sr_bf16(float x, uint32_t r16)
+{
+    uint32_t b = b_of(x);
+    if ((b & 0x7F800000u) == 0x7F800000u) return (uint16_t)(b >> 16);   /* inf / NaN kept */
+    return (uint16_t)((b + r16) >> 16);
+}
+
+void orc_stochastic_round(const float* x, uint16_t* out, int64_t n, uint64_t seed, uint32_t tensor, int64_t step)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = sr_bf16(x[i], orc_sr_bits(seed, tensor, step, i));
+}
+
+/* NAdam/Adam step without a residual, the new fp32 weight stochastically rounded to bf16
+ * (u16 or fp32 moments as in orc_nadam_step_tensor). */
+void orc_nadam_step_tensor_sr(uint16_t* hi, void* m, void* v, const uint16_t* g, int64_t n,
+                              orc_scale_t* sc, const orc_nadam_scalars_t* k, uint64_t seed,
+                              uint32_t tensor, int64_t step)
+{
+    /* the update itself is the no-residual step; only the final store differs */
+    int small = n <= ORC_SMALL_NUMEL;
+    float s_m = 0.0f, s_v = 0.0f;
+    orc_codec_t dec, enc;
+    if (!small) {
+        float G = orc_grad_absmax(g, n);
+        s_m = fmaf(k->b1, sc->a_m, k->omb1 * G);
+        s_v = fmaf(k->b2, sc->a_v, k->omb2 * (G * G));
+        orc_codec_consts(sc->s_m, sc->s_v, &dec);
+        orc_codec_consts(s_m, s_v, &enc);
+    }
+    float am = 0.0f, av = 0.0f;
+    uint16_t* mc = (uint16_t*)m;
+    uint16_t* vc = (uint16_t*)v;
+    float* mf = (float*)m;
+    float* vf = (float*)v;
+    for (int64_t i = 0; i < n; ++i) {
+        float w = bf16_to_f32(hi[i]);
+        float gg = bf16_to_f32(g[i]);
+        float mm = small ? mf[i] : orc_decode_m(mc[i], dec.qm);
+        float vv = small ? vf[i] : orc_decode_v(vc[i], dec.qv);
+        float sv;
+        w = nadam_elem(w, gg, &mm, &vv, &sv, k);
+        hi[i] = sr_bf16(w, orc_sr_bits(seed, tensor, step, i));
+        if (small) {
+            mf[i] = mm;
+            vf[i] = vv;
+        } else {
+            mc[i] = orc_encode_m(mm, enc.rm);
+            vc[i] = orc_encode_v(sv, enc.rv);
+            am = fmaxf(am, fabsf(mm));
+            av = fmaxf(av, vv);
+        }
+    }
+    if (!small) {
+        sc->s_m = s_m;
+        sc->s_v = s_v;
+        sc->a_m = am;
+        sc->a_v = av;
+    }
+}
+
+/* ----------------------------------------------------------------------------------------
+ * Adan ("a cpu-offloading version of ADAN ... needs four optimizer parameters for each model
+ * parameter", sd-scripts PR #2187, fourth post; Algorithm 1 of the linked paper, arXiv
+ * 2208.06677, with its convention that beta weights the new term):
+ *   d = g - g_prev
+ *   m = (1-b1) m + b1 g;  v = (1-b2) v + b2 d;  n = (1-b3) n + b3 (g + (1-b2) d)^2
+ *   w = (w - lr (m + (1-b2) v) / (sqrt(n) + eps)) / (1 + lr wd)
+ * Readings: the first step initialises m = g, v = 0, n = g^2 (zero difference), the second sets
+ * v = d exactly (the paper's v_1 = g_1 - g_0); states m, v, n fp32 (the pages leave their
+ * compression unspecified) and g_prev the previous bf16 gradient.  Per element, fma = one rounding:
+ *   m  = fma(omb1, m, b1 g);  v = fma(omb2, v, b2 d);  c = fma(omb2, d, g);  n = fma(omb3, n, b3 (c c))
+ *   den = sqrt(n) + eps;  u = fma(omb2, v, m);  w = (w - lr (u / den)) * inv_decay
+ * with inv_decay = 1/(1 + lr wd) computed once per step in double.
+ * mnv: fp32 [3n] planes m, v, n; gprev: bf16 bits [n].
+ * -------------------------------------------------------------------------------------- */
+typedef struct {
+    float lr, b1, omb1, b2, omb2, b3, omb3, eps, inv_decay;
+} orc_adan_scalars_t;
+
+void orc_adan_scalars(float lr, float b1, float b2, float b3, float eps, float wd, orc_adan_scalars_t* k)
+{
+    k->lr = lr;
+    k->b1 = b1;
+    k->omb1 = (float)(1.0 - (double)b1);
+    k->b2 = b2;
+    k->omb2 = (float)(1.0 - (double)b2);
+    k->b3 = b3;
+    k->omb3 = (float)(1.0 - (double)b3);
+    k->eps = eps;
+    k->inv_decay = (float)(1.0 / (1.0 + (double)lr * (double)wd));
+}
+
+void orc_adan_step_tensor(uint16_t* hi, uint16_t* lo, float* mnv, uint16_t* gprev, const uint16_t* g,
+                          int64_t n, int64_t step, const orc_adan_scalars_t* k, int32_t sr, uint64_t seed,
+                          uint32_t tensor)
+{
+    float* m = mnv;
+    float* v = mnv + n;
+    float* nn = mnv + 2 * n;
+    for (int64_t i = 0; i < n; ++i) {
+        float w = lo ? f_of(((uint32_t)hi[i] << 16) | lo[i]) : bf16_to_f32(hi[i]);
+        float gg = bf16_to_f32(g[i]);
+        float gp = bf16_to_f32(gprev[i]);
+        float d = gg - gp;
+        float mm, vv, n2;
+        if (step == 1) {
+            mm = gg;
+            vv = 0.0f;
+            n2 = gg * gg;
+        } else {
+            mm = fmaf(k->omb1, m[i], k->b1 * gg);
+            vv = step == 2 ? d : fmaf(k->omb2, v[i], k->b2 * d);
+            float c = fmaf(k->omb2, d, gg);
+            n2 = fmaf(k->omb3, nn[i], k->b3 * (c * c));
+        }
+        float den = sqrtf(n2) + k->eps;
+        float u = fmaf(k->omb2, vv, mm);
+        w = (w - k->lr * (u / den)) * k->inv_decay;
+        m[i] = mm;
+        v[i] = vv;
+        nn[i] = n2;
+        gprev[i] = g[i];
+        if (lo) {
+            uint32_t b = b_of(w);
+            hi[i] = (uint16_t)(b >> 16);
+            lo[i] = (uint16_t)(b & 0xFFFFu);
+        } else if (sr) {
+            hi[i] = sr_bf16(w, orc_sr_bits(seed, tensor, step, i));
+        } else {
+            hi[i] = rne_bf16(w);
+        }
     }
 }
 

@@ -187,3 +187,77 @@ def test_deterministic_two_runs(eng):
     for a, b in zip(*outs):
         assert torch.equal(a.view(torch.int32) if a.dtype == torch.float32 else a,
                            b.view(torch.int32) if b.dtype == torch.float32 else b)
+
+
+@pytest.mark.parametrize("variant", ["nadamw", "adam"])
+def test_f24_moments_bit_exact(orc, eng, variant):
+    """f24 moment storage (NADAM_F24 groups): weights, residuals and both moment planes
+    bit-identical to the oracle; sizes include fp32-moment tensors, ragged tails and byte planes
+    that are not 8-byte aligned (element-by-element path)."""
+    sizes = [100, 4096, 4097, 16384, 16389, 40000, 131072]
+    seed = 21
+    hp = dict(HP, lr=1e-3, nesterov=variant.startswith("n"), weight_decay=0.02 if variant.endswith("w") else 0.0,
+              wd_mode=1 if variant.endswith("w") else 0)
+    masters = [W.master_weights((n,), seed, i) for i, n in enumerate(sizes)]
+    ora = []
+    for x in masters:
+        hi, lo = orc.kahan_split(x.numpy())
+        n = x.numel()
+        st = (np.zeros(n, np.float32), np.zeros(n, np.float32)) if n <= 4096 else (np.zeros(3 * n, np.uint8), np.zeros(3 * n, np.uint8))
+        ora.append(dict(hi=hi, lo=lo, m=st[0], v=st[1]))
+    grp = eng.NadamGroup.from_masters([m.cuda() for m in masters], states="f24")
+    mp = 1.0
+    for t in range(1, 5):
+        grads = [W.grad_bf16((n,), seed, i, t, 1e-3, zero_frac=0.01) for i, n in enumerate(sizes)]
+        k, mp = orc.nadam_scalars(t, hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"],
+                                  hp["wd_mode"] == 1, hp["nesterov"], hp["momentum_decay"], mp)
+        for o, g in zip(ora, grads):
+            orc.nadam_step_tensor_f24(o["hi"], o["lo"], o["m"], o["v"], W.bits16(g), k)
+        grp.step([g.cuda() for g in grads], hp)
+    torch.cuda.synchronize()
+    for i, o in enumerate(ora):
+        assert np.array_equal(cuda_bits(grp.weights[i]), o["hi"]), i
+        assert np.array_equal(cuda_bits(grp.res[i]), o["lo"]), i
+        if sizes[i] <= 4096:
+            assert np.array_equal(grp.m[i].cpu().numpy().view(np.uint32), o["m"].view(np.uint32))
+            assert np.array_equal(grp.v[i].cpu().numpy().view(np.uint32), o["v"].view(np.uint32))
+        else:
+            assert np.array_equal(grp.m[i].cpu().numpy(), o["m"]), i
+            assert np.array_equal(grp.v[i].cpu().numpy(), o["v"]), i
+
+
+@pytest.mark.parametrize("states", ["u16", "f24"])
+def test_stochastic_rounding_bit_exact(orc, eng, states):
+    """Tensors without a residual and stochastic_rounding = 1: the stored bf16 weights follow the
+    oracle's Philox4x64-10 draws bit for bit (vector and element-by-element paths)."""
+    sizes = [300, 4097, 16384, 20003, 65536]
+    seed, key = 23, 0xDEADBEEF12345
+    hp = dict(HP, lr=1e-3, stochastic_rounding=1, seed=key)
+    masters = [W.master_weights((n,), seed, i) for i, n in enumerate(sizes)]
+    w0 = [m.to(torch.bfloat16) for m in masters]
+    grp = eng.NadamGroup([w.cuda() for w in w0], kahan=False, states=states)
+    ora = []
+    for w in w0:
+        n = w.numel()
+        hi = W.bits16(w).copy()
+        if n <= 4096:
+            st = (np.zeros(n, np.float32), np.zeros(n, np.float32))
+        elif states == "u16":
+            st = (np.full(n, 32768, np.uint16), np.zeros(n, np.uint16))
+        else:
+            st = (np.zeros(3 * n, np.uint8), np.zeros(3 * n, np.uint8))
+        ora.append(dict(hi=hi, m=st[0], v=st[1]))
+    ost = orc.NadamState(len(sizes))
+    mp = 1.0
+    for t in range(1, 4):
+        grads = [W.grad_bf16((n,), seed, i, t, 1e-3) for i, n in enumerate(sizes)]
+        k, mp = orc.nadam_scalars(t, hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], 0.0, False, True, 0.004, mp)
+        for i, (o, g) in enumerate(zip(ora, grads)):
+            if states == "u16":
+                orc.nadam_step_tensor_sr(o["hi"], o["m"], o["v"], W.bits16(g), ost.scales[i], k, key, i, t)
+            else:
+                orc.nadam_step_tensor_f24(o["hi"], None, o["m"], o["v"], W.bits16(g), k, True, key, i, t)
+        grp.step([g.cuda() for g in grads], hp)
+        torch.cuda.synchronize()
+        for i, o in enumerate(ora):
+            assert np.array_equal(cuda_bits(grp.weights[i]), o["hi"]), (t, i)

@@ -1,0 +1,64 @@
+"""Pins of the oracle's Adan step (Algorithm 1 of the Adan paper the pages link, fp32 states):
+closed forms for constant and two-valued gradient sequences, and the decay factor."""
+import numpy as np
+
+from test_oracle_nadam import bf16_bits, bits_to_f32
+
+B1, B2, B3 = 0.02, 0.08, 0.01
+
+
+def run(orc, w0, grads, lr, wd=0.0, eps=0.0):
+    n = w0.size
+    hi, lo = orc.kahan_split(w0)
+    mnv = np.zeros(3 * n, np.float32)
+    gp = np.zeros(n, np.uint16)
+    k = orc.adan_scalars(lr, B1, B2, B3, eps, wd)
+    for t, g in enumerate(grads, start=1):
+        orc.adan_step_tensor(hi, lo, mnv, gp, g, t, k)
+    return orc.kahan_merge(hi, lo).astype(np.float64), mnv, gp
+
+
+def test_constant_gradient_moves_by_lr_sign():
+    """Constant g: the difference is zero, so v = 0, m = g, n = g^2 at every step and each step
+    is exactly w - lr sign(g) (eps = 0, no decay)."""
+    import oracle as orc
+    rng = np.random.default_rng(40)
+    n = 2000
+    g = bf16_bits(rng.choice([-1.0, 1.0], n) * 2.0 ** rng.integers(-12, -4, n))
+    lr = 2.0 ** -10
+    w, mnv, gp = run(orc, np.zeros(n, np.float32), [g] * 6, lr)
+    assert np.array_equal(w, -6 * lr * np.sign(bits_to_f32(g)))
+    assert np.array_equal(mnv[:n], bits_to_f32(g)) and np.all(mnv[n:2 * n] == 0)
+    assert np.array_equal(gp, g)
+
+
+def test_two_gradients_closed_form():
+    """g1 then g2: step 1 moves by -lr sign(g1); step 2 uses m = (1-b1) g1 + b1 g2, v = g2 - g1,
+    n = (1-b3) g1^2 + b3 (g2 + (1-b2)(g2 - g1))^2 (computed here in float64)."""
+    import oracle as orc
+    rng = np.random.default_rng(41)
+    n = 3000
+    g1 = bf16_bits(rng.standard_normal(n) * 1e-3)
+    g2 = bf16_bits(rng.standard_normal(n) * 1e-3)
+    a, b = bits_to_f32(g1).astype(np.float64), bits_to_f32(g2).astype(np.float64)
+    lr, eps = 1e-3, 1e-8
+    w, _, _ = run(orc, np.zeros(n, np.float32), [g1, g2], lr, eps=eps)
+    w1 = -lr * a / (np.abs(a) + eps)
+    m = (1 - B1) * a + B1 * b
+    v = b - a
+    nn = (1 - B3) * a * a + B3 * (b + (1 - B2) * (b - a)) ** 2
+    expect = w1 - lr * (m + (1 - B2) * v) / (np.sqrt(nn) + eps)
+    # two steps of size ~lr each: fp32 rounding of each is a few ulps of lr (the sum may cancel)
+    assert np.all(np.abs(w - expect) <= 2e-6 * lr)
+
+
+def test_decay_only():
+    import oracle as orc
+    rng = np.random.default_rng(42)
+    n = 1000
+    w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    z = np.zeros(n, np.uint16)
+    lr, wd = 1e-2, 0.1
+    w, _, _ = run(orc, w0, [z] * 5, lr, wd=wd, eps=1e-8)
+    expect = w0.astype(np.float64) / (1 + lr * wd) ** 5
+    assert np.all(np.abs(w - expect) <= 5 * np.spacing(np.abs(w0)))
