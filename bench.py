@@ -48,6 +48,8 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="flux19")
     p.add_argument("--states", default="u16", choices=["u16", "f24"], help="moment storage of NAdam workloads")
+    p.add_argument("--optimizer", default="nadam", choices=["nadam", "adan"],
+                   help="adan: fp32 m, v, n + previous gradient, Kahan residual (38 B/param)")
     p.add_argument("--rounding", default="kahan", choices=["kahan", "sr"],
                    help="kahan: bf16 weight + u16 residual; sr: no residual, stochastic rounding")
     p.add_argument("--no-e2e", action="store_true")
@@ -510,6 +512,58 @@ def run_offload(args, cfg):
     return 0
 
 
+def run_adan(args, cfg):
+    """Adan over the NAdam workload's tensors (flux19 by default): one kernel per group call."""
+    import torch
+    from memory_lean_optimizer_gb300 import build, engine, lmopt, workloads as W
+    world, rank, local = dist_info()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    build.build()
+    lmopt.load()
+    groups, grads, params, tid = [], [], 0, 0
+    for shapes in cfg["groups"]:
+        masters = [W.master_weights(s, cfg["seed"], tid + i, device=device) for i, s in enumerate(shapes)]
+        grads.append([W.grad_bf16(s, cfg["seed"], tid + i, 1, cfg["g_std"], device=device) for i, s in enumerate(shapes)])
+        groups.append(engine.AdanGroup.from_masters(masters))
+        params += sum(W.numel(s) for s in shapes)
+        tid += len(shapes)
+        del masters
+    hp = dict(lr=3.3e-5, beta1=0.02, beta2=0.08, beta3=0.01, eps=1e-8, weight_decay=0.02)
+    stream = torch.cuda.current_stream()
+
+    def one_step():
+        for g, gs in zip(groups, grads):
+            g.step(gs, hp, stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    start.record(stream)
+    for _ in range(args.steps):
+        one_step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    step_s = start.elapsed_time(end) / 1e3 / args.steps
+    peak, src = peaks()
+    gbs = 38 * params / step_s / 1e9
+    print(json.dumps({
+        "metric": METRIC, "value": params / step_s, "unit": "params/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * step_s, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "params": params, "optimizer": "Adan + Kahan, fp32 m/v/n + previous bf16 grad"},
+        "roofline": {"bound": "hbm", "kernel": "k_adan_step", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                     "frac": gbs / peak, "traffic": None, "peak_source": src, "bytes_per_param": 38},
+        "gpu_launches": len(groups) * args.steps, "clocks": clk}), flush=True)
+    for g in groups:
+        g.close()
+    return 0
+
+
 def factored_bytes(shape):
     """Algorithmic HBM bytes of one factored step of a tensor: g read once (2 B/elem), weight and
     residual read and written (8 B/elem), fp32 statistics read and written."""
@@ -597,6 +651,8 @@ def main():
         return run_offload(args, cfg)
     if cfg["kind"] == "factored":
         return run_factored(args, cfg)
+    if args.optimizer == "adan":
+        return run_adan(args, cfg)
     return run_ours(args, cfg)
 
 

@@ -312,7 +312,10 @@ __global__ void __launch_bounds__(kThreads) k_stats(Dev D, const Item* items, K 
         const int64_t b = it.x;
         const int64_t col0 = (int64_t)it.cb * kTC + lane * 8;
         const int ncols = cols_in(t.C - col0);
-        const bool vec = aligned16(g) && (t.C % 8 == 0) && ncols == 8;
+        // The branch below must be the same for every lane: both sides contain full-warp
+        // shuffles.  With C a multiple of 8 a lane's group is either whole (8) or empty (0).
+        const bool vec = aligned16(g) && (t.C % 8 == 0);
+        const bool lane_ok = ncols == 8;
         const int64_t row0 = (int64_t)it.band * kTR + warp;
         float cacc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         if (vec) {
@@ -321,21 +324,24 @@ __global__ void __launch_bounds__(kThreads) k_stats(Dev D, const Item* items, K 
 #pragma unroll
             for (int kk = 0; kk < kTR / 8; ++kk) {
                 const int64_t row = row0 + 8 * kk;
-                x[kk] = row < t.R ? __ldcg(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0))
-                                  : make_uint4(0, 0, 0, 0);
+                x[kk] = (row < t.R && lane_ok)
+                            ? __ldcg(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0))
+                            : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int kk = 0; kk < kTR / 8; ++kk) {
                 const int64_t row = row0 + 8 * kk;
                 const uint32_t wd[4] = {x[kk].x, x[kk].y, x[kk].z, x[kk].w};
                 float rs = 0.f;
+                if (lane_ok && row < t.R) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float q = qval(__uint_as_float((j & 1) ? (wd[j >> 1] & 0xFFFF0000u) : (wd[j >> 1] << 16)), k);
-                    rs = __fadd_rn(rs, q);
-                    if (row < t.R) cacc[j] = __fadd_rn(cacc[j], q);
+                    for (int j = 0; j < 8; ++j) {
+                        const float q = qval(__uint_as_float((j & 1) ? (wd[j >> 1] & 0xFFFF0000u) : (wd[j >> 1] << 16)), k);
+                        rs = __fadd_rn(rs, q);
+                        cacc[j] = __fadd_rn(cacc[j], q);
+                    }
                 }
-                rs = warp_sum_f32(rs);
+                rs = warp_sum_f32(rs);   // every lane of the warp, every iteration
                 if (lane == 0 && row < t.R) D.rowpart[t.rowpart_off + (b * t.R + row) * t.ncb + it.cb] = rs;
             }
         } else {
@@ -463,7 +469,8 @@ __global__ void __launch_bounds__(kThreads) k_rms(Dev D, const Item* items, K k)
     const int64_t b = it.x;
     const int64_t col0 = (int64_t)it.cb * kTC + lane * 8;
     const int ncols = cols_in(t.C - col0);
-    const bool vec = aligned16(g) && (t.C % 8 == 0) && ncols == 8;
+    const bool vec = aligned16(g) && (t.C % 8 == 0);      // same for every lane of the block
+    const bool lane_ok = ncols == 8;                       // C % 8 == 0: 8 or 0 columns
     const float rbar = D.rbar[t.mat_off + b];
     const int64_t row0 = (int64_t)it.band * kTR + warp;
     float ccv[8];
@@ -475,13 +482,13 @@ __global__ void __launch_bounds__(kThreads) k_rms(Dev D, const Item* items, K k)
 #pragma unroll
         for (int kk = 0; kk < kTR / 8; ++kk) {
             const int64_t row = row0 + 8 * kk;
-            x[kk] = row < t.R ? __ldcg(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0))
-                              : make_uint4(0, 0, 0, 0);
+            x[kk] = (row < t.R && lane_ok) ? __ldcg(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0))
+                                           : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int kk = 0; kk < kTR / 8; ++kk) {
             const int64_t row = row0 + 8 * kk;
-            if (row >= t.R) break;
+            if (row >= t.R || !lane_ok) break;
             const float rr = rsqrt_rn(__fdiv_rn(t.row[b * t.R + row], rbar));
             const uint32_t wd[4] = {x[kk].x, x[kk].y, x[kk].z, x[kk].w};
 #pragma unroll
@@ -805,4 +812,3 @@ int launch_factored_step(const FactoredPlan* p, const uint16_t* const* d_grads, 
 }
 
 }  // namespace lmo
-
