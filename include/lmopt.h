@@ -149,6 +149,24 @@ int optim_step_nadam_kahan(optim_group_t* group, const void* const* grads_bf16, 
 int optim_step_factored(optim_group_t* group, const void* const* grads_bf16, int64_t step,
                         const optim_factored_hparams_t* hp, void* stream);
 
+/* Single-tensor factored step that allocates nothing (the pages have no counterpart; this entry
+ * exists for callers that cannot call cudaMalloc -- e.g. code whose device memory is entirely
+ * owned by another allocator or fixed pool, or a long-running job that must not allocate once it
+ * has been set up).  optim_step_factored allocates its scratch when the group is created; this
+ * variant instead uses one fixed 32 MiB device array that the library holds on every GPU that
+ * loads it, until the process exits.  The caller passes the tensor (weights, optional residual,
+ * factored state, as in optim_tensor_desc_t for FACTORED groups) and its bf16 gradient; results
+ * are identical to a FACTORED group holding just this tensor.  `step` is the caller's own
+ * counter (>= 1; no sequence check).  A tensor whose scratch would exceed the array (about
+ * 2^26 elements for a matrix) is rejected with OPTIM_EINVAL and a message giving both sizes.
+ * The first call on a device looks up the array's device address (once per device); make that
+ * first call outside any stream capture.  All calls share the array and it keeps the previous
+ * call's contents (the call clears the parts that must start at zero), so calls whose work
+ * overlaps on the GPU -- different streams without ordering, or several host threads -- race:
+ * order them on one stream.  Calls no cudaMalloc, cudaFree or other allocating routine. */
+int optim_step_factored_noalloc(const optim_tensor_desc_t* tensor, const void* grad_bf16, int64_t step,
+                                const optim_factored_hparams_t* hp, void* stream);
+
 /* Adan hyper-parameters (Algorithm 1 of the Adan paper linked by "Amazing Flux FFT quality on a
  * 5090", sd-scripts PR #2187, fourth post; beta weights the new term, as in the paper).
  * stochastic_rounding / seed as in optim_nadam_hparams_t (tensors without a residual). */

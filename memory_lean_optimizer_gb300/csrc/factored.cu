@@ -23,6 +23,8 @@
 // and counter), summing the partials in a fixed order.  Every reduction is in a fixed order, so
 // results are deterministic; sums are fp32 trees, with compensated (Neumaier) sums across partials.
 #include <algorithm>
+#include <cmath>
+#include <mutex>
 #include <vector>
 
 #include "factored.h"
@@ -812,3 +814,143 @@ int launch_factored_step(const FactoredPlan* p, const uint16_t* const* d_grads, 
 }
 
 }  // namespace lmo
+// ------------------------------------------------------------------------------------ no-alloc
+// A single-tensor factored step for callers that cannot allocate device memory: all of its
+// scratch (tensor record, work items, gradient-pointer slot, partial sums, column factors, row
+// means, sum-of-squares partials, clip divisor, counters) lives in one fixed file-scope device
+// array.  The array is created with the module on every GPU that loads the library and stays
+// until the process exits; all calls share it.
+namespace lmo {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 32ull << 20;   // 32 MiB per device
+constexpr int kNoAllocMaxDevices = 64;
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once per device (host
+// code cannot use the symbol itself: its host-side name is only a stand-in).
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    int rc = check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
+    if (rc) return rc;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return set_error(OPTIM_EINVAL, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        rc = check_cuda(cudaGetSymbolAddress(&p, g_noalloc_scratch), "cudaGetSymbolAddress(no-alloc scratch)");
+        if (rc) return rc;
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return OPTIM_OK;
+}
+
+size_t carve(size_t& off, size_t bytes) {
+    const size_t at = off;
+    off = (off + bytes + 255) & ~size_t(255);
+    return at;
+}
+
+}  // namespace
+}  // namespace lmo
+
+extern "C" int optim_step_factored_noalloc(const optim_tensor_desc_t* tensor, const void* grad_bf16, int64_t step,
+                                           const optim_factored_hparams_t* hp, void* stream) {
+    using namespace lmo;
+    if (!tensor || !hp) return set_error(OPTIM_EINVAL, "tensor or hparams is NULL");
+    const optim_tensor_desc_t& d = *tensor;
+    if (step < 1) return set_error(OPTIM_EINVAL, "step %lld < 1", (long long)step);
+    if (d.numel < 0 || d.ndim < 1 || d.ndim > 4) return set_error(OPTIM_EINVAL, "bad numel or ndim");
+    int64_t prod = 1;
+    for (int k = 0; k < d.ndim; ++k) {
+        if (d.shape[k] < 0) return set_error(OPTIM_EINVAL, "negative dim");
+        prod *= d.shape[k];
+    }
+    if (prod != d.numel) return set_error(OPTIM_EINVAL, "shape product %lld != numel %lld", (long long)prod, (long long)d.numel);
+    if (d.numel == 0) return OPTIM_OK;
+    if (!d.w_bf16 || !d.v || (d.ndim >= 2 && !d.m) || !grad_bf16)
+        return set_error(OPTIM_EINVAL, "weight, state or gradient pointer is NULL");
+    if (!is_aligned(d.w_bf16, 2) || (d.res_u16 && !is_aligned(d.res_u16, 2)) || !is_aligned(grad_bf16, 2) ||
+        !is_aligned(d.v, 4) || (d.m && !is_aligned(d.m, 4)))
+        return set_error(OPTIM_EALIGN, "a buffer is not aligned to its element size");
+    if (!(hp->lr >= 0.0f) || !std::isfinite(hp->lr) || !(hp->clip_threshold > 0.0f) || !std::isfinite(hp->clip_threshold) ||
+        !(hp->weight_decay >= 0.0f) || !std::isfinite(hp->weight_decay) || !(hp->eps1 >= 0.0f) || !(hp->eps2 >= 0.0f) ||
+        (hp->mode != 0 && hp->mode != 1) || !std::isfinite(hp->decay_rate) ||
+        (hp->mode == 1 && (!(hp->beta2 >= 0.0f && hp->beta2 < 1.0f) || !(hp->d >= 0.0f) || !std::isfinite(hp->d))))
+        return set_error(OPTIM_EINVAL, "invalid factored hyper-parameters");
+
+    // layout of this tensor's plan inside the fixed scratch
+    PlanLayout L;
+    plan_layout(std::vector<optim_tensor_desc_t>(1, d), L);
+    size_t off = 0;
+    const size_t o_ts = carve(off, sizeof(FTensor));
+    const size_t o_items = carve(off, L.items.size() * sizeof(Item));
+    const size_t o_fin = carve(off, L.fin.size() * sizeof(Item));
+    const size_t o_grad = carve(off, sizeof(void*));
+    const size_t o_rowpart = carve(off, (size_t)L.rowpart * 4), o_colpart = carve(off, (size_t)L.colpart * 4);
+    const size_t o_cc = carve(off, (size_t)L.cc * 4), o_rbar = carve(off, (size_t)L.mats * 4);
+    const size_t o_rbarpart = carve(off, (size_t)L.rbarpart * 4), o_rcounter = carve(off, (size_t)L.mats * 4);
+    const size_t o_ss = carve(off, (size_t)L.ss * 4), o_den = carve(off, 4), o_counter = carve(off, 4);
+    if (off > kNoAllocScratchBytes)
+        return set_error(OPTIM_EINVAL, "tensor of %lld elements needs %zu bytes of scratch; the fixed no-alloc scratch holds %zu",
+                         (long long)d.numel, off, kNoAllocScratchBytes);
+
+    void* base = nullptr;
+    int rc = noalloc_scratch(&base);
+    if (rc) return rc;
+    char* sb = static_cast<char*>(base);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    const double td = (double)step;
+    FactoredScalars k{};
+    k.mode = hp->mode;
+    k.clip = hp->clip_threshold;
+    k.eps1 = hp->eps1;
+    k.eps2 = hp->eps2;
+    if (hp->mode == 0) {
+        const double beta2t = 1.0 - std::pow(td, (double)hp->decay_rate);
+        k.b2t = (float)beta2t;
+        k.alpha = (float)(1.0 - beta2t);
+        k.lr_eff = hp->lr;
+    } else {
+        k.b2t = hp->beta2;
+        k.alpha = (float)((double)hp->d * (double)hp->d * (1.0 - (double)hp->beta2));
+        k.lr_eff = (float)((double)hp->d * (double)hp->lr);
+    }
+    k.nwdlr = (float)(-(double)hp->weight_decay * (double)k.lr_eff);
+
+    // tables (pageable host memory: staged by the runtime before the call returns), counters
+    // cleared because the previous call's contents stay in the shared array
+    const void* gp = grad_bf16;
+    rc = check_cuda(cudaMemcpyAsync(sb + o_ts, L.ts.data(), sizeof(FTensor), cudaMemcpyHostToDevice, s), "no-alloc upload");
+    if (!rc && !L.items.empty())
+        rc = check_cuda(cudaMemcpyAsync(sb + o_items, L.items.data(), L.items.size() * sizeof(Item), cudaMemcpyHostToDevice, s), "no-alloc upload");
+    if (!rc && !L.fin.empty())
+        rc = check_cuda(cudaMemcpyAsync(sb + o_fin, L.fin.data(), L.fin.size() * sizeof(Item), cudaMemcpyHostToDevice, s), "no-alloc upload");
+    if (!rc) rc = check_cuda(cudaMemcpyAsync(sb + o_grad, &gp, sizeof(void*), cudaMemcpyHostToDevice, s), "no-alloc upload");
+    if (!rc && L.mats) rc = check_cuda(cudaMemsetAsync(sb + o_rcounter, 0, (size_t)L.mats * 4, s), "no-alloc clear");
+    if (!rc) rc = check_cuda(cudaMemsetAsync(sb + o_counter, 0, 4, s), "no-alloc clear");
+    if (rc) return rc;
+
+    FactoredPlan plan;
+    plan.waves = L.waves;
+    plan.d_tensors = reinterpret_cast<FTensor*>(sb + o_ts);
+    plan.d_items = reinterpret_cast<Item*>(sb + o_items);
+    plan.d_fin = reinterpret_cast<Item*>(sb + o_fin);
+    Dev& D = plan.dev;
+    D.tensors = plan.d_tensors;
+    D.rowpart = reinterpret_cast<float*>(sb + o_rowpart);
+    D.colpart = reinterpret_cast<float*>(sb + o_colpart);
+    D.cc = reinterpret_cast<float*>(sb + o_cc);
+    D.rbar = reinterpret_cast<float*>(sb + o_rbar);
+    D.rbarpart = reinterpret_cast<float*>(sb + o_rbarpart);
+    D.rcounter = reinterpret_cast<unsigned*>(sb + o_rcounter);
+    D.ss = reinterpret_cast<float*>(sb + o_ss);
+    D.den = reinterpret_cast<float*>(sb + o_den);
+    D.counter = reinterpret_cast<unsigned*>(sb + o_counter);
+    return launch_factored_step(&plan, reinterpret_cast<const uint16_t* const*>(sb + o_grad), k, s, nullptr);
+}

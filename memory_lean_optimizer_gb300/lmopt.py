@@ -36,7 +36,7 @@ EXPORTED = (
     "state_pack_u16", "state_unpack_u16", "optim_kahan_split", "optim_kahan_merge",
     "optim_query_scales", "optim_set_scales", "optim_group_get_step", "optim_group_set_step",
     "optim_query_nonfinite", "optim_group_set_profile_event", "optim_last_error",
-    "optim_step_adan",
+    "optim_step_factored_noalloc", "optim_step_adan",
     "optim_offload_create", "optim_offload_destroy", "optim_group_attach_offload",
     "optim_offload_prefetch", "optim_offload_sync",
 )
@@ -94,6 +94,7 @@ def load(path: str = LIB_PATH):
             "optim_step_nadam_kahan": [P, P, I64, ctypes.POINTER(NadamHparams), P],
             "optim_step_factored": [P, P, I64, ctypes.POINTER(FactoredHparams), P],
             "optim_step_adan": [P, P, I64, ctypes.POINTER(AdanHparams), P],
+            "optim_step_factored_noalloc": [ctypes.POINTER(TensorDesc), P, I64, ctypes.POINTER(FactoredHparams), P],
             "state_pack_u16": [P, P, P, I64, I32, P],
             "state_unpack_u16": [P, P, P, I64, I32, P],
             "optim_kahan_split": [P, P, P, I64, P],
@@ -156,6 +157,12 @@ def optim_step_nadam_kahan(handle: int, grad_ptrs, step: int, hp: NadamHparams, 
 
 def optim_step_factored(handle: int, grad_ptrs, step: int, hp: FactoredHparams, stream: int = 0) -> None:
     check(load().optim_step_factored(handle, _ptr_array(grad_ptrs), step, ctypes.byref(hp), stream))
+
+
+def optim_step_factored_noalloc(desc: TensorDesc, grad_ptr: int, step: int, hp: FactoredHparams,
+                                stream: int = 0) -> None:
+    """Single-tensor factored step using the library's fixed device scratch (no allocation)."""
+    check(load().optim_step_factored_noalloc(ctypes.byref(desc), grad_ptr, step, ctypes.byref(hp), stream))
 
 
 def optim_step_adan(handle: int, grad_ptrs, step: int, hp: AdanHparams, stream: int = 0) -> None:
