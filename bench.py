@@ -577,8 +577,8 @@ def factored_bytes(shape):
 
 
 def run_factored(args, cfg):
-    """Factored workload (sdxl_like): Adafactor mode over 1332 SDXL-UNet-like tensors in groups
-    of 16, every step all 84 group calls; reports params/s and HBM GB/s at the algorithmic bytes."""
+    """Factored workload (sdxl_like): Adafactor mode over 1332 SDXL-UNet-like tensors in 10
+    groups, every step all group calls; reports params/s and HBM GB/s at the algorithmic bytes."""
     import torch
     from memory_lean_optimizer_gb300 import build, engine, lmopt, workloads as W
     world, rank, local = dist_info()

@@ -10,8 +10,9 @@
 // Factoring is over the last two dims; leading dims are a batch of matrices.
 //
 // Tensor classes and their kernels:
-//   wide  (ndim >= 2, rows*cols > 16): 64x256 tiles, 256 threads (8 warps x 8 rows, lane = 8 cols)
-//   tiny  (ndim >= 2, rows*cols <= 16, e.g. 3x3 conv kernels): one thread per matrix
+//   wide  (ndim >= 2, rows*cols > 16): 128x256 tiles, 256 threads (8 warps x 16 rows, lane = 8 cols)
+//   tiny  (ndim >= 2, rows*cols <= 16, e.g. 3x3 conv kernels): 2048 matrices per CTA, staged
+//         through shared memory in sub-batches of 256, one thread per matrix
 //   vector (ndim == 1): one thread per element, full fp32 second moment
 // Per wave of tensors (waves keep the wave's gradients, read three times, within L2):
 //   1. k_stats  : wide tiles -> row/column partial sums of q;  tiny/vector -> state EMA, u, sum u^2
@@ -33,11 +34,13 @@ namespace lmo {
 
 namespace {
 
-constexpr int kTR = 64;      // rows per wide tile
+constexpr int kTR = 128;     // rows per wide tile (16 per warp, in two batches of eight)
 constexpr int kTC = 256;     // columns per wide tile
 constexpr int kFinRowsPerItem = 256;   // rows per finalize row block (one per thread)
-constexpr int kFinColsPerItem = 64;    // columns per finalize column block (4 band groups)
-constexpr int kTinyPerCta = kThreads;
+constexpr int kFinColsPerItem = 32;    // columns per finalize column block
+constexpr int kFinGroups = kThreads / kFinColsPerItem;   // band groups of a column block (8)
+constexpr int kTinySub = kThreads;     // small matrices per staged sub-batch (one per thread)
+constexpr int kTinyPerCta = 8 * kTinySub;
 constexpr int kVecPerCta = kThreads * 8;
 constexpr int64_t kWaveGradBytes = 64ll << 20;   // gradient bytes per wave (L2-resident target)
 
@@ -171,36 +174,47 @@ __device__ void finish_ss(const Dev& D, const FTensor& t, int tensor, int part, 
     }
 }
 
-// Loads 8 consecutive bf16 words (columns col0..col0+7 of one row) into w[8]; columns past
-// `ncols` read as 0.  vec: 16-byte aligned fast path.
-__device__ __forceinline__ void load8(const uint16_t* p, int ncols, bool vec, uint32_t (&v)[8]) {
-    if (vec && ncols == 8) {
-        uint4 x = __ldcg(reinterpret_cast<const uint4*>(p));
-        v[0] = x.x & 0xFFFFu; v[1] = x.x >> 16; v[2] = x.y & 0xFFFFu; v[3] = x.y >> 16;
-        v[4] = x.z & 0xFFFFu; v[5] = x.z >> 16; v[6] = x.w & 0xFFFFu; v[7] = x.w >> 16;
-    } else {
+// Loads 8 consecutive bf16 words (columns col0..col0+7 of one row) into v[8]; columns past
+// `ncols` read as 0.
+__device__ __forceinline__ void load8(const uint16_t* p, int ncols, uint32_t (&v)[8]) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = j < ncols ? p[j] : 0u;
-    }
+    for (int j = 0; j < 8; ++j) v[j] = j < ncols ? p[j] : 0u;
 }
 
-// Copies n 16-bit words from global memory to shared memory, 128 bits at a time when aligned.
-__device__ __forceinline__ void stage_u16(uint16_t* dst, const uint16_t* src, int n) {
-    if (aligned16(src) && (n & 7) == 0) {
-        for (int i = threadIdx.x; i < (n >> 3); i += blockDim.x)
+// Copies n elements from global to shared memory (or back), 128 bits at a time when both sides
+// are 16-byte aligned and the byte count is a multiple of 16.  Called by the whole CTA.
+template <class T>
+__device__ __forceinline__ void stage(T* dst, const T* src, int n) {
+    if (aligned16(src) && aligned16(dst) && ((n * (int)sizeof(T)) & 15) == 0) {
+        const int nv = n * (int)sizeof(T) / 16;
+        for (int i = threadIdx.x; i < nv; i += blockDim.x)
             reinterpret_cast<uint4*>(dst)[i] = __ldcg(reinterpret_cast<const uint4*>(src) + i);
     } else {
         for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = src[i];
     }
 }
-__device__ __forceinline__ void unstage_u16(uint16_t* dst, const uint16_t* src, int n) {
-    if (aligned16(dst) && (n & 7) == 0) {
-        for (int i = threadIdx.x; i < (n >> 3); i += blockDim.x)
-            st_stream(reinterpret_cast<uint4*>(dst) + i, reinterpret_cast<const uint4*>(src)[i]);
+template <class T>
+__device__ __forceinline__ void unstage(T* dst, const T* src, int n, bool streaming) {
+    if (aligned16(src) && aligned16(dst) && ((n * (int)sizeof(T)) & 15) == 0) {
+        const int nv = n * (int)sizeof(T) / 16;
+        for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+            const uint4 x = reinterpret_cast<const uint4*>(src)[i];
+            if (streaming) st_stream(reinterpret_cast<uint4*>(dst) + i, x);
+            else reinterpret_cast<uint4*>(dst)[i] = x;
+        }
     } else {
         for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = src[i];
     }
 }
+
+// Shared-memory staging area of the small-matrix class: per sub-batch of kTinySub matrices,
+// gradient / weight / residual words (up to 16 per matrix) and the R then C statistics (up to 17
+// floats per matrix, since rows*cols <= 16 implies rows + cols <= 17).
+constexpr int kTinyWords = kTinySub * 16;
+constexpr int kTinyStats = kTinySub * 17;
+constexpr int kStatsSmem = kTinyWords * 2 + kTinyStats * 4;
+constexpr int kApplySmem = 3 * kTinyWords * 2 + kTinyStats * 4;
+static_assert(kStatsSmem >= 8 * (kTC + 1) * 4, "wide column buffer must fit the shared area");
 
 // One small matrix (rows*cols <= 16) of a tiny-class tensor: R, C EMAs (written back), mean(R),
 // and the matrix's sum of squared updates.  The fixed-size form keeps everything in registers.
@@ -273,7 +287,7 @@ __device__ float tiny_stats_any(const uint16_t* gm, float* Rs, float* Cs, int r,
     return acc;
 }
 
-// Apply step of one small matrix on staged words (w, res, g in shared memory).
+// Apply step of one small matrix on staged words (w, res, g and R, C in shared memory).
 template <int RR, int CC>
 __device__ __forceinline__ void tiny_apply(uint16_t* wm, uint16_t* rm, const uint16_t* gm, const float* Rs,
                                            const float* Cs, bool has_res, float den, const K& k) {
@@ -299,18 +313,41 @@ __device__ __forceinline__ void tiny_apply(uint16_t* wm, uint16_t* rm, const uin
         }
     }
 }
+__device__ void tiny_apply_any(uint16_t* wm, uint16_t* rm, const uint16_t* gm, const float* Rs, const float* Cs,
+                               int r, int c, bool has_res, float den, const K& k) {
+    float rtot = 0.f, cfac[16];
+    for (int i = 0; i < r; ++i) rtot = __fadd_rn(rtot, Rs[i]);
+    const float rbar = __fdiv_rn(rtot, (float)r);
+    for (int j = 0; j < c; ++j) cfac[j] = rsqrt_rn(Cs[j]);
+    for (int i = 0; i < r; ++i) {
+        const float rr = rsqrt_rn(__fdiv_rn(Rs[i], rbar));
+        for (int j = 0; j < c; ++j) {
+            const int e = i * c + j;
+            uint32_t hi = wm[e], lo = has_res ? rm[e] : 0u;
+            apply_elem(hi, lo, has_res, __fmul_rn(__fmul_rn(rr, cfac[j]), bf16_to_f32(gm[e])), den, k);
+            wm[e] = (uint16_t)hi;
+            if (has_res) rm[e] = (uint16_t)lo;
+        }
+    }
+}
+
+// Eight gradient words of one 128-bit load, as fp32 (bf16 -> fp32 is exact).
+__device__ __forceinline__ float g_at(const uint4& x, int j) {
+    const uint32_t w = j < 2 ? x.x : (j < 4 ? x.y : (j < 6 ? x.z : x.w));
+    return __uint_as_float((j & 1) ? (w & 0xFFFF0000u) : (w << 16));
+}
 
 // ------------------------------------------------------------------------------------ stats
-__global__ void __launch_bounds__(kThreads) k_stats(Dev D, const Item* items, K k) {
+__global__ void __launch_bounds__(kThreads, 4) k_stats(Dev D, const Item* items, K k) {
     __shared__ float sm[32];
-    __shared__ float cols[8][kTC + 1];
-    __shared__ __align__(16) uint16_t tile_g[kTinyPerCta * 16];
+    __shared__ __align__(16) unsigned char smem[kStatsSmem];
     const Item it = items[blockIdx.x];
     const FTensor t = D.tensors[it.tensor];
     const uint16_t* __restrict__ g = D.grads[it.tensor];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
     if (it.cls == kWide) {
+        float (*cols)[kTC + 1] = reinterpret_cast<float (*)[kTC + 1]>(smem);
         const int64_t b = it.x;
         const int64_t col0 = (int64_t)it.cb * kTC + lane * 8;
         const int ncols = cols_in(t.C - col0);
@@ -318,40 +355,42 @@ __global__ void __launch_bounds__(kThreads) k_stats(Dev D, const Item* items, K 
         // shuffles.  With C a multiple of 8 a lane's group is either whole (8) or empty (0).
         const bool vec = aligned16(g) && (t.C % 8 == 0);
         const bool lane_ok = ncols == 8;
-        const int64_t row0 = (int64_t)it.band * kTR + warp;
+        const int64_t row0 = (int64_t)it.band * kTR + warp;   // this warp's rows: row0 + 8*kk
         float cacc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         if (vec) {
-            // all eight rows' loads issued before any use (memory-level parallelism)
-            uint4 x[kTR / 8];
+#pragma unroll 1
+            for (int kb = 0; kb < kTR / 64; ++kb) {
+                // eight rows' loads issued before any use (memory-level parallelism)
+                uint4 x[8];
 #pragma unroll
-            for (int kk = 0; kk < kTR / 8; ++kk) {
-                const int64_t row = row0 + 8 * kk;
-                x[kk] = (row < t.R && lane_ok)
-                            ? __ldcg(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0))
-                            : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int kk = 0; kk < kTR / 8; ++kk) {
-                const int64_t row = row0 + 8 * kk;
-                const uint32_t wd[4] = {x[kk].x, x[kk].y, x[kk].z, x[kk].w};
-                float rs = 0.f;
-                if (lane_ok && row < t.R) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float q = qval(__uint_as_float((j & 1) ? (wd[j >> 1] & 0xFFFF0000u) : (wd[j >> 1] << 16)), k);
-                        rs = __fadd_rn(rs, q);
-                        cacc[j] = __fadd_rn(cacc[j], q);
-                    }
+                for (int kk = 0; kk < 8; ++kk) {
+                    const int64_t row = row0 + 64 * kb + 8 * kk;
+                    x[kk] = (row < t.R && lane_ok)
+                                ? __ldcg(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0))
+                                : make_uint4(0, 0, 0, 0);
                 }
-                rs = warp_sum_f32(rs);   // every lane of the warp, every iteration
-                if (lane == 0 && row < t.R) D.rowpart[t.rowpart_off + (b * t.R + row) * t.ncb + it.cb] = rs;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const int64_t row = row0 + 64 * kb + 8 * kk;
+                    float rs = 0.f;
+                    if (lane_ok && row < t.R) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float q = qval(g_at(x[kk], j), k);
+                            rs = __fadd_rn(rs, q);
+                            cacc[j] = __fadd_rn(cacc[j], q);
+                        }
+                    }
+                    rs = warp_sum_f32(rs);   // every lane of the warp, every iteration
+                    if (lane == 0 && row < t.R) D.rowpart[t.rowpart_off + (b * t.R + row) * t.ncb + it.cb] = rs;
+                }
             }
         } else {
             for (int kk = 0; kk < kTR / 8; ++kk) {
                 const int64_t row = row0 + 8 * kk;
-                if (row >= t.R) break;
+                if (row >= t.R) break;   // same for the whole warp
                 uint32_t v[8];
-                load8(g + (b * t.R + row) * t.C + col0, ncols, false, v);
+                load8(g + (b * t.R + row) * t.C + col0, ncols, v);
                 float rs = 0.f;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -378,16 +417,28 @@ __global__ void __launch_bounds__(kThreads) k_stats(Dev D, const Item* items, K 
 
     float acc = 0.f;
     if (it.cls == kTiny) {
+        // kTinyPerCta matrices in sub-batches of kTinySub (one matrix per thread), gradients and
+        // statistics staged through shared memory with 128-bit copies
         const int r = (int)t.R, c = (int)t.C, rc = r * c;
-        const int64_t m0 = it.x;
-        const int nm = (int)(t.B - m0 < kTinyPerCta ? t.B - m0 : kTinyPerCta);
-        stage_u16(tile_g, g + m0 * rc, nm * rc);
-        __syncthreads();
-        if ((int)threadIdx.x < nm) {
-            const uint16_t* gm = tile_g + threadIdx.x * rc;
-            float* Rs = t.row + (m0 + threadIdx.x) * r;
-            float* Cs = t.col + (m0 + threadIdx.x) * c;
-            acc = (r == 3 && c == 3) ? tiny_stats<3, 3>(gm, Rs, Cs, k) : tiny_stats_any(gm, Rs, Cs, r, c, k);
+        uint16_t* sg = reinterpret_cast<uint16_t*>(smem);
+        float* sf = reinterpret_cast<float*>(smem + kTinyWords * 2);
+        const int64_t mend = t.B < (int64_t)it.x + kTinyPerCta ? t.B : (int64_t)it.x + kTinyPerCta;
+        for (int64_t m0 = it.x; m0 < mend; m0 += kTinySub) {
+            const int nm = (int)(mend - m0 < kTinySub ? mend - m0 : kTinySub);
+            float* sR = sf;
+            float* sC = sf + nm * r;
+            stage(sg, g + m0 * rc, nm * rc);
+            stage(sR, t.row + m0 * r, nm * r);
+            stage(sC, t.col + m0 * c, nm * c);
+            __syncthreads();
+            const int i = threadIdx.x;
+            if (i < nm)
+                acc = __fadd_rn(acc, (r == 3 && c == 3) ? tiny_stats<3, 3>(sg + i * rc, sR + i * r, sC + i * c, k)
+                                                        : tiny_stats_any(sg + i * rc, sR + i * r, sC + i * c, r, c, k));
+            __syncthreads();
+            unstage(t.row + m0 * r, sR, nm * r, false);
+            unstage(t.col + m0 * c, sC, nm * c, false);
+            __syncthreads();
         }
     } else {  // kVec
         const int64_t e0 = (int64_t)it.x * kVecPerCta;
@@ -407,7 +458,7 @@ __global__ void __launch_bounds__(kThreads) k_stats(Dev D, const Item* items, K 
 // ------------------------------------------------------------------------------------ finalize
 __global__ void __launch_bounds__(kThreads) k_final(Dev D, const Item* items, K k) {
     __shared__ float sm[32];
-    __shared__ float part[4][kFinColsPerItem];
+    __shared__ float part[kFinGroups][kFinColsPerItem];
     __shared__ bool last;
     const Item it = items[blockIdx.x];
     const FTensor t = D.tensors[it.tensor];
@@ -419,7 +470,15 @@ __global__ void __launch_bounds__(kThreads) k_final(Dev D, const Item* items, K 
         if (i < t.R) {
             const float* rp = D.rowpart + t.rowpart_off + (b * t.R + i) * t.ncb;
             Comp s;
-            for (int cb = 0; cb < t.ncb; ++cb) s.add(rp[cb]);
+            int cb = 0;
+            for (; cb + 4 <= t.ncb; cb += 4) {   // four independent loads in flight
+                const float x0 = rp[cb], x1 = rp[cb + 1], x2 = rp[cb + 2], x3 = rp[cb + 3];
+                s.add(x0);
+                s.add(x1);
+                s.add(x2);
+                s.add(x3);
+            }
+            for (; cb < t.ncb; ++cb) s.add(rp[cb]);
             nr = ema(t.row[b * t.R + i], __fdiv_rn(s.value(), (float)t.C), k);
             t.row[b * t.R + i] = nr;
         }
@@ -442,18 +501,28 @@ __global__ void __launch_bounds__(kThreads) k_final(Dev D, const Item* items, K 
             D.rcounter[mat] = 0u;
         }
     } else {
-        // C EMA of 64 columns: 4 groups of 64 threads split the row bands, combined in order
+        // C EMA of 32 columns: 8 warps split the row bands (band = warp + 8*n), combined in order
         const int cl = threadIdx.x & (kFinColsPerItem - 1), grp = threadIdx.x / kFinColsPerItem;
         const int64_t j = (int64_t)it.cb * kFinColsPerItem + cl;
         Comp s;
         if (j < t.C) {
             const float* cp = D.colpart + t.colpart_off + b * t.nbands * t.C + j;
-            for (int band = grp; band < t.nbands; band += 4) s.add(cp[(int64_t)band * t.C]);
+            int band = grp;
+            for (; band + 3 * kFinGroups < t.nbands; band += 4 * kFinGroups) {   // four loads in flight
+                const float x0 = cp[(int64_t)band * t.C], x1 = cp[(int64_t)(band + kFinGroups) * t.C];
+                const float x2 = cp[(int64_t)(band + 2 * kFinGroups) * t.C], x3 = cp[(int64_t)(band + 3 * kFinGroups) * t.C];
+                s.add(x0);
+                s.add(x1);
+                s.add(x2);
+                s.add(x3);
+            }
+            for (; band < t.nbands; band += kFinGroups) s.add(cp[(int64_t)band * t.C]);
         }
         part[grp][cl] = s.value();
         __syncthreads();
         if (grp == 0 && j < t.C) {
-            const float c = __fadd_rn(__fadd_rn(part[0][cl], part[1][cl]), __fadd_rn(part[2][cl], part[3][cl]));
+            const float c = __fadd_rn(__fadd_rn(__fadd_rn(part[0][cl], part[1][cl]), __fadd_rn(part[2][cl], part[3][cl])),
+                                      __fadd_rn(__fadd_rn(part[4][cl], part[5][cl]), __fadd_rn(part[6][cl], part[7][cl])));
             const float nc = ema(t.col[b * t.C + j], __fdiv_rn(c, (float)t.R), k);
             t.col[b * t.C + j] = nc;
             D.cc[t.cc_off + b * t.C + j] = rsqrt_rn(nc);
@@ -462,7 +531,7 @@ __global__ void __launch_bounds__(kThreads) k_final(Dev D, const Item* items, K 
 }
 
 // ------------------------------------------------------------------------------------ rms
-__global__ void __launch_bounds__(kThreads) k_rms(Dev D, const Item* items, K k) {
+__global__ void __launch_bounds__(kThreads, 4) k_rms(Dev D, const Item* items, K k) {
     __shared__ float sm[32];
     const Item it = items[blockIdx.x];
     const FTensor t = D.tensors[it.tensor];
@@ -480,24 +549,27 @@ __global__ void __launch_bounds__(kThreads) k_rms(Dev D, const Item* items, K k)
     for (int j = 0; j < 8; ++j) ccv[j] = j < ncols ? D.cc[t.cc_off + b * t.C + col0 + j] : 0.f;
     float acc = 0.f;
     if (vec) {
-        uint4 x[kTR / 8];
+#pragma unroll 1
+        for (int kb = 0; kb < kTR / 64; ++kb) {
+            uint4 x[8];
+            float rv[8];
 #pragma unroll
-        for (int kk = 0; kk < kTR / 8; ++kk) {
-            const int64_t row = row0 + 8 * kk;
-            x[kk] = (row < t.R && lane_ok) ? __ldcg(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0))
-                                           : make_uint4(0, 0, 0, 0);
-        }
+            for (int kk = 0; kk < 8; ++kk) {
+                const int64_t row = row0 + 64 * kb + 8 * kk;
+                const bool ok = row < t.R && lane_ok;
+                x[kk] = ok ? __ldcg(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0)) : make_uint4(0, 0, 0, 0);
+                rv[kk] = ok ? t.row[b * t.R + row] : 0.f;
+            }
 #pragma unroll
-        for (int kk = 0; kk < kTR / 8; ++kk) {
-            const int64_t row = row0 + 8 * kk;
-            if (row >= t.R || !lane_ok) break;
-            const float rr = rsqrt_rn(__fdiv_rn(t.row[b * t.R + row], rbar));
-            const uint32_t wd[4] = {x[kk].x, x[kk].y, x[kk].z, x[kk].w};
+            for (int kk = 0; kk < 8; ++kk) {
+                const int64_t row = row0 + 64 * kb + 8 * kk;
+                if (row >= t.R || !lane_ok) break;
+                const float rr = rsqrt_rn(__fdiv_rn(rv[kk], rbar));
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float gv = __uint_as_float((j & 1) ? (wd[j >> 1] & 0xFFFF0000u) : (wd[j >> 1] << 16));
-                const float u = __fmul_rn(__fmul_rn(rr, ccv[j]), gv);
-                acc = __fadd_rn(acc, __fmul_rn(u, u));
+                for (int j = 0; j < 8; ++j) {
+                    const float u = __fmul_rn(__fmul_rn(rr, ccv[j]), g_at(x[kk], j));
+                    acc = __fadd_rn(acc, __fmul_rn(u, u));
+                }
             }
         }
     } else {
@@ -506,7 +578,7 @@ __global__ void __launch_bounds__(kThreads) k_rms(Dev D, const Item* items, K k)
             if (row >= t.R) break;
             const float rr = rsqrt_rn(__fdiv_rn(t.row[b * t.R + row], rbar));
             uint32_t v[8];
-            load8(g + (b * t.R + row) * t.C + col0, ncols, false, v);
+            load8(g + (b * t.R + row) * t.C + col0, ncols, v);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 if (j < ncols) {
@@ -521,10 +593,30 @@ __global__ void __launch_bounds__(kThreads) k_rms(Dev D, const Item* items, K k)
 }
 
 // ------------------------------------------------------------------------------------ apply
-__global__ void __launch_bounds__(kThreads) k_apply(Dev D, const Item* items, K k) {
-    __shared__ __align__(16) uint16_t tile_g[kTinyPerCta * 9];
-    __shared__ __align__(16) uint16_t tile_w[kTinyPerCta * 9];
-    __shared__ __align__(16) uint16_t tile_r[kTinyPerCta * 9];
+// Applies the update to the eight elements of one row held in (W, Rv) with gradients G.
+__device__ __forceinline__ void apply8(const uint4& G, uint4& Wv, uint4& Rv, float rr, const float (&ccv)[8],
+                                       bool has_res, float den, const K& k) {
+    uint32_t* w32 = reinterpret_cast<uint32_t*>(&Wv);
+    uint32_t* r32 = reinterpret_cast<uint32_t*>(&Rv);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t ow = 0, orr = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int sh = 16 * h;
+            uint32_t hi = (w32[q] >> sh) & 0xFFFFu, lo = (r32[q] >> sh) & 0xFFFFu;
+            const float u = __fmul_rn(__fmul_rn(rr, ccv[2 * q + h]), g_at(G, 2 * q + h));
+            apply_elem(hi, lo, has_res, u, den, k);
+            ow |= hi << sh;
+            orr |= lo << sh;
+        }
+        w32[q] = ow;
+        r32[q] = orr;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items, K k) {
+    __shared__ __align__(16) unsigned char smem[kApplySmem];
     const Item it = items[blockIdx.x];
     const FTensor t = D.tensors[it.tensor];
     const uint16_t* __restrict__ g = D.grads[it.tensor];
@@ -541,37 +633,41 @@ __global__ void __launch_bounds__(kThreads) k_apply(Dev D, const Item* items, K 
 #pragma unroll
         for (int j = 0; j < 8; ++j) ccv[j] = j < ncols ? D.cc[t.cc_off + b * t.C + col0 + j] : 0.f;
         const float rbar = D.rbar[t.mat_off + b];
-#pragma unroll 2
-        for (int kk = 0; kk < kTR / 8; ++kk) {
-            const int64_t row = (int64_t)it.band * kTR + warp + 8 * kk;
-            if (row >= t.R) break;
-            const float rr = rsqrt_rn(__fdiv_rn(t.row[b * t.R + row], rbar));
-            const int64_t off = (b * t.R + row) * t.C + col0;
-            if (vec && ncols == 8) {
-                const uint4 G = __ldcg(reinterpret_cast<const uint4*>(g + off));
-                uint4 Wv = ld_stream(reinterpret_cast<const uint4*>(t.w + off));
-                uint4 Rv = has_res ? ld_stream(reinterpret_cast<const uint4*>(t.res + off)) : make_uint4(0, 0, 0, 0);
-                const uint32_t* g32 = reinterpret_cast<const uint32_t*>(&G);
-                uint32_t* w32 = reinterpret_cast<uint32_t*>(&Wv);
-                uint32_t* r32 = reinterpret_cast<uint32_t*>(&Rv);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t ow = 0, orr = 0;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int sh = 16 * h;
-                        uint32_t hi = (w32[q] >> sh) & 0xFFFFu, lo = (r32[q] >> sh) & 0xFFFFu;
-                        const float u = __fmul_rn(__fmul_rn(rr, ccv[2 * q + h]), bf16_to_f32((g32[q] >> sh) & 0xFFFFu));
-                        apply_elem(hi, lo, has_res, u, den, k);
-                        ow |= hi << sh;
-                        orr |= lo << sh;
-                    }
-                    w32[q] = ow;
-                    r32[q] = orr;
+        const int64_t row0 = (int64_t)it.band * kTR + warp;
+        if (vec) {
+            if (ncols != 8) return;   // no shuffles below: lanes may leave independently
+            // two rows per iteration, all six 128-bit loads issued before the arithmetic
+#pragma unroll 1
+            for (int kk = 0; kk < kTR / 8; kk += 2) {
+                const int64_t rowA = row0 + 8 * kk, rowB = rowA + 8;
+                if (rowA >= t.R) break;
+                const bool hasB = rowB < t.R;
+                const int64_t offA = (b * t.R + rowA) * t.C + col0, offB = offA + 8 * t.C;
+                const uint4 GA = __ldcg(reinterpret_cast<const uint4*>(g + offA));
+                uint4 WA = ld_stream(reinterpret_cast<const uint4*>(t.w + offA));
+                uint4 RA = has_res ? ld_stream(reinterpret_cast<const uint4*>(t.res + offA)) : make_uint4(0, 0, 0, 0);
+                uint4 GB = make_uint4(0, 0, 0, 0), WB = GB, RB = GB;
+                if (hasB) {
+                    GB = __ldcg(reinterpret_cast<const uint4*>(g + offB));
+                    WB = ld_stream(reinterpret_cast<const uint4*>(t.w + offB));
+                    if (has_res) RB = ld_stream(reinterpret_cast<const uint4*>(t.res + offB));
                 }
-                st_stream(reinterpret_cast<uint4*>(t.w + off), Wv);
-                if (has_res) st_stream(reinterpret_cast<uint4*>(t.res + off), Rv);
-            } else {
+                const float rvA = t.row[b * t.R + rowA], rvB = hasB ? t.row[b * t.R + rowB] : 1.0f;
+                apply8(GA, WA, RA, rsqrt_rn(__fdiv_rn(rvA, rbar)), ccv, has_res, den, k);
+                st_stream(reinterpret_cast<uint4*>(t.w + offA), WA);
+                if (has_res) st_stream(reinterpret_cast<uint4*>(t.res + offA), RA);
+                if (hasB) {
+                    apply8(GB, WB, RB, rsqrt_rn(__fdiv_rn(rvB, rbar)), ccv, has_res, den, k);
+                    st_stream(reinterpret_cast<uint4*>(t.w + offB), WB);
+                    if (has_res) st_stream(reinterpret_cast<uint4*>(t.res + offB), RB);
+                }
+            }
+        } else {
+            for (int kk = 0; kk < kTR / 8; ++kk) {
+                const int64_t row = row0 + 8 * kk;
+                if (row >= t.R) break;
+                const float rr = rsqrt_rn(__fdiv_rn(t.row[b * t.R + row], rbar));
+                const int64_t off = (b * t.R + row) * t.C + col0;
                 for (int j = 0; j < ncols; ++j) {
                     uint32_t hi = t.w[off + j], lo = has_res ? t.res[off + j] : 0u;
                     const float u = __fmul_rn(__fmul_rn(rr, ccv[j]), bf16_to_f32(g[off + j]));
@@ -585,41 +681,32 @@ __global__ void __launch_bounds__(kThreads) k_apply(Dev D, const Item* items, K 
     }
     if (it.cls == kTiny) {
         const int r = (int)t.R, c = (int)t.C, rc = r * c;
-        const int64_t m0 = it.x;
-        const int nm = (int)(t.B - m0 < kTinyPerCta ? t.B - m0 : kTinyPerCta);
-        if (r == 3 && c == 3) {
-            stage_u16(tile_g, g + m0 * rc, nm * rc);
-            stage_u16(tile_w, t.w + m0 * rc, nm * rc);
-            if (has_res) stage_u16(tile_r, t.res + m0 * rc, nm * rc);
+        uint16_t* sg = reinterpret_cast<uint16_t*>(smem);
+        uint16_t* sw = sg + kTinyWords;
+        uint16_t* sr = sw + kTinyWords;
+        float* sf = reinterpret_cast<float*>(sr + kTinyWords);
+        const int64_t mend = t.B < (int64_t)it.x + kTinyPerCta ? t.B : (int64_t)it.x + kTinyPerCta;
+        for (int64_t m0 = it.x; m0 < mend; m0 += kTinySub) {
+            const int nm = (int)(mend - m0 < kTinySub ? mend - m0 : kTinySub);
+            float* sR = sf;
+            float* sC = sf + nm * r;
+            stage(sg, g + m0 * rc, nm * rc);
+            stage(sw, t.w + m0 * rc, nm * rc);
+            if (has_res) stage(sr, t.res + m0 * rc, nm * rc);
+            stage(sR, t.row + m0 * r, nm * r);
+            stage(sC, t.col + m0 * c, nm * c);
             __syncthreads();
-            if ((int)threadIdx.x < nm)
-                tiny_apply<3, 3>(tile_w + threadIdx.x * rc, tile_r + threadIdx.x * rc, tile_g + threadIdx.x * rc,
-                                 t.row + (m0 + threadIdx.x) * r, t.col + (m0 + threadIdx.x) * c, has_res, den, k);
-            __syncthreads();
-            unstage_u16(t.w + m0 * rc, tile_w, nm * rc);
-            if (has_res) unstage_u16(t.res + m0 * rc, tile_r, nm * rc);
-            return;
-        }
-        const int64_t mat = m0 + threadIdx.x;
-        if (mat >= t.B) return;
-        const float* Rs = t.row + mat * r;
-        const float* Cs = t.col + mat * c;
-        float rtot = 0.f;
-        for (int i = 0; i < r; ++i) rtot = __fadd_rn(rtot, Rs[i]);
-        const float rbar = __fdiv_rn(rtot, (float)r);
-        float ccv[16];
-        for (int j = 0; j < c; ++j) ccv[j] = rsqrt_rn(Cs[j]);
-        const int64_t base = mat * r * c;
-        for (int i = 0; i < r; ++i) {
-            const float rr = rsqrt_rn(__fdiv_rn(Rs[i], rbar));
-            for (int j = 0; j < c; ++j) {
-                const int64_t e = base + i * c + j;
-                uint32_t hi = t.w[e], lo = has_res ? t.res[e] : 0u;
-                const float u = __fmul_rn(__fmul_rn(rr, ccv[j]), bf16_to_f32(g[e]));
-                apply_elem(hi, lo, has_res, u, den, k);
-                t.w[e] = (uint16_t)hi;
-                if (has_res) t.res[e] = (uint16_t)lo;
+            const int i = threadIdx.x;
+            if (i < nm) {
+                if (r == 3 && c == 3)
+                    tiny_apply<3, 3>(sw + i * rc, sr + i * rc, sg + i * rc, sR + i * r, sC + i * c, has_res, den, k);
+                else
+                    tiny_apply_any(sw + i * rc, sr + i * rc, sg + i * rc, sR + i * r, sC + i * c, r, c, has_res, den, k);
             }
+            __syncthreads();
+            unstage(t.w + m0 * rc, sw, nm * rc, true);
+            if (has_res) unstage(t.res + m0 * rc, sr, nm * rc, true);
+            __syncthreads();
         }
         return;
     }
@@ -719,12 +806,19 @@ static void plan_layout(const std::vector<optim_tensor_desc_t>& desc, PlanLayout
         t.ss_off = L.ss;
         L.ss += t.ss_cnt;
     }
-    // waves: consecutive tensors until the wave's gradient bytes reach the L2-resident target
+    // waves: consecutive tensors, at most kWaveGradBytes of gradients each (the L2-resident
+    // target), balanced so that no wave is much smaller than the others: the group's gradient
+    // bytes are split into ceil(total / kWaveGradBytes) near-equal targets
+    int64_t total = 0;
+    for (int32_t q = 0; q < n; ++q) total += 2 * L.ts[q].numel;
+    const int64_t nw = total > 0 ? (total + kWaveGradBytes - 1) / kWaveGradBytes : 1;
+    const int64_t target = (total + nw - 1) / nw;
     int32_t i = 0;
     while (i < n) {
         int64_t bytes = 0;
         int32_t j = i;
-        while (j < n && (j == i || bytes + 2 * L.ts[j].numel <= kWaveGradBytes)) bytes += 2 * L.ts[j++].numel;
+        while (j < n && (j == i || (bytes + 2 * L.ts[j].numel <= kWaveGradBytes && bytes + L.ts[j].numel <= target)))
+            bytes += 2 * L.ts[j++].numel;
         Wave wv{};
         wv.item_off = (int32_t)L.items.size();
         wv.fin_off = (int32_t)L.fin.size();

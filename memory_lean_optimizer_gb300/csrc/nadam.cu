@@ -65,6 +65,20 @@ __device__ __forceinline__ void sr_lanes8(const Prm& k, uint32_t tensor, int64_t
     r[2] = (uint32_t)b;
     r[3] = (uint32_t)(b >> 32);
 }
+// Both halves of the 16-lane block starting at element i0 (i0 % 16 == 0): one generator call.
+__device__ __forceinline__ void sr_lanes16(const Prm& k, uint32_t tensor, int64_t i0, uint32_t (&ra)[4],
+                                           uint32_t (&rb)[4]) {
+    uint64_t c0 = (uint64_t)i0 >> 4, c1 = k.step, c2 = 0, c3 = 0;
+    philox4x64_10(c0, c1, c2, c3, k.seed, tensor);
+    ra[0] = (uint32_t)c0;
+    ra[1] = (uint32_t)(c0 >> 32);
+    ra[2] = (uint32_t)c1;
+    ra[3] = (uint32_t)(c1 >> 32);
+    rb[0] = (uint32_t)c2;
+    rb[1] = (uint32_t)(c2 >> 32);
+    rb[2] = (uint32_t)c3;
+    rb[3] = (uint32_t)(c3 >> 32);
+}
 __device__ __forceinline__ uint32_t sr_lane1(const Prm& k, uint32_t tensor, int64_t i) {
     uint64_t c0 = (uint64_t)i >> 4, c1 = k.step, c2 = 0, c3 = 0;
     philox4x64_10(c0, c1, c2, c3, k.seed, tensor);
@@ -196,12 +210,10 @@ __device__ __forceinline__ void step2_f32(const Prm& k, bool has_res, bool sr, u
 // i0: index of the first of the 8 elements (for the stochastic-rounding lanes).  kSR: the
 // stochastic-rounding variant (compiled separately so the residual path carries none of it).
 template <bool kSR>
-__device__ __forceinline__ void step8_u16(const Prm& k, const Codec& cd, bool has_res, uint32_t tensor,
-                                          int64_t i0, uint4& W, uint4& R, const uint4& G, uint4& M, uint4& V,
+__device__ __forceinline__ void step8_u16(const Prm& k, const Codec& cd, bool has_res, const uint32_t (&r)[4],
+                                          uint4& W, uint4& R, const uint4& G, uint4& M, uint4& V,
                                           float& am, float& av, uint32_t& nf) {
     const bool sr = kSR && !has_res;
-    uint32_t r[4] = {0u, 0u, 0u, 0u};
-    if (sr) sr_lanes8(k, tensor, i0, r);
     step2_u16(k, cd, has_res, sr, r[0], W.x, R.x, G.x, M.x, V.x, am, av, nf);
     step2_u16(k, cd, has_res, sr, r[1], W.y, R.y, G.y, M.y, V.y, am, av, nf);
     step2_u16(k, cd, has_res, sr, r[2], W.z, R.z, G.z, M.z, V.z, am, av, nf);
@@ -262,32 +274,40 @@ __global__ void __launch_bounds__(kThreads, 4) k_nadam_step(NadamLaunch L, Prm k
         if (!small) {
             uint4* mv = reinterpret_cast<uint4*>(static_cast<uint16_t*>(t.m) + start);
             uint4* vv = reinterpret_cast<uint4*>(static_cast<uint16_t*>(t.v) + start);
-            int64_t i = threadIdx.x;
-            // two independent 8-element groups per iteration: ten 128-bit loads in flight
-            for (; i + kThreads < nv; i += 2 * kThreads) {
-                const int64_t i1 = i + kThreads;
+            const bool sr = kSR && !has_res;
+            // two independent 8-element groups per iteration: ten 128-bit loads in flight.  With
+            // stochastic rounding the two groups are the halves of one 16-element block, so one
+            // generator call serves both; otherwise they are kThreads vectors apart.
+            int64_t p = threadIdx.x;
+            for (; sr ? (2 * p + 1 < nv) : (p + kThreads < nv); p += sr ? kThreads : 2 * kThreads) {
+                const int64_t i = sr ? 2 * p : p, i1 = sr ? 2 * p + 1 : p + kThreads;
                 uint4 W0 = ld_stream(wv + i), W1 = ld_stream(wv + i1);
                 uint4 R0 = has_res ? ld_stream(rv + i) : make_uint4(0, 0, 0, 0);
                 uint4 R1 = has_res ? ld_stream(rv + i1) : make_uint4(0, 0, 0, 0);
                 uint4 G0 = ld_stream(gv + i), G1 = ld_stream(gv + i1);
                 uint4 M0 = ld_stream(mv + i), M1 = ld_stream(mv + i1);
                 uint4 V0 = ld_stream(vv + i), V1 = ld_stream(vv + i1);
-                step8_u16<kSR>(k, cd, has_res, c.tensor, start + 8 * i, W0, R0, G0, M0, V0, am, av, nf);
+                uint32_t ra[4] = {0u, 0u, 0u, 0u}, rb[4] = {0u, 0u, 0u, 0u};
+                if (sr) sr_lanes16(k, c.tensor, start + 16 * p, ra, rb);
+                step8_u16<kSR>(k, cd, has_res, ra, W0, R0, G0, M0, V0, am, av, nf);
                 st_stream(wv + i, W0);
                 if (has_res) st_stream(rv + i, R0);
                 st_stream(mv + i, M0);
                 st_stream(vv + i, V0);
-                step8_u16<kSR>(k, cd, has_res, c.tensor, start + 8 * i1, W1, R1, G1, M1, V1, am, av, nf);
+                step8_u16<kSR>(k, cd, has_res, rb, W1, R1, G1, M1, V1, am, av, nf);
                 st_stream(wv + i1, W1);
                 if (has_res) st_stream(rv + i1, R1);
                 st_stream(mv + i1, M1);
                 st_stream(vv + i1, V1);
             }
-            for (; i < nv; i += kThreads) {
+            // remaining vectors one at a time
+            for (int64_t i = sr ? 2 * p : p; i < nv; i += kThreads) {
                 uint4 W0 = ld_stream(wv + i);
                 uint4 R0 = has_res ? ld_stream(rv + i) : make_uint4(0, 0, 0, 0);
                 uint4 G0 = ld_stream(gv + i), M0 = ld_stream(mv + i), V0 = ld_stream(vv + i);
-                step8_u16<kSR>(k, cd, has_res, c.tensor, start + 8 * i, W0, R0, G0, M0, V0, am, av, nf);
+                uint32_t ra[4] = {0u, 0u, 0u, 0u};
+                if (sr) sr_lanes8(k, c.tensor, start + 8 * i, ra);
+                step8_u16<kSR>(k, cd, has_res, ra, W0, R0, G0, M0, V0, am, av, nf);
                 st_stream(wv + i, W0);
                 if (has_res) st_stream(rv + i, R0);
                 st_stream(mv + i, M0);

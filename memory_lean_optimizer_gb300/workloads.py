@@ -10,7 +10,8 @@ synthetic):
   nadam_1m     one 1024x1024 bf16 weight, 10 steps
   flux19       19 Flux-like double-stream blocks x {3072x9216, 3072x3072, 3072x12288,
                12288x3072, 3072x18432}: 3,227,516,928 parameters, one group per block
-  sdxl_like    SDXL-UNet-like linears, 3x3 convs and 1-D tensors, 2,602,705,920 parameters
+  sdxl_like    SDXL-UNet-like linears, 3x3 convs and 1-D tensors, 2,602,705,920 parameters,
+               10 groups
   ragged20k    20,000 tensors, sizes round(2^U(6,22)), 1% exact-zero gradients
   flux35       35 Flux-like blocks (5,945,425,920 parameters) for the host-offload pipeline
 """
@@ -53,6 +54,23 @@ def sdxl_like_shapes():
 
 def numel(shape) -> int:
     return int(math.prod(shape))
+
+
+def balanced_groups(shapes, n_groups: int):
+    """Contiguous split of a tensor list into n_groups groups of roughly equal element count."""
+    n_groups = max(1, min(n_groups, len(shapes)))
+    total = sum(numel(s) for s in shapes)
+    groups, cur, acc = [], [], 0
+    for i, s in enumerate(shapes):
+        cur.append(s)
+        acc += numel(s)
+        left_groups, left_shapes = n_groups - len(groups) - 1, len(shapes) - i - 1
+        if left_groups > 0 and (acc >= total * (len(groups) + 1) / n_groups or left_shapes == left_groups):
+            groups.append(cur)
+            cur = []
+    if cur:
+        groups.append(cur)
+    return groups
 
 
 def _gen(seed: int, tensor: int, step: int, stream: int, device) -> torch.Generator:
@@ -105,14 +123,15 @@ def config(name: str):
         return dict(kind="nadam", groups=[[(n,) for n in ragged_sizes(20000, 0)]], hp=dict(NADAM_HP),
                     steps=5, g_std=1e-3, zero_frac=0.01, seed=0)
     if name == "sdxl_like":
+        # ten optimizer groups: the group count the SDXL optimizer-groups option recommends (4-10)
         shapes = sdxl_like_shapes()
-        return dict(kind="factored", groups=[shapes[i:i + 16] for i in range(0, len(shapes), 16)],
+        return dict(kind="factored", groups=balanced_groups(shapes, 10),
                     hp=dict(lr=2e-6, beta2=0.999, decay_rate=-0.8, eps1=1e-30, eps2=1e-30, d=1.0,
                             clip_threshold=1.0, weight_decay=0.0, mode=0),
                     steps=5, g_std=1e-4, zero_frac=0.0, seed=0)
-    if name == "sdxl_like_4":   # the first 4 groups of sdxl_like: the factored profiling case
+    if name == "sdxl_like_1":   # the first group of sdxl_like (~260M parameters): the profiling case
         c = config("sdxl_like")
-        c["groups"] = c["groups"][:4]
+        c["groups"] = c["groups"][:1]
         return c
     if name == "flux35":
         return dict(kind="nadam", groups=flux_shapes(35), hp=dict(NADAM_HP), steps=3, g_std=1e-4,

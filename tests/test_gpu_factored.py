@@ -99,8 +99,10 @@ def run_parity(orc, eng, shapes, steps, hp, seed=0, g_std=1e-3, kahan=True, scal
     return ora, grp
 
 
+# (45, 50, 3, 3): 2250 small matrices, one full CTA of 2048 and a ragged one (202: no 128-bit
+# staging); (600, 2, 2): the generic small-matrix path over three sub-batches
 SHAPES = [(64, 80), (300, 257), (1000, 640), (3, 40, 72), (1, 300), (300, 1), (4, 6, 3, 3), (32, 16, 3, 3),
-          (2, 2), (1280,), (77,), (5000,)]
+          (2, 2), (1280,), (77,), (5000,), (45, 50, 3, 3), (600, 2, 2)]
 
 
 @pytest.mark.parametrize("mode", [0, 1])

@@ -116,7 +116,7 @@ def test_ragged20k_full(orc, eng):
 
 
 def test_sdxl_like_full(orc, eng):
-    """SDXL-like factored workload (1332 tensors, 2,602,705,920 params) in groups of 16,
+    """SDXL-like factored workload (1332 tensors, 2,602,705,920 params) in its 10 groups,
     Adafactor mode, 2 steps; one linear of each kind, a 3x3 conv and 1-D tensors replayed whole."""
     from test_gpu_factored import OracleFactored
     cfg = W.config("sdxl_like")
@@ -130,17 +130,19 @@ def test_sdxl_like_full(orc, eng):
             seen.add(tuple(s))
     masters = [W.master_weights(s, 0, i, device="cuda") for i, s in enumerate(shapes)]
     ora = OracleFactored(orc, [masters[i].cpu().numpy() for i in sample], [shapes[i] for i in sample])
-    groups = [eng.FactoredGroup.from_masters(masters[k:k + 16]) for k in range(0, len(shapes), 16)]
+    bounds = np.cumsum([0] + [len(g) for g in cfg["groups"]])
+    groups = [eng.FactoredGroup.from_masters(masters[bounds[k]:bounds[k + 1]]) for k in range(len(cfg["groups"]))]
     del masters
     for t in range(1, steps + 1):
         grads = [W.grad_bf16(s, 0, i, t, cfg["g_std"], device="cuda") for i, s in enumerate(shapes)]
         ora.step([_bits(grads[i]) for i in sample], hp)
         for k, grp in enumerate(groups):
-            grp.step(grads[16 * k:16 * k + 16], hp)
+            grp.step(grads[bounds[k]:bounds[k + 1]], hp)
         del grads
     torch.cuda.synchronize()
     for j, i in enumerate(sample):
-        grp, li = groups[i // 16], i % 16
+        k = int(np.searchsorted(bounds, i, side="right")) - 1
+        grp, li = groups[k], i - int(bounds[k])
         ot = ora.t[j]
         ref = orc.kahan_merge(ot["hi"], ot["lo"]).astype(np.float64)
         got = grp.masters()[li].cpu().numpy().reshape(-1).astype(np.float64)
