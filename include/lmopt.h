@@ -145,7 +145,11 @@ int optim_step_nadam_kahan(optim_group_t* group, const void* const* grads_bf16, 
 /* One factored-second-moment step (Adafactor / Prodigy with beta1 = 0) of a FACTORED group:
  * row and column EMAs of g^2 over the last two dims, rank-1 reconstruction
  * V_ij = R_i C_j / mean(R), update u = g / sqrt(V), RMS clipping, decoupled decay, Kahan split.
- * 1-D tensors keep a full second moment.  Arguments as optim_step_nadam_kahan. */
+ * 1-D tensors keep a full second moment.  Arguments as optim_step_nadam_kahan.  A group larger
+ * than one wave (64 MiB of gradients) is processed wave by wave, with consecutive waves on two
+ * streams: `stream` and a stream owned by the group, which waits for the work already on `stream`
+ * and which `stream` waits for before any later work -- to the caller the call is ordered on
+ * `stream` as usual. */
 int optim_step_factored(optim_group_t* group, const void* const* grads_bf16, int64_t step,
                         const optim_factored_hparams_t* hp, void* stream);
 
@@ -238,7 +242,8 @@ int optim_offload_sync(optim_offload_t* engine, uint64_t* bytes_h2d, uint64_t* b
 /* Profiling hook: when `event` (a cudaEvent_t passed as void*) is not NULL, the next step calls
  * of this group record it on their stream between the pre-pass (gradient max, or the factored
  * statistics passes) and the update kernel, so that a caller can time the two phases with its
- * own events around the call.  NULL turns it off. */
+ * own events around the call (factored groups of several waves: before the last wave's update
+ * kernel, on the stream that wave runs on).  NULL turns it off. */
 int optim_group_set_profile_event(optim_group_t* group, void* event);
 
 const char* optim_last_error(void);

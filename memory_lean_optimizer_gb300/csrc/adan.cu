@@ -60,7 +60,22 @@ __device__ __forceinline__ float adan_elem(const AdanPrm& k, float w, float g, f
     return __fmul_rn(__fsub_rn(w, __fmul_rn(k.lr, __fdiv_rn(u, den))), k.inv_decay);
 }
 
-__global__ void __launch_bounds__(kThreads) k_adan_step(NadamLaunch L, AdanPrm k) {
+// Stores the updated weight (Kahan split, stochastic rounding or RNE); returns the bf16 word.
+__device__ __forceinline__ uint32_t store_bits(float w1, bool has_res, bool sr, uint32_t rnd, uint32_t& lo) {
+    const uint32_t b = __float_as_uint(w1);
+    if (has_res) {
+        lo = b & 0xFFFFu;
+        return b >> 16;
+    }
+    lo = 0u;
+    if (sr) return ((b & 0x7F800000u) == 0x7F800000u) ? (b >> 16) : ((b + rnd) >> 16);
+    return rne_bf16(w1);
+}
+
+// kSR: stochastic rounding of weights without a residual (a template flag so that the Philox
+// state stays out of the register budget of the other variants).
+template <bool kSR>
+__global__ void __launch_bounds__(kThreads, 4) k_adan_step(NadamLaunch L, AdanPrm k) {
     __shared__ uint32_t red[32];
     const Chunk c = L.chunks[blockIdx.x];
     const TensorRec t = L.tensors[c.tensor];
@@ -76,7 +91,63 @@ __global__ void __launch_bounds__(kThreads) k_adan_step(NadamLaunch L, AdanPrm k
     uint16_t* __restrict__ w = t.w;
     uint16_t* __restrict__ res = t.res;
     uint32_t nf = 0u;
-    for (int64_t i = start + threadIdx.x; i < end; i += kThreads) {
+    // 8 elements per thread per iteration with 128-bit accesses when every plane is 16-byte
+    // aligned (chunk starts are multiples of 8 elements); the rest element by element
+    const bool vec = aligned16(w) && (!has_res || aligned16(res)) && aligned16(g) && aligned16(gprev) &&
+                     aligned16(mp) && (n & 3) == 0;
+    const int64_t vend = vec ? start + ((end - start) & ~int64_t(7)) : start;
+    for (int64_t i = start + 8 * (int64_t)threadIdx.x; i < vend; i += 8 * kThreads) {
+        const uint4 W = ld_stream(reinterpret_cast<const uint4*>(w + i));
+        const uint4 R = has_res ? ld_stream(reinterpret_cast<const uint4*>(res + i)) : make_uint4(0, 0, 0, 0);
+        const uint4 G = ld_stream(reinterpret_cast<const uint4*>(g + i));
+        const uint4 GP = ld_stream(reinterpret_cast<const uint4*>(gprev + i));
+        float ma[8], va[8], na[8];
+        *reinterpret_cast<float4*>(ma) = ld_stream(reinterpret_cast<const float4*>(mp + i));
+        *reinterpret_cast<float4*>(ma + 4) = ld_stream(reinterpret_cast<const float4*>(mp + i + 4));
+        *reinterpret_cast<float4*>(va) = ld_stream(reinterpret_cast<const float4*>(vp + i));
+        *reinterpret_cast<float4*>(va + 4) = ld_stream(reinterpret_cast<const float4*>(vp + i + 4));
+        *reinterpret_cast<float4*>(na) = ld_stream(reinterpret_cast<const float4*>(np_ + i));
+        *reinterpret_cast<float4*>(na + 4) = ld_stream(reinterpret_cast<const float4*>(np_ + i + 4));
+        uint64_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+        if (kSR && !has_res) {   // one Philox block covers the 16-element group holding these 8
+            c0 = (uint64_t)i >> 4;
+            c1 = (uint64_t)k.step;
+            philox4x64_10(c0, c1, c2, c3, k.seed, c.tensor);
+        }
+        const uint32_t w32[4] = {W.x, W.y, W.z, W.w}, r32[4] = {R.x, R.y, R.z, R.w};
+        const uint32_t g32[4] = {G.x, G.y, G.z, G.w}, p32[4] = {GP.x, GP.y, GP.z, GP.w};
+        uint32_t wo[4], ro[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            wo[q] = 0u;
+            ro[q] = 0u;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int e = 2 * q + h, sh = 16 * h;
+                const uint32_t hw = (w32[q] >> sh) & 0xFFFFu, lw = (r32[q] >> sh) & 0xFFFFu;
+                const float w0 = has_res ? __uint_as_float((hw << 16) | lw) : bf16_to_f32(hw);
+                const float w1 = adan_elem(k, w0, bf16_to_f32((g32[q] >> sh) & 0xFFFFu),
+                                           bf16_to_f32((p32[q] >> sh) & 0xFFFFu), ma[e], va[e], na[e]);
+                const int lane = (int)(i & 15) + e;
+                const uint64_t wsel = lane < 4 ? c0 : (lane < 8 ? c1 : (lane < 12 ? c2 : c3));
+                uint32_t lo;
+                const uint32_t hi = store_bits(w1, has_res, kSR, (uint32_t)(wsel >> (16 * (lane & 3))) & 0xFFFFu, lo);
+                wo[q] |= hi << sh;
+                ro[q] |= lo << sh;
+                nf = max(nf, hi & 0x7FFFu);
+            }
+        }
+        st_stream(reinterpret_cast<uint4*>(w + i), make_uint4(wo[0], wo[1], wo[2], wo[3]));
+        if (has_res) st_stream(reinterpret_cast<uint4*>(res + i), make_uint4(ro[0], ro[1], ro[2], ro[3]));
+        st_stream(reinterpret_cast<uint4*>(gprev + i), G);
+        st_stream(reinterpret_cast<float4*>(mp + i), *reinterpret_cast<const float4*>(ma));
+        st_stream(reinterpret_cast<float4*>(mp + i + 4), *reinterpret_cast<const float4*>(ma + 4));
+        st_stream(reinterpret_cast<float4*>(vp + i), *reinterpret_cast<const float4*>(va));
+        st_stream(reinterpret_cast<float4*>(vp + i + 4), *reinterpret_cast<const float4*>(va + 4));
+        st_stream(reinterpret_cast<float4*>(np_ + i), *reinterpret_cast<const float4*>(na));
+        st_stream(reinterpret_cast<float4*>(np_ + i + 4), *reinterpret_cast<const float4*>(na + 4));
+    }
+    for (int64_t i = vend + threadIdx.x; i < end; i += kThreads) {
         const float w0 = has_res ? __uint_as_float(((uint32_t)w[i] << 16) | res[i]) : bf16_to_f32(w[i]);
         const uint32_t gb = __ldcs(g + i);
         float m = __ldcs(mp + i), v = __ldcs(vp + i), nn = __ldcs(np_ + i);
@@ -85,17 +156,9 @@ __global__ void __launch_bounds__(kThreads) k_adan_step(NadamLaunch L, AdanPrm k
         __stcs(vp + i, v);
         __stcs(np_ + i, nn);
         __stcs(gprev + i, (uint16_t)gb);
-        const uint32_t b = __float_as_uint(w1);
-        uint32_t hi;
-        if (has_res) {
-            hi = b >> 16;
-            res[i] = (uint16_t)(b & 0xFFFFu);
-        } else if (k.sr) {
-            const uint32_t r = sr_lane(k, c.tensor, i);
-            hi = ((b & 0x7F800000u) == 0x7F800000u) ? (b >> 16) : ((b + r) >> 16);
-        } else {
-            hi = rne_bf16(w1);
-        }
+        uint32_t lo;
+        const uint32_t hi = store_bits(w1, has_res, kSR, (kSR && !has_res) ? sr_lane(k, c.tensor, i) : 0u, lo);
+        if (has_res) res[i] = (uint16_t)lo;
         w[i] = (uint16_t)hi;
         nf = max(nf, hi & 0x7FFFu);
     }
@@ -109,7 +172,8 @@ __global__ void __launch_bounds__(kThreads) k_adan_step(NadamLaunch L, AdanPrm k
 int launch_adan_step(const NadamLaunch& L, const AdanScalars& s, cudaStream_t stream) {
     AdanPrm k{s.lr, s.b1, s.omb1, s.b2, s.omb2, s.b3, s.omb3, s.eps, s.inv_decay, s.sr, s.step, s.seed};
     if (L.n_chunks_total == 0) return OPTIM_OK;
-    k_adan_step<<<L.n_chunks_total, kThreads, 0, stream>>>(L, k);
+    if (s.sr) k_adan_step<true><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k);
+    else k_adan_step<false><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k);
     return check_cuda(cudaGetLastError(), "adan step launch");
 }
 

@@ -42,7 +42,16 @@ constexpr int kFinGroups = kThreads / kFinColsPerItem;   // band groups of a col
 constexpr int kTinySub = kThreads;     // small matrices per staged sub-batch (one per thread)
 constexpr int kTinyPerCta = 8 * kTinySub;
 constexpr int kVecPerCta = kThreads * 8;
-constexpr int64_t kWaveGradBytes = 64ll << 20;   // gradient bytes per wave (L2-resident target)
+// Gradient bytes per wave (the L2-resident target) and the number of waves in flight at once
+// (the caller's stream plus kWaveStreams - 1 internal streams).
+#ifndef LMOPT_WAVE_MB
+#define LMOPT_WAVE_MB 64
+#endif
+#ifndef LMOPT_WAVE_STREAMS
+#define LMOPT_WAVE_STREAMS 2
+#endif
+constexpr int64_t kWaveGradBytes = (int64_t)LMOPT_WAVE_MB << 20;
+constexpr int kWaveStreams = LMOPT_WAVE_STREAMS;
 
 enum : int32_t { kWide = 0, kTiny = 1, kVec = 2 };
 enum : int32_t { kFinRows = 0, kFinCols = 1 };
@@ -736,6 +745,13 @@ struct FactoredPlan {
     Item* d_fin = nullptr;
     std::vector<Wave> waves;
     std::vector<void*> allocs;
+    // waves are independent (disjoint tensors and scratch), so consecutive waves run on
+    // different streams: the caller's and n_aux internal ones, forked from and joined back into
+    // the caller's stream by events
+    int n_aux = 0;
+    cudaStream_t aux[kWaveStreams > 1 ? kWaveStreams - 1 : 1] = {};
+    cudaEvent_t fork_ev = nullptr;
+    cudaEvent_t join_ev[kWaveStreams > 1 ? kWaveStreams - 1 : 1] = {};
 };
 
 template <class T>
@@ -875,11 +891,25 @@ int factored_plan_build(FactoredPlan*& plan, const std::vector<optim_tensor_desc
     if (!rc) rc = alloc_dev(p, &D.den, n, "clip divisors");
     if (!rc) rc = alloc_dev(p, &D.counter, n, "partial counters");
     D.tensors = p->d_tensors;
+    const int n_aux = std::min<int>(kWaveStreams - 1, (int)L.waves.size() - 1);
+    if (!rc && n_aux > 0) {
+        rc = check_cuda(cudaEventCreateWithFlags(&p->fork_ev, cudaEventDisableTiming), "wave fork event");
+        for (int a = 0; !rc && a < n_aux; ++a) {
+            rc = check_cuda(cudaStreamCreateWithFlags(&p->aux[a], cudaStreamNonBlocking), "wave stream");
+            if (!rc) rc = check_cuda(cudaEventCreateWithFlags(&p->join_ev[a], cudaEventDisableTiming), "wave join event");
+            if (!rc) p->n_aux = a + 1;
+        }
+    }
     return rc;
 }
 
 void factored_plan_free(FactoredPlan*& plan) {
     if (!plan) return;
+    for (int a = 0; a < (int)(sizeof(plan->aux) / sizeof(plan->aux[0])); ++a) {
+        if (plan->aux[a]) cudaStreamDestroy(plan->aux[a]);
+        if (plan->join_ev[a]) cudaEventDestroy(plan->join_ev[a]);
+    }
+    if (plan->fork_ev) cudaEventDestroy(plan->fork_ev);
     for (void* a : plan->allocs) cudaFree(a);
     delete plan;
     plan = nullptr;
@@ -890,21 +920,32 @@ int launch_factored_step(const FactoredPlan* p, const uint16_t* const* d_grads, 
     K k{s.b2t, s.alpha, s.eps1, s.eps2, s.clip, s.lr_eff, s.nwdlr, s.mode};
     Dev D = p->dev;
     D.grads = d_grads;
-    for (size_t w = 0; w < p->waves.size(); ++w) {
-        const Wave& wv = p->waves[w];
-        const Item* items = p->d_items + wv.item_off;
-        if (wv.n_total > 0) k_stats<<<wv.n_total, kThreads, 0, stream>>>(D, items, k);
-        if (wv.n_fin > 0) k_final<<<wv.n_fin, kThreads, 0, stream>>>(D, p->d_fin + wv.fin_off, k);
-        if (wv.n_wide > 0) k_rms<<<wv.n_wide, kThreads, 0, stream>>>(D, items, k);
-        if (mid && w + 1 == p->waves.size()) {
-            int rc = check_cuda(cudaEventRecord(mid, stream), "profile event");
-            if (rc) return rc;
-        }
-        if (wv.n_total > 0) k_apply<<<wv.n_total, kThreads, 0, stream>>>(D, items, k);
-        int rc = check_cuda(cudaGetLastError(), "factored step launch");
+    const int ns = 1 + p->n_aux;   // streams in use: wave w runs on stream w % ns (0 = caller's)
+    int rc = OPTIM_OK;
+    if (ns > 1) {
+        rc = check_cuda(cudaEventRecord(p->fork_ev, stream), "wave fork");
+        for (int a = 0; !rc && a < p->n_aux; ++a) rc = check_cuda(cudaStreamWaitEvent(p->aux[a], p->fork_ev, 0), "wave fork");
         if (rc) return rc;
     }
-    return OPTIM_OK;
+    for (size_t w = 0; w < p->waves.size() && !rc; ++w) {
+        const Wave& wv = p->waves[w];
+        const cudaStream_t st = (w % ns == 0) ? stream : p->aux[w % ns - 1];
+        const Item* items = p->d_items + wv.item_off;
+        if (wv.n_total > 0) k_stats<<<wv.n_total, kThreads, 0, st>>>(D, items, k);
+        if (wv.n_fin > 0) k_final<<<wv.n_fin, kThreads, 0, st>>>(D, p->d_fin + wv.fin_off, k);
+        if (wv.n_wide > 0) k_rms<<<wv.n_wide, kThreads, 0, st>>>(D, items, k);
+        if (mid && w + 1 == p->waves.size()) rc = check_cuda(cudaEventRecord(mid, st), "profile event");
+        if (wv.n_total > 0) k_apply<<<wv.n_total, kThreads, 0, st>>>(D, items, k);
+        if (!rc) rc = check_cuda(cudaGetLastError(), "factored step launch");
+    }
+    // join every internal stream back into the caller's (also after a launch error, so that no
+    // internal stream is left ahead of the caller's)
+    for (int a = 0; a < p->n_aux && ns > 1; ++a) {
+        int r2 = check_cuda(cudaEventRecord(p->join_ev[a], p->aux[a]), "wave join");
+        if (!r2) r2 = check_cuda(cudaStreamWaitEvent(stream, p->join_ev[a], 0), "wave join");
+        if (!rc) rc = r2;
+    }
+    return rc;
 }
 
 }  // namespace lmo

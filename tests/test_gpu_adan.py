@@ -16,7 +16,9 @@ HP = dict(lr=3.3e-5, beta1=0.02, beta2=0.08, beta3=0.01, eps=1e-8, weight_decay=
 def test_adan_bit_exact(orc, rounding):
     from memory_lean_optimizer_gb300 import build, engine
     build.build()
-    sizes = [1, 100, 4097, 16384, 50001]
+    # 128-bit path where n % 4 == 0 (100, 16384, 40004: whole chunks, 8-element tails), element
+    # path otherwise (1, 4097, 50001)
+    sizes = [1, 100, 4097, 16384, 50001, 40004]
     seed, key = 50, 777
     hp = dict(HP, stochastic_rounding=int(rounding == "sr"), seed=key)
     masters = [W.master_weights((n,), seed, i) for i, n in enumerate(sizes)]
