@@ -12,7 +12,8 @@
 // Tensor classes and their kernels:
 //   wide  (ndim >= 2, rows*cols > 16): 128x256 tiles, 256 threads (8 warps x 16 rows, lane = 8 cols)
 //   tiny  (ndim >= 2, rows*cols <= 16, e.g. 3x3 conv kernels): 2048 matrices per CTA, staged
-//         through shared memory in sub-batches of 256, one thread per matrix
+//         through shared memory in sub-batches of 256 (64 for shapes beyond 9 elements or 6
+//         statistics), one thread per matrix, cp.async double buffering
 //   vector (ndim == 1): one thread per element, full fp32 second moment
 // Per wave of tensors (waves keep the wave's gradients, read three times, within L2):
 //   1. k_stats  : wide tiles -> row/column partial sums of q;  tiny/vector -> state EMA, u, sum u^2
@@ -45,7 +46,7 @@ constexpr int kVecPerCta = kThreads * 8;
 // Gradient bytes per wave (the L2-resident target) and the number of waves in flight at once
 // (the caller's stream plus kWaveStreams - 1 internal streams).
 #ifndef LMOPT_WAVE_MB
-#define LMOPT_WAVE_MB 64
+#define LMOPT_WAVE_MB 96
 #endif
 #ifndef LMOPT_WAVE_STREAMS
 #define LMOPT_WAVE_STREAMS 2
@@ -127,6 +128,20 @@ struct Comp {
     }
     __device__ __forceinline__ float value() const { return __fadd_rn(s, c); }
 };
+
+// Programmatic dependent launch.  The four kernels of a wave are launched so that each may
+// start while its predecessor on the stream drains.  pdl_wait blocks (in hardware) until the
+// predecessor grid has completed and its writes are visible; before it a kernel only reads what
+// no kernel of the step writes (its work items, the tensor table, gradients, and in the update
+// kernel the weight words, which only that kernel writes).  Every kernel signals its dependents
+// only after its own wait, so a kernel that starts early can rely on everything before its
+// predecessor having completed.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_sync() {
+    pdl_wait();
+    pdl_release();
+}
 
 // Block-wide fp32 sum in a fixed tree; result valid in every thread.
 __device__ float block_sum(float x, float* sm /* 32 floats */) {
@@ -216,14 +231,34 @@ __device__ __forceinline__ void unstage(T* dst, const T* src, int n, bool stream
     }
 }
 
-// Shared-memory staging area of the small-matrix class: per sub-batch of kTinySub matrices,
-// gradient / weight / residual words (up to 16 per matrix) and the R then C statistics (up to 17
-// floats per matrix, since rows*cols <= 16 implies rows + cols <= 17).
-constexpr int kTinyWords = kTinySub * 16;
-constexpr int kTinyStats = kTinySub * 17;
-constexpr int kStatsSmem = kTinyWords * 2 + kTinyStats * 4;
-constexpr int kApplySmem = 3 * kTinyWords * 2 + kTinyStats * 4;
+// Shared-memory staging of the small-matrix class, two buffers (double buffering).  A buffer
+// holds one sub-batch: gradient / weight / residual words and the R then C statistics.  It is
+// sized for kTinySub matrices of up to 9 words and 6 statistics (3x3, 1x1, 2x2, 2x4 ...); other
+// small shapes (rows*cols <= 16, hence rows + cols <= 17) take sub-batches of kTinySub / 4.
+constexpr int kTinyWords = kTinySub * 9;    // u16 words per word plane per buffer
+constexpr int kTinyStats = kTinySub * 6;    // floats per buffer
+static_assert((kTinySub / 4) * 16 <= kTinyWords && (kTinySub / 4) * 17 <= kTinyStats, "small sub-batch must fit");
+constexpr int kStatsSmem = 2 * (kTinyWords * 2 + kTinyStats * 4);
+constexpr int kApplySmem = 2 * (3 * kTinyWords * 2 + kTinyStats * 4);
 static_assert(kStatsSmem >= 8 * (kTC + 1) * 4, "wide column buffer must fit the shared area");
+static_assert((kTinyWords * 2) % 16 == 0 && (kTinyStats * 4) % 16 == 0, "buffers must stay 16-byte aligned");
+
+__device__ __forceinline__ int tiny_sub(int r, int c) { return (r * c <= 9 && r + c <= 6) ? kTinySub : kTinySub / 4; }
+
+// Asynchronous 16-byte global -> shared copies (cp.async, completion tracked per thread by
+// commit groups; the hardware wait needs no polling loop).
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+// `bytes` a multiple of 16, both addresses 16-byte aligned.
+__device__ __forceinline__ void stage_async(void* dst, const void* src, int bytes) {
+    for (int i = threadIdx.x; i < (bytes >> 4); i += blockDim.x)
+        cp_async16(static_cast<char*>(dst) + 16 * i, static_cast<const char*>(src) + 16 * i);
+}
 
 // One small matrix (rows*cols <= 16) of a tiny-class tensor: R, C EMAs (written back), mean(R),
 // and the matrix's sum of squared updates.  The fixed-size form keeps everything in registers.
@@ -265,7 +300,7 @@ __device__ __forceinline__ float tiny_stats(const uint16_t* gm, float* Rs, float
     }
     return acc;
 }
-__device__ float tiny_stats_any(const uint16_t* gm, float* Rs, float* Cs, int r, int c, const K& k) {
+__device__ __forceinline__ float tiny_stats_any(const uint16_t* gm, float* Rs, float* Cs, int r, int c, const K& k) {
     float q[16], rsum[16], csum[16];
     for (int e = 0; e < r * c; ++e) q[e] = qval(bf16_to_f32(gm[e]), k);
     float rtot = 0.f;
@@ -296,6 +331,11 @@ __device__ float tiny_stats_any(const uint16_t* gm, float* Rs, float* Cs, int r,
     return acc;
 }
 
+// Statistics of one staged small matrix (the 3x3 form fully in registers).
+__device__ __noinline__ float tiny_stats_one(const uint16_t* gm, float* Rs, float* Cs, int r, int c, const K& k) {
+    return (r == 3 && c == 3) ? tiny_stats<3, 3>(gm, Rs, Cs, k) : tiny_stats_any(gm, Rs, Cs, r, c, k);
+}
+
 // Apply step of one small matrix on staged words (w, res, g and R, C in shared memory).
 template <int RR, int CC>
 __device__ __forceinline__ void tiny_apply(uint16_t* wm, uint16_t* rm, const uint16_t* gm, const float* Rs,
@@ -322,7 +362,7 @@ __device__ __forceinline__ void tiny_apply(uint16_t* wm, uint16_t* rm, const uin
         }
     }
 }
-__device__ void tiny_apply_any(uint16_t* wm, uint16_t* rm, const uint16_t* gm, const float* Rs, const float* Cs,
+__device__ __forceinline__ void tiny_apply_any(uint16_t* wm, uint16_t* rm, const uint16_t* gm, const float* Rs, const float* Cs,
                                int r, int c, bool has_res, float den, const K& k) {
     float rtot = 0.f, cfac[16];
     for (int i = 0; i < r; ++i) rtot = __fadd_rn(rtot, Rs[i]);
@@ -340,6 +380,13 @@ __device__ void tiny_apply_any(uint16_t* wm, uint16_t* rm, const uint16_t* gm, c
     }
 }
 
+// Apply step of one staged small matrix (the 3x3 form fully in registers).
+__device__ __noinline__ void tiny_apply_one(uint16_t* wm, uint16_t* rm, const uint16_t* gm, const float* Rs,
+                                            const float* Cs, int r, int c, bool has_res, float den, const K& k) {
+    if (r == 3 && c == 3) tiny_apply<3, 3>(wm, rm, gm, Rs, Cs, has_res, den, k);
+    else tiny_apply_any(wm, rm, gm, Rs, Cs, r, c, has_res, den, k);
+}
+
 // Eight gradient words of one 128-bit load, as fp32 (bf16 -> fp32 is exact).
 __device__ __forceinline__ float g_at(const uint4& x, int j) {
     const uint32_t w = j < 2 ? x.x : (j < 4 ? x.y : (j < 6 ? x.z : x.w));
@@ -354,6 +401,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_stats(Dev D, const Item* items,
     const FTensor t = D.tensors[it.tensor];
     const uint16_t* __restrict__ g = D.grads[it.tensor];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    pdl_sync();
 
     if (it.cls == kWide) {
         float (*cols)[kTC + 1] = reinterpret_cast<float (*)[kTC + 1]>(smem);
@@ -426,28 +474,65 @@ __global__ void __launch_bounds__(kThreads, 4) k_stats(Dev D, const Item* items,
 
     float acc = 0.f;
     if (it.cls == kTiny) {
-        // kTinyPerCta matrices in sub-batches of kTinySub (one matrix per thread), gradients and
-        // statistics staged through shared memory with 128-bit copies
-        const int r = (int)t.R, c = (int)t.C, rc = r * c;
-        uint16_t* sg = reinterpret_cast<uint16_t*>(smem);
-        float* sf = reinterpret_cast<float*>(smem + kTinyWords * 2);
+        // kTinyPerCta matrices in sub-batches (one matrix per thread), gradients and statistics
+        // staged through shared memory; when every sub-batch is whole and aligned, the next
+        // sub-batch's copies are in flight while the current one is computed
+        const int r = (int)t.R, c = (int)t.C, rc = r * c, sub = tiny_sub(r, c);
+        // buffer b: words at smem + b*kTinyWords*2, statistics after both word buffers
+        auto words = [&](int b) { return reinterpret_cast<uint16_t*>(smem + b * (kTinyWords * 2)); };
+        auto stats = [&](int b) { return reinterpret_cast<float*>(smem + 2 * kTinyWords * 2 + b * (kTinyStats * 4)); };
         const int64_t mend = t.B < (int64_t)it.x + kTinyPerCta ? t.B : (int64_t)it.x + kTinyPerCta;
-        for (int64_t m0 = it.x; m0 < mend; m0 += kTinySub) {
-            const int nm = (int)(mend - m0 < kTinySub ? mend - m0 : kTinySub);
-            float* sR = sf;
-            float* sC = sf + nm * r;
-            stage(sg, g + m0 * rc, nm * rc);
-            stage(sR, t.row + m0 * r, nm * r);
-            stage(sC, t.col + m0 * c, nm * c);
-            __syncthreads();
-            const int i = threadIdx.x;
-            if (i < nm)
-                acc = __fadd_rn(acc, (r == 3 && c == 3) ? tiny_stats<3, 3>(sg + i * rc, sR + i * r, sC + i * c, k)
-                                                        : tiny_stats_any(sg + i * rc, sR + i * r, sC + i * c, r, c, k));
-            __syncthreads();
-            unstage(t.row + m0 * r, sR, nm * r, false);
-            unstage(t.col + m0 * c, sC, nm * c, false);
-            __syncthreads();
+        const int64_t nmat = mend - it.x;
+        const bool pipe = nmat % sub == 0 && aligned16(g) && aligned16(t.row) && aligned16(t.col);
+        const int nsub = (int)((nmat + sub - 1) / sub);
+        if (pipe) {
+            for (int kk = -1; kk < nsub; ++kk) {
+                // issue sub-batch kk+1 (its buffer was released by the barrier ending kk-1)
+                if (kk + 1 < nsub) {
+                    const int64_t m1 = it.x + (int64_t)(kk + 1) * sub;
+                    const int b1 = (kk + 1) & 1;
+                    stage_async(words(b1), g + m1 * rc, sub * rc * 2);
+                    stage_async(stats(b1), t.row + m1 * r, sub * r * 4);
+                    stage_async(stats(b1) + sub * r, t.col + m1 * c, sub * c * 4);
+                    cp_async_commit();
+                }
+                if (kk < 0) continue;
+                if (kk + 1 < nsub) cp_async_wait<1>();
+                else cp_async_wait<0>();
+                __syncthreads();
+                const int b = kk & 1, i = threadIdx.x;
+                float* sR = stats(b);
+                float* sC = sR + sub * r;
+                if (i < sub) {
+                    const uint16_t* gm = words(b) + i * rc;
+                    acc = __fadd_rn(acc, tiny_stats_one(gm, sR + i * r, sC + i * c, r, c, k));
+                }
+                __syncthreads();
+                const int64_t m0 = it.x + (int64_t)kk * sub;
+                unstage(t.row + m0 * r, sR, sub * r, false);
+                unstage(t.col + m0 * c, sC, sub * c, false);
+                __syncthreads();
+            }
+        } else {
+            for (int kk = 0; kk < nsub; ++kk) {
+                const int64_t m0 = it.x + (int64_t)kk * sub;
+                const int nm = (int)(mend - m0 < sub ? mend - m0 : sub);
+                float* sR = stats(0);
+                float* sC = sR + nm * r;
+                stage(words(0), g + m0 * rc, nm * rc);
+                stage(sR, t.row + m0 * r, nm * r);
+                stage(sC, t.col + m0 * c, nm * c);
+                __syncthreads();
+                const int i = threadIdx.x;
+                if (i < nm) {
+                    const uint16_t* gm = words(0) + i * rc;
+                    acc = __fadd_rn(acc, tiny_stats_one(gm, sR + i * r, sC + i * c, r, c, k));
+                }
+                __syncthreads();
+                unstage(t.row + m0 * r, sR, nm * r, false);
+                unstage(t.col + m0 * c, sC, nm * c, false);
+                __syncthreads();
+            }
         }
     } else {  // kVec
         const int64_t e0 = (int64_t)it.x * kVecPerCta;
@@ -472,6 +557,7 @@ __global__ void __launch_bounds__(kThreads) k_final(Dev D, const Item* items, K 
     const Item it = items[blockIdx.x];
     const FTensor t = D.tensors[it.tensor];
     const int64_t b = it.x;
+    pdl_sync();
     if (it.cls == kFinRows) {
         // R EMA of 256 rows (one per thread), their sum, and mean(R) by the matrix's last block
         const int64_t i = (int64_t)it.cb * kFinRowsPerItem + threadIdx.x;
@@ -551,8 +637,17 @@ __global__ void __launch_bounds__(kThreads, 4) k_rms(Dev D, const Item* items, K
     const int ncols = cols_in(t.C - col0);
     const bool vec = aligned16(g) && (t.C % 8 == 0);      // same for every lane of the block
     const bool lane_ok = ncols == 8;                       // C % 8 == 0: 8 or 0 columns
-    const float rbar = D.rbar[t.mat_off + b];
     const int64_t row0 = (int64_t)it.band * kTR + warp;
+    // the first eight rows' gradients are loaded before waiting for the finalize kernel
+    uint4 x[8];
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const int64_t row = row0 + 8 * kk;
+        x[kk] = (vec && row < t.R && lane_ok)
+                    ? __ldcg(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0)) : make_uint4(0, 0, 0, 0);
+    }
+    pdl_sync();
+    const float rbar = D.rbar[t.mat_off + b];
     float ccv[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) ccv[j] = j < ncols ? D.cc[t.cc_off + b * t.C + col0 + j] : 0.f;
@@ -560,13 +655,13 @@ __global__ void __launch_bounds__(kThreads, 4) k_rms(Dev D, const Item* items, K
     if (vec) {
 #pragma unroll 1
         for (int kb = 0; kb < kTR / 64; ++kb) {
-            uint4 x[8];
             float rv[8];
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const int64_t row = row0 + 64 * kb + 8 * kk;
                 const bool ok = row < t.R && lane_ok;
-                x[kk] = ok ? __ldcg(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0)) : make_uint4(0, 0, 0, 0);
+                if (kb > 0)
+                    x[kk] = ok ? __ldcg(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0)) : make_uint4(0, 0, 0, 0);
                 rv[kk] = ok ? t.row[b * t.R + row] : 0.f;
             }
 #pragma unroll
@@ -629,7 +724,6 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
     const Item it = items[blockIdx.x];
     const FTensor t = D.tensors[it.tensor];
     const uint16_t* __restrict__ g = D.grads[it.tensor];
-    const float den = D.den[it.tensor];
     const bool has_res = t.res != nullptr;
 
     if (it.cls == kWide) {
@@ -638,29 +732,40 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
         const int64_t col0 = (int64_t)it.cb * kTC + lane * 8;
         const int ncols = cols_in(t.C - col0);
         const bool vec = aligned16(g) && aligned16(t.w) && (!has_res || aligned16(t.res)) && (t.C % 8 == 0);
-        float ccv[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) ccv[j] = j < ncols ? D.cc[t.cc_off + b * t.C + col0 + j] : 0.f;
-        const float rbar = D.rbar[t.mat_off + b];
         const int64_t row0 = (int64_t)it.band * kTR + warp;
         if (vec) {
             if (ncols != 8) return;   // no shuffles below: lanes may leave independently
-            // two rows per iteration, all six 128-bit loads issued before the arithmetic
+            // two rows per iteration, all six 128-bit loads issued before the arithmetic; the
+            // first pair is loaded before waiting for the RMS kernel (gradients and weights are
+            // written by no earlier kernel of the step)
+            uint4 GA = make_uint4(0, 0, 0, 0), WA = GA, RA = GA, GB = GA, WB = GA, RB = GA;
+            auto load_pair = [&](int kk) {
+                const int64_t rowA = row0 + 8 * kk;
+                if (rowA >= t.R) return;
+                const int64_t offA = (b * t.R + rowA) * t.C + col0, offB = offA + 8 * t.C;
+                GA = __ldcg(reinterpret_cast<const uint4*>(g + offA));
+                WA = ld_stream(reinterpret_cast<const uint4*>(t.w + offA));
+                if (has_res) RA = ld_stream(reinterpret_cast<const uint4*>(t.res + offA));
+                if (rowA + 8 < t.R) {
+                    GB = __ldcg(reinterpret_cast<const uint4*>(g + offB));
+                    WB = ld_stream(reinterpret_cast<const uint4*>(t.w + offB));
+                    if (has_res) RB = ld_stream(reinterpret_cast<const uint4*>(t.res + offB));
+                }
+            };
+            load_pair(0);
+            pdl_sync();
+            const float den = D.den[it.tensor];
+            float ccv[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) ccv[j] = D.cc[t.cc_off + b * t.C + col0 + j];
+            const float rbar = D.rbar[t.mat_off + b];
 #pragma unroll 1
             for (int kk = 0; kk < kTR / 8; kk += 2) {
                 const int64_t rowA = row0 + 8 * kk, rowB = rowA + 8;
                 if (rowA >= t.R) break;
                 const bool hasB = rowB < t.R;
                 const int64_t offA = (b * t.R + rowA) * t.C + col0, offB = offA + 8 * t.C;
-                const uint4 GA = __ldcg(reinterpret_cast<const uint4*>(g + offA));
-                uint4 WA = ld_stream(reinterpret_cast<const uint4*>(t.w + offA));
-                uint4 RA = has_res ? ld_stream(reinterpret_cast<const uint4*>(t.res + offA)) : make_uint4(0, 0, 0, 0);
-                uint4 GB = make_uint4(0, 0, 0, 0), WB = GB, RB = GB;
-                if (hasB) {
-                    GB = __ldcg(reinterpret_cast<const uint4*>(g + offB));
-                    WB = ld_stream(reinterpret_cast<const uint4*>(t.w + offB));
-                    if (has_res) RB = ld_stream(reinterpret_cast<const uint4*>(t.res + offB));
-                }
+                if (kk > 0) load_pair(kk);
                 const float rvA = t.row[b * t.R + rowA], rvB = hasB ? t.row[b * t.R + rowB] : 1.0f;
                 apply8(GA, WA, RA, rsqrt_rn(__fdiv_rn(rvA, rbar)), ccv, has_res, den, k);
                 st_stream(reinterpret_cast<uint4*>(t.w + offA), WA);
@@ -672,6 +777,12 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
                 }
             }
         } else {
+            pdl_sync();
+            const float den = D.den[it.tensor];
+            float ccv[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) ccv[j] = j < ncols ? D.cc[t.cc_off + b * t.C + col0 + j] : 0.f;
+            const float rbar = D.rbar[t.mat_off + b];
             for (int kk = 0; kk < kTR / 8; ++kk) {
                 const int64_t row = row0 + 8 * kk;
                 if (row >= t.R) break;
@@ -688,34 +799,80 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
         }
         return;
     }
+    pdl_sync();
+    const float den = D.den[it.tensor];
     if (it.cls == kTiny) {
-        const int r = (int)t.R, c = (int)t.C, rc = r * c;
-        uint16_t* sg = reinterpret_cast<uint16_t*>(smem);
-        uint16_t* sw = sg + kTinyWords;
-        uint16_t* sr = sw + kTinyWords;
-        float* sf = reinterpret_cast<float*>(sr + kTinyWords);
+        // as in k_stats: sub-batches staged through shared memory, double-buffered when whole
+        // and aligned; w and res are updated in shared memory and streamed back
+        const int r = (int)t.R, c = (int)t.C, rc = r * c, sub = tiny_sub(r, c);
+        constexpr int kBuf = 3 * kTinyWords * 2 + kTinyStats * 4;
+        uint16_t* sg[2];
+        uint16_t* sw[2];
+        uint16_t* sr[2];
+        float* sf[2];
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            sg[b] = reinterpret_cast<uint16_t*>(smem + b * kBuf);
+            sw[b] = sg[b] + kTinyWords;
+            sr[b] = sw[b] + kTinyWords;
+            sf[b] = reinterpret_cast<float*>(sr[b] + kTinyWords);
+        }
         const int64_t mend = t.B < (int64_t)it.x + kTinyPerCta ? t.B : (int64_t)it.x + kTinyPerCta;
-        for (int64_t m0 = it.x; m0 < mend; m0 += kTinySub) {
-            const int nm = (int)(mend - m0 < kTinySub ? mend - m0 : kTinySub);
-            float* sR = sf;
-            float* sC = sf + nm * r;
-            stage(sg, g + m0 * rc, nm * rc);
-            stage(sw, t.w + m0 * rc, nm * rc);
-            if (has_res) stage(sr, t.res + m0 * rc, nm * rc);
-            stage(sR, t.row + m0 * r, nm * r);
-            stage(sC, t.col + m0 * c, nm * c);
-            __syncthreads();
+        const int64_t nmat = mend - it.x;
+        const bool pipe = nmat % sub == 0 && aligned16(g) && aligned16(t.w) && (!has_res || aligned16(t.res)) &&
+                          aligned16(t.row) && aligned16(t.col);
+        const int nsub = (int)((nmat + sub - 1) / sub);
+        auto compute = [&](int b, int nm) {
             const int i = threadIdx.x;
-            if (i < nm) {
-                if (r == 3 && c == 3)
-                    tiny_apply<3, 3>(sw + i * rc, sr + i * rc, sg + i * rc, sR + i * r, sC + i * c, has_res, den, k);
-                else
-                    tiny_apply_any(sw + i * rc, sr + i * rc, sg + i * rc, sR + i * r, sC + i * c, r, c, has_res, den, k);
+            if (i >= nm) return;
+            const float* sR = sf[b];
+            const float* sC = sf[b] + nm * r;
+            tiny_apply_one(sw[b] + i * rc, sr[b] + i * rc, sg[b] + i * rc, sR + i * r, sC + i * c, r, c, has_res, den, k);
+        };
+        if (pipe) {
+            auto issue = [&](int kk) {
+                const int64_t m0 = it.x + (int64_t)kk * sub;
+                const int b = kk & 1;
+                stage_async(sg[b], g + m0 * rc, sub * rc * 2);
+                stage_async(sw[b], t.w + m0 * rc, sub * rc * 2);
+                if (has_res) stage_async(sr[b], t.res + m0 * rc, sub * rc * 2);
+                stage_async(sf[b], t.row + m0 * r, sub * r * 4);
+                stage_async(sf[b] + sub * r, t.col + m0 * c, sub * c * 4);
+                cp_async_commit();
+            };
+            issue(0);
+            for (int kk = 0; kk < nsub; ++kk) {
+                if (kk + 1 < nsub) {
+                    issue(kk + 1);   // its buffer was released by the barrier ending iteration kk-1
+                    cp_async_wait<1>();
+                } else {
+                    cp_async_wait<0>();
+                }
+                __syncthreads();
+                const int b = kk & 1;
+                compute(b, sub);
+                __syncthreads();
+                const int64_t m0 = it.x + (int64_t)kk * sub;
+                unstage(t.w + m0 * rc, sw[b], sub * rc, true);
+                if (has_res) unstage(t.res + m0 * rc, sr[b], sub * rc, true);
+                __syncthreads();
             }
-            __syncthreads();
-            unstage(t.w + m0 * rc, sw, nm * rc, true);
-            if (has_res) unstage(t.res + m0 * rc, sr, nm * rc, true);
-            __syncthreads();
+        } else {
+            for (int kk = 0; kk < nsub; ++kk) {
+                const int64_t m0 = it.x + (int64_t)kk * sub;
+                const int nm = (int)(mend - m0 < sub ? mend - m0 : sub);
+                stage(sg[0], g + m0 * rc, nm * rc);
+                stage(sw[0], t.w + m0 * rc, nm * rc);
+                if (has_res) stage(sr[0], t.res + m0 * rc, nm * rc);
+                stage(sf[0], t.row + m0 * r, nm * r);
+                stage(sf[0] + nm * r, t.col + m0 * c, nm * c);
+                __syncthreads();
+                compute(0, nm);
+                __syncthreads();
+                unstage(t.w + m0 * rc, sw[0], nm * rc, true);
+                if (has_res) unstage(t.res + m0 * rc, sr[0], nm * rc, true);
+                __syncthreads();
+            }
         }
         return;
     }
@@ -915,6 +1072,23 @@ void factored_plan_free(FactoredPlan*& plan) {
     plan = nullptr;
 }
 
+// Launches one kernel of the step with programmatic stream serialization allowed (the kernel
+// may start while its predecessor on the stream drains; it waits with griddepcontrol.wait).
+template <typename Kern, typename... Args>
+static cudaError_t launch_pdl(Kern kern, int grid, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 int launch_factored_step(const FactoredPlan* p, const uint16_t* const* d_grads, const FactoredScalars& s,
                          cudaStream_t stream, cudaEvent_t mid) {
     K k{s.b2t, s.alpha, s.eps1, s.eps2, s.clip, s.lr_eff, s.nwdlr, s.mode};
@@ -931,12 +1105,12 @@ int launch_factored_step(const FactoredPlan* p, const uint16_t* const* d_grads, 
         const Wave& wv = p->waves[w];
         const cudaStream_t st = (w % ns == 0) ? stream : p->aux[w % ns - 1];
         const Item* items = p->d_items + wv.item_off;
-        if (wv.n_total > 0) k_stats<<<wv.n_total, kThreads, 0, st>>>(D, items, k);
-        if (wv.n_fin > 0) k_final<<<wv.n_fin, kThreads, 0, st>>>(D, p->d_fin + wv.fin_off, k);
-        if (wv.n_wide > 0) k_rms<<<wv.n_wide, kThreads, 0, st>>>(D, items, k);
-        if (mid && w + 1 == p->waves.size()) rc = check_cuda(cudaEventRecord(mid, st), "profile event");
-        if (wv.n_total > 0) k_apply<<<wv.n_total, kThreads, 0, st>>>(D, items, k);
-        if (!rc) rc = check_cuda(cudaGetLastError(), "factored step launch");
+        const Item* fin = p->d_fin + wv.fin_off;
+        if (wv.n_total > 0) rc = check_cuda(launch_pdl(k_stats, wv.n_total, st, D, items, k), "factored stats launch");
+        if (!rc && wv.n_fin > 0) rc = check_cuda(launch_pdl(k_final, wv.n_fin, st, D, fin, k), "factored finalize launch");
+        if (!rc && wv.n_wide > 0) rc = check_cuda(launch_pdl(k_rms, wv.n_wide, st, D, items, k), "factored rms launch");
+        if (!rc && mid && w + 1 == p->waves.size()) rc = check_cuda(cudaEventRecord(mid, st), "profile event");
+        if (!rc && wv.n_total > 0) rc = check_cuda(launch_pdl(k_apply, wv.n_total, st, D, items, k), "factored apply launch");
     }
     // join every internal stream back into the caller's (also after a launch error, so that no
     // internal stream is left ahead of the caller's)
