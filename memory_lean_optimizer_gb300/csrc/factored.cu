@@ -155,9 +155,16 @@ __device__ float block_sum(float x, float* sm /* 32 floats */) {
     return y;
 }
 
-__device__ __forceinline__ void apply_elem(uint32_t& hi, uint32_t& lo, bool has_res, float u, float den, const K& k) {
+// Per-tensor update scale: lr when the update is not clipped (den == 1), else fl(lr / den).  The
+// clipped update is then fl(u * fl(lr / den)) rather than fl(fl(u / den) * lr): one multiply per
+// element instead of a division, within about one ulp of the update.
+__device__ __forceinline__ float update_scale(float den, const K& k) {
+    return den == 1.0f ? k.lr_eff : __fdiv_rn(k.lr_eff, den);
+}
+
+__device__ __forceinline__ void apply_elem(uint32_t& hi, uint32_t& lo, bool has_res, float u, float s, const K& k) {
     float w = has_res ? __uint_as_float((hi << 16) | lo) : bf16_to_f32(hi);
-    const float uu = den == 1.0f ? __fmul_rn(u, k.lr_eff) : __fmul_rn(__fdiv_rn(u, den), k.lr_eff);
+    const float uu = __fmul_rn(u, s);
     if (k.nwdlr != 0.0f) w = __fadd_rn(w, __fmul_rn(w, k.nwdlr));
     w = __fsub_rn(w, uu);
     const uint32_t b = __float_as_uint(w);
@@ -339,7 +346,7 @@ __device__ __noinline__ float tiny_stats_one(const uint16_t* gm, float* Rs, floa
 // Apply step of one small matrix on staged words (w, res, g and R, C in shared memory).
 template <int RR, int CC>
 __device__ __forceinline__ void tiny_apply(uint16_t* wm, uint16_t* rm, const uint16_t* gm, const float* Rs,
-                                           const float* Cs, bool has_res, float den, const K& k) {
+                                           const float* Cs, bool has_res, float us, const K& k) {
     float rtot = 0.f, rv[RR], cfac[CC];
 #pragma unroll
     for (int i = 0; i < RR; ++i) {
@@ -356,14 +363,14 @@ __device__ __forceinline__ void tiny_apply(uint16_t* wm, uint16_t* rm, const uin
         for (int j = 0; j < CC; ++j) {
             const int e = i * CC + j;
             uint32_t hi = wm[e], lo = has_res ? rm[e] : 0u;
-            apply_elem(hi, lo, has_res, __fmul_rn(__fmul_rn(rr, cfac[j]), bf16_to_f32(gm[e])), den, k);
+            apply_elem(hi, lo, has_res, __fmul_rn(__fmul_rn(rr, cfac[j]), bf16_to_f32(gm[e])), us, k);
             wm[e] = (uint16_t)hi;
             if (has_res) rm[e] = (uint16_t)lo;
         }
     }
 }
 __device__ __forceinline__ void tiny_apply_any(uint16_t* wm, uint16_t* rm, const uint16_t* gm, const float* Rs, const float* Cs,
-                               int r, int c, bool has_res, float den, const K& k) {
+                               int r, int c, bool has_res, float us, const K& k) {
     float rtot = 0.f, cfac[16];
     for (int i = 0; i < r; ++i) rtot = __fadd_rn(rtot, Rs[i]);
     const float rbar = __fdiv_rn(rtot, (float)r);
@@ -373,7 +380,7 @@ __device__ __forceinline__ void tiny_apply_any(uint16_t* wm, uint16_t* rm, const
         for (int j = 0; j < c; ++j) {
             const int e = i * c + j;
             uint32_t hi = wm[e], lo = has_res ? rm[e] : 0u;
-            apply_elem(hi, lo, has_res, __fmul_rn(__fmul_rn(rr, cfac[j]), bf16_to_f32(gm[e])), den, k);
+            apply_elem(hi, lo, has_res, __fmul_rn(__fmul_rn(rr, cfac[j]), bf16_to_f32(gm[e])), us, k);
             wm[e] = (uint16_t)hi;
             if (has_res) rm[e] = (uint16_t)lo;
         }
@@ -382,9 +389,40 @@ __device__ __forceinline__ void tiny_apply_any(uint16_t* wm, uint16_t* rm, const
 
 // Apply step of one staged small matrix (the 3x3 form fully in registers).
 __device__ __noinline__ void tiny_apply_one(uint16_t* wm, uint16_t* rm, const uint16_t* gm, const float* Rs,
-                                            const float* Cs, int r, int c, bool has_res, float den, const K& k) {
-    if (r == 3 && c == 3) tiny_apply<3, 3>(wm, rm, gm, Rs, Cs, has_res, den, k);
-    else tiny_apply_any(wm, rm, gm, Rs, Cs, r, c, has_res, den, k);
+                                            const float* Cs, int r, int c, bool has_res, float us, const K& k) {
+    if (r == 3 && c == 3) tiny_apply<3, 3>(wm, rm, gm, Rs, Cs, has_res, us, k);
+    else tiny_apply_any(wm, rm, gm, Rs, Cs, r, c, has_res, us, k);
+}
+
+// Packed fp32 pairs: __fmul2_rn / __fadd2_rn / __ffma2_rn round each component exactly as the
+// scalar _rn operations, so pairing changes no result, only the instruction count.
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+// The two bf16 values of one 32-bit word as fp32 (exact), low half first.
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// Sums each of v[0..7] over the 32 lanes of the warp in 9 shuffles (a transposing butterfly:
+// every exchange halves the number of values a lane carries).  Lanes 4r..4r+3 return the total
+// of v[r]; the tree is fixed and each pairwise add is commutative, so the four copies agree.
+__device__ __forceinline__ float warp_sum8(const float (&v)[8], int lane) {
+    const unsigned full = 0xFFFFFFFFu;
+    float a[4], b[2];
+    const bool h4 = lane & 16, h3 = lane & 8, h2 = lane & 4;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float keep = h4 ? v[i + 4] : v[i], send = h4 ? v[i] : v[i + 4];
+        a[i] = __fadd_rn(keep, __shfl_xor_sync(full, send, 16));
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float keep = h3 ? a[i + 2] : a[i], send = h3 ? a[i] : a[i + 2];
+        b[i] = __fadd_rn(keep, __shfl_xor_sync(full, send, 8));
+    }
+    const float keep = h2 ? b[1] : b[0], send = h2 ? b[0] : b[1];
+    float c = __fadd_rn(keep, __shfl_xor_sync(full, send, 4));
+    c = __fadd_rn(c, __shfl_xor_sync(full, c, 2));
+    return __fadd_rn(c, __shfl_xor_sync(full, c, 1));
 }
 
 // Eight gradient words of one 128-bit load, as fp32 (bf16 -> fp32 is exact).
@@ -415,6 +453,8 @@ __global__ void __launch_bounds__(kThreads, 4) k_stats(Dev D, const Item* items,
         const int64_t row0 = (int64_t)it.band * kTR + warp;   // this warp's rows: row0 + 8*kk
         float cacc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         if (vec) {
+            const float eq = k.mode == 0 ? k.eps1 : 0.0f;   // + 0 leaves g*g unchanged (Prodigy mode)
+            float2 c2[4] = {f2(0.f), f2(0.f), f2(0.f), f2(0.f)};
 #pragma unroll 1
             for (int kb = 0; kb < kTR / 64; ++kb) {
                 // eight rows' loads issued before any use (memory-level parallelism)
@@ -426,21 +466,33 @@ __global__ void __launch_bounds__(kThreads, 4) k_stats(Dev D, const Item* items,
                                 ? __ldcg(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0))
                                 : make_uint4(0, 0, 0, 0);
                 }
+                float rs[8];
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const int64_t row = row0 + 64 * kb + 8 * kk;
-                    float rs = 0.f;
+                    rs[kk] = 0.f;
                     if (lane_ok && row < t.R) {
+                        const uint32_t wd[4] = {x[kk].x, x[kk].y, x[kk].z, x[kk].w};
+                        float2 r2 = f2(0.f);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float q = qval(g_at(x[kk], j), k);
-                            rs = __fadd_rn(rs, q);
-                            cacc[j] = __fadd_rn(cacc[j], q);
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 gq = bf16x2_to_f2(wd[q]);
+                            const float2 qq = __fadd2_rn(__fmul2_rn(gq, gq), f2(eq));
+                            r2 = __fadd2_rn(r2, qq);
+                            c2[q] = __fadd2_rn(c2[q], qq);
                         }
+                        rs[kk] = __fadd_rn(r2.x, r2.y);
                     }
-                    rs = warp_sum_f32(rs);   // every lane of the warp, every iteration
-                    if (lane == 0 && row < t.R) D.rowpart[t.rowpart_off + (b * t.R + row) * t.ncb + it.cb] = rs;
                 }
+                // every lane, every batch: lanes 4r..4r+3 get row (row0 + 64 kb + 8 r)
+                const float tot = warp_sum8(rs, lane);
+                const int64_t row = row0 + 64 * kb + 8 * (lane >> 2);
+                if ((lane & 3) == 0 && row < t.R) D.rowpart[t.rowpart_off + (b * t.R + row) * t.ncb + it.cb] = tot;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                cacc[2 * q] = c2[q].x;
+                cacc[2 * q + 1] = c2[q].y;
             }
         } else {
             for (int kk = 0; kk < kTR / 8; ++kk) {
@@ -653,29 +705,38 @@ __global__ void __launch_bounds__(kThreads, 4) k_rms(Dev D, const Item* items, K
     for (int j = 0; j < 8; ++j) ccv[j] = j < ncols ? D.cc[t.cc_off + b * t.C + col0 + j] : 0.f;
     float acc = 0.f;
     if (vec) {
+        // row factor rsqrt(R_i / mean R) of the warp's 16 rows: lane l (and l + 16) computes row
+        // row0 + 8 l, each row's value is then broadcast by one shuffle
+        const int64_t my_row = row0 + 8 * (lane & 15);
+        const float rr_mine = my_row < t.R ? rsqrt_rn(__fdiv_rn(t.row[b * t.R + my_row], rbar)) : 0.f;
+        const float2 cc2[4] = {make_float2(ccv[0], ccv[1]), make_float2(ccv[2], ccv[3]), make_float2(ccv[4], ccv[5]),
+                               make_float2(ccv[6], ccv[7])};
+        float2 acc2 = f2(0.f);
 #pragma unroll 1
         for (int kb = 0; kb < kTR / 64; ++kb) {
-            float rv[8];
+            if (kb > 0) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const int64_t row = row0 + 64 * kb + 8 * kk;
-                const bool ok = row < t.R && lane_ok;
-                if (kb > 0)
-                    x[kk] = ok ? __ldcg(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0)) : make_uint4(0, 0, 0, 0);
-                rv[kk] = ok ? t.row[b * t.R + row] : 0.f;
+                for (int kk = 0; kk < 8; ++kk) {
+                    const int64_t row = row0 + 64 * kb + 8 * kk;
+                    x[kk] = (row < t.R && lane_ok)
+                                ? __ldcg(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0)) : make_uint4(0, 0, 0, 0);
+                }
             }
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const int64_t row = row0 + 64 * kb + 8 * kk;
-                if (row >= t.R || !lane_ok) break;
-                const float rr = rsqrt_rn(__fdiv_rn(rv[kk], rbar));
+                const float rr = __shfl_sync(0xFFFFFFFFu, rr_mine, 8 * kb + kk);   // every lane
+                if (lane_ok && row < t.R) {
+                    const uint32_t wd[4] = {x[kk].x, x[kk].y, x[kk].z, x[kk].w};
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float u = __fmul_rn(__fmul_rn(rr, ccv[j]), g_at(x[kk], j));
-                    acc = __fadd_rn(acc, __fmul_rn(u, u));
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 u = __fmul2_rn(__fmul2_rn(f2(rr), cc2[q]), bf16x2_to_f2(wd[q]));
+                        acc2 = __ffma2_rn(u, u, acc2);
+                    }
                 }
             }
         }
+        acc = __fadd_rn(acc2.x, acc2.y);
     } else {
         for (int kk = 0; kk < kTR / 8; ++kk) {
             const int64_t row = row0 + 8 * kk;
@@ -697,25 +758,28 @@ __global__ void __launch_bounds__(kThreads, 4) k_rms(Dev D, const Item* items, K
 }
 
 // ------------------------------------------------------------------------------------ apply
-// Applies the update to the eight elements of one row held in (W, Rv) with gradients G.
-__device__ __forceinline__ void apply8(const uint4& G, uint4& Wv, uint4& Rv, float rr, const float (&ccv)[8],
-                                       bool has_res, float den, const K& k) {
+// Applies the update to the eight elements of one row held in (Wv, Rv) with gradients G, in
+// packed pairs: u = (rr * cc_j) * g_j;  w = w + w*nwdlr (when decaying);  w = w + u*(-s);  split.
+__device__ __forceinline__ void apply8x2(const uint4& G, uint4& Wv, uint4& Rv, float rr, const float2 (&cc2)[4],
+                                         bool has_res, bool decay, float2 nwd2, float2 ns2) {
+    const uint32_t g32[4] = {G.x, G.y, G.z, G.w};
     uint32_t* w32 = reinterpret_cast<uint32_t*>(&Wv);
     uint32_t* r32 = reinterpret_cast<uint32_t*>(&Rv);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        uint32_t ow = 0, orr = 0;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int sh = 16 * h;
-            uint32_t hi = (w32[q] >> sh) & 0xFFFFu, lo = (r32[q] >> sh) & 0xFFFFu;
-            const float u = __fmul_rn(__fmul_rn(rr, ccv[2 * q + h]), g_at(G, 2 * q + h));
-            apply_elem(hi, lo, has_res, u, den, k);
-            ow |= hi << sh;
-            orr |= lo << sh;
+        float2 w2 = has_res ? make_float2(__uint_as_float(__byte_perm(r32[q], w32[q], 0x5410)),
+                                          __uint_as_float(__byte_perm(r32[q], w32[q], 0x7632)))
+                            : bf16x2_to_f2(w32[q]);
+        const float2 u2 = __fmul2_rn(__fmul2_rn(f2(rr), cc2[q]), bf16x2_to_f2(g32[q]));
+        if (decay) w2 = __fadd2_rn(w2, __fmul2_rn(w2, nwd2));
+        w2 = __fadd2_rn(w2, __fmul2_rn(u2, ns2));
+        const uint32_t b0 = __float_as_uint(w2.x), b1 = __float_as_uint(w2.y);
+        if (has_res) {
+            w32[q] = pack_hi16(b0, b1);
+            r32[q] = pack_lo16(b0, b1);
+        } else {
+            w32[q] = pack_lo16(rne_bf16(w2.x), rne_bf16(w2.y));
         }
-        w32[q] = ow;
-        r32[q] = orr;
     }
 }
 
@@ -734,14 +798,14 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
         const bool vec = aligned16(g) && aligned16(t.w) && (!has_res || aligned16(t.res)) && (t.C % 8 == 0);
         const int64_t row0 = (int64_t)it.band * kTR + warp;
         if (vec) {
-            if (ncols != 8) return;   // no shuffles below: lanes may leave independently
+            const bool lane_ok = ncols == 8;   // C % 8 == 0: a lane's group is whole or empty
             // two rows per iteration, all six 128-bit loads issued before the arithmetic; the
             // first pair is loaded before waiting for the RMS kernel (gradients and weights are
             // written by no earlier kernel of the step)
             uint4 GA = make_uint4(0, 0, 0, 0), WA = GA, RA = GA, GB = GA, WB = GA, RB = GA;
             auto load_pair = [&](int kk) {
                 const int64_t rowA = row0 + 8 * kk;
-                if (rowA >= t.R) return;
+                if (rowA >= t.R || !lane_ok) return;
                 const int64_t offA = (b * t.R + rowA) * t.C + col0, offB = offA + 8 * t.C;
                 GA = __ldcg(reinterpret_cast<const uint4*>(g + offA));
                 WA = ld_stream(reinterpret_cast<const uint4*>(t.w + offA));
@@ -754,31 +818,40 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
             };
             load_pair(0);
             pdl_sync();
-            const float den = D.den[it.tensor];
-            float ccv[8];
+            const float us = update_scale(D.den[it.tensor], k);
+            const float2 ns2 = f2(-us), nwd2 = f2(k.nwdlr);
+            const bool decay = k.nwdlr != 0.0f;
+            float2 cc2[4];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) ccv[j] = D.cc[t.cc_off + b * t.C + col0 + j];
+            for (int q = 0; q < 4; ++q)
+                cc2[q] = lane_ok ? make_float2(D.cc[t.cc_off + b * t.C + col0 + 2 * q], D.cc[t.cc_off + b * t.C + col0 + 2 * q + 1])
+                                 : f2(0.f);
             const float rbar = D.rbar[t.mat_off + b];
+            // row factors of the warp's 16 rows, one per lane (l and l + 16), broadcast per row
+            const int64_t my_row = row0 + 8 * (lane & 15);
+            const float rr_mine = my_row < t.R ? rsqrt_rn(__fdiv_rn(t.row[b * t.R + my_row], rbar)) : 0.f;
 #pragma unroll 1
             for (int kk = 0; kk < kTR / 8; kk += 2) {
                 const int64_t rowA = row0 + 8 * kk, rowB = rowA + 8;
-                if (rowA >= t.R) break;
+                if (rowA >= t.R) break;   // the same for every lane of the warp
+                const float rrA = __shfl_sync(0xFFFFFFFFu, rr_mine, kk);
+                const float rrB = __shfl_sync(0xFFFFFFFFu, rr_mine, kk + 1);
+                if (!lane_ok) continue;
                 const bool hasB = rowB < t.R;
                 const int64_t offA = (b * t.R + rowA) * t.C + col0, offB = offA + 8 * t.C;
                 if (kk > 0) load_pair(kk);
-                const float rvA = t.row[b * t.R + rowA], rvB = hasB ? t.row[b * t.R + rowB] : 1.0f;
-                apply8(GA, WA, RA, rsqrt_rn(__fdiv_rn(rvA, rbar)), ccv, has_res, den, k);
+                apply8x2(GA, WA, RA, rrA, cc2, has_res, decay, nwd2, ns2);
                 st_stream(reinterpret_cast<uint4*>(t.w + offA), WA);
                 if (has_res) st_stream(reinterpret_cast<uint4*>(t.res + offA), RA);
                 if (hasB) {
-                    apply8(GB, WB, RB, rsqrt_rn(__fdiv_rn(rvB, rbar)), ccv, has_res, den, k);
+                    apply8x2(GB, WB, RB, rrB, cc2, has_res, decay, nwd2, ns2);
                     st_stream(reinterpret_cast<uint4*>(t.w + offB), WB);
                     if (has_res) st_stream(reinterpret_cast<uint4*>(t.res + offB), RB);
                 }
             }
         } else {
             pdl_sync();
-            const float den = D.den[it.tensor];
+            const float us = update_scale(D.den[it.tensor], k);
             float ccv[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) ccv[j] = j < ncols ? D.cc[t.cc_off + b * t.C + col0 + j] : 0.f;
@@ -791,7 +864,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
                 for (int j = 0; j < ncols; ++j) {
                     uint32_t hi = t.w[off + j], lo = has_res ? t.res[off + j] : 0u;
                     const float u = __fmul_rn(__fmul_rn(rr, ccv[j]), bf16_to_f32(g[off + j]));
-                    apply_elem(hi, lo, has_res, u, den, k);
+                    apply_elem(hi, lo, has_res, u, us, k);
                     t.w[off + j] = (uint16_t)hi;
                     if (has_res) t.res[off + j] = (uint16_t)lo;
                 }
@@ -800,7 +873,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
         return;
     }
     pdl_sync();
-    const float den = D.den[it.tensor];
+    const float us = update_scale(D.den[it.tensor], k);
     if (it.cls == kTiny) {
         // as in k_stats: sub-batches staged through shared memory, double-buffered when whole
         // and aligned; w and res are updated in shared memory and streamed back
@@ -827,7 +900,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
             if (i >= nm) return;
             const float* sR = sf[b];
             const float* sC = sf[b] + nm * r;
-            tiny_apply_one(sw[b] + i * rc, sr[b] + i * rc, sg[b] + i * rc, sR + i * r, sC + i * c, r, c, has_res, den, k);
+            tiny_apply_one(sw[b] + i * rc, sr[b] + i * rc, sg[b] + i * rc, sR + i * r, sC + i * c, r, c, has_res, us, k);
         };
         if (pipe) {
             auto issue = [&](int kk) {
@@ -881,7 +954,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
     for (int64_t e = e0 + threadIdx.x; e < e1; e += kThreads) {
         uint32_t hi = t.w[e], lo = has_res ? t.res[e] : 0u;
         const float u = __fmul_rn(rsqrt_rn(t.col[e]), bf16_to_f32(g[e]));
-        apply_elem(hi, lo, has_res, u, den, k);
+        apply_elem(hi, lo, has_res, u, us, k);
         t.w[e] = (uint16_t)hi;
         if (has_res) t.res[e] = (uint16_t)lo;
     }
