@@ -152,6 +152,10 @@ __device__ __forceinline__ float elem(const Prm& k, float w, float g, float& m, 
     return __fmaf_rn(-k.lr, __fdiv_rn(num, den), w);
 }
 
+// Packed fp32 pairs: __fmul2_rn / __fadd2_rn round each component exactly as the scalar _rn
+// operation, so the paired decode and encode below give the same bits as the scalar helpers.
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+
 // Weight words in/out for two elements packed in 32-bit words W (bf16 weights) and R (residuals).
 __device__ __forceinline__ void unpack_w(uint32_t W, uint32_t R, bool has_res, float& w0, float& w1) {
     w0 = __uint_as_float(has_res ? __byte_perm(R, W, 0x5410) : (W << 16));
@@ -180,18 +184,34 @@ struct Codec {
 __device__ __forceinline__ void step2_u16(const Prm& k, const Codec& cd, bool has_res, bool sr, uint32_t rnd,
                                           uint32_t& W, uint32_t& R, uint32_t G, uint32_t& M, uint32_t& V,
                                           float& am, float& av, uint32_t& nf) {
-    float w0, w1;
-    unpack_w(W, R, has_res, w0, w1);
-    float m0 = dec_m_field<0x7610>(M, cd.dec.qm), m1 = dec_m_field<0x7632>(M, cd.dec.qm);
-    float v0 = dec_v_field<0x7610>(V, cd.dec.qv), v1 = dec_v_field<0x7632>(V, cd.dec.qv);
-    float s0, s1;
-    w0 = elem(k, w0, __uint_as_float(G << 16), m0, v0, s0);
-    w1 = elem(k, w1, __uint_as_float(G & 0xFFFF0000u), m1, v1, s1);
-    pack_w(w0, w1, has_res, sr, rnd, W, R);
-    M = pack_lo16(enc_m_bits(m0, cd.enc.rm), enc_m_bits(m1, cd.enc.rm));
-    V = pack_lo16(enc_v_bits(s0, cd.enc.rv), enc_v_bits(s1, cd.enc.rv));
-    am = fmaxf(am, fmaxf(fabsf(m0), fabsf(m1)));
-    av = fmaxf(av, fmaxf(v0, v1));
+    float2 w;
+    unpack_w(W, R, has_res, w.x, w.y);
+    // decode, as dec_m_field / dec_v_field, in pairs: t = (c - 32768) qm, m = t|t|;
+    // z = c qv, v = (z z)(z z)  (codes to fp32 by the 2^23 mantissa trick)
+    const float2 cm = make_float2(__uint_as_float(__byte_perm(M, 0x4B000000u, 0x7610)),
+                                  __uint_as_float(__byte_perm(M, 0x4B000000u, 0x7632)));
+    const float2 cv = make_float2(__uint_as_float(__byte_perm(V, 0x4B000000u, 0x7610)),
+                                  __uint_as_float(__byte_perm(V, 0x4B000000u, 0x7632)));
+    const float2 t = __fmul2_rn(__fadd2_rn(cm, f2(-8421376.0f)), f2(cd.dec.qm));
+    float2 m = make_float2(__fmul_rn(t.x, fabsf(t.x)), __fmul_rn(t.y, fabsf(t.y)));
+    const float2 z = __fmul2_rn(__fadd2_rn(cv, f2(-8388608.0f)), f2(cd.dec.qv));
+    const float2 z2 = __fmul2_rn(z, z);
+    float2 v = __fmul2_rn(z2, z2);
+    float2 sv;
+    w.x = elem(k, w.x, __uint_as_float(G << 16), m.x, v.x, sv.x);
+    w.y = elem(k, w.y, __uint_as_float(G & 0xFFFF0000u), m.y, v.y, sv.y);
+    pack_w(w.x, w.y, has_res, sr, rnd, W, R);
+    // encode, as enc_m_bits / enc_v_bits, with the scaling multiply and the rounding add paired
+    const float2 ym = make_float2(copysignf(fminf(__fsqrt_rn(__fmul_rn(fabsf(m.x), cd.enc.rm)), 32767.0f), m.x),
+                                  copysignf(fminf(__fsqrt_rn(__fmul_rn(fabsf(m.y), cd.enc.rm)), 32767.0f), m.y));
+    const float2 em = __fadd2_rn(f2(12615680.0f), ym);
+    const float2 xv = __fmul2_rn(sv, f2(cd.enc.rv));
+    const float2 yv = make_float2(fminf(__fsqrt_rn(xv.x), 65535.0f), fminf(__fsqrt_rn(xv.y), 65535.0f));
+    const float2 ev = __fadd2_rn(f2(12582912.0f), yv);
+    M = pack_lo16(__float_as_uint(em.x), __float_as_uint(em.y));
+    V = pack_lo16(__float_as_uint(ev.x), __float_as_uint(ev.y));
+    am = fmaxf(am, fmaxf(fabsf(m.x), fabsf(m.y)));
+    av = fmaxf(av, fmaxf(v.x, v.y));
     nf = __vmaxu2(nf, W & 0x7FFF7FFFu);
 }
 

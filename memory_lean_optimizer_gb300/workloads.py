@@ -133,6 +133,10 @@ def config(name: str):
         c = config("sdxl_like")
         c["groups"] = c["groups"][:1]
         return c
+    if name == "sdxl_like_conv":   # the 3x3 convolutions of sdxl_like, one group: small-matrix profiling
+        c = config("sdxl_like")
+        c["groups"] = [[s for s in sdxl_like_shapes() if len(s) == 4]]
+        return c
     if name == "flux35":
         return dict(kind="nadam", groups=flux_shapes(35), hp=dict(NADAM_HP), steps=3, g_std=1e-4,
                     zero_frac=0.0, seed=0)
