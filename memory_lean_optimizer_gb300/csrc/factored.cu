@@ -111,7 +111,8 @@ __device__ __forceinline__ float ema(float s, float x, const K& k) {
     float r = __fadd_rn(__fmul_rn(k.b2t, s), __fmul_rn(k.alpha, x));
     return k.mode == 1 ? __fadd_rn(r, k.eps2) : r;
 }
-__device__ __forceinline__ float rsqrt_rn(float x) { return __fdiv_rn(1.0f, __fsqrt_rn(x)); }
+// 1/sqrt(x) rounded once (correctly rounded reciprocal square root).
+__device__ __forceinline__ float rsqrt_rn(float x) { return __frsqrt_rn(x); }
 // Columns of a lane's 8-column group that lie inside the matrix (0..8).
 __device__ __forceinline__ int cols_in(int64_t remaining) {
     return remaining <= 0 ? 0 : (remaining >= 8 ? 8 : (int)remaining);
@@ -267,47 +268,9 @@ __device__ __forceinline__ void stage_async(void* dst, const void* src, int byte
         cp_async16(static_cast<char*>(dst) + 16 * i, static_cast<const char*>(src) + 16 * i);
 }
 
-// One small matrix (rows*cols <= 16) of a tiny-class tensor: R, C EMAs (written back), mean(R),
-// and the matrix's sum of squared updates.  The fixed-size form keeps everything in registers.
-template <int RR, int CC>
-__device__ __forceinline__ float tiny_stats(const uint16_t* gm, float* Rs, float* Cs, const K& k) {
-    float q[RR * CC], rsum[RR], cfac[CC];
-#pragma unroll
-    for (int e = 0; e < RR * CC; ++e) q[e] = qval(bf16_to_f32(gm[e]), k);
-    float rtot = 0.f;
-#pragma unroll
-    for (int i = 0; i < RR; ++i) {
-        float s = 0.f;
-#pragma unroll
-        for (int j = 0; j < CC; ++j) s = __fadd_rn(s, q[i * CC + j]);
-        const float nr = ema(Rs[i], __fdiv_rn(s, (float)CC), k);
-        Rs[i] = nr;
-        rsum[i] = nr;
-        rtot = __fadd_rn(rtot, nr);
-    }
-#pragma unroll
-    for (int j = 0; j < CC; ++j) {
-        float s = 0.f;
-#pragma unroll
-        for (int i = 0; i < RR; ++i) s = __fadd_rn(s, q[i * CC + j]);
-        const float nc = ema(Cs[j], __fdiv_rn(s, (float)RR), k);
-        Cs[j] = nc;
-        cfac[j] = rsqrt_rn(nc);
-    }
-    const float rbar = __fdiv_rn(rtot, (float)RR);
-    float acc = 0.f;
-#pragma unroll
-    for (int i = 0; i < RR; ++i) {
-        const float rr = rsqrt_rn(__fdiv_rn(rsum[i], rbar));
-#pragma unroll
-        for (int j = 0; j < CC; ++j) {
-            const float u = __fmul_rn(__fmul_rn(rr, cfac[j]), bf16_to_f32(gm[i * CC + j]));
-            acc = __fadd_rn(acc, __fmul_rn(u, u));
-        }
-    }
-    return acc;
-}
-__device__ __forceinline__ float tiny_stats_any(const uint16_t* gm, float* Rs, float* Cs, int r, int c, const K& k) {
+// Any small matrix (rows*cols <= 16): R, C EMAs (written back), mean(R), and the matrix's sum of
+// squared updates.
+__device__ __noinline__ float tiny_stats_any(const uint16_t* gm, float* Rs, float* Cs, int r, int c, const K& k) {
     float q[16], rsum[16], csum[16];
     for (int e = 0; e < r * c; ++e) q[e] = qval(bf16_to_f32(gm[e]), k);
     float rtot = 0.f;
@@ -338,38 +301,86 @@ __device__ __forceinline__ float tiny_stats_any(const uint16_t* gm, float* Rs, f
     return acc;
 }
 
-// Statistics of one staged small matrix (the 3x3 form fully in registers).
-__device__ __noinline__ float tiny_stats_one(const uint16_t* gm, float* Rs, float* Cs, int r, int c, const K& k) {
-    return (r == 3 && c == 3) ? tiny_stats<3, 3>(gm, Rs, Cs, k) : tiny_stats_any(gm, Rs, Cs, r, c, k);
+// 3x3 matrices (the convolution kernels) with the per-tensor switches as template parameters:
+// Prodigy mode (eps2 after the EMA), a residual, decoupled decay.  The factors use the hardware
+// reciprocal square root rsqrtf (at most 2 ulp from 1/sqrt, CUDA's documented bound), the means
+// products with fl(1/3), so the per-matrix work is a few dozen instructions; both kernels compute
+// the factors the same way.
+struct Fac3 {
+    float rr[3], cc[3];
+};
+__device__ __forceinline__ Fac3 factors3(float r0, float r1, float r2, const float* Cs) {
+    Fac3 f;
+    const float inv_rbar = __frcp_rn(__fmul_rn(__fadd_rn(__fadd_rn(r0, r1), r2), 1.0f / 3.0f));
+    f.rr[0] = rsqrtf(__fmul_rn(r0, inv_rbar));
+    f.rr[1] = rsqrtf(__fmul_rn(r1, inv_rbar));
+    f.rr[2] = rsqrtf(__fmul_rn(r2, inv_rbar));
+    f.cc[0] = rsqrtf(Cs[0]);
+    f.cc[1] = rsqrtf(Cs[1]);
+    f.cc[2] = rsqrtf(Cs[2]);
+    return f;
 }
-
-// Apply step of one small matrix on staged words (w, res, g and R, C in shared memory).
-template <int RR, int CC>
-__device__ __forceinline__ void tiny_apply(uint16_t* wm, uint16_t* rm, const uint16_t* gm, const float* Rs,
-                                           const float* Cs, bool has_res, float us, const K& k) {
-    float rtot = 0.f, rv[RR], cfac[CC];
+template <bool kProdigy>
+__device__ __forceinline__ float stats3(const uint16_t* gm, float* Rs, float* Cs, const K& k) {
+    float q[9];
 #pragma unroll
-    for (int i = 0; i < RR; ++i) {
-        rv[i] = Rs[i];
-        rtot = __fadd_rn(rtot, rv[i]);
+    for (int e = 0; e < 9; ++e) {
+        const float g = bf16_to_f32(gm[e]);
+        q[e] = kProdigy ? __fmul_rn(g, g) : __fadd_rn(__fmul_rn(g, g), k.eps1);
     }
-    const float rbar = __fdiv_rn(rtot, (float)RR);
+    float nr[3];
 #pragma unroll
-    for (int j = 0; j < CC; ++j) cfac[j] = rsqrt_rn(Cs[j]);
+    for (int i = 0; i < 3; ++i) {
+        const float s = __fadd_rn(__fadd_rn(q[3 * i], q[3 * i + 1]), q[3 * i + 2]);
+        float v = __fadd_rn(__fmul_rn(k.b2t, Rs[i]), __fmul_rn(k.alpha, __fmul_rn(s, 1.0f / 3.0f)));
+        if (kProdigy) v = __fadd_rn(v, k.eps2);
+        Rs[i] = v;
+        nr[i] = v;
+    }
 #pragma unroll
-    for (int i = 0; i < RR; ++i) {
-        const float rr = rsqrt_rn(__fdiv_rn(rv[i], rbar));
+    for (int j = 0; j < 3; ++j) {
+        const float s = __fadd_rn(__fadd_rn(q[j], q[3 + j]), q[6 + j]);
+        float v = __fadd_rn(__fmul_rn(k.b2t, Cs[j]), __fmul_rn(k.alpha, __fmul_rn(s, 1.0f / 3.0f)));
+        if (kProdigy) v = __fadd_rn(v, k.eps2);
+        Cs[j] = v;
+    }
+    const Fac3 f = factors3(nr[0], nr[1], nr[2], Cs);
+    float acc = 0.f;
 #pragma unroll
-        for (int j = 0; j < CC; ++j) {
-            const int e = i * CC + j;
-            uint32_t hi = wm[e], lo = has_res ? rm[e] : 0u;
-            apply_elem(hi, lo, has_res, __fmul_rn(__fmul_rn(rr, cfac[j]), bf16_to_f32(gm[e])), us, k);
-            wm[e] = (uint16_t)hi;
-            if (has_res) rm[e] = (uint16_t)lo;
+    for (int e = 0; e < 9; ++e) {
+        const float u = __fmul_rn(__fmul_rn(f.rr[e / 3], f.cc[e % 3]), bf16_to_f32(gm[e]));
+        acc = __fmaf_rn(u, u, acc);
+    }
+    return acc;
+}
+template <bool kRes, bool kDecay>
+__device__ __forceinline__ void apply3(uint16_t* wm, uint16_t* rm, const uint16_t* gm, const float* Rs,
+                                       const float* Cs, float us, float nwdlr) {
+    const Fac3 f = factors3(Rs[0], Rs[1], Rs[2], Cs);
+#pragma unroll
+    for (int e = 0; e < 9; ++e) {
+        float w = kRes ? __uint_as_float(((uint32_t)wm[e] << 16) | rm[e]) : bf16_to_f32(wm[e]);
+        const float u = __fmul_rn(__fmul_rn(f.rr[e / 3], f.cc[e % 3]), bf16_to_f32(gm[e]));
+        if (kDecay) w = __fadd_rn(w, __fmul_rn(w, nwdlr));
+        w = __fsub_rn(w, __fmul_rn(u, us));
+        const uint32_t b = __float_as_uint(w);
+        if (kRes) {
+            wm[e] = (uint16_t)(b >> 16);
+            rm[e] = (uint16_t)(b & 0xFFFFu);
+        } else {
+            wm[e] = (uint16_t)rne_bf16(w);
         }
     }
 }
-__device__ __forceinline__ void tiny_apply_any(uint16_t* wm, uint16_t* rm, const uint16_t* gm, const float* Rs, const float* Cs,
+
+// Statistics of one staged small matrix, out of line (the ragged / unaligned staging path).
+__device__ __noinline__ float tiny_stats_call(const uint16_t* gm, float* Rs, float* Cs, int r, int c, const K& k) {
+    if (r == 3 && c == 3) return k.mode == 1 ? stats3<true>(gm, Rs, Cs, k) : stats3<false>(gm, Rs, Cs, k);
+    return tiny_stats_any(gm, Rs, Cs, r, c, k);
+}
+
+// Apply step of any small matrix on staged words (w, res, g and R, C in shared memory).
+__device__ __noinline__ void tiny_apply_any(uint16_t* wm, uint16_t* rm, const uint16_t* gm, const float* Rs, const float* Cs,
                                int r, int c, bool has_res, float us, const K& k) {
     float rtot = 0.f, cfac[16];
     for (int i = 0; i < r; ++i) rtot = __fadd_rn(rtot, Rs[i]);
@@ -385,13 +396,6 @@ __device__ __forceinline__ void tiny_apply_any(uint16_t* wm, uint16_t* rm, const
             if (has_res) rm[e] = (uint16_t)lo;
         }
     }
-}
-
-// Apply step of one staged small matrix (the 3x3 form fully in registers).
-__device__ __noinline__ void tiny_apply_one(uint16_t* wm, uint16_t* rm, const uint16_t* gm, const float* Rs,
-                                            const float* Cs, int r, int c, bool has_res, float us, const K& k) {
-    if (r == 3 && c == 3) tiny_apply<3, 3>(wm, rm, gm, Rs, Cs, has_res, us, k);
-    else tiny_apply_any(wm, rm, gm, Rs, Cs, r, c, has_res, us, k);
 }
 
 // Packed fp32 pairs: __fmul2_rn / __fadd2_rn / __ffma2_rn round each component exactly as the
@@ -425,11 +429,6 @@ __device__ __forceinline__ float warp_sum8(const float (&v)[8], int lane) {
     return __fadd_rn(c, __shfl_xor_sync(full, c, 1));
 }
 
-// Eight gradient words of one 128-bit load, as fp32 (bf16 -> fp32 is exact).
-__device__ __forceinline__ float g_at(const uint4& x, int j) {
-    const uint32_t w = j < 2 ? x.x : (j < 4 ? x.y : (j < 6 ? x.z : x.w));
-    return __uint_as_float((j & 1) ? (w & 0xFFFF0000u) : (w << 16));
-}
 
 // ------------------------------------------------------------------------------------ stats
 __global__ void __launch_bounds__(kThreads, 4) k_stats(Dev D, const Item* items, K k) {
@@ -557,7 +556,12 @@ __global__ void __launch_bounds__(kThreads, 4) k_stats(Dev D, const Item* items,
                 float* sC = sR + sub * r;
                 if (i < sub) {
                     const uint16_t* gm = words(b) + i * rc;
-                    acc = __fadd_rn(acc, tiny_stats_one(gm, sR + i * r, sC + i * c, r, c, k));
+                    float a;
+                    if (r == 3 && c == 3)
+                        a = k.mode == 1 ? stats3<true>(gm, sR + i * r, sC + i * c, k) : stats3<false>(gm, sR + i * r, sC + i * c, k);
+                    else
+                        a = tiny_stats_any(gm, sR + i * r, sC + i * c, r, c, k);
+                    acc = __fadd_rn(acc, a);
                 }
                 __syncthreads();
                 const int64_t m0 = it.x + (int64_t)kk * sub;
@@ -578,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_stats(Dev D, const Item* items,
                 const int i = threadIdx.x;
                 if (i < nm) {
                     const uint16_t* gm = words(0) + i * rc;
-                    acc = __fadd_rn(acc, tiny_stats_one(gm, sR + i * r, sC + i * c, r, c, k));
+                    acc = __fadd_rn(acc, tiny_stats_call(gm, sR + i * r, sC + i * c, r, c, k));
                 }
                 __syncthreads();
                 unstage(t.row + m0 * r, sR, nm * r, false);
@@ -900,7 +904,21 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
             if (i >= nm) return;
             const float* sR = sf[b];
             const float* sC = sf[b] + nm * r;
-            tiny_apply_one(sw[b] + i * rc, sr[b] + i * rc, sg[b] + i * rc, sR + i * r, sC + i * c, r, c, has_res, us, k);
+            if (r == 3 && c == 3) {
+                uint16_t* wm = sw[b] + i * rc;
+                uint16_t* rm = sr[b] + i * rc;
+                const uint16_t* gm = sg[b] + i * rc;
+                const float* Rs = sR + i * r;
+                const float* Cs = sC + i * c;
+                if (has_res) {
+                    if (k.nwdlr != 0.0f) apply3<true, true>(wm, rm, gm, Rs, Cs, us, k.nwdlr);
+                    else apply3<true, false>(wm, rm, gm, Rs, Cs, us, k.nwdlr);
+                } else {
+                    if (k.nwdlr != 0.0f) apply3<false, true>(wm, rm, gm, Rs, Cs, us, k.nwdlr);
+                    else apply3<false, false>(wm, rm, gm, Rs, Cs, us, k.nwdlr);
+                }
+            } else
+                tiny_apply_any(sw[b] + i * rc, sr[b] + i * rc, sg[b] + i * rc, sR + i * r, sC + i * c, r, c, has_res, us, k);
         };
         if (pipe) {
             auto issue = [&](int kk) {

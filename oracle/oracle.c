@@ -625,6 +625,9 @@ float orc_factored_step_tensor(uint16_t* hi, uint16_t* lo, const uint16_t* g, in
                                const orc_factored_scalars_t* k)
 {
     int64_t n = B * R * C;
+    /* A tensor without elements has no gradient: nothing is updated, its state included (a mean
+     * over zero rows or columns has no value). */
+    if (n == 0) return 1.0f;
     /* 1. EMA of row and column means of q */
     for (int64_t b = 0; b < B; ++b) {
         const uint16_t* gb = g + b * R * C;

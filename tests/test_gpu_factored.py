@@ -153,3 +153,78 @@ def test_factored_validation(eng):
         lmopt.optim_step_factored(grp.handle, [g.data_ptr()], 1, bad, 0)
     with pytest.raises(lmopt.LmoptError):
         lmopt.optim_step_nadam_kahan(grp.handle, [g.data_ptr()], 1, lmopt.NadamHparams(lr=1e-3, beta1=0.9, beta2=0.99), 0)
+
+
+def test_two_waves_on_two_streams(orc, eng):
+    """A group larger than one wave (two 4096x6144 linears, 100 MB of gradients, and a 3x3 conv):
+    its waves run on the caller's stream and the group's second stream."""
+    shapes = [(4096, 6144), (4096, 6144), (640, 640, 3, 3), (1280,)]
+    run_parity(orc, eng, shapes, 2, dict(HP, lr=2e-6), seed=7, g_std=1e-4)
+
+
+def test_misaligned_buffers_and_empty_tensors(orc, eng):
+    """Weights, residuals, gradients and states 2 or 4 bytes (not 16) aligned take the
+    element-by-element paths; empty tensors (no rows, no columns, no elements) are left alone."""
+    from helpers import alloc_offset, cuda_bits
+    from memory_lean_optimizer_gb300 import lmopt
+    shapes = [(96, 64), (40, 50, 3, 3), (700,), (0, 64), (5, 0), (0,), (33, 40)]
+    seed, steps, hp = 8, 3, dict(HP)
+    masters = [W.master_weights(s, seed, i) for i, s in enumerate(shapes)]
+    ora = OracleFactored(orc, [m.numpy() for m in masters], shapes)
+    keep, descs, ws, rs, rows, cols = [], [], [], [], [], []
+    for i, s in enumerate(shapes):
+        n = W.numel(s)
+        ot = ora.t[i]
+        b1, w = alloc_offset(n, torch.int16, 1)
+        b2, r = alloc_offset(n, torch.int16, 3)
+        if n:
+            w.copy_(torch.from_numpy(ot["hi"].view(np.int16)))
+            r.copy_(torch.from_numpy(ot["lo"].view(np.int16)))
+        if "row" in ot:
+            b3, rw = alloc_offset(ot["row"].size, torch.float32, 1)
+            b4, cl = alloc_offset(ot["col"].size, torch.float32, 1)
+            rw.zero_(), cl.zero_()
+        else:
+            b3, rw = None, None
+            b4, cl = alloc_offset(n, torch.float32, 1)
+            cl.zero_()
+        keep += [b1, b2, b3, b4]
+        d = lmopt.TensorDesc(w_bf16=w.data_ptr() if n else None, res_u16=r.data_ptr() if n else None,
+                             m=rw.data_ptr() if (rw is not None and rw.numel()) else None,
+                             v=cl.data_ptr() if cl.numel() else None, numel=n, ndim=len(s))
+        for k, dim in enumerate(s):
+            d.shape[k] = dim
+        descs.append(d)
+        ws.append(w), rs.append(r), rows.append(rw), cols.append(cl)
+    h = lmopt.optim_group_create(descs, lmopt.OPTIM_KIND_FACTORED)
+    H = lmopt.FactoredHparams(lr=hp["lr"], beta2=hp["beta2"], decay_rate=hp["decay_rate"], eps1=hp["eps1"],
+                              eps2=hp["eps2"], d=hp["d"], clip_threshold=hp["clip_threshold"],
+                              weight_decay=hp["weight_decay"], mode=hp["mode"])
+    try:
+        for t in range(1, steps + 1):
+            grads = [W.grad_bf16(s, seed, i, t, 1e-3) for i, s in enumerate(shapes)]
+            ora.step([W.bits16(g).reshape(-1) for g in grads], hp)
+            gbufs, ptrs = [], []
+            for g in grads:
+                b, gg = alloc_offset(g.numel(), torch.int16, 1)
+                if g.numel():
+                    gg.copy_(g.reshape(-1).view(torch.int16))
+                gbufs.append(b)
+                ptrs.append(gg.data_ptr() if g.numel() else None)
+            lmopt.optim_step_factored(h, ptrs, t, H, 0)
+            torch.cuda.synchronize()
+        for i, ot in enumerate(ora.t):
+            if ot["hi"].size:
+                ref = orc.kahan_merge(ot["hi"], ot["lo"]).astype(np.float64)
+                got = orc.kahan_merge(cuda_bits(ws[i]), cuda_bits(rs[i])).astype(np.float64)
+                tol = 1e-6 * np.abs(ref) + 1e-6 * hp["lr"] * steps
+                assert np.all(np.abs(got - ref) <= tol), f"tensor {i} {shapes[i]}: masters differ"
+            if "row" in ot:
+                for st, r in ((rows[i], ot["row"]), (cols[i], ot["col"])):
+                    gv = st.cpu().numpy().astype(np.float64)
+                    assert np.all(np.abs(gv - r) <= 2e-6 * np.abs(r) + 1e-37), f"tensor {i}: state differs"
+            else:
+                gv = cols[i].cpu().numpy().astype(np.float64)
+                assert np.all(np.abs(gv - ot["V"]) <= 2e-6 * np.abs(ot["V"]) + 1e-37), f"tensor {i}: V differs"
+    finally:
+        lmopt.optim_group_destroy(h)

@@ -145,3 +145,25 @@ def test_zero_grad_is_identity(orc, shape):
     z = np.zeros(shape, np.uint16)
     w, t, _ = run(orc, shape, w0, [z, z, z], dict(HP, eps1=1e-30))
     assert np.array_equal(w, w0)
+
+
+@pytest.mark.parametrize("shape", [(0, 64), (5, 0), (0, 3, 3, 3), (0,)])
+def test_empty_tensor_leaves_state(orc, shape):
+    """A tensor without elements has no gradient: its state stays as it was (no 0/0 mean) and the
+    other tensors of the group step as they would alone."""
+    rng = np.random.default_rng(26)
+    other = (rng.standard_normal((12, 8)) * 0.02).astype(np.float32)
+    g_other = bf16_bits(rng.standard_normal((12, 8)) * 1e-3)
+    empty = make(orc, shape, np.zeros(shape, np.float32))
+    for name in ("row", "col", "V"):
+        if name in empty:
+            empty[name][:] = 0.5
+    t_alone = make(orc, (12, 8), other)
+    t_group = make(orc, (12, 8), other)
+    orc.factored_group_step([t_alone], [g_other.reshape(-1)], 1, HP)
+    _, dens = orc.factored_group_step([empty, t_group], [np.zeros(0, np.uint16), g_other.reshape(-1)], 1, HP)
+    for name in ("row", "col", "V"):
+        if name in empty:
+            assert np.all(empty[name] == 0.5)
+    assert dens[0] == 1.0
+    assert np.array_equal(t_group["hi"], t_alone["hi"]) and np.array_equal(t_group["lo"], t_alone["lo"])
