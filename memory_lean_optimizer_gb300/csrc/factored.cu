@@ -373,6 +373,109 @@ __device__ __forceinline__ void apply3(uint16_t* wm, uint16_t* rm, const uint16_
     }
 }
 
+// 3x3 tensors whose every sub-batch is whole and whose buffers are 16-byte aligned (the
+// convolution kernels): the staging loops have compile-time trip counts.  Per sub-batch of
+// kTinySub matrices: 288 gradient (weight, residual) chunks of 16 bytes, 192 R and 192 C chunks.
+constexpr int k3Words = kTinySub * 9 * 2 / 16;   // 16-byte chunks of one word plane
+constexpr int k3Stats = kTinySub * 3 * 4 / 16;   // 16-byte chunks of R (and of C)
+static_assert(k3Words > kTinySub && k3Words <= 2 * kTinySub && k3Stats <= kTinySub, "chunk counts per thread");
+
+template <bool kProdigy>
+__device__ __forceinline__ float conv3_stats(const uint16_t* g, float* row, float* col, int64_t m_first, int nsub,
+                                             unsigned char* smem, const K& k) {
+    const int tid = threadIdx.x;
+    auto gbuf = [&](int b) { return reinterpret_cast<uint4*>(smem + b * (kTinyWords * 2)); };
+    auto sbuf = [&](int b) { return reinterpret_cast<uint4*>(smem + 2 * kTinyWords * 2 + b * (kTinyStats * 4)); };
+    auto issue = [&](int kk) {
+        const int64_t m = m_first + (int64_t)kk * kTinySub;
+        const uint4* gs = reinterpret_cast<const uint4*>(g + m * 9);
+        const uint4* rs = reinterpret_cast<const uint4*>(row + m * 3);
+        const uint4* cs = reinterpret_cast<const uint4*>(col + m * 3);
+        uint4* gd = gbuf(kk & 1);
+        uint4* sd = sbuf(kk & 1);
+        cp_async16(gd + tid, gs + tid);
+        if (tid < k3Words - kTinySub) cp_async16(gd + kTinySub + tid, gs + kTinySub + tid);
+        if (tid < k3Stats) {
+            cp_async16(sd + tid, rs + tid);
+            cp_async16(sd + k3Stats + tid, cs + tid);
+        }
+        cp_async_commit();
+    };
+    float acc = 0.f;
+    issue(0);
+    for (int kk = 0; kk < nsub; ++kk) {
+        if (kk + 1 < nsub) {
+            issue(kk + 1);   // its buffer was released by the barrier ending iteration kk-1
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        const int b = kk & 1;
+        float* R = reinterpret_cast<float*>(sbuf(b));
+        acc = __fadd_rn(acc, stats3<kProdigy>(reinterpret_cast<const uint16_t*>(gbuf(b)) + tid * 9, R + tid * 3,
+                                              R + kTinySub * 3 + tid * 3, k));
+        __syncthreads();
+        const int64_t m = m_first + (int64_t)kk * kTinySub;
+        if (tid < k3Stats) {
+            reinterpret_cast<uint4*>(row + m * 3)[tid] = sbuf(b)[tid];
+            reinterpret_cast<uint4*>(col + m * 3)[tid] = sbuf(b)[k3Stats + tid];
+        }
+        __syncthreads();
+    }
+    return acc;
+}
+
+template <bool kRes, bool kDecay>
+__device__ __forceinline__ void conv3_apply(const uint16_t* g, uint16_t* w, uint16_t* res, const float* row,
+                                            const float* col, int64_t m_first, int nsub, unsigned char* smem, float us,
+                                            float nwdlr) {
+    constexpr int kBuf = 3 * kTinyWords * 2 + kTinyStats * 4;
+    const int tid = threadIdx.x;
+    auto plane = [&](int b, int a) { return reinterpret_cast<uint4*>(smem + b * kBuf + a * (kTinyWords * 2)); };
+    auto issue = [&](int kk) {
+        const int64_t m = m_first + (int64_t)kk * kTinySub;
+        const int b = kk & 1;
+        const uint4* src[3] = {reinterpret_cast<const uint4*>(g + m * 9), reinterpret_cast<const uint4*>(w + m * 9),
+                               kRes ? reinterpret_cast<const uint4*>(res + m * 9) : nullptr};
+#pragma unroll
+        for (int a = 0; a < (kRes ? 3 : 2); ++a) {
+            cp_async16(plane(b, a) + tid, src[a] + tid);
+            if (tid < k3Words - kTinySub) cp_async16(plane(b, a) + kTinySub + tid, src[a] + kTinySub + tid);
+        }
+        if (tid < k3Stats) {
+            cp_async16(plane(b, 3) + tid, reinterpret_cast<const uint4*>(row + m * 3) + tid);
+            cp_async16(plane(b, 3) + k3Stats + tid, reinterpret_cast<const uint4*>(col + m * 3) + tid);
+        }
+        cp_async_commit();
+    };
+    issue(0);
+    for (int kk = 0; kk < nsub; ++kk) {
+        if (kk + 1 < nsub) {
+            issue(kk + 1);   // its buffer was released by the barrier ending iteration kk-1
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        const int b = kk & 1;
+        const float* R = reinterpret_cast<const float*>(plane(b, 3));
+        apply3<kRes, kDecay>(reinterpret_cast<uint16_t*>(plane(b, 1)) + tid * 9, reinterpret_cast<uint16_t*>(plane(b, 2)) + tid * 9,
+                             reinterpret_cast<const uint16_t*>(plane(b, 0)) + tid * 9, R + tid * 3, R + kTinySub * 3 + tid * 3,
+                             us, nwdlr);
+        __syncthreads();
+        const int64_t m = m_first + (int64_t)kk * kTinySub;
+#pragma unroll
+        for (int a = 1; a < (kRes ? 3 : 2); ++a) {
+            uint16_t* base = a == 1 ? w : res;   // a == 2 only with a residual
+            uint4* dst = reinterpret_cast<uint4*>(base + m * 9);
+            st_stream(dst + tid, plane(b, a)[tid]);
+            if (tid < k3Words - kTinySub) st_stream(dst + kTinySub + tid, plane(b, a)[kTinySub + tid]);
+        }
+        __syncthreads();
+    }
+}
+
 // Statistics of one staged small matrix, out of line (the ragged / unaligned staging path).
 __device__ __noinline__ float tiny_stats_call(const uint16_t* gm, float* Rs, float* Cs, int r, int c, const K& k) {
     if (r == 3 && c == 3) return k.mode == 1 ? stats3<true>(gm, Rs, Cs, k) : stats3<false>(gm, Rs, Cs, k);
@@ -536,7 +639,10 @@ __global__ void __launch_bounds__(kThreads, 4) k_stats(Dev D, const Item* items,
         const int64_t nmat = mend - it.x;
         const bool pipe = nmat % sub == 0 && aligned16(g) && aligned16(t.row) && aligned16(t.col);
         const int nsub = (int)((nmat + sub - 1) / sub);
-        if (pipe) {
+        if (pipe && r == 3 && c == 3) {
+            acc = k.mode == 1 ? conv3_stats<true>(g, t.row, t.col, it.x, nsub, smem, k)
+                              : conv3_stats<false>(g, t.row, t.col, it.x, nsub, smem, k);
+        } else if (pipe) {
             for (int kk = -1; kk < nsub; ++kk) {
                 // issue sub-batch kk+1 (its buffer was released by the barrier ending kk-1)
                 if (kk + 1 < nsub) {
@@ -899,6 +1005,16 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
         const bool pipe = nmat % sub == 0 && aligned16(g) && aligned16(t.w) && (!has_res || aligned16(t.res)) &&
                           aligned16(t.row) && aligned16(t.col);
         const int nsub = (int)((nmat + sub - 1) / sub);
+        if (pipe && r == 3 && c == 3) {
+            if (has_res) {
+                if (k.nwdlr != 0.0f) conv3_apply<true, true>(g, t.w, t.res, t.row, t.col, it.x, nsub, smem, us, k.nwdlr);
+                else conv3_apply<true, false>(g, t.w, t.res, t.row, t.col, it.x, nsub, smem, us, k.nwdlr);
+            } else {
+                if (k.nwdlr != 0.0f) conv3_apply<false, true>(g, t.w, t.res, t.row, t.col, it.x, nsub, smem, us, k.nwdlr);
+                else conv3_apply<false, false>(g, t.w, t.res, t.row, t.col, it.x, nsub, smem, us, k.nwdlr);
+            }
+            return;
+        }
         auto compute = [&](int b, int nm) {
             const int i = threadIdx.x;
             if (i >= nm) return;
