@@ -142,6 +142,29 @@ int optim_group_destroy(optim_group_t* group);
 int optim_step_nadam_kahan(optim_group_t* group, const void* const* grads_bf16, int64_t step,
                            const optim_nadam_hparams_t* hp, void* stream);
 
+/* The same step in two calls, for a tensor split into slices across ranks (each rank's group
+ * holds its slices as tensors).  The codec scale belongs to the whole tensor: it is bounded by
+ * the maxima over all slices of max|g| (this step) and of the moment maxima (previous step), so
+ * the ranks combine them between the gradient pre-pass and the update.  Splitting is otherwise
+ * exact -- the update of an element depends only on its own values and the scale -- so slices
+ * stepped this way are bit-identical to the unsplit tensor, provided every slice of a tensor of
+ * more than 4096 elements has more than 4096 elements too (a slice of 4096 or fewer keeps fp32
+ * moments, as a whole tensor of that size would).  The pages have no counterpart: their step
+ * is per parameter on one GPU; this is the data-parallel form of the same step.
+ *   begin    : validates, uploads gradient pointers, enqueues the pre-pass; if `exchange` (a device
+ *              buffer of 3 floats per tensor, 4-byte aligned, caller-owned) is not NULL, copies
+ *              into it, per tensor i, {max|g|, max|m| of the previous step, max v of the previous
+ *              step} at [3i, 3i+1, 3i+2] (non-negative values; NaN if a gradient held NaN).
+ *   (caller) : MAX all-reduce of `exchange` across the ranks holding slices of the same tensors
+ *              (the same tensor order on every rank), on `stream` or ordered after it.
+ *   end      : if `exchange` is not NULL, writes its values back, then enqueues the update.
+ * Between begin and end the group accepts no other call that changes its state (OPTIM_ESTATE);
+ * begin twice, or end without begin, is OPTIM_ESTATE.  optim_step_nadam_kahan is begin + end with
+ * no exchange.  f24 groups have no scale: their exchange values are carried but unused. */
+int optim_step_nadam_begin(optim_group_t* group, const void* const* grads_bf16, int64_t step,
+                           const optim_nadam_hparams_t* hp, void* stream, float* exchange);
+int optim_step_nadam_end(optim_group_t* group, const float* exchange, void* stream);
+
 /* One factored-second-moment step (Adafactor / Prodigy with beta1 = 0) of a FACTORED group:
  * row and column EMAs of g^2 over the last two dims, rank-1 reconstruction
  * V_ij = R_i C_j / mean(R), update u = g / sqrt(V), RMS clipping, decoupled decay, Kahan split.

@@ -245,11 +245,12 @@ int optim_group_destroy(optim_group_t* g) {
     return OPTIM_OK;
 }
 
-int optim_step_nadam_kahan(optim_group_t* g, const void* const* grads, int64_t step,
-                           const optim_nadam_hparams_t* hp, void* stream) {
+int optim_step_nadam_begin(optim_group_t* g, const void* const* grads, int64_t step,
+                           const optim_nadam_hparams_t* hp, void* stream, float* exchange) {
     if (!g || !hp) return set_error(OPTIM_EINVAL, "group or hparams is NULL");
     if (g->kind != OPTIM_KIND_NADAM && g->kind != OPTIM_KIND_NADAM_F24)
         return set_error(OPTIM_EINVAL, "not a NADAM group");
+    if (g->pending) return set_error(OPTIM_ESTATE, "step %lld was begun and not ended", (long long)g->pending_step);
     if (step != g->last_step + 1)
         return set_error(OPTIM_EINVAL, "step %lld but the group expects %lld", (long long)step,
                          (long long)(g->last_step + 1));
@@ -259,6 +260,7 @@ int optim_step_nadam_kahan(optim_group_t* g, const void* const* grads, int64_t s
         (hp->wd_mode != 0 && hp->wd_mode != 1) || (hp->nesterov != 0 && hp->nesterov != 1) ||
         (hp->stochastic_rounding != 0 && hp->stochastic_rounding != 1))
         return set_error(OPTIM_EINVAL, "invalid NAdam hyper-parameters (wd_mode must be 0 or 1)");
+    if (exchange && !is_aligned(exchange, 4)) return set_error(OPTIM_EALIGN, "exchange buffer not 4-byte aligned");
     int rc = check_device(g);
     if (!rc) rc = validate_grads(g, grads);
     if (rc) return rc;
@@ -302,14 +304,45 @@ int optim_step_nadam_kahan(optim_group_t* g, const void* const* grads, int64_t s
     }
     NadamLaunch L{table, g->d_grads, g->d_scales, g->d_chunks, g->d_nonfinite,
                   g->n_chunks_large, g->n_chunks_total, g->kind == OPTIM_KIND_NADAM_F24};
-    rc = launch_nadam_step(L, k, s, g->profile_ev);
+    rc = launch_nadam_prepass(L, k, s);
+    if (!rc && exchange) rc = launch_scales_gather(g->d_scales, exchange, g->n, k.parity, s);
     if (rc) return rc;
-    g->last_step = step;
-    g->mu_product = mu_product;
+    g->pending = true;
+    g->pending_step = step;
+    g->pending_mu = mu_product;
+    g->pending_k = k;
+    g->pending_table = table;
+    g->pending_stream = s;
+    return OPTIM_OK;
+}
+
+int optim_step_nadam_end(optim_group_t* g, const float* exchange, void* stream) {
+    if (!g) return set_error(OPTIM_EINVAL, "group is NULL");
+    if (!g->pending) return set_error(OPTIM_ESTATE, "no NAdam step was begun on this group");
+    if (exchange && !is_aligned(exchange, 4)) return set_error(OPTIM_EALIGN, "exchange buffer not 4-byte aligned");
+    int rc = check_device(g);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const NadamScalars& k = g->pending_k;
+    NadamLaunch L{g->pending_table, g->d_grads, g->d_scales, g->d_chunks, g->d_nonfinite,
+                  g->n_chunks_large, g->n_chunks_total, g->kind == OPTIM_KIND_NADAM_F24};
+    if (exchange) rc = launch_scales_scatter(g->d_scales, exchange, g->n, k.parity, s);
+    if (!rc) rc = launch_nadam_update(L, k, s, g->profile_ev);
+    if (rc) return rc;
+    g->pending = false;
+    g->last_step = g->pending_step;
+    g->mu_product = g->pending_mu;
     g->next_parity ^= 1;
     g->last_stream = s;
     if (g->offload) return offload_step_end(g, s);
     return OPTIM_OK;
+}
+
+int optim_step_nadam_kahan(optim_group_t* g, const void* const* grads, int64_t step,
+                           const optim_nadam_hparams_t* hp, void* stream) {
+    int rc = optim_step_nadam_begin(g, grads, step, hp, stream, nullptr);
+    if (rc) return rc;
+    return optim_step_nadam_end(g, nullptr, stream);
 }
 
 int optim_step_adan(optim_group_t* g, const void* const* grads, int64_t step, const optim_adan_hparams_t* hp,
@@ -428,6 +461,7 @@ int optim_query_scales(optim_group_t* g, float* host_out) {
 int optim_set_scales(optim_group_t* g, const float* host_in) {
     if (!g || !host_in) return set_error(OPTIM_EINVAL, "group or input is NULL");
     if (g->kind != OPTIM_KIND_NADAM) return set_error(OPTIM_EINVAL, "not a NADAM group");
+    if (g->pending) return set_error(OPTIM_ESTATE, "a NAdam step was begun and not ended");
     int rc = check_device(g);
     if (!rc) rc = sync_group(g);
     if (rc) return rc;
@@ -455,6 +489,7 @@ int optim_group_get_step(optim_group_t* g, int64_t* step, double* mu_product) {
 
 int optim_group_set_step(optim_group_t* g, int64_t step, double mu_product) {
     if (!g || step < 0 || !std::isfinite(mu_product)) return set_error(OPTIM_EINVAL, "bad step or mu product");
+    if (g->pending) return set_error(OPTIM_ESTATE, "a NAdam step was begun and not ended");
     g->last_step = step;
     g->mu_product = mu_product;
     return OPTIM_OK;

@@ -41,6 +41,13 @@ struct optim_group {
     cudaStream_t last_stream = nullptr;
     cudaEvent_t profile_ev = nullptr;
     lmo::OffloadBinding* offload = nullptr;   // non-NULL: res/m/v are pinned host buffers
+    // a NAdam step begun (pre-pass enqueued) and not yet ended
+    bool pending = false;
+    int64_t pending_step = 0;
+    double pending_mu = 1.0;
+    lmo::NadamScalars pending_k{};
+    const lmo::TensorRec* pending_table = nullptr;
+    cudaStream_t pending_stream = nullptr;
 };
 
 namespace lmo {

@@ -49,7 +49,13 @@ struct NadamLaunch {
     int32_t n_chunks_total;
     int32_t f24;              // moments stored as f24 planes instead of u16 codes
 };
-int launch_nadam_step(const NadamLaunch& L, const NadamScalars& k, cudaStream_t s, cudaEvent_t mid);
+// K1 (gradient maxima; nothing for f24 moments), then K2 (the update; `mid`, if not null, is
+// recorded on the stream before it).  A step is both, in this order, on one stream.
+int launch_nadam_prepass(const NadamLaunch& L, const NadamScalars& k, cudaStream_t s);
+int launch_nadam_update(const NadamLaunch& L, const NadamScalars& k, cudaStream_t s, cudaEvent_t mid);
+// Per tensor {G (this step), A_m, A_v (previous step)} to / from 3 consecutive floats.
+int launch_scales_gather(const ScaleRec* sc, float* buf, int n, int parity, cudaStream_t s);
+int launch_scales_scatter(ScaleRec* sc, const float* buf, int n, int parity, cudaStream_t s);
 
 // Per-step scalars of the Adan kernel.
 struct AdanScalars {

@@ -524,35 +524,63 @@ __global__ void __launch_bounds__(kThreads, 4) k_nadam_f24(NadamLaunch L, Prm k)
     if (threadIdx.x == 0 && r[0]) atomicAdd(L.nonfinite, 1ull);
 }
 
+// ------------------------------------------------------------------------------------ scale exchange
+// The codec scale of a tensor split across ranks needs the maxima over all of its slices: the
+// step's gradient maximum G (slot p, from K1) and the previous step's moment maxima A_m, A_v
+// (slot q).  Gather copies them per tensor into three consecutive floats (non-negative values,
+// so a MAX reduction of the floats is a MAX of the bit patterns); scatter writes them back.
+__global__ void k_scales_gather(const ScaleRec* sc, float* buf, int n, int parity) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const int p = parity, q = parity ^ 1;
+    buf[3 * i] = __uint_as_float(sc[i].g[p]);
+    buf[3 * i + 1] = __uint_as_float(sc[i].a_m[q]);
+    buf[3 * i + 2] = __uint_as_float(sc[i].a_v[q]);
+}
+__global__ void k_scales_scatter(ScaleRec* sc, const float* buf, int n, int parity) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const int p = parity, q = parity ^ 1;
+    sc[i].g[p] = __float_as_uint(buf[3 * i]);
+    sc[i].a_m[q] = __float_as_uint(buf[3 * i + 1]);
+    sc[i].a_v[q] = __float_as_uint(buf[3 * i + 2]);
+}
+
 }  // namespace
 
-int launch_nadam_step(const NadamLaunch& L, const NadamScalars& s, cudaStream_t stream, cudaEvent_t mid) {
+int launch_nadam_prepass(const NadamLaunch& L, const NadamScalars& s, cudaStream_t stream) {
+    if (L.f24 || L.n_chunks_large == 0) return OPTIM_OK;   // f24 moments need no scale
+    k_grad_absmax<<<L.n_chunks_large, kThreads, 0, stream>>>(L, s.parity);
+    return check_cuda(cudaGetLastError(), "grad absmax launch");
+}
+
+int launch_nadam_update(const NadamLaunch& L, const NadamScalars& s, cudaStream_t stream, cudaEvent_t mid) {
     Prm k{s.lr, s.b1, s.omb1, s.b2, s.omb2, s.eps, s.lr_wd, s.c_m, s.c_g, s.k2, s.decoupled, s.sr, s.seed, s.step};
-    if (L.f24) {
-        if (mid) {
-            int rc = check_cuda(cudaEventRecord(mid, stream), "profile event");
-            if (rc) return rc;
-        }
-        if (L.n_chunks_total == 0) return OPTIM_OK;
-        if (k.sr) k_nadam_f24<true><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k);
-        else k_nadam_f24<false><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k);
-        return check_cuda(cudaGetLastError(), "nadam f24 step launch");
-    }
-    if (L.n_chunks_large > 0) {
-        k_grad_absmax<<<L.n_chunks_large, kThreads, 0, stream>>>(L, s.parity);
-        int rc = check_cuda(cudaGetLastError(), "grad absmax launch");
-        if (rc) return rc;
-    }
     if (mid) {
         int rc = check_cuda(cudaEventRecord(mid, stream), "profile event");
         if (rc) return rc;
     }
-    if (L.n_chunks_total > 0) {
-        if (k.sr) k_nadam_step<true><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k, s.parity);
-        else k_nadam_step<false><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k, s.parity);
-        return check_cuda(cudaGetLastError(), "nadam step launch");
+    if (L.n_chunks_total == 0) return OPTIM_OK;
+    if (L.f24) {
+        if (k.sr) k_nadam_f24<true><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k);
+        else k_nadam_f24<false><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k);
+        return check_cuda(cudaGetLastError(), "nadam f24 step launch");
     }
-    return OPTIM_OK;
+    if (k.sr) k_nadam_step<true><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k, s.parity);
+    else k_nadam_step<false><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k, s.parity);
+    return check_cuda(cudaGetLastError(), "nadam step launch");
+}
+
+int launch_scales_gather(const ScaleRec* sc, float* buf, int n, int parity, cudaStream_t stream) {
+    if (n == 0) return OPTIM_OK;
+    k_scales_gather<<<(n + kThreads - 1) / kThreads, kThreads, 0, stream>>>(sc, buf, n, parity);
+    return check_cuda(cudaGetLastError(), "scale gather launch");
+}
+
+int launch_scales_scatter(ScaleRec* sc, const float* buf, int n, int parity, cudaStream_t stream) {
+    if (n == 0) return OPTIM_OK;
+    k_scales_scatter<<<(n + kThreads - 1) / kThreads, kThreads, 0, stream>>>(sc, buf, n, parity);
+    return check_cuda(cudaGetLastError(), "scale scatter launch");
 }
 
 }  // namespace lmo

@@ -201,6 +201,7 @@ int optim_group_attach_offload(optim_group_t* g, optim_offload_t* e) {
     if (!g || !e) return set_error(OPTIM_EINVAL, "group or engine is NULL");
     if (g->kind != OPTIM_KIND_NADAM) return set_error(OPTIM_EINVAL, "only NADAM groups with u16 moments can be offloaded");
     if (g->offload) return set_error(OPTIM_ESTATE, "group already attached");
+    if (g->pending) return set_error(OPTIM_ESTATE, "a NAdam step was begun and not ended");
     if (g->device != e->device) return set_error(OPTIM_EINVAL, "group and engine are on different devices");
     OffloadBinding* b = new OffloadBinding();
     b->eng = e;

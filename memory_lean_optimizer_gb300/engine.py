@@ -196,12 +196,31 @@ class NadamGroup(_Group):
             rs.append(lo)
         return cls(ws, rs, offload=offload, states=states)
 
+    @staticmethod
+    def _hparams(hp: dict) -> lmopt.NadamHparams:
+        return lmopt.NadamHparams(lr=hp["lr"], beta1=hp["beta1"], beta2=hp["beta2"], eps=hp["eps"],
+                                  weight_decay=hp.get("weight_decay", 0.0), wd_mode=hp.get("wd_mode", 0),
+                                  nesterov=hp.get("nesterov", 1), momentum_decay=hp.get("momentum_decay", 0.004),
+                                  stochastic_rounding=hp.get("stochastic_rounding", 0), seed=hp.get("seed", 0))
+
     def step(self, grads: Sequence[torch.Tensor], hp: dict, stream=None):
-        h = lmopt.NadamHparams(lr=hp["lr"], beta1=hp["beta1"], beta2=hp["beta2"], eps=hp["eps"],
-                               weight_decay=hp.get("weight_decay", 0.0), wd_mode=hp.get("wd_mode", 0),
-                               nesterov=hp.get("nesterov", 1), momentum_decay=hp.get("momentum_decay", 0.004),
-                               stochastic_rounding=hp.get("stochastic_rounding", 0), seed=hp.get("seed", 0))
-        lmopt.optim_step_nadam_kahan(self.handle, self._grad_ptrs(grads), self.step_count + 1, h, _stream_ptr(stream))
+        lmopt.optim_step_nadam_kahan(self.handle, self._grad_ptrs(grads), self.step_count + 1, self._hparams(hp),
+                                     _stream_ptr(stream))
+        self.step_count += 1
+
+    def exchange_buffer(self) -> torch.Tensor:
+        """Device buffer of 3 floats per tensor for optim_step_nadam_begin / _end."""
+        return torch.zeros(3 * len(self.weights), dtype=torch.float32, device=self.weights[0].device)
+
+    def step_begin(self, grads: Sequence[torch.Tensor], hp: dict, exchange: torch.Tensor | None = None, stream=None):
+        """Gradient pre-pass; fills `exchange` with the per-tensor maxima to MAX-reduce across ranks."""
+        lmopt.optim_step_nadam_begin(self.handle, self._grad_ptrs(grads), self.step_count + 1, self._hparams(hp),
+                                     _stream_ptr(stream), exchange.data_ptr() if exchange is not None else None)
+
+    def step_end(self, exchange: torch.Tensor | None = None, stream=None):
+        """Update, after the reduced maxima are written back from `exchange`."""
+        lmopt.optim_step_nadam_end(self.handle, exchange.data_ptr() if exchange is not None else None,
+                                   _stream_ptr(stream))
         self.step_count += 1
 
     def masters(self):

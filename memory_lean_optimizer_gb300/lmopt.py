@@ -38,7 +38,7 @@ EXPORTED = (
     "optim_query_nonfinite", "optim_group_set_profile_event", "optim_last_error",
     "optim_step_factored_noalloc", "optim_step_adan",
     "optim_offload_create", "optim_offload_destroy", "optim_group_attach_offload",
-    "optim_offload_prefetch", "optim_offload_sync",
+    "optim_offload_prefetch", "optim_offload_sync", "optim_step_nadam_begin", "optim_step_nadam_end",
 )
 
 
@@ -92,6 +92,8 @@ def load(path: str = LIB_PATH):
             "optim_group_create": [ctypes.POINTER(TensorDesc), I32, I32, ctypes.POINTER(P)],
             "optim_group_destroy": [P],
             "optim_step_nadam_kahan": [P, P, I64, ctypes.POINTER(NadamHparams), P],
+            "optim_step_nadam_begin": [P, P, I64, ctypes.POINTER(NadamHparams), P, P],
+            "optim_step_nadam_end": [P, P, P],
             "optim_step_factored": [P, P, I64, ctypes.POINTER(FactoredHparams), P],
             "optim_step_adan": [P, P, I64, ctypes.POINTER(AdanHparams), P],
             "optim_step_factored_noalloc": [ctypes.POINTER(TensorDesc), P, I64, ctypes.POINTER(FactoredHparams), P],
@@ -153,6 +155,18 @@ def optim_group_destroy(handle: int) -> None:
 
 def optim_step_nadam_kahan(handle: int, grad_ptrs, step: int, hp: NadamHparams, stream: int = 0) -> None:
     check(load().optim_step_nadam_kahan(handle, _ptr_array(grad_ptrs), step, ctypes.byref(hp), stream))
+
+
+def optim_step_nadam_begin(handle: int, grad_ptrs, step: int, hp: NadamHparams, stream: int = 0,
+                           exchange: int | None = None) -> None:
+    """Pre-pass of a step; with `exchange` (device pointer, 3 floats per tensor) the per-tensor
+    maxima to be MAX-reduced across ranks are copied there."""
+    check(load().optim_step_nadam_begin(handle, _ptr_array(grad_ptrs), step, ctypes.byref(hp), stream, exchange))
+
+
+def optim_step_nadam_end(handle: int, exchange: int | None = None, stream: int = 0) -> None:
+    """Update of the step begun by optim_step_nadam_begin, after writing back the reduced maxima."""
+    check(load().optim_step_nadam_end(handle, exchange, stream))
 
 
 def optim_step_factored(handle: int, grad_ptrs, step: int, hp: FactoredHparams, stream: int = 0) -> None:

@@ -96,6 +96,8 @@ def _load():
             "orc_grad_absmax": (F, [P, I64]),
             "orc_nadam_step_tensor": (None, [P, P, P, P, P, I64, ctypes.POINTER(Scale),
                                              ctypes.POINTER(NadamScalars)]),
+            "orc_nadam_step_slice": (None, [P, P, P, P, P, I64, I32, F, ctypes.POINTER(Scale),
+                                            ctypes.POINTER(NadamScalars)]),
             "orc_nadam_step_fp32": (None, [P, P, P, P, I64, ctypes.POINTER(NadamScalars)]),
             "orc_nadam_step_tensor_f24": (None, [P, P, P, P, P, I64, ctypes.POINTER(NadamScalars), I32,
                                                  ctypes.c_uint64, ctypes.c_uint32, I64]),
@@ -293,6 +295,14 @@ def f24_merge(buf: np.ndarray) -> np.ndarray:
 
 def nadam_step_fp32(w, m, v, g, k: NadamScalars):
     _load().orc_nadam_step_fp32(_p(w), _p(m), _p(v), _p(_u16(g)), w.size, ctypes.byref(k))
+
+
+def nadam_step_slice(hi, lo, m, v, g, small: bool, G: float, scale: Scale, k: NadamScalars):
+    """One slice of a tensor split across ranks: G and the scale record's A_m, A_v are the maxima
+    over all slices (in place, as nadam_step_tensor)."""
+    n = hi.size
+    _load().orc_nadam_step_slice(_p(hi), _p(lo), _p(m), _p(v), _p(_u16(g)), n, int(small), float(G),
+                                 ctypes.byref(scale), ctypes.byref(k))
 
 
 def nadam_group_step(tensors, grads, state: NadamState, t, hp):

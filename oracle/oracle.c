@@ -254,14 +254,16 @@ static float nadam_elem(float w, float gg, float* mm, float* vv, float* sv,
     return fmaf(-k->lr, num / den, w);
 }
 
-void orc_nadam_step_tensor(uint16_t* hi, uint16_t* lo, void* m, void* v, const uint16_t* g,
-                           int64_t n, orc_scale_t* sc, const orc_nadam_scalars_t* k)
+/* One step of one tensor whose gradient maximum G is given: the scale is a property of the
+ * whole tensor, so a tensor split into slices steps each slice with the maximum over all slices
+ * (and with the maxima A_m, A_v over all slices in the scale record).  `small` chooses the fp32
+ * moments of tensors of 4096 or fewer elements, decided on the whole tensor. */
+void orc_nadam_step_slice(uint16_t* hi, uint16_t* lo, void* m, void* v, const uint16_t* g,
+                          int64_t n, int32_t small, float G, orc_scale_t* sc, const orc_nadam_scalars_t* k)
 {
-    int small = n <= ORC_SMALL_NUMEL;
     float s_m = 0.0f, s_v = 0.0f;
     orc_codec_t dec, enc;
     if (!small) {
-        float G = orc_grad_absmax(g, n);
         s_m = fmaf(k->b1, sc->a_m, k->omb1 * G);
         s_v = fmaf(k->b2, sc->a_v, k->omb2 * (G * G));
         orc_codec_consts(sc->s_m, sc->s_v, &dec);
@@ -302,6 +304,13 @@ void orc_nadam_step_tensor(uint16_t* hi, uint16_t* lo, void* m, void* v, const u
         sc->a_m = am;
         sc->a_v = av;
     }
+}
+
+void orc_nadam_step_tensor(uint16_t* hi, uint16_t* lo, void* m, void* v, const uint16_t* g,
+                           int64_t n, orc_scale_t* sc, const orc_nadam_scalars_t* k)
+{
+    int small = n <= ORC_SMALL_NUMEL;
+    orc_nadam_step_slice(hi, lo, m, v, g, n, small, small ? 0.0f : orc_grad_absmax(g, n), sc, k);
 }
 
 /* ----------------------------------------------------------------------------------------

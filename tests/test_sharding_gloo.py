@@ -97,3 +97,104 @@ def test_two_rank_sharded_step_matches_single_process(orc):
         for gi in range(len(SHAPES)):
             for i in range(len(SHAPES[gi])):
                 assert np.array_equal(weights[gi][i].view(np.uint16), ref[gi][i]), (rank, gi, i)
+
+
+# ---------------------------------------------------------------- one tensor split across ranks
+SPLIT_SIZES = [20000, 9000, 3000, 70001, 5000]
+
+
+def _split_inputs(ti, n, t=None):
+    rng = np.random.default_rng(5000 + 10 * ti + (t or 0))
+    if t is None:
+        return (rng.standard_normal(n) * 0.02).astype(np.float32)
+    g = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    return torch.from_numpy(g).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _split_worker(rank, world, port, q):
+    import sys
+    sys.path.insert(0, os.path.dirname(__file__))
+    import oracle as orc
+    from memory_lean_optimizer_gb300.sharding import plan_slices, rank_slices
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    plan = plan_slices(SPLIT_SIZES, world)
+    mine, n_split = rank_slices(plan, rank)
+    st, scales = [], (orc.Scale * max(1, len(mine)))()
+    for ti, a, b in mine:
+        small = SPLIT_SIZES[ti] <= 4096        # decided on the whole tensor
+        hi, lo = orc.kahan_split(_split_inputs(ti, SPLIT_SIZES[ti])[a:b])
+        m = np.zeros(b - a, np.float32) if small else np.full(b - a, 32768, np.uint16)
+        v = np.zeros(b - a, np.float32) if small else np.zeros(b - a, np.uint16)
+        st.append(dict(hi=hi, lo=lo, m=m, v=v, small=small))
+    mu = 1.0
+    for t in range(1, 4):
+        k, mu = orc.nadam_scalars(t, HP["lr"], HP["beta1"], HP["beta2"], HP["eps"], HP["weight_decay"], True,
+                                  True, HP["momentum_decay"], mu)
+        grads = [_split_inputs(ti, SPLIT_SIZES[ti], t)[a:b] for ti, a, b in mine]
+        ex = torch.zeros(3 * len(mine), dtype=torch.float32)
+        for j, g in enumerate(grads):
+            ex[3 * j] = 0.0 if st[j]["small"] else orc.grad_absmax(g)
+            ex[3 * j + 1], ex[3 * j + 2] = scales[j].a_m, scales[j].a_v
+        if n_split:
+            red = ex[: 3 * n_split].clone()
+            dist.all_reduce(red, op=dist.ReduceOp.MAX)
+            ex[: 3 * n_split] = red
+        for j, (s, g) in enumerate(zip(st, grads)):
+            scales[j].a_m, scales[j].a_v = float(ex[3 * j + 1]), float(ex[3 * j + 2])
+            orc.nadam_step_slice(s["hi"], s["lo"], s["m"], s["v"], g, s["small"], float(ex[3 * j]), scales[j], k)
+    q.put((rank, [(ti, a, b, s["hi"], s["lo"], s["m"], s["v"]) for (ti, a, b), s in zip(mine, st)]))
+    dist.destroy_process_group()
+
+
+def test_plan_slices_cover_and_align():
+    from memory_lean_optimizer_gb300.sharding import plan_slices, rank_slices
+    sizes = [20000, 9000, 3000, 70001, 5000, 8200, 8217, 0]
+    for world in (1, 2, 3, 4):
+        plan = plan_slices(sizes, world)
+        for n, sl in zip(sizes, plan):
+            covered = sorted((a, b) for _, a, b in sl)
+            assert covered[0][0] == 0 and covered[-1][1] == n
+            assert all(b0 == a1 for (_, b0), (a1, _) in zip(covered, covered[1:]))
+            if len(sl) > 1:
+                assert len(sl) == world and sorted(r for r, _, _ in sl) == list(range(world))
+                assert all(b - a > 4096 and a % 8 == 0 for _, a, b in sl)
+        n_split = sum(len(sl) > 1 for sl in plan)
+        for r in range(world):
+            mine, ns = rank_slices(plan, r)
+            assert ns == n_split and [ti for ti, _, _ in mine[:ns]] == [ti for ti, sl in enumerate(plan) if len(sl) > 1]
+
+
+@pytest.mark.slow
+def test_two_rank_split_tensors_match_unsplit(orc):
+    """Tensors split across 2 gloo ranks, the codec maxima MAX-reduced between the pre-pass and
+    the update: weights, residuals and moment codes of every slice equal the unsplit step's."""
+    from helpers import OracleNadam
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_split_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    results = []
+    for _ in procs:
+        try:
+            results.append(q.get(timeout=180))
+        except Exception:
+            break
+    assert len(results) == 2, f"worker exit codes {[p.exitcode for p in procs]}"
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    ref = OracleNadam(orc, [_split_inputs(ti, n) for ti, n in enumerate(SPLIT_SIZES)])
+    for t in range(1, 4):
+        ref.step([_split_inputs(ti, n, t) for ti, n in enumerate(SPLIT_SIZES)], dict(HP))
+    seen = 0
+    for rank, slices in results:
+        for ti, a, b, hi, lo, m, v in slices:
+            rt = ref.t[ti]
+            assert np.array_equal(hi, rt["hi"][a:b]) and np.array_equal(lo, rt["lo"][a:b]), (rank, ti)
+            assert np.array_equal(m.view(np.uint8), rt["m"][a:b].view(np.uint8)), (rank, ti)
+            assert np.array_equal(v.view(np.uint8), rt["v"][a:b].view(np.uint8)), (rank, ti)
+            seen += b - a
+    assert seen == sum(SPLIT_SIZES)
