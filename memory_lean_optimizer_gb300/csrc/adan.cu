@@ -55,9 +55,9 @@ __device__ __forceinline__ float adan_elem(const AdanPrm& k, float w, float g, f
         const float c = __fmaf_rn(k.omb2, d, g);
         n = __fmaf_rn(k.omb3, n, __fmul_rn(k.b3, __fmul_rn(c, c)));
     }
-    const float den = __fadd_rn(__fsqrt_rn(n), k.eps);
+    const float den = __fadd_rn(sqrt_rn_z(n), k.eps);
     const float u = __fmaf_rn(k.omb2, v, m);
-    return __fmul_rn(__fsub_rn(w, __fmul_rn(k.lr, __fdiv_rn(u, den))), k.inv_decay);
+    return __fmul_rn(__fsub_rn(w, __fmul_rn(k.lr, div_rn_z(u, den))), k.inv_decay);
 }
 
 // Stores the updated weight (Kahan split, stochastic rounding or RNE); returns the bf16 word.

@@ -80,6 +80,7 @@ static void group_free(optim_group* g) {
     cudaFree(g->d_scales);
     cudaFree(g->d_chunks);
     cudaFree(g->d_nonfinite);
+    cudaFree(g->d_zero_chunk);
     factored_plan_free(g->fplan);
     delete g;
 }
@@ -219,6 +220,7 @@ int optim_group_create(const optim_tensor_desc_t* tensors, int32_t n, int32_t ki
         if (!rc) rc = dev_upload(&g->d_chunks, chunks, "chunk table");
         if (!rc) rc = dev_upload(&g->d_scales, std::vector<ScaleRec>(n, ScaleRec{}), "scale table");
         if (!rc) rc = dev_upload(&g->d_nonfinite, std::vector<unsigned long long>(1, 0ull), "counter");
+        if (!rc) rc = dev_upload(&g->d_zero_chunk, std::vector<uint8_t>(std::max<int32_t>(g->n_chunks_large, 1), 1), "zero flags");
         if (!rc) rc = dev_upload(&g->d_grads, std::vector<const uint16_t*>(n, nullptr), "gradient table");
         for (int s = 0; s < 2 && !rc; ++s) {
             if (cudaHostAlloc(reinterpret_cast<void**>(&g->h_stage[s]), sizeof(void*) * n, cudaHostAllocDefault) != cudaSuccess) {
@@ -303,7 +305,7 @@ int optim_step_nadam_begin(optim_group_t* g, const void* const* grads, int64_t s
         if (rc) return rc;
     }
     NadamLaunch L{table, g->d_grads, g->d_scales, g->d_chunks, g->d_nonfinite,
-                  g->n_chunks_large, g->n_chunks_total, g->kind == OPTIM_KIND_NADAM_F24};
+                  g->n_chunks_large, g->n_chunks_total, g->kind == OPTIM_KIND_NADAM_F24, g->d_zero_chunk};
     rc = launch_nadam_prepass(L, k, s);
     if (!rc && exchange) rc = launch_scales_gather(g->d_scales, exchange, g->n, k.parity, s);
     if (rc) return rc;
@@ -325,7 +327,7 @@ int optim_step_nadam_end(optim_group_t* g, const float* exchange, void* stream) 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const NadamScalars& k = g->pending_k;
     NadamLaunch L{g->pending_table, g->d_grads, g->d_scales, g->d_chunks, g->d_nonfinite,
-                  g->n_chunks_large, g->n_chunks_total, g->kind == OPTIM_KIND_NADAM_F24};
+                  g->n_chunks_large, g->n_chunks_total, g->kind == OPTIM_KIND_NADAM_F24, g->d_zero_chunk};
     if (exchange) rc = launch_scales_scatter(g->d_scales, exchange, g->n, k.parity, s);
     if (!rc) rc = launch_nadam_update(L, k, s, g->profile_ev);
     if (rc) return rc;
@@ -377,7 +379,7 @@ int optim_step_adan(optim_group_t* g, const void* const* grads, int64_t step, co
     rc = upload_grads(g, grads, s);
     if (rc) return rc;
     NadamLaunch L{g->d_tensors, g->d_grads, g->d_scales, g->d_chunks, g->d_nonfinite, g->n_chunks_large,
-                  g->n_chunks_total, 0};
+                  g->n_chunks_total, 0, nullptr};
     rc = launch_adan_step(L, k, s);
     if (rc) return rc;
     g->last_step = step;

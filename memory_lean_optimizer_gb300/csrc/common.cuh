@@ -57,6 +57,22 @@ struct Chunk {
 
 __device__ __forceinline__ float bf16_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
 
+// IEEE square root and quotient with an exact-zero operand kept out of the library routines'
+// special-value branch: a lane whose argument is zero computes on 1 instead and selects the
+// exact answer (sqrt(+-0) = +-0; +-0 / b = +-0 for b > 0; any other b divides as usual).  Same
+// results as __fsqrt_rn / __fdiv_rn; without it, exact-zero gradients (a few per warp) make
+// whole warps diverge.
+__device__ __forceinline__ float sqrt_rn_z(float x) {
+    const bool z = x == 0.0f;
+    const float r = __fsqrt_rn(z ? 1.0f : x);
+    return z ? x : r;
+}
+__device__ __forceinline__ float div_rn_z(float a, float b) {
+    const bool z = a == 0.0f && b > 0.0f;
+    const float r = __fdiv_rn(z ? b : a, b);
+    return z ? a : r;
+}
+
 // Round-to-nearest-even fp32 -> bf16 bits (store used when no residual is kept); NaN keeps
 // its payload's upper bits with the quiet bit set.
 __device__ __forceinline__ uint32_t rne_bf16(float x) {
@@ -110,12 +126,12 @@ __device__ __forceinline__ float dec_v(uint32_t c, float qv) { return dec_v_fiel
 // biased exp_avg code) rounds the clamped root to the nearest integer, ties to even, exactly as
 // rint, and leaves it in the low mantissa bits.
 __device__ __forceinline__ uint32_t enc_m_bits(float m, float rm) {
-    const float y = fminf(__fsqrt_rn(__fmul_rn(fabsf(m), rm)), 32767.0f);
+    const float y = fminf(sqrt_rn_z(__fmul_rn(fabsf(m), rm)), 32767.0f);
     return __float_as_uint(__fadd_rn(12615680.0f, copysignf(y, m)));
 }
 // sv = sqrt(v), shared with the update's denominator.
 __device__ __forceinline__ uint32_t enc_v_bits(float sv, float rv) {
-    const float y = fminf(__fsqrt_rn(__fmul_rn(sv, rv)), 65535.0f);
+    const float y = fminf(sqrt_rn_z(__fmul_rn(sv, rv)), 65535.0f);
     return __float_as_uint(__fadd_rn(12582912.0f, y));
 }
 __device__ __forceinline__ uint32_t enc_m(float m, float rm) { return enc_m_bits(m, rm) & 0xFFFFu; }

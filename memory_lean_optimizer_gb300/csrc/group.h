@@ -24,6 +24,7 @@ struct optim_group {
     lmo::ScaleRec* d_scales = nullptr;
     lmo::Chunk* d_chunks = nullptr;
     unsigned long long* d_nonfinite = nullptr;
+    uint8_t* d_zero_chunk = nullptr;   // one flag per u16-state chunk, written by the pre-pass
     int32_t n_chunks_large = 0;
     int32_t n_chunks_total = 0;
     lmo::FactoredPlan* fplan = nullptr;

@@ -48,6 +48,8 @@ struct NadamLaunch {
     int32_t n_chunks_large;   // chunks of u16-state tensors come first
     int32_t n_chunks_total;
     int32_t f24;              // moments stored as f24 planes instead of u16 codes
+    uint8_t* zero_chunk;      // per u16 chunk: the gradient pre-pass saw an exact zero (K2 then
+                              // takes the zero-guarded arithmetic for that chunk)
 };
 // K1 (gradient maxima; nothing for f24 moments), then K2 (the update; `mid`, if not null, is
 // recorded on the stream before it).  A step is both, in this order, on one stream.

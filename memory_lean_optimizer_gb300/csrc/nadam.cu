@@ -95,7 +95,7 @@ __device__ __forceinline__ uint32_t sr_bf16(float x, uint32_t r16) {
 
 // ------------------------------------------------------------------------------------ K1
 __global__ void __launch_bounds__(kThreads) k_grad_absmax(NadamLaunch L, int parity) {
-    __shared__ uint32_t red[32];
+    __shared__ uint32_t red[2 * 32];
     const Chunk c = L.chunks[blockIdx.x];
     const int64_t numel = L.tensors[c.tensor].numel;
     const uint16_t* __restrict__ g = L.grads[c.tensor];
@@ -109,6 +109,14 @@ __global__ void __launch_bounds__(kThreads) k_grad_absmax(NadamLaunch L, int par
     const int64_t start = (int64_t)c.index * kChunk;
     const int64_t end = min(numel, start + kChunk);
     uint32_t mx = 0u;
+    // exact zeros: a 16-bit magnitude t (bit 15 clear) is zero iff t - 1 sets bit 15; the
+    // borrow into the upper half matters only when the lower half is zero, which is flagged anyway
+    uint32_t zb = 0u;
+    auto scan = [&](uint32_t x) {
+        const uint32_t t = x & 0x7FFF7FFFu;
+        zb |= t - 0x00010001u;
+        return t;
+    };
     int64_t done = start;
     if (aligned16(g)) {
         const int64_t nv = (end - start) >> 3;
@@ -117,39 +125,54 @@ __global__ void __launch_bounds__(kThreads) k_grad_absmax(NadamLaunch L, int par
         for (; i + 3 * kThreads < nv; i += 4 * kThreads) {
             uint4 x0 = __ldcg(gv + i), x1 = __ldcg(gv + i + kThreads);
             uint4 x2 = __ldcg(gv + i + 2 * kThreads), x3 = __ldcg(gv + i + 3 * kThreads);
-            mx = __vmaxu2(mx, __vmaxu2(x0.x & 0x7FFF7FFFu, x0.y & 0x7FFF7FFFu));
-            mx = __vmaxu2(mx, __vmaxu2(x0.z & 0x7FFF7FFFu, x0.w & 0x7FFF7FFFu));
-            mx = __vmaxu2(mx, __vmaxu2(x1.x & 0x7FFF7FFFu, x1.y & 0x7FFF7FFFu));
-            mx = __vmaxu2(mx, __vmaxu2(x1.z & 0x7FFF7FFFu, x1.w & 0x7FFF7FFFu));
-            mx = __vmaxu2(mx, __vmaxu2(x2.x & 0x7FFF7FFFu, x2.y & 0x7FFF7FFFu));
-            mx = __vmaxu2(mx, __vmaxu2(x2.z & 0x7FFF7FFFu, x2.w & 0x7FFF7FFFu));
-            mx = __vmaxu2(mx, __vmaxu2(x3.x & 0x7FFF7FFFu, x3.y & 0x7FFF7FFFu));
-            mx = __vmaxu2(mx, __vmaxu2(x3.z & 0x7FFF7FFFu, x3.w & 0x7FFF7FFFu));
+            mx = __vmaxu2(mx, __vmaxu2(scan(x0.x), scan(x0.y)));
+            mx = __vmaxu2(mx, __vmaxu2(scan(x0.z), scan(x0.w)));
+            mx = __vmaxu2(mx, __vmaxu2(scan(x1.x), scan(x1.y)));
+            mx = __vmaxu2(mx, __vmaxu2(scan(x1.z), scan(x1.w)));
+            mx = __vmaxu2(mx, __vmaxu2(scan(x2.x), scan(x2.y)));
+            mx = __vmaxu2(mx, __vmaxu2(scan(x2.z), scan(x2.w)));
+            mx = __vmaxu2(mx, __vmaxu2(scan(x3.x), scan(x3.y)));
+            mx = __vmaxu2(mx, __vmaxu2(scan(x3.z), scan(x3.w)));
         }
         for (; i < nv; i += kThreads) {
             uint4 x = __ldcg(gv + i);
-            mx = __vmaxu2(mx, __vmaxu2(x.x & 0x7FFF7FFFu, x.y & 0x7FFF7FFFu));
-            mx = __vmaxu2(mx, __vmaxu2(x.z & 0x7FFF7FFFu, x.w & 0x7FFF7FFFu));
+            mx = __vmaxu2(mx, __vmaxu2(scan(x.x), scan(x.y)));
+            mx = __vmaxu2(mx, __vmaxu2(scan(x.z), scan(x.w)));
         }
         mx = max(mx & 0xFFFFu, mx >> 16);
         done = start + (nv << 3);
     }
-    for (int64_t i = done + threadIdx.x; i < end; i += kThreads) mx = max(mx, (uint32_t)(g[i] & 0x7FFFu));
-    uint32_t v[1] = {mx};
-    block_max_u32<1>(v, red);
-    if (threadIdx.x == 0 && v[0] != 0u) atomicMax(&sr->g[p], v[0] << 16);
+    for (int64_t i = done + threadIdx.x; i < end; i += kThreads) {
+        const uint32_t t = g[i] & 0x7FFFu;
+        mx = max(mx, t);
+        if (t == 0u) zb |= 0x8000u;
+    }
+    uint32_t v[2] = {mx, (zb & 0x80008000u) ? 1u : 0u};
+    block_max_u32<2>(v, red);
+    if (threadIdx.x == 0) {
+        if (v[0] != 0u) atomicMax(&sr->g[p], v[0] << 16);
+        L.zero_chunk[blockIdx.x] = (uint8_t)v[1];
+    }
 }
 
 // ------------------------------------------------------------------------------------ K2
+// Square root and quotient: kGuard selects the forms that keep exact zeros out of the library
+// routines' special-value branch (same results; used where exact-zero gradients occur).
+template <bool kGuard>
+__device__ __forceinline__ float sqrt_k(float x) { return kGuard ? sqrt_rn_z(x) : __fsqrt_rn(x); }
+template <bool kGuard>
+__device__ __forceinline__ float div_k(float a, float b) { return kGuard ? div_rn_z(a, b) : __fdiv_rn(a, b); }
+
 // One element: w, g fp32; m, v in: decoded (or fp32) moments, out: new moments; sv = sqrt(v).
+template <bool kGuard>
 __device__ __forceinline__ float elem(const Prm& k, float w, float g, float& m, float& v, float& sv) {
     m = __fmaf_rn(k.b1, m, __fmul_rn(k.omb1, g));
     v = __fmaf_rn(k.b2, v, __fmul_rn(k.omb2, __fmul_rn(g, g)));
     if (k.decoupled) w = __fmaf_rn(-k.lr_wd, w, w);
-    sv = __fsqrt_rn(v);
+    sv = sqrt_k<kGuard>(v);
     const float den = __fmaf_rn(sv, k.k2, k.eps);
     const float num = __fmaf_rn(k.c_m, m, __fmul_rn(k.c_g, g));
-    return __fmaf_rn(-k.lr, __fdiv_rn(num, den), w);
+    return __fmaf_rn(-k.lr, div_k<kGuard>(num, den), w);
 }
 
 // Packed fp32 pairs: __fmul2_rn / __fadd2_rn round each component exactly as the scalar _rn
@@ -181,6 +204,7 @@ struct Codec {
 
 // Two u16-state elements.  am/av: running max |m|, max v (NaN skipped); nf: running max of the
 // bf16 weight magnitudes (>= 0x7F80 in either half means a non-finite weight).
+template <bool kGuard>
 __device__ __forceinline__ void step2_u16(const Prm& k, const Codec& cd, bool has_res, bool sr, uint32_t rnd,
                                           uint32_t& W, uint32_t& R, uint32_t G, uint32_t& M, uint32_t& V,
                                           float& am, float& av, uint32_t& nf) {
@@ -198,15 +222,15 @@ __device__ __forceinline__ void step2_u16(const Prm& k, const Codec& cd, bool ha
     const float2 z2 = __fmul2_rn(z, z);
     float2 v = __fmul2_rn(z2, z2);
     float2 sv;
-    w.x = elem(k, w.x, __uint_as_float(G << 16), m.x, v.x, sv.x);
-    w.y = elem(k, w.y, __uint_as_float(G & 0xFFFF0000u), m.y, v.y, sv.y);
+    w.x = elem<kGuard>(k, w.x, __uint_as_float(G << 16), m.x, v.x, sv.x);
+    w.y = elem<kGuard>(k, w.y, __uint_as_float(G & 0xFFFF0000u), m.y, v.y, sv.y);
     pack_w(w.x, w.y, has_res, sr, rnd, W, R);
     // encode, as enc_m_bits / enc_v_bits, with the scaling multiply and the rounding add paired
-    const float2 ym = make_float2(copysignf(fminf(__fsqrt_rn(__fmul_rn(fabsf(m.x), cd.enc.rm)), 32767.0f), m.x),
-                                  copysignf(fminf(__fsqrt_rn(__fmul_rn(fabsf(m.y), cd.enc.rm)), 32767.0f), m.y));
+    const float2 ym = make_float2(copysignf(fminf(sqrt_k<kGuard>(__fmul_rn(fabsf(m.x), cd.enc.rm)), 32767.0f), m.x),
+                                  copysignf(fminf(sqrt_k<kGuard>(__fmul_rn(fabsf(m.y), cd.enc.rm)), 32767.0f), m.y));
     const float2 em = __fadd2_rn(f2(12615680.0f), ym);
     const float2 xv = __fmul2_rn(sv, f2(cd.enc.rv));
-    const float2 yv = make_float2(fminf(__fsqrt_rn(xv.x), 65535.0f), fminf(__fsqrt_rn(xv.y), 65535.0f));
+    const float2 yv = make_float2(fminf(sqrt_k<kGuard>(xv.x), 65535.0f), fminf(sqrt_k<kGuard>(xv.y), 65535.0f));
     const float2 ev = __fadd2_rn(f2(12582912.0f), yv);
     M = pack_lo16(__float_as_uint(em.x), __float_as_uint(em.y));
     V = pack_lo16(__float_as_uint(ev.x), __float_as_uint(ev.y));
@@ -221,23 +245,23 @@ __device__ __forceinline__ void step2_f32(const Prm& k, bool has_res, bool sr, u
                                           uint32_t& nf) {
     float w0, w1, s0, s1;
     unpack_w(W, R, has_res, w0, w1);
-    w0 = elem(k, w0, __uint_as_float(G << 16), m0, v0, s0);
-    w1 = elem(k, w1, __uint_as_float(G & 0xFFFF0000u), m1, v1, s1);
+    w0 = elem<true>(k, w0, __uint_as_float(G << 16), m0, v0, s0);
+    w1 = elem<true>(k, w1, __uint_as_float(G & 0xFFFF0000u), m1, v1, s1);
     pack_w(w0, w1, has_res, sr, rnd, W, R);
     nf = __vmaxu2(nf, W & 0x7FFF7FFFu);
 }
 
 // i0: index of the first of the 8 elements (for the stochastic-rounding lanes).  kSR: the
 // stochastic-rounding variant (compiled separately so the residual path carries none of it).
-template <bool kSR>
+template <bool kSR, bool kGuard>
 __device__ __forceinline__ void step8_u16(const Prm& k, const Codec& cd, bool has_res, const uint32_t (&r)[4],
                                           uint4& W, uint4& R, const uint4& G, uint4& M, uint4& V,
                                           float& am, float& av, uint32_t& nf) {
     const bool sr = kSR && !has_res;
-    step2_u16(k, cd, has_res, sr, r[0], W.x, R.x, G.x, M.x, V.x, am, av, nf);
-    step2_u16(k, cd, has_res, sr, r[1], W.y, R.y, G.y, M.y, V.y, am, av, nf);
-    step2_u16(k, cd, has_res, sr, r[2], W.z, R.z, G.z, M.z, V.z, am, av, nf);
-    step2_u16(k, cd, has_res, sr, r[3], W.w, R.w, G.w, M.w, V.w, am, av, nf);
+    step2_u16<kGuard>(k, cd, has_res, sr, r[0], W.x, R.x, G.x, M.x, V.x, am, av, nf);
+    step2_u16<kGuard>(k, cd, has_res, sr, r[1], W.y, R.y, G.y, M.y, V.y, am, av, nf);
+    step2_u16<kGuard>(k, cd, has_res, sr, r[2], W.z, R.z, G.z, M.z, V.z, am, av, nf);
+    step2_u16<kGuard>(k, cd, has_res, sr, r[3], W.w, R.w, G.w, M.w, V.w, am, av, nf);
 }
 
 template <bool kSR>
@@ -250,6 +274,52 @@ __device__ __forceinline__ void step8_f32(const Prm& k, bool has_res, uint32_t t
     step2_f32(k, has_res, sr, r[1], W.y, R.y, G.y, M[0].z, M[0].w, V[0].z, V[0].w, nf);
     step2_f32(k, has_res, sr, r[2], W.z, R.z, G.z, M[1].x, M[1].y, V[1].x, V[1].y, nf);
     step2_f32(k, has_res, sr, r[3], W.w, R.w, G.w, M[1].z, M[1].w, V[1].z, V[1].w, nf);
+}
+
+// The u16-state 128-bit path of one chunk (nv vectors of 8 elements starting at element `start`).
+template <bool kSR, bool kGuard>
+__device__ __forceinline__ void u16_vectors(const Prm& k, const Codec& cd, bool has_res, uint32_t tensor, int64_t start,
+                                            int64_t nv, uint4* wv, uint4* rv, const uint4* gv, uint4* mv, uint4* vv,
+                                            float& am, float& av, uint32_t& nf) {
+    const bool sr = kSR && !has_res;
+    // two independent 8-element groups per iteration: ten 128-bit loads in flight.  With
+    // stochastic rounding the two groups are the halves of one 16-element block, so one
+    // generator call serves both; otherwise they are kThreads vectors apart.
+    int64_t p = threadIdx.x;
+    for (; sr ? (2 * p + 1 < nv) : (p + kThreads < nv); p += sr ? kThreads : 2 * kThreads) {
+        const int64_t i = sr ? 2 * p : p, i1 = sr ? 2 * p + 1 : p + kThreads;
+        uint4 W0 = ld_stream(wv + i), W1 = ld_stream(wv + i1);
+        uint4 R0 = has_res ? ld_stream(rv + i) : make_uint4(0, 0, 0, 0);
+        uint4 R1 = has_res ? ld_stream(rv + i1) : make_uint4(0, 0, 0, 0);
+        uint4 G0 = ld_stream(gv + i), G1 = ld_stream(gv + i1);
+        uint4 M0 = ld_stream(mv + i), M1 = ld_stream(mv + i1);
+        uint4 V0 = ld_stream(vv + i), V1 = ld_stream(vv + i1);
+        uint32_t ra[4] = {0u, 0u, 0u, 0u}, rb[4] = {0u, 0u, 0u, 0u};
+        if (sr) sr_lanes16(k, tensor, start + 16 * p, ra, rb);
+        step8_u16<kSR, kGuard>(k, cd, has_res, ra, W0, R0, G0, M0, V0, am, av, nf);
+        st_stream(wv + i, W0);
+        if (has_res) st_stream(rv + i, R0);
+        st_stream(mv + i, M0);
+        st_stream(vv + i, V0);
+        step8_u16<kSR, kGuard>(k, cd, has_res, rb, W1, R1, G1, M1, V1, am, av, nf);
+        st_stream(wv + i1, W1);
+        if (has_res) st_stream(rv + i1, R1);
+        st_stream(mv + i1, M1);
+        st_stream(vv + i1, V1);
+    }
+    // remaining vectors one at a time
+    for (int64_t i = sr ? 2 * p : p; i < nv; i += kThreads) {
+        uint4 W0 = ld_stream(wv + i);
+        uint4 R0 = has_res ? ld_stream(rv + i) : make_uint4(0, 0, 0, 0);
+        uint4 G0 = ld_stream(gv + i), M0 = ld_stream(mv + i), V0 = ld_stream(vv + i);
+        uint32_t ra[4] = {0u, 0u, 0u, 0u};
+        if (sr) sr_lanes8(k, tensor, start + 8 * i, ra);
+        step8_u16<kSR, kGuard>(k, cd, has_res, ra, W0, R0, G0, M0, V0, am, av, nf);
+        st_stream(wv + i, W0);
+        if (has_res) st_stream(rv + i, R0);
+        st_stream(mv + i, M0);
+        st_stream(vv + i, V0);
+    }
 }
 
 template <bool kSR>
@@ -294,45 +364,12 @@ __global__ void __launch_bounds__(kThreads, 4) k_nadam_step(NadamLaunch L, Prm k
         if (!small) {
             uint4* mv = reinterpret_cast<uint4*>(static_cast<uint16_t*>(t.m) + start);
             uint4* vv = reinterpret_cast<uint4*>(static_cast<uint16_t*>(t.v) + start);
-            const bool sr = kSR && !has_res;
-            // two independent 8-element groups per iteration: ten 128-bit loads in flight.  With
-            // stochastic rounding the two groups are the halves of one 16-element block, so one
-            // generator call serves both; otherwise they are kThreads vectors apart.
-            int64_t p = threadIdx.x;
-            for (; sr ? (2 * p + 1 < nv) : (p + kThreads < nv); p += sr ? kThreads : 2 * kThreads) {
-                const int64_t i = sr ? 2 * p : p, i1 = sr ? 2 * p + 1 : p + kThreads;
-                uint4 W0 = ld_stream(wv + i), W1 = ld_stream(wv + i1);
-                uint4 R0 = has_res ? ld_stream(rv + i) : make_uint4(0, 0, 0, 0);
-                uint4 R1 = has_res ? ld_stream(rv + i1) : make_uint4(0, 0, 0, 0);
-                uint4 G0 = ld_stream(gv + i), G1 = ld_stream(gv + i1);
-                uint4 M0 = ld_stream(mv + i), M1 = ld_stream(mv + i1);
-                uint4 V0 = ld_stream(vv + i), V1 = ld_stream(vv + i1);
-                uint32_t ra[4] = {0u, 0u, 0u, 0u}, rb[4] = {0u, 0u, 0u, 0u};
-                if (sr) sr_lanes16(k, c.tensor, start + 16 * p, ra, rb);
-                step8_u16<kSR>(k, cd, has_res, ra, W0, R0, G0, M0, V0, am, av, nf);
-                st_stream(wv + i, W0);
-                if (has_res) st_stream(rv + i, R0);
-                st_stream(mv + i, M0);
-                st_stream(vv + i, V0);
-                step8_u16<kSR>(k, cd, has_res, rb, W1, R1, G1, M1, V1, am, av, nf);
-                st_stream(wv + i1, W1);
-                if (has_res) st_stream(rv + i1, R1);
-                st_stream(mv + i1, M1);
-                st_stream(vv + i1, V1);
-            }
-            // remaining vectors one at a time
-            for (int64_t i = sr ? 2 * p : p; i < nv; i += kThreads) {
-                uint4 W0 = ld_stream(wv + i);
-                uint4 R0 = has_res ? ld_stream(rv + i) : make_uint4(0, 0, 0, 0);
-                uint4 G0 = ld_stream(gv + i), M0 = ld_stream(mv + i), V0 = ld_stream(vv + i);
-                uint32_t ra[4] = {0u, 0u, 0u, 0u};
-                if (sr) sr_lanes8(k, c.tensor, start + 8 * i, ra);
-                step8_u16<kSR>(k, cd, has_res, ra, W0, R0, G0, M0, V0, am, av, nf);
-                st_stream(wv + i, W0);
-                if (has_res) st_stream(rv + i, R0);
-                st_stream(mv + i, M0);
-                st_stream(vv + i, V0);
-            }
+            // exact-zero gradients in this chunk (seen by the pre-pass): the zero-guarded
+            // arithmetic, else the plain one (a branch taken by the whole CTA)
+            if (L.zero_chunk == nullptr || L.zero_chunk[blockIdx.x])
+                u16_vectors<kSR, true>(k, cd, has_res, c.tensor, start, nv, wv, rv, gv, mv, vv, am, av, nf);
+            else
+                u16_vectors<kSR, false>(k, cd, has_res, c.tensor, start, nv, wv, rv, gv, mv, vv, am, av, nf);
         } else {
             float4* mv = reinterpret_cast<float4*>(static_cast<float*>(t.m) + start);
             float4* vv = reinterpret_cast<float4*>(static_cast<float*>(t.v) + start);
@@ -364,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_nadam_step(NadamLaunch L, Prm k
             m = dec_m(static_cast<uint16_t*>(t.m)[i], cd.dec.qm);
             v = dec_v(static_cast<uint16_t*>(t.v)[i], cd.dec.qv);
         }
-        const float w1 = elem(k, w0, bf16_to_f32(g[i]), m, v, sv);
+        const float w1 = elem<true>(k, w0, bf16_to_f32(g[i]), m, v, sv);
         const uint32_t b = __float_as_uint(w1);
         const uint32_t hi = has_res ? (b >> 16) : (kSR ? sr_bf16(w1, sr_lane1(k, c.tensor, i)) : rne_bf16(w1));
         w[i] = (uint16_t)hi;
@@ -425,8 +462,8 @@ __device__ __forceinline__ void step8_f24(const Prm& k, bool has_res, uint32_t t
         const uint32_t lm = ml[j >> 1] >> (16 * (j & 1)), lv = vl[j >> 1] >> (16 * (j & 1));
         float m0 = f24_value(mh[j] & 0xFFFFu, lm & 0xFFu), m1 = f24_value(mh[j] >> 16, (lm >> 8) & 0xFFu);
         float v0 = f24_value(vh[j] & 0xFFFFu, lv & 0xFFu), v1 = f24_value(vh[j] >> 16, (lv >> 8) & 0xFFu);
-        w0 = elem(k, w0, __uint_as_float(g32[j] << 16), m0, v0, s0);
-        w1 = elem(k, w1, __uint_as_float(g32[j] & 0xFFFF0000u), m1, v1, s1);
+        w0 = elem<false>(k, w0, __uint_as_float(g32[j] << 16), m0, v0, s0);
+        w1 = elem<false>(k, w1, __uint_as_float(g32[j] & 0xFFFF0000u), m1, v1, s1);
         pack_w(w0, w1, has_res, sr, rnd[j], w32[j], r32[j]);
         nf = __vmaxu2(nf, w32[j] & 0x7FFF7FFFu);
         mb[2 * j] = __float_as_uint(m0);
@@ -491,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_nadam_f24(NadamLaunch L, Prm k)
         for (int64_t i = done + threadIdx.x; i < end; i += kThreads) {
             const float w0 = has_res ? __uint_as_float(((uint32_t)w[i] << 16) | res[i]) : bf16_to_f32(w[i]);
             float m = f24_value(mhi[i], mlo[i]), v = f24_value(vhi[i], vlo[i]), sv;
-            const float w1 = elem(k, w0, bf16_to_f32(g[i]), m, v, sv);
+            const float w1 = elem<true>(k, w0, bf16_to_f32(g[i]), m, v, sv);
             const uint32_t b = __float_as_uint(w1);
             const uint32_t hi = has_res ? (b >> 16) : (kSR ? sr_bf16(w1, sr_lane1(k, c.tensor, i)) : rne_bf16(w1));
             w[i] = (uint16_t)hi;
@@ -509,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_nadam_f24(NadamLaunch L, Prm k)
         for (int64_t i = start + threadIdx.x; i < end; i += kThreads) {
             const float w0 = has_res ? __uint_as_float(((uint32_t)w[i] << 16) | res[i]) : bf16_to_f32(w[i]);
             float m = mf[i], v = vf[i], sv;
-            const float w1 = elem(k, w0, bf16_to_f32(g[i]), m, v, sv);
+            const float w1 = elem<true>(k, w0, bf16_to_f32(g[i]), m, v, sv);
             const uint32_t b = __float_as_uint(w1);
             const uint32_t hi = has_res ? (b >> 16) : (kSR ? sr_bf16(w1, sr_lane1(k, c.tensor, i)) : rne_bf16(w1));
             w[i] = (uint16_t)hi;

@@ -122,6 +122,10 @@ def config(name: str):
     if name == "ragged20k":
         return dict(kind="nadam", groups=[[(n,) for n in ragged_sizes(20000, 0)]], hp=dict(NADAM_HP),
                     steps=5, g_std=1e-3, zero_frac=0.01, seed=0)
+    if name == "ragged1k":   # the first 1,000 tensors of ragged20k (~0.4e9 parameters): its profiling case
+        c = config("ragged20k")
+        c["groups"] = [c["groups"][0][:1000]]
+        return c
     if name == "sdxl_like":
         # ten optimizer groups: the group count the SDXL optimizer-groups option recommends (4-10)
         shapes = sdxl_like_shapes()
