@@ -184,8 +184,9 @@ int optim_step_factored(optim_group_t* group, const void* const* grads_bf16, int
  * loads it, until the process exits.  The caller passes the tensor (weights, optional residual,
  * factored state, as in optim_tensor_desc_t for FACTORED groups) and its bf16 gradient; results
  * are identical to a FACTORED group holding just this tensor.  `step` is the caller's own
- * counter (>= 1; no sequence check).  A tensor whose scratch would exceed the array (about
- * 2^26 elements for a matrix) is rejected with OPTIM_EINVAL and a message giving both sizes.
+ * counter (>= 1; no sequence check).  A tensor whose scratch would exceed the array (about 3/64
+ * byte per element of a matrix: some 7e8 elements) is rejected with OPTIM_EINVAL and a message
+ * giving both sizes.
  * The first call on a device looks up the array's device address (once per device); make that
  * first call outside any stream capture.  All calls share the array and it keeps the previous
  * call's contents (the call clears the parts that must start at zero), so calls whose work
