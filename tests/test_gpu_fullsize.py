@@ -202,3 +202,42 @@ def test_flux35_offload_full(orc, eng):
     off.close()
     del groups
     torch.cuda.empty_cache()
+
+
+def test_tensor_beyond_2_31_elements(orc, eng):
+    """One tensor of 2^31 + 13 elements (64-bit element offsets, 131,073 chunks), one NAdamW
+    step: sampled elements -- chunk edges, both sides of 2^31, the last one, random ones -- equal
+    the oracle's step of the same element, given the tensor's max|g| computed on the host."""
+    n = (1 << 31) + 13
+    hp = dict(W.NADAM_HP, weight_decay=0.01, wd_mode=1)
+    master = W.master_weights((n,), 3, 0, device="cuda")
+    grp = eng.NadamGroup.from_masters([master])
+    rng = np.random.default_rng(0)
+    idx = np.unique(np.concatenate([[0, 1, 7, 8, 16383, 16384, (1 << 31) - 1, 1 << 31, (1 << 31) + 5, n - 1],
+                                    rng.integers(0, n, 200)]))
+    it = torch.from_numpy(idx).cuda()
+    x = master[it].cpu().numpy()
+    del master
+    torch.cuda.empty_cache()
+    g = W.grad_bf16((n,), 3, 0, 1, 1e-4, device="cuda")
+    gmax = 0
+    for c in range(0, n, 1 << 28):          # max |g| on the host, in pieces
+        part = W.bits16(g[c:c + (1 << 28)]) & 0x7FFF
+        gmax = max(gmax, int(part.max()))
+    G = float(np.array([gmax << 16], np.uint32).view(np.float32)[0])
+    gs = W.bits16(g[it])
+    grp.step([g], hp)
+    torch.cuda.synchronize()
+    got = {name: W.bits16(t[it]) for name, t in (("hi", grp.weights[0]), ("lo", grp.res[0]), ("m", grp.m[0]), ("v", grp.v[0]))}
+    k, _ = orc.nadam_scalars(1, hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"], True, True,
+                             hp["momentum_decay"], 1.0)
+    for j in range(idx.size):
+        hi, lo = orc.kahan_split(x[j:j + 1])
+        m, v = np.full(1, 32768, np.uint16), np.zeros(1, np.uint16)
+        sc = orc.Scale()
+        orc.nadam_step_slice(hi, lo, m, v, gs[j:j + 1], False, G, sc, k)
+        for name, want in (("hi", hi), ("lo", lo), ("m", m), ("v", v)):
+            assert got[name][j] == want[0], f"element {idx[j]}: {name} {got[name][j]} != {want[0]}"
+    grp.close()
+    del g, grp
+    torch.cuda.empty_cache()
