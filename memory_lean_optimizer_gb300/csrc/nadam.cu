@@ -279,15 +279,16 @@ __device__ __forceinline__ void step8_f32(const Prm& k, bool has_res, uint32_t t
 // The u16-state 128-bit path of one chunk (nv vectors of 8 elements starting at element `start`).
 template <bool kSR, bool kGuard>
 __device__ __forceinline__ void u16_vectors(const Prm& k, const Codec& cd, bool has_res, uint32_t tensor, int64_t start,
-                                            int64_t nv, uint4* wv, uint4* rv, const uint4* gv, uint4* mv, uint4* vv,
+                                            int nv, uint4* wv, uint4* rv, const uint4* gv, uint4* mv, uint4* vv,
                                             float& am, float& av, uint32_t& nf) {
+    // nv <= kChunk / 8: 32-bit vector indices within the chunk
     const bool sr = kSR && !has_res;
     // two independent 8-element groups per iteration: ten 128-bit loads in flight.  With
     // stochastic rounding the two groups are the halves of one 16-element block, so one
     // generator call serves both; otherwise they are kThreads vectors apart.
-    int64_t p = threadIdx.x;
+    int p = threadIdx.x;
     for (; sr ? (2 * p + 1 < nv) : (p + kThreads < nv); p += sr ? kThreads : 2 * kThreads) {
-        const int64_t i = sr ? 2 * p : p, i1 = sr ? 2 * p + 1 : p + kThreads;
+        const int i = sr ? 2 * p : p, i1 = sr ? 2 * p + 1 : p + kThreads;
         uint4 W0 = ld_stream(wv + i), W1 = ld_stream(wv + i1);
         uint4 R0 = has_res ? ld_stream(rv + i) : make_uint4(0, 0, 0, 0);
         uint4 R1 = has_res ? ld_stream(rv + i1) : make_uint4(0, 0, 0, 0);
@@ -295,7 +296,7 @@ __device__ __forceinline__ void u16_vectors(const Prm& k, const Codec& cd, bool 
         uint4 M0 = ld_stream(mv + i), M1 = ld_stream(mv + i1);
         uint4 V0 = ld_stream(vv + i), V1 = ld_stream(vv + i1);
         uint32_t ra[4] = {0u, 0u, 0u, 0u}, rb[4] = {0u, 0u, 0u, 0u};
-        if (sr) sr_lanes16(k, tensor, start + 16 * p, ra, rb);
+        if (sr) sr_lanes16(k, tensor, start + 16 * (int64_t)p, ra, rb);
         step8_u16<kSR, kGuard>(k, cd, has_res, ra, W0, R0, G0, M0, V0, am, av, nf);
         st_stream(wv + i, W0);
         if (has_res) st_stream(rv + i, R0);
@@ -308,12 +309,12 @@ __device__ __forceinline__ void u16_vectors(const Prm& k, const Codec& cd, bool 
         st_stream(vv + i1, V1);
     }
     // remaining vectors one at a time
-    for (int64_t i = sr ? 2 * p : p; i < nv; i += kThreads) {
+    for (int i = sr ? 2 * p : p; i < nv; i += kThreads) {
         uint4 W0 = ld_stream(wv + i);
         uint4 R0 = has_res ? ld_stream(rv + i) : make_uint4(0, 0, 0, 0);
         uint4 G0 = ld_stream(gv + i), M0 = ld_stream(mv + i), V0 = ld_stream(vv + i);
         uint32_t ra[4] = {0u, 0u, 0u, 0u};
-        if (sr) sr_lanes8(k, tensor, start + 8 * i, ra);
+        if (sr) sr_lanes8(k, tensor, start + 8 * (int64_t)i, ra);
         step8_u16<kSR, kGuard>(k, cd, has_res, ra, W0, R0, G0, M0, V0, am, av, nf);
         st_stream(wv + i, W0);
         if (has_res) st_stream(rv + i, R0);
@@ -367,9 +368,9 @@ __global__ void __launch_bounds__(kThreads, 4) k_nadam_step(NadamLaunch L, Prm k
             // exact-zero gradients in this chunk (seen by the pre-pass): the zero-guarded
             // arithmetic, else the plain one (a branch taken by the whole CTA)
             if (L.zero_chunk == nullptr || L.zero_chunk[blockIdx.x])
-                u16_vectors<kSR, true>(k, cd, has_res, c.tensor, start, nv, wv, rv, gv, mv, vv, am, av, nf);
+                u16_vectors<kSR, true>(k, cd, has_res, c.tensor, start, (int)nv, wv, rv, gv, mv, vv, am, av, nf);
             else
-                u16_vectors<kSR, false>(k, cd, has_res, c.tensor, start, nv, wv, rv, gv, mv, vv, am, av, nf);
+                u16_vectors<kSR, false>(k, cd, has_res, c.tensor, start, (int)nv, wv, rv, gv, mv, vv, am, av, nf);
         } else {
             float4* mv = reinterpret_cast<float4*>(static_cast<float*>(t.m) + start);
             float4* vv = reinterpret_cast<float4*>(static_cast<float*>(t.v) + start);
