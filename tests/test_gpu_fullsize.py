@@ -1,5 +1,5 @@
 """Parity at full workload sizes, in the launch configuration the benchmark times (one library
-group per Flux-like block, 16 tensors per factored group, one group of 20,000 ragged tensors, the
+group per Flux-like block, the ten SDXL-like factored groups, one group of 20,000 ragged tensors, the
 35-group host-offload pipeline).  The oracle replays whole sampled tensors -- their inputs are
 copied back from the device before each step -- and the remaining tensors are checked through
 properties that hold at any size (finite results, scale records bounding their maxima)."""
