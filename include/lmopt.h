@@ -169,10 +169,10 @@ int optim_step_nadam_end(optim_group_t* group, const float* exchange, void* stre
  * row and column EMAs of g^2 over the last two dims, rank-1 reconstruction
  * V_ij = R_i C_j / mean(R), update u = g / sqrt(V), RMS clipping, decoupled decay, Kahan split.
  * 1-D tensors keep a full second moment.  Arguments as optim_step_nadam_kahan.  A group larger
- * than one wave (96 MiB of gradients) is processed wave by wave, with consecutive waves on two
- * streams: `stream` and a stream owned by the group, which waits for the work already on `stream`
- * and which `stream` waits for before any later work -- to the caller the call is ordered on
- * `stream` as usual. */
+ * than one wave (96 MiB of gradients) is processed wave by wave, with consecutive waves on up to
+ * three streams: `stream` and two streams owned by the group, which wait for the work already on
+ * `stream` and which `stream` waits for before any later work -- to the caller the call is
+ * ordered on `stream` as usual. */
 int optim_step_factored(optim_group_t* group, const void* const* grads_bf16, int64_t step,
                         const optim_factored_hparams_t* hp, void* stream);
 

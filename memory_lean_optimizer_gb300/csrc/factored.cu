@@ -49,7 +49,7 @@ constexpr int kVecPerCta = kThreads * 8;
 #define LMOPT_WAVE_MB 96
 #endif
 #ifndef LMOPT_WAVE_STREAMS
-#define LMOPT_WAVE_STREAMS 2
+#define LMOPT_WAVE_STREAMS 3
 #endif
 constexpr int64_t kWaveGradBytes = (int64_t)LMOPT_WAVE_MB << 20;
 constexpr int kWaveStreams = LMOPT_WAVE_STREAMS;
