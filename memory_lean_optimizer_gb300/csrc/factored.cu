@@ -180,7 +180,8 @@ __device__ __forceinline__ void apply_elem(uint32_t& hi, uint32_t& lo, bool has_
 // Clip divisor from the tensor's fp32 sum of squares.
 __device__ __forceinline__ float clip_den(float ss, int64_t n, float clip) {
     const float ms = __fdiv_rn(ss, (float)n);
-    return fmaxf(1.0f, __fdiv_rn(__fsqrt_rn(ms), clip));
+    const float r = __fdiv_rn(__fsqrt_rn(ms), clip);
+    return r < 1.0f ? 1.0f : r;   // a NaN RMS stays NaN (clamp(min=1) semantics), as in the oracle
 }
 
 // Writes this CTA's partial; the last CTA of the tensor sums all partials (fixed order) and

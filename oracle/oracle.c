@@ -619,12 +619,15 @@ static void apply_update(uint16_t* hi, uint16_t* lo, int64_t i, float u, float d
     }
 }
 
+/* max(1, RMS/clip) as the listing's clamp(min=1) computes it: a NaN RMS (an undefined update)
+ * stays NaN and makes the whole update NaN, rather than being replaced by 1. */
 static float clip_divisor(double ss, int64_t n, float clip)
 {
     float ss32 = (float)ss;
     float ms = ss32 / (float)n;
     float rms = sqrtf(ms);
-    return fmaxf(1.0f, rms / clip);
+    float r = rms / clip;
+    return (r < 1.0f) ? 1.0f : r;
 }
 
 /* Factored tensor viewed as B matrices of R rows x C columns (the last two dims), row-major.
@@ -703,6 +706,7 @@ float orc_factored_step_tensor(uint16_t* hi, uint16_t* lo, const uint16_t* g, in
 float orc_factored_step_vector(uint16_t* hi, uint16_t* lo, const uint16_t* g, int64_t n,
                                float* V, const orc_factored_scalars_t* k)
 {
+    if (n == 0) return 1.0f;   /* no elements: nothing to update (as for matrices) */
     double ss = 0.0;
     for (int64_t i = 0; i < n; ++i) {
         float gg = bf16_to_f32(g[i]);

@@ -229,3 +229,25 @@ def test_misaligned_buffers_and_empty_tensors(orc, eng):
                 assert np.all(np.abs(gv - ot["V"]) <= 2e-6 * np.abs(ot["V"]) + 1e-37), f"tensor {i}: V differs"
     finally:
         lmopt.optim_group_destroy(h)
+
+
+def test_zero_row_with_eps1_zero_is_nan_like_the_oracle(orc, eng):
+    """eps1 = 0 and an all-zero gradient row (a wide matrix, and one row of one 3x3 matrix): the
+    row's factor is infinite, 0 * inf is NaN, and the clip's clamp keeps the NaN RMS, so every
+    weight of both tensors is NaN -- in the oracle and in the kernels alike."""
+    shapes = [(40, 64), (4, 2, 3, 3)]
+    hp = dict(HP, eps1=0.0)
+    masters = [W.master_weights(s, 11, i) for i, s in enumerate(shapes)]
+    ora = OracleFactored(orc, [m.numpy() for m in masters], shapes)
+    grp = eng.FactoredGroup.from_masters([m.cuda() for m in masters])
+    grads = [W.grad_bf16(s, 11, i, 1, 1e-3) for i, s in enumerate(shapes)]
+    grads[0][5, :] = 0
+    grads[1][2, 1, 0, :] = 0
+    ora.step([W.bits16(g).reshape(-1) for g in grads], hp)
+    grp.step([g.cuda() for g in grads], hp)
+    torch.cuda.synchronize()
+    for i, got in enumerate(grp.masters()):
+        ref = orc.kahan_merge(ora.t[i]["hi"], ora.t[i]["lo"])
+        assert np.isnan(ref).all(), f"tensor {i}: the oracle should report NaN"
+        assert np.isnan(got.cpu().numpy()).all(), f"tensor {i}: the kernels should report NaN"
+    grp.close()

@@ -167,3 +167,21 @@ def test_empty_tensor_leaves_state(orc, shape):
             assert np.all(empty[name] == 0.5)
     assert dens[0] == 1.0
     assert np.array_equal(t_group["hi"], t_alone["hi"]) and np.array_equal(t_group["lo"], t_alone["lo"])
+
+
+def test_zero_row_with_eps1_zero_is_flagged(orc):
+    """eps1 = 0 and an all-zero gradient row: that row's R is 0, its factor rsqrt(0) is infinite
+    and 0 * inf is NaN, so the row's update -- and through the RMS clip, whose clamp(min=1) keeps
+    a NaN, the whole tensor -- is NaN.  The oracle reports this (non-finite weights) instead of
+    hiding it; with eps1 > 0 the same gradient gives finite weights and leaves the zero row's
+    weights unchanged."""
+    rng = np.random.default_rng(27)
+    shape = (8, 12)
+    w0 = (rng.standard_normal(shape) * 0.02).astype(np.float32)
+    g = rng.standard_normal(shape).astype(np.float32)
+    g[3, :] = 0.0
+    gb = bf16_bits(g)
+    w_nan, _, _ = run(orc, shape, w0, [gb], dict(HP, eps1=0.0))
+    assert np.isnan(w_nan[3]).all() and np.isnan(w_nan).all()
+    w_ok, _, _ = run(orc, shape, w0, [gb], dict(HP, eps1=1e-30))
+    assert np.isfinite(w_ok).all() and np.array_equal(w_ok[3], w0[3])
