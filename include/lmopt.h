@@ -235,7 +235,9 @@ int optim_set_scales(optim_group_t* group, const float* host_in);
 int optim_group_get_step(optim_group_t* group, int64_t* step, double* mu_product);
 int optim_group_set_step(optim_group_t* group, int64_t step, double mu_product);
 /* Non-finite detection: the number of (step, chunk) pairs in which an updated weight came out
- * NaN or infinite, summed over all steps so far (a chunk is up to 16384 elements of one tensor). */
+ * NaN or infinite, summed over all steps so far (a chunk is up to 16384 elements of one tensor;
+ * in FACTORED groups, one unit of the update kernel: a 128x256 tile, up to 2048 small matrices,
+ * or up to 2048 elements of a 1-D tensor). */
 int optim_query_nonfinite(optim_group_t* group, uint64_t* count);
 
 /* ---- pinned-host offload of the states between steps --------------------------------------

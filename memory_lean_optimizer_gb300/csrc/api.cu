@@ -424,7 +424,7 @@ int optim_step_factored(optim_group_t* g, const void* const* grads, int64_t step
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     rc = upload_grads(g, grads, s);
     if (rc) return rc;
-    rc = launch_factored_step(g->fplan, g->d_grads, k, s, g->profile_ev);
+    rc = launch_factored_step(g->fplan, g->d_grads, k, s, g->profile_ev, g->d_nonfinite);
     if (rc) return rc;
     g->last_step = step;
     g->last_stream = s;

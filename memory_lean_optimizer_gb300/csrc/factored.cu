@@ -96,6 +96,7 @@ struct Dev {
     float* den;
     unsigned* counter;  // per tensor (sum of squares)
     unsigned* rcounter; // per matrix (mean of R)
+    unsigned long long* nonfinite;   // CTAs of the update that stored a non-finite weight (or null)
 };
 
 struct K {
@@ -154,6 +155,18 @@ __device__ float block_sum(float x, float* sm /* 32 floats */) {
     float y = lane < (int)(blockDim.x >> 5) ? sm[lane] : 0.f;
     y = warp_sum_f32(y);
     return y;
+}
+
+// Counts this CTA once if any of its threads stored a non-finite weight (nf: the largest bf16
+// magnitude a thread stored; 0x7F80 and above is infinity or NaN).  Every thread of the CTA calls
+// it once (a barrier).
+__device__ __forceinline__ void count_nonfinite(const Dev& D, uint32_t nf) {
+    const int any = __syncthreads_or(nf >= 0x7F80u);
+    if (any && threadIdx.x == 0 && D.nonfinite) atomicAdd(D.nonfinite, 1ull);
+}
+__device__ __forceinline__ uint32_t max_bf16_mag(uint32_t nf, const uint4& W) {
+    uint32_t x = __vmaxu2(__vmaxu2(W.x & 0x7FFF7FFFu, W.y & 0x7FFF7FFFu), __vmaxu2(W.z & 0x7FFF7FFFu, W.w & 0x7FFF7FFFu));
+    return max(nf, max(x & 0xFFFFu, x >> 16));
 }
 
 // Per-tensor update scale: lr when the update is not clipped (den == 1), else fl(lr / den).  The
@@ -428,11 +441,12 @@ __device__ __forceinline__ float conv3_stats(const uint16_t* g, float* row, floa
 }
 
 template <bool kRes, bool kDecay>
-__device__ __forceinline__ void conv3_apply(const uint16_t* g, uint16_t* w, uint16_t* res, const float* row,
+__device__ __forceinline__ uint32_t conv3_apply(const uint16_t* g, uint16_t* w, uint16_t* res, const float* row,
                                             const float* col, int64_t m_first, int nsub, unsigned char* smem, float us,
                                             float nwdlr) {
     constexpr int kBuf = 3 * kTinyWords * 2 + kTinyStats * 4;
     const int tid = threadIdx.x;
+    uint32_t nf = 0u;
     auto plane = [&](int b, int a) { return reinterpret_cast<uint4*>(smem + b * kBuf + a * (kTinyWords * 2)); };
     auto issue = [&](int kk) {
         const int64_t m = m_first + (int64_t)kk * kTinySub;
@@ -470,11 +484,18 @@ __device__ __forceinline__ void conv3_apply(const uint16_t* g, uint16_t* w, uint
         for (int a = 1; a < (kRes ? 3 : 2); ++a) {
             uint16_t* base = a == 1 ? w : res;   // a == 2 only with a residual
             uint4* dst = reinterpret_cast<uint4*>(base + m * 9);
-            st_stream(dst + tid, plane(b, a)[tid]);
-            if (tid < k3Words - kTinySub) st_stream(dst + kTinySub + tid, plane(b, a)[kTinySub + tid]);
+            const uint4 x0 = plane(b, a)[tid];
+            st_stream(dst + tid, x0);
+            if (a == 1) nf = max_bf16_mag(nf, x0);
+            if (tid < k3Words - kTinySub) {
+                const uint4 x1 = plane(b, a)[kTinySub + tid];
+                st_stream(dst + kTinySub + tid, x1);
+                if (a == 1) nf = max_bf16_mag(nf, x1);
+            }
         }
         __syncthreads();
     }
+    return nf;
 }
 
 // Statistics of one staged small matrix, out of line (the ragged / unaligned staging path).
@@ -900,6 +921,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
     const FTensor t = D.tensors[it.tensor];
     const uint16_t* __restrict__ g = D.grads[it.tensor];
     const bool has_res = t.res != nullptr;
+    uint32_t nf = 0u;   // largest bf16 magnitude this thread stored (non-finite detection)
 
     if (it.cls == kWide) {
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -952,10 +974,12 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
                 const int64_t offA = (b * t.R + rowA) * t.C + col0, offB = offA + 8 * t.C;
                 if (kk > 0) load_pair(kk);
                 apply8x2(GA, WA, RA, rrA, cc2, has_res, decay, nwd2, ns2);
+                nf = max_bf16_mag(nf, WA);
                 st_stream(reinterpret_cast<uint4*>(t.w + offA), WA);
                 if (has_res) st_stream(reinterpret_cast<uint4*>(t.res + offA), RA);
                 if (hasB) {
                     apply8x2(GB, WB, RB, rrB, cc2, has_res, decay, nwd2, ns2);
+                    nf = max_bf16_mag(nf, WB);
                     st_stream(reinterpret_cast<uint4*>(t.w + offB), WB);
                     if (has_res) st_stream(reinterpret_cast<uint4*>(t.res + offB), RB);
                 }
@@ -976,11 +1000,13 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
                     uint32_t hi = t.w[off + j], lo = has_res ? t.res[off + j] : 0u;
                     const float u = __fmul_rn(__fmul_rn(rr, ccv[j]), bf16_to_f32(g[off + j]));
                     apply_elem(hi, lo, has_res, u, us, k);
+                    nf = max(nf, hi & 0x7FFFu);
                     t.w[off + j] = (uint16_t)hi;
                     if (has_res) t.res[off + j] = (uint16_t)lo;
                 }
             }
         }
+        count_nonfinite(D, nf);
         return;
     }
     pdl_sync();
@@ -1008,12 +1034,13 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
         const int nsub = (int)((nmat + sub - 1) / sub);
         if (pipe && r == 3 && c == 3) {
             if (has_res) {
-                if (k.nwdlr != 0.0f) conv3_apply<true, true>(g, t.w, t.res, t.row, t.col, it.x, nsub, smem, us, k.nwdlr);
-                else conv3_apply<true, false>(g, t.w, t.res, t.row, t.col, it.x, nsub, smem, us, k.nwdlr);
+                if (k.nwdlr != 0.0f) nf = conv3_apply<true, true>(g, t.w, t.res, t.row, t.col, it.x, nsub, smem, us, k.nwdlr);
+                else nf = conv3_apply<true, false>(g, t.w, t.res, t.row, t.col, it.x, nsub, smem, us, k.nwdlr);
             } else {
-                if (k.nwdlr != 0.0f) conv3_apply<false, true>(g, t.w, t.res, t.row, t.col, it.x, nsub, smem, us, k.nwdlr);
-                else conv3_apply<false, false>(g, t.w, t.res, t.row, t.col, it.x, nsub, smem, us, k.nwdlr);
+                if (k.nwdlr != 0.0f) nf = conv3_apply<false, true>(g, t.w, t.res, t.row, t.col, it.x, nsub, smem, us, k.nwdlr);
+                else nf = conv3_apply<false, false>(g, t.w, t.res, t.row, t.col, it.x, nsub, smem, us, k.nwdlr);
             }
+            count_nonfinite(D, nf);
             return;
         }
         auto compute = [&](int b, int nm) {
@@ -1036,6 +1063,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
                 }
             } else
                 tiny_apply_any(sw[b] + i * rc, sr[b] + i * rc, sg[b] + i * rc, sR + i * r, sC + i * c, r, c, has_res, us, k);
+            for (int e = 0; e < rc; ++e) nf = max(nf, (uint32_t)(sw[b][i * rc + e] & 0x7FFFu));
         };
         if (pipe) {
             auto issue = [&](int kk) {
@@ -1082,6 +1110,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
                 __syncthreads();
             }
         }
+        count_nonfinite(D, nf);
         return;
     }
     const int64_t e0 = (int64_t)it.x * kVecPerCta;
@@ -1090,9 +1119,11 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
         uint32_t hi = t.w[e], lo = has_res ? t.res[e] : 0u;
         const float u = __fmul_rn(rsqrt_rn(t.col[e]), bf16_to_f32(g[e]));
         apply_elem(hi, lo, has_res, u, us, k);
+        nf = max(nf, hi & 0x7FFFu);
         t.w[e] = (uint16_t)hi;
         if (has_res) t.res[e] = (uint16_t)lo;
     }
+    count_nonfinite(D, nf);
 }
 
 }  // namespace
@@ -1298,10 +1329,11 @@ static cudaError_t launch_pdl(Kern kern, int grid, cudaStream_t st, Args... args
 }
 
 int launch_factored_step(const FactoredPlan* p, const uint16_t* const* d_grads, const FactoredScalars& s,
-                         cudaStream_t stream, cudaEvent_t mid) {
+                         cudaStream_t stream, cudaEvent_t mid, unsigned long long* nonfinite) {
     K k{s.b2t, s.alpha, s.eps1, s.eps2, s.clip, s.lr_eff, s.nwdlr, s.mode};
     Dev D = p->dev;
     D.grads = d_grads;
+    D.nonfinite = nonfinite;
     const int ns = 1 + p->n_aux;   // streams in use: wave w runs on stream w % ns (0 = caller's)
     int rc = OPTIM_OK;
     if (ns > 1) {
@@ -1469,5 +1501,5 @@ extern "C" int optim_step_factored_noalloc(const optim_tensor_desc_t* tensor, co
     D.ss = reinterpret_cast<float*>(sb + o_ss);
     D.den = reinterpret_cast<float*>(sb + o_den);
     D.counter = reinterpret_cast<unsigned*>(sb + o_counter);
-    return launch_factored_step(&plan, reinterpret_cast<const uint16_t* const*>(sb + o_grad), k, s, nullptr);
+    return launch_factored_step(&plan, reinterpret_cast<const uint16_t* const*>(sb + o_grad), k, s, nullptr, nullptr);
 }

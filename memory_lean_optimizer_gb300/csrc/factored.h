@@ -16,7 +16,8 @@ struct FactoredScalars {
 struct FactoredPlan;
 int factored_plan_build(FactoredPlan*& plan, const std::vector<optim_tensor_desc_t>& desc);
 void factored_plan_free(FactoredPlan*& plan);
+// `nonfinite` (may be null): counter of update CTAs that stored a non-finite weight.
 int launch_factored_step(const FactoredPlan* plan, const uint16_t* const* d_grads,
-                         const FactoredScalars& k, cudaStream_t s, cudaEvent_t mid);
+                         const FactoredScalars& k, cudaStream_t s, cudaEvent_t mid, unsigned long long* nonfinite);
 
 }  // namespace lmo

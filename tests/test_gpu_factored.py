@@ -96,6 +96,8 @@ def run_parity(orc, eng, shapes, steps, hp, seed=0, g_std=1e-3, kahan=True, scal
         grp.step([g.cuda() for g in grads], hp)
     torch.cuda.synchronize()
     compare(ora, grp, hp, steps, kahan=kahan)
+    from memory_lean_optimizer_gb300 import lmopt
+    assert lmopt.optim_query_nonfinite(grp.handle) == 0
     return ora, grp
 
 
@@ -250,4 +252,7 @@ def test_zero_row_with_eps1_zero_is_nan_like_the_oracle(orc, eng):
         ref = orc.kahan_merge(ora.t[i]["hi"], ora.t[i]["lo"])
         assert np.isnan(ref).all(), f"tensor {i}: the oracle should report NaN"
         assert np.isnan(got.cpu().numpy()).all(), f"tensor {i}: the kernels should report NaN"
+    from memory_lean_optimizer_gb300 import lmopt
+    # the wide matrix's 1 tile and the small-matrix tensor's 1 block stored non-finite weights
+    assert lmopt.optim_query_nonfinite(grp.handle) == 2
     grp.close()
