@@ -78,9 +78,10 @@ typedef struct {
 /* Group kinds.  NADAM_F24 is NADAM with f24 moment storage: the upper three bytes of each fp32
  * moment ("f24 is the upper three bytes [of f32] - i.e. with 8 more bits of mantissa", "Amazing
  * Flux FFT quality on a 5090", sd-scripts PR #2187, third post), truncated.  Its m and v buffers
- * (numel > 4096) hold 3*numel bytes: numel uint16 upper words, then numel bytes of bits 8..15;
- * 16-byte aligned planes (numel a multiple of 8) take the 128-bit path.  No scale records and no
- * gradient pre-pass are involved; tensors of 4096 or fewer elements keep fp32 moments. */
+ * (numel > 4096) hold L + numel bytes, L = 2*numel rounded up to a multiple of 16: numel uint16
+ * upper words, padding up to byte L, then numel bytes of bits 8..15.  Buffers that start on a
+ * 16-byte boundary take the 128-bit path whatever numel is.  No scale records and no gradient
+ * pre-pass are involved; tensors of 4096 or fewer elements keep fp32 moments. */
 enum { OPTIM_KIND_NADAM = 0, OPTIM_KIND_FACTORED = 1, OPTIM_KIND_NADAM_F24 = 2, OPTIM_KIND_ADAN = 3 };
 /* ADAN groups: m -> fp32 [3*numel] (planes m, v, n), v -> uint16 [numel] (previous bf16 gradient),
  * all zero at creation. */

@@ -436,6 +436,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_nadam_step(NadamLaunch L, Prm k
 // sd-scripts PR #2187, third post), stored as a plane of n upper 16-bit words followed by a
 // plane of n bytes (bits 8..15).  Storage only: the update runs on the decoded fp32 values, and
 // no scale (hence no gradient pre-pass) is needed.  22 bytes per element per step.
+__device__ __forceinline__ int64_t f24_lo_offset(int64_t n) { return (2 * n + 15) & ~(int64_t)15; }
 __device__ __forceinline__ float f24_value(uint32_t hi16, uint32_t lo8) { return __uint_as_float((hi16 << 16) | (lo8 << 8)); }
 
 // Bits 8..15 of four fp32 patterns, packed into one word (element 0 in the low byte).
@@ -463,8 +464,8 @@ __device__ __forceinline__ void step8_f24(const Prm& k, bool has_res, uint32_t t
         const uint32_t lm = ml[j >> 1] >> (16 * (j & 1)), lv = vl[j >> 1] >> (16 * (j & 1));
         float m0 = f24_value(mh[j] & 0xFFFFu, lm & 0xFFu), m1 = f24_value(mh[j] >> 16, (lm >> 8) & 0xFFu);
         float v0 = f24_value(vh[j] & 0xFFFFu, lv & 0xFFu), v1 = f24_value(vh[j] >> 16, (lv >> 8) & 0xFFu);
-        w0 = elem<false>(k, w0, __uint_as_float(g32[j] << 16), m0, v0, s0);
-        w1 = elem<false>(k, w1, __uint_as_float(g32[j] & 0xFFFF0000u), m1, v1, s1);
+        w0 = elem<true>(k, w0, __uint_as_float(g32[j] << 16), m0, v0, s0);
+        w1 = elem<true>(k, w1, __uint_as_float(g32[j] & 0xFFFF0000u), m1, v1, s1);
         pack_w(w0, w1, has_res, sr, rnd[j], w32[j], r32[j]);
         nf = __vmaxu2(nf, w32[j] & 0x7FFF7FFFu);
         mb[2 * j] = __float_as_uint(m0);
@@ -498,8 +499,10 @@ __global__ void __launch_bounds__(kThreads, 4) k_nadam_f24(NadamLaunch L, Prm k)
     if (!small) {
         uint16_t* mhi = static_cast<uint16_t*>(t.m);
         uint16_t* vhi = static_cast<uint16_t*>(t.v);
-        uint8_t* mlo = reinterpret_cast<uint8_t*>(mhi + n);
-        uint8_t* vlo = reinterpret_cast<uint8_t*>(vhi + n);
+        // The byte plane starts at 2n rounded up to 16 bytes, so that every tensor's planes are
+        // 16-byte aligned together and ragged sizes keep the 128-bit path.
+        uint8_t* mlo = static_cast<uint8_t*>(t.m) + f24_lo_offset(n);
+        uint8_t* vlo = static_cast<uint8_t*>(t.v) + f24_lo_offset(n);
         const bool vec = aligned16(w) && (!has_res || aligned16(res)) && aligned16(g) && aligned16(mhi) &&
                          aligned16(vhi) && ((reinterpret_cast<uintptr_t>(mlo) | reinterpret_cast<uintptr_t>(vlo)) & 7u) == 0u;
         if (vec) {

@@ -171,9 +171,10 @@ class NadamGroup(_Group):
             if n <= SMALL:
                 self.m.append(_state_buffer(n, torch.float32, dev, pinned))
                 self.v.append(_state_buffer(n, torch.float32, dev, pinned))
-            elif states == "f24":       # n upper 16-bit words, then n low bytes, all zero
-                self.m.append(torch.zeros(3 * n, dtype=torch.uint8, device=dev))
-                self.v.append(torch.zeros(3 * n, dtype=torch.uint8, device=dev))
+            elif states == "f24":       # n upper 16-bit words, padding to 16 B, n low bytes, all zero
+                nbytes = (2 * n + 15) // 16 * 16 + n
+                self.m.append(torch.zeros(nbytes, dtype=torch.uint8, device=dev))
+                self.v.append(torch.zeros(nbytes, dtype=torch.uint8, device=dev))
             else:
                 self.m.append(_state_buffer(n, torch.int16, dev, pinned, 32768))
                 self.v.append(_state_buffer(n, torch.int16, dev, pinned, 0))

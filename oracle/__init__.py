@@ -235,8 +235,8 @@ def nadam_step_tensor(hi, lo, m, v, g, scale: Scale, k: NadamScalars):
 
 
 def nadam_step_tensor_f24(hi, lo, m, v, g, k: NadamScalars, sr=False, seed=0, tensor=0, step=0):
-    """f24 moments: m, v are uint8 buffers of 3n bytes (n uint16 upper words, then n low bytes),
-    or float32 arrays when n <= 4096.  sr (lo None): stochastic rounding of the weight."""
+    """f24 moments: m, v are uint8 buffers of f24_nbytes(n) bytes (n uint16 upper words, zero
+    padding to byte f24_lo_offset(n), then n low bytes), or float32 arrays when n <= 4096.  sr (lo None): stochastic rounding of the weight."""
     _load().orc_nadam_step_tensor_f24(_p(hi), _p(lo), _p(m), _p(v), _p(_u16(g)), hi.size, ctypes.byref(k),
                                       int(sr), seed, tensor, step)
 
@@ -277,19 +277,29 @@ def adan_step_tensor(hi, lo, mnv, gprev, g, step, k: AdanScalars, sr=False, seed
                                  ctypes.byref(k), int(sr), seed, tensor)
 
 
+def f24_lo_offset(n: int) -> int:
+    """Byte offset of the bits-8..15 plane in an f24 buffer: 2n rounded up to 16."""
+    return (2 * n + 15) // 16 * 16
+
+
+def f24_nbytes(n: int) -> int:
+    return f24_lo_offset(n) + n
+
+
 def f24_split(x: np.ndarray) -> np.ndarray:
-    """fp32 values -> 3n-byte f24 buffer (upper 16 bits plane, then bits 8..15 plane)."""
+    """fp32 values -> f24 buffer (upper 16 bits plane, zero padding, then bits 8..15 plane)."""
     b = np.ascontiguousarray(x, np.float32).view(np.uint32).reshape(-1)
-    out = np.empty(3 * b.size, np.uint8)
-    out[:2 * b.size].view(np.uint16)[:] = (b >> 16).astype(np.uint16)
-    out[2 * b.size:] = ((b >> 8) & 0xFF).astype(np.uint8)
+    n = b.size
+    out = np.zeros(f24_nbytes(n), np.uint8)
+    out[:2 * n].view(np.uint16)[:] = (b >> 16).astype(np.uint16)
+    out[f24_lo_offset(n):] = ((b >> 8) & 0xFF).astype(np.uint8)
     return out
 
 
-def f24_merge(buf: np.ndarray) -> np.ndarray:
-    n = buf.size // 3
+def f24_merge(buf: np.ndarray, n: int) -> np.ndarray:
+    assert buf.size == f24_nbytes(n)
     hi = buf[:2 * n].view(np.uint16).astype(np.uint32)
-    lo = buf[2 * n:].astype(np.uint32)
+    lo = buf[f24_lo_offset(n):].astype(np.uint32)
     return ((hi << 16) | (lo << 8)).view(np.float32)
 
 

@@ -318,20 +318,21 @@ void orc_nadam_step_tensor(uint16_t* hi, uint16_t* lo, void* m, void* v, const u
  * mantissa ... it can only be used for storage rather than operations", sd-scripts PR #2187,
  * third post).  Reading: the stored value is the f32 pattern truncated to its upper 24 bits
  * (like the Kahan split); decode appends a zero byte.  Layout per moment buffer of n elements:
- * n uint16 words of the upper 16 bits, then n bytes of bits 8..15.  No scale is needed, so no
+ * n uint16 words of the upper 16 bits, zero padding up to byte offset 2n rounded up to a
+ * multiple of 16, then n bytes of bits 8..15 (storage only: the padding carries no value).  No scale is needed, so no
  * gradient maximum either.  Tensors of 4096 or fewer elements keep fp32 moments as before.
  * -------------------------------------------------------------------------------------- */
 static float f24_load(const uint8_t* buf, int64_t n, int64_t i)
 {
     const uint16_t* hi = (const uint16_t*)buf;
-    const uint8_t* lo = buf + 2 * n;
+    const uint8_t* lo = buf + ((2 * n + 15) / 16) * 16;
     return f_of(((uint32_t)hi[i] << 16) | ((uint32_t)lo[i] << 8));
 }
 
 static void f24_store(uint8_t* buf, int64_t n, int64_t i, float x)
 {
     uint16_t* hi = (uint16_t*)buf;
-    uint8_t* lo = buf + 2 * n;
+    uint8_t* lo = buf + ((2 * n + 15) / 16) * 16;
     uint32_t b = b_of(x);
     hi[i] = (uint16_t)(b >> 16);
     lo[i] = (uint8_t)((b >> 8) & 0xFFu);

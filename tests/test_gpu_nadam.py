@@ -192,8 +192,8 @@ def test_deterministic_two_runs(eng):
 @pytest.mark.parametrize("variant", ["nadamw", "adam"])
 def test_f24_moments_bit_exact(orc, eng, variant):
     """f24 moment storage (NADAM_F24 groups): weights, residuals and both moment planes
-    bit-identical to the oracle; sizes include fp32-moment tensors, ragged tails and byte planes
-    that are not 8-byte aligned (element-by-element path)."""
+    bit-identical to the oracle; sizes include fp32-moment tensors and ragged tails (the byte
+    plane is padded to a 16-byte offset, so ragged sizes stay on the 128-bit path)."""
     sizes = [100, 4096, 4097, 16384, 16389, 40000, 131072]
     seed = 21
     hp = dict(HP, lr=1e-3, nesterov=variant.startswith("n"), weight_decay=0.02 if variant.endswith("w") else 0.0,
@@ -203,7 +203,8 @@ def test_f24_moments_bit_exact(orc, eng, variant):
     for x in masters:
         hi, lo = orc.kahan_split(x.numpy())
         n = x.numel()
-        st = (np.zeros(n, np.float32), np.zeros(n, np.float32)) if n <= 4096 else (np.zeros(3 * n, np.uint8), np.zeros(3 * n, np.uint8))
+        st = ((np.zeros(n, np.float32), np.zeros(n, np.float32)) if n <= 4096 else
+              (np.zeros(orc.f24_nbytes(n), np.uint8), np.zeros(orc.f24_nbytes(n), np.uint8)))
         ora.append(dict(hi=hi, lo=lo, m=st[0], v=st[1]))
     grp = eng.NadamGroup.from_masters([m.cuda() for m in masters], states="f24")
     mp = 1.0
@@ -226,6 +227,56 @@ def test_f24_moments_bit_exact(orc, eng, variant):
             assert np.array_equal(grp.v[i].cpu().numpy(), o["v"]), i
 
 
+def test_f24_misaligned_buffers_take_scalar_path(orc, eng):
+    """f24 groups whose buffers start 2 bytes past a 16-byte boundary go element by element and
+    give the oracle's bits, padding bytes included."""
+    from memory_lean_optimizer_gb300 import lmopt
+    sizes = [5000, 20003]
+    seed = 31
+    masters = [W.master_weights((n,), seed, i) for i, n in enumerate(sizes)]
+    keep, descs, dev, ora = [], [], [], []
+    for i, n in enumerate(sizes):
+        hi, lo = orc.kahan_split(masters[i].numpy())
+        b1, w = alloc_offset(n, torch.int16, 1)
+        b2, r = alloc_offset(n, torch.int16, 1)
+        b3, m = alloc_offset(orc.f24_nbytes(n), torch.uint8, 2)
+        b4, v = alloc_offset(orc.f24_nbytes(n), torch.uint8, 2)
+        w.copy_(torch.from_numpy(hi.view(np.int16)))
+        r.copy_(torch.from_numpy(lo.view(np.int16)))
+        keep += [b1, b2, b3, b4]
+        d = lmopt.TensorDesc(w_bf16=w.data_ptr(), res_u16=r.data_ptr(), m=m.data_ptr(), v=v.data_ptr(),
+                             numel=n, ndim=1)
+        d.shape[0] = n
+        descs.append(d)
+        dev.append((w, r, m, v))
+        ora.append(dict(hi=hi, lo=lo, m=np.zeros(orc.f24_nbytes(n), np.uint8),
+                        v=np.zeros(orc.f24_nbytes(n), np.uint8)))
+    h = lmopt.optim_group_create(descs, lmopt.OPTIM_KIND_NADAM_F24)
+    H = lmopt.NadamHparams(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, wd_mode=0,
+                           nesterov=1, momentum_decay=0.004)
+    mp = 1.0
+    try:
+        for t in range(1, 4):
+            grads = [W.grad_bf16((n,), seed, i, t, 1e-3) for i, n in enumerate(sizes)]
+            k, mp = orc.nadam_scalars(t, 1e-3, 0.9, 0.999, 1e-8, 0.0, False, True, 0.004, mp)
+            for o, g in zip(ora, grads):
+                orc.nadam_step_tensor_f24(o["hi"], o["lo"], o["m"], o["v"], W.bits16(g), k)
+            gbufs = []
+            for g in grads:
+                b, gg = alloc_offset(g.numel(), torch.int16, 1)
+                gg.copy_(g.view(torch.int16))
+                gbufs += [b, gg]
+            lmopt.optim_step_nadam_kahan(h, [gbufs[2 * i + 1].data_ptr() for i in range(len(sizes))], t, H, 0)
+            torch.cuda.synchronize()
+            for (w, r, m, v), o in zip(dev, ora):
+                assert np.array_equal(cuda_bits(w), o["hi"])
+                assert np.array_equal(cuda_bits(r), o["lo"])
+                assert np.array_equal(m.cpu().numpy(), o["m"])
+                assert np.array_equal(v.cpu().numpy(), o["v"])
+    finally:
+        lmopt.optim_group_destroy(h)
+
+
 @pytest.mark.parametrize("states", ["u16", "f24"])
 def test_stochastic_rounding_bit_exact(orc, eng, states):
     """Tensors without a residual and stochastic_rounding = 1: the stored bf16 weights follow the
@@ -245,7 +296,7 @@ def test_stochastic_rounding_bit_exact(orc, eng, states):
         elif states == "u16":
             st = (np.full(n, 32768, np.uint16), np.zeros(n, np.uint16))
         else:
-            st = (np.zeros(3 * n, np.uint8), np.zeros(3 * n, np.uint8))
+            st = (np.zeros(orc.f24_nbytes(n), np.uint8), np.zeros(orc.f24_nbytes(n), np.uint8))
         ora.append(dict(hi=hi, m=st[0], v=st[1]))
     ost = orc.NadamState(len(sizes))
     mp = 1.0

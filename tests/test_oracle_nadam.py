@@ -198,26 +198,36 @@ def test_f24_moments_are_truncated_fp32(orc):
     """f24 storage: each stored moment is the fp32 moment of a plain fp32-moment step truncated to
     its upper 24 bits, step after step (checked by replaying each step from the stored state)."""
     rng = np.random.default_rng(17)
-    n = 10000
+    n = 10003
     w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
     hi, lo = orc.kahan_split(w0)
-    m = np.zeros(3 * n, np.uint8)
-    v = np.zeros(3 * n, np.uint8)
+    m = np.zeros(orc.f24_nbytes(n), np.uint8)
+    v = np.zeros(orc.f24_nbytes(n), np.uint8)
     mp = 1.0
     for t in range(1, 6):
         g = bf16_bits(rng.standard_normal(n) * 1e-3)
         k, mp = orc.nadam_scalars(t, 1e-3, 0.9, 0.999, 1e-8, 0.0, False, True, 0.004, mp)
         # reference: the same step with fp32 moments started from the decoded f24 state
         w_ref = orc.kahan_merge(hi, lo).copy()
-        m_ref = orc.f24_merge(m).copy()
-        v_ref = orc.f24_merge(v).copy()
+        m_ref = orc.f24_merge(m, n).copy()
+        v_ref = orc.f24_merge(v, n).copy()
         orc.nadam_step_fp32(w_ref, m_ref, v_ref, g, k)
         orc.nadam_step_tensor_f24(hi, lo, m, v, g, k)
         assert np.array_equal(orc.kahan_merge(hi, lo).view(np.uint32), w_ref.view(np.uint32))
         mask = np.uint32(0xFFFFFF00)
-        assert np.array_equal(orc.f24_merge(m).view(np.uint32), m_ref.view(np.uint32) & mask)
-        assert np.array_equal(orc.f24_merge(v).view(np.uint32), v_ref.view(np.uint32) & mask)
+        assert np.array_equal(orc.f24_merge(m, n).view(np.uint32), m_ref.view(np.uint32) & mask)
+        assert np.array_equal(orc.f24_merge(v, n).view(np.uint32), v_ref.view(np.uint32) & mask)
     # 8 more mantissa bits than bf16: relative storage error below 2^-15
     x = (rng.standard_normal(1000) * 1e-4).astype(np.float32)
-    rel = np.abs(orc.f24_merge(orc.f24_split(x)) - x) / np.abs(x)
+    rel = np.abs(orc.f24_merge(orc.f24_split(x), x.size) - x) / np.abs(x)
     assert rel.max() < 2.0 ** -15
+    # storage layout: the padding between the two planes stays zero, the byte plane starts at 2n
+    # rounded up to 16, and the upper plane holds the top 16 bits
+    pad = slice(2 * n, orc.f24_lo_offset(n))
+    assert orc.f24_lo_offset(n) == 20016 and pad.stop - pad.start == 10
+    assert not m[pad].any() and not v[pad].any()
+    y = np.array([1.0, -2.5, 3.0e-7], np.float32)
+    buf = orc.f24_split(y)
+    assert buf.size == 16 + 3
+    assert list(buf[:6].view(np.uint16)) == [0x3F80, 0xC020, (y.view(np.uint32)[2] >> 16)]
+    assert list(buf[16:]) == [0, 0, (y.view(np.uint32)[2] >> 8) & 0xFF]
