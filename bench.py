@@ -37,7 +37,13 @@ BYTES_PER_PARAM_F32 = 26      # fp32 moments: m, v 4 bytes each way
 BYTES_PER_PARAM_F24 = 22      # f24 moments: m, v 3 bytes each way
 PREPASS_BYTES_PER_PARAM = 2   # gradient-max pre-pass re-reads g
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["memory_lean_optimizer_gb300/csrc/nadam.cu", "memory_lean_optimizer_gb300/csrc/common.cuh"]
+# Source files of each measured kernel: a DRAM-traffic record is used only while they are unchanged.
+KERNEL_SOURCES = {
+    "k_nadam_step": ["memory_lean_optimizer_gb300/csrc/nadam.cu", "memory_lean_optimizer_gb300/csrc/common.cuh"],
+    "k_nadam_step<sr>": ["memory_lean_optimizer_gb300/csrc/nadam.cu", "memory_lean_optimizer_gb300/csrc/common.cuh"],
+    "k_nadam_f24": ["memory_lean_optimizer_gb300/csrc/nadam.cu", "memory_lean_optimizer_gb300/csrc/common.cuh"],
+    "k_adan_step": ["memory_lean_optimizer_gb300/csrc/adan.cu", "memory_lean_optimizer_gb300/csrc/common.cuh"],
+}
 
 
 def parse():
@@ -79,26 +85,28 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_hash():
+def kernel_hash(kernel):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def traffic_per_launch(params_per_launch):
-    """DRAM bytes per launch of the update kernel from the committed ncu summary, scaled to the
-    launch's parameter count; None when absent or taken on different kernel source."""
-    path = os.path.join(ROOT, "profiles", "k_nadam_step_traffic.json")
+def traffic_per_launch(kernel, params_per_launch):
+    """DRAM bytes per launch of `kernel` from the committed ncu record, scaled to the launch's
+    parameter count (the kernels stream every parameter once, so traffic grows in proportion);
+    None when absent or taken on different kernel source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(path):
         return None
     try:
         with open(path) as f:
             d = json.load(f)
-        if d.get("kernel_source_sha") != kernel_hash():
+        e = d["kernels"].get(kernel)
+        if e is None or e.get("kernel_source_sha") != kernel_hash(kernel):
             return None
-        return d["dram_bytes_per_param"] * params_per_launch
+        return e["dram_bytes_per_param"] * params_per_launch
     except Exception:
         return None
 
@@ -339,7 +347,8 @@ def run_ours(args, cfg):
     k2_gbs = k2_bytes_total / k2_time_total / 1e9
     peak, peak_src = peaks()
     params_per_launch = sum(group_params) / len(group_params)
-    traffic = traffic_per_launch(params_per_launch)
+    k2_name = ("k_nadam_f24" if args.states == "f24" else "k_nadam_step") + ("<sr>" if args.rounding == "sr" else "")
+    traffic = traffic_per_launch(k2_name, params_per_launch)
 
     step_s = elapsed / args.steps
     value = world * params * args.steps / elapsed
@@ -354,11 +363,10 @@ def run_ours(args, cfg):
                    "parallelism": f"replicas x{world}"},
         "hbm_gbs_step": sum(group_bytes) / step_s / 1e9,
         "hbm_gbs_step_as_run": (sum(group_bytes) + (PREPASS_BYTES_PER_PARAM * params if args.states == "u16" else 0)) / step_s / 1e9,
-        "roofline": {"bound": "hbm", "kernel": ("k_nadam_f24" if args.states == "f24" else "k_nadam_step")
-                     + ("<sr>" if args.rounding == "sr" else ""),
+        "roofline": {"bound": "hbm", "kernel": k2_name,
                      "achieved": k2_gbs, "peak": peak, "unit": "GB/s",
                      "frac": k2_gbs / peak,
-                     "traffic": traffic if (args.states == "u16" and args.rounding == "kahan") else None,
+                     "traffic": traffic,
                      "peak_source": peak_src,
                      "bytes_per_param": (BYTES_PER_PARAM_F24 if args.states == "f24" else BYTES_PER_PARAM_U16)
                      - (4 if args.rounding == "sr" else 0),
@@ -557,7 +565,8 @@ def run_adan(args, cfg):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, "params": params, "optimizer": "Adan + Kahan, fp32 m/v/n + previous bf16 grad"},
         "roofline": {"bound": "hbm", "kernel": "k_adan_step", "achieved": gbs, "peak": peak, "unit": "GB/s",
-                     "frac": gbs / peak, "traffic": None, "peak_source": src, "bytes_per_param": 38},
+                     "frac": gbs / peak, "traffic": traffic_per_launch("k_adan_step", params / len(groups)),
+                     "peak_source": src, "bytes_per_param": 38},
         "gpu_launches": len(groups) * args.steps, "clocks": clk}), flush=True)
     for g in groups:
         g.close()
