@@ -42,6 +42,7 @@ KERNEL_SOURCES = {
     "k_nadam_step": ["memory_lean_optimizer_gb300/csrc/nadam.cu", "memory_lean_optimizer_gb300/csrc/common.cuh"],
     "k_nadam_step<sr>": ["memory_lean_optimizer_gb300/csrc/nadam.cu", "memory_lean_optimizer_gb300/csrc/common.cuh"],
     "k_nadam_f24": ["memory_lean_optimizer_gb300/csrc/nadam.cu", "memory_lean_optimizer_gb300/csrc/common.cuh"],
+    "k_nadam_f24<sr>": ["memory_lean_optimizer_gb300/csrc/nadam.cu", "memory_lean_optimizer_gb300/csrc/common.cuh"],
     "k_adan_step": ["memory_lean_optimizer_gb300/csrc/adan.cu", "memory_lean_optimizer_gb300/csrc/common.cuh"],
 }
 

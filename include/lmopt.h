@@ -95,8 +95,10 @@ enum { OPTIM_KIND_NADAM = 0, OPTIM_KIND_FACTORED = 1, OPTIM_KIND_NADAM_F24 = 2, 
  *             rounded to bf16 instead of round-to-nearest (sd-scripts' default alternative to
  *             Kahan summation, "Kahan summation for Adafactor-optimized Flux FFT", PR #2159, PR
  *             description): 16 random bits are added below the kept half.  The bits come from
- *             Philox4x64-10 with key (seed, tensor index in the group) and counter (element / 16,
- *             step, 0, 0), element i taking 16-bit lane i mod 16; results are reproducible.
+ *             Philox4x32-10 (Salmon et al., SC 2011) with key (seed mod 2^32, seed / 2^32) and
+ *             counter (b mod 2^32, b / 2^32, tensor index in the group, step mod 2^32) for the
+ *             block b = element / 8, element i taking 16-bit lane i mod 8 (word (i mod 8) / 2, low
+ *             half first); results are reproducible.
  *   seed     : key of the stochastic rounding */
 typedef struct {
     float lr, beta1, beta2, eps, weight_decay;

@@ -18,29 +18,39 @@ struct AdanPrm {
     uint64_t seed;
 };
 
-__device__ __forceinline__ void philox4x64_10(uint64_t& c0, uint64_t& c1, uint64_t& c2, uint64_t& c3,
-                                              uint64_t k0, uint64_t k1) {
-    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
-    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
+// SC 2011), the same stream as the NAdam kernels: key (seed low, seed high), counter (b low,
+// b high, tensor, step mod 2^32) for the 8-element block b = i / 8; element i takes 16-bit lane
+// i mod 8 (word (i mod 8) / 2, low half for even i).
+__device__ __forceinline__ void philox4x32_10(uint32_t (&c)[4], uint32_t k0, uint32_t k1) {
+    constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u, W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
-        const uint64_t hi0 = __umul64hi(M0, c0), lo0 = M0 * c0;
-        const uint64_t hi1 = __umul64hi(M1, c2), lo1 = M1 * c2;
-        const uint64_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
-        c0 = n0;
-        c1 = lo1;
-        c2 = n2;
-        c3 = lo0;
+        const uint64_t p0 = (uint64_t)M0 * c[0], p1 = (uint64_t)M1 * c[2];
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c[1] ^ k0;
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c[3] ^ k1;
+        c[0] = n0;
+        c[1] = (uint32_t)p1;
+        c[2] = n2;
+        c[3] = (uint32_t)p0;
         k0 += W0;
         k1 += W1;
     }
 }
+__device__ __forceinline__ void sr_block(const AdanPrm& k, uint32_t tensor, int64_t i, uint32_t (&r)[4]) {
+    const uint64_t b = (uint64_t)i >> 3;
+    r[0] = (uint32_t)b;
+    r[1] = (uint32_t)(b >> 32);
+    r[2] = tensor;
+    r[3] = (uint32_t)k.step;
+    philox4x32_10(r, (uint32_t)k.seed, (uint32_t)(k.seed >> 32));
+}
 __device__ __forceinline__ uint32_t sr_lane(const AdanPrm& k, uint32_t tensor, int64_t i) {
-    uint64_t c0 = (uint64_t)i >> 4, c1 = (uint64_t)k.step, c2 = 0, c3 = 0;
-    philox4x64_10(c0, c1, c2, c3, k.seed, tensor);
-    const int lane = (int)(i & 15);
-    const uint64_t wsel = lane < 4 ? c0 : (lane < 8 ? c1 : (lane < 12 ? c2 : c3));
-    return (uint32_t)(wsel >> (16 * (lane & 3))) & 0xFFFFu;
+    uint32_t r[4];
+    sr_block(k, tensor, i, r);
+    const int lane = (int)(i & 7);
+    const uint32_t wsel = lane < 2 ? r[0] : (lane < 4 ? r[1] : (lane < 6 ? r[2] : r[3]));
+    return (wsel >> (16 * (lane & 1))) & 0xFFFFu;
 }
 
 __device__ __forceinline__ float adan_elem(const AdanPrm& k, float w, float g, float gp, float& m, float& v, float& n) {
@@ -108,12 +118,8 @@ __global__ void __launch_bounds__(kThreads, 4) k_adan_step(NadamLaunch L, AdanPr
         *reinterpret_cast<float4*>(va + 4) = ld_stream(reinterpret_cast<const float4*>(vp + i + 4));
         *reinterpret_cast<float4*>(na) = ld_stream(reinterpret_cast<const float4*>(np_ + i));
         *reinterpret_cast<float4*>(na + 4) = ld_stream(reinterpret_cast<const float4*>(np_ + i + 4));
-        uint64_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;
-        if (kSR && !has_res) {   // one Philox block covers the 16-element group holding these 8
-            c0 = (uint64_t)i >> 4;
-            c1 = (uint64_t)k.step;
-            philox4x64_10(c0, c1, c2, c3, k.seed, c.tensor);
-        }
+        uint32_t rnd[4] = {0u, 0u, 0u, 0u};
+        if (kSR && !has_res) sr_block(k, c.tensor, i, rnd);   // one block for these 8 elements
         const uint32_t w32[4] = {W.x, W.y, W.z, W.w}, r32[4] = {R.x, R.y, R.z, R.w};
         const uint32_t g32[4] = {G.x, G.y, G.z, G.w}, p32[4] = {GP.x, GP.y, GP.z, GP.w};
         uint32_t wo[4], ro[4];
@@ -128,10 +134,8 @@ __global__ void __launch_bounds__(kThreads, 4) k_adan_step(NadamLaunch L, AdanPr
                 const float w0 = has_res ? __uint_as_float((hw << 16) | lw) : bf16_to_f32(hw);
                 const float w1 = adan_elem(k, w0, bf16_to_f32((g32[q] >> sh) & 0xFFFFu),
                                            bf16_to_f32((p32[q] >> sh) & 0xFFFFu), ma[e], va[e], na[e]);
-                const int lane = (int)(i & 15) + e;
-                const uint64_t wsel = lane < 4 ? c0 : (lane < 8 ? c1 : (lane < 12 ? c2 : c3));
                 uint32_t lo;
-                const uint32_t hi = store_bits(w1, has_res, kSR, (uint32_t)(wsel >> (16 * (lane & 3))) & 0xFFFFu, lo);
+                const uint32_t hi = store_bits(w1, has_res, kSR, (rnd[q] >> sh) & 0xFFFFu, lo);
                 wo[q] |= hi << sh;
                 ro[q] |= lo << sh;
                 nf = max(nf, hi & 0x7FFFu);

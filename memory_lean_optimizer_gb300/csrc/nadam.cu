@@ -35,56 +35,45 @@ struct Prm {
     uint64_t step;
 };
 
-// Philox4x64-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
-// SC 2011): ten rounds of two 64x64->128 multiplies with Weyl-sequence key bumps.
-__device__ __forceinline__ void philox4x64_10(uint64_t& c0, uint64_t& c1, uint64_t& c2, uint64_t& c3,
-                                              uint64_t k0, uint64_t k1) {
-    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
-    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
+// SC 2011): ten rounds of two 32x32->64 multiplies with Weyl-sequence key bumps.
+__device__ __forceinline__ void philox4x32_10(uint32_t (&c)[4], uint32_t k0, uint32_t k1) {
+    constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u, W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
-        const uint64_t hi0 = __umul64hi(M0, c0), lo0 = M0 * c0;
-        const uint64_t hi1 = __umul64hi(M1, c2), lo1 = M1 * c2;
-        const uint64_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
-        c0 = n0;
-        c1 = lo1;
-        c2 = n2;
-        c3 = lo0;
+        const uint64_t p0 = (uint64_t)M0 * c[0], p1 = (uint64_t)M1 * c[2];
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c[1] ^ k0;
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c[3] ^ k1;
+        c[0] = n0;
+        c[1] = (uint32_t)p1;
+        c[2] = n2;
+        c[3] = (uint32_t)p0;
         k0 += W0;
         k1 += W1;
     }
 }
-// Random 16-bit lanes for 8 consecutive elements starting at element i0 (i0 % 8 == 0) of
-// tensor `tensor`: key (seed, tensor), counter (i0 / 16, step, 0, 0); lanes low to high.
+// Random 16-bit lanes for the 8 elements i0 .. i0+7 (i0 % 8 == 0) of tensor `tensor`: key
+// (seed low, seed high), counter (b low, b high, tensor, step mod 2^32) with b = i0 / 8; word j
+// holds lanes 2j (low half) and 2j+1.
 __device__ __forceinline__ void sr_lanes8(const Prm& k, uint32_t tensor, int64_t i0, uint32_t (&r)[4]) {
-    uint64_t c0 = (uint64_t)i0 >> 4, c1 = k.step, c2 = 0, c3 = 0;
-    philox4x64_10(c0, c1, c2, c3, k.seed, tensor);
-    const uint64_t a = (i0 & 8) ? c2 : c0, b = (i0 & 8) ? c3 : c1;
-    r[0] = (uint32_t)a;          // lanes 0,1 (low half = first element)
-    r[1] = (uint32_t)(a >> 32);  // lanes 2,3
-    r[2] = (uint32_t)b;
-    r[3] = (uint32_t)(b >> 32);
+    const uint64_t b = (uint64_t)i0 >> 3;
+    r[0] = (uint32_t)b;
+    r[1] = (uint32_t)(b >> 32);
+    r[2] = tensor;
+    r[3] = (uint32_t)k.step;
+    philox4x32_10(r, (uint32_t)k.seed, (uint32_t)(k.seed >> 32));
 }
-// Both halves of the 16-lane block starting at element i0 (i0 % 16 == 0): one generator call.
 __device__ __forceinline__ void sr_lanes16(const Prm& k, uint32_t tensor, int64_t i0, uint32_t (&ra)[4],
                                            uint32_t (&rb)[4]) {
-    uint64_t c0 = (uint64_t)i0 >> 4, c1 = k.step, c2 = 0, c3 = 0;
-    philox4x64_10(c0, c1, c2, c3, k.seed, tensor);
-    ra[0] = (uint32_t)c0;
-    ra[1] = (uint32_t)(c0 >> 32);
-    ra[2] = (uint32_t)c1;
-    ra[3] = (uint32_t)(c1 >> 32);
-    rb[0] = (uint32_t)c2;
-    rb[1] = (uint32_t)(c2 >> 32);
-    rb[2] = (uint32_t)c3;
-    rb[3] = (uint32_t)(c3 >> 32);
+    sr_lanes8(k, tensor, i0, ra);
+    sr_lanes8(k, tensor, i0 + 8, rb);
 }
 __device__ __forceinline__ uint32_t sr_lane1(const Prm& k, uint32_t tensor, int64_t i) {
-    uint64_t c0 = (uint64_t)i >> 4, c1 = k.step, c2 = 0, c3 = 0;
-    philox4x64_10(c0, c1, c2, c3, k.seed, tensor);
-    const int lane = (int)(i & 15);
-    const uint64_t wsel = lane < 4 ? c0 : (lane < 8 ? c1 : (lane < 12 ? c2 : c3));
-    return (uint32_t)(wsel >> (16 * (lane & 3))) & 0xFFFFu;
+    uint32_t r[4];
+    sr_lanes8(k, tensor, i & ~(int64_t)7, r);
+    const int lane = (int)(i & 7);
+    const uint32_t wsel = lane < 2 ? r[0] : (lane < 4 ? r[1] : (lane < 6 ? r[2] : r[3]));
+    return (wsel >> (16 * (lane & 1))) & 0xFFFFu;
 }
 // Stochastic rounding to bf16 bits: add 16 random bits below the kept half (inf/NaN kept).
 __device__ __forceinline__ uint32_t sr_bf16(float x, uint32_t r16) {
@@ -283,12 +272,11 @@ __device__ __forceinline__ void u16_vectors(const Prm& k, const Codec& cd, bool 
                                             float& am, float& av, uint32_t& nf) {
     // nv <= kChunk / 8: 32-bit vector indices within the chunk
     const bool sr = kSR && !has_res;
-    // two independent 8-element groups per iteration: ten 128-bit loads in flight.  With
-    // stochastic rounding the two groups are the halves of one 16-element block, so one
-    // generator call serves both; otherwise they are kThreads vectors apart.
+    // two independent 8-element groups per iteration, kThreads vectors apart: ten 128-bit
+    // loads in flight (one generator call per group under stochastic rounding).
     int p = threadIdx.x;
-    for (; sr ? (2 * p + 1 < nv) : (p + kThreads < nv); p += sr ? kThreads : 2 * kThreads) {
-        const int i = sr ? 2 * p : p, i1 = sr ? 2 * p + 1 : p + kThreads;
+    for (; p + kThreads < nv; p += 2 * kThreads) {
+        const int i = p, i1 = p + kThreads;
         uint4 W0 = ld_stream(wv + i), W1 = ld_stream(wv + i1);
         uint4 R0 = has_res ? ld_stream(rv + i) : make_uint4(0, 0, 0, 0);
         uint4 R1 = has_res ? ld_stream(rv + i1) : make_uint4(0, 0, 0, 0);
@@ -296,12 +284,13 @@ __device__ __forceinline__ void u16_vectors(const Prm& k, const Codec& cd, bool 
         uint4 M0 = ld_stream(mv + i), M1 = ld_stream(mv + i1);
         uint4 V0 = ld_stream(vv + i), V1 = ld_stream(vv + i1);
         uint32_t ra[4] = {0u, 0u, 0u, 0u}, rb[4] = {0u, 0u, 0u, 0u};
-        if (sr) sr_lanes16(k, tensor, start + 16 * (int64_t)p, ra, rb);
+        if (sr) sr_lanes8(k, tensor, start + 8 * (int64_t)i, ra);
         step8_u16<kSR, kGuard>(k, cd, has_res, ra, W0, R0, G0, M0, V0, am, av, nf);
         st_stream(wv + i, W0);
         if (has_res) st_stream(rv + i, R0);
         st_stream(mv + i, M0);
         st_stream(vv + i, V0);
+        if (sr) sr_lanes8(k, tensor, start + 8 * (int64_t)i1, rb);
         step8_u16<kSR, kGuard>(k, cd, has_res, rb, W1, R1, G1, M1, V1, am, av, nf);
         st_stream(wv + i1, W1);
         if (has_res) st_stream(rv + i1, R1);
@@ -309,7 +298,7 @@ __device__ __forceinline__ void u16_vectors(const Prm& k, const Codec& cd, bool 
         st_stream(vv + i1, V1);
     }
     // remaining vectors one at a time
-    for (int i = sr ? 2 * p : p; i < nv; i += kThreads) {
+    for (int i = p; i < nv; i += kThreads) {
         uint4 W0 = ld_stream(wv + i);
         uint4 R0 = has_res ? ld_stream(rv + i) : make_uint4(0, 0, 0, 0);
         uint4 G0 = ld_stream(gv + i), M0 = ld_stream(mv + i), V0 = ld_stream(vv + i);

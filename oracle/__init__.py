@@ -101,7 +101,7 @@ def _load():
             "orc_nadam_step_fp32": (None, [P, P, P, P, I64, ctypes.POINTER(NadamScalars)]),
             "orc_nadam_step_tensor_f24": (None, [P, P, P, P, P, I64, ctypes.POINTER(NadamScalars), I32,
                                                  ctypes.c_uint64, ctypes.c_uint32, I64]),
-            "orc_philox4x64_10": (None, [P, P, P]),
+            "orc_philox4x32_10": (None, [P, P, P]),
             "orc_adan_scalars": (None, [F, F, F, F, F, F, ctypes.POINTER(AdanScalars)]),
             "orc_adan_step_tensor": (None, [P, P, P, P, P, I64, I64, ctypes.POINTER(AdanScalars), I32,
                                             ctypes.c_uint64, ctypes.c_uint32]),
@@ -241,11 +241,11 @@ def nadam_step_tensor_f24(hi, lo, m, v, g, k: NadamScalars, sr=False, seed=0, te
                                       int(sr), seed, tensor, step)
 
 
-def philox4x64_10(ctr, key):
-    c = np.ascontiguousarray(ctr, np.uint64)
-    k = np.ascontiguousarray(key, np.uint64)
-    out = np.zeros(4, np.uint64)
-    _load().orc_philox4x64_10(_p(c), _p(k), _p(out))
+def philox4x32_10(ctr, key):
+    c = np.ascontiguousarray(ctr, np.uint32)
+    k = np.ascontiguousarray(key, np.uint32)
+    out = np.zeros(4, np.uint32)
+    _load().orc_philox4x32_10(_p(c), _p(k), _p(out))
     return out
 
 

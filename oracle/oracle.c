@@ -376,28 +376,26 @@ void orc_nadam_step_tensor_f24(uint16_t* hi, uint16_t* lo, void* m, void* v, con
  * depending on the distance", "Kahan summation for Adafactor-optimized Flux FFT", sd-scripts
  * PR #2159, PR description).  Reading: add 16 uniform random bits to the f32 pattern and keep
  * the upper half, which rounds the magnitude up with probability (low 16 bits)/65536.
- * Random bits: Philox4x64-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as
- * 1, 2, 3", SC 2011), key (seed, tensor index), counter (element index / 16, step, 0, 0); element
- * i takes 16-bit lane i mod 16 of the 256-bit block (lanes low to high within each 64-bit word).
+ * Random bits: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as
+ * 1, 2, 3", SC 2011): four 32-bit counter words, two key words, ten rounds; each round forms
+ * the two 64-bit products M0*c0 and M1*c2, the new words are (hi(M1*c2) ^ c1 ^ k0, lo(M1*c2),
+ * hi(M0*c0) ^ c3 ^ k1, lo(M0*c0)), and the key is bumped by the Weyl constants.  The pages do
+ * not name a generator; this one is chosen as a published counter-based generator that both
+ * sides can compute independently per element.  Key (seed mod 2^32, seed / 2^32); counter
+ * (b mod 2^32, b / 2^32, tensor index, step mod 2^32) with b = i / 8; element i takes 16-bit
+ * lane i mod 8 of the 128-bit block (word (i mod 8) / 2, low half for even i).
  * -------------------------------------------------------------------------------------- */
-static void mulhilo64(uint64_t a, uint64_t b, uint64_t* hi, uint64_t* lo)
+void orc_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4])
 {
-    unsigned __int128 p = (unsigned __int128)a * (unsigned __int128)b;
-    *hi = (uint64_t)(p >> 64);
-    *lo = (uint64_t)p;
-}
-
-void orc_philox4x64_10(const uint64_t ctr_in[4], const uint64_t key_in[2], uint64_t out[4])
-{
-    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
-    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
-    uint64_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
-    uint64_t k0 = key_in[0], k1 = key_in[1];
+    const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+    const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+    uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint32_t k0 = key_in[0], k1 = key_in[1];
     for (int r = 0; r < 10; ++r) {
-        uint64_t hi0, lo0, hi1, lo1;
-        mulhilo64(M0, c0, &hi0, &lo0);
-        mulhilo64(M1, c2, &hi1, &lo1);
-        uint64_t n0 = hi1 ^ c1 ^ k0, n1 = lo1, n2 = hi0 ^ c3 ^ k1, n3 = lo0;
+        uint64_t p0 = (uint64_t)M0 * (uint64_t)c0;
+        uint64_t p1 = (uint64_t)M1 * (uint64_t)c2;
+        uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0, n1 = (uint32_t)p1;
+        uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1, n3 = (uint32_t)p0;
         c0 = n0; c1 = n1; c2 = n2; c3 = n3;
         k0 += W0;
         k1 += W1;
@@ -407,10 +405,12 @@ void orc_philox4x64_10(const uint64_t ctr_in[4], const uint64_t key_in[2], uint6
 
 uint32_t orc_sr_bits(uint64_t seed, uint32_t tensor, int64_t step, int64_t i)
 {
-    uint64_t ctr[4] = {(uint64_t)i >> 4, (uint64_t)step, 0, 0}, key[2] = {seed, tensor}, out[4];
-    orc_philox4x64_10(ctr, key, out);
-    int lane = (int)(i & 15);
-    return (uint32_t)((out[lane >> 2] >> (16 * (lane & 3))) & 0xFFFFu);
+    uint64_t b = (uint64_t)i >> 3;
+    uint32_t ctr[4] = {(uint32_t)b, (uint32_t)(b >> 32), tensor, (uint32_t)step};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)}, out[4];
+    orc_philox4x32_10(ctr, key, out);
+    int lane = (int)(i & 7);
+    return (out[lane >> 1] >> (16 * (lane & 1))) & 0xFFFFu;
 }
 
 static uint16_t sr_bf16(float x, uint32_t r16)

@@ -1,22 +1,44 @@
-"""Pins of the oracle's stochastic rounding: its Philox4x64-10 against numpy's implementation of
-the same published generator, exactness on bf16 values, unbiasedness, and the rounding
+"""Pins of the oracle's stochastic rounding: its Philox4x32-10 against the generator's published
+known-answer vectors, the element-to-lane layout, exactness on bf16 values, and the rounding
 probability equal to the distance to the lower bf16 neighbour."""
+import os
+
 import numpy as np
 import pytest
 import torch
 
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "philox4x32_10_kat.txt")
 
-def test_philox_matches_numpy(orc):
-    """numpy advances its 256-bit counter before each block, so its block k is Philox at k+1."""
-    rng = np.random.default_rng(30)
-    for _ in range(20):
-        ctr = rng.integers(0, 2 ** 63, 4, dtype=np.uint64)
-        ctr[0] = ctr[0] >> np.uint64(1)            # no carry out of the first word
-        key = rng.integers(0, 2 ** 63, 2, dtype=np.uint64)
-        start = ctr.copy()
-        start[0] -= np.uint64(1)
-        ref = np.random.Philox(counter=start, key=key).random_raw(4)
-        assert np.array_equal(orc.philox4x64_10(ctr, key), ref.astype(np.uint64))
+
+def test_philox_known_answers(orc):
+    rows = [l.split() for l in open(GOLDEN) if l.strip() and not l.startswith("#")]
+    assert len(rows) == 3
+    for r in rows:
+        w = [int(x, 16) for x in r]
+        assert list(orc.philox4x32_10(w[0:4], w[4:6])) == w[6:10]
+
+
+def test_sr_lanes_cover_the_block(orc):
+    """Eight consecutive elements from i = 8b take the eight 16-bit halves of one block, low half
+    first; the block's counter is (b, tensor, step) under key seed, and blocks differ."""
+    seed, tensor, step = 0x1234567890ABCDEF, 7, 3
+    b = (1 << 33) + 5                      # a block index above 2^32: both counter words used
+    out = orc.philox4x32_10([b & 0xFFFFFFFF, b >> 32, tensor, step], [seed & 0xFFFFFFFF, seed >> 32])
+    lanes = [orc.sr_bits(seed, tensor, step, 8 * b + j) for j in range(8)]
+    assert lanes == [(int(out[j // 2]) >> (16 * (j % 2))) & 0xFFFF for j in range(8)]
+    nxt = [orc.sr_bits(seed, tensor, step, 8 * (b + 1) + j) for j in range(8)]
+    other_t = [orc.sr_bits(seed, tensor + 1, step, 8 * b + j) for j in range(8)]
+    other_s = [orc.sr_bits(seed, tensor, step + 1, 8 * b + j) for j in range(8)]
+    assert lanes != nxt and lanes != other_t and lanes != other_s
+
+
+def test_sr_bits_uniform(orc):
+    """The 16-bit lanes are uniform: chi-square over 64 bins of 65,536 draws (63 degrees of
+    freedom; the 1e-6 tail is near 130)."""
+    draws = np.array([orc.sr_bits(99, 1, 2, i) for i in range(65536)], np.uint32)
+    counts = np.bincount(draws >> 10, minlength=64)
+    e = draws.size / 64
+    assert ((counts - e) ** 2 / e).sum() < 130
 
 
 def test_sr_exact_on_bf16_values_and_keeps_specials(orc):
