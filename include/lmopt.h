@@ -83,8 +83,9 @@ typedef struct {
  * 16-byte boundary take the 128-bit path whatever numel is.  No scale records and no gradient
  * pre-pass are involved; tensors of 4096 or fewer elements keep fp32 moments. */
 enum { OPTIM_KIND_NADAM = 0, OPTIM_KIND_FACTORED = 1, OPTIM_KIND_NADAM_F24 = 2, OPTIM_KIND_ADAN = 3 };
-/* ADAN groups: m -> fp32 [3*numel] (planes m, v, n), v -> uint16 [numel] (previous bf16 gradient),
- * all zero at creation. */
+/* ADAN groups: m -> fp32 [3*P] (planes m, v, n, each P = numel rounded up to a multiple of 4
+ * floats, so that every plane of a 16-byte aligned buffer is 16-byte aligned and takes the
+ * 128-bit path), v -> uint16 [numel] (previous bf16 gradient), all zero at creation. */
 
 /* Adam / NAdam(W) hyper-parameters ("(N)AdamW / Adan with fused backwards pass & CPU
  * offloading", sd-scripts PR #2187, first post: NAdamOffload, AdamOffload, NAdamWOffload).

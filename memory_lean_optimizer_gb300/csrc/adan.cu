@@ -95,16 +95,18 @@ __global__ void __launch_bounds__(kThreads, 4) k_adan_step(NadamLaunch L, AdanPr
     const int64_t start = (int64_t)c.index * kChunk;
     const int64_t end = min(n, start + kChunk);
     float* __restrict__ mp = static_cast<float*>(t.m);
-    float* __restrict__ vp = mp + n;
-    float* __restrict__ np_ = mp + 2 * n;
+    const int64_t plane = (n + 3) & ~int64_t(3);   // plane stride: n rounded up to 4 floats
+    float* __restrict__ vp = mp + plane;
+    float* __restrict__ np_ = mp + 2 * plane;
     uint16_t* __restrict__ gprev = static_cast<uint16_t*>(t.v);
     uint16_t* __restrict__ w = t.w;
     uint16_t* __restrict__ res = t.res;
     uint32_t nf = 0u;
-    // 8 elements per thread per iteration with 128-bit accesses when every plane is 16-byte
-    // aligned (chunk starts are multiples of 8 elements); the rest element by element
+    // 8 elements per thread per iteration with 128-bit accesses when every buffer is 16-byte
+    // aligned (chunk starts are multiples of 8 elements, plane strides multiples of 4 floats);
+    // the rest element by element
     const bool vec = aligned16(w) && (!has_res || aligned16(res)) && aligned16(g) && aligned16(gprev) &&
-                     aligned16(mp) && (n & 3) == 0;
+                     aligned16(mp);
     const int64_t vend = vec ? start + ((end - start) & ~int64_t(7)) : start;
     for (int64_t i = start + 8 * (int64_t)threadIdx.x; i < vend; i += 8 * kThreads) {
         const uint4 W = ld_stream(reinterpret_cast<const uint4*>(w + i));

@@ -291,7 +291,9 @@ class AdanGroup(_Group):
         if residuals is None:
             residuals = [_u16_empty(w.numel(), dev, 0) if kahan else None for w in self.weights]
         self.res = list(residuals)
-        self.mvn = [torch.zeros(3 * w.numel(), dtype=torch.float32, device=dev) for w in self.weights]
+        # planes m, v, n, each numel rounded up to a multiple of 4 floats (16-byte aligned planes)
+        self.mvn = [torch.zeros(3 * ((w.numel() + 3) // 4 * 4), dtype=torch.float32, device=dev)
+                    for w in self.weights]
         self.gprev = [torch.zeros(w.numel(), dtype=torch.int16, device=dev) for w in self.weights]
         descs = [_desc(w, r, m, v, w.shape) for w, r, m, v in zip(self.weights, self.res, self.mvn, self.gprev)]
         self.handle = lmopt.optim_group_create(descs, self.kind)

@@ -271,8 +271,15 @@ def adan_scalars(lr, b1, b2, b3, eps, wd) -> AdanScalars:
     return k
 
 
+def adan_plane(n: int) -> int:
+    """Stride of the m, v, n planes of an Adan state buffer: n rounded up to a multiple of 4."""
+    return (n + 3) // 4 * 4
+
+
 def adan_step_tensor(hi, lo, mnv, gprev, g, step, k: AdanScalars, sr=False, seed=0, tensor=0):
-    """In place: hi/lo uint16 (lo may be None), mnv float32 [3n] (m, v, n planes), gprev uint16."""
+    """In place: hi/lo uint16 (lo may be None), mnv float32 [3 adan_plane(n)] (m, v, n planes),
+    gprev uint16."""
+    assert mnv.size == 3 * adan_plane(hi.size)
     _load().orc_adan_step_tensor(_p(hi), _p(lo), _p(mnv), _p(gprev), _p(_u16(g)), hi.size, int(step),
                                  ctypes.byref(k), int(sr), seed, tensor)
 

@@ -486,7 +486,8 @@ void orc_nadam_step_tensor_sr(uint16_t* hi, void* m, void* v, const uint16_t* g,
  *   m  = fma(omb1, m, b1 g);  v = fma(omb2, v, b2 d);  c = fma(omb2, d, g);  n = fma(omb3, n, b3 (c c))
  *   den = sqrt(n) + eps;  u = fma(omb2, v, m);  w = (w - lr (u / den)) * inv_decay
  * with inv_decay = 1/(1 + lr wd) computed once per step in double.
- * mnv: fp32 [3n] planes m, v, n; gprev: bf16 bits [n].
+ * mnv: fp32 planes m, v, n, each P = n rounded up to a multiple of 4 long (the padding is
+ * storage only: it keeps every plane 16-byte aligned); gprev: bf16 bits [n].
  * -------------------------------------------------------------------------------------- */
 typedef struct {
     float lr, b1, omb1, b2, omb2, b3, omb3, eps, inv_decay;
@@ -509,9 +510,10 @@ void orc_adan_step_tensor(uint16_t* hi, uint16_t* lo, float* mnv, uint16_t* gpre
                           int64_t n, int64_t step, const orc_adan_scalars_t* k, int32_t sr, uint64_t seed,
                           uint32_t tensor)
 {
+    const int64_t P = (n + 3) / 4 * 4;
     float* m = mnv;
-    float* v = mnv + n;
-    float* nn = mnv + 2 * n;
+    float* v = mnv + P;
+    float* nn = mnv + 2 * P;
     for (int64_t i = 0; i < n; ++i) {
         float w = lo ? f_of(((uint32_t)hi[i] << 16) | lo[i]) : bf16_to_f32(hi[i]);
         float gg = bf16_to_f32(g[i]);

@@ -16,8 +16,8 @@ HP = dict(lr=3.3e-5, beta1=0.02, beta2=0.08, beta3=0.01, eps=1e-8, weight_decay=
 def test_adan_bit_exact(orc, rounding):
     from memory_lean_optimizer_gb300 import build, engine
     build.build()
-    # 128-bit path where n % 4 == 0 (100, 16384, 40004: whole chunks, 8-element tails), element
-    # path otherwise (1, 4097, 50001)
+    # 128-bit path for every size (planes padded to 4 floats): whole chunks, 8-element tails and
+    # sizes that are not multiples of 4 (1, 4097, 50001)
     sizes = [1, 100, 4097, 16384, 50001, 40004]
     seed, key = 50, 777
     hp = dict(HP, stochastic_rounding=int(rounding == "sr"), seed=key)
@@ -29,7 +29,7 @@ def test_adan_bit_exact(orc, rounding):
         grp = engine.AdanGroup([m.cuda().to(torch.bfloat16) for m in masters], kahan=False)
         ora = [dict(hi=W.bits16(m.to(torch.bfloat16)).copy(), lo=None) for m in masters]
     for o, n in zip(ora, sizes):
-        o["mnv"] = np.zeros(3 * n, np.float32)
+        o["mnv"] = np.zeros(3 * orc.adan_plane(n), np.float32)
         o["gp"] = np.zeros(n, np.uint16)
     k = orc.adan_scalars(hp["lr"], hp["beta1"], hp["beta2"], hp["beta3"], hp["eps"], hp["weight_decay"])
     for t in range(1, 5):

@@ -10,7 +10,7 @@ B1, B2, B3 = 0.02, 0.08, 0.01
 def run(orc, w0, grads, lr, wd=0.0, eps=0.0):
     n = w0.size
     hi, lo = orc.kahan_split(w0)
-    mnv = np.zeros(3 * n, np.float32)
+    mnv = np.zeros(3 * orc.adan_plane(n), np.float32)
     gp = np.zeros(n, np.uint16)
     k = orc.adan_scalars(lr, B1, B2, B3, eps, wd)
     for t, g in enumerate(grads, start=1):
@@ -23,12 +23,18 @@ def test_constant_gradient_moves_by_lr_sign():
     is exactly w - lr sign(g) (eps = 0, no decay)."""
     import oracle as orc
     rng = np.random.default_rng(40)
-    n = 2000
+    n = 2003
     g = bf16_bits(rng.choice([-1.0, 1.0], n) * 2.0 ** rng.integers(-12, -4, n))
     lr = 2.0 ** -10
     w, mnv, gp = run(orc, np.zeros(n, np.float32), [g] * 6, lr)
     assert np.array_equal(w, -6 * lr * np.sign(bits_to_f32(g)))
-    assert np.array_equal(mnv[:n], bits_to_f32(g)) and np.all(mnv[n:2 * n] == 0)
+    # planes at 0, P, 2P with P = n rounded up to 4; the padding stays zero
+    P = orc.adan_plane(n)
+    assert P == 2004 and mnv.size == 3 * P
+    gf = bits_to_f32(g)
+    assert np.array_equal(mnv[:n], gf) and np.all(mnv[P:P + n] == 0)
+    assert np.array_equal(mnv[2 * P:2 * P + n], gf * gf)
+    assert np.all(mnv[n:P] == 0) and np.all(mnv[2 * P + n:] == 0)
     assert np.array_equal(gp, g)
 
 
