@@ -67,7 +67,7 @@ class AdanScalars(ctypes.Structure):
 class FactoredScalars(ctypes.Structure):
     _fields_ = [(n, ctypes.c_float) for n in
                 ("b2t", "alpha", "eps1", "eps2", "clip", "lr_eff", "nwdlr")] + \
-               [("mode", ctypes.c_int32)]
+               [("mode", ctypes.c_int32), ("unum", ctypes.c_float)]
 
 
 def _load():
@@ -114,6 +114,12 @@ def _load():
             "orc_factored_step_tensor": (F, [P, P, P, I64, I64, I64, P, P,
                                              ctypes.POINTER(FactoredScalars)]),
             "orc_factored_step_vector": (F, [P, P, P, I64, P, ctypes.POINTER(FactoredScalars)]),
+            "orc_prodigy_slice_len": (I64, [I64, I32]),
+            "orc_prodigy_snapshot": (None, [P, P, I64, I32, P, P]),
+            "orc_prodigy_tensor_stats": (None, [P, P, P, I64, I32, P, P, F, F, ctypes.POINTER(ctypes.c_double),
+                                                ctypes.POINTER(ctypes.c_double)]),
+            "orc_prodigy_end_step": (None, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
+                                            ctypes.c_double, ctypes.c_double, ctypes.c_double]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -350,6 +356,74 @@ def factored_step_tensor(hi, lo, g, B, R, C, row, col, k: FactoredScalars) -> fl
 def factored_step_vector(hi, lo, g, V, k: FactoredScalars) -> float:
     return _load().orc_factored_step_vector(_p(hi), _p(lo), _p(_u16(g)), hi.size, _p(V),
                                             ctypes.byref(k))
+
+
+# ---------------------------------------------------------------- Prodigy d (R19)
+def prodigy_slice_len(n: int, slice_p: int) -> int:
+    return _load().orc_prodigy_slice_len(int(n), int(slice_p))
+
+
+def prodigy_snapshot(hi, lo, slice_p: int):
+    """(p0, s) float32 buffers of the sampled elements of the current master."""
+    n = hi.size
+    L = prodigy_slice_len(n, slice_p)
+    p0 = np.zeros(L, np.float32)
+    s = np.zeros(L, np.float32)
+    _load().orc_prodigy_snapshot(_p(hi), _p(lo), n, int(slice_p), _p(p0), _p(s))
+    return p0, s
+
+
+def prodigy_tensor_stats(hi, lo, g, slice_p, p0, s, beta3, cs):
+    """Updates s in place; returns (sum g (p0 - x), sum |s|) of the tensor (before its step)."""
+    dot = ctypes.c_double(0.0)
+    l1 = ctypes.c_double(0.0)
+    _load().orc_prodigy_tensor_stats(_p(hi), _p(lo), _p(_u16(g)), hi.size, int(slice_p), _p(p0), _p(s),
+                                     beta3, cs, ctypes.byref(dot), ctypes.byref(l1))
+    return dot.value, l1.value
+
+
+class ProdigyState:
+    """d and the numerator r shared by every group of a model (double)."""
+
+    def __init__(self, d0: float, beta3: float, slice_p: int):
+        self.d = ctypes.c_double(d0)
+        self.r = ctypes.c_double(0.0)
+        self.beta3 = float(np.float32(beta3))   # one fp32 beta3 for s and for r
+        self.slice_p = slice_p
+
+    def end_step(self, cdot: float, l1: float):
+        _load().orc_prodigy_end_step(ctypes.byref(self.d), ctypes.byref(self.r), float(self.beta3), cdot, l1)
+
+    @property
+    def d32(self) -> float:
+        return float(np.float32(self.d.value))
+
+
+def prodigy_step(state: ProdigyState, groups, t: int):
+    """One step of every group sharing d.  groups: list of (tensors, grads, hp) where each
+    tensor is a dict(hi, lo, shape, row, col (or V), p0, s) and hp the factored hyper-parameters
+    (mode 1; hp["d"] is ignored).  Statistics are taken before each tensor's update."""
+    d = state.d32
+    cdot, l1 = 0.0, 0.0
+    beta3 = state.beta3
+    for tensors, grads, hp in groups:
+        cr = float(np.float32(hp["lr"])) * d * d
+        cs = float(np.float32(cr))
+        dot_g = 0.0
+        for tt, g in zip(tensors, grads):
+            dt, lt = prodigy_tensor_stats(tt["hi"], tt.get("lo"), g, state.slice_p, tt["p0"], tt["s"], beta3, cs)
+            dot_g += dt
+            l1 += lt
+        cdot += cr * dot_g
+        k = factored_scalars(t, hp["lr"], hp["beta2"], hp.get("decay_rate", -0.8), hp["eps1"], hp["eps2"], d,
+                             hp["clip_threshold"], hp["weight_decay"], 1)
+        for tt, g in zip(tensors, grads):
+            fac, B, R, C = factored_dims(tt["shape"])
+            if fac:
+                factored_step_tensor(tt["hi"], tt.get("lo"), g, B, R, C, tt["row"], tt["col"], k)
+            else:
+                factored_step_vector(tt["hi"], tt.get("lo"), g, tt["col"], k)
+    state.end_step(cdot, l1)
 
 
 def factored_dims(shape):

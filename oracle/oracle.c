@@ -30,11 +30,14 @@
  *   R5  Tensors of 4096 or fewer elements keep fp32 moments (no codec).
  *   R6  Factored second moment: means of g^2+eps1 over the last dim (rows) and the second-to-last
  *       dim (columns); V^ = R C / mean(R); update clipped by max(1, RMS/clip).
+ *   R19 Prodigy's step-size estimate d over the factored step, on a sliced subsample (see the
+ *       section of that name).
  *
  * Parity pins (tests/test_oracle_*.py) tie this file to what the pages and mathematics fix:
  * exhaustive split/merge round trip, IEEE bit patterns, exhaustive codec round trip, Adam
  * step-1 = lr sign(g), NAdam step-1 closed form, torch.optim.{Adam,AdamW,NAdam,Adafactor}
- * special cases, rank-1 factored case, zero-gradient and decay-only closed forms.
+ * special cases, rank-1 factored case, zero-gradient and decay-only closed forms, Prodigy's
+ * d under a constant gradient (a scalar recurrence) and its independence of the slicing.
  */
 #include <math.h>
 #include <stdint.h>
@@ -572,12 +575,15 @@ void orc_nadam_step_fp32(float* w, float* m, float* v, const uint16_t* g, int64_
  * mode 1 (Prodigy):   q = g g, R = b2 R + d^2 (1-b2) mean_j q + eps2, C likewise
  * V^_ij = R_i C_j / mean_i(R);  u_ij = (rsqrt(R_i / mean R) rsqrt(C_j)) g_ij
  * 1-D:   V = b2t V + (1-b2t) q (mode 1: + eps2);  u = rsqrt(V) g
+ * mode 1 then takes u = u d: with beta1 = 0 Prodigy's first moment is d g, so the numerator
+ * carries d as the second moment carries d^2.
  * then   u = (u / max(1, RMS(u)/clip)) lr_eff;  w = w + w (-wd lr_eff);  w = w - u;  split.
  * lr_eff = lr in mode 0 and d lr in mode 1.
  * -------------------------------------------------------------------------------------- */
 typedef struct {
     float b2t, alpha, eps1, eps2, clip, lr_eff, nwdlr;
     int32_t mode;
+    float unum;     /* numerator factor: 1 in mode 0, d in mode 1 */
 } orc_factored_scalars_t;
 
 void orc_factored_scalars(int64_t t, float lr, float beta2, float decay_rate, float eps1,
@@ -594,10 +600,12 @@ void orc_factored_scalars(int64_t t, float lr, float beta2, float decay_rate, fl
         k->b2t = (float)beta2t;
         k->alpha = (float)(1.0 - beta2t);
         k->lr_eff = lr;
+        k->unum = 1.0f;
     } else {
         k->b2t = beta2;
         k->alpha = (float)((double)d * (double)d * (1.0 - (double)beta2));
         k->lr_eff = (float)((double)d * (double)lr);
+        k->unum = d;
     }
     k->nwdlr = (float)(-(double)wd * (double)k->lr_eff);
 }
@@ -682,6 +690,7 @@ float orc_factored_step_tensor(uint16_t* hi, uint16_t* lo, const uint16_t* g, in
             for (int64_t j = 0; j < C; ++j) {
                 float cc = rsqrt_rn(col[b * C + j]);
                 float u = (rr * cc) * bf16_to_f32(g[(b * R + i) * C + j]);
+                if (k->mode == 1) u = u * k->unum;
                 ss += (double)u * (double)u;
             }
         }
@@ -698,6 +707,7 @@ float orc_factored_step_tensor(uint16_t* hi, uint16_t* lo, const uint16_t* g, in
                 float cc = rsqrt_rn(col[b * C + j]);
                 int64_t e = (b * R + i) * C + j;
                 float u = (rr * cc) * bf16_to_f32(g[e]);
+                if (k->mode == 1) u = u * k->unum;
                 apply_update(hi, lo, e, u, den, k);
             }
         }
@@ -718,12 +728,88 @@ float orc_factored_step_vector(uint16_t* hi, uint16_t* lo, const uint16_t* g, in
         if (k->mode == 1) nv = nv + k->eps2;
         V[i] = nv;
         float u = rsqrt_rn(nv) * gg;
+        if (k->mode == 1) u = u * k->unum;
         ss += (double)u * (double)u;
     }
     float den = clip_divisor(ss, n, k->clip);
     for (int64_t i = 0; i < n; ++i) {
         float u = rsqrt_rn(V[i]) * bf16_to_f32(g[i]);
+        if (k->mode == 1) u = u * k->unum;
         apply_update(hi, lo, i, u, den, k);
     }
     return den;
+}
+
+/* ----------------------------------------------------------------------------------------
+ * R19: Prodigy's estimate of the step size d on top of the factored step (mode 1).  The pages
+ * discuss it (prodigy PR #25: d0, the numerator built from p - p0, "s, which is the denominator
+ * in the calculation of d_hat", the EMAs scaled by d) but print no formula; this follows the
+ * Adam form of Prodigy in the paper the PR belongs to (Mishchenko, Defazio, "Prodigy: An
+ * Expeditiously Adaptive Parameter-Free Learner", 2023), with beta1 = 0 and the factored second
+ * moment above.  Over every tensor of every group that shares d, at step k with d_k:
+ *     r   = beta3 r + lr d_k^2 sum_e g_e (p0_e - x_e)        (x: the master before the step)
+ *     s_e = beta3 s_e + lr d_k^2 g_e
+ *     d_{k+1} = max(d_k, r / sum_e |s_e|)                     (d unchanged while sum |s| = 0)
+ * (the paper's factor 1 - beta3 on both increments cancels in the quotient and is left out).
+ * The statistics are kept on a subsample ("sliced", prodigy PR #22, named by PR #25): of each
+ * tensor's flat elements, the 16-element blocks whose block index is a multiple of slice_p
+ * (slice_p = 1: every element).  p0 and s hold the sampled elements in order, 16 per sampled
+ * block, zero where a block runs past the tensor's end.  A step's d is the fp32 value of d_k;
+ * lr d_k^2 is formed in double from it, rounded to fp32 for s.
+ * -------------------------------------------------------------------------------------- */
+int64_t orc_prodigy_slice_len(int64_t n, int32_t slice_p)
+{
+    int64_t blocks = (n + 15) / 16;
+    return 16 * ((blocks + slice_p - 1) / slice_p);
+}
+
+static float master_of(const uint16_t* hi, const uint16_t* lo, int64_t e)
+{
+    return lo ? f_of(((uint32_t)hi[e] << 16) | lo[e]) : bf16_to_f32(hi[e]);
+}
+
+/* Flat element of sampled entry j. */
+static int64_t sampled_element(int64_t j, int32_t slice_p)
+{
+    return (j / 16) * (int64_t)slice_p * 16 + (j % 16);
+}
+
+void orc_prodigy_snapshot(const uint16_t* hi, const uint16_t* lo, int64_t n, int32_t slice_p, float* p0, float* s)
+{
+    int64_t len = orc_prodigy_slice_len(n, slice_p);
+    for (int64_t j = 0; j < len; ++j) {
+        int64_t e = sampled_element(j, slice_p);
+        p0[j] = e < n ? master_of(hi, lo, e) : 0.0f;
+        s[j] = 0.0f;
+    }
+}
+
+/* One tensor's share of a step: updates s and adds sum g (p0 - x) to *dot and sum |s| to *l1.
+ * cs = fl32(lr d_k^2). */
+void orc_prodigy_tensor_stats(const uint16_t* hi, const uint16_t* lo, const uint16_t* g, int64_t n,
+                              int32_t slice_p, const float* p0, float* s, float beta3, float cs,
+                              double* dot, double* l1)
+{
+    int64_t len = orc_prodigy_slice_len(n, slice_p);
+    for (int64_t j = 0; j < len; ++j) {
+        int64_t e = sampled_element(j, slice_p);
+        if (e >= n) continue;
+        float x = master_of(hi, lo, e);
+        float gg = bf16_to_f32(g[e]);
+        float diff = p0[j] - x;
+        *dot += (double)(gg * diff);
+        float sn = beta3 * s[j] + cs * gg;
+        s[j] = sn;
+        *l1 += (double)fabsf(sn);
+    }
+}
+
+/* End of a step over all groups: cdot = sum over groups of (lr_g d_k^2) dot_g, in double. */
+void orc_prodigy_end_step(double* d, double* r, double beta3, double cdot, double l1)
+{
+    *r = beta3 * *r + cdot;
+    if (l1 > 0.0) {
+        double dhat = *r / l1;
+        if (dhat > *d) *d = dhat;
+    }
 }
