@@ -55,8 +55,10 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="flux19")
     p.add_argument("--states", default="u16", choices=["u16", "f24"], help="moment storage of NAdam workloads")
-    p.add_argument("--optimizer", default="nadam", choices=["nadam", "adan"],
-                   help="adan: fp32 m, v, n + previous gradient, Kahan residual (38 B/param)")
+    p.add_argument("--optimizer", default="nadam", choices=["nadam", "adan", "prodigy"],
+                   help="adan: fp32 m, v, n + previous gradient, Kahan residual (38 B/param); "
+                        "prodigy (factored workloads): Prodigy mode with the step size d estimated each step")
+    p.add_argument("--slice-p", type=int, default=11, help="prodigy: statistics on every slice_p-th 64-element block")
     p.add_argument("--rounding", default="kahan", choices=["kahan", "sr"],
                    help="kahan: bf16 weight + u16 residual; sr: no residual, stochastic rounding")
     p.add_argument("--no-e2e", action="store_true")
@@ -586,9 +588,19 @@ def factored_bytes(shape):
     return 10 * n + 8 * state
 
 
+def prodigy_bytes(shape, slice_p):
+    """Algorithmic HBM bytes of one tensor's Prodigy statistics: p0 read, s read and written
+    (12 B per sampled element; the sampled weights and gradients are counted once, by the
+    factored step)."""
+    blocks = (W_numel(shape) + 63) // 64
+    return 12 * 64 * ((blocks + slice_p - 1) // slice_p)
+
+
 def run_factored(args, cfg):
     """Factored workload (sdxl_like): Adafactor mode over 1332 SDXL-UNet-like tensors in 10
-    groups, every step all group calls; reports params/s and HBM GB/s at the algorithmic bytes."""
+    groups, every step all group calls; reports params/s and HBM GB/s at the algorithmic bytes.
+    --optimizer prodigy: Prodigy mode (lr 1, beta2 0.999) with every group attached to one
+    controller, each step all group calls and the controller's end of step."""
     import torch
     from memory_lean_optimizer_gb300 import build, engine, lmopt, workloads as W
     world, rank, local = dist_info()
@@ -607,10 +619,19 @@ def run_factored(args, cfg):
         del masters
     hp = cfg["hp"]
     stream = torch.cuda.current_stream()
+    ctrl = None
+    if args.optimizer == "prodigy":
+        hp = dict(hp, mode=1, lr=1.0, beta2=0.999, eps2=1e-30)
+        ctrl = engine.ProdigyController(d0=1e-6, beta2=0.999, slice_p=args.slice_p)
+        for g in groups:
+            g.attach_prodigy(ctrl, stream)
+        nbytes += sum(prodigy_bytes(s, args.slice_p) for shapes in cfg["groups"] for s in shapes)
 
     def one_step():
         for g, gs in zip(groups, grads):
             g.step(gs, hp, stream)
+        if ctrl is not None:
+            ctrl.end_step(stream)
 
     for _ in range(args.warmup):
         one_step()
@@ -632,12 +653,17 @@ def run_factored(args, cfg):
         "warmup": args.warmup, "ms_per_step": 1e3 * step_s, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, "params": params, "groups": len(groups),
-                   "optimizer": "Adafactor factored v, beta1=0, Kahan, clip 1.0",
+                   "optimizer": ("Adafactor factored v, beta1=0, Kahan, clip 1.0" if ctrl is None else
+                                 f"Prodigy factored v, beta1=0, d estimated each step (slice_p {args.slice_p}), "
+                                 "Kahan, clip 1.0"),
                    "bytes_per_step_algorithmic": nbytes},
         "roofline": {"bound": "hbm", "kernel": "factored step (stats+final+rms+apply)", "achieved": gbs,
                      "peak": peak, "unit": "GB/s", "frac": gbs / peak, "traffic": None, "peak_source": src},
         "clocks": clk,
     }
+    if ctrl is not None:
+        result["prodigy_d"] = ctrl.get()[0]
+        ctrl.close()
     for g in groups:
         g.close()
     print(json.dumps(result), flush=True)

@@ -115,7 +115,9 @@ typedef struct {
  *          adafactor_step_param): beta2_t = 1 - t^decay_rate, eps1 added to g^2 before the means.
  *   mode 1 Prodigy ("more VRAM savings: no first moment and factored second moment",
  *          prodigy PR #25): constant beta2, EMAs weighted by d^2 (1-beta2), eps2 added after the
- *          EMA; the step size is d*lr with d fixed (no d-adaptation).
+ *          EMA; the update's numerator is d g (Prodigy's first moment with beta1 = 0) and the
+ *          step size d*lr.  d is hp->d, or, in a group attached to a Prodigy controller
+ *          (optim_group_attach_prodigy), the controller's current estimate.
  *   clip_threshold : update clipping, u /= max(1, RMS(u)/clip_threshold)
  *   weight_decay   : decoupled, w += w * (-wd * lr_eff) before the update */
 typedef struct {
@@ -198,6 +200,43 @@ int optim_step_factored(optim_group_t* group, const void* const* grads_bf16, int
  * order them on one stream.  Calls no cudaMalloc, cudaFree or other allocating routine. */
 int optim_step_factored_noalloc(const optim_tensor_desc_t* tensor, const void* grad_bf16, int64_t step,
                                 const optim_factored_hparams_t* hp, void* stream);
+
+/* ---- Prodigy's step-size estimate d over FACTORED groups (mode 1) ---------------------------
+ * The pages discuss Prodigy's d (prodigy PR #25: d0, the numerator built from p - p0, "s, which
+ * is the denominator in the calculation of d_hat", the EMAs scaled by d) without printing its
+ * update; this follows the Adam form of Prodigy (Mishchenko, Defazio, "Prodigy: An Expeditiously
+ * Adaptive Parameter-Free Learner", 2023) with beta1 = 0.  Over every tensor of every group
+ * attached to one controller, a step k with d_k (the fp32 value of the controller's d) does,
+ * before the group's update and with x the master weight before it:
+ *     r   = beta3 r + lr d_k^2 sum_e g_e (p0_e - x_e),     s_e = beta3 s_e + fl(lr d_k^2) g_e
+ * and optim_prodigy_end_step, after all attached groups have stepped, sets
+ *     d_{k+1} = max(d_k, r / sum_e |s_e|)      (unchanged while the sum is 0).
+ * The sums run over a subsample ("sliced", prodigy PR #22): the 64-element blocks of each
+ * tensor's flat elements whose block index is a multiple of slice_p (1: every element).  p0 and
+ * s hold the sampled elements in order, 64 per sampled block.  d, r and the step's partial sums
+ * live in device memory: no call of a step synchronises. */
+typedef struct optim_prodigy optim_prodigy_t;
+/* d0 > 0 (the first d), 0 <= beta3 < 1 (Prodigy's default: sqrt(beta2)), slice_p >= 1. */
+int optim_prodigy_create(double d0, float beta3, int32_t slice_p, optim_prodigy_t** out);
+/* OPTIM_ESTATE while groups are attached (destroy them first). */
+int optim_prodigy_destroy(optim_prodigy_t* pd);
+/* Floats in each of a tensor's p0 and s buffers: 64 * ceil(ceil(numel / 64) / slice_p); -1 if
+ * numel < 0 or slice_p < 1. */
+int64_t optim_prodigy_slice_len(int64_t numel, int32_t slice_p);
+/* Attaches a FACTORED group (between steps).  p0[i], s[i]: caller-owned fp32 DEVICE buffers of
+ * optim_prodigy_slice_len(numel_i, slice_p) floats, 4-byte aligned, one pair per tensor, kept
+ * alive while attached.  Enqueued on `stream`: p0 takes the current master weights at the
+ * sampled elements (0 past a tensor's end), s is zeroed.  The group's later steps must use
+ * mode 1; hp->d is then ignored.  A group attaches once. */
+int optim_group_attach_prodigy(optim_group_t* group, optim_prodigy_t* pd, void* const* p0, void* const* s,
+                               void* stream);
+/* Ends a step of the controller's groups: reduces the statistics the attached groups' steps
+ * left (in a fixed order) and updates r and d.  Enqueued on `stream`, which must be ordered after
+ * those steps (the same stream, or one that waits for them); groups not stepped add nothing. */
+int optim_prodigy_end_step(optim_prodigy_t* pd, void* stream);
+/* Current d and r (synchronises the device); set them between steps, e.g. on checkpoint resume. */
+int optim_prodigy_get(optim_prodigy_t* pd, double* d, double* r);
+int optim_prodigy_set(optim_prodigy_t* pd, double d, double r);
 
 /* Adan hyper-parameters (Algorithm 1 of the Adan paper linked by "Amazing Flux FFT quality on a
  * 5090", sd-scripts PR #2187, fourth post; beta weights the new term, as in the paper).

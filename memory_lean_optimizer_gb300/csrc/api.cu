@@ -9,6 +9,7 @@
 #include <vector>
 
 #include "group.h"
+#include "prodigy.h"
 
 namespace lmo {
 
@@ -67,6 +68,7 @@ using namespace lmo;
 static void group_free(optim_group* g) {
     if (!g) return;
     offload_unbind(g);
+    prodigy_detach(g);
     for (int s = 0; s < 2; ++s) {
         if (g->stage_ev[s]) {
             cudaEventSynchronize(g->stage_ev[s]);
@@ -397,33 +399,22 @@ int optim_step_factored(optim_group_t* g, const void* const* grads, int64_t step
     if (!finite_nonneg(hp->lr) || !(hp->clip_threshold > 0.0f) || !std::isfinite(hp->clip_threshold) ||
         !finite_nonneg(hp->weight_decay) || !finite_nonneg(hp->eps1) || !finite_nonneg(hp->eps2) ||
         (hp->mode != 0 && hp->mode != 1) || !std::isfinite(hp->decay_rate) ||
-        (hp->mode == 1 && (!(hp->beta2 >= 0.0f && hp->beta2 < 1.0f) || !finite_nonneg(hp->d))))
+        (hp->mode == 1 && (!(hp->beta2 >= 0.0f && hp->beta2 < 1.0f) || (!g->prodigy && !finite_nonneg(hp->d)))))
         return set_error(OPTIM_EINVAL, "invalid factored hyper-parameters");
+    if (g->prodigy && hp->mode != 1)
+        return set_error(OPTIM_EINVAL, "a group attached to a Prodigy controller steps in mode 1");
     int rc = check_device(g);
     if (!rc) rc = validate_grads(g, grads);
     if (rc) return rc;
 
-    const double td = (double)step;
-    FactoredScalars k{};
-    k.mode = hp->mode;
-    k.clip = hp->clip_threshold;
-    k.eps1 = hp->eps1;
-    k.eps2 = hp->eps2;
-    if (hp->mode == 0) {
-        const double beta2t = 1.0 - std::pow(td, (double)hp->decay_rate);
-        k.b2t = (float)beta2t;
-        k.alpha = (float)(1.0 - beta2t);
-        k.lr_eff = hp->lr;
-    } else {
-        k.b2t = hp->beta2;
-        k.alpha = (float)((double)hp->d * (double)hp->d * (1.0 - (double)hp->beta2));
-        k.lr_eff = (float)((double)hp->d * (double)hp->lr);
-    }
-    k.nwdlr = (float)(-(double)hp->weight_decay * (double)k.lr_eff);
-
+    FactoredScalars k = factored_scalars(hp, step, g->prodigy ? 1.0f : hp->d);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     rc = upload_grads(g, grads, s);
     if (rc) return rc;
+    if (g->prodigy) {
+        rc = prodigy_step_begin(g, hp, s, &k.kdev);
+        if (rc) return rc;
+    }
     rc = launch_factored_step(g->fplan, g->d_grads, k, s, g->profile_ev, g->d_nonfinite);
     if (rc) return rc;
     g->last_step = step;

@@ -102,7 +102,20 @@ struct Dev {
 struct K {
     float b2t, alpha, eps1, eps2, clip, lr_eff, nwdlr;
     int32_t mode;
+    float unum, lr_u;
+    const FactoredDevScalars* kdev;
 };
+// The d-dependent scalars from device memory when d is adaptive; called by every kernel right
+// after its programmatic-launch wait, so that the statistics kernel that wrote them is complete.
+__device__ __forceinline__ void load_k(K& k) {
+    if (k.kdev == nullptr) return;
+    const FactoredDevScalars v = *k.kdev;
+    k.alpha = v.alpha;
+    k.lr_eff = v.lr_eff;
+    k.nwdlr = v.nwdlr;
+    k.unum = v.unum;
+    k.lr_u = v.lr_u;
+}
 
 __device__ __forceinline__ float qval(float g, const K& k) {
     float gg = __fmul_rn(g, g);
@@ -173,7 +186,7 @@ __device__ __forceinline__ uint32_t max_bf16_mag(uint32_t nf, const uint4& W) {
 // clipped update is then fl(u * fl(lr / den)) rather than fl(fl(u / den) * lr): one multiply per
 // element instead of a division, within about one ulp of the update.
 __device__ __forceinline__ float update_scale(float den, const K& k) {
-    return den == 1.0f ? k.lr_eff : __fdiv_rn(k.lr_eff, den);
+    return den == 1.0f ? k.lr_u : __fdiv_rn(k.lr_u, den);
 }
 
 __device__ __forceinline__ void apply_elem(uint32_t& hi, uint32_t& lo, bool has_res, float u, float s, const K& k) {
@@ -191,9 +204,10 @@ __device__ __forceinline__ void apply_elem(uint32_t& hi, uint32_t& lo, bool has_
 }
 
 // Clip divisor from the tensor's fp32 sum of squares.
-__device__ __forceinline__ float clip_den(float ss, int64_t n, float clip) {
+// ss: sum of squares of the update before its numerator factor unum (1, or d in Prodigy mode).
+__device__ __forceinline__ float clip_den(float ss, int64_t n, float clip, float unum) {
     const float ms = __fdiv_rn(ss, (float)n);
-    const float r = __fdiv_rn(__fsqrt_rn(ms), clip);
+    const float r = __fdiv_rn(__fmul_rn(__fsqrt_rn(ms), unum), clip);
     return r < 1.0f ? 1.0f : r;   // a NaN RMS stays NaN (clamp(min=1) semantics), as in the oracle
 }
 
@@ -215,7 +229,7 @@ __device__ void finish_ss(const Dev& D, const FTensor& t, int tensor, int part, 
     for (int i = threadIdx.x; i < t.ss_cnt; i += blockDim.x) acc.add(__ldcg(D.ss + t.ss_off + i));
     const float tot = block_sum(acc.value(), sm);
     if (threadIdx.x == 0) {
-        D.den[tensor] = clip_den(tot, t.numel, k.clip);
+        D.den[tensor] = clip_den(tot, t.numel, k.clip, k.unum);
         D.counter[tensor] = 0u;
     }
 }
@@ -564,6 +578,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_stats(Dev D, const Item* items,
     const uint16_t* __restrict__ g = D.grads[it.tensor];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     pdl_sync();
+    load_k(k);
 
     if (it.cls == kWide) {
         float (*cols)[kTC + 1] = reinterpret_cast<float (*)[kTC + 1]>(smem);
@@ -742,6 +757,7 @@ __global__ void __launch_bounds__(kThreads) k_final(Dev D, const Item* items, K 
     const FTensor t = D.tensors[it.tensor];
     const int64_t b = it.x;
     pdl_sync();
+    load_k(k);
     if (it.cls == kFinRows) {
         // R EMA of 256 rows (one per thread), their sum, and mean(R) by the matrix's last block
         const int64_t i = (int64_t)it.cb * kFinRowsPerItem + threadIdx.x;
@@ -831,6 +847,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_rms(Dev D, const Item* items, K
                     ? __ldcg(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0)) : make_uint4(0, 0, 0, 0);
     }
     pdl_sync();
+    load_k(k);
     const float rbar = D.rbar[t.mat_off + b];
     float ccv[8];
 #pragma unroll
@@ -951,6 +968,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
             };
             load_pair(0);
             pdl_sync();
+            load_k(k);
             const float us = update_scale(D.den[it.tensor], k);
             const float2 ns2 = f2(-us), nwd2 = f2(k.nwdlr);
             const bool decay = k.nwdlr != 0.0f;
@@ -986,6 +1004,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
             }
         } else {
             pdl_sync();
+            load_k(k);
             const float us = update_scale(D.den[it.tensor], k);
             float ccv[8];
 #pragma unroll
@@ -1010,6 +1029,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
         return;
     }
     pdl_sync();
+    load_k(k);
     const float us = update_scale(D.den[it.tensor], k);
     if (it.cls == kTiny) {
         // as in k_stats: sub-batches staged through shared memory, double-buffered when whole
@@ -1328,9 +1348,33 @@ static cudaError_t launch_pdl(Kern kern, int grid, cudaStream_t st, Args... args
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+FactoredScalars factored_scalars(const optim_factored_hparams_t* hp, int64_t step, float d) {
+    FactoredScalars k{};
+    k.mode = hp->mode;
+    k.clip = hp->clip_threshold;
+    k.eps1 = hp->eps1;
+    k.eps2 = hp->eps2;
+    if (hp->mode == 0) {
+        const double beta2t = 1.0 - std::pow((double)step, (double)hp->decay_rate);
+        k.b2t = (float)beta2t;
+        k.alpha = (float)(1.0 - beta2t);
+        k.lr_eff = hp->lr;
+        k.unum = 1.0f;
+    } else {
+        k.b2t = hp->beta2;
+        k.alpha = (float)((double)d * (double)d * (1.0 - (double)hp->beta2));
+        k.lr_eff = (float)((double)d * (double)hp->lr);
+        k.unum = d;
+    }
+    k.nwdlr = (float)(-(double)hp->weight_decay * (double)k.lr_eff);
+    k.lr_u = (float)((double)k.lr_eff * (double)k.unum);
+    k.kdev = nullptr;
+    return k;
+}
+
 int launch_factored_step(const FactoredPlan* p, const uint16_t* const* d_grads, const FactoredScalars& s,
                          cudaStream_t stream, cudaEvent_t mid, unsigned long long* nonfinite) {
-    K k{s.b2t, s.alpha, s.eps1, s.eps2, s.clip, s.lr_eff, s.nwdlr, s.mode};
+    K k{s.b2t, s.alpha, s.eps1, s.eps2, s.clip, s.lr_eff, s.nwdlr, s.mode, s.unum, s.lr_u, s.kdev};
     Dev D = p->dev;
     D.grads = d_grads;
     D.nonfinite = nonfinite;
@@ -1454,23 +1498,7 @@ extern "C" int optim_step_factored_noalloc(const optim_tensor_desc_t* tensor, co
     char* sb = static_cast<char*>(base);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    const double td = (double)step;
-    FactoredScalars k{};
-    k.mode = hp->mode;
-    k.clip = hp->clip_threshold;
-    k.eps1 = hp->eps1;
-    k.eps2 = hp->eps2;
-    if (hp->mode == 0) {
-        const double beta2t = 1.0 - std::pow(td, (double)hp->decay_rate);
-        k.b2t = (float)beta2t;
-        k.alpha = (float)(1.0 - beta2t);
-        k.lr_eff = hp->lr;
-    } else {
-        k.b2t = hp->beta2;
-        k.alpha = (float)((double)hp->d * (double)hp->d * (1.0 - (double)hp->beta2));
-        k.lr_eff = (float)((double)hp->d * (double)hp->lr);
-    }
-    k.nwdlr = (float)(-(double)hp->weight_decay * (double)k.lr_eff);
+    const FactoredScalars k = factored_scalars(hp, step, hp->d);
 
     // tables (pageable host memory: staged by the runtime before the call returns), counters
     // cleared because the previous call's contents stay in the shared array

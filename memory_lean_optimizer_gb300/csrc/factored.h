@@ -7,11 +7,25 @@
 
 namespace lmo {
 
-// Per-step scalars (host-computed: double, then one rounding to fp32).
+// The scalars of a Prodigy-mode step that depend on d, when d lives in device memory (written
+// each step by the Prodigy statistics kernel before the factored kernels read it).
+struct FactoredDevScalars {
+    float alpha, lr_eff, nwdlr, unum, lr_u;
+};
+
+// Per-step scalars (host-computed: double, then one rounding to fp32).  unum: the update's
+// numerator factor (1 for Adafactor, d for Prodigy); lr_u = fl(lr_eff unum).  kdev (may be
+// null): device copy of the d-dependent scalars, which then replace the host values.
 struct FactoredScalars {
     float b2t, alpha, eps1, eps2, clip, lr_eff, nwdlr;
     int32_t mode;
+    float unum, lr_u;
+    const FactoredDevScalars* kdev;
 };
+
+// The scalars of a step with hyper-parameters hp at step `step` with step size d (hp->d unless
+// a Prodigy controller supplies it).
+FactoredScalars factored_scalars(const optim_factored_hparams_t* hp, int64_t step, float d);
 
 struct FactoredPlan;
 int factored_plan_build(FactoredPlan*& plan, const std::vector<optim_tensor_desc_t>& desc);

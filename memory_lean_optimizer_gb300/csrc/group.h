@@ -8,6 +8,7 @@
 
 namespace lmo {
 struct OffloadBinding;
+struct ProdigyAttach;
 // Bounded host wait: polls the event until it completes or `timeout_s` passes (OPTIM_ETIMEOUT).
 int wait_event(cudaEvent_t ev, double timeout_s, const char* what);
 constexpr double kWaitTimeout = 120.0;
@@ -42,6 +43,7 @@ struct optim_group {
     cudaStream_t last_stream = nullptr;
     cudaEvent_t profile_ev = nullptr;
     lmo::OffloadBinding* offload = nullptr;   // non-NULL: res/m/v are pinned host buffers
+    lmo::ProdigyAttach* prodigy = nullptr;    // non-NULL: d comes from a Prodigy controller
     // a NAdam step begun (pre-pass enqueued) and not yet ended
     bool pending = false;
     int64_t pending_step = 0;

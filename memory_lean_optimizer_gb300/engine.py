@@ -277,6 +277,54 @@ class FactoredGroup(_Group):
     def masters(self):
         return [kahan_merge(w, r) for w, r in zip(self.weights, self.res)]
 
+    def attach_prodigy(self, ctrl: "ProdigyController", stream=None):
+        """Shares d with every other group of `ctrl`: allocates the sampled p0 / s buffers,
+        snapshots the current weights into p0; later steps use mode 1 with the controller's d."""
+        dev = self.weights[0].device
+        p0, s = [], []
+        for w in self.weights:
+            n = lmopt.optim_prodigy_slice_len(w.numel(), ctrl.slice_p)
+            p0.append(torch.zeros(max(n, 1), dtype=torch.float32, device=dev))
+            s.append(torch.zeros(max(n, 1), dtype=torch.float32, device=dev))
+        lmopt.optim_group_attach_prodigy(self.handle, ctrl.handle, [t.data_ptr() for t in p0],
+                                         [t.data_ptr() for t in s], _stream_ptr(stream))
+        self.p0, self.s = p0, s     # kept alive while attached
+        ctrl.groups.append(self)
+
+
+class ProdigyController:
+    """Prodigy's step-size estimate d shared by the FACTORED groups attached to it: step every
+    group (mode 1), then call end_step() once."""
+
+    def __init__(self, d0: float = 1e-6, beta3: float | None = None, beta2: float = 0.999, slice_p: int = 11):
+        self.slice_p = slice_p
+        self.beta3 = float(beta3) if beta3 is not None else float(beta2) ** 0.5
+        self.handle = lmopt.optim_prodigy_create(d0, self.beta3, slice_p)
+        self.groups = []
+
+    def end_step(self, stream=None):
+        lmopt.optim_prodigy_end_step(self.handle, _stream_ptr(stream))
+
+    def get(self):
+        return lmopt.optim_prodigy_get(self.handle)
+
+    def set(self, d: float, r: float):
+        lmopt.optim_prodigy_set(self.handle, d, r)
+
+    def close(self):
+        if self.handle:
+            for g in self.groups:
+                g.close()
+            self.groups = []
+            lmopt.optim_prodigy_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
 
 class AdanGroup(_Group):
     """Adan state (fp32 m, v, n planes and the previous bf16 gradient) for a list of bf16 weights."""

@@ -39,6 +39,8 @@ EXPORTED = (
     "optim_step_factored_noalloc", "optim_step_adan",
     "optim_offload_create", "optim_offload_destroy", "optim_group_attach_offload",
     "optim_offload_prefetch", "optim_offload_sync", "optim_step_nadam_begin", "optim_step_nadam_end",
+    "optim_prodigy_create", "optim_prodigy_destroy", "optim_prodigy_slice_len", "optim_group_attach_prodigy",
+    "optim_prodigy_end_step", "optim_prodigy_get", "optim_prodigy_set",
 )
 
 
@@ -112,11 +114,19 @@ def load(path: str = LIB_PATH):
             "optim_group_attach_offload": [P, P],
             "optim_offload_prefetch": [P],
             "optim_offload_sync": [P, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)],
+            "optim_prodigy_create": [ctypes.c_double, F, I32, ctypes.POINTER(P)],
+            "optim_prodigy_destroy": [P],
+            "optim_group_attach_prodigy": [P, P, P, P, P],
+            "optim_prodigy_end_step": [P, P],
+            "optim_prodigy_get": [P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)],
+            "optim_prodigy_set": [P, ctypes.c_double, ctypes.c_double],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
             fn.argtypes = args
             fn.restype = ctypes.c_int
+        lib.optim_prodigy_slice_len.argtypes = [I64, I32]
+        lib.optim_prodigy_slice_len.restype = I64
         lib.optim_last_error.argtypes = []
         lib.optim_last_error.restype = ctypes.c_char_p
         _lib = lib
@@ -256,3 +266,39 @@ def optim_offload_sync(engine: int):
     a, b = ctypes.c_uint64(), ctypes.c_uint64()
     check(load().optim_offload_sync(engine, ctypes.byref(a), ctypes.byref(b)))
     return a.value, b.value
+
+
+def optim_prodigy_create(d0: float, beta3: float, slice_p: int) -> int:
+    out = ctypes.c_void_p()
+    check(load().optim_prodigy_create(d0, beta3, slice_p, ctypes.byref(out)))
+    return out.value
+
+
+def optim_prodigy_destroy(pd: int) -> None:
+    check(load().optim_prodigy_destroy(pd))
+
+
+def optim_prodigy_slice_len(numel: int, slice_p: int) -> int:
+    return int(load().optim_prodigy_slice_len(numel, slice_p))
+
+
+def optim_group_attach_prodigy(handle: int, pd: int, p0_ptrs, s_ptrs, stream: int = 0) -> None:
+    n = len(p0_ptrs)
+    a = (ctypes.c_void_p * max(n, 1))(*p0_ptrs)
+    b = (ctypes.c_void_p * max(n, 1))(*s_ptrs)
+    check(load().optim_group_attach_prodigy(handle, pd, a, b, stream))
+
+
+def optim_prodigy_end_step(pd: int, stream: int = 0) -> None:
+    check(load().optim_prodigy_end_step(pd, stream))
+
+
+def optim_prodigy_get(pd: int):
+    """(d, r) of the controller (synchronises the device)."""
+    d, r = ctypes.c_double(), ctypes.c_double()
+    check(load().optim_prodigy_get(pd, ctypes.byref(d), ctypes.byref(r)))
+    return d.value, r.value
+
+
+def optim_prodigy_set(pd: int, d: float, r: float) -> None:
+    check(load().optim_prodigy_set(pd, d, r))

@@ -401,8 +401,9 @@ class ProdigyState:
 
 def prodigy_step(state: ProdigyState, groups, t: int):
     """One step of every group sharing d.  groups: list of (tensors, grads, hp) where each
-    tensor is a dict(hi, lo, shape, row, col (or V), p0, s) and hp the factored hyper-parameters
-    (mode 1; hp["d"] is ignored).  Statistics are taken before each tensor's update."""
+    tensor is a dict(hi, lo, shape, row, col or V, p0, s) as for factored_group_step and hp the
+    factored hyper-parameters (mode 1; hp["d"] is ignored).  Statistics are taken before each
+    tensor's update."""
     d = state.d32
     cdot, l1 = 0.0, 0.0
     beta3 = state.beta3
@@ -415,14 +416,7 @@ def prodigy_step(state: ProdigyState, groups, t: int):
             dot_g += dt
             l1 += lt
         cdot += cr * dot_g
-        k = factored_scalars(t, hp["lr"], hp["beta2"], hp.get("decay_rate", -0.8), hp["eps1"], hp["eps2"], d,
-                             hp["clip_threshold"], hp["weight_decay"], 1)
-        for tt, g in zip(tensors, grads):
-            fac, B, R, C = factored_dims(tt["shape"])
-            if fac:
-                factored_step_tensor(tt["hi"], tt.get("lo"), g, B, R, C, tt["row"], tt["col"], k)
-            else:
-                factored_step_vector(tt["hi"], tt.get("lo"), g, tt["col"], k)
+        factored_group_step(tensors, grads, t, dict(hp, d=d, mode=1, decay_rate=hp.get("decay_rate", -0.8)))
     state.end_step(cdot, l1)
 
 

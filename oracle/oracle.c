@@ -752,15 +752,16 @@ float orc_factored_step_vector(uint16_t* hi, uint16_t* lo, const uint16_t* g, in
  *     d_{k+1} = max(d_k, r / sum_e |s_e|)                     (d unchanged while sum |s| = 0)
  * (the paper's factor 1 - beta3 on both increments cancels in the quotient and is left out).
  * The statistics are kept on a subsample ("sliced", prodigy PR #22, named by PR #25): of each
- * tensor's flat elements, the 16-element blocks whose block index is a multiple of slice_p
- * (slice_p = 1: every element).  p0 and s hold the sampled elements in order, 16 per sampled
- * block, zero where a block runs past the tensor's end.  A step's d is the fp32 value of d_k;
+ * tensor's flat elements, the 64-element blocks whose block index is a multiple of slice_p
+ * (slice_p = 1: every element; a block of 64 bf16 values is one 128-byte line).  p0 and s hold
+ * the sampled elements in order, 64 per sampled block, zero where a block runs past the
+ * tensor's end.  A step's d is the fp32 value of d_k;
  * lr d_k^2 is formed in double from it, rounded to fp32 for s.
  * -------------------------------------------------------------------------------------- */
 int64_t orc_prodigy_slice_len(int64_t n, int32_t slice_p)
 {
-    int64_t blocks = (n + 15) / 16;
-    return 16 * ((blocks + slice_p - 1) / slice_p);
+    int64_t blocks = (n + 63) / 64;
+    return 64 * ((blocks + slice_p - 1) / slice_p);
 }
 
 static float master_of(const uint16_t* hi, const uint16_t* lo, int64_t e)
@@ -771,7 +772,7 @@ static float master_of(const uint16_t* hi, const uint16_t* lo, int64_t e)
 /* Flat element of sampled entry j. */
 static int64_t sampled_element(int64_t j, int32_t slice_p)
 {
-    return (j / 16) * (int64_t)slice_p * 16 + (j % 16);
+    return (j / 64) * (int64_t)slice_p * 64 + (j % 64);
 }
 
 void orc_prodigy_snapshot(const uint16_t* hi, const uint16_t* lo, int64_t n, int32_t slice_p, float* p0, float* s)

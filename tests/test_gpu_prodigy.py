@@ -1,0 +1,157 @@
+"""GPU parity of Prodigy's step-size estimate d over FACTORED groups (mode 1) against the oracle,
+through the C ABI: two groups sharing one controller, mixed tensor classes (wide matrices, batched
+matrices, 3x3 convolutions, vectors), sliced and unsliced statistics.
+
+Tolerances, derived from the arithmetic:
+  s (sampled denominators) : the same fp32 operations per element, with fl(lr d_k^2) from d_k:
+                             1e-5 of the tensor's largest |s| (see the check)
+  d                        : 1e-5 relative.  Both sides sum the same fp32 terms; the oracle in
+                             double in element order, the kernels in fp32 over 32 terms per thread
+                             and double beyond (a few fp32 roundings of the partial sums), and the
+                             weights they were computed from carry the factored step's own
+                             ~1e-6 differences.
+  fp32 masters             : |w - w_ref| <= 1e-6 |w_ref| + 2e-5 * sum_k lr d_k  (the update is
+                             lr d_k per step; a 1e-5-relative difference in d_k, plus the factored
+                             step's 1e-6)
+"""
+import numpy as np
+import pytest
+import torch
+
+from memory_lean_optimizer_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+HP = dict(beta2=0.99, decay_rate=-0.8, eps1=1e-30, eps2=1e-30, d=1.0, clip_threshold=1.0, weight_decay=0.0,
+          mode=1)
+GROUPS = [[(64, 80), (3, 40, 72), (8, 8, 3, 3), (300,), (45, 50, 3, 3)],
+          [(1000, 640), (600, 2, 2), (77,), (5000,)]]
+
+
+@pytest.fixture(scope="module")
+def eng():
+    from memory_lean_optimizer_gb300 import build, engine
+    build.build()
+    return engine
+
+
+def oracle_tensor(orc, x, shape, slice_p):
+    x = np.ascontiguousarray(x, np.float32).reshape(-1)
+    hi, lo = orc.kahan_split(x)
+    fac, B, R, C = orc.factored_dims(shape)
+    t = dict(hi=hi, lo=lo, shape=shape)
+    if fac:
+        t["row"] = np.zeros(B * R, np.float32)
+        t["col"] = np.zeros(B * C, np.float32)
+    else:
+        t["V"] = np.zeros(x.size, np.float32)
+    t["p0"], t["s"] = orc.prodigy_snapshot(hi, lo, slice_p)
+    return t
+
+
+def run(orc, eng, slice_p, steps, hps, d0=1e-4, seed=70):
+    beta3 = float(np.float32(np.sqrt(0.99)))
+    st = orc.ProdigyState(d0, beta3, slice_p)
+    ctrl = eng.ProdigyController(d0=d0, beta3=beta3, slice_p=slice_p)
+    ora, grps, bias = [], [], []
+    tid = 0
+    for shapes in GROUPS:
+        masters = [W.master_weights(s, seed, tid + i) for i, s in enumerate(shapes)]
+        ora.append([oracle_tensor(orc, m.numpy(), s, slice_p) for m, s in zip(masters, shapes)])
+        grp = eng.FactoredGroup.from_masters([m.cuda() for m in masters])
+        grp.attach_prodigy(ctrl)
+        grps.append(grp)
+        bias.append([W.grad_bf16(s, seed + 1, tid + i, 0, 1e-3).float() for i, s in enumerate(shapes)])
+        tid += len(shapes)
+    ds, ds_ref, lrd = [], [], 0.0
+    for t in range(1, steps + 1):
+        step_groups = []
+        tid = 0
+        for gi, shapes in enumerate(GROUPS):
+            # a persistent component makes the displacement correlate with the gradients, so d grows
+            grads = [(bias[gi][i] + W.grad_bf16(s, seed, tid + i, t, 3e-4).float()).to(torch.bfloat16)
+                     for i, s in enumerate(shapes)]
+            tid += len(shapes)
+            step_groups.append(([W.bits16(g).reshape(-1) for g in grads], grads))
+        lrd += max(h["lr"] for h in hps) * st.d32
+        orc.prodigy_step(st, [(ora[gi], step_groups[gi][0], hps[gi]) for gi in range(len(GROUPS))], t)
+        for gi, grp in enumerate(grps):
+            grp.step([g.cuda() for g in step_groups[gi][1]], hps[gi])
+        ctrl.end_step()
+        ds.append(ctrl.get()[0])
+        ds_ref.append(st.d.value)
+    torch.cuda.synchronize()
+    return ora, grps, ctrl, ds, ds_ref, lrd
+
+
+def check(orc, ora, grps, ds, ds_ref, lrd):
+    assert np.allclose(ds, ds_ref, rtol=1e-5, atol=0), (ds, ds_ref)
+    from memory_lean_optimizer_gb300 import lmopt
+    for og, grp in zip(ora, grps):
+        masters = grp.masters()
+        for i, ot in enumerate(og):
+            ref = orc.kahan_merge(ot["hi"], ot["lo"]).astype(np.float64)
+            got = masters[i].cpu().numpy().reshape(-1).astype(np.float64)
+            tol = 1e-6 * np.abs(ref) + 2e-5 * lrd
+            bad = np.abs(got - ref) > tol
+            assert not bad.any(), f"{ot['shape']}: {bad.sum()} masters out of tolerance"
+            assert np.array_equal(grp.p0[i][:ot["p0"].size].cpu().numpy().view(np.uint32), ot["p0"].view(np.uint32))
+            # s = sum_j beta3^(k-j) fl(lr d_j^2) g_j: a 1e-5-relative difference in d_j moves it by
+            # up to 1e-5 of the sum of the terms' magnitudes, which cancellation can leave far
+            # above |s| itself; bounded here by the tensor's largest |s|
+            s_got = grp.s[i][:ot["s"].size].cpu().numpy().astype(np.float64)
+            s_ref = ot["s"].astype(np.float64)
+            err = np.abs(s_got - s_ref)
+            assert np.all(err <= 1e-5 * np.abs(s_ref) + 1e-5 * np.abs(s_ref).max()), \
+                f"{ot['shape']}: s differs (max error {err.max():.3e}, max |s| {np.abs(s_ref).max():.3e})"
+        assert lmopt.optim_query_nonfinite(grp.handle) == 0
+
+
+@pytest.mark.parametrize("slice_p", [1, 3, 11])
+def test_prodigy_d_adaptation_parity(orc, eng, slice_p):
+    hps = [dict(HP, lr=1.0), dict(HP, lr=0.5, weight_decay=0.01)]
+    ora, grps, ctrl, ds, ds_ref, lrd = run(orc, eng, slice_p, 8, hps)
+    assert ds_ref[0] == 1e-4 and ds_ref[-1] > 2e-4          # d grows within the run
+    check(orc, ora, grps, ds, ds_ref, lrd)
+    ctrl.close()
+
+
+def test_prodigy_checkpoint_resume(orc, eng):
+    """d and r read back after a run equal the last step's d; set() writes both exactly (the
+    checkpoint-restore path) and get() reads them back."""
+    hps = [dict(HP, lr=1.0), dict(HP, lr=0.5)]
+    ora, grps, ctrl, ds, ds_ref, lrd = run(orc, eng, 3, 4, hps)
+    d, r = ctrl.get()
+    assert d == ds[-1]
+    ctrl.set(d * 2.0, r)
+    assert ctrl.get() == (d * 2.0, r)
+    ctrl.set(d, r)
+    assert ctrl.get() == (d, r)
+    ctrl.close()
+
+
+def test_prodigy_api_errors(eng):
+    from memory_lean_optimizer_gb300 import lmopt
+    with pytest.raises(lmopt.LmoptError):
+        lmopt.optim_prodigy_create(0.0, 0.9, 1)
+    with pytest.raises(lmopt.LmoptError):
+        lmopt.optim_prodigy_create(1e-6, 1.0, 1)
+    with pytest.raises(lmopt.LmoptError):
+        lmopt.optim_prodigy_create(1e-6, 0.9, 0)
+    assert lmopt.optim_prodigy_slice_len(400, 3) == 192 and lmopt.optim_prodigy_slice_len(-1, 3) == -1
+    ctrl = eng.ProdigyController(d0=1e-6, slice_p=4)
+    grp = eng.FactoredGroup.from_masters([torch.randn(64, 32, device="cuda") * 0.02])
+    grp.attach_prodigy(ctrl)
+    with pytest.raises(lmopt.LmoptError) as e:          # destroy while a group is attached
+        lmopt.optim_prodigy_destroy(ctrl.handle)
+    assert e.value.code == lmopt.OPTIM_ESTATE
+    g = [torch.zeros(64, 32, dtype=torch.bfloat16, device="cuda")]
+    with pytest.raises(lmopt.LmoptError):                # attached groups step in mode 1
+        grp.step(g, dict(HP, lr=1.0, mode=0))
+    with pytest.raises(lmopt.LmoptError) as e:           # attaches once
+        grp.attach_prodigy(ctrl)
+    assert e.value.code == lmopt.OPTIM_ESTATE
+    grp.step(g, dict(HP, lr=1.0))
+    ctrl.end_step()
+    assert ctrl.get()[0] == 1e-6                          # zero gradients: s stays 0, d unchanged
+    ctrl.close()

@@ -12,7 +12,7 @@ HP = dict(lr=1.0, beta2=0.99, decay_rate=-0.8, eps1=1e-30, eps2=0.0, clip_thresh
 def vector_tensor(orc, x0, slice_p):
     hi, lo = orc.kahan_split(np.asarray(x0, np.float32))
     p0, s = orc.prodigy_snapshot(hi, lo, slice_p)
-    return dict(hi=hi, lo=lo, shape=(x0.size,), row=None, col=np.zeros(x0.size, np.float32), p0=p0, s=s)
+    return dict(hi=hi, lo=lo, shape=(x0.size,), V=np.zeros(x0.size, np.float32), p0=p0, s=s)
 
 
 def test_numerator_carries_d(orc):
@@ -34,16 +34,16 @@ def test_numerator_carries_d(orc):
 
 
 def test_snapshot_layout(orc):
-    """n = 100, slice_p = 3: blocks 0, 3, 6 (elements 0-15, 48-63, 96-99) in order, 16 entries
-    per block, zero past the end; s starts at zero."""
-    x = (np.arange(100, dtype=np.float32) + 1) * np.float32(0.25)
+    """n = 400, slice_p = 3: blocks 0, 3, 6 (elements 0-63, 192-255, 384-399) in order, 64
+    entries per block, zero past the end; s starts at zero."""
+    x = (np.arange(400, dtype=np.float32) + 1) * np.float32(0.25)
     hi, lo = orc.kahan_split(x)
     p0, s = orc.prodigy_snapshot(hi, lo, 3)
-    assert orc.prodigy_slice_len(100, 3) == 48 and p0.size == 48
-    assert np.array_equal(p0[:16], x[:16]) and np.array_equal(p0[16:32], x[48:64])
-    assert np.array_equal(p0[32:36], x[96:100]) and not p0[36:].any() and not s.any()
-    assert orc.prodigy_slice_len(0, 5) == 0 and orc.prodigy_slice_len(16, 1) == 16
-    assert orc.prodigy_slice_len(17, 1) == 32 and orc.prodigy_slice_len(160, 11) == 16
+    assert orc.prodigy_slice_len(400, 3) == 192 and p0.size == 192
+    assert np.array_equal(p0[:64], x[:64]) and np.array_equal(p0[64:128], x[192:256])
+    assert np.array_equal(p0[128:144], x[384:400]) and not p0[144:].any() and not s.any()
+    assert orc.prodigy_slice_len(0, 5) == 0 and orc.prodigy_slice_len(64, 1) == 64
+    assert orc.prodigy_slice_len(65, 1) == 128 and orc.prodigy_slice_len(640, 11) == 64
 
 
 def test_constant_gradient_recurrence(orc):
@@ -78,10 +78,10 @@ def test_constant_gradient_recurrence(orc):
 
 
 def test_d_independent_of_slicing_for_alike_blocks(orc):
-    """When every 16-element block of a tensor holds the same values (weights and gradients),
+    """When every 64-element block of a tensor holds the same values (weights and gradients),
     each sampled block contributes the same to both sums, so d does not depend on slice_p."""
     rng = np.random.default_rng(61)
-    nb = 30
+    nb = 120                                 # 16-periodic values: 30 alike 64-element blocks
     x0 = np.tile((rng.standard_normal(16) * 0.02).astype(np.float32), nb)
     bias = rng.standard_normal(16) * 1e-3
     grads = [np.tile(bf16_bits(bias + rng.standard_normal(16) * 2e-4), nb) for _ in range(8)]
@@ -112,6 +112,7 @@ def test_d_monotone_and_first_step(orc):
         t = vector_tensor(orc, x0, 3)
         t["shape"] = shp
         if len(shp) == 2:
+            del t["V"]
             t["row"] = np.zeros(shp[0], np.float32)
             t["col"] = np.zeros(shp[1], np.float32)
         groups.append(([t], rng.standard_normal(n) * 1e-3, dict(HP, lr=0.3 + 0.2 * i)))
