@@ -234,6 +234,13 @@ int optim_group_attach_prodigy(optim_group_t* group, optim_prodigy_t* pd, void* 
  * left (in a fixed order) and updates r and d.  Enqueued on `stream`, which must be ordered after
  * those steps (the same stream, or one that waits for them); groups not stepped add nothing. */
 int optim_prodigy_end_step(optim_prodigy_t* pd, void* stream);
+/* The same in two halves, for data-parallel processes that each step their own groups and share
+ * one d: reduce writes this process's sums (sum over its groups of lr d^2 sum g (p0 - x), and
+ * sum |s|) as 2 doubles to `partial` (DEVICE, 8-byte aligned) and clears the statistics; the
+ * caller SUM-reduces the 2 doubles across processes (e.g. an all-reduce) and passes the totals
+ * to finish, which updates r and d the same way on every process.  Both enqueued on `stream`. */
+int optim_prodigy_reduce(optim_prodigy_t* pd, double* partial, void* stream);
+int optim_prodigy_finish(optim_prodigy_t* pd, const double* total, void* stream);
 /* Current d and r (synchronises the device); set them between steps, e.g. on checkpoint resume. */
 int optim_prodigy_get(optim_prodigy_t* pd, double* d, double* r);
 int optim_prodigy_set(optim_prodigy_t* pd, double d, double r);

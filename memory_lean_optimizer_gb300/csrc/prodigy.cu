@@ -211,8 +211,8 @@ __global__ void __launch_bounds__(kPdThreads) k_pd_stats(const PdTensor* T, cons
     if (threadIdx.x == 0) slots[blockIdx.x] = make_double2(cr * bd, bl);
 }
 
-// One CTA: sums every slot in a fixed order, clears them, updates r and d.
-__global__ void __launch_bounds__(kPdEndThreads) k_pd_end(PdState* st, double2* slots, int64_t n, double beta3) {
+// One CTA: sums every slot in a fixed order into out = (sum lr d^2 dot, sum |s|) and clears them.
+__global__ void __launch_bounds__(kPdEndThreads) k_pd_reduce(double2* slots, int64_t n, double* out) {
     __shared__ double sm[kPdEndThreads / 32];
     double a = 0.0, b = 0.0;
     for (int64_t i = threadIdx.x; i < n; i += kPdEndThreads) {
@@ -224,15 +224,21 @@ __global__ void __launch_bounds__(kPdEndThreads) k_pd_end(PdState* st, double2* 
     const double cdot = block_sum_f64<kPdEndThreads>(a, sm);
     const double l1 = block_sum_f64<kPdEndThreads>(b, sm);
     if (threadIdx.x == 0) {
-        const double r = beta3 * st->r + cdot;
-        double d = st->d;
-        if (l1 > 0.0) {
-            const double dhat = r / l1;
-            if (dhat > d) d = dhat;
-        }
-        st->r = r;
-        st->d = d;
+        out[0] = cdot;
+        out[1] = l1;
     }
+}
+
+// One thread: r and d from the step's totals.
+__global__ void k_pd_finish(PdState* st, const double* total, double beta3) {
+    const double r = beta3 * st->r + total[0];
+    double d = st->d;
+    if (total[1] > 0.0) {
+        const double dhat = r / total[1];
+        if (dhat > d) d = dhat;
+    }
+    st->r = r;
+    st->d = d;
 }
 
 }  // namespace
@@ -255,6 +261,7 @@ struct optim_prodigy {
     float beta3 = 0.f;
     int32_t slice_p = 1;
     lmo::PdState* d_state = nullptr;
+    double* d_total = nullptr;   // this process's sums of a step (end_step's reduce/finish buffer)
     double2* d_slots = nullptr;
     int64_t n_slots = 0;
     int32_t attached = 0;
@@ -304,7 +311,8 @@ int optim_prodigy_create(double d0, float beta3, int32_t slice_p, optim_prodigy_
     pd->beta3 = beta3;
     pd->slice_p = slice_p;
     int rc = check_cuda(cudaGetDevice(&pd->device), "cudaGetDevice");
-    if (!rc && cudaMalloc(reinterpret_cast<void**>(&pd->d_state), sizeof(PdState)) != cudaSuccess) {
+    if (!rc && (cudaMalloc(reinterpret_cast<void**>(&pd->d_state), sizeof(PdState)) != cudaSuccess ||
+                cudaMalloc(reinterpret_cast<void**>(&pd->d_total), 2 * sizeof(double)) != cudaSuccess)) {
         cudaGetLastError();
         rc = set_error(OPTIM_ENOMEM, "prodigy state allocation failed");
     }
@@ -314,6 +322,7 @@ int optim_prodigy_create(double d0, float beta3, int32_t slice_p, optim_prodigy_
     }
     if (rc) {
         cudaFree(pd->d_state);
+        cudaFree(pd->d_total);
         delete pd;
         return rc;
     }
@@ -325,6 +334,7 @@ int optim_prodigy_destroy(optim_prodigy_t* pd) {
     if (!pd) return set_error(OPTIM_EINVAL, "controller is NULL");
     if (pd->attached > 0) return set_error(OPTIM_ESTATE, "%d groups are still attached", pd->attached);
     cudaFree(pd->d_state);
+    cudaFree(pd->d_total);
     cudaFree(pd->d_slots);
     delete pd;
     return OPTIM_OK;
@@ -407,12 +417,27 @@ int optim_group_attach_prodigy(optim_group_t* g, optim_prodigy_t* pd, void* cons
     return OPTIM_OK;
 }
 
+int optim_prodigy_reduce(optim_prodigy_t* pd, double* partial, void* stream) {
+    if (!pd || !partial) return set_error(OPTIM_EINVAL, "controller or partial is NULL");
+    if (!is_aligned(partial, 8)) return set_error(OPTIM_EALIGN, "partial must be 8-byte aligned");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (pd->n_slots == 0) return check_cuda(cudaMemsetAsync(partial, 0, 2 * sizeof(double), st), "partial clear");
+    k_pd_reduce<<<1, kPdEndThreads, 0, st>>>(pd->d_slots, pd->n_slots, partial);
+    return check_cuda(cudaGetLastError(), "prodigy reduce launch");
+}
+
+int optim_prodigy_finish(optim_prodigy_t* pd, const double* total, void* stream) {
+    if (!pd || !total) return set_error(OPTIM_EINVAL, "controller or total is NULL");
+    if (!is_aligned(total, 8)) return set_error(OPTIM_EALIGN, "total must be 8-byte aligned");
+    k_pd_finish<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(pd->d_state, total, (double)pd->beta3);
+    return check_cuda(cudaGetLastError(), "prodigy finish launch");
+}
+
 int optim_prodigy_end_step(optim_prodigy_t* pd, void* stream) {
     if (!pd) return set_error(OPTIM_EINVAL, "controller is NULL");
-    if (pd->n_slots == 0) return OPTIM_OK;
-    k_pd_end<<<1, kPdEndThreads, 0, static_cast<cudaStream_t>(stream)>>>(pd->d_state, pd->d_slots, pd->n_slots,
-                                                                        (double)pd->beta3);
-    return check_cuda(cudaGetLastError(), "prodigy end-of-step launch");
+    int rc = optim_prodigy_reduce(pd, pd->d_total, stream);
+    if (!rc) rc = optim_prodigy_finish(pd, pd->d_total, stream);
+    return rc;
 }
 
 int optim_prodigy_get(optim_prodigy_t* pd, double* d, double* r) {

@@ -302,8 +302,19 @@ class ProdigyController:
         self.handle = lmopt.optim_prodigy_create(d0, self.beta3, slice_p)
         self.groups = []
 
-    def end_step(self, stream=None):
-        lmopt.optim_prodigy_end_step(self.handle, _stream_ptr(stream))
+    def end_step(self, stream=None, all_reduce_sum=None):
+        """After every attached group stepped.  With data-parallel processes that share d, pass
+        all_reduce_sum (a callable SUM-reducing a float64 device tensor in place, e.g.
+        torch.distributed.all_reduce): this process's two sums are reduced across processes
+        before d is updated."""
+        if all_reduce_sum is None:
+            lmopt.optim_prodigy_end_step(self.handle, _stream_ptr(stream))
+            return
+        dev = self.groups[0].weights[0].device if self.groups else torch.device("cuda")
+        buf = torch.empty(2, dtype=torch.float64, device=dev)
+        lmopt.optim_prodigy_reduce(self.handle, buf.data_ptr(), _stream_ptr(stream))
+        all_reduce_sum(buf)
+        lmopt.optim_prodigy_finish(self.handle, buf.data_ptr(), _stream_ptr(stream))
 
     def get(self):
         return lmopt.optim_prodigy_get(self.handle)

@@ -40,7 +40,8 @@ EXPORTED = (
     "optim_offload_create", "optim_offload_destroy", "optim_group_attach_offload",
     "optim_offload_prefetch", "optim_offload_sync", "optim_step_nadam_begin", "optim_step_nadam_end",
     "optim_prodigy_create", "optim_prodigy_destroy", "optim_prodigy_slice_len", "optim_group_attach_prodigy",
-    "optim_prodigy_end_step", "optim_prodigy_get", "optim_prodigy_set",
+    "optim_prodigy_end_step", "optim_prodigy_get", "optim_prodigy_set", "optim_prodigy_reduce",
+    "optim_prodigy_finish",
 )
 
 
@@ -118,6 +119,8 @@ def load(path: str = LIB_PATH):
             "optim_prodigy_destroy": [P],
             "optim_group_attach_prodigy": [P, P, P, P, P],
             "optim_prodigy_end_step": [P, P],
+            "optim_prodigy_reduce": [P, P, P],
+            "optim_prodigy_finish": [P, P, P],
             "optim_prodigy_get": [P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)],
             "optim_prodigy_set": [P, ctypes.c_double, ctypes.c_double],
         }
@@ -291,6 +294,14 @@ def optim_group_attach_prodigy(handle: int, pd: int, p0_ptrs, s_ptrs, stream: in
 
 def optim_prodigy_end_step(pd: int, stream: int = 0) -> None:
     check(load().optim_prodigy_end_step(pd, stream))
+
+
+def optim_prodigy_reduce(pd: int, partial_ptr: int, stream: int = 0) -> None:
+    check(load().optim_prodigy_reduce(pd, partial_ptr, stream))
+
+
+def optim_prodigy_finish(pd: int, total_ptr: int, stream: int = 0) -> None:
+    check(load().optim_prodigy_finish(pd, total_ptr, stream))
 
 
 def optim_prodigy_get(pd: int):

@@ -400,9 +400,16 @@ class ProdigyState:
 
 
 def prodigy_step(state: ProdigyState, groups, t: int):
-    """One step of every group sharing d.  groups: list of (tensors, grads, hp) where each
-    tensor is a dict(hi, lo, shape, row, col or V, p0, s) as for factored_group_step and hp the
-    factored hyper-parameters (mode 1; hp["d"] is ignored).  Statistics are taken before each
+    """One step of every group sharing d: prodigy_partials, then the end of the step."""
+    cdot, l1 = prodigy_partials(state, groups, t)
+    state.end_step(cdot, l1)
+
+
+def prodigy_partials(state: ProdigyState, groups, t: int):
+    """Steps every group with the current d and returns this caller's sums (sum over groups of
+    lr d^2 dot, sum |s|) without ending the step.  groups: list of (tensors, grads, hp) where
+    each tensor is a dict(hi, lo, shape, row, col or V, p0, s) as for factored_group_step and hp
+    the factored hyper-parameters (mode 1; hp["d"] is ignored).  Statistics are taken before each
     tensor's update."""
     d = state.d32
     cdot, l1 = 0.0, 0.0
@@ -417,7 +424,7 @@ def prodigy_step(state: ProdigyState, groups, t: int):
             l1 += lt
         cdot += cr * dot_g
         factored_group_step(tensors, grads, t, dict(hp, d=d, mode=1, decay_rate=hp.get("decay_rate", -0.8)))
-    state.end_step(cdot, l1)
+    return cdot, l1
 
 
 def factored_dims(shape):

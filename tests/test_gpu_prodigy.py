@@ -155,3 +155,50 @@ def test_prodigy_api_errors(eng):
     ctrl.end_step()
     assert ctrl.get()[0] == 1e-6                          # zero gradients: s stays 0, d unchanged
     ctrl.close()
+
+
+def test_two_ranks_share_d_through_reduce_finish(orc, eng):
+    """Two controllers (as two data-parallel ranks on one GPU, stepped one after the other), one
+    group each: their reduce() sums are added and passed to both finish() calls, so both hold the
+    same d, which follows the oracle stepping both groups under one d."""
+    from memory_lean_optimizer_gb300 import lmopt
+    slice_p, d0, seed = 3, 1e-4, 71
+    hps = [dict(HP, lr=1.0), dict(HP, lr=0.5)]
+    beta3 = float(np.float32(np.sqrt(0.99)))
+    st = orc.ProdigyState(d0, beta3, slice_p)
+    ctrls = [eng.ProdigyController(d0=d0, beta3=beta3, slice_p=slice_p) for _ in GROUPS]
+    ora, grps, bias = [], [], []
+    tid = 0
+    for gi, shapes in enumerate(GROUPS):
+        masters = [W.master_weights(s, seed, tid + i) for i, s in enumerate(shapes)]
+        ora.append([oracle_tensor(orc, m.numpy(), s, slice_p) for m, s in zip(masters, shapes)])
+        grp = eng.FactoredGroup.from_masters([m.cuda() for m in masters])
+        grp.attach_prodigy(ctrls[gi])
+        grps.append(grp)
+        bias.append([W.grad_bf16(s, seed + 1, tid + i, 0, 1e-3).float() for i, s in enumerate(shapes)])
+        tid += len(shapes)
+    for t in range(1, 9):
+        step_groups = []
+        tid = 0
+        for gi, shapes in enumerate(GROUPS):
+            grads = [(bias[gi][i] + W.grad_bf16(s, seed, tid + i, t, 3e-4).float()).to(torch.bfloat16)
+                     for i, s in enumerate(shapes)]
+            tid += len(shapes)
+            step_groups.append(grads)
+        orc.prodigy_step(st, [(ora[gi], [W.bits16(g).reshape(-1) for g in step_groups[gi]], hps[gi])
+                              for gi in range(len(GROUPS))], t)
+        parts = []
+        for gi, grp in enumerate(grps):
+            grp.step([g.cuda() for g in step_groups[gi]], hps[gi])
+            buf = torch.empty(2, dtype=torch.float64, device="cuda")
+            lmopt.optim_prodigy_reduce(ctrls[gi].handle, buf.data_ptr(), 0)
+            parts.append(buf)
+        total = parts[0] + parts[1]
+        for c in ctrls:
+            lmopt.optim_prodigy_finish(c.handle, total.data_ptr(), 0)
+        da, db = ctrls[0].get()[0], ctrls[1].get()[0]
+        assert da == db
+        assert abs(da - st.d.value) <= 1e-5 * st.d.value, (t, da, st.d.value)
+    assert st.d.value > 2 * d0
+    for c in ctrls:
+        c.close()

@@ -198,3 +198,94 @@ def test_two_rank_split_tensors_match_unsplit(orc):
             assert np.array_equal(v.view(np.uint8), rt["v"][a:b].view(np.uint8)), (rank, ti)
             seen += b - a
     assert seen == sum(SPLIT_SIZES)
+
+
+# ---------------------------------------------------------------- Prodigy's d shared by ranks
+PD_SHAPES = [[(40, 70), (333,)], [(3, 20, 16)], [(500,), (24, 24)]]
+PD_HP = dict(beta2=0.99, decay_rate=-0.8, eps1=1e-30, eps2=1e-30, clip_threshold=1.0, weight_decay=0.0)
+
+
+def _pd_groups(orc, gis, slice_p):
+    groups = []
+    for gi in gis:
+        ts = []
+        for i, shp in enumerate(PD_SHAPES[gi]):
+            hi, lo = orc.kahan_split(_inputs(50 + gi, i, shp).reshape(-1))
+            fac, B, R, C = orc.factored_dims(shp)
+            t = dict(hi=hi, lo=lo, shape=shp)
+            if fac:
+                t["row"], t["col"] = np.zeros(B * R, np.float32), np.zeros(B * C, np.float32)
+            else:
+                t["V"] = np.zeros(hi.size, np.float32)
+            t["p0"], t["s"] = orc.prodigy_snapshot(hi, lo, slice_p)
+            ts.append(t)
+        groups.append((gi, ts))
+    return groups
+
+
+def _pd_grads(gi, i, shp, t):
+    rng = np.random.default_rng(7000 + 100 * gi + i)
+    bias = rng.standard_normal(shp) * 1e-3
+    noise = np.random.default_rng(9000 + 100 * gi + 10 * i + t).standard_normal(shp) * 3e-4
+    g = (bias + noise).astype(np.float32).reshape(-1)
+    return torch.from_numpy(g).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _pd_step_args(groups, t):
+    return [(ts, [_pd_grads(gi, i, tt["shape"], t) for i, tt in enumerate(ts)], dict(PD_HP, lr=0.5 + 0.25 * gi))
+            for gi, ts in groups]
+
+
+def _pd_worker(rank, world, port, q):
+    import sys
+    sys.path.insert(0, os.path.dirname(__file__))
+    import oracle as orc
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    sizes = [sum(int(np.prod(s)) for s in g) for g in PD_SHAPES]
+    st = orc.ProdigyState(1e-4, 0.995, 3)
+    groups = _pd_groups(orc, my_groups(sizes, rank, world), 3)
+    ds = []
+    for t in range(1, 9):
+        cdot, l1 = orc.prodigy_partials(st, _pd_step_args(groups, t), t)
+        buf = torch.tensor([cdot, l1], dtype=torch.float64)
+        dist.all_reduce(buf, op=dist.ReduceOp.SUM)
+        st.end_step(float(buf[0]), float(buf[1]))
+        ds.append(st.d.value)
+    q.put((rank, ds, {gi: [orc.kahan_merge(t["hi"], t["lo"]).copy() for t in ts] for gi, ts in groups}))
+    dist.destroy_process_group()
+
+
+def test_two_rank_prodigy_d_matches_single_process(orc):
+    """Whole groups on 2 gloo ranks sharing one d: each rank's two sums are SUM-reduced before
+    d is updated, so both ranks hold the same d at every step, equal (to double rounding of the
+    regrouped sums) to one process stepping every group, and the same weights."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_pd_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    results = []
+    for _ in procs:
+        try:
+            results.append(q.get(timeout=180))
+        except Exception:
+            break
+    assert len(results) == 2, f"worker exit codes {[p.exitcode for p in procs]}"
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    st = orc.ProdigyState(1e-4, 0.995, 3)
+    groups = _pd_groups(orc, range(len(PD_SHAPES)), 3)
+    ref = []
+    for t in range(1, 9):
+        orc.prodigy_step(st, _pd_step_args(groups, t), t)
+        ref.append(st.d.value)
+    (r0, d0, w0), (r1, d1, w1) = sorted(results, key=lambda x: x[0])
+    assert d0 == d1 and d0[-1] > 1e-4
+    assert np.allclose(d0, ref, rtol=1e-12, atol=0)
+    for gi, ts in groups:
+        got = w0.get(gi, w1.get(gi))
+        for i, t in enumerate(ts):
+            assert np.allclose(got[i], orc.kahan_merge(t["hi"], t["lo"]), rtol=1e-6, atol=1e-9)
