@@ -225,11 +225,13 @@ int optim_prodigy_destroy(optim_prodigy_t* pd);
 int64_t optim_prodigy_slice_len(int64_t numel, int32_t slice_p);
 /* Attaches a FACTORED group (between steps).  p0[i], s[i]: caller-owned fp32 DEVICE buffers of
  * optim_prodigy_slice_len(numel_i, slice_p) floats, 4-byte aligned, one pair per tensor, kept
- * alive while attached.  Enqueued on `stream`: p0 takes the current master weights at the
- * sampled elements (0 past a tensor's end), s is zeroed.  The group's later steps must use
- * mode 1; hp->d is then ignored.  A group attaches once. */
+ * alive while attached.  snapshot = 1: enqueued on `stream`, p0 takes the current master
+ * weights at the sampled elements (0 past a tensor's end) and s is zeroed (the start of
+ * training); snapshot = 0: the buffers are used as they are (resuming from a checkpoint that
+ * saved them).  The group's later steps must use mode 1; hp->d is then ignored.  A group
+ * attaches once. */
 int optim_group_attach_prodigy(optim_group_t* group, optim_prodigy_t* pd, void* const* p0, void* const* s,
-                               void* stream);
+                               int32_t snapshot, void* stream);
 /* Ends a step of the controller's groups: reduces the statistics the attached groups' steps
  * left (in a fixed order) and updates r and d.  Enqueued on `stream`, which must be ordered after
  * those steps (the same stream, or one that waits for them); groups not stepped add nothing. */

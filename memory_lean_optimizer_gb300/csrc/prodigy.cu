@@ -340,8 +340,10 @@ int optim_prodigy_destroy(optim_prodigy_t* pd) {
     return OPTIM_OK;
 }
 
-int optim_group_attach_prodigy(optim_group_t* g, optim_prodigy_t* pd, void* const* p0, void* const* s, void* stream) {
+int optim_group_attach_prodigy(optim_group_t* g, optim_prodigy_t* pd, void* const* p0, void* const* s,
+                               int32_t snapshot, void* stream) {
     if (!g || !pd || !p0 || !s) return set_error(OPTIM_EINVAL, "group, controller, p0 or s is NULL");
+    if (snapshot != 0 && snapshot != 1) return set_error(OPTIM_EINVAL, "snapshot must be 0 or 1");
     if (g->kind != OPTIM_KIND_FACTORED) return set_error(OPTIM_EINVAL, "not a FACTORED group");
     if (g->prodigy) return set_error(OPTIM_ESTATE, "group is already attached to a controller");
     int dev = -1;
@@ -400,7 +402,7 @@ int optim_group_attach_prodigy(optim_group_t* g, optim_prodigy_t* pd, void* cons
         return fail(rc);
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (a->n_items > 0) {
+    if (snapshot && a->n_items > 0) {
         k_pd_snapshot<<<(unsigned)a->n_items, kPdThreads, 0, st>>>(a->d_tensors, a->d_items, pd->slice_p);
         rc = check_cuda(cudaGetLastError(), "prodigy snapshot launch");
         if (rc) {

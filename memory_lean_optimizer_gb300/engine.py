@@ -277,17 +277,25 @@ class FactoredGroup(_Group):
     def masters(self):
         return [kahan_merge(w, r) for w, r in zip(self.weights, self.res)]
 
-    def attach_prodigy(self, ctrl: "ProdigyController", stream=None):
-        """Shares d with every other group of `ctrl`: allocates the sampled p0 / s buffers,
-        snapshots the current weights into p0; later steps use mode 1 with the controller's d."""
+    def attach_prodigy(self, ctrl: "ProdigyController", stream=None, p0=None, s=None):
+        """Shares d with every other group of `ctrl`: allocates the sampled p0 / s buffers and
+        snapshots the current weights into p0, or (p0 and s given, e.g. from a checkpoint)
+        takes copies of them as they are; later steps use mode 1 with the controller's d."""
         dev = self.weights[0].device
+        restore = p0 is not None
+        src_p0, src_s = p0, s
         p0, s = [], []
-        for w in self.weights:
+        for i, w in enumerate(self.weights):
             n = lmopt.optim_prodigy_slice_len(w.numel(), ctrl.slice_p)
-            p0.append(torch.zeros(max(n, 1), dtype=torch.float32, device=dev))
-            s.append(torch.zeros(max(n, 1), dtype=torch.float32, device=dev))
+            if restore:
+                assert src_p0[i].numel() == max(n, 1) and src_s[i].numel() == max(n, 1)
+                p0.append(src_p0[i].to(dev, torch.float32).clone())
+                s.append(src_s[i].to(dev, torch.float32).clone())
+            else:
+                p0.append(torch.zeros(max(n, 1), dtype=torch.float32, device=dev))
+                s.append(torch.zeros(max(n, 1), dtype=torch.float32, device=dev))
         lmopt.optim_group_attach_prodigy(self.handle, ctrl.handle, [t.data_ptr() for t in p0],
-                                         [t.data_ptr() for t in s], _stream_ptr(stream))
+                                         [t.data_ptr() for t in s], 0 if restore else 1, _stream_ptr(stream))
         self.p0, self.s = p0, s     # kept alive while attached
         ctrl.groups.append(self)
 

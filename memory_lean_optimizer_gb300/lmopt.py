@@ -117,7 +117,7 @@ def load(path: str = LIB_PATH):
             "optim_offload_sync": [P, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)],
             "optim_prodigy_create": [ctypes.c_double, F, I32, ctypes.POINTER(P)],
             "optim_prodigy_destroy": [P],
-            "optim_group_attach_prodigy": [P, P, P, P, P],
+            "optim_group_attach_prodigy": [P, P, P, P, I32, P],
             "optim_prodigy_end_step": [P, P],
             "optim_prodigy_reduce": [P, P, P],
             "optim_prodigy_finish": [P, P, P],
@@ -285,11 +285,11 @@ def optim_prodigy_slice_len(numel: int, slice_p: int) -> int:
     return int(load().optim_prodigy_slice_len(numel, slice_p))
 
 
-def optim_group_attach_prodigy(handle: int, pd: int, p0_ptrs, s_ptrs, stream: int = 0) -> None:
+def optim_group_attach_prodigy(handle: int, pd: int, p0_ptrs, s_ptrs, snapshot: int = 1, stream: int = 0) -> None:
     n = len(p0_ptrs)
     a = (ctypes.c_void_p * max(n, 1))(*p0_ptrs)
     b = (ctypes.c_void_p * max(n, 1))(*s_ptrs)
-    check(load().optim_group_attach_prodigy(handle, pd, a, b, stream))
+    check(load().optim_group_attach_prodigy(handle, pd, a, b, int(snapshot), stream))
 
 
 def optim_prodigy_end_step(pd: int, stream: int = 0) -> None:

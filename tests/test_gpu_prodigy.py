@@ -116,17 +116,72 @@ def test_prodigy_d_adaptation_parity(orc, eng, slice_p):
     ctrl.close()
 
 
-def test_prodigy_checkpoint_resume(orc, eng):
-    """d and r read back after a run equal the last step's d; set() writes both exactly (the
-    checkpoint-restore path) and get() reads them back."""
-    hps = [dict(HP, lr=1.0), dict(HP, lr=0.5)]
-    ora, grps, ctrl, ds, ds_ref, lrd = run(orc, eng, 3, 4, hps)
+def _pd_grads(shapes, gi, tid0, t, seed):
+    bias = [W.grad_bf16(s, seed + 1, tid0 + i, 0, 1e-3).float() for i, s in enumerate(shapes)]
+    return [(bias[i] + W.grad_bf16(s, seed, tid0 + i, t, 3e-4).float()).to(torch.bfloat16).cuda()
+            for i, s in enumerate(shapes)]
+
+
+def _pd_build(eng, slice_p, d0, beta3, seed):
+    ctrl = eng.ProdigyController(d0=d0, beta3=beta3, slice_p=slice_p)
+    grps, tid = [], 0
+    for shapes in GROUPS:
+        masters = [W.master_weights(s, seed, tid + i) for i, s in enumerate(shapes)]
+        grp = eng.FactoredGroup.from_masters([m.cuda() for m in masters])
+        grp.attach_prodigy(ctrl)
+        grps.append(grp)
+        tid += len(shapes)
+    return ctrl, grps
+
+
+def _pd_steps(ctrl, grps, hps, t0, t1, seed):
+    for t in range(t0, t1 + 1):
+        tid = 0
+        for gi, (shapes, grp) in enumerate(zip(GROUPS, grps)):
+            grp.step(_pd_grads(shapes, gi, tid, t, seed), hps[gi])
+            tid += len(shapes)
+        ctrl.end_step()
+
+
+def test_prodigy_checkpoint_resume_bit_identical(orc, eng):
+    """k steps, save (weights, residuals, R and C or V, p0, s, d, r, step), restore into new groups
+    and a new controller attached without a snapshot: N-k more steps equal N uninterrupted steps
+    bit for bit (every reduction on this path has a fixed order)."""
+    from memory_lean_optimizer_gb300 import lmopt
+    slice_p, d0, seed, N, k = 3, 1e-4, 72, 8, 4
+    hps = [dict(HP, lr=1.0), dict(HP, lr=0.5, weight_decay=0.01)]
+    beta3 = float(np.float32(np.sqrt(0.99)))
+    ctrl, grps = _pd_build(eng, slice_p, d0, beta3, seed)
+    _pd_steps(ctrl, grps, hps, 1, N, seed)
+    ref = [[(w.clone(), r.clone()) for w, r in zip(g.weights, g.res)] for g in grps]
+    d_ref = ctrl.get()
+    ctrl.close()
+
+    ctrl, grps = _pd_build(eng, slice_p, d0, beta3, seed)
+    _pd_steps(ctrl, grps, hps, 1, k, seed)
+    saved = [dict(w=[w.clone() for w in g.weights], res=[r.clone() for r in g.res],
+                  row=[x.clone() if x is not None else None for x in g.row], col=[x.clone() for x in g.col],
+                  p0=[x.clone() for x in g.p0], s=[x.clone() for x in g.s]) for g in grps]
     d, r = ctrl.get()
-    assert d == ds[-1]
-    ctrl.set(d * 2.0, r)
-    assert ctrl.get() == (d * 2.0, r)
+    ctrl.close()
+
+    ctrl = eng.ProdigyController(d0=d0, beta3=beta3, slice_p=slice_p)
     ctrl.set(d, r)
-    assert ctrl.get() == (d, r)
+    grps = []
+    for sv in saved:
+        grp = eng.FactoredGroup(sv["w"], sv["res"])
+        for dst, src in zip(grp.row + grp.col, sv["row"] + sv["col"]):
+            if dst is not None:
+                dst.copy_(src)
+        lmopt.optim_group_set_step(grp.handle, k, 1.0)
+        grp.step_count = k
+        grp.attach_prodigy(ctrl, p0=sv["p0"], s=sv["s"])
+        grps.append(grp)
+    _pd_steps(ctrl, grps, hps, k + 1, N, seed)
+    assert ctrl.get() == d_ref
+    for g, rg in zip(grps, ref):
+        for w, r, (w0, r0) in zip(g.weights, g.res, rg):
+            assert torch.equal(w, w0) and torch.equal(r, r0)
     ctrl.close()
 
 
