@@ -35,6 +35,16 @@ def my_groups(sizes: Sequence[int], rank: int, world: int) -> list[int]:
     return [gi for gi, r in enumerate(assign_groups(sizes, world)) if r == rank]
 
 
+def my_tensors(sizes: Sequence[int], rank: int, world: int) -> list[int]:
+    """Whole tensors (not groups) onto ranks, largest first onto the least-loaded rank: the
+    sharding of factored workloads, whose step couples the elements of a tensor (row and column
+    means, the RMS clip) but nothing across tensors.  Each rank builds its own groups from its
+    tensors; no exchange is needed on the data path.  With many tensors of equal size (the SDXL-like
+    workload: 1332 tensors) the ranks end up balanced to within a fraction of a percent, where
+    whole groups of 1/10 of the model would not be."""
+    return [ti for ti, r in enumerate(assign_groups(sizes, world)) if r == rank]
+
+
 def replicate_weights(weights_by_group: Sequence[Sequence], owner: Sequence[int], group=None) -> None:
     """After a sharded step: each group's owner broadcasts its updated bf16 weights so that every
     rank holds the same replica (2 bytes per parameter on the wire)."""
