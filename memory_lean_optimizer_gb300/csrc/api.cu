@@ -411,11 +411,19 @@ int optim_step_factored(optim_group_t* g, const void* const* grads, int64_t step
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     rc = upload_grads(g, grads, s);
     if (rc) return rc;
+    cudaEvent_t apply_wait = nullptr;
     if (g->prodigy) {
-        rc = prodigy_step_begin(g, hp, s, &k.kdev);
-        if (rc) return rc;
+        rc = prodigy_step_begin(g, hp, s, &k.kdev, &apply_wait);
+        if (rc) {
+            prodigy_step_join(g, s);
+            return rc;
+        }
     }
-    rc = launch_factored_step(g->fplan, g->d_grads, k, s, g->profile_ev, g->d_nonfinite);
+    rc = launch_factored_step(g->fplan, g->d_grads, k, s, g->profile_ev, g->d_nonfinite, apply_wait);
+    if (g->prodigy) {
+        const int r2 = prodigy_step_join(g, s);
+        if (!rc) rc = r2;
+    }
     if (rc) return rc;
     g->last_step = step;
     g->last_stream = s;

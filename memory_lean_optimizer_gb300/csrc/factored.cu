@@ -1373,7 +1373,7 @@ FactoredScalars factored_scalars(const optim_factored_hparams_t* hp, int64_t ste
 }
 
 int launch_factored_step(const FactoredPlan* p, const uint16_t* const* d_grads, const FactoredScalars& s,
-                         cudaStream_t stream, cudaEvent_t mid, unsigned long long* nonfinite) {
+                         cudaStream_t stream, cudaEvent_t mid, unsigned long long* nonfinite, cudaEvent_t apply_wait) {
     K k{s.b2t, s.alpha, s.eps1, s.eps2, s.clip, s.lr_eff, s.nwdlr, s.mode, s.unum, s.lr_u, s.kdev};
     Dev D = p->dev;
     D.grads = d_grads;
@@ -1394,6 +1394,8 @@ int launch_factored_step(const FactoredPlan* p, const uint16_t* const* d_grads, 
         if (!rc && wv.n_fin > 0) rc = check_cuda(launch_pdl(k_final, wv.n_fin, st, D, fin, k), "factored finalize launch");
         if (!rc && wv.n_wide > 0) rc = check_cuda(launch_pdl(k_rms, wv.n_wide, st, D, items, k), "factored rms launch");
         if (!rc && mid && w + 1 == p->waves.size()) rc = check_cuda(cudaEventRecord(mid, st), "profile event");
+        // the first update on each stream waits for apply_wait; later ones follow it on the stream
+        if (!rc && apply_wait && (int)w < ns) rc = check_cuda(cudaStreamWaitEvent(st, apply_wait, 0), "apply wait");
         if (!rc && wv.n_total > 0) rc = check_cuda(launch_pdl(k_apply, wv.n_total, st, D, items, k), "factored apply launch");
     }
     // join every internal stream back into the caller's (also after a launch error, so that no
@@ -1529,5 +1531,6 @@ extern "C" int optim_step_factored_noalloc(const optim_tensor_desc_t* tensor, co
     D.ss = reinterpret_cast<float*>(sb + o_ss);
     D.den = reinterpret_cast<float*>(sb + o_den);
     D.counter = reinterpret_cast<unsigned*>(sb + o_counter);
-    return launch_factored_step(&plan, reinterpret_cast<const uint16_t* const*>(sb + o_grad), k, s, nullptr, nullptr);
+    return launch_factored_step(&plan, reinterpret_cast<const uint16_t* const*>(sb + o_grad), k, s, nullptr, nullptr,
+                                nullptr);
 }

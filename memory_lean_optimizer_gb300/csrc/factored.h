@@ -31,7 +31,10 @@ struct FactoredPlan;
 int factored_plan_build(FactoredPlan*& plan, const std::vector<optim_tensor_desc_t>& desc);
 void factored_plan_free(FactoredPlan*& plan);
 // `nonfinite` (may be null): counter of update CTAs that stored a non-finite weight.
+// `apply_wait` (may be null): an event that every update kernel of the step waits for (work
+// that must read the weights before they change).
 int launch_factored_step(const FactoredPlan* plan, const uint16_t* const* d_grads,
-                         const FactoredScalars& k, cudaStream_t s, cudaEvent_t mid, unsigned long long* nonfinite);
+                         const FactoredScalars& k, cudaStream_t s, cudaEvent_t mid, unsigned long long* nonfinite,
+                         cudaEvent_t apply_wait);
 
 }  // namespace lmo

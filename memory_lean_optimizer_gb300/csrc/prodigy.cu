@@ -12,9 +12,10 @@
 // Sampled elements: the 64-element blocks of a tensor's flat elements whose block index is a
 // multiple of slice_p; p0 and s hold them in order, 64 per sampled block.
 //
-// Work per step: one statistics kernel per group call (before the group's factored kernels; it
-// also writes the group's d-dependent scalars, which those kernels read after their
-// programmatic-launch wait) and one one-CTA reduction per controller step.  The statistics
+// Work per step, per group call: a one-thread kernel writing the group's d-dependent scalars (read
+// by the factored kernels after their programmatic-launch wait), and the statistics kernel on
+// the group's own stream, concurrent with the factored kernels until their update kernels, which
+// wait for it (it reads the weights they overwrite); per controller step, a one-CTA reduction.  The statistics
 // touch 1/slice_p of the weights and gradients (whole 128-byte lines: 64 bf16 per block) and
 // read/write p0 and s (12 bytes per sampled element).  Sums: fp32 over a thread's 32 entries of
 // an item, compensated fp32 over its items, double across threads, CTAs and groups, each in a
@@ -33,7 +34,12 @@ constexpr int kPdThreads = 256;
 constexpr int kPdPerThread = 32;
 constexpr int64_t kPdPerCta = (int64_t)kPdThreads * kPdPerThread;   // sampled entries per CTA
 constexpr int kPdEndThreads = 1024;
-constexpr int kPdCtasPerSm = 4;      // resident statistics CTAs per SM (persistent grid)
+// Statistics CTAs per SM (persistent grid).  A sparse sample (slice_p >= 4) is a small share of
+// the step and runs beside the factored kernels up to their update, so it takes one CTA per SM
+// and leaves them room (sdxl_like, slice_p 11: 6.87 ms per step against 6.98 with four); a dense
+// one is as large as the step itself and takes four (slice_p 1: 13.0 against 14.7 ms with one).
+constexpr int kPdCtasPerSmSparse = 1;
+constexpr int kPdCtasPerSmDense = 4;
 
 struct PdTensor {
     const uint16_t* w;
@@ -106,6 +112,19 @@ __device__ __forceinline__ void pd_entry(float x, float gg, float p0, float& s, 
     l1 = __fadd_rn(l1, fabsf(s));
 }
 
+// One thread: the group's d-dependent scalars of the step, the same values as the host scalars
+// of a mode-1 step with d = fl32(d).
+__global__ void k_pd_scalars(const PdState* st, PdStep p, FactoredDevScalars* kdev) {
+    const float df = (float)st->d;
+    FactoredDevScalars v;
+    v.alpha = (float)((double)df * (double)df * (1.0 - (double)p.beta2));
+    v.lr_eff = (float)((double)df * (double)p.lr);
+    v.nwdlr = (float)(-(double)p.wd * (double)v.lr_eff);
+    v.unum = df;
+    v.lr_u = (float)((double)v.lr_eff * (double)df);
+    *kdev = v;
+}
+
 // Neumaier-compensated fp32 accumulation (a thread's sum over its items).
 struct PdComp {
     float s = 0.f, c = 0.f;
@@ -161,25 +180,14 @@ __device__ __forceinline__ void pd_scalar8(const PdTensor& t, const uint16_t* __
 // taking groups of 8 consecutive entries (8 consecutive elements of one sampled block) with
 // 128-bit loads when every buffer is 16-byte aligned, element by element otherwise and at a
 // tensor's end.  A thread sums each item's 32 entries in fp32 and its items with compensation;
-// one block reduction (double) per CTA.  Block 0 also writes the group's d-dependent scalars.
-// slot[b]: (lr d^2 * dot, l1) of CTA b.
+// one block reduction (double) per CTA.  slot[b]: (lr d^2 * dot, l1) of CTA b.
 __global__ void __launch_bounds__(kPdThreads) k_pd_stats(const PdTensor* T, const PdItem* items,
                                                          const uint16_t* const* grads, const PdState* st,
-                                                         PdStep p, double2* slots, FactoredDevScalars* kdev) {
+                                                         PdStep p, double2* slots) {
     __shared__ double sm[kPdThreads / 32];
     const float df = (float)st->d;
     const double cr = ((double)p.lr * (double)df) * (double)df;
     const float cs = (float)cr;
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        // the same values as the host scalars of a mode-1 step with d = df
-        FactoredDevScalars v;
-        v.alpha = (float)((double)df * (double)df * (1.0 - (double)p.beta2));
-        v.lr_eff = (float)((double)df * (double)p.lr);
-        v.nwdlr = (float)(-(double)p.wd * (double)v.lr_eff);
-        v.unum = df;
-        v.lr_u = (float)((double)v.lr_eff * (double)df);
-        *kdev = v;
-    }
     PdComp cdot, cl1;
     for (int b = blockIdx.x; b < p.n_items; b += gridDim.x) {
         const PdItem it = items[b];
@@ -249,6 +257,8 @@ struct ProdigyAttach {
     PdItem* d_items = nullptr;
     FactoredDevScalars* d_kdev = nullptr;
     int32_t n_items = 0;
+    cudaStream_t stream = nullptr;     // the statistics kernel's own stream
+    cudaEvent_t start_ev = nullptr, done_ev = nullptr;
     int64_t slot_off = 0;
     int64_t n_slots = 0;   // CTAs of the statistics kernel (persistent grid, at least 1)
 };
@@ -275,6 +285,10 @@ void prodigy_detach(optim_group* g) {
     ProdigyAttach* a = g->prodigy;
     if (!a) return;
     if (a->pd) a->pd->attached -= 1;
+    if (a->stream) cudaStreamSynchronize(a->stream);
+    if (a->start_ev) cudaEventDestroy(a->start_ev);
+    if (a->done_ev) cudaEventDestroy(a->done_ev);
+    if (a->stream) cudaStreamDestroy(a->stream);
     cudaFree(a->d_tensors);
     cudaFree(a->d_items);
     cudaFree(a->d_kdev);
@@ -283,14 +297,27 @@ void prodigy_detach(optim_group* g) {
 }
 
 int prodigy_step_begin(optim_group* g, const optim_factored_hparams_t* hp, cudaStream_t s,
-                       const FactoredDevScalars** kdev) {
+                       const FactoredDevScalars** kdev, cudaEvent_t* done) {
     ProdigyAttach* a = g->prodigy;
     optim_prodigy* pd = a->pd;
     PdStep p{hp->lr, hp->beta2, hp->weight_decay, pd->beta3, pd->slice_p, a->n_items};
-    k_pd_stats<<<(unsigned)a->n_slots, kPdThreads, 0, s>>>(a->d_tensors, a->d_items, g->d_grads, pd->d_state, p,
-                                                           pd->d_slots + a->slot_off, a->d_kdev);
+    k_pd_scalars<<<1, 1, 0, s>>>(pd->d_state, p, a->d_kdev);
+    int rc = check_cuda(cudaGetLastError(), "prodigy scalars launch");
+    if (!rc) rc = check_cuda(cudaEventRecord(a->start_ev, s), "prodigy fork");
+    if (!rc) rc = check_cuda(cudaStreamWaitEvent(a->stream, a->start_ev, 0), "prodigy fork");
+    if (rc) return rc;
+    k_pd_stats<<<(unsigned)a->n_slots, kPdThreads, 0, a->stream>>>(a->d_tensors, a->d_items, g->d_grads, pd->d_state,
+                                                                   p, pd->d_slots + a->slot_off);
+    rc = check_cuda(cudaGetLastError(), "prodigy statistics launch");
+    // recorded even after a failed launch, so that waiting on it never waits on a stale step
+    const int r2 = check_cuda(cudaEventRecord(a->done_ev, a->stream), "prodigy statistics event");
     *kdev = a->d_kdev;
-    return check_cuda(cudaGetLastError(), "prodigy statistics launch");
+    *done = a->done_ev;
+    return rc ? rc : r2;
+}
+
+int prodigy_step_join(optim_group* g, cudaStream_t s) {
+    return check_cuda(cudaStreamWaitEvent(s, g->prodigy->done_ev, 0), "prodigy join");
 }
 
 }  // namespace lmo
@@ -367,9 +394,13 @@ int optim_group_attach_prodigy(optim_group_t* g, optim_prodigy_t* pd, void* cons
     ProdigyAttach* a = new ProdigyAttach();
     a->pd = pd;
     a->n_items = (int32_t)items.size();
-    const int64_t grid = std::min<int64_t>(a->n_items, (int64_t)kPdCtasPerSm * sm_count());
+    const int per_sm = pd->slice_p >= 4 ? kPdCtasPerSmSparse : kPdCtasPerSmDense;
+    const int64_t grid = std::min<int64_t>(a->n_items, (int64_t)per_sm * sm_count());
     a->n_slots = grid > 0 ? grid : 1;
     auto fail = [&](int code) {
+        if (a->start_ev) cudaEventDestroy(a->start_ev);
+        if (a->done_ev) cudaEventDestroy(a->done_ev);
+        if (a->stream) cudaStreamDestroy(a->stream);
         cudaFree(a->d_tensors);
         cudaFree(a->d_items);
         cudaFree(a->d_kdev);
@@ -382,6 +413,10 @@ int optim_group_attach_prodigy(optim_group_t* g, optim_prodigy_t* pd, void* cons
         cudaGetLastError();
         return fail(set_error(OPTIM_ENOMEM, "prodigy table allocation failed"));
     }
+    rc = check_cuda(cudaStreamCreateWithFlags(&a->stream, cudaStreamNonBlocking), "prodigy stream");
+    if (!rc) rc = check_cuda(cudaEventCreateWithFlags(&a->start_ev, cudaEventDisableTiming), "prodigy event");
+    if (!rc) rc = check_cuda(cudaEventCreateWithFlags(&a->done_ev, cudaEventDisableTiming), "prodigy event");
+    if (rc) return fail(rc);
     // grow the controller's slot array (between steps: the device is idle after the sync)
     rc = check_cuda(cudaDeviceSynchronize(), "device synchronize");
     double2* slots = nullptr;
