@@ -44,7 +44,8 @@ class FusedStepper:
     """
 
     def __init__(self, params: Sequence[torch.Tensor], n_groups: int, hp: dict,
-                 make_group: Callable[[list], object], on_step: Callable | None = None):
+                 make_group: Callable[[list], object], on_step: Callable | None = None,
+                 on_all: Callable | None = None):
         self.params = list(params)
         self.hp = hp
         self.index = split_groups(self.params, n_groups)
@@ -55,6 +56,8 @@ class FusedStepper:
                 self.group_of[id(self.params[i])] = gi
         self.pending = [len(idx) for idx in self.index]
         self.on_step = on_step
+        self.on_all = on_all          # called once every group has stepped (end of a backward)
+        self.stepped = 0
         self.steps_taken = [0] * len(self.groups)
         self.handles = [p.register_post_accumulate_grad_hook(self._hook) for p in self.params]
 
@@ -72,6 +75,11 @@ class FusedStepper:
         for i in idx:
             self.params[i].grad = None
         self.pending[gi] = len(idx)
+        self.stepped += 1
+        if self.stepped == len(self.groups):
+            self.stepped = 0
+            if self.on_all is not None:
+                self.on_all()
 
     def remove(self):
         for h in self.handles:
@@ -95,3 +103,20 @@ def attach_fused_factored(params: Sequence[torch.nn.Parameter], n_groups: int, h
     def make(ps):
         return FactoredGroup([p.data for p in ps])
     return FusedStepper(params, n_groups, hp, make, on_step)
+
+
+def attach_fused_prodigy(params: Sequence[torch.nn.Parameter], n_groups: int, hp: dict, d0: float = 1e-6,
+                         slice_p: int = 11, on_step=None) -> FusedStepper:
+    """Factored groups in Prodigy mode sharing one step-size estimate d: each group steps from its
+    hooks with the current d, and once every group has stepped in a backward pass the
+    controller's end of step forms the next d (stepper.prodigy holds the controller)."""
+    from .engine import FactoredGroup, ProdigyController
+    ctrl = ProdigyController(d0=d0, beta2=hp.get("beta2", 0.999), slice_p=slice_p)
+
+    def make(ps):
+        g = FactoredGroup([p.data for p in ps])
+        g.attach_prodigy(ctrl)
+        return g
+    stepper = FusedStepper(params, n_groups, dict(hp, mode=1), make, on_step, on_all=ctrl.end_step)
+    stepper.prodigy = ctrl
+    return stepper
