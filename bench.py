@@ -441,7 +441,11 @@ def e2e_run(args, groups, grads, hp, params, stream, world, device):
                 for h, w in zip(host_w[k], groups[k].weights):
                     h.copy_(w, non_blocking=True)
 
-    one()
+    # warm-up passes as for the device timing: the first passes over freshly pinned host buffers
+    # run far below the link's rate (a bidirectional copy probe: 44 GB/s on its first repeat, 341
+    # on the next), so one pass is not enough
+    for _ in range(max(args.warmup, 1)):
+        one()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -456,7 +460,7 @@ def e2e_run(args, groups, grads, hp, params, stream, world, device):
         dt = float(t.item())
     nbytes = 2 * params
     return {"value": world * params * steps / dt, "unit": "params/s", "h2d_bytes_per_step": nbytes,
-            "d2h_bytes_per_step": nbytes, "steps": steps,
+            "d2h_bytes_per_step": nbytes, "steps": steps, "warmup": max(args.warmup, 1),
             "link_gbs": 2 * nbytes * steps / dt / 1e9}
 
 
