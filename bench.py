@@ -58,6 +58,7 @@ def parse():
     p.add_argument("--optimizer", default="nadam", choices=["nadam", "adan", "prodigy"],
                    help="adan: fp32 m, v, n + previous gradient, Kahan residual (38 B/param); "
                         "prodigy (factored workloads): Prodigy mode with the step size d estimated each step")
+    p.add_argument("--offload-slots", type=int, default=3, help="flux35: device staging slots of the offload engine")
     p.add_argument("--slice-p", type=int, default=11, help="prodigy: statistics on every slice_p-th 64-element block")
     p.add_argument("--rounding", default="kahan", choices=["kahan", "sr"],
                    help="kahan: bf16 weight + u16 residual; sr: no residual, stochastic rounding")
@@ -479,7 +480,7 @@ def run_offload(args, cfg):
     lmopt.load()
     shapes = cfg["groups"][0]
     slot = engine.offload_slot_bytes([W.numel(s) for s in shapes])
-    off = engine.OffloadEngine(slot, 3)
+    off = engine.OffloadEngine(slot, args.offload_slots)
     grads = [W.grad_bf16(s, cfg["seed"], i, 1, cfg["g_std"], device=device) for i, s in enumerate(shapes)]
     groups, params = [], 0
     t_setup = time.perf_counter()
@@ -523,7 +524,7 @@ def run_offload(args, cfg):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * step_s, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, "params": params, "groups": len(groups),
-                   "states": "pinned host, 6 B/param", "staging_slots": 3, "slot_bytes": slot,
+                   "states": "pinned host, 6 B/param", "staging_slots": args.offload_slots, "slot_bytes": slot,
                    "setup_s": t_setup},
         "link_gbs": (h2d + d2h) / step_s / 1e9, "h2d_gbs": h2d / step_s / 1e9, "d2h_gbs": d2h / step_s / 1e9,
         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
