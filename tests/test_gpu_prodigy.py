@@ -257,3 +257,86 @@ def test_two_ranks_share_d_through_reduce_finish(orc, eng):
     assert st.d.value > 2 * d0
     for c in ctrls:
         c.close()
+
+
+def test_prodigy_misaligned_buffers_and_empty_tensors(orc, eng):
+    """Weights, residuals and gradients 2 bytes aligned and p0 / s 4 bytes (not 16) aligned take
+    the statistics kernel's element-by-element path; empty tensors add nothing.  d, s and the
+    weights follow the oracle as in the aligned case."""
+    from helpers import alloc_offset, cuda_bits
+    from memory_lean_optimizer_gb300 import lmopt
+    shapes = [(96, 64), (40, 50, 3, 3), (700,), (0, 64), (0,), (33, 40)]
+    seed, steps, slice_p, d0 = 9, 6, 3, 1e-4
+    hp = dict(HP, lr=1.0)
+    beta3 = float(np.float32(np.sqrt(0.99)))
+    st = orc.ProdigyState(d0, beta3, slice_p)
+    masters = [W.master_weights(s, seed, i) for i, s in enumerate(shapes)]
+    ora = [oracle_tensor(orc, m.numpy(), s, slice_p) for m, s in zip(masters, shapes)]
+    keep, descs, ws, rs, p0s, ss = [], [], [], [], [], []
+    for i, s in enumerate(shapes):
+        n = W.numel(s)
+        ot = ora[i]
+        b1, w = alloc_offset(n, torch.int16, 1)
+        b2, r = alloc_offset(n, torch.int16, 3)
+        if n:
+            w.copy_(torch.from_numpy(ot["hi"].view(np.int16)))
+            r.copy_(torch.from_numpy(ot["lo"].view(np.int16)))
+        if "row" in ot:
+            b3, rw = alloc_offset(ot["row"].size, torch.float32, 1)
+            b4, cl = alloc_offset(ot["col"].size, torch.float32, 1)
+            rw.zero_(), cl.zero_()
+        else:
+            b3, rw = None, None
+            b4, cl = alloc_offset(n, torch.float32, 1)
+            cl.zero_()
+        L = max(lmopt.optim_prodigy_slice_len(n, slice_p), 1)
+        b5, p0 = alloc_offset(L, torch.float32, 1)
+        b6, sv = alloc_offset(L, torch.float32, 1)
+        keep += [b1, b2, b3, b4, b5, b6]
+        d = lmopt.TensorDesc(w_bf16=w.data_ptr() if n else None, res_u16=r.data_ptr() if n else None,
+                             m=rw.data_ptr() if (rw is not None and rw.numel()) else None,
+                             v=cl.data_ptr() if cl.numel() else None, numel=n, ndim=len(s))
+        for k, dim in enumerate(s):
+            d.shape[k] = dim
+        descs.append(d)
+        ws.append(w), rs.append(r), p0s.append(p0), ss.append(sv)
+    h = lmopt.optim_group_create(descs, lmopt.OPTIM_KIND_FACTORED)
+    pd = lmopt.optim_prodigy_create(d0, beta3, slice_p)
+    H = lmopt.FactoredHparams(lr=hp["lr"], beta2=hp["beta2"], decay_rate=hp["decay_rate"], eps1=hp["eps1"],
+                              eps2=hp["eps2"], d=1.0, clip_threshold=hp["clip_threshold"],
+                              weight_decay=hp["weight_decay"], mode=1)
+    try:
+        lmopt.optim_group_attach_prodigy(h, pd, [x.data_ptr() for x in p0s], [x.data_ptr() for x in ss], 1, 0)
+        lrd = 0.0
+        for t in range(1, steps + 1):
+            bias = [W.grad_bf16(s, seed + 1, i, 0, 1e-3).float() for i, s in enumerate(shapes)]
+            grads = [(bias[i] + W.grad_bf16(s, seed, i, t, 3e-4).float()).to(torch.bfloat16)
+                     for i, s in enumerate(shapes)]
+            lrd += hp["lr"] * st.d32
+            orc.prodigy_step(st, [(ora, [W.bits16(g).reshape(-1) for g in grads], hp)], t)
+            gbufs, ptrs = [], []
+            for g in grads:
+                b, gg = alloc_offset(g.numel(), torch.int16, 1)
+                if g.numel():
+                    gg.copy_(g.reshape(-1).view(torch.int16))
+                gbufs.append(b)
+                ptrs.append(gg.data_ptr() if g.numel() else None)
+            lmopt.optim_step_factored(h, ptrs, t, H, 0)
+            lmopt.optim_prodigy_end_step(pd, 0)
+            torch.cuda.synchronize()
+            d_gpu, _ = lmopt.optim_prodigy_get(pd)
+            assert abs(d_gpu - st.d.value) <= 1e-5 * st.d.value, (t, d_gpu, st.d.value)
+        assert st.d.value > d0
+        for i, ot in enumerate(ora):
+            if ot["hi"].size == 0:
+                continue
+            ref = orc.kahan_merge(ot["hi"], ot["lo"]).astype(np.float64)
+            got = orc.kahan_merge(cuda_bits(ws[i]), cuda_bits(rs[i])).astype(np.float64)
+            assert np.all(np.abs(got - ref) <= 1e-6 * np.abs(ref) + 2e-5 * lrd), f"tensor {i} {shapes[i]}"
+            assert np.array_equal(p0s[i][:ot["p0"].size].cpu().numpy().view(np.uint32), ot["p0"].view(np.uint32))
+            s_ref = ot["s"].astype(np.float64)
+            err = np.abs(ss[i][:ot["s"].size].cpu().numpy().astype(np.float64) - s_ref)
+            assert np.all(err <= 1e-5 * np.abs(s_ref) + 1e-5 * np.abs(s_ref).max()), f"tensor {i}: s differs"
+    finally:
+        lmopt.optim_group_destroy(h)
+        lmopt.optim_prodigy_destroy(pd)
