@@ -132,6 +132,21 @@ __device__ __forceinline__ int cols_in(int64_t remaining) {
     return remaining <= 0 ? 0 : (remaining >= 8 ? 8 : (int)remaining);
 }
 
+// L2 eviction priority of the gradient loads: the statistics and RMS kernels keep a wave's
+// gradients (read again by the next kernels) ahead of streaming data; the update kernel, their
+// last reader, marks them first to go.
+__device__ __forceinline__ uint64_t l2_keep_policy() {
+    uint64_t p;
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint4 ld_keep(const uint4* a, uint64_t pol) {
+    uint4 v;
+    asm("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(a), "l"(pol));
+    return v;
+}
+
 // Neumaier-compensated accumulation.
 struct Comp {
     float s = 0.f, c = 0.f;
@@ -580,6 +595,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_stats(Dev D, const Item* items,
     pdl_sync();
     load_k(k);
 
+    const uint64_t keep = l2_keep_policy();
     if (it.cls == kWide) {
         float (*cols)[kTC + 1] = reinterpret_cast<float (*)[kTC + 1]>(smem);
         const int64_t b = it.x;
@@ -602,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_stats(Dev D, const Item* items,
                 for (int kk = 0; kk < 8; ++kk) {
                     const int64_t row = row0 + 64 * kb + 8 * kk;
                     x[kk] = (row < t.R && lane_ok)
-                                ? __ldcg(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0))
+                                ? ld_keep(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0), keep)
                                 : make_uint4(0, 0, 0, 0);
                 }
                 float rs[8];
@@ -839,12 +855,13 @@ __global__ void __launch_bounds__(kThreads, 4) k_rms(Dev D, const Item* items, K
     const bool lane_ok = ncols == 8;                       // C % 8 == 0: 8 or 0 columns
     const int64_t row0 = (int64_t)it.band * kTR + warp;
     // the first eight rows' gradients are loaded before waiting for the finalize kernel
+    const uint64_t keep = l2_keep_policy();
     uint4 x[8];
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
         const int64_t row = row0 + 8 * kk;
         x[kk] = (vec && row < t.R && lane_ok)
-                    ? __ldcg(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0)) : make_uint4(0, 0, 0, 0);
+                    ? ld_keep(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0), keep) : make_uint4(0, 0, 0, 0);
     }
     pdl_sync();
     load_k(k);
@@ -868,7 +885,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_rms(Dev D, const Item* items, K
                 for (int kk = 0; kk < 8; ++kk) {
                     const int64_t row = row0 + 64 * kb + 8 * kk;
                     x[kk] = (row < t.R && lane_ok)
-                                ? __ldcg(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0)) : make_uint4(0, 0, 0, 0);
+                                ? ld_keep(reinterpret_cast<const uint4*>(g + (b * t.R + row) * t.C + col0), keep) : make_uint4(0, 0, 0, 0);
                 }
             }
 #pragma unroll
