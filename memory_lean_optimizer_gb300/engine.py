@@ -302,7 +302,8 @@ class FactoredGroup(_Group):
 
 class ProdigyController:
     """Prodigy's step-size estimate d shared by the FACTORED groups attached to it: step every
-    group (mode 1), then call end_step() once."""
+    group (mode 1), then call end_step() once.  close() destroys the attached groups as well (the
+    controller cannot be freed while groups are attached)."""
 
     def __init__(self, d0: float = 1e-6, beta3: float | None = None, beta2: float = 0.999, slice_p: int = 11):
         self.slice_p = slice_p

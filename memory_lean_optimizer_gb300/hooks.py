@@ -109,7 +109,9 @@ def attach_fused_prodigy(params: Sequence[torch.nn.Parameter], n_groups: int, hp
                          slice_p: int = 11, on_step=None) -> FusedStepper:
     """Factored groups in Prodigy mode sharing one step-size estimate d: each group steps from its
     hooks with the current d, and once every group has stepped in a backward pass the
-    controller's end of step forms the next d (stepper.prodigy holds the controller)."""
+    controller's end of step forms the next d (stepper.prodigy holds the controller).  Every
+    parameter must receive a gradient in every backward pass (no frozen parameters): the end of
+    step waits for all groups."""
     from .engine import FactoredGroup, ProdigyController
     ctrl = ProdigyController(d0=d0, beta2=hp.get("beta2", 0.999), slice_p=slice_p)
 
