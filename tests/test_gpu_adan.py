@@ -45,3 +45,28 @@ def test_adan_bit_exact(orc, rounding):
                 assert np.array_equal(cuda_bits(grp.res[i]), o["lo"]), (t, i)
             assert np.array_equal(grp.mvn[i].cpu().numpy().view(np.uint32), o["mnv"].view(np.uint32)), (t, i)
             assert np.array_equal(cuda_bits(grp.gprev[i]), o["gp"]), (t, i)
+
+
+def test_adan_empty_tensors(orc):
+    """Tensors without elements among ordinary ones: the others follow the oracle bit for bit."""
+    from memory_lean_optimizer_gb300 import build, engine
+    build.build()
+    sizes = [0, 4097, 0, 300]
+    seed = 51
+    masters = [W.master_weights((n,), seed, i) for i, n in enumerate(sizes)]
+    grp = engine.AdanGroup.from_masters([m.cuda() for m in masters])
+    ora = [dict(zip(("hi", "lo"), orc.kahan_split(m.numpy()))) for m in masters]
+    for o, n in zip(ora, sizes):
+        o["mnv"] = np.zeros(3 * orc.adan_plane(n), np.float32)
+        o["gp"] = np.zeros(n, np.uint16)
+    k = orc.adan_scalars(HP["lr"], HP["beta1"], HP["beta2"], HP["beta3"], HP["eps"], HP["weight_decay"])
+    for t in range(1, 4):
+        grads = [W.grad_bf16((n,), seed, i, t, 1e-3) for i, n in enumerate(sizes)]
+        for i, (o, g) in enumerate(zip(ora, grads)):
+            if sizes[i]:
+                orc.adan_step_tensor(o["hi"], o["lo"], o["mnv"], o["gp"], W.bits16(g), t, k)
+        grp.step([g.cuda() for g in grads], HP)
+    torch.cuda.synchronize()
+    for i, o in enumerate(ora):
+        if sizes[i]:
+            assert np.array_equal(cuda_bits(grp.weights[i]), o["hi"]) and np.array_equal(cuda_bits(grp.res[i]), o["lo"])

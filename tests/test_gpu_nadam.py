@@ -41,6 +41,28 @@ def run_parity(orc, eng, shapes, steps, hp, seed=0, g_std=1e-3, zero_frac=0.0, k
     return ora, grp
 
 
+@pytest.mark.parametrize("states", ["u16", "f24"])
+def test_empty_tensors_in_a_group(orc, eng, states):
+    """Tensors without elements (no gradient, nothing to update) among ordinary ones: the others
+    step bit-identically to the oracle and the empty ones are left alone."""
+    shapes = [(5000,), (0,), (3, 0), (300,), (0, 7), (20000,)]
+    seed, hp = 12, dict(HP, lr=1e-3)
+    masters = [W.master_weights(s, seed, i) for i, s in enumerate(shapes)]
+    ora = OracleNadam(orc, [m.numpy() for m in masters])
+    grp = eng.NadamGroup.from_masters([m.cuda() for m in masters], states=states)
+    for t in range(1, 4):
+        grads = [W.grad_bf16(s, seed, i, t, 1e-3) for i, s in enumerate(shapes)]
+        if states == "u16":
+            ora.step([W.bits16(g).reshape(-1) for g in grads], hp)
+        grp.step([g.cuda() for g in grads], hp)
+    torch.cuda.synchronize()
+    from memory_lean_optimizer_gb300 import lmopt
+    assert lmopt.optim_query_nonfinite(grp.handle) == 0
+    assert all(grp.weights[i].numel() == 0 for i, s in enumerate(shapes) if W.numel(s) == 0)
+    if states == "u16":
+        assert_nadam_equal(ora, grp, "empty tensors")
+
+
 def test_one_1024x1024_ten_steps(orc, eng):
     """The 1024x1024 single-tensor workload, NAdam, lr 3.5e-6, 10 steps, seed 0."""
     run_parity(orc, eng, [(1024, 1024)], 10, HP, g_std=1e-3)
