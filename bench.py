@@ -44,6 +44,7 @@ KERNEL_SOURCES = {
     "k_nadam_f24": ["memory_lean_optimizer_gb300/csrc/nadam.cu", "memory_lean_optimizer_gb300/csrc/common.cuh"],
     "k_nadam_f24<sr>": ["memory_lean_optimizer_gb300/csrc/nadam.cu", "memory_lean_optimizer_gb300/csrc/common.cuh"],
     "k_adan_step": ["memory_lean_optimizer_gb300/csrc/adan.cu", "memory_lean_optimizer_gb300/csrc/common.cuh"],
+    "factored_step": ["memory_lean_optimizer_gb300/csrc/factored.cu", "memory_lean_optimizer_gb300/csrc/common.cuh"],
 }
 
 
@@ -686,7 +687,11 @@ def run_factored(args, cfg):
                    "bytes_per_step_algorithmic": nbytes, "parallelism": f"replicas x{world}",
                    "l2": "inputs ~26 GB, far above the 129 MB L2: no flush needed"},
         "roofline": {"bound": "hbm", "kernel": "factored step (stats+final+rms+apply)", "achieved": gbs,
-                     "peak": peak, "unit": "GB/s", "frac": gbs / peak, "traffic": None, "peak_source": src},
+                     "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     # per step (the roofline object covers the whole step): the Adafactor step's
+                     # DRAM bytes per parameter from a warm-L2 capture, scaled to this step
+                     "traffic": traffic_per_launch("factored_step", params) if ctrl is None else None,
+                     "peak_source": src},
         "clocks": clk,
     }
     if ctrl is not None:
