@@ -178,7 +178,8 @@ int optim_step_nadam_end(optim_group_t* group, const float* exchange, void* stre
  * than one wave (96 MiB of gradients) is processed wave by wave, with consecutive waves on up to
  * three streams: `stream` and two streams owned by the group, which wait for the work already on
  * `stream` and which `stream` waits for before any later work -- to the caller the call is
- * ordered on `stream` as usual. */
+ * ordered on `stream` as usual.  A group attached to a Prodigy controller also runs its
+ * statistics on a fourth stream of its own, ordered the same way. */
 int optim_step_factored(optim_group_t* group, const void* const* grads_bf16, int64_t step,
                         const optim_factored_hparams_t* hp, void* stream);
 
