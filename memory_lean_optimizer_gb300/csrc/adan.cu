@@ -92,8 +92,8 @@ __global__ void __launch_bounds__(kThreads, 4) k_adan_step(NadamLaunch L, AdanPr
     const uint16_t* __restrict__ g = L.grads[c.tensor];
     const bool has_res = (t.flags & kFlagRes) != 0;
     const int64_t n = t.numel;
-    const int64_t start = (int64_t)c.index * kChunk;
-    const int64_t end = min(n, start + kChunk);
+    const int64_t start = (int64_t)c.index * L.chunk;
+    const int64_t end = min(n, start + L.chunk);
     float* __restrict__ mp = static_cast<float*>(t.m);
     const int64_t plane = (n + 3) & ~int64_t(3);   // plane stride: n rounded up to 4 floats
     float* __restrict__ vp = mp + plane;

@@ -206,11 +206,19 @@ int optim_group_create(const optim_tensor_desc_t* tensors, int32_t n, int32_t ki
             r.pad = 0;
         }
         if (kind == OPTIM_KIND_NADAM || kind == OPTIM_KIND_NADAM_F24 || kind == OPTIM_KIND_ADAN) {
+            // a group whose kChunk-element chunks would not give every SM two CTAs is cut finer
+            // (down to kChunkMin): the launch-bound small case then spreads over the whole GPU
+            auto count = [&](int64_t ch) {
+                int64_t c = 0;
+                for (int32_t i = 0; i < n; ++i) c += (tensors[i].numel + ch - 1) / ch;
+                return c;
+            };
+            while (g->chunk > kChunkMin && count(g->chunk) < 2 * (int64_t)sm_count()) g->chunk /= 2;
             for (int pass = 0; pass < 2; ++pass) {   // u16-state tensors first, then fp32-state
                 for (int32_t i = 0; i < n; ++i) {
                     const int64_t ne = tensors[i].numel;
                     if (ne == 0 || (pass == 0) != (ne > kSmall)) continue;
-                    const int64_t nc = (ne + kChunk - 1) / kChunk;
+                    const int64_t nc = (ne + g->chunk - 1) / g->chunk;
                     for (int64_t c = 0; c < nc; ++c) chunks.push_back(Chunk{i, (int32_t)c});
                 }
                 if (pass == 0) g->n_chunks_large = (int32_t)chunks.size();
@@ -307,7 +315,7 @@ int optim_step_nadam_begin(optim_group_t* g, const void* const* grads, int64_t s
         if (rc) return rc;
     }
     NadamLaunch L{table, g->d_grads, g->d_scales, g->d_chunks, g->d_nonfinite,
-                  g->n_chunks_large, g->n_chunks_total, g->kind == OPTIM_KIND_NADAM_F24, g->d_zero_chunk};
+                  g->n_chunks_large, g->n_chunks_total, g->kind == OPTIM_KIND_NADAM_F24, g->d_zero_chunk, g->chunk};
     rc = launch_nadam_prepass(L, k, s);
     if (!rc && exchange) rc = launch_scales_gather(g->d_scales, exchange, g->n, k.parity, s);
     if (rc) return rc;
@@ -329,7 +337,7 @@ int optim_step_nadam_end(optim_group_t* g, const float* exchange, void* stream) 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const NadamScalars& k = g->pending_k;
     NadamLaunch L{g->pending_table, g->d_grads, g->d_scales, g->d_chunks, g->d_nonfinite,
-                  g->n_chunks_large, g->n_chunks_total, g->kind == OPTIM_KIND_NADAM_F24, g->d_zero_chunk};
+                  g->n_chunks_large, g->n_chunks_total, g->kind == OPTIM_KIND_NADAM_F24, g->d_zero_chunk, g->chunk};
     if (exchange) rc = launch_scales_scatter(g->d_scales, exchange, g->n, k.parity, s);
     if (!rc) rc = launch_nadam_update(L, k, s, g->profile_ev);
     if (rc) return rc;
@@ -381,7 +389,7 @@ int optim_step_adan(optim_group_t* g, const void* const* grads, int64_t step, co
     rc = upload_grads(g, grads, s);
     if (rc) return rc;
     NadamLaunch L{g->d_tensors, g->d_grads, g->d_scales, g->d_chunks, g->d_nonfinite, g->n_chunks_large,
-                  g->n_chunks_total, 0, nullptr};
+                  g->n_chunks_total, 0, nullptr, g->chunk};
     rc = launch_adan_step(L, k, s);
     if (rc) return rc;
     g->last_step = step;

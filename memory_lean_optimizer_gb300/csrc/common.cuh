@@ -17,6 +17,7 @@ namespace lmo {
 
 constexpr int kThreads = 256;          // threads per CTA of the streaming kernels
 constexpr int64_t kChunk = 16384;      // elements per CTA (u16-state tensors); multiple of 8
+constexpr int64_t kChunkMin = 2048;    // smallest chunk a small group is cut into
 constexpr int64_t kSmall = OPTIM_SMALL_NUMEL;
 
 // Flags of a tensor record.
@@ -49,7 +50,8 @@ struct ScaleRec {
 };
 static_assert(sizeof(ScaleRec) == 64, "ScaleRec layout");
 
-// One CTA's work item: elements [index*kChunk, min(numel, (index+1)*kChunk)) of a tensor.
+// One CTA's work item: elements [index*chunk, min(numel, (index+1)*chunk)) of a tensor, chunk the
+// group's chunk size (kChunk, or a smaller power of two for groups too small to fill the GPU).
 struct Chunk {
     int32_t tensor;
     int32_t index;

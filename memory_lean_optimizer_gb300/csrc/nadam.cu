@@ -95,8 +95,8 @@ __global__ void __launch_bounds__(kThreads) k_grad_absmax(NadamLaunch L, int par
         sr->a_v[p] = 0u;
         sr->g[q] = 0u;     // next step's gradient max accumulates here
     }
-    const int64_t start = (int64_t)c.index * kChunk;
-    const int64_t end = min(numel, start + kChunk);
+    const int64_t start = (int64_t)c.index * L.chunk;
+    const int64_t end = min(numel, start + L.chunk);
     uint32_t mx = 0u;
     // exact zeros: a 16-bit magnitude t (bit 15 clear) is zero iff t - 1 sets bit 15; the
     // borrow into the upper half matters only when the lower half is zero, which is flagged anyway
@@ -270,7 +270,7 @@ template <bool kSR, bool kGuard>
 __device__ __forceinline__ void u16_vectors(const Prm& k, const Codec& cd, bool has_res, uint32_t tensor, int64_t start,
                                             int nv, uint4* wv, uint4* rv, const uint4* gv, uint4* mv, uint4* vv,
                                             float& am, float& av, uint32_t& nf) {
-    // nv <= kChunk / 8: 32-bit vector indices within the chunk
+    // nv <= chunk / 8 <= kChunk / 8: 32-bit vector indices within the chunk
     const bool sr = kSR && !has_res;
     // two independent 8-element groups per iteration, kThreads vectors apart: ten 128-bit
     // loads in flight (one generator call per group under stochastic rounding).
@@ -312,7 +312,8 @@ __device__ __forceinline__ void u16_vectors(const Prm& k, const Codec& cd, bool 
     }
 }
 
-template <bool kSR>
+// kFull: the group's chunk is kChunk (every group but small ones), known at compile time.
+template <bool kSR, bool kFull>
 __global__ void __launch_bounds__(kThreads, 4) k_nadam_step(NadamLaunch L, Prm k, int parity) {
     __shared__ uint32_t red[3 * 32];
     const Chunk c = L.chunks[blockIdx.x];
@@ -321,8 +322,9 @@ __global__ void __launch_bounds__(kThreads, 4) k_nadam_step(NadamLaunch L, Prm k
     const int p = parity, q = parity ^ 1;
     const bool small = (t.flags & kFlagSmall) != 0;
     const bool has_res = (t.flags & kFlagRes) != 0;
-    const int64_t start = (int64_t)c.index * kChunk;
-    const int64_t end = min(t.numel, start + kChunk);
+    const int64_t chunk = kFull ? kChunk : L.chunk;
+    const int64_t start = (int64_t)c.index * chunk;
+    const int64_t end = min(t.numel, start + chunk);
 
     Codec cd{};
     ScaleRec* sr = L.scales + c.tensor;
@@ -479,8 +481,8 @@ __global__ void __launch_bounds__(kThreads, 4) k_nadam_f24(NadamLaunch L, Prm k)
     const bool small = (t.flags & kFlagSmall) != 0;
     const bool has_res = (t.flags & kFlagRes) != 0;
     const int64_t n = t.numel;
-    const int64_t start = (int64_t)c.index * kChunk;
-    const int64_t end = min(n, start + kChunk);
+    const int64_t start = (int64_t)c.index * L.chunk;
+    const int64_t end = min(n, start + L.chunk);
     uint32_t nf = 0u;
     uint16_t* __restrict__ w = t.w;
     uint16_t* __restrict__ res = t.res;
@@ -596,8 +598,14 @@ int launch_nadam_update(const NadamLaunch& L, const NadamScalars& s, cudaStream_
         else k_nadam_f24<false><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k);
         return check_cuda(cudaGetLastError(), "nadam f24 step launch");
     }
-    if (k.sr) k_nadam_step<true><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k, s.parity);
-    else k_nadam_step<false><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k, s.parity);
+    const bool full = L.chunk == kChunk;
+    if (k.sr) {
+        if (full) k_nadam_step<true, true><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k, s.parity);
+        else k_nadam_step<true, false><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k, s.parity);
+    } else {
+        if (full) k_nadam_step<false, true><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k, s.parity);
+        else k_nadam_step<false, false><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k, s.parity);
+    }
     return check_cuda(cudaGetLastError(), "nadam step launch");
 }
 
