@@ -20,7 +20,8 @@
  *  - bf16 and uint16 buffers are arrays of 16-bit words and must be 2-byte aligned; fp32 buffers
  *    4-byte aligned.  16-byte alignment of every buffer of a tensor enables 128-bit accesses;
  *    other alignments take a slower element-by-element path with identical results.
- *  - All arithmetic is IEEE fp32, every operation rounded to nearest-even, no contraction; the
+ *  - All arithmetic is IEEE fp32, each operation rounded once to nearest-even: the update's
+ *    a*b+c steps are fused multiply-adds (one rounding), nothing else is contracted.  The
  *    results are deterministic run to run.
  */
 #ifndef LMOPT_H
@@ -44,9 +45,9 @@ enum {
     OPTIM_ESTATE = -7      /* call not valid in the group's current state */
 };
 
-/* Tensors of this many elements or fewer keep fp32 moments instead of u16 codes ("any tensors
- * that have 4096 or fewer elements ... are just stored ... in f32 format", "Amazing Flux FFT
- * quality on a 5090", sd-scripts PR #2187, second post). */
+/* Tensors of this many elements or fewer keep fp32 moments instead of u16 codes (small tensors
+ * skip the compact format and stay in f32, "Amazing Flux FFT quality on a 5090", sd-scripts
+ * PR #2187, second post). */
 #define OPTIM_SMALL_NUMEL 4096
 
 typedef struct optim_group optim_group_t;
@@ -76,9 +77,9 @@ typedef struct {
 } optim_tensor_desc_t;
 
 /* Group kinds.  NADAM_F24 is NADAM with f24 moment storage: the upper three bytes of each fp32
- * moment ("f24 is the upper three bytes [of f32] - i.e. with 8 more bits of mantissa", "Amazing
- * Flux FFT quality on a 5090", sd-scripts PR #2187, third post), truncated.  Its m and v buffers
- * (numel > 4096) hold L + numel bytes, L = 2*numel rounded up to a multiple of 16: numel uint16
+ * moment, truncated (the f24 format of "Amazing Flux FFT quality on a 5090", sd-scripts PR
+ * #2187, third post: fp32 cut to its top three bytes, eight mantissa bits more than bf16).
+ * Its m and v buffers (numel > 4096) hold L + numel bytes, L = 2*numel rounded up to a multiple of 16: numel uint16
  * upper words, padding up to byte L, then numel bytes of bits 8..15.  Buffers that start on a
  * 16-byte boundary take the 128-bit path whatever numel is.  No scale records and no gradient
  * pre-pass are involved; tensors of 4096 or fewer elements keep fp32 moments. */

@@ -1,6 +1,6 @@
-// adan.cu -- fused Adan step ("a cpu-offloading version of ADAN ... four optimizer parameters
-// for each model parameter", "Amazing Flux FFT quality on a 5090", sd-scripts PR #2187, fourth
-// post; Algorithm 1 of the linked Adan paper).  States per element: m, v, n (fp32 planes of one
+// adan.cu -- fused Adan step (the page "Amazing Flux FFT quality on a 5090", sd-scripts PR #2187,
+// fourth post, offers an offloaded Adan whose four states per parameter are kept small by
+// compression; Algorithm 1 of the linked Adan paper).  States per element: m, v, n (fp32 planes of one
 // buffer) and the previous bf16 gradient.  One pass per element; the weight is stored with the
 // Kahan residual, stochastically rounded, or round-to-nearest.  38 bytes per element per step.
 //   d = g - g_prev;  m = fma(1-b1, m, b1 g);  v = fma(1-b2, v, b2 d);  c = fma(1-b2, d, g)

@@ -423,8 +423,8 @@ __global__ void __launch_bounds__(kThreads, 4) k_nadam_step(NadamLaunch L, Prm k
 }
 
 // ------------------------------------------------------------------------------------ f24
-// f24 moments: the upper 24 bits of the fp32 moment ("f24 is the upper three bytes [of f32]",
-// sd-scripts PR #2187, third post), stored as a plane of n upper 16-bit words followed by a
+// f24 moments: the upper 24 bits of the fp32 moment (the f24 format of sd-scripts PR #2187,
+// third post: fp32 cut to its top three bytes, eight mantissa bits more than bf16), stored as a plane of n upper 16-bit words followed by a
 // plane of n bytes (bits 8..15).  Storage only: the update runs on the decoded fp32 values, and
 // no scale (hence no gradient pre-pass) is needed.  22 bytes per element per step.
 __device__ __forceinline__ int64_t f24_lo_offset(int64_t n) { return (2 * n + 15) & ~(int64_t)15; }

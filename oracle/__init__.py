@@ -11,8 +11,21 @@ Parity status of each function (pins live in ``tests/test_oracle_*.py``):
                                  monotonicity, hand-derived fixtures (tie to even)
   nadam_scalars / nadam_step     pinned: Adam step-1 = -lr sign(g), NAdam step-1 closed form,
                                  torch.optim.Adam/AdamW/NAdam trajectories, zero grad, decay-only
+  scale record (S_m, S_v, A_m, A_v)  pinned: closed forms at t = 1 (S = (1-b) G, (1-b2) G^2) and
+                                 the recurrence at t = 2 on hand-chosen maxima, both store paths
+  nadam_step_slice               pinned: slices stepped with the whole tensor's maxima equal the
+                                 unsplit step (gloo tests)
+  nadam_step_tensor_f24          pinned: replay of the fp32-moment step truncated to 24 bits,
+                                 2^-15 storage bound, hand-computed plane layout
+  philox4x32_10 / sr_bits / stochastic_round / nadam_step_tensor_sr
+                                 pinned: the generator's published known-answer vectors, lane
+                                 uniformity, rounding probability equal to the distance, SR step
+                                 = RNE-free rounding of the no-residual step
+  adan_step_tensor               pinned: constant-gradient and two-gradient closed forms, decay only
   factored_step                  pinned: torch.optim.Adafactor special case, rank-1 g^2 gives
                                  u = sign(g), 1-D step-1 sign, clipped RMS == clip, zero grad
+  prodigy_* (d estimate)         pinned: closed-form numerator at t = 1, constant-gradient scalar
+                                 recurrence, slicing independence, monotone d
 """
 from __future__ import annotations
 

@@ -94,8 +94,8 @@ void orc_round_bf16(const float* x, uint16_t* out, int64_t n)
 }
 
 /* ----------------------------------------------------------------------------------------
- * R3: u16 companded codec ("I scale the exp_avg[_sq] structures and store them in
- * scaled/biased uint16 format ... apply a pow() function", sd-scripts PR #2187, second post).
+ * R3: u16 companded codec (sd-scripts PR #2187, second post: both moments are scaled, stored as
+ * biased uint16 codes, and pass through a power curve; the constants are not given).
  * Curve: exp_avg code = 32768 + sgn(m) rint(32767 (|m|/S)^(1/2)), exp_avg_sq code =
  * rint(65535 (v/S)^(1/4)).  The code step and the scale are folded into per-tensor constants,
  * computed once per tensor from S:
@@ -176,7 +176,7 @@ void orc_state_unpack(const uint16_t* codes, float scale, float* x, int64_t n, i
  *   NAdam: mu_t = b1 (1 - 0.5*0.96^(t psi)), P_t = P_{t-1} mu_t,
  *          c_g = (1-mu_t)/(1-P_t), c_m = mu_{t+1}/(1 - P_t mu_{t+1})
  *   both:  k2 = 1/sqrt(1-b2^t)
- * The pages name "Nesterov Momentum (i.e. NAdamW)" (sd-scripts PR #2187, first post) without
+ * The pages name Nesterov momentum, that is NAdamW (sd-scripts PR #2187, first post), without
  * printing a formula; this is Dozat's NAdam with the usual momentum-decay schedule.
  * -------------------------------------------------------------------------------------- */
 typedef struct {
@@ -241,7 +241,7 @@ float orc_grad_absmax(const uint16_t* g, int64_t n)
  *   sv = sqrt(v);  den = fma(sv, k2, eps);  num = fma(c_m, m, c_g g)
  *   w  = fma(-lr, num / den, w);  (hi, lo) = split(w)
  * The update uses the fp32 moments just computed; quantisation happens only between steps
- * ("it can only be used for storage rather than operations", PR #2187, third post).
+ * (PR #2187, third post: the compact format holds values between steps and is not computed in).
  * The scale maxima A_m = max |m|, A_v = max v skip NaN (fmax semantics).
  * -------------------------------------------------------------------------------------- */
 static float nadam_elem(float w, float gg, float* mm, float* vv, float* sv,
@@ -317,9 +317,8 @@ void orc_nadam_step_tensor(uint16_t* hi, uint16_t* lo, void* m, void* v, const u
 }
 
 /* ----------------------------------------------------------------------------------------
- * f24 moment storage ("f24 is the upper three bytes [of f32] - i.e. with 8 more bits of
- * mantissa ... it can only be used for storage rather than operations", sd-scripts PR #2187,
- * third post).  Reading: the stored value is the f32 pattern truncated to its upper 24 bits
+ * f24 moment storage (sd-scripts PR #2187, third post: f24 keeps the top three bytes of an fp32
+ * value, eight mantissa bits more than bf16, and serves as storage only, not for arithmetic).  Reading: the stored value is the f32 pattern truncated to its upper 24 bits
  * (like the Kahan split); decode appends a zero byte.  Layout per moment buffer of n elements:
  * n uint16 words of the upper 16 bits, zero padding up to byte offset 2n rounded up to a
  * multiple of 16, then n bytes of bits 8..15 (storage only: the padding carries no value).  No scale is needed, so no
@@ -374,10 +373,9 @@ void orc_nadam_step_tensor_f24(uint16_t* hi, uint16_t* lo, void* m, void* v, con
 }
 
 /* ----------------------------------------------------------------------------------------
- * Stochastic rounding of the fp32 master to bf16, in place of the Kahan residual ("stochastic
- * rounding ... randomly moving the value either up or down to the next rounded bfloat16 value,
- * depending on the distance", "Kahan summation for Adafactor-optimized Flux FFT", sd-scripts
- * PR #2159, PR description).  Reading: add 16 uniform random bits to the f32 pattern and keep
+ * Stochastic rounding of the fp32 master to bf16, in place of the Kahan residual ("Kahan summation
+ * for Adafactor-optimized Flux FFT", sd-scripts PR #2159, PR description: the value goes to the
+ * bf16 neighbour above or below at random, with odds set by how close it is to each).  Reading: add 16 uniform random bits to the f32 pattern and keep
  * the upper half, which rounds the magnitude up with probability (low 16 bits)/65536.
  * Random bits: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as
  * 1, 2, 3", SC 2011): four 32-bit counter words, two key words, ten rounds; each round forms
@@ -477,8 +475,8 @@ void orc_nadam_step_tensor_sr(uint16_t* hi, void* m, void* v, const uint16_t* g,
 }
 
 /* ----------------------------------------------------------------------------------------
- * Adan ("a cpu-offloading version of ADAN ... needs four optimizer parameters for each model
- * parameter", sd-scripts PR #2187, fourth post; Algorithm 1 of the linked paper, arXiv
+ * Adan (sd-scripts PR #2187, fourth post: an offloaded Adan, which keeps four states per
+ * parameter; Algorithm 1 of the linked paper, arXiv
  * 2208.06677, with its convention that beta weights the new term):
  *   d = g - g_prev
  *   m = (1-b1) m + b1 g;  v = (1-b2) v + b2 d;  n = (1-b3) n + b3 (g + (1-b2) d)^2

@@ -302,7 +302,7 @@ def test_f24_misaligned_buffers_take_scalar_path(orc, eng):
 @pytest.mark.parametrize("states", ["u16", "f24"])
 def test_stochastic_rounding_bit_exact(orc, eng, states):
     """Tensors without a residual and stochastic_rounding = 1: the stored bf16 weights follow the
-    oracle's Philox4x64-10 draws bit for bit (vector and element-by-element paths)."""
+    oracle's Philox4x32-10 draws bit for bit (vector and element-by-element paths)."""
     sizes = [300, 4097, 16384, 20003, 65536]
     seed, key = 23, 0xDEADBEEF12345
     hp = dict(HP, lr=1e-3, stochastic_rounding=1, seed=key)

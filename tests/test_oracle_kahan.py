@@ -2,7 +2,7 @@
 
 The residual is the 16 low bits clipped from the f32 value and the live weight is its bf16 upper
 half, so that the bit-identical f32 value is restored ("Kahan summation for Adafactor-optimized
-Flux FFT", sd-scripts PR #2159, first comment; "bf16 is the upper two bytes of f32",
+Flux FFT", sd-scripts PR #2159, first comment; bf16 as the high half of an f32 pattern,
 "Amazing Flux FFT quality on a 5090", sd-scripts PR #2187, third post).
 """
 import os

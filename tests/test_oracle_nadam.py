@@ -4,7 +4,7 @@ The pages recommend NAdam (Nesterov momentum) and its W variant with decoupled w
 without printing a formula ("Amazing Flux FFT quality on a 5090", sd-scripts PR #2187, first
 post).  The oracle takes Dozat's NAdam with the momentum-decay schedule; these tests pin it to
 closed forms and to torch.optim's Adam, AdamW and NAdam (library routines), using tensors of
-4096 or fewer elements, which keep fp32 moments (same post, "4096 or fewer elements").
+4096 or fewer elements, which keep fp32 moments (second post of the same page).
 """
 import numpy as np
 import pytest
@@ -231,3 +231,70 @@ def test_f24_moments_are_truncated_fp32(orc):
     assert buf.size == 16 + 3
     assert list(buf[:6].view(np.uint16)) == [0x3F80, 0xC020, (y.view(np.uint32)[2] >> 16)]
     assert list(buf[16:]) == [0, 0, (y.view(np.uint32)[2] >> 8) & 0xFF]
+
+
+def _scale_fixture(n=6000, seed=18):
+    """Two hand-shaped gradients of a tensor above 4096 elements (u16 moments): random values of
+    magnitude ~1e-3 plus one planted extreme, so that G = max|g| is a chosen power-of-two multiple
+    (G1 = 2^-7 at t = 1, G2 = 3 * 2^-8 at t = 2)."""
+    rng = np.random.default_rng(seed)
+    g1 = rng.standard_normal(n) * 1e-3
+    g1[17] = -2.0 ** -7
+    g2 = rng.standard_normal(n) * 1e-3
+    g2[4321] = 3.0 * 2.0 ** -8
+    return bf16_bits(g1), bf16_bits(g2)
+
+
+def _close(a, b, rel=4 * 2.0 ** -24):
+    return abs(float(a) - float(b)) <= rel * abs(float(b))
+
+
+@pytest.mark.parametrize("sr", [False, True])
+def test_scale_record_closed_form(orc, sr):
+    """The per-tensor scale record written out by hand (reading R4: the scale of step t bounds the
+    moments of step t; sd-scripts PR #2187, second post, says only that the moments are
+    scaled).  With b = beta and A(0) = 0:
+        t = 1:  S_m = (1-b1) G1,  S_v = (1-b2) G1^2,  A_m = max|m1|, A_v = max v1 with
+                m1 = (1-b1) g1 and v1 = (1-b2) g1^2 (fresh moments decode to 0 exactly);
+        t = 2:  S_m = b1 A_m(1) + (1-b1) G2,  S_v = b2 A_v(1) + (1-b2) G2^2,
+                A_m(2), A_v(2) the maxima of the step-2 moments, within the codec's error of the
+                same moments computed in double from exact m1, v1.
+    G enters S_v squared: S_v ~ 1e-3 * G^2 here, three orders of magnitude below (1-b2) G.
+    Both store paths carry the record: the Kahan store and stochastic rounding (no residual).
+    The hyper-parameters are fp32 values, so b is the fp32 number nearest 0.9 (0.999)."""
+    b1, b2 = float(np.float32(0.9)), float(np.float32(0.999))
+    g1, g2 = _scale_fixture()
+    n = g1.size
+    G1, G2 = float(bits_to_f32(g1).__abs__().max()), float(bits_to_f32(g2).__abs__().max())
+    assert G1 == 2.0 ** -7 and G2 == 3.0 * 2.0 ** -8
+    w0 = (np.random.default_rng(19).standard_normal(n) * 0.02).astype(np.float32)
+    t = make_tensor(orc, w0, small=False)
+    st = orc.NadamState(1)
+    mp = 1.0
+    recs = []
+    for step, g in enumerate((g1, g2), start=1):
+        k, mp = orc.nadam_scalars(step, 1e-3, b1, b2, 1e-8, 0.0, False, True, 0.004, mp)
+        if sr:
+            orc.nadam_step_tensor_sr(t["hi"], t["m"], t["v"], g, st.scales[0], k, 7, 0, step)
+        else:
+            orc.nadam_step_tensor(t["hi"], t["lo"], t["m"], t["v"], g, st.scales[0], k)
+        recs.append(st.scale(0))
+    (s_m1, s_v1, a_m1, a_v1), (s_m2, s_v2, a_m2, a_v2) = recs
+    # t = 1: closed forms in double
+    assert _close(s_m1, (1 - b1) * G1), (s_m1, (1 - b1) * G1)
+    assert _close(s_v1, (1 - b2) * G1 * G1), (s_v1, (1 - b2) * G1 * G1)
+    x1 = bits_to_f32(g1).astype(np.float64)
+    m1, v1 = (1 - b1) * x1, (1 - b2) * x1 * x1
+    assert _close(a_m1, np.abs(m1).max()) and _close(a_v1, v1.max())
+    # t = 2: the recurrence on the recorded maxima, in double
+    assert _close(s_m2, b1 * a_m1 + (1 - b1) * G2, rel=8 * 2.0 ** -24)
+    assert _close(s_v2, b2 * a_v1 + (1 - b2) * G2 * G2, rel=8 * 2.0 ** -24)
+    x2 = bits_to_f32(g2).astype(np.float64)
+    m2, v2 = b1 * m1 + (1 - b1) * x2, b2 * v1 + (1 - b2) * x2 * x2
+    # decoded m1, v1 differ from the exact ones by at most half a code step in y: about
+    # 2 * 0.5/32767 of S_m and 4 * 0.5/65535 of S_v (relative to the scale, not the value)
+    assert abs(a_m2 - np.abs(m2).max()) <= b1 * s_m1 * 1.0 / 32767 + 1e-7 * a_m2
+    assert abs(a_v2 - v2.max()) <= b2 * s_v1 * 2.0 / 65535 + 1e-7 * a_v2
+    # both records bound what they describe
+    assert a_m1 <= s_m1 * (1 + 2.0 ** -20) and a_v1 <= s_v1 * (1 + 2.0 ** -20)
+    assert a_m2 <= s_m2 * (1 + 2.0 ** -20) and a_v2 <= s_v2 * (1 + 2.0 ** -20)
