@@ -83,10 +83,23 @@ typedef struct {
  * upper words, padding up to byte L, then numel bytes of bits 8..15.  Buffers that start on a
  * 16-byte boundary take the 128-bit path whatever numel is.  No scale records and no gradient
  * pre-pass are involved; tensors of 4096 or fewer elements keep fp32 moments. */
-enum { OPTIM_KIND_NADAM = 0, OPTIM_KIND_FACTORED = 1, OPTIM_KIND_NADAM_F24 = 2, OPTIM_KIND_ADAN = 3 };
+enum {
+    OPTIM_KIND_NADAM = 0,
+    OPTIM_KIND_FACTORED = 1,
+    OPTIM_KIND_NADAM_F24 = 2,
+    OPTIM_KIND_ADAN = 3,
+    OPTIM_KIND_ADAN_F24 = 4
+};
 /* ADAN groups: m -> fp32 [3*P] (planes m, v, n, each P = numel rounded up to a multiple of 4
  * floats, so that every plane of a 16-byte aligned buffer is 16-byte aligned and takes the
- * 128-bit path), v -> uint16 [numel] (previous bf16 gradient), all zero at creation. */
+ * 128-bit path), v -> uint16 [numel] (previous bf16 gradient), all zero at creation.
+ * ADAN_F24 groups keep Adan's three states in the f24 storage of NADAM_F24 (the page offering
+ * the offloaded Adan, "Amazing Flux FFT quality on a 5090", sd-scripts PR #2187, fourth post,
+ * names compression of its four states without fixing one): for numel > 4096, m holds three
+ * f24 buffers of the NADAM_F24 layout -- m, v and n -- each padded to F = (L + numel) rounded up
+ * to 16 bytes, buffer j at byte j*F (3F bytes); tensors of 4096 or fewer elements keep the fp32
+ * planes of ADAN.  Storage only: the update computes on the decoded fp32 values.  v as ADAN.
+ * 32 bytes per element per step instead of 38. */
 
 /* Adam / NAdam(W) hyper-parameters ("(N)AdamW / Adan with fused backwards pass & CPU
  * offloading", sd-scripts PR #2187, first post: NAdamOffload, AdamOffload, NAdamWOffload).
@@ -259,7 +272,7 @@ typedef struct {
     uint64_t seed;
 } optim_adan_hparams_t;
 
-/* One fused Adan step of an ADAN group: d = g - g_prev, m, v, n EMAs, w = (w - lr (m + (1-b2) v) /
+/* One fused Adan step of an ADAN or ADAN_F24 group: d = g - g_prev, m, v, n EMAs, w = (w - lr (m + (1-b2) v) /
  * (sqrt(n) + eps)) / (1 + lr wd), Kahan split (or stochastic / nearest rounding), g_prev = g.
  * Step 1 starts from m = g, v = 0, n = g^2 and step 2 sets v = d.  Arguments as
  * optim_step_nadam_kahan; one enqueued kernel. */
@@ -295,28 +308,63 @@ int optim_group_set_step(optim_group_t* group, int64_t step, double mu_product);
 int optim_query_nonfinite(optim_group_t* group, uint64_t* count);
 
 /* ---- pinned-host offload of the states between steps --------------------------------------
- * The pages keep the moments and Kahan residuals in CPU memory between steps and move each
- * parameter group's states in for its update and back out afterwards ("Amazing Flux FFT quality
- * on a 5090", sd-scripts PR #2187, first post; "Kahan summation for Adafactor-optimized Flux
- * FFT", sd-scripts PR #2159, PR description).  An engine owns n_slots device staging slots of
- * slot_bytes each and two copy streams (H2D, D2H).  A NADAM group attached to it keeps res_u16,
- * m and v in PINNED HOST memory (the pointers of its descriptors); weights, gradients and the
- * per-tensor scale records stay on the device.  optim_step_nadam_kahan on such a group
- * prefetches if needed, makes the caller's stream wait (device-side) for the copy-in, runs the
- * update on the staging slot and enqueues the copy-out; the host never blocks.  Calling
- * optim_offload_prefetch for the next group before stepping the current one overlaps the copies
- * with the kernels.  At most n_slots - 1 groups may be prefetched ahead of the one being stepped
- * (else OPTIM_ESTATE).  Host states are valid again after optim_offload_sync. */
+ * The pages keep the optimizer states and Kahan residuals in CPU memory between steps and move
+ * each parameter group's states in for its update and back out afterwards ("Amazing Flux FFT
+ * quality on a 5090", sd-scripts PR #2187, first post, and its fourth post for Adan; "Kahan
+ * summation for Adafactor-optimized Flux FFT", sd-scripts PR #2159, PR description).  NADAM,
+ * NADAM_F24, ADAN and ADAN_F24 groups can be offloaded: their residuals and m, v buffers then
+ * live in PINNED HOST memory, while weights, gradients and the per-tensor scale records stay on
+ * the device.  Each step runs on a device staging slot: the copy-in (prefetch) must precede the
+ * step, the copy-out (write-back) follows it; every dependency between them is a device-side
+ * event wait, so the host never blocks.  Prefetching group k+1 and writing back group k-1 while
+ * group k steps overlaps the copies with the kernels.  A group holds its slot from prefetch to
+ * write-back; the slots are taken round-robin, and a prefetch whose next slot is still held
+ * returns OPTIM_ESTATE (so at most n_slots - 1 groups can be prefetched ahead).
+ *
+ * Two ways to attach a group:
+ *   optim_group_attach_host (the per-group form): the caller gives one pinned buffer, the
+ *     group's host image, and enqueues prefetch and write-back itself on copy streams of its
+ *     choice; one copy per direction.  Staging slots come from the library's own ring on the
+ *     group's device (three slots, sized to the largest attached group, freed with the last).
+ *   optim_group_attach_offload (an engine the caller creates): the group's descriptors point at
+ *     pinned host buffers; a step prefetches if the caller has not, and enqueues its own
+ *     write-back on the engine's D2H stream. */
 typedef struct optim_offload optim_offload_t;
 int optim_offload_create(size_t slot_bytes, int32_t n_slots, optim_offload_t** out);
 /* Waits (bounded) for the engine's copies, then frees it; OPTIM_ESTATE while groups are attached. */
 int optim_offload_destroy(optim_offload_t* engine);
-/* Binds a NADAM group (before its first offloaded step); OPTIM_EINVAL if a state buffer is not
- * pinned host memory or the group does not fit in one slot. Destroying the group unbinds it. */
+/* Binds a group to an engine (before its first offloaded step); OPTIM_EINVAL if a state buffer is
+ * not pinned host memory or the group does not fit in one slot.  Destroying the group unbinds it. */
 int optim_group_attach_offload(optim_group_t* group, optim_offload_t* engine);
-/* Enqueues the copy-in of the group's states into the next staging slot. */
-int optim_offload_prefetch(optim_group_t* group);
-/* Bounded wait for every enqueued copy; returns the bytes copied in each direction so far. */
+
+/* Layout of a group's host image: total_bytes (the image size), and, if offsets is not NULL,
+ * 3 byte offsets per tensor in group order -- residual, m buffer, v buffer, each at a 256-byte
+ * boundary, -1 for a buffer the tensor does not have (no residual, or numel 0).  The buffers
+ * hold exactly what the group's device buffers would (lmopt.h layouts of each kind); the gaps
+ * between them carry nothing.  OPTIM_EINVAL for a group kind that cannot be offloaded. */
+int optim_offload_layout(optim_group_t* group, int64_t* offsets, int64_t* total_bytes);
+/* Moves the group's states into `image`: caller-owned PINNED host memory of at least
+ * optim_offload_layout's total_bytes, valid while the group lives.  Between steps only
+ * (synchronises the group's last stream, then copies every residual, m and v buffer named at
+ * create into the image, from device or host).  From then on the group never touches those
+ * buffers again (the caller may free them); the states live in the image and in a staging slot
+ * from optim_offload_prefetch to optim_offload_writeback.  OPTIM_EINVAL: not pinned, too small,
+ * or a kind that cannot be offloaded; OPTIM_ESTATE: already attached, or the library's ring
+ * must grow while another group's states are on the device. */
+int optim_group_attach_host(optim_group_t* group, void* image, size_t bytes);
+/* Enqueues on `copy` the copy-in of the group's states into a staging slot (nothing if the group
+ * already holds one).  The copy waits (device-side) until the slot's previous write-back is done.
+ * copy: a cudaStream_t as void*; NULL = the library's own H2D stream (the engine's, or the
+ * library ring's).  A later step of the group waits for the copy on its own stream. */
+int optim_offload_prefetch(optim_group_t* group, void* copy);
+/* Enqueues on `copy` the copy-out of the group's states after its last step (device-side wait
+ * for that step) and releases the slot; the image is valid once `copy` has finished it.  NULL =
+ * the library's own D2H stream (waited for by optim_offload_sync(NULL, ...)).  For groups
+ * attached with optim_group_attach_host; engine-attached groups write back at the end of every
+ * step, and this call does nothing for them.  OPTIM_ESTATE if the group holds no slot. */
+int optim_offload_writeback(optim_group_t* group, void* copy);
+/* Bounded wait for the copies on the engine's own streams (engine NULL: the library ring of the
+ * current device); returns the bytes copied in each direction so far. */
 int optim_offload_sync(optim_offload_t* engine, uint64_t* bytes_h2d, uint64_t* bytes_d2h);
 
 /* Profiling hook: when `event` (a cudaEvent_t passed as void*) is not NULL, the next step calls

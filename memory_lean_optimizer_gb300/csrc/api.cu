@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <thread>
 #include <vector>
@@ -47,8 +48,16 @@ unsigned grid_for(int64_t units) {
     return (unsigned)(blocks < 1 ? 1 : blocks);
 }
 
-// Bounded host wait: polls the event until it completes or `timeout_s` passes.
+bool fault_injected(const char* what) {
+    const char* f = std::getenv("LMOPT_FAULT_INJECT");
+    return f && std::strcmp(f, what) == 0;
+}
+
+// Bounded host wait: polls the event until it completes or `timeout_s` passes.  With
+// LMOPT_FAULT_INJECT=timeout every wait runs out at once (tests of the error path; nothing on
+// the GPU is disturbed).
 int wait_event(cudaEvent_t ev, double timeout_s, const char* what) {
+    if (fault_injected("timeout")) return set_error(OPTIM_ETIMEOUT, "%s: no completion (injected timeout)", what);
     auto t0 = std::chrono::steady_clock::now();
     for (;;) {
         cudaError_t e = cudaEventQuery(ev);
@@ -87,7 +96,8 @@ static void group_free(optim_group* g) {
     delete g;
 }
 
-static int check_device(const optim_group* g) {
+namespace lmo {
+int check_group_device(const optim_group* g) {
     int dev = -1;
     int rc = check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
     if (rc) return rc;
@@ -95,6 +105,14 @@ static int check_device(const optim_group* g) {
         return set_error(OPTIM_EINVAL, "group was created on device %d but device %d is current", g->device, dev);
     return OPTIM_OK;
 }
+
+// Bounded wait for the work of the group's last step call (on the stream it was enqueued on).
+int sync_group(optim_group* g) {
+    int rc = check_cuda(cudaEventRecord(g->sync_ev, g->last_stream), "sync event");
+    if (rc) return rc;
+    return wait_event(g->sync_ev, kWaitTimeout, "group stream");
+}
+}  // namespace lmo
 
 static int validate_desc(const optim_tensor_desc_t& d, int32_t i, int32_t kind) {
     if (d.numel < 0) return set_error(OPTIM_EINVAL, "tensor %d: numel %lld < 0", i, (long long)d.numel);
@@ -116,7 +134,7 @@ static int validate_desc(const optim_tensor_desc_t& d, int32_t i, int32_t kind) 
         size_t a = d.numel <= kSmall ? 4 : 2;
         if (!is_aligned(d.m, a) || !is_aligned(d.v, a))
             return set_error(OPTIM_EALIGN, "tensor %d: m/v not %zu-byte aligned", i, a);
-    } else if (kind == OPTIM_KIND_ADAN) {
+    } else if (kind == OPTIM_KIND_ADAN || kind == OPTIM_KIND_ADAN_F24) {
         if (!d.m || !d.v) return set_error(OPTIM_EINVAL, "tensor %d: Adan state or previous gradient is NULL", i);
         if (!is_aligned(d.m, 4) || !is_aligned(d.v, 2))
             return set_error(OPTIM_EALIGN, "tensor %d: Adan buffers not aligned", i);
@@ -179,7 +197,7 @@ int optim_group_create(const optim_tensor_desc_t* tensors, int32_t n, int32_t ki
     *out = nullptr;
     if (!tensors || n < 1) return set_error(OPTIM_EINVAL, "need n >= 1 tensors");
     if (kind != OPTIM_KIND_NADAM && kind != OPTIM_KIND_FACTORED && kind != OPTIM_KIND_NADAM_F24 &&
-        kind != OPTIM_KIND_ADAN)
+        kind != OPTIM_KIND_ADAN && kind != OPTIM_KIND_ADAN_F24)
         return set_error(OPTIM_EINVAL, "unknown group kind %d", kind);
     for (int32_t i = 0; i < n; ++i) {
         int rc = validate_desc(tensors[i], i, kind);
@@ -205,7 +223,7 @@ int optim_group_create(const optim_tensor_desc_t* tensors, int32_t n, int32_t ki
             r.flags = (d.numel <= kSmall ? kFlagSmall : 0) | (d.res_u16 ? kFlagRes : 0);
             r.pad = 0;
         }
-        if (kind == OPTIM_KIND_NADAM || kind == OPTIM_KIND_NADAM_F24 || kind == OPTIM_KIND_ADAN) {
+        if (kind != OPTIM_KIND_FACTORED) {
             // a group whose kChunk-element chunks would not give every SM two CTAs is cut finer
             // (down to kChunkMin): the launch-bound small case then spreads over the whole GPU
             auto count = [&](int64_t ch) {
@@ -273,7 +291,7 @@ int optim_step_nadam_begin(optim_group_t* g, const void* const* grads, int64_t s
         (hp->stochastic_rounding != 0 && hp->stochastic_rounding != 1))
         return set_error(OPTIM_EINVAL, "invalid NAdam hyper-parameters (wd_mode must be 0 or 1)");
     if (exchange && !is_aligned(exchange, 4)) return set_error(OPTIM_EALIGN, "exchange buffer not 4-byte aligned");
-    int rc = check_device(g);
+    int rc = check_group_device(g);
     if (!rc) rc = validate_grads(g, grads);
     if (rc) return rc;
 
@@ -332,7 +350,7 @@ int optim_step_nadam_end(optim_group_t* g, const float* exchange, void* stream) 
     if (!g) return set_error(OPTIM_EINVAL, "group is NULL");
     if (!g->pending) return set_error(OPTIM_ESTATE, "no NAdam step was begun on this group");
     if (exchange && !is_aligned(exchange, 4)) return set_error(OPTIM_EALIGN, "exchange buffer not 4-byte aligned");
-    int rc = check_device(g);
+    int rc = check_group_device(g);
     if (rc) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const NadamScalars& k = g->pending_k;
@@ -360,7 +378,7 @@ int optim_step_nadam_kahan(optim_group_t* g, const void* const* grads, int64_t s
 int optim_step_adan(optim_group_t* g, const void* const* grads, int64_t step, const optim_adan_hparams_t* hp,
                     void* stream) {
     if (!g || !hp) return set_error(OPTIM_EINVAL, "group or hparams is NULL");
-    if (g->kind != OPTIM_KIND_ADAN) return set_error(OPTIM_EINVAL, "not an ADAN group");
+    if (g->kind != OPTIM_KIND_ADAN && g->kind != OPTIM_KIND_ADAN_F24) return set_error(OPTIM_EINVAL, "not an ADAN group");
     if (step != g->last_step + 1)
         return set_error(OPTIM_EINVAL, "step %lld but the group expects %lld", (long long)step,
                          (long long)(g->last_step + 1));
@@ -369,7 +387,7 @@ int optim_step_adan(optim_group_t* g, const void* const* grads, int64_t step, co
         !finite_nonneg(hp->eps) || !finite_nonneg(hp->weight_decay) ||
         (hp->stochastic_rounding != 0 && hp->stochastic_rounding != 1))
         return set_error(OPTIM_EINVAL, "invalid Adan hyper-parameters");
-    int rc = check_device(g);
+    int rc = check_group_device(g);
     if (!rc) rc = validate_grads(g, grads);
     if (rc) return rc;
     AdanScalars k{};
@@ -388,12 +406,18 @@ int optim_step_adan(optim_group_t* g, const void* const* grads, int64_t step, co
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     rc = upload_grads(g, grads, s);
     if (rc) return rc;
-    NadamLaunch L{g->d_tensors, g->d_grads, g->d_scales, g->d_chunks, g->d_nonfinite, g->n_chunks_large,
-                  g->n_chunks_total, 0, nullptr, g->chunk};
+    const TensorRec* table = g->d_tensors;
+    if (g->offload) {
+        rc = offload_step_begin(g, s, &table);
+        if (rc) return rc;
+    }
+    NadamLaunch L{table, g->d_grads, g->d_scales, g->d_chunks, g->d_nonfinite, g->n_chunks_large,
+                  g->n_chunks_total, g->kind == OPTIM_KIND_ADAN_F24, nullptr, g->chunk};
     rc = launch_adan_step(L, k, s);
     if (rc) return rc;
     g->last_step = step;
     g->last_stream = s;
+    if (g->offload) return offload_step_end(g, s);
     return OPTIM_OK;
 }
 
@@ -411,7 +435,7 @@ int optim_step_factored(optim_group_t* g, const void* const* grads, int64_t step
         return set_error(OPTIM_EINVAL, "invalid factored hyper-parameters");
     if (g->prodigy && hp->mode != 1)
         return set_error(OPTIM_EINVAL, "a group attached to a Prodigy controller steps in mode 1");
-    int rc = check_device(g);
+    int rc = check_group_device(g);
     if (!rc) rc = validate_grads(g, grads);
     if (rc) return rc;
 
@@ -438,16 +462,11 @@ int optim_step_factored(optim_group_t* g, const void* const* grads, int64_t step
     return OPTIM_OK;
 }
 
-static int sync_group(optim_group* g) {
-    int rc = check_cuda(cudaEventRecord(g->sync_ev, g->last_stream), "sync event");
-    if (rc) return rc;
-    return wait_event(g->sync_ev, kWaitTimeout, "group stream");
-}
 
 int optim_query_scales(optim_group_t* g, float* host_out) {
     if (!g || !host_out) return set_error(OPTIM_EINVAL, "group or output is NULL");
     if (g->kind != OPTIM_KIND_NADAM) return set_error(OPTIM_EINVAL, "not a NADAM group");
-    int rc = check_device(g);
+    int rc = check_group_device(g);
     if (!rc) rc = sync_group(g);
     if (rc) return rc;
     std::vector<ScaleRec> recs(g->n);
@@ -471,7 +490,7 @@ int optim_set_scales(optim_group_t* g, const float* host_in) {
     if (!g || !host_in) return set_error(OPTIM_EINVAL, "group or input is NULL");
     if (g->kind != OPTIM_KIND_NADAM) return set_error(OPTIM_EINVAL, "not a NADAM group");
     if (g->pending) return set_error(OPTIM_ESTATE, "a NAdam step was begun and not ended");
-    int rc = check_device(g);
+    int rc = check_group_device(g);
     if (!rc) rc = sync_group(g);
     if (rc) return rc;
     std::vector<ScaleRec> recs(g->n, ScaleRec{});
@@ -512,7 +531,7 @@ int optim_group_set_profile_event(optim_group_t* g, void* event) {
 
 int optim_query_nonfinite(optim_group_t* g, uint64_t* count) {
     if (!g || !count) return set_error(OPTIM_EINVAL, "NULL argument");
-    int rc = check_device(g);
+    int rc = check_group_device(g);
     if (!rc) rc = sync_group(g);
     if (rc) return rc;
     unsigned long long c = 0;

@@ -143,6 +143,18 @@ __device__ __forceinline__ uint32_t enc_v(float sv, float rv) { return enc_v_bit
 __device__ __forceinline__ uint32_t pack_lo16(uint32_t e0, uint32_t e1) { return __byte_perm(e0, e1, 0x5410); }
 __device__ __forceinline__ uint32_t pack_hi16(uint32_t e0, uint32_t e1) { return __byte_perm(e0, e1, 0x7632); }
 
+// ---- f24 storage: the upper 24 bits of an fp32 value, as a plane of n upper 16-bit words,
+// zero padding up to byte 2n rounded up to 16, then a plane of n bytes (bits 8..15) ----
+__device__ __forceinline__ int64_t f24_lo_offset(int64_t n) { return (2 * n + 15) & ~(int64_t)15; }
+// Bytes between consecutive f24 buffers of one allocation (Adan's m, v, n): the buffer's bytes
+// rounded up to 16, so that every buffer starts 16-byte aligned.
+__device__ __forceinline__ int64_t f24_stride(int64_t n) { return (f24_lo_offset(n) + n + 15) & ~(int64_t)15; }
+__device__ __forceinline__ float f24_value(uint32_t hi16, uint32_t lo8) { return __uint_as_float((hi16 << 16) | (lo8 << 8)); }
+// Bits 8..15 of four fp32 patterns, packed into one word (element 0 in the low byte).
+__device__ __forceinline__ uint32_t pack_byte1(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+    return __byte_perm(__byte_perm(b0, b1, 0x0051), __byte_perm(b2, b3, 0x0051), 0x5410);
+}
+
 // ---- block reductions (kThreads threads) ----
 __device__ __forceinline__ uint32_t warp_max_u32(uint32_t x) {
 #pragma unroll

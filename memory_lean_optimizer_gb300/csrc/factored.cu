@@ -1207,7 +1207,8 @@ struct PlanLayout {
     int64_t rowpart = 0, colpart = 0, cc = 0, ss = 0, mats = 0, rbarpart = 0;
 };
 
-static void plan_layout(const std::vector<optim_tensor_desc_t>& desc, PlanLayout& L) {
+// Per-tensor classes and scratch offsets (no work items yet).
+static void plan_tensors(const std::vector<optim_tensor_desc_t>& desc, PlanLayout& L) {
     const int32_t n = (int32_t)desc.size();
     L.ts.assign(n, FTensor{});
     for (int32_t i = 0; i < n; ++i) {
@@ -1255,6 +1256,23 @@ static void plan_layout(const std::vector<optim_tensor_desc_t>& desc, PlanLayout
         t.ss_off = L.ss;
         L.ss += t.ss_cnt;
     }
+}
+
+// Work items of one tensor planned by plan_tensors: statistics / RMS / update items, finalize items.
+static void item_counts(const FTensor& t, int64_t& items, int64_t& fin) {
+    items = fin = 0;
+    if (t.numel == 0) return;
+    if (t.cls == kWide) {
+        items = t.B * t.nbands * t.ncb;
+        fin = t.B * (t.n_rowitems + (t.C + kFinColsPerItem - 1) / kFinColsPerItem);
+    } else {
+        items = t.ss_cnt;
+    }
+}
+
+// Waves and work items over the tensors planned by plan_tensors.
+static void plan_waves(PlanLayout& L) {
+    const int32_t n = (int32_t)L.ts.size();
     // waves: consecutive tensors, at most kWaveGradBytes of gradients each (the L2-resident
     // target), balanced so that no wave is much smaller than the others: the group's gradient
     // bytes are split into ceil(total / kWaveGradBytes) near-equal targets
@@ -1297,6 +1315,11 @@ static void plan_layout(const std::vector<optim_tensor_desc_t>& desc, PlanLayout
         L.waves.push_back(wv);
         i = j;
     }
+}
+
+static void plan_layout(const std::vector<optim_tensor_desc_t>& desc, PlanLayout& L) {
+    plan_tensors(desc, L);
+    plan_waves(L);
 }
 
 int factored_plan_build(FactoredPlan*& plan, const std::vector<optim_tensor_desc_t>& desc) {
@@ -1489,19 +1512,24 @@ extern "C" int optim_step_factored_noalloc(const optim_tensor_desc_t* tensor, co
     if (!is_aligned(d.w_bf16, 2) || (d.res_u16 && !is_aligned(d.res_u16, 2)) || !is_aligned(grad_bf16, 2) ||
         !is_aligned(d.v, 4) || (d.m && !is_aligned(d.m, 4)))
         return set_error(OPTIM_EALIGN, "a buffer is not aligned to its element size");
-    if (!(hp->lr >= 0.0f) || !std::isfinite(hp->lr) || !(hp->clip_threshold > 0.0f) || !std::isfinite(hp->clip_threshold) ||
-        !(hp->weight_decay >= 0.0f) || !std::isfinite(hp->weight_decay) || !(hp->eps1 >= 0.0f) || !(hp->eps2 >= 0.0f) ||
+    // the same checks as optim_step_factored (finite, non-negative lr, decay, eps1, eps2, d)
+    auto finite_nonneg = [](float x) { return std::isfinite(x) && x >= 0.0f; };
+    if (!finite_nonneg(hp->lr) || !(hp->clip_threshold > 0.0f) || !std::isfinite(hp->clip_threshold) ||
+        !finite_nonneg(hp->weight_decay) || !finite_nonneg(hp->eps1) || !finite_nonneg(hp->eps2) ||
         (hp->mode != 0 && hp->mode != 1) || !std::isfinite(hp->decay_rate) ||
-        (hp->mode == 1 && (!(hp->beta2 >= 0.0f && hp->beta2 < 1.0f) || !(hp->d >= 0.0f) || !std::isfinite(hp->d))))
+        (hp->mode == 1 && (!(hp->beta2 >= 0.0f && hp->beta2 < 1.0f) || !finite_nonneg(hp->d))))
         return set_error(OPTIM_EINVAL, "invalid factored hyper-parameters");
 
-    // layout of this tensor's plan inside the fixed scratch
+    // layout of this tensor's plan inside the fixed scratch, sized from the tensor's shape before
+    // any work item is built (an oversized tensor is rejected without building its tables)
     PlanLayout L;
-    plan_layout(std::vector<optim_tensor_desc_t>(1, d), L);
+    plan_tensors(std::vector<optim_tensor_desc_t>(1, d), L);
+    int64_t n_items = 0, n_fin = 0;
+    item_counts(L.ts[0], n_items, n_fin);
     size_t off = 0;
     const size_t o_ts = carve(off, sizeof(FTensor));
-    const size_t o_items = carve(off, L.items.size() * sizeof(Item));
-    const size_t o_fin = carve(off, L.fin.size() * sizeof(Item));
+    const size_t o_items = carve(off, (size_t)n_items * sizeof(Item));
+    const size_t o_fin = carve(off, (size_t)n_fin * sizeof(Item));
     const size_t o_grad = carve(off, sizeof(void*));
     const size_t o_rowpart = carve(off, (size_t)L.rowpart * 4), o_colpart = carve(off, (size_t)L.colpart * 4);
     const size_t o_cc = carve(off, (size_t)L.cc * 4), o_rbar = carve(off, (size_t)L.mats * 4);
@@ -1510,6 +1538,9 @@ extern "C" int optim_step_factored_noalloc(const optim_tensor_desc_t* tensor, co
     if (off > kNoAllocScratchBytes)
         return set_error(OPTIM_EINVAL, "tensor of %lld elements needs %zu bytes of scratch; the fixed no-alloc scratch holds %zu",
                          (long long)d.numel, off, kNoAllocScratchBytes);
+    plan_waves(L);
+    if ((int64_t)L.items.size() != n_items || (int64_t)L.fin.size() != n_fin)
+        return set_error(OPTIM_EINVAL, "internal: work-item count differs from its estimate");
 
     void* base = nullptr;
     int rc = noalloc_scratch(&base);

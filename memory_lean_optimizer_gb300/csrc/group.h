@@ -59,6 +59,10 @@ namespace lmo {
 // are (being) copied into a staging slot, make `compute` wait for that copy, and return the
 // device tensor table that points into the slot.  end: enqueue the write-back after the kernels.
 int offload_step_begin(optim_group* g, cudaStream_t compute, const TensorRec** table);
+// OPTIM_EINVAL unless the group's device is current.
+int check_group_device(const optim_group* g);
+// Bounded wait for the work of the group's last step call.
+int sync_group(optim_group* g);
 int offload_step_end(optim_group* g, cudaStream_t compute);
 void offload_unbind(optim_group* g);
 }  // namespace lmo

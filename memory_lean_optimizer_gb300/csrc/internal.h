@@ -10,6 +10,9 @@
 
 namespace lmo {
 
+// True when the environment variable LMOPT_FAULT_INJECT equals `what` (host-side fault
+// injection for the error-path tests: h2d, d2h, alloc, timeout).
+bool fault_injected(const char* what);
 // Records the thread-local error message and returns `code`.
 int set_error(int code, const char* fmt, ...);
 // OPTIM_OK if e == cudaSuccess, else records "<what>: <cuda message>" and returns OPTIM_ECUDA.

@@ -424,16 +424,10 @@ __global__ void __launch_bounds__(kThreads, 4) k_nadam_step(NadamLaunch L, Prm k
 
 // ------------------------------------------------------------------------------------ f24
 // f24 moments: the upper 24 bits of the fp32 moment (the f24 format of sd-scripts PR #2187,
-// third post: fp32 cut to its top three bytes, eight mantissa bits more than bf16), stored as a plane of n upper 16-bit words followed by a
-// plane of n bytes (bits 8..15).  Storage only: the update runs on the decoded fp32 values, and
+// third post: fp32 cut to its top three bytes, eight mantissa bits more than bf16), stored as a
+// plane of n upper 16-bit words followed by a plane of n bytes (bits 8..15; helpers in
+// common.cuh).  Storage only: the update runs on the decoded fp32 values, and
 // no scale (hence no gradient pre-pass) is needed.  22 bytes per element per step.
-__device__ __forceinline__ int64_t f24_lo_offset(int64_t n) { return (2 * n + 15) & ~(int64_t)15; }
-__device__ __forceinline__ float f24_value(uint32_t hi16, uint32_t lo8) { return __uint_as_float((hi16 << 16) | (lo8 << 8)); }
-
-// Bits 8..15 of four fp32 patterns, packed into one word (element 0 in the low byte).
-__device__ __forceinline__ uint32_t pack_byte1(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
-    return __byte_perm(__byte_perm(b0, b1, 0x0051), __byte_perm(b2, b3, 0x0051), 0x5410);
-}
 
 template <bool kSR>
 __device__ __forceinline__ void step8_f24(const Prm& k, bool has_res, uint32_t tensor, int64_t i0, uint4& W, uint4& R,

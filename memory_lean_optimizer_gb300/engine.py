@@ -96,6 +96,35 @@ class _Group:
         except Exception:
             pass
 
+    # attribute names of the (residual, m, v) state lists, in the order of optim_offload_layout
+    _state_attrs = ("res", "m", "v")
+
+    def attach_host(self):
+        """Moves the group's residuals and states into one pinned host image (optim_group_attach_host);
+        afterwards each step needs prefetch() before and writeback() after it, and the state lists
+        of this object are views into the image (valid once the write-back has completed)."""
+        total, offs = lmopt.optim_offload_layout(self.handle, len(self.weights))
+        image = torch.zeros(max(total, 1), dtype=torch.uint8, pin_memory=True)
+        lmopt.optim_group_attach_host(self.handle, image.data_ptr(), total)
+        self.image = image
+        for k, name in enumerate(self._state_attrs):
+            views = []
+            for i, t in enumerate(getattr(self, name)):
+                if t is None or offs[i][k] < 0:
+                    views.append(t if t is None else t.cpu())
+                    continue
+                nbytes = t.numel() * t.element_size()
+                views.append(image[offs[i][k]:offs[i][k] + nbytes].view(t.dtype).view(t.shape))
+            setattr(self, name, views)     # the device buffers are no longer used: dropped here
+
+    def prefetch(self, stream=None):
+        """Copy-in of an offloaded group's states (stream None: the library's own copy stream)."""
+        lmopt.optim_offload_prefetch(self.handle, 0 if stream is None else int(stream.cuda_stream))
+
+    def writeback(self, stream=None):
+        """Copy-out after the last step of a group attached with attach_host()."""
+        lmopt.optim_offload_writeback(self.handle, 0 if stream is None else int(stream.cuda_stream))
+
     def _grad_ptrs(self, grads):
         assert len(grads) == len(self.weights)
         ptrs = []
@@ -109,23 +138,39 @@ def _round256(x: int) -> int:
     return (x + 255) & ~255
 
 
-def offload_slot_bytes(numels: Sequence[int], kahan: bool = True) -> int:
-    """Staging bytes one offloaded NADAM group of tensors with these sizes needs in a slot."""
+def offload_slot_bytes(numels: Sequence[int], kahan: bool = True, kind: int = lmopt.OPTIM_KIND_NADAM) -> int:
+    """Staging bytes one offloaded group of tensors with these sizes needs in a slot (the layout
+    of optim_offload_layout: residual, m, v per tensor, each at a 256-byte boundary)."""
     tot = 0
     for n in numels:
-        sm = (4 if n <= SMALL else 2) * n
-        tot += (_round256(2 * n) if kahan else 0) + 2 * _round256(sm)
+        if n == 0:
+            continue
+        small = n <= SMALL
+        f24 = (2 * n + 15) // 16 * 16 + n
+        if kind == lmopt.OPTIM_KIND_NADAM:
+            m = v = (4 if small else 2) * n
+        elif kind == lmopt.OPTIM_KIND_NADAM_F24:
+            m = v = 4 * n if small else f24
+        else:
+            m = 12 * ((n + 3) // 4 * 4) if (small or kind == lmopt.OPTIM_KIND_ADAN) else 3 * adan_f24_stride(n)
+            v = 2 * n
+        tot += (_round256(2 * n) if kahan else 0) + _round256(m) + _round256(v)
     return tot
 
 
 class OffloadEngine:
-    """Device staging ring + copy streams for groups whose states live in pinned host memory."""
+    """Device staging ring + copy streams for groups whose states live in pinned host memory
+    (None: the library's own ring of the current device, used by attach_host groups)."""
 
     def __init__(self, slot_bytes: int, n_slots: int = 3):
         self.handle = lmopt.optim_offload_create(int(slot_bytes), int(n_slots))
 
     def sync(self):
         return lmopt.optim_offload_sync(self.handle)
+
+    @staticmethod
+    def sync_library_ring():
+        return lmopt.optim_offload_sync(None)
 
     def close(self):
         if self.handle:
@@ -158,7 +203,7 @@ class NadamGroup(_Group):
             assert w.dtype == torch.bfloat16 and w.is_cuda and w.is_contiguous()
         dev = self.weights[0].device
         pinned = offload is not None
-        assert states in ("u16", "f24") and not (pinned and states == "f24")
+        assert states in ("u16", "f24")
         self.kind = lmopt.OPTIM_KIND_NADAM_F24 if states == "f24" else lmopt.OPTIM_KIND_NADAM
         if residuals is None:
             residuals = [_state_buffer(w.numel(), torch.int16, dev, pinned) if kahan else None for w in self.weights]
@@ -173,8 +218,8 @@ class NadamGroup(_Group):
                 self.v.append(_state_buffer(n, torch.float32, dev, pinned))
             elif states == "f24":       # n upper 16-bit words, padding to 16 B, n low bytes, all zero
                 nbytes = (2 * n + 15) // 16 * 16 + n
-                self.m.append(torch.zeros(nbytes, dtype=torch.uint8, device=dev))
-                self.v.append(torch.zeros(nbytes, dtype=torch.uint8, device=dev))
+                self.m.append(_state_buffer(nbytes, torch.uint8, dev, pinned))
+                self.v.append(_state_buffer(nbytes, torch.uint8, dev, pinned))
             else:
                 self.m.append(_state_buffer(n, torch.int16, dev, pinned, 32768))
                 self.v.append(_state_buffer(n, torch.int16, dev, pinned, 0))
@@ -183,9 +228,6 @@ class NadamGroup(_Group):
         self.offload = offload
         if offload is not None:
             lmopt.optim_group_attach_offload(self.handle, offload.handle)
-
-    def prefetch(self):
-        lmopt.optim_offload_prefetch(self.handle)
 
     @classmethod
     def from_masters(cls, masters: Sequence[torch.Tensor], stream=None, offload: OffloadEngine | None = None,
@@ -346,34 +388,57 @@ class ProdigyController:
             pass
 
 
+def adan_f24_stride(n: int) -> int:
+    """Bytes between the m, v and n f24 buffers of an ADAN_F24 state: f24 bytes rounded up to 16."""
+    return ((2 * n + 15) // 16 * 16 + n + 15) // 16 * 16
+
+
 class AdanGroup(_Group):
-    """Adan state (fp32 m, v, n planes and the previous bf16 gradient) for a list of bf16 weights."""
+    """Adan state (m, v, n and the previous bf16 gradient) for a list of bf16 weights: fp32 planes,
+    or with states="f24" three f24 buffers for tensors above 4096 elements.  With `offload`
+    (an OffloadEngine) the residuals and states live in pinned host memory."""
 
     kind = lmopt.OPTIM_KIND_ADAN
+    _state_attrs = ("res", "mvn", "gprev")
 
     def __init__(self, weights: Sequence[torch.Tensor], residuals: Sequence[torch.Tensor] | None = None,
-                 kahan: bool = True):
+                 kahan: bool = True, states: str = "fp32", offload: OffloadEngine | None = None):
         super().__init__()
+        assert states in ("fp32", "f24")
+        self.kind = lmopt.OPTIM_KIND_ADAN_F24 if states == "f24" else lmopt.OPTIM_KIND_ADAN
         self.weights = list(weights)
         dev = self.weights[0].device
+        pinned = offload is not None
         if residuals is None:
-            residuals = [_u16_empty(w.numel(), dev, 0) if kahan else None for w in self.weights]
+            residuals = [_state_buffer(w.numel(), torch.int16, dev, pinned) if kahan else None for w in self.weights]
+        elif pinned:
+            residuals = [r.cpu().pin_memory() if r is not None else None for r in residuals]
         self.res = list(residuals)
-        # planes m, v, n, each numel rounded up to a multiple of 4 floats (16-byte aligned planes)
-        self.mvn = [torch.zeros(3 * ((w.numel() + 3) // 4 * 4), dtype=torch.float32, device=dev)
-                    for w in self.weights]
-        self.gprev = [torch.zeros(w.numel(), dtype=torch.int16, device=dev) for w in self.weights]
+        # planes m, v, n, each numel rounded up to a multiple of 4 floats (16-byte aligned planes);
+        # f24: three f24 buffers of adan_f24_stride bytes each
+        self.mvn = []
+        for w in self.weights:
+            n = w.numel()
+            if states == "f24" and n > SMALL:
+                self.mvn.append(_state_buffer(3 * adan_f24_stride(n), torch.uint8, dev, pinned))
+            else:
+                self.mvn.append(_state_buffer(3 * ((n + 3) // 4 * 4), torch.float32, dev, pinned))
+        self.gprev = [_state_buffer(w.numel(), torch.int16, dev, pinned) for w in self.weights]
         descs = [_desc(w, r, m, v, w.shape) for w, r, m, v in zip(self.weights, self.res, self.mvn, self.gprev)]
         self.handle = lmopt.optim_group_create(descs, self.kind)
+        self.offload = offload
+        if offload is not None:
+            lmopt.optim_group_attach_offload(self.handle, offload.handle)
 
     @classmethod
-    def from_masters(cls, masters: Sequence[torch.Tensor], stream=None):
+    def from_masters(cls, masters: Sequence[torch.Tensor], stream=None, states: str = "fp32",
+                     offload: OffloadEngine | None = None):
         ws, rs = [], []
         for x in masters:
             hi, lo = kahan_split(x.contiguous(), stream=stream)
             ws.append(hi)
             rs.append(lo)
-        return cls(ws, rs)
+        return cls(ws, rs, states=states, offload=offload)
 
     def step(self, grads: Sequence[torch.Tensor], hp: dict, stream=None):
         h = lmopt.AdanHparams(lr=hp["lr"], beta1=hp.get("beta1", 0.02), beta2=hp.get("beta2", 0.08),
@@ -384,4 +449,4 @@ class AdanGroup(_Group):
         self.step_count += 1
 
     def masters(self):
-        return [kahan_merge(w, r) for w, r in zip(self.weights, self.res)]
+        return [kahan_merge(w, r.to(w.device)) for w, r in zip(self.weights, self.res)]

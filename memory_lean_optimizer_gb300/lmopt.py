@@ -26,6 +26,7 @@ OPTIM_KIND_NADAM = 0
 OPTIM_KIND_FACTORED = 1
 OPTIM_KIND_NADAM_F24 = 2
 OPTIM_KIND_ADAN = 3
+OPTIM_KIND_ADAN_F24 = 4
 SMALL_NUMEL = 4096
 
 ERROR_NAMES = {OPTIM_EINVAL: "EINVAL", OPTIM_ECUDA: "ECUDA", OPTIM_ENOMEM: "ENOMEM", OPTIM_EALIGN: "EALIGN",
@@ -38,7 +39,8 @@ EXPORTED = (
     "optim_query_nonfinite", "optim_group_set_profile_event", "optim_last_error",
     "optim_step_factored_noalloc", "optim_step_adan",
     "optim_offload_create", "optim_offload_destroy", "optim_group_attach_offload",
-    "optim_offload_prefetch", "optim_offload_sync", "optim_step_nadam_begin", "optim_step_nadam_end",
+    "optim_offload_prefetch", "optim_offload_sync", "optim_offload_writeback", "optim_group_attach_host",
+    "optim_offload_layout", "optim_step_nadam_begin", "optim_step_nadam_end",
     "optim_prodigy_create", "optim_prodigy_destroy", "optim_prodigy_slice_len", "optim_group_attach_prodigy",
     "optim_prodigy_end_step", "optim_prodigy_get", "optim_prodigy_set", "optim_prodigy_reduce",
     "optim_prodigy_finish",
@@ -113,7 +115,10 @@ def load(path: str = LIB_PATH):
             "optim_offload_create": [ctypes.c_size_t, I32, ctypes.POINTER(P)],
             "optim_offload_destroy": [P],
             "optim_group_attach_offload": [P, P],
-            "optim_offload_prefetch": [P],
+            "optim_offload_prefetch": [P, P],
+            "optim_offload_writeback": [P, P],
+            "optim_group_attach_host": [P, P, ctypes.c_size_t],
+            "optim_offload_layout": [P, ctypes.POINTER(I64), ctypes.POINTER(I64)],
             "optim_offload_sync": [P, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)],
             "optim_prodigy_create": [ctypes.c_double, F, I32, ctypes.POINTER(P)],
             "optim_prodigy_destroy": [P],
@@ -260,12 +265,31 @@ def optim_group_attach_offload(handle: int, engine: int) -> None:
     check(load().optim_group_attach_offload(handle, engine))
 
 
-def optim_offload_prefetch(handle: int) -> None:
-    check(load().optim_offload_prefetch(handle))
+def optim_offload_prefetch(handle: int, copy_stream: int = 0) -> None:
+    """Copy-in of an offloaded group's states on `copy_stream` (0: the library's own H2D stream)."""
+    check(load().optim_offload_prefetch(handle, copy_stream))
 
 
-def optim_offload_sync(engine: int):
-    """Returns (bytes copied host->device, bytes copied device->host) so far."""
+def optim_offload_writeback(handle: int, copy_stream: int = 0) -> None:
+    """Copy-out after the group's last step on `copy_stream` (0: the library's own D2H stream)."""
+    check(load().optim_offload_writeback(handle, copy_stream))
+
+
+def optim_offload_layout(handle: int, n_tensors: int):
+    """(total bytes of the group's host image, [(res, m, v) byte offsets per tensor, -1 if absent])."""
+    offs = (ctypes.c_int64 * max(1, 3 * n_tensors))()
+    total = ctypes.c_int64()
+    check(load().optim_offload_layout(handle, offs, ctypes.byref(total)))
+    return total.value, [tuple(offs[3 * i:3 * i + 3]) for i in range(n_tensors)]
+
+
+def optim_group_attach_host(handle: int, image_ptr: int, nbytes: int) -> None:
+    check(load().optim_group_attach_host(handle, image_ptr, nbytes))
+
+
+def optim_offload_sync(engine: int | None):
+    """Returns (bytes copied host->device, bytes copied device->host) so far; engine None: the
+    library's own staging ring of the current device."""
     a, b = ctypes.c_uint64(), ctypes.c_uint64()
     check(load().optim_offload_sync(engine, ctypes.byref(a), ctypes.byref(b)))
     return a.value, b.value

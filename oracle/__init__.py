@@ -40,21 +40,32 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
-_CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-Wall"]
+_LIB_MT_PATH = os.path.join(_OUT_DIR, "liboracle_mt.so")
+_CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-Wall",
+           "-Wno-unknown-pragmas"]
 
 _lock = threading.Lock()
 _lib = None
+_lib_mt = None
 
 SMALL_NUMEL = 4096
 
 
 def build(force: bool = False) -> str:
-    """Compile oracle.c into oracle/_build/liboracle.so (gcc); returns the path."""
+    """Compile oracle.c into oracle/_build/liboracle.so (gcc, single-threaded: the parity
+    reference) and, from the same source with OpenMP, liboracle_mt.so (its threaded timing driver;
+    without OpenMP in the compiler it is built single-threaded); returns the first path."""
     os.makedirs(_OUT_DIR, exist_ok=True)
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
-        tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", *_CFLAGS, "-o", tmp, _SRC, "-lm"])
-        os.replace(tmp, _LIB_PATH)
+    for path, extra in ((_LIB_PATH, []), (_LIB_MT_PATH, ["-fopenmp"])):
+        if force or not os.path.exists(path) or os.path.getmtime(path) < os.path.getmtime(_SRC):
+            tmp = path + f".tmp{os.getpid()}"
+            try:
+                subprocess.check_call(["gcc", *_CFLAGS, *extra, "-o", tmp, _SRC, "-lm"])
+            except subprocess.CalledProcessError:
+                if not extra:
+                    raise
+                subprocess.check_call(["gcc", *_CFLAGS, "-o", tmp, _SRC, "-lm"])
+            os.replace(tmp, path)
     return _LIB_PATH
 
 
@@ -118,6 +129,9 @@ def _load():
             "orc_adan_scalars": (None, [F, F, F, F, F, F, ctypes.POINTER(AdanScalars)]),
             "orc_adan_step_tensor": (None, [P, P, P, P, P, I64, I64, ctypes.POINTER(AdanScalars), I32,
                                             ctypes.c_uint64, ctypes.c_uint32]),
+            "orc_adan_step_tensor_f24": (None, [P, P, P, P, P, I64, I64, ctypes.POINTER(AdanScalars), I32,
+                                                ctypes.c_uint64, ctypes.c_uint32]),
+            "orc_adan_f24_stride": (I64, [I64]),
             "orc_sr_bits": (ctypes.c_uint32, [ctypes.c_uint64, ctypes.c_uint32, I64, I64]),
             "orc_stochastic_round": (None, [P, P, I64, ctypes.c_uint64, ctypes.c_uint32, I64]),
             "orc_nadam_step_tensor_sr": (None, [P, P, P, P, I64, ctypes.POINTER(Scale), ctypes.POINTER(NadamScalars),
@@ -140,6 +154,26 @@ def _load():
             fn.argtypes = args
         _lib = lib
         return lib
+
+
+def _load_mt():
+    global _lib_mt
+    with _lock:
+        if _lib_mt is None:
+            build()
+            lib = ctypes.CDLL(_LIB_MT_PATH)
+            lib.orc_threads.argtypes = []
+            lib.orc_threads.restype = ctypes.c_int32
+            lib.orc_nadam_group_step_mt.argtypes = [ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                                    ctypes.POINTER(Scale), ctypes.POINTER(NadamScalars)]
+            lib.orc_nadam_group_step_mt.restype = None
+            _lib_mt = lib
+        return _lib_mt
+
+
+def threads() -> int:
+    """Threads the threaded timing driver uses (OpenMP's default: every host core)."""
+    return int(_load_mt().orc_threads())
 
 
 def _p(a: np.ndarray | None):
@@ -303,6 +337,26 @@ def adan_step_tensor(hi, lo, mnv, gprev, g, step, k: AdanScalars, sr=False, seed
                                  ctypes.byref(k), int(sr), seed, tensor)
 
 
+def adan_f24_stride(n: int) -> int:
+    """Bytes between the m, v and n f24 buffers of an Adan f24 state (f24 bytes of n, rounded up
+    to 16)."""
+    return int(_load().orc_adan_f24_stride(n))
+
+
+def adan_f24_nbytes(n: int) -> int:
+    """Bytes of an Adan f24 state buffer: three f24 buffers above 4096 elements, else the fp32
+    planes of adan_step_tensor."""
+    return 3 * adan_f24_stride(n) if n > SMALL_NUMEL else 12 * adan_plane(n)
+
+
+def adan_step_tensor_f24(hi, lo, buf, gprev, g, step, k: AdanScalars, sr=False, seed=0, tensor=0):
+    """In place, as adan_step_tensor, with m, v, n stored as f24 in `buf` (uint8,
+    adan_f24_nbytes(n) bytes; fp32 planes for 4096 or fewer elements)."""
+    assert buf.dtype == np.uint8 and buf.size == adan_f24_nbytes(hi.size)
+    _load().orc_adan_step_tensor_f24(_p(hi), _p(lo), _p(buf), _p(gprev), _p(_u16(g)), hi.size, int(step),
+                                     ctypes.byref(k), int(sr), seed, tensor)
+
+
 def f24_lo_offset(n: int) -> int:
     """Byte offset of the bits-8..15 plane in an f24 buffer: 2n rounded up to 16."""
     return (2 * n + 15) // 16 * 16
@@ -350,6 +404,27 @@ def nadam_group_step(tensors, grads, state: NadamState, t, hp):
         hp["wd_mode"] == 1, hp["nesterov"], hp["momentum_decay"], state.mu_product.value)
     for i, (tt, g) in enumerate(zip(tensors, grads)):
         nadam_step_tensor(tt["hi"], tt.get("lo"), tt["m"], tt["v"], g, state.scales[i], k)
+    return k
+
+
+def nadam_group_step_mt(tensors, grads, state: NadamState, t, hp):
+    """nadam_group_step on all host threads (the threaded timing driver of oracle.c): every
+    element is updated by the same single-threaded step function on a slice of its tensor, so the
+    results are bit-identical to nadam_group_step."""
+    k, state.mu_product.value = nadam_scalars(
+        t, hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"],
+        hp["wd_mode"] == 1, hp["nesterov"], hp["momentum_decay"], state.mu_product.value)
+    n = len(tensors)
+    ptrs = (ctypes.c_void_p * (5 * max(n, 1)))()
+    sizes = (ctypes.c_int64 * max(n, 1))()
+    keep = []
+    for i, (tt, g) in enumerate(zip(tensors, grads)):
+        g = _u16(g)
+        keep.append(g)
+        for j, a in enumerate((tt["hi"], tt.get("lo"), tt["m"], tt["v"], g)):
+            ptrs[5 * i + j] = _p(a)
+        sizes[i] = tt["hi"].size
+    _load_mt().orc_nadam_group_step_mt(n, ptrs, sizes, state.scales, ctypes.byref(k))
     return k
 
 

@@ -43,6 +43,7 @@
 #include <stdint.h>
 #include <string.h>
 #include <float.h>
+#include <stdlib.h>
 
 #define ORC_SMALL_NUMEL 4096
 
@@ -507,6 +508,39 @@ void orc_adan_scalars(float lr, float b1, float b2, float b3, float eps, float w
     k->inv_decay = (float)(1.0 / (1.0 + (double)lr * (double)wd));
 }
 
+static float adan_elem(float w, float gg, float gp, float* m, float* v, float* nn, int64_t step,
+                       const orc_adan_scalars_t* k)
+{
+    float d = gg - gp;
+    if (step == 1) {
+        *m = gg;
+        *v = 0.0f;
+        *nn = gg * gg;
+    } else {
+        *m = fmaf(k->omb1, *m, k->b1 * gg);
+        *v = step == 2 ? d : fmaf(k->omb2, *v, k->b2 * d);
+        float c = fmaf(k->omb2, d, gg);
+        *nn = fmaf(k->omb3, *nn, k->b3 * (c * c));
+    }
+    float den = sqrtf(*nn) + k->eps;
+    float u = fmaf(k->omb2, *v, *m);
+    return (w - k->lr * (u / den)) * k->inv_decay;
+}
+
+static void adan_store_w(uint16_t* hi, uint16_t* lo, int64_t i, float w, int32_t sr, uint64_t seed,
+                         uint32_t tensor, int64_t step)
+{
+    if (lo) {
+        uint32_t b = b_of(w);
+        hi[i] = (uint16_t)(b >> 16);
+        lo[i] = (uint16_t)(b & 0xFFFFu);
+    } else if (sr) {
+        hi[i] = sr_bf16(w, orc_sr_bits(seed, tensor, step, i));
+    } else {
+        hi[i] = rne_bf16(w);
+    }
+}
+
 void orc_adan_step_tensor(uint16_t* hi, uint16_t* lo, float* mnv, uint16_t* gprev, const uint16_t* g,
                           int64_t n, int64_t step, const orc_adan_scalars_t* k, int32_t sr, uint64_t seed,
                           uint32_t tensor)
@@ -517,36 +551,49 @@ void orc_adan_step_tensor(uint16_t* hi, uint16_t* lo, float* mnv, uint16_t* gpre
     float* nn = mnv + 2 * P;
     for (int64_t i = 0; i < n; ++i) {
         float w = lo ? f_of(((uint32_t)hi[i] << 16) | lo[i]) : bf16_to_f32(hi[i]);
-        float gg = bf16_to_f32(g[i]);
-        float gp = bf16_to_f32(gprev[i]);
-        float d = gg - gp;
-        float mm, vv, n2;
-        if (step == 1) {
-            mm = gg;
-            vv = 0.0f;
-            n2 = gg * gg;
-        } else {
-            mm = fmaf(k->omb1, m[i], k->b1 * gg);
-            vv = step == 2 ? d : fmaf(k->omb2, v[i], k->b2 * d);
-            float c = fmaf(k->omb2, d, gg);
-            n2 = fmaf(k->omb3, nn[i], k->b3 * (c * c));
-        }
-        float den = sqrtf(n2) + k->eps;
-        float u = fmaf(k->omb2, vv, mm);
-        w = (w - k->lr * (u / den)) * k->inv_decay;
+        float mm = m[i], vv = v[i], n2 = nn[i];
+        w = adan_elem(w, bf16_to_f32(g[i]), bf16_to_f32(gprev[i]), &mm, &vv, &n2, step, k);
         m[i] = mm;
         v[i] = vv;
         nn[i] = n2;
         gprev[i] = g[i];
-        if (lo) {
-            uint32_t b = b_of(w);
-            hi[i] = (uint16_t)(b >> 16);
-            lo[i] = (uint16_t)(b & 0xFFFFu);
-        } else if (sr) {
-            hi[i] = sr_bf16(w, orc_sr_bits(seed, tensor, step, i));
-        } else {
-            hi[i] = rne_bf16(w);
-        }
+        adan_store_w(hi, lo, i, w, sr, seed, tensor, step);
+    }
+}
+
+/* Adan with its three states stored as f24 (the compact storage the same page describes for the
+ * NAdam moments, applied to Adan's m, v and n, whose compression that page leaves open).  Each
+ * state is an f24 buffer as above (upper-16-bit plane, zero padding to 16 bytes, byte plane),
+ * padded to a multiple of 16 bytes; the three follow each other in `buf`, state j at byte
+ * j * F, F = f24 bytes of n rounded up to 16.  Tensors of 4096 or fewer elements keep the fp32
+ * planes of orc_adan_step_tensor.  As for the NAdam moments, the update computes on the
+ * decoded fp32 states and only the stored values are truncated. */
+int64_t orc_adan_f24_stride(int64_t n)
+{
+    return (((2 * n + 15) / 16) * 16 + n + 15) / 16 * 16;
+}
+
+void orc_adan_step_tensor_f24(uint16_t* hi, uint16_t* lo, uint8_t* buf, uint16_t* gprev, const uint16_t* g,
+                              int64_t n, int64_t step, const orc_adan_scalars_t* k, int32_t sr, uint64_t seed,
+                              uint32_t tensor)
+{
+    if (n <= ORC_SMALL_NUMEL) {
+        orc_adan_step_tensor(hi, lo, (float*)buf, gprev, g, n, step, k, sr, seed, tensor);
+        return;
+    }
+    const int64_t F = orc_adan_f24_stride(n);
+    uint8_t* mb = buf;
+    uint8_t* vb = buf + F;
+    uint8_t* nb = buf + 2 * F;
+    for (int64_t i = 0; i < n; ++i) {
+        float w = lo ? f_of(((uint32_t)hi[i] << 16) | lo[i]) : bf16_to_f32(hi[i]);
+        float mm = f24_load(mb, n, i), vv = f24_load(vb, n, i), n2 = f24_load(nb, n, i);
+        w = adan_elem(w, bf16_to_f32(g[i]), bf16_to_f32(gprev[i]), &mm, &vv, &n2, step, k);
+        f24_store(mb, n, i, mm);
+        f24_store(vb, n, i, vv);
+        f24_store(nb, n, i, n2);
+        gprev[i] = g[i];
+        adan_store_w(hi, lo, i, w, sr, seed, tensor, step);
     }
 }
 
@@ -811,4 +858,89 @@ void orc_prodigy_end_step(double* d, double* r, double beta3, double cdot, doubl
         double dhat = *r / l1;
         if (dhat > *d) *d = dhat;
     }
+}
+
+/* ----------------------------------------------------------------------------------------
+ * Timing driver: one NAdam group step spread over the host's threads.  It is not a second
+ * definition of the step: every element is updated by orc_nadam_step_slice, unchanged, on a
+ * contiguous slice of its tensor; only the per-tensor maxima are combined across slices
+ * (max over the slices of max |g|, and of A_m and A_v, which the step takes with fmax, so the
+ * result does not depend on how a tensor is cut).  The results are therefore bit-identical to
+ * orc_nadam_step_tensor on every tensor (checked by a test).  Built with OpenMP when the
+ * compiler has it (the same source, a second library); otherwise it runs on one thread.
+ * ptrs[5*i .. 5*i+4] = hi, lo (or NULL), m, v, g of tensor i; n[i] its element count.
+ * -------------------------------------------------------------------------------------- */
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+int32_t orc_threads(void)
+{
+#ifdef _OPENMP
+    return (int32_t)omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+#define ORC_SLICE (1 << 20)
+
+void orc_nadam_group_step_mt(int32_t n_tensors, void* const* ptrs, const int64_t* n, orc_scale_t* sc,
+                             const orc_nadam_scalars_t* k)
+{
+    /* work items: (tensor, first element) for every ORC_SLICE elements of every tensor; tensors of
+     * 4096 or fewer elements (fp32 moments, no scale) are one item */
+    int64_t n_items = 0;
+    for (int32_t i = 0; i < n_tensors; ++i)
+        n_items += n[i] <= 0 ? 0 : (n[i] + ORC_SLICE - 1) / ORC_SLICE;
+    int32_t* it_t = (int32_t*)malloc((size_t)(n_items > 0 ? n_items : 1) * sizeof(int32_t));
+    int64_t* it_a = (int64_t*)malloc((size_t)(n_items > 0 ? n_items : 1) * sizeof(int64_t));
+    float* part_g = (float*)malloc((size_t)(n_items > 0 ? n_items : 1) * sizeof(float));
+    orc_scale_t* part_s = (orc_scale_t*)malloc((size_t)(n_items > 0 ? n_items : 1) * sizeof(orc_scale_t));
+    float* tensor_g = (float*)calloc((size_t)(n_tensors > 0 ? n_tensors : 1), sizeof(float));
+    int64_t q = 0;
+    for (int32_t i = 0; i < n_tensors; ++i)
+        for (int64_t a = 0; a < n[i]; a += ORC_SLICE) {
+            it_t[q] = i;
+            it_a[q] = a;
+            ++q;
+        }
+    /* 1: max |g| of each slice, then of each tensor (exact: a max of bf16 magnitudes) */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t j = 0; j < n_items; ++j) {
+        int32_t i = it_t[j];
+        int64_t a = it_a[j], len = n[i] - a < ORC_SLICE ? n[i] - a : ORC_SLICE;
+        part_g[j] = orc_grad_absmax((const uint16_t*)ptrs[5 * i + 4] + a, len);
+    }
+    for (int64_t j = 0; j < n_items; ++j)
+        if (part_g[j] > tensor_g[it_t[j]]) tensor_g[it_t[j]] = part_g[j];
+    /* 2: every slice steps with its tensor's G and the tensor's scale record as it was */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t j = 0; j < n_items; ++j) {
+        int32_t i = it_t[j];
+        int64_t a = it_a[j], len = n[i] - a < ORC_SLICE ? n[i] - a : ORC_SLICE;
+        int small = n[i] <= ORC_SMALL_NUMEL;
+        size_t ms = small ? 4 : 2;
+        uint16_t* lo = (uint16_t*)ptrs[5 * i + 1];
+        part_s[j] = sc[i];
+        orc_nadam_step_slice((uint16_t*)ptrs[5 * i] + a, lo ? lo + a : NULL, (char*)ptrs[5 * i + 2] + ms * (size_t)a,
+                             (char*)ptrs[5 * i + 3] + ms * (size_t)a, (const uint16_t*)ptrs[5 * i + 4] + a, len,
+                             small, small ? 0.0f : tensor_g[i], &part_s[j], k);
+    }
+    /* 3: the new record: S from any slice (all equal), A the max over the slices */
+    for (int64_t j = 0; j < n_items; ++j) {          /* items are in tensor order, slice 0 first */
+        int32_t i = it_t[j];
+        if (n[i] <= ORC_SMALL_NUMEL) continue;
+        if (it_a[j] == 0) {
+            sc[i] = part_s[j];
+        } else {
+            sc[i].a_m = fmaxf(sc[i].a_m, part_s[j].a_m);
+            sc[i].a_v = fmaxf(sc[i].a_v, part_s[j].a_v);
+        }
+    }
+    free(it_t);
+    free(it_a);
+    free(part_g);
+    free(part_s);
+    free(tensor_g);
 }

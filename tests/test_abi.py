@@ -26,7 +26,9 @@ def lib_path():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("optim_step_nadam_kahan", "optim_step_factored", "state_pack_u16", "state_unpack_u16",
-                     "optim_kahan_split", "optim_kahan_merge", "optim_group_create", "optim_group_destroy"):
+                     "optim_kahan_split", "optim_kahan_merge", "optim_group_create", "optim_group_destroy",
+                     "optim_group_attach_host", "optim_offload_prefetch", "optim_offload_writeback",
+                     "optim_query_scales", "optim_query_nonfinite"):
         assert required in names
 
 
@@ -61,6 +63,12 @@ def test_invalid_arguments_fail_without_gpu(lib_path):
     d.w_bf16, d.m, d.v = 0x1001, 0x2000, 0x3000
     assert lib.optim_group_create(ctypes.byref(d), 1, 0, ctypes.byref(out)) == lmopt.OPTIM_EALIGN
     assert lib.optim_group_destroy(None) == lmopt.OPTIM_EINVAL
+    # the per-group offload calls check their handles first
+    assert lib.optim_group_attach_host(None, None, 0) == lmopt.OPTIM_EINVAL
+    assert lib.optim_offload_prefetch(None, None) == lmopt.OPTIM_EINVAL
+    assert lib.optim_offload_writeback(None, None) == lmopt.OPTIM_EINVAL
+    total = ctypes.c_int64()
+    assert lib.optim_offload_layout(None, None, ctypes.byref(total)) == lmopt.OPTIM_EINVAL
 
 
 def test_workload_sizes():

@@ -4,7 +4,9 @@ oracle, through the C ABI.
 The oracle sums rows, columns and squares in double; the kernels use fp32 trees (and compensated
 sums across tiles), so R, C and the clip divisor agree to a few fp32 roundings, not bit for bit.
 Tolerances, derived from that:
-  R, C states      : 2e-6 relative  (at most ~20 fp32 roundings of positive terms: 20 * 2^-24)
+  R, C states      : 1e-6 relative  (sums of positive terms: a tree of n terms rounds at most
+                     ceil(log2 n) times per term, 14 * 2^-24 = 8.3e-7 for 10240 columns, plus the
+                     EMA's two roundings; the cases here reach 2.4e-7)
   fp32 masters     : |w - w_ref| <= 1e-6 |w_ref| + 1e-6 * lr * steps  (the update is ~lr per step;
                      a 1e-6-relative difference in it, plus one rounding of w)
 """
@@ -78,11 +80,11 @@ def compare(ora, grp, hp, steps, kahan=True, upd_tol=1e-6, moved_tol=0.0):
             for name, st in (("row", grp.row[i]), ("col", grp.col[i])):
                 r = ot[name].astype(np.float64)
                 gv = st.cpu().numpy().astype(np.float64)
-                assert np.all(np.abs(gv - r) <= 2e-6 * np.abs(r) + 1e-37), f"tensor {i}: {name} state differs"
+                assert np.all(np.abs(gv - r) <= 1e-6 * np.abs(r) + 1e-37), f"tensor {i}: {name} state differs"
         else:
             r = ot["V"].astype(np.float64)
             gv = grp.col[i].cpu().numpy().astype(np.float64)
-            assert np.all(np.abs(gv - r) <= 2e-6 * np.abs(r) + 1e-37), f"tensor {i}: V state differs"
+            assert np.all(np.abs(gv - r) <= 1e-6 * np.abs(r) + 1e-37), f"tensor {i}: V state differs"
 
 
 def run_parity(orc, eng, shapes, steps, hp, seed=0, g_std=1e-3, kahan=True, scale_rows=False, upd_tol=1e-6,
@@ -244,10 +246,10 @@ def test_misaligned_buffers_and_empty_tensors(orc, eng):
             if "row" in ot:
                 for st, r in ((rows[i], ot["row"]), (cols[i], ot["col"])):
                     gv = st.cpu().numpy().astype(np.float64)
-                    assert np.all(np.abs(gv - r) <= 2e-6 * np.abs(r) + 1e-37), f"tensor {i}: state differs"
+                    assert np.all(np.abs(gv - r) <= 1e-6 * np.abs(r) + 1e-37), f"tensor {i}: state differs"
             else:
                 gv = cols[i].cpu().numpy().astype(np.float64)
-                assert np.all(np.abs(gv - ot["V"]) <= 2e-6 * np.abs(ot["V"]) + 1e-37), f"tensor {i}: V differs"
+                assert np.all(np.abs(gv - ot["V"]) <= 1e-6 * np.abs(ot["V"]) + 1e-37), f"tensor {i}: V differs"
     finally:
         lmopt.optim_group_destroy(h)
 

@@ -127,3 +127,216 @@ def test_injected_failures_leave_state_untouched(eng, monkeypatch):
     assert not torch.equal(grp.weights[0], w0) or not torch.equal(grp.res[0], r0)
     grp.close()
     off.close()
+
+
+# ---------------------------------------------------------------- every offloadable group kind
+ADAN_HP = dict(lr=3.3e-5, beta1=0.02, beta2=0.08, beta3=0.01, eps=1e-8, weight_decay=0.02)
+KINDS = ["nadam-u16", "nadam-f24", "adan-fp32", "adan-f24"]
+
+
+def _bytes(a):
+    if isinstance(a, torch.Tensor):
+        return a.contiguous().cpu().view(torch.uint8).numpy().reshape(-1)
+    return np.ascontiguousarray(a).view(np.uint8).reshape(-1)
+
+
+class OracleGroup:
+    """Oracle states of one group of any offloadable kind, stepped tensor by tensor."""
+
+    def __init__(self, orc, masters, kind):
+        self.orc, self.kind, self.t = orc, kind, []
+        self.nstate = orc.NadamState(len(masters))
+        self.mp, self.steps = 1.0, 0
+        for x in masters:
+            hi, lo = orc.kahan_split(np.ascontiguousarray(x, np.float32).reshape(-1))
+            n = hi.size
+            d = dict(hi=hi, lo=lo)
+            if kind == "nadam-u16":
+                d["m"] = np.zeros(n, np.float32) if n <= 4096 else np.full(n, 32768, np.uint16)
+                d["v"] = np.zeros(n, np.float32) if n <= 4096 else np.zeros(n, np.uint16)
+            elif kind == "nadam-f24":
+                d["m"] = np.zeros(n, np.float32) if n <= 4096 else np.zeros(orc.f24_nbytes(n), np.uint8)
+                d["v"] = np.zeros(n, np.float32) if n <= 4096 else np.zeros(orc.f24_nbytes(n), np.uint8)
+            else:
+                d["m"] = (np.zeros(orc.adan_f24_nbytes(n), np.uint8) if kind == "adan-f24"
+                          else np.zeros(3 * orc.adan_plane(n), np.float32))
+                d["v"] = np.zeros(n, np.uint16)
+            self.t.append(d)
+
+    def step(self, grads):
+        self.steps += 1
+        orc, t = self.orc, self.steps
+        g = [W.bits16(x).reshape(-1) for x in grads]
+        if self.kind == "nadam-u16":
+            orc.nadam_group_step(self.t, g, self.nstate, t, HP)
+        elif self.kind == "nadam-f24":
+            k, self.mp = orc.nadam_scalars(t, HP["lr"], HP["beta1"], HP["beta2"], HP["eps"], HP["weight_decay"],
+                                           HP["wd_mode"] == 1, HP["nesterov"], HP["momentum_decay"], self.mp)
+            for d, gg in zip(self.t, g):
+                orc.nadam_step_tensor_f24(d["hi"], d["lo"], d["m"], d["v"], gg, k)
+        else:
+            k = orc.adan_scalars(ADAN_HP["lr"], ADAN_HP["beta1"], ADAN_HP["beta2"], ADAN_HP["beta3"],
+                                 ADAN_HP["eps"], ADAN_HP["weight_decay"])
+            fn = orc.adan_step_tensor_f24 if self.kind == "adan-f24" else orc.adan_step_tensor
+            for d, gg in zip(self.t, g):
+                fn(d["hi"], d["lo"], d["m"], d["v"], gg, t, k)
+
+
+def make_group(eng, masters, kind, offload=None):
+    fam, states = kind.split("-")
+    if fam == "nadam":
+        return eng.NadamGroup.from_masters(masters, offload=offload, states=states)
+    return eng.AdanGroup.from_masters(masters, states=states, offload=offload)
+
+
+def step_group(grp, kind, grads, stream):
+    grp.step(grads, HP if kind.startswith("nadam") else ADAN_HP, stream)
+
+
+def assert_group_equal(o, grp, tag):
+    states = (grp.res, grp.m, grp.v) if o.kind.startswith("nadam") else (grp.res, grp.mvn, grp.gprev)
+    for i, d in enumerate(o.t):
+        assert np.array_equal(host_bits(grp.weights[i]), d["hi"]), f"{tag}: tensor {i} weights"
+        for name, got, want in zip(("residual", "m", "v"), states, (d["lo"], d["m"], d["v"])):
+            assert np.array_equal(_bytes(got[i]), _bytes(want)), f"{tag}: tensor {i} {name}"
+
+
+GROUP_SHAPES = [[(3000,), (70000,), (20001,)], [(5000,)], [(131075,), (64,)], [(40000,), (1,)]]
+
+
+def _grads(group_shapes, seed, t):
+    out, tid = [], 0
+    for shapes in group_shapes:
+        out.append([W.grad_bf16(s, seed, tid + i, t, 1e-3, zero_frac=0.01) for i, s in enumerate(shapes)])
+        tid += len(shapes)
+    return out
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_engine_offload_every_kind(orc, eng, kind):
+    """Groups of every offloadable kind attached to an engine (states in pinned host buffers, the
+    step prefetching and writing back): bit-identical to the oracle after 3 steps."""
+    from memory_lean_optimizer_gb300 import lmopt
+    kid = {"nadam-u16": lmopt.OPTIM_KIND_NADAM, "nadam-f24": lmopt.OPTIM_KIND_NADAM_F24,
+           "adan-fp32": lmopt.OPTIM_KIND_ADAN, "adan-f24": lmopt.OPTIM_KIND_ADAN_F24}[kind]
+    seed = 31
+    off = eng.OffloadEngine(max(eng.offload_slot_bytes([W.numel(s) for s in g], kind=kid) for g in GROUP_SHAPES), 3)
+    oras, grps, tid = [], [], 0
+    for shapes in GROUP_SHAPES:
+        masters = [W.master_weights(s, seed, tid + i) for i, s in enumerate(shapes)]
+        oras.append(OracleGroup(orc, [m.numpy() for m in masters], kind))
+        grps.append(make_group(eng, [m.cuda() for m in masters], kind, offload=off))
+        tid += len(shapes)
+    stream = torch.cuda.current_stream()
+    for t in range(1, 4):
+        grads = _grads(GROUP_SHAPES, seed, t)
+        grps[0].prefetch()
+        for k, (o, g) in enumerate(zip(oras, grps)):
+            if k + 1 < len(grps):
+                grps[k + 1].prefetch()
+            o.step(grads[k])
+            step_group(g, kind, [x.cuda() for x in grads[k]], stream)
+    off.sync()
+    torch.cuda.synchronize()
+    for k, (o, g) in enumerate(zip(oras, grps)):
+        assert_group_equal(o, g, f"{kind} group {k}")
+    for g in grps:
+        g.close()
+    off.close()
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_attach_host_pipeline_every_kind(orc, eng, kind):
+    """The per-group offload calls: each group's states moved into one pinned host image
+    (optim_group_attach_host); per step prefetch(k+1) on a copy-in stream before step(k), and
+    write-back(k) on a copy-out stream after it, through the library's own staging ring.  The
+    images equal the oracle's states bit for bit after 3 steps, and the device buffers named at
+    create are no longer used (they are dropped by attach_host)."""
+    seed = 32
+    oras, grps, tid = [], [], 0
+    for shapes in GROUP_SHAPES:
+        masters = [W.master_weights(s, seed, tid + i) for i, s in enumerate(shapes)]
+        oras.append(OracleGroup(orc, [m.numpy() for m in masters], kind))
+        g = make_group(eng, [m.cuda() for m in masters], kind)
+        g.attach_host()
+        grps.append(g)
+        tid += len(shapes)
+    stream = torch.cuda.current_stream()
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+    for t in range(1, 4):
+        grads = _grads(GROUP_SHAPES, seed, t)
+        grps[0].prefetch(cin)
+        for k, (o, g) in enumerate(zip(oras, grps)):
+            if k + 1 < len(grps):
+                grps[k + 1].prefetch(cin)
+            o.step(grads[k])
+            step_group(g, kind, [x.cuda() for x in grads[k]], stream)
+            g.writeback(cout)
+    torch.cuda.synchronize()
+    for k, (o, g) in enumerate(zip(oras, grps)):
+        assert_group_equal(o, g, f"{kind} group {k}")
+    for g in grps:
+        g.close()
+
+
+def test_attach_host_errors_and_ring_growth(orc, eng):
+    """Misuse of the per-group offload calls returns an error and changes nothing: an image too
+    small or not pinned, a factored group, a step before prefetch, a write-back without a slot,
+    growing the library's ring while a group's states are on the device.  A larger group then
+    grows the ring, and both groups step bit-identically to the oracle."""
+    from memory_lean_optimizer_gb300 import lmopt
+    small = eng.NadamGroup.from_masters([W.master_weights((6000,), 33, 0).cuda()])
+    total, offs = lmopt.optim_offload_layout(small.handle, 1)
+    assert total == 3 * 12032 and offs == [(0, 12032, 24064)]     # 12000 bytes each, 256-byte aligned
+    pinned = torch.zeros(total, dtype=torch.uint8, pin_memory=True)
+    dev = torch.zeros(total, dtype=torch.uint8, device="cuda")
+    for ptr, nb in ((pinned.data_ptr(), total - 1), (dev.data_ptr(), total)):
+        with pytest.raises(lmopt.LmoptError) as e:
+            lmopt.optim_group_attach_host(small.handle, ptr, nb)
+        assert e.value.code == lmopt.OPTIM_EINVAL
+    fac = eng.FactoredGroup.from_masters([torch.zeros(64, 64, device="cuda")])
+    with pytest.raises(lmopt.LmoptError) as e:
+        lmopt.optim_offload_layout(fac.handle, 1)
+    assert e.value.code == lmopt.OPTIM_EINVAL
+    fac.close()
+    with pytest.raises(lmopt.LmoptError) as e:         # not attached
+        small.writeback()
+    assert e.value.code == lmopt.OPTIM_EINVAL
+    ora_s = OracleGroup(orc, [W.master_weights((6000,), 33, 0).numpy()], "nadam-u16")
+    small.attach_host()
+    g1 = W.grad_bf16((6000,), 33, 0, 1, 1e-3)
+    with pytest.raises(lmopt.LmoptError) as e:         # no prefetch yet
+        small.step([g1.cuda()], HP)
+    assert e.value.code == lmopt.OPTIM_ESTATE
+    with pytest.raises(lmopt.LmoptError) as e:         # holds no slot
+        small.writeback()
+    assert e.value.code == lmopt.OPTIM_ESTATE
+    assert lmopt.optim_group_get_step(small.handle)[0] == 0
+    small.prefetch()
+    big = eng.NadamGroup.from_masters([W.master_weights((50000,), 33, 1).cuda()])
+    with pytest.raises(lmopt.LmoptError) as e:         # the ring must grow, a slot is held
+        big.attach_host()
+    assert e.value.code == lmopt.OPTIM_ESTATE
+    small.step([g1.cuda()], HP)
+    ora_s.step([g1])
+    small.writeback()
+    ora_b = OracleGroup(orc, [W.master_weights((50000,), 33, 1).numpy()], "nadam-u16")
+    big.attach_host()                                  # grows the ring (no slot held now)
+    for t in (2, 3):
+        gs = W.grad_bf16((6000,), 33, 0, t, 1e-3)
+        gb = W.grad_bf16((50000,), 33, 1, t, 1e-3)
+        small.prefetch()
+        big.prefetch()
+        small.step([gs.cuda()], HP)
+        big.step([gb.cuda()], dict(HP))
+        small.writeback()
+        big.writeback()
+        ora_s.step([gs])
+        ora_b.step([gb])
+    eng.OffloadEngine.sync_library_ring()
+    torch.cuda.synchronize()
+    assert_group_equal(ora_s, small, "small group")
+    # the big group stepped twice (t = 1, 2 of its own counter)
+    assert_group_equal(ora_b, big, "big group")
+    small.close()
+    big.close()

@@ -68,3 +68,74 @@ def test_decay_only():
     w, _, _ = run(orc, w0, [z] * 5, lr, wd=wd, eps=1e-8)
     expect = w0.astype(np.float64) / (1 + lr * wd) ** 5
     assert np.all(np.abs(w - expect) <= 5 * np.spacing(np.abs(w0)))
+
+
+def run_f24(orc, w0, grads, lr, wd=0.0, eps=0.0):
+    n = w0.size
+    hi, lo = orc.kahan_split(w0)
+    buf = np.zeros(orc.adan_f24_nbytes(n), np.uint8)
+    gp = np.zeros(n, np.uint16)
+    k = orc.adan_scalars(lr, B1, B2, B3, eps, wd)
+    for t, g in enumerate(grads, start=1):
+        orc.adan_step_tensor_f24(hi, lo, buf, gp, g, t, k)
+    return orc.kahan_merge(hi, lo).astype(np.float64), buf, gp
+
+
+def test_f24_constant_gradient_closed_form_and_layout():
+    """f24 states (above 4096 elements), constant gradient: m = g and n = g^2 have at most 16
+    significant bits (g is bf16), so f24 stores them exactly and every step is w - lr sign(g), as
+    with fp32 states.  Layout by hand for n = 5000: each state buffer holds 10000 bytes of upper
+    words, then 5000 bytes of bits 8..15, padded to 15008; m at byte 0, v at 15008, n at 30016."""
+    import oracle as orc
+    rng = np.random.default_rng(43)
+    n = 5000
+    g = bf16_bits(rng.choice([-1.0, 1.0], n) * 2.0 ** rng.integers(-12, -4, n))
+    lr = 2.0 ** -10
+    w, buf, gp = run_f24(orc, np.zeros(n, np.float32), [g] * 4, lr)
+    assert np.array_equal(w, -4 * lr * np.sign(bits_to_f32(g)))
+    F = orc.adan_f24_stride(n)
+    assert F == 15008 and buf.size == 3 * F == orc.adan_f24_nbytes(n)
+    gb = bits_to_f32(g).view(np.uint32)
+    g2 = (bits_to_f32(g) * bits_to_f32(g)).view(np.uint32)
+    for j, want in ((0, gb), (1, np.zeros(n, np.uint32)), (2, g2)):
+        sub = buf[j * F:(j + 1) * F]
+        assert np.array_equal(sub[:2 * n].view(np.uint16), (want >> 16).astype(np.uint16))
+        assert np.array_equal(sub[10000:15000], ((want >> 8) & 0xFF).astype(np.uint8))
+        assert not sub[15000:].any()
+    assert np.array_equal(gp, g)
+
+
+def test_f24_states_are_truncated_fp32_states():
+    """Replay: each step of the f24 path equals the fp32-state step started from the decoded f24
+    states, with m, v, n stored truncated to their upper 24 bits and the Kahan weight bit-identical;
+    4096 or fewer elements keep the fp32 planes (same results as the fp32 path)."""
+    import oracle as orc
+    rng = np.random.default_rng(44)
+    lr, eps, wd = 1e-3, 1e-8, 0.02
+    k = orc.adan_scalars(lr, B1, B2, B3, eps, wd)
+    for n in (4096, 10003):
+        w0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+        hi, lo = orc.kahan_split(w0)
+        buf = np.zeros(orc.adan_f24_nbytes(n), np.uint8)
+        gp = np.zeros(n, np.uint16)
+        F = orc.adan_f24_stride(n)
+        P = orc.adan_plane(n)
+        mask = np.uint32(0xFFFFFF00)
+        for t in range(1, 6):
+            g = bf16_bits(rng.standard_normal(n) * 1e-3)
+            hi_r, lo_r, gp_r = hi.copy(), lo.copy(), gp.copy()
+            if n > 4096:
+                mnv = np.zeros(3 * P, np.float32)
+                for j in range(3):
+                    mnv[j * P:j * P + n] = orc.f24_merge(buf[j * F:j * F + orc.f24_nbytes(n)], n)
+            else:
+                mnv = buf.view(np.float32).copy()
+            orc.adan_step_tensor(hi_r, lo_r, mnv, gp_r, g, t, k)
+            orc.adan_step_tensor_f24(hi, lo, buf, gp, g, t, k)
+            assert np.array_equal(hi, hi_r) and np.array_equal(lo, lo_r) and np.array_equal(gp, gp_r)
+            if n > 4096:
+                for j in range(3):
+                    got = orc.f24_merge(buf[j * F:j * F + orc.f24_nbytes(n)], n).view(np.uint32)
+                    assert np.array_equal(got, mnv[j * P:j * P + n].view(np.uint32) & mask), (t, j)
+            else:
+                assert np.array_equal(buf.view(np.float32), mnv)
