@@ -11,10 +11,13 @@ the timed region; together they are ~32 GB, far larger than L2, so no L2 flush i
 
 The JSON line reports params updated/s (whole job, all ranks), the step's HBM GB/s at the
 algorithmic 18 bytes per parameter, a roofline record for the dominant kernel timed live with
-CUDA events, the oracle's CPU throughput on a bounded sample, and an end-to-end figure through
-the public API with the gradients copied in from pinned host memory and the weights copied back
-every step.  With N > 1 (torchrun), every rank steps its own copy of the workload (weak scaling,
-no collective on the data path) and the slowest rank's time is used.
+CUDA events, the oracle's throughput on all host cores on a bounded sample, and an end-to-end
+figure through the public API with the gradients copied in from pinned host memory and the
+weights copied back every step.  The default run (flux19, one GPU) adds a `workloads` record with
+the other workloads measured the same way, one after the other, each freed before the next: the
+20,000-tensor ragged NAdam group, the SDXL-like factored step, the 35-group host-offload pipeline
+and the single 1024x1024 tensor.  With N > 1 (torchrun), every rank steps its own copy of the
+workload (weak scaling, no collective on the data path) and the slowest rank's time is used.
 """
 from __future__ import annotations
 
@@ -44,6 +47,7 @@ KERNEL_SOURCES = {
     "k_nadam_f24": ["memory_lean_optimizer_gb300/csrc/nadam.cu", "memory_lean_optimizer_gb300/csrc/common.cuh"],
     "k_nadam_f24<sr>": ["memory_lean_optimizer_gb300/csrc/nadam.cu", "memory_lean_optimizer_gb300/csrc/common.cuh"],
     "k_adan_step": ["memory_lean_optimizer_gb300/csrc/adan.cu", "memory_lean_optimizer_gb300/csrc/common.cuh"],
+    "k_adan_step<f24>": ["memory_lean_optimizer_gb300/csrc/adan.cu", "memory_lean_optimizer_gb300/csrc/common.cuh"],
     "factored_step": ["memory_lean_optimizer_gb300/csrc/factored.cu", "memory_lean_optimizer_gb300/csrc/common.cuh"],
 }
 
@@ -55,15 +59,20 @@ def parse():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="flux19")
-    p.add_argument("--states", default="u16", choices=["u16", "f24"], help="moment storage of NAdam workloads")
+    p.add_argument("--states", default="u16", choices=["u16", "f24"],
+                   help="state storage: NAdam u16 codes or f24; Adan fp32 (the default) or f24")
     p.add_argument("--optimizer", default="nadam", choices=["nadam", "adan", "prodigy"],
                    help="adan: fp32 m, v, n + previous gradient, Kahan residual (38 B/param); "
                         "prodigy (factored workloads): Prodigy mode with the step size d estimated each step")
-    p.add_argument("--offload-slots", type=int, default=3, help="flux35: device staging slots of the offload engine")
+    p.add_argument("--offload-slots", type=int, default=3, help="offload: device staging slots of the engine")
+    p.add_argument("--offload", action="store_true",
+                   help="run the host-offload pipeline on this workload (flux35 always does); with "
+                        "--optimizer adan the Adan states (fp32, or f24 with --states f24) are offloaded")
     p.add_argument("--slice-p", type=int, default=11, help="prodigy: statistics on every slice_p-th 64-element block")
     p.add_argument("--rounding", default="kahan", choices=["kahan", "sr"],
                    help="kahan: bf16 weight + u16 residual; sr: no residual, stochastic rounding")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-workloads", action="store_true", help="headline line only (no other workloads)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     return p.parse_args()
@@ -217,98 +226,187 @@ def bytes_alg(shapes, states="u16", rounding="kahan"):
     return tot
 
 
-def cpu_baseline(cfg, target_s):
-    """The oracle, as it stands (single-threaded C), on a bounded sample of the workload: the
-    tensors of the first groups, stepped until about target_s seconds of CPU time."""
+def _oracle_tensors(shapes, seed, first_tid, g_std, zero_frac):
+    """Host copies of a list of tensors of the workload for the oracle: Kahan pair of the seeded
+    fp32 masters, zero states, the step-1 bf16 gradients (the GPU arm's resident set)."""
+    import numpy as np
     import oracle
     from memory_lean_optimizer_gb300 import workloads as W
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    oracle.build()
-    shapes = [s for grp in cfg["groups"] for s in grp]
-    done_params, spent, steps_done = 0, 0.0, 0
-    sample = []
-    tid = 0
-    while spent < target_s and tid < len(shapes):
-        s = shapes[tid]
-        x = W.master_weights(s, cfg["seed"], tid).numpy().reshape(-1)
+    ts, gs = [], []
+    for i, s in enumerate(shapes):
+        x = W.master_weights(s, seed, first_tid + i).numpy().reshape(-1)
         hi, lo = oracle.kahan_split(x)
         n = x.size
         if n <= 4096:
-            import numpy as np
             m, v = np.zeros(n, np.float32), np.zeros(n, np.float32)
         else:
-            import numpy as np
             m, v = np.full(n, 32768, np.uint16), np.zeros(n, np.uint16)
-        st = oracle.NadamState(1)
-        t = dict(hi=hi, lo=lo, m=m, v=v)
+        ts.append(dict(hi=hi, lo=lo, m=m, v=v))
+        gs.append(W.bits16(W.grad_bf16(s, seed, first_tid + i, 1, g_std, zero_frac=zero_frac)).reshape(-1))
+    return ts, gs
+
+
+def cpu_baseline(cfg, target_s):
+    """The oracle, as it stands, on every host core (its threaded timing driver: the same
+    single-threaded step function over slices of the tensors, bit-identical results), on a bounded
+    sample of the workload: its first groups, two steps each, until about target_s seconds of CPU
+    time (wall time x threads) are spent."""
+    import oracle
+    oracle.build()
+    cores = oracle.threads()
+    done_params, wall, groups_done, tid = 0, 0.0, 0, 0
+    for shapes in cfg["groups"]:
+        if wall * cores >= target_s:
+            break
+        ts, gs = _oracle_tensors(shapes, cfg["seed"], tid, cfg["g_std"], cfg["zero_frac"])
+        st = oracle.NadamState(len(ts))
         for step in (1, 2):
-            g = W.bits16(W.grad_bf16(s, cfg["seed"], tid, step, cfg["g_std"], zero_frac=cfg["zero_frac"])).reshape(-1)
             t0 = time.perf_counter()
-            oracle.nadam_group_step([t], [g], st, step, cfg["hp"])
-            spent += time.perf_counter() - t0
-            done_params += n
-            steps_done += 1
-        sample.append(tuple(s))
-        tid += 1
-    return {"value": done_params / spent, "unit": "params/s", "cores": 1, "kind": "oracle",
-            "sample": f"{len(sample)} tensors of the workload ({sum(W.numel(s) for s in sample)} params) x 2 steps, "
-                      f"{spent:.1f} s single-threaded C"}
+            oracle.nadam_group_step_mt(ts, gs, st, step, cfg["hp"])
+            wall += time.perf_counter() - t0
+            done_params += sum(t["hi"].size for t in ts)
+        tid += len(shapes)
+        groups_done += 1
+        del ts, gs
+    return {"value": done_params / wall, "unit": "params/s", "cores": cores, "kind": "oracle",
+            "sample": f"the first {groups_done} groups of the workload ({done_params // 2} params) x 2 steps, "
+                      f"{wall:.2f} s on {cores} threads ({wall * cores:.1f} thread-s)"}
 
 
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(args, cfg):
+    """The oracle (threaded timing driver, every host core) stepping the whole workload: each step
+    is every group call of the workload, as on the GPU, over the same tensors (inputs generated on
+    the host with the same seeds and one resident gradient set).  Rank 0 only."""
     world, rank, _ = dist_info()
     if rank != 0:
         return 0
     import oracle
-    from memory_lean_optimizer_gb300 import workloads as W
-    import numpy as np
     oracle.build()
-    shapes = [s for grp in cfg["groups"] for s in grp]
-    # each step: the oracle over a bounded sample (the workload's first tensor), sized so that
-    # --steps K --warmup W ends within a few minutes
-    s = shapes[0]
-    x = W.master_weights(s, cfg["seed"], 0).numpy().reshape(-1)
-    n = x.size
-    hi, lo = oracle.kahan_split(x)
-    t = dict(hi=hi, lo=lo, m=np.full(n, 32768, np.uint16) if n > 4096 else np.zeros(n, np.float32),
-             v=np.zeros(n, np.uint16) if n > 4096 else np.zeros(n, np.float32))
-    st = oracle.NadamState(1)
-    g = W.bits16(W.grad_bf16(s, cfg["seed"], 0, 1, cfg["g_std"])).reshape(-1)
+    cores = oracle.threads()
+    t_setup = time.perf_counter()
+    groups, tid, params = [], 0, 0
+    for shapes in cfg["groups"]:
+        ts, gs = _oracle_tensors(shapes, cfg["seed"], tid, cfg["g_std"], cfg["zero_frac"])
+        groups.append((ts, gs, oracle.NadamState(len(ts))))
+        tid += len(shapes)
+        params += sum(t["hi"].size for t in ts)
+    t_setup = time.perf_counter() - t_setup
     step = 0
-    for _ in range(args.warmup):
+
+    def one_step():
+        nonlocal step
         step += 1
-        oracle.nadam_group_step([t], [g], st, step, cfg["hp"])
+        for ts, gs, st in groups:
+            oracle.nadam_group_step_mt(ts, gs, st, step, cfg["hp"])
+
+    for _ in range(args.warmup):
+        one_step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        step += 1
-        oracle.nadam_group_step([t], [g], st, step, cfg["hp"])
+        one_step()
     dt = time.perf_counter() - t0
-    value = n * args.steps / dt
+    value = params * args.steps / dt
     line = {"metric": METRIC, "value": value, "unit": "params/s", "impl": "reference", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": {"workload": args.workload, "sample_params_per_step": n},
-            "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
-                             "sample": f"one {s} tensor per step (single-threaded C oracle)"},
+            "data": "synthetic", "config": workload_config(args, cfg, params, len(groups), world),
+            "cpu_baseline": {"value": value, "unit": "params/s", "cores": cores, "kind": "oracle",
+                             "sample": f"the whole workload ({params} params, {len(groups)} group calls) per step, "
+                                       f"{cores} threads; setup {t_setup:.1f} s untimed"},
             "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
 
+def workload_config(args, cfg, params, n_groups, world):
+    """The `config` record of a NAdam workload line (shared by both arms)."""
+    return {"workload": args.workload, "params_per_gpu": params, "groups": n_groups,
+            "tensors": sum(len(s) for s in cfg["groups"]),
+            "optimizer": f"NAdamW+{'Kahan' if args.rounding == 'kahan' else 'stochastic rounding'}, {args.states} moments",
+            "lr": cfg["hp"]["lr"], "weight_decay": cfg["hp"]["weight_decay"],
+            "grads": "one resident set reused each step",
+            "l2": (f"inputs {params * 10 / 1e6:.1f} MB, inside the 129 MB L2: timed warm, reported only"
+                   if params * 10 < 129e6 else
+                   f"inputs ~{params * 10 / 1e9:.0f} GB per GPU, far above the 129 MB L2: no flush needed"),
+            "parallelism": f"replicas x{world}"}
+
+
 # ----------------------------------------------------------------------------- our arm
 def run_ours(args, cfg):
+    """The headline line: the NAdam workload (flux19 by default) with its e2e leg, then, on one GPU
+    with the default workload, the other workloads as a `workloads` record, then the oracle
+    baseline on the host."""
     import torch
     import torch.distributed as dist
-    from memory_lean_optimizer_gb300 import build, lmopt
+    from memory_lean_optimizer_gb300 import build, lmopt, workloads as W
 
     world, rank, local = dist_info()
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
     build.build()
     lmopt.load()
+    result = measure_nadam(args, cfg, e2e=not args.no_e2e)
+    torch.cuda.empty_cache()
+    if world == 1 and args.workload == "flux19" and not args.no_workloads:
+        result["workloads"] = other_workloads(args)
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    return 0
+
+
+def other_workloads(args):
+    """The other workloads, each measured as its own bench line would be (same timing rules, live
+    CUDA-event roofline of its dominant kernel, clocks sampled inside its timed region), one after
+    the other, each freed before the next.  Returns name -> summary."""
+    import copy
+    import torch
+    from memory_lean_optimizer_gb300 import workloads as W
+    out = {}
+    keep = ("ms_per_step", "value", "unit", "steps", "warmup", "roofline", "clocks", "ms_per_step_median",
+            "first_step_ms", "hbm_gbs_step", "hbm_gbs_step_as_run", "link_gbs", "h2d_gbs", "d2h_gbs",
+            "hbm_gbs_kernels_over_step", "link_peak_gbs", "gpu_launches")
+    plan = [("ragged20k", "nadam", {}), ("sdxl_like", "factored", {}), ("flux35", "offload", {"steps": 3}),
+            ("nadam_1m", "nadam", {"steps": 100})]
+    for name, kind, over in plan:
+        a = copy.copy(args)
+        a.workload = name
+        a.steps = over.get("steps", min(args.steps, 10))
+        a.warmup = max(3, args.warmup)
+        a.states, a.rounding, a.optimizer = "u16", "kahan", "nadam"
+        cfg = W.config(name)
+        try:
+            if kind == "nadam":
+                r = measure_nadam(a, cfg, e2e=False)
+            elif kind == "factored":
+                r = measure_factored(a, cfg)
+            else:
+                r = measure_offload(a, cfg)
+            summary = {k: r[k] for k in keep if k in r}
+            summary["config"] = r.get("config")
+            out[name] = summary
+        except Exception as e:            # one workload failing must not lose the headline line
+            out[name] = {"error": f"{type(e).__name__}: {e}"[:400]}
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
+def measure_nadam(args, cfg, e2e=True):
+    """One NAdam workload (flux19, ragged20k, nadam_1m, ...): params/s, K2 roofline from live
+    CUDA events, clocks; with e2e the public-API leg with host copies."""
+    import torch
+    import torch.distributed as dist
+    from memory_lean_optimizer_gb300 import lmopt
+
+    world, rank, local = dist_info()
+    device = torch.device("cuda", local)
 
     groups, grads, params = build_groups(cfg, device, rank, args.states, args.rounding)
     hp = dict(cfg["hp"], stochastic_rounding=int(args.rounding == "sr"), seed=12345)
@@ -389,11 +487,7 @@ def run_ours(args, cfg):
         "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * step_s, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": args.workload, "params_per_gpu": params, "groups": len(groups),
-                   "tensors": sum(len(s) for s in cfg["groups"]), "optimizer": f"NAdamW+{'Kahan' if args.rounding == 'kahan' else 'stochastic rounding'}, {args.states} moments",
-                   "lr": hp["lr"], "weight_decay": hp["weight_decay"], "grads": "one resident set reused each step",
-                   "l2": "inputs ~32 GB per GPU, far above the 129 MB L2: no flush needed",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(args, cfg, params, len(groups), world),
         "hbm_gbs_step": sum(group_bytes) / step_s / 1e9,
         "hbm_gbs_step_as_run": (sum(group_bytes) + (PREPASS_BYTES_PER_PARAM * params if args.states == "u16" else 0)) / step_s / 1e9,
         "roofline": {"bound": "hbm", "kernel": k2_name,
@@ -410,20 +504,13 @@ def run_ours(args, cfg):
         "clocks": clk,
     }
 
-    if not args.no_e2e:
+    if e2e:
         result["e2e"] = e2e_run(args, groups, grads, hp, params, stream, world, device)
     for grp in groups:
         grp.close()
     del groups, grads
     torch.cuda.empty_cache()
-    if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
-    if world > 1:
-        dist.barrier()
-        dist.destroy_process_group()
-    if rank == 0:
-        print(json.dumps(result), flush=True)
-    return 0
+    return result
 
 
 def e2e_run(args, groups, grads, hp, params, stream, world, device):
@@ -486,32 +573,73 @@ def e2e_run(args, groups, grads, hp, params, stream, world, device):
 
 
 def run_offload(args, cfg):
+    import torch
+    from memory_lean_optimizer_gb300 import build, lmopt
+    torch.cuda.set_device(dist_info()[2])
+    build.build()
+    lmopt.load()
+    print(json.dumps(measure_offload(args, cfg)), flush=True)
+    return 0
+
+
+def link_probe(device, nbytes=1 << 30, reps=3):
+    """Pinned-host <-> device copy peak of this machine: both directions at once on two streams, best
+    of `reps` after one warm-up repeat (GB/s, bytes both ways / time)."""
+    import torch
+    h_in = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h_out = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    d_out = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    s1, s2 = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+    best = 0.0
+    for r in range(reps + 1):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(s1):
+            d_in.copy_(h_in, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_out, non_blocking=True)
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        if r > 0:
+            best = max(best, 2 * nbytes / dt / 1e9)
+    del h_in, h_out, d_in, d_out
+    return best
+
+
+def measure_offload(args, cfg):
     """Host-offload workload (flux35): 35 Flux-like blocks, one group each, residuals and u16
     moments in pinned host memory (6 bytes per parameter), weights and gradients on the device.
     Each step prefetches group k+1 while group k updates and group k-1 writes back, through the
-    engine's three staging slots.  Reports params/s, the host-link GB/s both ways and the HBM GB/s
-    of the update kernels."""
+    engine's three staging slots.  Reports params/s, the host-link GB/s both ways against a pinned
+    copy probe of the same box, and the HBM GB/s of the update kernels."""
     import torch
-    from memory_lean_optimizer_gb300 import build, engine, lmopt, workloads as W
+    from memory_lean_optimizer_gb300 import engine, workloads as W
     world, rank, local = dist_info()
-    torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    build.build()
-    lmopt.load()
+    link_peak = link_probe(device)
+    from memory_lean_optimizer_gb300 import lmopt
+    adan = args.optimizer == "adan"
+    kind = ((lmopt.OPTIM_KIND_ADAN_F24 if args.states == "f24" else lmopt.OPTIM_KIND_ADAN) if adan else
+            (lmopt.OPTIM_KIND_NADAM_F24 if args.states == "f24" else lmopt.OPTIM_KIND_NADAM))
     shapes = cfg["groups"][0]
-    slot = engine.offload_slot_bytes([W.numel(s) for s in shapes])
+    slot = max(engine.offload_slot_bytes([W.numel(s) for s in g], kind=kind) for g in cfg["groups"])
     off = engine.OffloadEngine(slot, args.offload_slots)
     grads = [W.grad_bf16(s, cfg["seed"], i, 1, cfg["g_std"], device=device) for i, s in enumerate(shapes)]
     groups, params = [], 0
     t_setup = time.perf_counter()
     for gi, grp_shapes in enumerate(cfg["groups"]):
         masters = [W.master_weights(s, cfg["seed"], 1000 * gi + i, device=device) for i, s in enumerate(grp_shapes)]
-        groups.append(engine.NadamGroup.from_masters(masters, offload=off))
+        if adan:
+            groups.append(engine.AdanGroup.from_masters(masters, offload=off,
+                                                        states="f24" if args.states == "f24" else "fp32"))
+        else:
+            groups.append(engine.NadamGroup.from_masters(masters, offload=off, states=args.states))
         params += sum(W.numel(s) for s in grp_shapes)
         del masters
     torch.cuda.synchronize()
     t_setup = time.perf_counter() - t_setup
-    hp = cfg["hp"]
+    hp = ADAN_HP if adan else cfg["hp"]
     stream = torch.cuda.current_stream()
 
     def one_step():
@@ -538,24 +666,33 @@ def run_offload(args, cfg):
     h2d = (b1[0] - b0[0]) / args.steps
     d2h = (b1[1] - b0[1]) / args.steps
     step_s = dt / args.steps
-    hbm_bytes = params * BYTES_PER_PARAM_U16
+    hbm_bytes = params * (38 if adan and args.states != "f24" else 32 if adan else
+                          BYTES_PER_PARAM_F24 if args.states == "f24" else BYTES_PER_PARAM_U16)
+    link = (h2d + d2h) / step_s / 1e9
     result = {
         "metric": METRIC, "value": params * args.steps / dt, "unit": "params/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * step_s, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, "params": params, "groups": len(groups),
-                   "states": "pinned host, 6 B/param", "staging_slots": args.offload_slots, "slot_bytes": slot,
-                   "setup_s": t_setup},
-        "link_gbs": (h2d + d2h) / step_s / 1e9, "h2d_gbs": h2d / step_s / 1e9, "d2h_gbs": d2h / step_s / 1e9,
-        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-        "hbm_gbs_kernels_over_step": hbm_bytes / step_s / 1e9, "gpu_launches": 2 * len(groups) * args.steps,
+                   "optimizer": ("Adan" if adan else "NAdam") + f" + Kahan, {args.states if (args.states == 'f24' or not adan) else 'fp32'} states",
+                   "states": f"pinned host, {h2d / params:.0f} B/param each way", "staging_slots": args.offload_slots,
+                   "slot_bytes": slot, "setup_s": t_setup},
+        "link_gbs": link, "h2d_gbs": h2d / step_s / 1e9, "d2h_gbs": d2h / step_s / 1e9,
+        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "link_peak_gbs": link_peak,
+        "roofline": {"bound": "host link", "kernel": "staging copies (both directions)", "achieved": link,
+                     "peak": link_peak, "unit": "GB/s", "frac": link / link_peak if link_peak else None,
+                     "traffic": None, "peak_source": "measured: pinned copy probe, both directions at once"},
+        "hbm_gbs_kernels_over_step": hbm_bytes / step_s / 1e9,
+        "gpu_launches": (1 if adan or args.states == "f24" else 2) * len(groups) * args.steps,
         "clocks": clk,
     }
     for g in groups:
         g.close()
     off.close()
-    print(json.dumps(result), flush=True)
-    return 0
+    return result
+
+
+ADAN_HP = dict(lr=3.3e-5, beta1=0.02, beta2=0.08, beta3=0.01, eps=1e-8, weight_decay=0.02)
 
 
 def run_adan(args, cfg):
@@ -571,11 +708,12 @@ def run_adan(args, cfg):
     for shapes in cfg["groups"]:
         masters = [W.master_weights(s, cfg["seed"], tid + i, device=device) for i, s in enumerate(shapes)]
         grads.append([W.grad_bf16(s, cfg["seed"], tid + i, 1, cfg["g_std"], device=device) for i, s in enumerate(shapes)])
-        groups.append(engine.AdanGroup.from_masters(masters))
+        groups.append(engine.AdanGroup.from_masters(masters, states="f24" if args.states == "f24" else "fp32"))
         params += sum(W.numel(s) for s in shapes)
         tid += len(shapes)
         del masters
-    hp = dict(lr=3.3e-5, beta1=0.02, beta2=0.08, beta3=0.01, eps=1e-8, weight_decay=0.02)
+    hp = ADAN_HP
+    bpp = 32 if args.states == "f24" else 38
     stream = torch.cuda.current_stream()
 
     def one_step():
@@ -596,15 +734,17 @@ def run_adan(args, cfg):
     clk = clocks.stop()
     step_s = start.elapsed_time(end) / 1e3 / args.steps
     peak, src = peaks()
-    gbs = 38 * params / step_s / 1e9
+    gbs = bpp * params / step_s / 1e9
     print(json.dumps({
         "metric": METRIC, "value": params / step_s, "unit": "params/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * step_s, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": args.workload, "params": params, "optimizer": "Adan + Kahan, fp32 m/v/n + previous bf16 grad"},
-        "roofline": {"bound": "hbm", "kernel": "k_adan_step", "achieved": gbs, "peak": peak, "unit": "GB/s",
-                     "frac": gbs / peak, "traffic": traffic_per_launch("k_adan_step", params / len(groups)),
-                     "peak_source": src, "bytes_per_param": 38},
+        "config": {"workload": args.workload, "params": params,
+                   "optimizer": f"Adan + Kahan, {'f24' if bpp == 32 else 'fp32'} m/v/n + previous bf16 grad"},
+        "roofline": {"bound": "hbm", "kernel": "k_adan_step" + ("<f24>" if bpp == 32 else ""), "achieved": gbs,
+                     "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "traffic": traffic_per_launch("k_adan_step" + ("<f24>" if bpp == 32 else ""), params / len(groups)),
+                     "peak_source": src, "bytes_per_param": bpp},
         "gpu_launches": len(groups) * args.steps, "clocks": clk}), flush=True)
     for g in groups:
         g.close()
@@ -632,20 +772,34 @@ def prodigy_bytes(shape, slice_p):
 
 
 def run_factored(args, cfg):
+    import torch
+    import torch.distributed as dist
+    from memory_lean_optimizer_gb300 import build, lmopt
+    world, rank, local = dist_info()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    build.build()
+    lmopt.load()
+    result = measure_factored(args, cfg)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    return 0
+
+
+def measure_factored(args, cfg):
     """Factored workload (sdxl_like): Adafactor mode over 1332 SDXL-UNet-like tensors in 10
     groups, every step all group calls; reports params/s and HBM GB/s at the algorithmic bytes.
     --optimizer prodigy: Prodigy mode (lr 1, beta2 0.999) with every group attached to one
     controller, each step all group calls and the controller's end of step."""
     import torch
     import torch.distributed as dist
-    from memory_lean_optimizer_gb300 import build, engine, lmopt, workloads as W
+    from memory_lean_optimizer_gb300 import engine, workloads as W
     world, rank, local = dist_info()
-    if world > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    build.build()
-    lmopt.load()
     groups, grads, params, nbytes, tid = [], [], 0, 0, 0
     for shapes in cfg["groups"]:
         masters = [W.master_weights(s, cfg["seed"], tid + i, device=device) for i, s in enumerate(shapes)]
@@ -718,12 +872,7 @@ def run_factored(args, cfg):
         ctrl.close()
     for g in groups:
         g.close()
-    if world > 1:
-        dist.barrier()
-        dist.destroy_process_group()
-    if rank == 0:
-        print(json.dumps(result), flush=True)
-    return 0
+    return result
 
 
 def W_numel(shape):
@@ -738,8 +887,12 @@ def main():
     from memory_lean_optimizer_gb300 import workloads as W
     cfg = W.config(args.workload)
     if args.impl == "reference":
+        if cfg["kind"] != "nadam" or args.optimizer != "nadam" or args.states != "u16":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the NAdam u16 oracle; "
+                              "other optimizers and storages are GPU-only lines"}), flush=True)
+            return 0
         return run_reference(args, cfg)
-    if args.workload == "flux35":
+    if args.workload == "flux35" or args.offload:
         return run_offload(args, cfg)
     if cfg["kind"] == "factored":
         return run_factored(args, cfg)

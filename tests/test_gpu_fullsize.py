@@ -1,8 +1,15 @@
 """Parity at full workload sizes, in the launch configuration the benchmark times (one library
 group per Flux-like block, the ten SDXL-like factored groups, one group of 20,000 ragged tensors, the
-35-group host-offload pipeline).  The oracle replays whole sampled tensors -- their inputs are
-copied back from the device before each step -- and the remaining tensors are checked through
-properties that hold at any size (finite results, scale records bounding their maxima)."""
+35-group host-offload pipeline), each for its configuration's own number of steps (5, and 3 for the
+offload pipeline).  Every tensor of every workload is replayed by the oracle: flux19 and ragged20k
+after step 1 and after their last step, sdxl_like and flux35 after their last step.  The oracle
+replays tensor by tensor on a thread pool (one single-threaded oracle call per tensor), each
+tensor's inputs regenerated from their seeds on the device and copied back, so host memory stays
+bounded by the tensors in flight."""
+import os
+from collections import deque
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import pytest
 import torch
@@ -24,137 +31,176 @@ def _bits(t):
     return W.bits16(t).reshape(-1)
 
 
-def _check_nadam_tensor(ora, i_ora, grp, i_grp, tag):
-    ot = ora.t[i_ora]
-    assert np.array_equal(_bits(grp.weights[i_grp]), ot["hi"]), f"{tag}: weights differ"
-    assert np.array_equal(_bits(grp.res[i_grp]), ot["lo"]), f"{tag}: residuals differ"
-    if ot["hi"].size > 4096:
-        assert np.array_equal(_bits(grp.m[i_grp]), ot["m"]), f"{tag}: m codes differ"
-        assert np.array_equal(_bits(grp.v[i_grp]), ot["v"]), f"{tag}: v codes differ"
+def _f32(t):
+    return t.detach().contiguous().cpu().numpy().reshape(-1)
+
+
+class Replays:
+    """Oracle replays of single tensors on every host core, at most `depth` in flight; a failed
+    comparison is raised by submit() or finish()."""
+
+    def __init__(self):
+        workers = os.cpu_count() or 4
+        self.pool = ThreadPoolExecutor(max_workers=workers)
+        self.depth = workers + 4
+        self.futs = deque()
+        self.done = 0
+
+    def submit(self, fn, *args):
+        while len(self.futs) >= self.depth:
+            self.futs.popleft().result()
+            self.done += 1
+        self.futs.append(self.pool.submit(fn, *args))
+
+    def finish(self):
+        while self.futs:
+            self.futs.popleft().result()
+            self.done += 1
+        self.pool.shutdown()
+        return self.done
+
+
+def _replay_nadam(orc, x, grads, hp, got, scale, tag):
+    """One tensor's NAdam trajectory in the oracle, compared bit for bit with the GPU's state
+    (weights, residuals, u16 codes or fp32 moments, scale record)."""
+    o = OracleNadam(orc, [x])
+    for g in grads:
+        o.step([g], hp)
+    ot = o.t[0]
+    for key in ("hi", "lo", "m", "v"):
+        want = ot[key].view(np.uint8) if ot[key].dtype == np.float32 else ot[key]
+        have = got[key].view(np.uint8) if got[key].dtype == np.float32 else got[key]
+        if not np.array_equal(have, want):
+            bad = np.flatnonzero(have != want)
+            raise AssertionError(f"{tag}: {key} differs in {bad.size} places, first {bad[:5]}")
+    if x.size > 4096:
+        assert np.array_equal(np.float32(scale), np.float32(o.scales()[0])), f"{tag}: scale record {scale} != {o.scales()[0]}"
+
+
+def _nadam_state(grp, i):
+    n = grp.weights[i].numel()
+    if n > 4096:
+        m, v = _bits(grp.m[i]), _bits(grp.v[i])
     else:
-        assert np.array_equal(grp.m[i_grp].cpu().numpy().reshape(-1), ot["m"])
-        assert np.array_equal(grp.v[i_grp].cpu().numpy().reshape(-1), ot["v"])
+        m, v = _f32(grp.m[i]), _f32(grp.v[i])
+    return dict(hi=_bits(grp.weights[i]), lo=_bits(grp.res[i]), m=m, v=v)
 
 
-def _scale_records_bound(grp, n):
+def _check_nadam_groups(orc, groups, shapes_per_group, tids, cfg, upto, tag):
+    """Every tensor of every group after `upto` steps against the oracle."""
     from memory_lean_optimizer_gb300 import lmopt
-    recs = lmopt.optim_query_scales(grp.handle, n)
-    for s_m, s_v, a_m, a_v in recs:
-        assert np.isfinite([s_m, s_v, a_m, a_v]).all()
-        assert a_m <= s_m * (1 + 1e-4) + 1e-30 and a_v <= s_v * (1 + 1e-4) + 1e-30
-    assert lmopt.optim_query_nonfinite(grp.handle) == 0
-
-
-def test_flux19_full(orc, eng):
-    """19 blocks x 5 Flux-like linears (3,227,516,928 params), NAdamW wd 0.01, 2 steps; block 0
-    and the last block's largest tensor replayed whole by the oracle."""
-    cfg = W.config("flux19")
-    hp, steps = cfg["hp"], 2
-    sample = {(0, i) for i in range(5)} | {(18, 4)}
-    groups, shapes_all, ora = [], [], {}
-    tid = 0
-    for b, shapes in enumerate(cfg["groups"]):
-        masters = []
+    rp = Replays()
+    for b, (grp, shapes) in enumerate(zip(groups, shapes_per_group)):
+        scales = lmopt.optim_query_scales(grp.handle, len(shapes))
         for i, s in enumerate(shapes):
-            x = W.master_weights(s, 0, tid, device="cuda")
-            if (b, i) in sample:
-                ora[(b, i)] = OracleNadam(orc, [x.cpu().numpy()])
-            masters.append(x)
-            tid += 1
+            tid = tids[b][i]
+            x = _f32(W.master_weights(s, cfg["seed"], tid, device="cuda"))
+            gs = [_bits(W.grad_bf16(s, cfg["seed"], tid, t, cfg["g_std"], device="cuda", zero_frac=cfg["zero_frac"]))
+                  for t in range(1, upto + 1)]
+            rp.submit(_replay_nadam, orc, x, gs, cfg["hp"], _nadam_state(grp, i), scales[i],
+                      f"{tag} step {upto} group {b} tensor {i} {tuple(s)}")
+        assert lmopt.optim_query_nonfinite(grp.handle) == 0
+    return rp.finish()
+
+
+def _run_nadam_workload(orc, eng, name):
+    cfg = W.config(name)
+    steps = cfg["steps"]
+    groups, tids, tid = [], [], 0
+    for shapes in cfg["groups"]:
+        ids = list(range(tid, tid + len(shapes)))
+        masters = [W.master_weights(s, cfg["seed"], j, device="cuda") for s, j in zip(shapes, ids)]
         groups.append(eng.NadamGroup.from_masters(masters))
-        shapes_all.append(shapes)
         del masters
-    for t in range(1, steps + 1):
-        tid = 0
-        for b, (grp, shapes) in enumerate(zip(groups, shapes_all)):
-            grads = []
-            for i, s in enumerate(shapes):
-                g = W.grad_bf16(s, 0, tid, t, cfg["g_std"], device="cuda")
-                if (b, i) in sample:
-                    ora[(b, i)].step([_bits(g)], hp)
-                grads.append(g)
-                tid += 1
-            grp.step(grads, hp)
+        tids.append(ids)
+        tid += len(shapes)
+
+    def gpu_step(t):
+        for grp, shapes, ids in zip(groups, cfg["groups"], tids):
+            grads = [W.grad_bf16(s, cfg["seed"], j, t, cfg["g_std"], device="cuda", zero_frac=cfg["zero_frac"])
+                     for s, j in zip(shapes, ids)]
+            grp.step(grads, cfg["hp"])
             del grads
+
+    gpu_step(1)
     torch.cuda.synchronize()
-    for (b, i), o in ora.items():
-        _check_nadam_tensor(o, 0, groups[b], i, f"block {b} tensor {i}")
+    n1 = _check_nadam_groups(orc, groups, cfg["groups"], tids, cfg, 1, name)
+    for t in range(2, steps + 1):
+        gpu_step(t)
+    torch.cuda.synchronize()
+    n2 = _check_nadam_groups(orc, groups, cfg["groups"], tids, cfg, steps, name)
+    assert n1 == n2 == tid
     for grp in groups:
-        _scale_records_bound(grp, 5)
         grp.close()
     del groups
     torch.cuda.empty_cache()
 
 
+def test_flux19_full(orc, eng):
+    """19 blocks x 5 Flux-like linears (3,227,516,928 params), NAdamW wd 0.01, 5 steps, one group
+    per block: all 95 tensors bit-identical to the oracle after step 1 and after step 5."""
+    _run_nadam_workload(orc, eng, "flux19")
+
+
 def test_ragged20k_full(orc, eng):
     """20,000 tensors (sizes round(2^U(6,22)), ~7.56e9 params, 37.5% with fp32 moments), 1%
-    exact-zero gradients, one group, 2 steps; 40 tensors replayed whole, including the largest
-    and several of 4096 or fewer elements."""
-    cfg = W.config("ragged20k")
-    hp, steps = cfg["hp"], 2
-    sizes = [s[0] for s in cfg["groups"][0]]
-    rng = np.random.default_rng(0)
-    sample = set(rng.choice(len(sizes), 36, replace=False).tolist()) | {int(np.argmax(sizes)), int(np.argmin(sizes))}
-    sample |= {i for i, n in enumerate(sizes) if n in (4096, 4097)}
-    sample = sorted(sample)[:40]
-    masters = [W.master_weights((n,), 0, i, device="cuda") for i, n in enumerate(sizes)]
-    ora = OracleNadam(orc, [masters[i].cpu().numpy() for i in sample])
-    grp = eng.NadamGroup.from_masters(masters)
-    del masters
-    for t in range(1, steps + 1):
-        grads = [W.grad_bf16((n,), 0, i, t, cfg["g_std"], device="cuda", zero_frac=0.01) for i, n in enumerate(sizes)]
-        ora.step([_bits(grads[i]) for i in sample], hp)
-        grp.step(grads, hp)
-        del grads
-    torch.cuda.synchronize()
-    for j, i in enumerate(sample):
-        _check_nadam_tensor(ora, j, grp, i, f"tensor {i} (n={sizes[i]})")
-    _scale_records_bound(grp, len(sizes))
-    grp.close()
-    del grp
-    torch.cuda.empty_cache()
+    exact-zero gradients, one group, 5 steps: every tensor bit-identical to the oracle after step 1
+    and after step 5."""
+    _run_nadam_workload(orc, eng, "ragged20k")
+
+
+def _replay_factored(orc, x, shape, grads, hp, got_master, got_states, tag):
+    from test_gpu_factored import OracleFactored
+    o = OracleFactored(orc, [x], [shape])
+    for g in grads:
+        o.step([g], hp)
+    ot = o.t[0]
+    steps = len(grads)
+    ref = orc.kahan_merge(ot["hi"], ot["lo"]).astype(np.float64)
+    got = got_master.astype(np.float64)
+    tol = 1e-6 * np.abs(ref) + 1e-6 * hp["lr"] * steps
+    bad = np.abs(got - ref) > tol
+    assert not bad.any(), f"{tag}: {bad.sum()} masters out of tolerance"
+    names = ("row", "col") if "row" in ot else ("V",)
+    for name, st in zip(names, got_states):
+        r = ot[name].astype(np.float64)
+        assert np.all(np.abs(st.astype(np.float64) - r) <= 1e-6 * np.abs(r) + 1e-37), f"{tag}: {name} state differs"
 
 
 def test_sdxl_like_full(orc, eng):
     """SDXL-like factored workload (1332 tensors, 2,602,705,920 params) in its 10 groups,
-    Adafactor mode, 2 steps; one linear of each kind, a 3x3 conv and 1-D tensors replayed whole."""
-    from test_gpu_factored import OracleFactored
+    Adafactor mode, 5 steps: every tensor's fp32 master within 1e-6 relative (+1e-6 lr per step)
+    and its row/column (or 1-D) statistics within 1e-6 relative of the oracle."""
     cfg = W.config("sdxl_like")
-    hp, steps = cfg["hp"], 2
+    hp, steps = cfg["hp"], cfg["steps"]
     shapes = [s for g in cfg["groups"] for s in g]
-    want = {(10240, 1280), (1280, 5120), (640, 640), (1280, 1280, 3, 3), (320, 320, 3, 3), (1280,), (320,)}
-    sample, seen = [], set()
-    for i, s in enumerate(shapes):
-        if tuple(s) in want and tuple(s) not in seen:
-            sample.append(i)
-            seen.add(tuple(s))
-    masters = [W.master_weights(s, 0, i, device="cuda") for i, s in enumerate(shapes)]
-    ora = OracleFactored(orc, [masters[i].cpu().numpy() for i in sample], [shapes[i] for i in sample])
     bounds = np.cumsum([0] + [len(g) for g in cfg["groups"]])
-    groups = [eng.FactoredGroup.from_masters(masters[bounds[k]:bounds[k + 1]]) for k in range(len(cfg["groups"]))]
-    del masters
+    groups = []
+    for k in range(len(cfg["groups"])):
+        masters = [W.master_weights(shapes[i], 0, i, device="cuda") for i in range(bounds[k], bounds[k + 1])]
+        groups.append(eng.FactoredGroup.from_masters(masters))
+        del masters
     for t in range(1, steps + 1):
-        grads = [W.grad_bf16(s, 0, i, t, cfg["g_std"], device="cuda") for i, s in enumerate(shapes)]
-        ora.step([_bits(grads[i]) for i in sample], hp)
         for k, grp in enumerate(groups):
-            grp.step(grads[bounds[k]:bounds[k + 1]], hp)
-        del grads
+            grads = [W.grad_bf16(shapes[i], 0, i, t, cfg["g_std"], device="cuda") for i in range(bounds[k], bounds[k + 1])]
+            grp.step(grads, hp)
+            del grads
     torch.cuda.synchronize()
-    for j, i in enumerate(sample):
-        k = int(np.searchsorted(bounds, i, side="right")) - 1
-        grp, li = groups[k], i - int(bounds[k])
-        ot = ora.t[j]
-        ref = orc.kahan_merge(ot["hi"], ot["lo"]).astype(np.float64)
-        got = grp.masters()[li].cpu().numpy().reshape(-1).astype(np.float64)
-        tol = 1e-6 * np.abs(ref) + 1e-6 * hp["lr"] * steps
-        assert np.all(np.abs(got - ref) <= tol), f"tensor {i} {shapes[i]}: masters differ"
-        if "row" in ot:
-            for name, st in (("row", grp.row[li]), ("col", grp.col[li])):
-                r = ot[name].astype(np.float64)
-                assert np.all(np.abs(st.cpu().numpy() - r) <= 2e-6 * np.abs(r) + 1e-37)
+    rp = Replays()
+    from memory_lean_optimizer_gb300 import lmopt
+    for k, grp in enumerate(groups):
+        masters = grp.masters()
+        for li, i in enumerate(range(bounds[k], bounds[k + 1])):
+            s = shapes[i]
+            x = _f32(W.master_weights(s, 0, i, device="cuda"))
+            gs = [_bits(W.grad_bf16(s, 0, i, t, cfg["g_std"], device="cuda")) for t in range(1, steps + 1)]
+            states = [_f32(grp.row[li]), _f32(grp.col[li])] if grp.row[li] is not None else [_f32(grp.col[li])]
+            rp.submit(_replay_factored, orc, x, tuple(s), gs, hp, _f32(masters[li]), states,
+                      f"sdxl_like step {steps} tensor {i} {tuple(s)}")
+        del masters
+        assert lmopt.optim_query_nonfinite(grp.handle) == 0
+    assert rp.finish() == len(shapes)
     for grp in groups:
-        for w in grp.masters():
-            assert torch.isfinite(w).all()
         grp.close()
     del groups
     torch.cuda.empty_cache()
@@ -162,25 +208,21 @@ def test_sdxl_like_full(orc, eng):
 
 def test_flux35_offload_full(orc, eng):
     """35 Flux-like blocks (5,945,425,920 params) with residuals and u16 moments in pinned host
-    memory (35.7 GB), 3 staging slots, 2 steps; block 0 and block 34 replayed whole."""
+    memory (35.7 GB), 3 staging slots, 3 steps: every tensor bit-identical to the oracle."""
     cfg = W.config("flux35")
-    hp, steps = cfg["hp"], 2
+    hp, steps = cfg["hp"], cfg["steps"]
     shapes = cfg["groups"][0]
     slot = eng.offload_slot_bytes([W.numel(s) for s in shapes])
     off = eng.OffloadEngine(slot, 3)
-    sample_blocks = (0, 34)
-    groups, ora = [], {}
+    groups = []
     for b in range(35):
         masters = [W.master_weights(s, 0, 1000 * b + i, device="cuda") for i, s in enumerate(shapes)]
-        if b in sample_blocks:
-            ora[b] = OracleNadam(orc, [x.cpu().numpy() for x in masters])
         groups.append(eng.NadamGroup.from_masters(masters, offload=off))
         del masters
+    host_grads = []
     for t in range(1, steps + 1):
         grads = [W.grad_bf16(s, 0, i, t, cfg["g_std"], device="cuda") for i, s in enumerate(shapes)]
-        gb = [_bits(g) for g in grads]
-        for b in sample_blocks:
-            ora[b].step(gb, hp)
+        host_grads.append([_bits(g) for g in grads])
         groups[0].prefetch()
         for k, grp in enumerate(groups):
             if k + 1 < len(groups):
@@ -189,14 +231,18 @@ def test_flux35_offload_full(orc, eng):
         del grads
     off.sync()
     torch.cuda.synchronize()
-    for b in sample_blocks:
-        for i in range(len(shapes)):
-            ot = ora[b].t[i]
-            g = groups[b]
-            assert np.array_equal(_bits(g.weights[i]), ot["hi"])
-            assert np.array_equal(g.res[i].numpy().view(np.uint16).reshape(-1), ot["lo"])
-            assert np.array_equal(g.m[i].numpy().view(np.uint16).reshape(-1), ot["m"])
-            assert np.array_equal(g.v[i].numpy().view(np.uint16).reshape(-1), ot["v"])
+    from memory_lean_optimizer_gb300 import lmopt
+    rp = Replays()
+    for b, grp in enumerate(groups):
+        scales = lmopt.optim_query_scales(grp.handle, len(shapes))
+        for i, s in enumerate(shapes):
+            x = _f32(W.master_weights(s, 0, 1000 * b + i, device="cuda"))
+            got = dict(hi=_bits(grp.weights[i]), lo=grp.res[i].numpy().view(np.uint16).reshape(-1).copy(),
+                       m=grp.m[i].numpy().view(np.uint16).reshape(-1).copy(),
+                       v=grp.v[i].numpy().view(np.uint16).reshape(-1).copy())
+            rp.submit(_replay_nadam, orc, x, [hg[i] for hg in host_grads], hp, got, scales[i],
+                      f"flux35 step {steps} block {b} tensor {i}")
+    assert rp.finish() == 35 * len(shapes)
     for g in groups:
         g.close()
     off.close()
