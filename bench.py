@@ -64,7 +64,10 @@ def parse():
     p.add_argument("--optimizer", default="nadam", choices=["nadam", "adan", "prodigy"],
                    help="adan: fp32 m, v, n + previous gradient, Kahan residual (38 B/param); "
                         "prodigy (factored workloads): Prodigy mode with the step size d estimated each step")
-    p.add_argument("--offload-slots", type=int, default=3, help="offload: device staging slots of the engine")
+    p.add_argument("--offload-slots", type=int, default=3, help="offload, engine form: device staging slots")
+    p.add_argument("--offload-form", default="host", choices=["host", "engine"],
+                   help="host: per-group calls (one pinned image per group, prefetch and write-back on the "
+                        "caller's copy streams, library ring); engine: an engine object and per-state buffers")
     p.add_argument("--offload", action="store_true",
                    help="run the host-offload pipeline on this workload (flux35 always does); with "
                         "--optimizer adan the Adan states (fp32, or f24 with --states f24) are offloaded")
@@ -610,9 +613,12 @@ def link_probe(device, nbytes=1 << 30, reps=3):
 def measure_offload(args, cfg):
     """Host-offload workload (flux35): 35 Flux-like blocks, one group each, residuals and u16
     moments in pinned host memory (6 bytes per parameter), weights and gradients on the device.
-    Each step prefetches group k+1 while group k updates and group k-1 writes back, through the
-    engine's three staging slots.  Reports params/s, the host-link GB/s both ways against a pinned
-    copy probe of the same box, and the HBM GB/s of the update kernels."""
+    Each step prefetches group k+1 while group k updates and group k-1 writes back, through three
+    staging slots: by default with the per-group calls (optim_group_attach_host: one pinned image per
+    group, prefetch on a copy-in stream before each group's step, write-back on a copy-out stream
+    after it), or with --offload-form engine through an engine object.  Reports params/s, the
+    host-link GB/s both ways against a pinned copy probe of the same box, and the HBM GB/s of the
+    update kernels."""
     import torch
     from memory_lean_optimizer_gb300 import engine, workloads as W
     world, rank, local = dist_info()
@@ -624,17 +630,20 @@ def measure_offload(args, cfg):
             (lmopt.OPTIM_KIND_NADAM_F24 if args.states == "f24" else lmopt.OPTIM_KIND_NADAM))
     shapes = cfg["groups"][0]
     slot = max(engine.offload_slot_bytes([W.numel(s) for s in g], kind=kind) for g in cfg["groups"])
-    off = engine.OffloadEngine(slot, args.offload_slots)
+    per_group = args.offload_form == "host"
+    off = None if per_group else engine.OffloadEngine(slot, args.offload_slots)
     grads = [W.grad_bf16(s, cfg["seed"], i, 1, cfg["g_std"], device=device) for i, s in enumerate(shapes)]
     groups, params = [], 0
     t_setup = time.perf_counter()
     for gi, grp_shapes in enumerate(cfg["groups"]):
         masters = [W.master_weights(s, cfg["seed"], 1000 * gi + i, device=device) for i, s in enumerate(grp_shapes)]
         if adan:
-            groups.append(engine.AdanGroup.from_masters(masters, offload=off,
-                                                        states="f24" if args.states == "f24" else "fp32"))
+            g = engine.AdanGroup.from_masters(masters, offload=off, states="f24" if args.states == "f24" else "fp32")
         else:
-            groups.append(engine.NadamGroup.from_masters(masters, offload=off, states=args.states))
+            g = engine.NadamGroup.from_masters(masters, offload=off, states=args.states)
+        if per_group:
+            g.attach_host()
+        groups.append(g)
         params += sum(W.numel(s) for s in grp_shapes)
         del masters
     torch.cuda.synchronize()
@@ -642,25 +651,31 @@ def measure_offload(args, cfg):
     hp = ADAN_HP if adan else cfg["hp"]
     stream = torch.cuda.current_stream()
 
+    cin, cout = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+
     def one_step():
-        groups[0].prefetch()
+        groups[0].prefetch(cin if per_group else None)
         for k, g in enumerate(groups):
             if k + 1 < len(groups):
-                groups[k + 1].prefetch()
+                groups[k + 1].prefetch(cin if per_group else None)
             g.step(grads, hp, stream)
+            if per_group:
+                g.writeback(cout)
+
+    def sync():
+        torch.cuda.synchronize()
+        return off.sync() if off is not None else engine.OffloadEngine.sync_library_ring()
 
     for _ in range(args.warmup):
         one_step()
-    off.sync()
-    torch.cuda.synchronize()
-    b0 = off.sync()
+    sync()
+    b0 = sync()
     clocks = ClockSampler(local)
     clocks.start()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         one_step()
-    torch.cuda.synchronize()
-    b1 = off.sync()
+    b1 = sync()
     dt = time.perf_counter() - t0
     clk = clocks.stop()
     h2d = (b1[0] - b0[0]) / args.steps
@@ -675,8 +690,10 @@ def measure_offload(args, cfg):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, "params": params, "groups": len(groups),
                    "optimizer": ("Adan" if adan else "NAdam") + f" + Kahan, {args.states if (args.states == 'f24' or not adan) else 'fp32'} states",
-                   "states": f"pinned host, {h2d / params:.0f} B/param each way", "staging_slots": args.offload_slots,
-                   "slot_bytes": slot, "setup_s": t_setup},
+                   "states": f"pinned host, {h2d / params:.0f} B/param each way",
+                   "offload_form": ("per-group calls, one image per group, copy-in and copy-out streams"
+                                    if per_group else f"engine, {args.offload_slots} staging slots"),
+                   "staging_slots": 3 if per_group else args.offload_slots, "slot_bytes": slot, "setup_s": t_setup},
         "link_gbs": link, "h2d_gbs": h2d / step_s / 1e9, "d2h_gbs": d2h / step_s / 1e9,
         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "link_peak_gbs": link_peak,
         "roofline": {"bound": "host link", "kernel": "staging copies (both directions)", "achieved": link,
@@ -688,7 +705,8 @@ def measure_offload(args, cfg):
     }
     for g in groups:
         g.close()
-    off.close()
+    if off is not None:
+        off.close()
     return result
 
 

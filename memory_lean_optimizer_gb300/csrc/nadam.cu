@@ -83,64 +83,79 @@ __device__ __forceinline__ uint32_t sr_bf16(float x, uint32_t r16) {
 }
 
 // ------------------------------------------------------------------------------------ K1
-__global__ void __launch_bounds__(kThreads) k_grad_absmax(NadamLaunch L, int parity) {
-    __shared__ uint32_t red[2 * 32];
-    const Chunk c = L.chunks[blockIdx.x];
-    const int64_t numel = L.tensors[c.tensor].numel;
-    const uint16_t* __restrict__ g = L.grads[c.tensor];
-    ScaleRec* sr = L.scales + c.tensor;
+// Per tensor max |g| (as the bf16 magnitude bits, atomicMax'ed into this step's slot) and, per
+// chunk, whether its gradients hold an exact zero.  A resident grid of CTAs walks the group's
+// u16-state chunks (CTA b takes chunks b, b + grid, ...): every thread issues all of its 128-bit
+// loads of a chunk at once, and no CTA is launched per chunk, which matters for groups of many
+// small tensors (hundreds of thousands of chunks).
+constexpr int kK1Warps = kThreads / 32;
+constexpr int kK1CtasPerSm = 8;   // 256-thread CTAs resident per SM (<= 32 registers per thread)
+
+__global__ void __launch_bounds__(kThreads, kK1CtasPerSm) k_grad_absmax(NadamLaunch L, int parity) {
+    __shared__ uint32_t red[2][2 * kK1Warps];   // by chunk parity: one barrier per chunk suffices
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int p = parity, q = parity ^ 1;
-    if (c.index == 0 && threadIdx.x == 0) {
-        sr->a_m[p] = 0u;   // this step's maxima accumulate here
-        sr->a_v[p] = 0u;
-        sr->g[q] = 0u;     // next step's gradient max accumulates here
-    }
-    const int64_t start = (int64_t)c.index * L.chunk;
-    const int64_t end = min(numel, start + L.chunk);
-    uint32_t mx = 0u;
-    // exact zeros: a 16-bit magnitude t (bit 15 clear) is zero iff t - 1 sets bit 15; the
-    // borrow into the upper half matters only when the lower half is zero, which is flagged anyway
-    uint32_t zb = 0u;
-    auto scan = [&](uint32_t x) {
-        const uint32_t t = x & 0x7FFF7FFFu;
-        zb |= t - 0x00010001u;
-        return t;
-    };
-    int64_t done = start;
-    if (aligned16(g)) {
-        const int64_t nv = (end - start) >> 3;
-        const uint4* gv = reinterpret_cast<const uint4*>(g + start);
-        int64_t i = threadIdx.x;
-        for (; i + 3 * kThreads < nv; i += 4 * kThreads) {
-            uint4 x0 = __ldcg(gv + i), x1 = __ldcg(gv + i + kThreads);
-            uint4 x2 = __ldcg(gv + i + 2 * kThreads), x3 = __ldcg(gv + i + 3 * kThreads);
-            mx = __vmaxu2(mx, __vmaxu2(scan(x0.x), scan(x0.y)));
-            mx = __vmaxu2(mx, __vmaxu2(scan(x0.z), scan(x0.w)));
-            mx = __vmaxu2(mx, __vmaxu2(scan(x1.x), scan(x1.y)));
-            mx = __vmaxu2(mx, __vmaxu2(scan(x1.z), scan(x1.w)));
-            mx = __vmaxu2(mx, __vmaxu2(scan(x2.x), scan(x2.y)));
-            mx = __vmaxu2(mx, __vmaxu2(scan(x2.z), scan(x2.w)));
-            mx = __vmaxu2(mx, __vmaxu2(scan(x3.x), scan(x3.y)));
-            mx = __vmaxu2(mx, __vmaxu2(scan(x3.z), scan(x3.w)));
+    int buf = 0;
+    for (int64_t ci = blockIdx.x; ci < L.n_chunks_large; ci += gridDim.x, buf ^= 1) {
+        const Chunk c = L.chunks[ci];
+        const int64_t numel = L.tensors[c.tensor].numel;
+        const uint16_t* __restrict__ g = L.grads[c.tensor];
+        ScaleRec* sr = L.scales + c.tensor;
+        if (c.index == 0 && threadIdx.x == 0) {
+            sr->a_m[p] = 0u;   // this step's maxima accumulate here
+            sr->a_v[p] = 0u;
+            sr->g[q] = 0u;     // next step's gradient max accumulates here
         }
-        for (; i < nv; i += kThreads) {
-            uint4 x = __ldcg(gv + i);
-            mx = __vmaxu2(mx, __vmaxu2(scan(x.x), scan(x.y)));
-            mx = __vmaxu2(mx, __vmaxu2(scan(x.z), scan(x.w)));
+        const int64_t start = (int64_t)c.index * L.chunk;
+        const int64_t end = min(numel, start + L.chunk);
+        uint32_t mx = 0u;
+        // exact zeros: a 16-bit magnitude t (bit 15 clear) is zero iff t - 1 sets bit 15; the
+        // borrow into the upper half matters only when the lower half is zero, which is flagged anyway
+        uint32_t zb = 0u;
+        auto scan = [&](uint32_t x) {
+            const uint32_t t = x & 0x7FFF7FFFu;
+            zb |= t - 0x00010001u;
+            return t;
+        };
+        auto scan4 = [&](const uint4& x) {
+            mx = __vmaxu2(mx, __vmaxu2(__vmaxu2(scan(x.x), scan(x.y)), __vmaxu2(scan(x.z), scan(x.w))));
+        };
+        int64_t done = start;
+        if (aligned16(g)) {
+            const int nv = (int)((end - start) >> 3);   // <= kChunk / 8 = 8 * kThreads vectors
+            const uint4* gv = reinterpret_cast<const uint4*>(g + start);
+            if (nv == 8 * kThreads) {                    // a whole chunk: eight loads per thread in flight
+                uint4 x[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) x[u] = __ldcg(gv + threadIdx.x + kThreads * u);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) scan4(x[u]);
+            } else {
+                for (int i = threadIdx.x; i < nv; i += kThreads) scan4(__ldcg(gv + i));
+            }
+            done = start + ((int64_t)nv << 3);
         }
         mx = max(mx & 0xFFFFu, mx >> 16);
-        done = start + (nv << 3);
-    }
-    for (int64_t i = done + threadIdx.x; i < end; i += kThreads) {
-        const uint32_t t = g[i] & 0x7FFFu;
-        mx = max(mx, t);
-        if (t == 0u) zb |= 0x8000u;
-    }
-    uint32_t v[2] = {mx, (zb & 0x80008000u) ? 1u : 0u};
-    block_max_u32<2>(v, red);
-    if (threadIdx.x == 0) {
-        if (v[0] != 0u) atomicMax(&sr->g[p], v[0] << 16);
-        L.zero_chunk[blockIdx.x] = (uint8_t)v[1];
+        for (int64_t i = done + threadIdx.x; i < end; i += kThreads) {
+            const uint32_t t = g[i] & 0x7FFFu;
+            mx = max(mx, t);
+            if (t == 0u) zb |= 0x8000u;
+        }
+        mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+        const uint32_t zero = __reduce_or_sync(0xFFFFFFFFu, (zb & 0x80008000u) ? 1u : 0u);
+        if (lane == 0) {
+            red[buf][warp] = mx;
+            red[buf][kK1Warps + warp] = zero;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, lane < kK1Warps ? red[buf][lane] : 0u);
+            const uint32_t z = __reduce_or_sync(0xFFFFFFFFu, lane < kK1Warps ? red[buf][kK1Warps + lane] : 0u);
+            if (lane == 0) {
+                if (m != 0u) atomicMax(&sr->g[p], m << 16);
+                L.zero_chunk[ci] = (uint8_t)z;
+            }
+        }
     }
 }
 
@@ -576,7 +591,11 @@ __global__ void k_scales_scatter(ScaleRec* sc, const float* buf, int n, int pari
 
 int launch_nadam_prepass(const NadamLaunch& L, const NadamScalars& s, cudaStream_t stream) {
     if (L.f24 || L.n_chunks_large == 0) return OPTIM_OK;   // f24 moments need no scale
-    k_grad_absmax<<<L.n_chunks_large, kThreads, 0, stream>>>(L, s.parity);
+    // at most the resident CTAs, each taking the same number of chunks (no partial last round)
+    const int64_t cap = (int64_t)sm_count() * kK1CtasPerSm;
+    const int64_t per = (L.n_chunks_large + cap - 1) / cap;
+    const int64_t grid = (L.n_chunks_large + per - 1) / per;
+    k_grad_absmax<<<(unsigned)grid, kThreads, 0, stream>>>(L, s.parity);
     return check_cuda(cudaGetLastError(), "grad absmax launch");
 }
 
