@@ -437,8 +437,8 @@ def measure_nadam(args, cfg, e2e=True):
     torch.cuda.synchronize()
     first_step_ms = f0.elapsed_time(f1) if args.warmup > 0 else None
 
-    launches_per_step = sum(2 if (args.states == "u16" and any(W_numel(s) > 4096 for s in shapes)) else 1
-                            for shapes in cfg["groups"])
+    launches_per_step = sum(grp.launches(hp) for grp in groups)
+    one_launch = all(grp.launches(hp) == 1 for grp in groups) and args.states == "u16"
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
             torch.cuda.Event(enable_timing=True)) for _ in groups] for _ in range(args.steps)]
     for per_step in ev:               # materialise the event handles the library records into
@@ -481,7 +481,8 @@ def measure_nadam(args, cfg, e2e=True):
     k2_gbs = k2_bytes_total / k2_time_total / 1e9
     peak, peak_src = peaks()
     params_per_launch = sum(group_params) / len(group_params)
-    k2_name = ("k_nadam_f24" if args.states == "f24" else "k_nadam_step") + ("<sr>" if args.rounding == "sr" else "")
+    k2_name = ("k_nadam_f24" if args.states == "f24" else "k_nadam_fused" if one_launch else "k_nadam_step") + \
+        ("<sr>" if args.rounding == "sr" else "")
     traffic = traffic_per_launch(k2_name, params_per_launch)
 
     step_s = elapsed / args.steps

@@ -158,9 +158,17 @@ int optim_group_destroy(optim_group_t* group);
  *   grads_bf16 : host array of n device pointers, one bf16 gradient per tensor, same order as at
  *                create (may change from call to call; unchanged pointers cost no upload)
  *   step       : 1 on the first call, then previous + 1; anything else is OPTIM_EINVAL
- * Two enqueued kernels (one if every tensor has 4096 or fewer elements). */
+ * Two enqueued kernels (one if every tensor has 4096 or fewer elements, or if the group is small
+ * enough for all of its 2048..16384-element chunks to run on the GPU at once: the pre-pass, a
+ * grid-wide barrier and the update then form one cooperative launch, with the same results).
+ * The barrier's wait is bounded (about a second); should it run out, the chunk is counted by
+ * optim_query_nonfinite and the step's results are not to be trusted. */
 int optim_step_nadam_kahan(optim_group_t* group, const void* const* grads_bf16, int64_t step,
                            const optim_nadam_hparams_t* hp, void* stream);
+/* Kernel launches one step of the group enqueues with these hyper-parameters (NADAM groups: 1 or
+ * 2, see optim_step_nadam_kahan; NADAM_F24, ADAN, ADAN_F24: 1; hp may be NULL for those).
+ * OPTIM_EINVAL for FACTORED groups, whose launches depend on their waves. */
+int optim_query_launches(optim_group_t* group, const optim_nadam_hparams_t* hp, int32_t* launches);
 
 /* The same step in two calls, for a tensor split into slices across ranks (each rank's group
  * holds its slices as tensors).  The codec scale belongs to the whole tensor: it is bounded by

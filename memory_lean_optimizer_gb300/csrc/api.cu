@@ -92,6 +92,7 @@ static void group_free(optim_group* g) {
     cudaFree(g->d_chunks);
     cudaFree(g->d_nonfinite);
     cudaFree(g->d_zero_chunk);
+    cudaFree(g->d_bar);
     factored_plan_free(g->fplan);
     delete g;
 }
@@ -250,6 +251,7 @@ int optim_group_create(const optim_tensor_desc_t* tensors, int32_t n, int32_t ki
         if (!rc) rc = dev_upload(&g->d_nonfinite, std::vector<unsigned long long>(1, 0ull), "counter");
         if (!rc) rc = dev_upload(&g->d_zero_chunk, std::vector<uint8_t>(std::max<int32_t>(g->n_chunks_large, 1), 1), "zero flags");
         if (!rc) rc = dev_upload(&g->d_grads, std::vector<const uint16_t*>(n, nullptr), "gradient table");
+        if (!rc && kind == OPTIM_KIND_NADAM) rc = dev_upload(&g->d_bar, std::vector<unsigned>(1, 0u), "barrier counter");
         for (int s = 0; s < 2 && !rc; ++s) {
             if (cudaHostAlloc(reinterpret_cast<void**>(&g->h_stage[s]), sizeof(void*) * n, cudaHostAllocDefault) != cudaSuccess) {
                 cudaGetLastError();
@@ -275,8 +277,12 @@ int optim_group_destroy(optim_group_t* g) {
     return OPTIM_OK;
 }
 
-int optim_step_nadam_begin(optim_group_t* g, const void* const* grads, int64_t step,
-                           const optim_nadam_hparams_t* hp, void* stream, float* exchange) {
+}  // extern "C"
+
+// Validation, per-step scalars, gradient upload and (unless `fused`) the pre-pass of a NAdam
+// step; with `fused` the pre-pass is left to the one-launch step enqueued by nadam_end.
+static int nadam_begin(optim_group_t* g, const void* const* grads, int64_t step, const optim_nadam_hparams_t* hp,
+                       void* stream, float* exchange, bool fused) {
     if (!g || !hp) return set_error(OPTIM_EINVAL, "group or hparams is NULL");
     if (g->kind != OPTIM_KIND_NADAM && g->kind != OPTIM_KIND_NADAM_F24)
         return set_error(OPTIM_EINVAL, "not a NADAM group");
@@ -334,16 +340,24 @@ int optim_step_nadam_begin(optim_group_t* g, const void* const* grads, int64_t s
     }
     NadamLaunch L{table, g->d_grads, g->d_scales, g->d_chunks, g->d_nonfinite,
                   g->n_chunks_large, g->n_chunks_total, g->kind == OPTIM_KIND_NADAM_F24, g->d_zero_chunk, g->chunk};
-    rc = launch_nadam_prepass(L, k, s);
+    if (!fused) rc = launch_nadam_prepass(L, k, s);
     if (!rc && exchange) rc = launch_scales_gather(g->d_scales, exchange, g->n, k.parity, s);
     if (rc) return rc;
     g->pending = true;
+    g->pending_fused = fused;
     g->pending_step = step;
     g->pending_mu = mu_product;
     g->pending_k = k;
     g->pending_table = table;
     g->pending_stream = s;
     return OPTIM_OK;
+}
+
+extern "C" {
+
+int optim_step_nadam_begin(optim_group_t* g, const void* const* grads, int64_t step,
+                           const optim_nadam_hparams_t* hp, void* stream, float* exchange) {
+    return nadam_begin(g, grads, step, hp, stream, exchange, false);
 }
 
 int optim_step_nadam_end(optim_group_t* g, const float* exchange, void* stream) {
@@ -357,9 +371,17 @@ int optim_step_nadam_end(optim_group_t* g, const float* exchange, void* stream) 
     NadamLaunch L{g->pending_table, g->d_grads, g->d_scales, g->d_chunks, g->d_nonfinite,
                   g->n_chunks_large, g->n_chunks_total, g->kind == OPTIM_KIND_NADAM_F24, g->d_zero_chunk, g->chunk};
     if (exchange) rc = launch_scales_scatter(g->d_scales, exchange, g->n, k.parity, s);
-    if (!rc) rc = launch_nadam_update(L, k, s, g->profile_ev);
+    if (!rc && g->pending_fused) {
+        if (g->profile_ev) rc = check_cuda(cudaEventRecord(g->profile_ev, s), "profile event");
+        const unsigned target = g->bar_total + (unsigned)g->n_chunks_total;
+        if (!rc) rc = launch_nadam_fused(L, k, s, g->d_bar, target);
+        if (!rc) g->bar_total = target;
+    } else if (!rc) {
+        rc = launch_nadam_update(L, k, s, g->profile_ev);
+    }
     if (rc) return rc;
     g->pending = false;
+    g->pending_fused = false;
     g->last_step = g->pending_step;
     g->mu_product = g->pending_mu;
     g->next_parity ^= 1;
@@ -368,11 +390,31 @@ int optim_step_nadam_end(optim_group_t* g, const float* exchange, void* stream) 
     return OPTIM_OK;
 }
 
+// One launch when the group's chunks all fit on the GPU at once (u16 groups with a pre-pass).
+static bool nadam_fusable(const optim_group* g, const optim_nadam_hparams_t* hp) {
+    if (!g || !hp || g->kind != OPTIM_KIND_NADAM || !g->d_bar || g->n_chunks_large == 0) return false;
+    const int cap = nadam_fused_capacity(hp->stochastic_rounding == 1);
+    return g->n_chunks_total <= cap;
+}
+
 int optim_step_nadam_kahan(optim_group_t* g, const void* const* grads, int64_t step,
                            const optim_nadam_hparams_t* hp, void* stream) {
-    int rc = optim_step_nadam_begin(g, grads, step, hp, stream, nullptr);
+    int rc = nadam_begin(g, grads, step, hp, stream, nullptr, nadam_fusable(g, hp));
     if (rc) return rc;
     return optim_step_nadam_end(g, nullptr, stream);
+}
+
+int optim_query_launches(optim_group_t* g, const optim_nadam_hparams_t* hp, int32_t* launches) {
+    if (!g || !launches) return set_error(OPTIM_EINVAL, "group or output is NULL");
+    if (g->kind == OPTIM_KIND_NADAM) {
+        if (!hp) return set_error(OPTIM_EINVAL, "hparams is NULL");
+        *launches = nadam_fusable(g, hp) ? 1 : (g->n_chunks_large > 0 ? 2 : 1);
+    } else if (g->kind == OPTIM_KIND_FACTORED) {
+        return set_error(OPTIM_EINVAL, "factored groups launch per wave (see optim_step_factored)");
+    } else {
+        *launches = 1;
+    }
+    return OPTIM_OK;
 }
 
 int optim_step_adan(optim_group_t* g, const void* const* grads, int64_t step, const optim_adan_hparams_t* hp,

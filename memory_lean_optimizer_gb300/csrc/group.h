@@ -45,8 +45,12 @@ struct optim_group {
     cudaEvent_t profile_ev = nullptr;
     lmo::OffloadBinding* offload = nullptr;   // non-NULL: res/m/v are pinned host buffers
     lmo::ProdigyAttach* prodigy = nullptr;    // non-NULL: d comes from a Prodigy controller
-    // a NAdam step begun (pre-pass enqueued) and not yet ended
+    // one-launch steps (k_nadam_fused): the group's grid-barrier counter and its running total
+    unsigned* d_bar = nullptr;
+    unsigned bar_total = 0;
+    // a NAdam step begun (pre-pass enqueued, or deferred into the one-launch step) and not yet ended
     bool pending = false;
+    bool pending_fused = false;
     int64_t pending_step = 0;
     double pending_mu = 1.0;
     lmo::NadamScalars pending_k{};

@@ -59,6 +59,11 @@ struct NadamLaunch {
 // recorded on the stream before it).  A step is both, in this order, on one stream.
 int launch_nadam_prepass(const NadamLaunch& L, const NadamScalars& k, cudaStream_t s);
 int launch_nadam_update(const NadamLaunch& L, const NadamScalars& k, cudaStream_t s, cudaEvent_t mid);
+// The pre-pass and the update in one cooperative launch (one CTA per chunk), for groups whose
+// chunks all fit on the GPU at once: nadam_fused_capacity() chunks at most (0: not available).
+// bar: the group's barrier counter; target: its value once every CTA of this launch has arrived.
+int nadam_fused_capacity(bool sr);
+int launch_nadam_fused(const NadamLaunch& L, const NadamScalars& k, cudaStream_t s, unsigned* bar, unsigned target);
 // Per tensor {G (this step), A_m, A_v (previous step)} to / from 3 consecutive floats.
 int launch_scales_gather(const ScaleRec* sc, float* buf, int n, int parity, cudaStream_t s);
 int launch_scales_scatter(ScaleRec* sc, const float* buf, int n, int parity, cudaStream_t s);

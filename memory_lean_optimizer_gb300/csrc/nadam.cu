@@ -91,72 +91,75 @@ __device__ __forceinline__ uint32_t sr_bf16(float x, uint32_t r16) {
 constexpr int kK1Warps = kThreads / 32;
 constexpr int kK1CtasPerSm = 8;   // 256-thread CTAs resident per SM (<= 32 registers per thread)
 
-__global__ void __launch_bounds__(kThreads, kK1CtasPerSm) k_grad_absmax(NadamLaunch L, int parity) {
-    __shared__ uint32_t red[2][2 * kK1Warps];   // by chunk parity: one barrier per chunk suffices
+// One chunk of the pre-pass (every thread of the CTA).  red: 2 * kK1Warps words of shared memory.
+__device__ __forceinline__ void k1_chunk(const NadamLaunch& L, int parity, int64_t ci, uint32_t* red) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int p = parity, q = parity ^ 1;
-    int buf = 0;
-    for (int64_t ci = blockIdx.x; ci < L.n_chunks_large; ci += gridDim.x, buf ^= 1) {
-        const Chunk c = L.chunks[ci];
-        const int64_t numel = L.tensors[c.tensor].numel;
-        const uint16_t* __restrict__ g = L.grads[c.tensor];
-        ScaleRec* sr = L.scales + c.tensor;
-        if (c.index == 0 && threadIdx.x == 0) {
-            sr->a_m[p] = 0u;   // this step's maxima accumulate here
-            sr->a_v[p] = 0u;
-            sr->g[q] = 0u;     // next step's gradient max accumulates here
-        }
-        const int64_t start = (int64_t)c.index * L.chunk;
-        const int64_t end = min(numel, start + L.chunk);
-        uint32_t mx = 0u;
-        // exact zeros: a 16-bit magnitude t (bit 15 clear) is zero iff t - 1 sets bit 15; the
-        // borrow into the upper half matters only when the lower half is zero, which is flagged anyway
-        uint32_t zb = 0u;
-        auto scan = [&](uint32_t x) {
-            const uint32_t t = x & 0x7FFF7FFFu;
-            zb |= t - 0x00010001u;
-            return t;
-        };
-        auto scan4 = [&](const uint4& x) {
-            mx = __vmaxu2(mx, __vmaxu2(__vmaxu2(scan(x.x), scan(x.y)), __vmaxu2(scan(x.z), scan(x.w))));
-        };
-        int64_t done = start;
-        if (aligned16(g)) {
-            const int nv = (int)((end - start) >> 3);   // <= kChunk / 8 = 8 * kThreads vectors
-            const uint4* gv = reinterpret_cast<const uint4*>(g + start);
-            if (nv == 8 * kThreads) {                    // a whole chunk: eight loads per thread in flight
-                uint4 x[8];
+    const Chunk c = L.chunks[ci];
+    const int64_t numel = L.tensors[c.tensor].numel;
+    const uint16_t* __restrict__ g = L.grads[c.tensor];
+    ScaleRec* sr = L.scales + c.tensor;
+    if (c.index == 0 && threadIdx.x == 0) {
+        sr->a_m[p] = 0u;   // this step's maxima accumulate here
+        sr->a_v[p] = 0u;
+        sr->g[q] = 0u;     // next step's gradient max accumulates here
+    }
+    const int64_t start = (int64_t)c.index * L.chunk;
+    const int64_t end = min(numel, start + L.chunk);
+    uint32_t mx = 0u;
+    // exact zeros: a 16-bit magnitude t (bit 15 clear) is zero iff t - 1 sets bit 15; the
+    // borrow into the upper half matters only when the lower half is zero, which is flagged anyway
+    uint32_t zb = 0u;
+    auto scan = [&](uint32_t x) {
+        const uint32_t t = x & 0x7FFF7FFFu;
+        zb |= t - 0x00010001u;
+        return t;
+    };
+    auto scan4 = [&](const uint4& x) {
+        mx = __vmaxu2(mx, __vmaxu2(__vmaxu2(scan(x.x), scan(x.y)), __vmaxu2(scan(x.z), scan(x.w))));
+    };
+    int64_t done = start;
+    if (aligned16(g)) {
+        const int nv = (int)((end - start) >> 3);   // <= kChunk / 8 = 8 * kThreads vectors
+        const uint4* gv = reinterpret_cast<const uint4*>(g + start);
+        if (nv == 8 * kThreads) {                    // a whole chunk: eight loads per thread in flight
+            uint4 x[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) x[u] = __ldcg(gv + threadIdx.x + kThreads * u);
+            for (int u = 0; u < 8; ++u) x[u] = __ldcg(gv + threadIdx.x + kThreads * u);
 #pragma unroll
-                for (int u = 0; u < 8; ++u) scan4(x[u]);
-            } else {
-                for (int i = threadIdx.x; i < nv; i += kThreads) scan4(__ldcg(gv + i));
-            }
-            done = start + ((int64_t)nv << 3);
+            for (int u = 0; u < 8; ++u) scan4(x[u]);
+        } else {
+            for (int i = threadIdx.x; i < nv; i += kThreads) scan4(__ldcg(gv + i));
         }
-        mx = max(mx & 0xFFFFu, mx >> 16);
-        for (int64_t i = done + threadIdx.x; i < end; i += kThreads) {
-            const uint32_t t = g[i] & 0x7FFFu;
-            mx = max(mx, t);
-            if (t == 0u) zb |= 0x8000u;
-        }
-        mx = __reduce_max_sync(0xFFFFFFFFu, mx);
-        const uint32_t zero = __reduce_or_sync(0xFFFFFFFFu, (zb & 0x80008000u) ? 1u : 0u);
+        done = start + ((int64_t)nv << 3);
+    }
+    mx = max(mx & 0xFFFFu, mx >> 16);
+    for (int64_t i = done + threadIdx.x; i < end; i += kThreads) {
+        const uint32_t t = g[i] & 0x7FFFu;
+        mx = max(mx, t);
+        if (t == 0u) zb |= 0x8000u;
+    }
+    mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+    const uint32_t zero = __reduce_or_sync(0xFFFFFFFFu, (zb & 0x80008000u) ? 1u : 0u);
+    if (lane == 0) {
+        red[warp] = mx;
+        red[kK1Warps + warp] = zero;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, lane < kK1Warps ? red[lane] : 0u);
+        const uint32_t z = __reduce_or_sync(0xFFFFFFFFu, lane < kK1Warps ? red[kK1Warps + lane] : 0u);
         if (lane == 0) {
-            red[buf][warp] = mx;
-            red[buf][kK1Warps + warp] = zero;
-        }
-        __syncthreads();
-        if (warp == 0) {
-            const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, lane < kK1Warps ? red[buf][lane] : 0u);
-            const uint32_t z = __reduce_or_sync(0xFFFFFFFFu, lane < kK1Warps ? red[buf][kK1Warps + lane] : 0u);
-            if (lane == 0) {
-                if (m != 0u) atomicMax(&sr->g[p], m << 16);
-                L.zero_chunk[ci] = (uint8_t)z;
-            }
+            if (m != 0u) atomicMax(&sr->g[p], m << 16);
+            L.zero_chunk[ci] = (uint8_t)z;
         }
     }
+}
+
+__global__ void __launch_bounds__(kThreads, kK1CtasPerSm) k_grad_absmax(NadamLaunch L, int parity) {
+    __shared__ uint32_t red[2][2 * kK1Warps];   // by chunk parity: one barrier per chunk suffices
+    int buf = 0;
+    for (int64_t ci = blockIdx.x; ci < L.n_chunks_large; ci += gridDim.x, buf ^= 1) k1_chunk(L, parity, ci, red[buf]);
 }
 
 // ------------------------------------------------------------------------------------ K2
@@ -328,10 +331,10 @@ __device__ __forceinline__ void u16_vectors(const Prm& k, const Codec& cd, bool 
 }
 
 // kFull: the group's chunk is kChunk (every group but small ones), known at compile time.
+// One chunk of the update (every thread of the CTA).  red: 3 * 32 words of shared memory.
 template <bool kSR, bool kFull>
-__global__ void __launch_bounds__(kThreads, 4) k_nadam_step(NadamLaunch L, Prm k, int parity) {
-    __shared__ uint32_t red[3 * 32];
-    const Chunk c = L.chunks[blockIdx.x];
+__device__ __forceinline__ void k2_chunk(const NadamLaunch& L, const Prm& k, int parity, int64_t ci, uint32_t* red) {
+    const Chunk c = L.chunks[ci];
     const TensorRec t = L.tensors[c.tensor];
     const uint16_t* __restrict__ g = L.grads[c.tensor];
     const int p = parity, q = parity ^ 1;
@@ -345,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_nadam_step(NadamLaunch L, Prm k
     ScaleRec* sr = L.scales + c.tensor;
     if (!small) {
         const float a_m = __uint_as_float(sr->a_m[q]), a_v = __uint_as_float(sr->a_v[q]);
-        const float G = __uint_as_float(sr->g[p]);
+        const float G = __uint_as_float(__ldcg(&sr->g[p]));
         const float s_m = __fmaf_rn(k.b1, a_m, __fmul_rn(k.omb1, G));
         const float s_v = __fmaf_rn(k.b2, a_v, __fmul_rn(k.omb2, __fmul_rn(G, G)));
         cd.dec = codec_consts(sr->s_m[q], sr->s_v[q]);
@@ -373,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_nadam_step(NadamLaunch L, Prm k
             uint4* vv = reinterpret_cast<uint4*>(static_cast<uint16_t*>(t.v) + start);
             // exact-zero gradients in this chunk (seen by the pre-pass): the zero-guarded
             // arithmetic, else the plain one (a branch taken by the whole CTA)
-            if (L.zero_chunk == nullptr || L.zero_chunk[blockIdx.x])
+            if (L.zero_chunk == nullptr || __ldcg(L.zero_chunk + ci))
                 u16_vectors<kSR, true>(k, cd, has_res, c.tensor, start, (int)nv, wv, rv, gv, mv, vv, am, av, nf);
             else
                 u16_vectors<kSR, false>(k, cd, has_res, c.tensor, start, (int)nv, wv, rv, gv, mv, vv, am, av, nf);
@@ -435,6 +438,51 @@ __global__ void __launch_bounds__(kThreads, 4) k_nadam_step(NadamLaunch L, Prm k
         }
         if (r[2]) atomicAdd(L.nonfinite, 1ull);
     }
+}
+
+template <bool kSR, bool kFull>
+__global__ void __launch_bounds__(kThreads, 4) k_nadam_step(NadamLaunch L, Prm k, int parity) {
+    __shared__ uint32_t red[3 * 32];
+    k2_chunk<kSR, kFull>(L, k, parity, blockIdx.x, red);
+}
+
+// ------------------------------------------------------------------------------------ one launch
+// A group whose chunks all fit on the GPU at once (a cooperative launch, one CTA per chunk) steps
+// in one kernel: the pre-pass of the CTA's chunk, a grid-wide barrier (the per-tensor gradient
+// maxima are then complete), the update of the chunk.  It saves the second launch and its gap,
+// which dominate a step of a small group (1024 x 1024: two launches of a few microseconds of
+// work each).  The barrier counter only grows: each call adds the grid size and waits for the
+// running total the host expects (compared modulo 2^32).  The wait is bounded (about a second);
+// running out counts as a non-finite chunk, and the update proceeds.
+constexpr long kBarrierSpin = 1L << 20;
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+template <bool kSR>
+__global__ void __launch_bounds__(kThreads, 4) k_nadam_fused(NadamLaunch L, Prm k, int parity, unsigned* bar,
+                                                             unsigned target) {
+    __shared__ uint32_t red[3 * 32];
+    const int64_t ci = blockIdx.x;
+    if (ci < L.n_chunks_large) k1_chunk(L, parity, ci, red);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(bar, 1u);
+        unsigned v = ld_acquire_u32(bar);
+        unsigned ns = 32;
+        for (long it = 0; (int)(v - target) < 0 && it < kBarrierSpin; ++it) {
+            __nanosleep(ns);
+            ns = ns < 1024 ? 2 * ns : ns;
+            v = ld_acquire_u32(bar);
+        }
+        if ((int)(v - target) < 0) atomicAdd(L.nonfinite, 1ull);
+    }
+    __syncthreads();
+    k2_chunk<kSR, false>(L, k, parity, ci, red);
 }
 
 // ------------------------------------------------------------------------------------ f24
@@ -597,6 +645,33 @@ int launch_nadam_prepass(const NadamLaunch& L, const NadamScalars& s, cudaStream
     const int64_t grid = (L.n_chunks_large + per - 1) / per;
     k_grad_absmax<<<(unsigned)grid, kThreads, 0, stream>>>(L, s.parity);
     return check_cuda(cudaGetLastError(), "grad absmax launch");
+}
+
+int nadam_fused_capacity(bool sr) {
+    static int cache[2][256] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return 0;
+    int& c = cache[sr ? 1 : 0][dev];
+    if (c == 0) {
+        int per_sm = 0, coop = 0;
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+        const cudaError_t e = sr ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_nadam_fused<true>, kThreads, 0)
+                                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_nadam_fused<false>, kThreads, 0);
+        if (e != cudaSuccess) cudaGetLastError();
+        c = (e == cudaSuccess && coop) ? per_sm * sm_count() : -1;
+    }
+    return c > 0 ? c : 0;
+}
+
+int launch_nadam_fused(const NadamLaunch& L, const NadamScalars& s, cudaStream_t stream, unsigned* bar,
+                       unsigned target) {
+    Prm k{s.lr, s.b1, s.omb1, s.b2, s.omb2, s.eps, s.lr_wd, s.c_m, s.c_g, s.k2, s.decoupled, s.sr, s.seed, s.step};
+    NadamLaunch Lc = L;
+    int parity = s.parity;
+    void* args[] = {&Lc, &k, &parity, &bar, &target};
+    const void* fn = s.sr ? reinterpret_cast<const void*>(k_nadam_fused<true>) : reinterpret_cast<const void*>(k_nadam_fused<false>);
+    return check_cuda(cudaLaunchCooperativeKernel(fn, dim3((unsigned)L.n_chunks_total), dim3(kThreads), args, 0, stream),
+                      "nadam one-launch step");
 }
 
 int launch_nadam_update(const NadamLaunch& L, const NadamScalars& s, cudaStream_t stream, cudaEvent_t mid) {

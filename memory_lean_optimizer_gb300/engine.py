@@ -251,6 +251,10 @@ class NadamGroup(_Group):
                                      _stream_ptr(stream))
         self.step_count += 1
 
+    def launches(self, hp: dict) -> int:
+        """Kernel launches one step enqueues (1 for groups small enough for the one-launch step)."""
+        return lmopt.optim_query_launches(self.handle, self._hparams(hp))
+
     def exchange_buffer(self) -> torch.Tensor:
         """Device buffer of 3 floats per tensor for optim_step_nadam_begin / _end."""
         return torch.zeros(3 * len(self.weights), dtype=torch.float32, device=self.weights[0].device)

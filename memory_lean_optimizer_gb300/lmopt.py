@@ -40,7 +40,7 @@ EXPORTED = (
     "optim_step_factored_noalloc", "optim_step_adan",
     "optim_offload_create", "optim_offload_destroy", "optim_group_attach_offload",
     "optim_offload_prefetch", "optim_offload_sync", "optim_offload_writeback", "optim_group_attach_host",
-    "optim_offload_layout", "optim_step_nadam_begin", "optim_step_nadam_end",
+    "optim_offload_layout", "optim_step_nadam_begin", "optim_step_nadam_end", "optim_query_launches",
     "optim_prodigy_create", "optim_prodigy_destroy", "optim_prodigy_slice_len", "optim_group_attach_prodigy",
     "optim_prodigy_end_step", "optim_prodigy_get", "optim_prodigy_set", "optim_prodigy_reduce",
     "optim_prodigy_finish",
@@ -111,6 +111,7 @@ def load(path: str = LIB_PATH):
             "optim_group_get_step": [P, ctypes.POINTER(I64), ctypes.POINTER(ctypes.c_double)],
             "optim_group_set_step": [P, I64, ctypes.c_double],
             "optim_query_nonfinite": [P, ctypes.POINTER(ctypes.c_uint64)],
+            "optim_query_launches": [P, P, ctypes.POINTER(I32)],
             "optim_group_set_profile_event": [P, P],
             "optim_offload_create": [ctypes.c_size_t, I32, ctypes.POINTER(P)],
             "optim_offload_destroy": [P],
@@ -249,6 +250,13 @@ def optim_query_nonfinite(handle: int) -> int:
     c = ctypes.c_uint64()
     check(load().optim_query_nonfinite(handle, ctypes.byref(c)))
     return c.value
+
+
+def optim_query_launches(handle: int, hp: NadamHparams | None = None) -> int:
+    """Kernel launches one step of the group enqueues (hp: the NAdam hyper-parameters, for NADAM groups)."""
+    n = ctypes.c_int32()
+    check(load().optim_query_launches(handle, ctypes.byref(hp) if hp is not None else None, ctypes.byref(n)))
+    return n.value
 
 
 def optim_offload_create(slot_bytes: int, n_slots: int) -> int:

@@ -64,8 +64,42 @@ def test_empty_tensors_in_a_group(orc, eng, states):
 
 
 def test_one_1024x1024_ten_steps(orc, eng):
-    """The 1024x1024 single-tensor workload, NAdam, lr 3.5e-6, 10 steps, seed 0."""
-    run_parity(orc, eng, [(1024, 1024)], 10, HP, g_std=1e-3)
+    """The 1024x1024 single-tensor workload, NAdam, lr 3.5e-6, 10 steps, seed 0 (one launch per
+    step: its 512 chunks fit on the GPU at once)."""
+    _, grp = run_parity(orc, eng, [(1024, 1024)], 10, HP, g_std=1e-3)
+    assert grp.launches(HP) == 1
+
+
+@pytest.mark.parametrize("sr", [False, True])
+def test_one_launch_step_equals_two_launches(orc, eng, sr):
+    """The one-launch step (pre-pass, grid barrier, update in one cooperative kernel) and the
+    two-kernel step (optim_step_nadam_begin / _end) give the same bits, 1% exact-zero gradients
+    included; a group too large for one launch reports two, and both agree with the oracle."""
+    from memory_lean_optimizer_gb300 import lmopt
+    shapes = [(4097,), (70001,), (300,), (2048, 96)]
+    hp = dict(HP, lr=1e-3, stochastic_rounding=int(sr), seed=99)
+    seed = 21
+    masters = [W.master_weights(s, seed, i).cuda() for i, s in enumerate(shapes)]
+    mk = (lambda: eng.NadamGroup([m.to(torch.bfloat16) for m in masters], kahan=False)) if sr else \
+         (lambda: eng.NadamGroup.from_masters([m.clone() for m in masters]))
+    one, two = mk(), mk()
+    assert one.launches(hp) == 1
+    for t in range(1, 4):
+        grads = [W.grad_bf16(s, seed, i, t, 1e-3, zero_frac=0.01).cuda() for i, s in enumerate(shapes)]
+        one.step(grads, hp)
+        two.step_begin(grads, hp)
+        two.step_end()
+    torch.cuda.synchronize()
+    for a, b in zip(one.weights + one.m + one.v, two.weights + two.m + two.v):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    if not sr:
+        assert all(torch.equal(a, b) for a, b in zip(one.res, two.res))
+    assert one.scales() == two.scales()
+    assert lmopt.optim_query_nonfinite(one.handle) == 0
+    big = eng.NadamGroup.from_masters([torch.zeros(40 * 16384 * 152, device="cuda")])
+    assert big.launches(hp) == 2
+    for g in (one, two, big):
+        g.close()
 
 
 @pytest.mark.parametrize("variant", ["adam", "nadam", "nadamw", "adamw"])
