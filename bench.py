@@ -366,38 +366,27 @@ def run_ours(args, cfg):
 
 def other_workloads(args):
     """The other workloads, each measured as its own bench line would be (same timing rules, live
-    CUDA-event roofline of its dominant kernel, clocks sampled inside its timed region), one after
-    the other, each freed before the next.  Returns name -> summary."""
-    import copy
-    import torch
-    from memory_lean_optimizer_gb300 import workloads as W
-    out = {}
+    CUDA-event roofline of its dominant kernel, clocks sampled inside its timed region), each in a
+    process of its own (so that no workload runs on the allocator state another one left), one
+    after the other.  Returns name -> summary."""
     keep = ("ms_per_step", "value", "unit", "steps", "warmup", "roofline", "clocks", "ms_per_step_median",
             "first_step_ms", "hbm_gbs_step", "hbm_gbs_step_as_run", "link_gbs", "h2d_gbs", "d2h_gbs",
-            "hbm_gbs_kernels_over_step", "link_peak_gbs", "gpu_launches")
-    plan = [("ragged20k", "nadam", {}), ("sdxl_like", "factored", {}), ("flux35", "offload", {"steps": 3}),
-            ("nadam_1m", "nadam", {"steps": 100})]
-    for name, kind, over in plan:
-        a = copy.copy(args)
-        a.workload = name
-        a.steps = over.get("steps", min(args.steps, 10))
-        a.warmup = max(3, args.warmup)
-        a.states, a.rounding, a.optimizer = "u16", "kahan", "nadam"
-        cfg = W.config(name)
+            "hbm_gbs_kernels_over_step", "link_peak_gbs", "gpu_launches", "config")
+    plan = [("ragged20k", min(args.steps, 10)), ("sdxl_like", min(args.steps, 10)), ("flux35", 3), ("nadam_1m", 100)]
+    out = {}
+    for name, steps in plan:
+        cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--workload", name, "--steps", str(steps),
+               "--warmup", str(max(3, args.warmup)), "--no-workloads", "--no-e2e", "--no-cpu-baseline"]
         try:
-            if kind == "nadam":
-                r = measure_nadam(a, cfg, e2e=False)
-            elif kind == "factored":
-                r = measure_factored(a, cfg)
-            else:
-                r = measure_offload(a, cfg)
-            summary = {k: r[k] for k in keep if k in r}
-            summary["config"] = r.get("config")
-            out[name] = summary
+            r = subprocess.run(cmd, capture_output=True, text=True, timeout=900, cwd=ROOT)
+            lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+            if r.returncode != 0 or not lines:
+                out[name] = {"error": f"exit {r.returncode}: {r.stderr.strip()[-300:]}"}
+                continue
+            d = json.loads(lines[-1])
+            out[name] = {k: d[k] for k in keep if k in d}
         except Exception as e:            # one workload failing must not lose the headline line
             out[name] = {"error": f"{type(e).__name__}: {e}"[:400]}
-        torch.cuda.synchronize()
-        torch.cuda.empty_cache()
     return out
 
 
