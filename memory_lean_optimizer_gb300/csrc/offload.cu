@@ -351,7 +351,11 @@ void offload_unbind(optim_group* g) {
                 break;
             }
         if (--e->bound == 0) {
+            // copies may still be queued on callers' copy streams: wait (bounded) for every
+            // slot's last events as well as the ring's own streams before freeing the slots
             stream_wait_all(e);
+            for (Slot& sl : e->slots)
+                for (cudaEvent_t ev : {sl.h2d_done, sl.comp_done, sl.d2h_done}) wait_event(ev, kWaitTimeout, "staging slot");
             g_ring[e->device] = nullptr;
             engine_free(e);
         }
