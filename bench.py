@@ -576,7 +576,7 @@ def run_offload(args, cfg):
 
 
 def link_probe(device, nbytes=1 << 30, reps=3):
-    """Pinned-host <-> device copy peak of this box: both directions at once on two streams, best
+    """Pinned-host <-> device copy peak of this machine: both directions at once on two streams, best
     of `reps` after one warm-up repeat (GB/s, bytes both ways / time)."""
     import torch
     h_in = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
@@ -607,7 +607,7 @@ def measure_offload(args, cfg):
     staging slots: by default with the per-group calls (optim_group_attach_host: one pinned image per
     group, prefetch on a copy-in stream before each group's step, write-back on a copy-out stream
     after it), or with --offload-form engine through an engine object.  Reports params/s, the
-    host-link GB/s both ways against a pinned copy probe of the same box, and the HBM GB/s of the
+    host-link GB/s both ways against a pinned copy probe on the same machine, and the HBM GB/s of the
     update kernels."""
     import torch
     from memory_lean_optimizer_gb300 import engine, workloads as W

@@ -1,5 +1,5 @@
 """The benchmark's host-side contract on CPU: the reference arm (the oracle timed on the host)
-prints one JSON line with the keys the driver reads, and the byte counts and DRAM-traffic record
+prints one JSON line with the keys of the benchmark contract, and the byte counts and DRAM-traffic record
 the GPU lines use behave as documented."""
 import json
 import os
