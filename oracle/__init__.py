@@ -190,17 +190,20 @@ def _u16(a):
 
 
 # ---------------------------------------------------------------- Kahan split / merge, bf16
-def kahan_split(x: np.ndarray):
+def kahan_split(x: np.ndarray, hi: np.ndarray | None = None, lo: np.ndarray | None = None):
+    """(hi, lo) halves of each fp32 pattern; hi / lo may be given (contiguous uint16, x's size)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    hi = np.empty(x.shape, np.uint16)
-    lo = np.empty(x.shape, np.uint16)
+    hi = np.empty(x.shape, np.uint16) if hi is None else hi
+    lo = np.empty(x.shape, np.uint16) if lo is None else lo
+    assert hi.dtype == lo.dtype == np.uint16 and hi.size == lo.size == x.size and hi.flags.c_contiguous and lo.flags.c_contiguous
     _load().orc_kahan_split(_p(x), _p(hi), _p(lo), x.size)
     return hi, lo
 
 
-def kahan_merge(hi: np.ndarray, lo: np.ndarray) -> np.ndarray:
+def kahan_merge(hi: np.ndarray, lo: np.ndarray, out: np.ndarray | None = None) -> np.ndarray:
     hi, lo = _u16(hi), _u16(lo)
-    out = np.empty(hi.shape, np.float32)
+    out = np.empty(hi.shape, np.float32) if out is None else out
+    assert out.dtype == np.float32 and out.size == hi.size and out.flags.c_contiguous
     _load().orc_kahan_merge(_p(hi), _p(lo), _p(out), hi.size)
     return out
 

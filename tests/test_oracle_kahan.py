@@ -40,16 +40,22 @@ def test_ieee_fixtures(orc):
 
 @pytest.mark.slow
 def test_split_merge_exhaustive(orc):
-    """merge(split(x)) is the identity on all 2^32 patterns, NaN payloads and -0 included."""
-    chunk = 1 << 26
+    """merge(split(x)) is the identity on all 2^32 patterns, NaN payloads and -0 included.  The
+    buffers are reused chunk after chunk (allocation, not arithmetic, dominated this test)."""
+    chunk = 1 << 24
+    base = np.arange(chunk, dtype=np.uint32)
+    bits = np.empty(chunk, np.uint32)
+    hi, lo = np.empty(chunk, np.uint16), np.empty(chunk, np.uint16)
+    back = np.empty(chunk, np.float32)
+    halves = bits.view(np.uint16)          # little-endian: [2i] the low half, [2i + 1] the high half
+    assert np.little_endian
     for start in range(0, 1 << 32, chunk):
-        bits = np.arange(start, start + chunk, dtype=np.uint64).astype(np.uint32)
-        x = bits.view(np.float32)
-        hi, lo = orc.kahan_split(x)
+        np.add(base, np.uint32(start), out=bits)
+        orc.kahan_split(bits.view(np.float32), hi, lo)
         # the halves are the upper and lower 16 bits of the pattern
-        assert np.array_equal(hi, (bits >> 16).astype(np.uint16))
-        assert np.array_equal(lo, (bits & 0xFFFF).astype(np.uint16))
-        back = orc.kahan_merge(hi, lo)
+        assert np.array_equal(hi, halves[1::2])
+        assert np.array_equal(lo, halves[0::2])
+        orc.kahan_merge(hi, lo, back)
         assert np.array_equal(back.view(np.uint32), bits)
 
 
