@@ -326,8 +326,8 @@ int optim_query_nonfinite(optim_group_t* group, uint64_t* count);
  * step, the copy-out (write-back) follows it; every dependency between them is a device-side
  * event wait, so the host never blocks.  Prefetching group k+1 and writing back group k-1 while
  * group k steps overlaps the copies with the kernels.  A group holds its slot from prefetch to
- * write-back; the slots are taken round-robin, and a prefetch whose next slot is still held
- * returns OPTIM_ESTATE (so at most n_slots - 1 groups can be prefetched ahead).
+ * write-back; a prefetch takes the first free slot after the one taken last, and returns
+ * OPTIM_ESTATE when every slot is held (at most n_slots groups hold slots at once).
  *
  * Two ways to attach a group:
  *   optim_group_attach_host (the per-group form): the caller gives one pinned buffer, the

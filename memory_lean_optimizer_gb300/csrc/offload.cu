@@ -155,10 +155,16 @@ static int prefetch(optim_group* g, cudaStream_t copy) {
     OffloadBinding* b = g->offload;
     optim_offload* e = b->eng;
     if (b->slot >= 0) return OPTIM_OK;
-    const int s = (int)(e->next % e->slots.size());
-    Slot& sl = e->slots[s];
-    if (sl.owner != nullptr)
+    // the first free slot from the ring's cursor on (its previous write-back is waited for below)
+    const int n_slots = (int)e->slots.size();
+    int s = -1;
+    for (int i = 0; i < n_slots && s < 0; ++i) {
+        const int c = (int)((e->next + i) % n_slots);
+        if (e->slots[c].owner == nullptr) s = c;
+    }
+    if (s < 0)
         return set_error(OPTIM_ESTATE, "no free staging slot: step (and write back) the groups already prefetched first");
+    Slot& sl = e->slots[s];
     if (fault("h2d")) return set_error(OPTIM_ECUDA, "injected H2D copy failure");
     cudaStream_t cs = copy ? copy : e->h2d;
     int rc = check_cuda(cudaStreamWaitEvent(cs, sl.d2h_done, 0), "offload h2d wait");
@@ -175,7 +181,7 @@ static int prefetch(optim_group* g, cudaStream_t copy) {
     sl.owner = g;
     b->slot = s;
     b->stepped = false;
-    e->next++;
+    e->next = (uint64_t)s + 1;
     return OPTIM_OK;
 }
 

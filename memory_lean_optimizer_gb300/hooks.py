@@ -59,6 +59,7 @@ class FusedStepper:
         self.on_all = on_all          # called once every group has stepped (end of a backward)
         self.stepped = 0
         self.steps_taken = [0] * len(self.groups)
+        self.ahead = None             # group whose offloaded states were prefetched ahead of its hook
         self.handles = [p.register_post_accumulate_grad_hook(self._hook) for p in self.params]
 
     def _hook(self, p: torch.Tensor):
@@ -70,7 +71,21 @@ class FusedStepper:
         grads = [self.params[i].grad for i in idx]
         if self.on_step is not None:
             self.on_step(gi, grads)
-        self.groups[gi].step(grads, self.hp, None)
+        g = self.groups[gi]
+        host = getattr(g, "image", None) is not None   # states in a pinned host image (attach_host)
+        if host:
+            g.prefetch()                                # nothing if already prefetched
+            if self.ahead == gi:
+                self.ahead = None
+        g.step(grads, self.hp, None)
+        if host:
+            g.writeback()
+            # gradients arrive roughly in reverse parameter order: bring the next group's states
+            # in while the backward pass goes on (one group ahead at most, so that with the ring's
+            # three slots a group about to step always finds one)
+            if self.ahead is None and gi > 0 and getattr(self.groups[gi - 1], "image", None) is not None:
+                self.groups[gi - 1].prefetch()
+                self.ahead = gi - 1
         self.steps_taken[gi] += 1
         for i in idx:
             self.params[i].grad = None
@@ -87,13 +102,20 @@ class FusedStepper:
         self.handles = []
 
 
-def attach_fused_nadam(params: Sequence[torch.nn.Parameter], n_groups: int, hp: dict, on_step=None) -> FusedStepper:
+def attach_fused_nadam(params: Sequence[torch.nn.Parameter], n_groups: int, hp: dict, on_step=None,
+                       offload: bool = False) -> FusedStepper:
     """bf16 parameters stepped in place by the fused NAdam+Kahan engine (the parameter's bf16
-    storage is the live weight; residuals and u16 moments are allocated per group)."""
+    storage is the live weight; residuals and u16 moments are allocated per group).  offload:
+    each group's residuals and moments live in a pinned host image between its steps (the
+    per-group offload calls; each hook prefetches, steps, writes back, and prefetches the group
+    whose gradients come next)."""
     from .engine import NadamGroup
 
     def make(ps):
-        return NadamGroup([p.data for p in ps])
+        g = NadamGroup([p.data for p in ps])
+        if offload:
+            g.attach_host()
+        return g
     return FusedStepper(params, n_groups, hp, make, on_step)
 
 

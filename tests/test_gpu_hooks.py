@@ -14,8 +14,12 @@ pytestmark = pytest.mark.gpu
 HP = dict(W.NADAM_HP, lr=1e-3)
 
 
-def test_fused_backward_hooks_match_oracle(orc):
+@pytest.mark.parametrize("offload", [False, True])
+def test_fused_backward_hooks_match_oracle(orc, offload):
+    """offload: the groups' residuals and moments live in pinned host images between steps (the
+    per-group offload calls from the hooks)."""
     from memory_lean_optimizer_gb300 import build
+    from memory_lean_optimizer_gb300.engine import OffloadEngine
     from memory_lean_optimizer_gb300.hooks import attach_fused_nadam
     build.build()
     torch.manual_seed(0)
@@ -28,12 +32,14 @@ def test_fused_backward_hooks_match_oracle(orc):
     def on_step(gi, grads):
         captured.setdefault(gi, []).append([W.bits16(g).reshape(-1).copy() for g in grads])
 
-    stepper = attach_fused_nadam(params, 3, HP, on_step=on_step)
+    stepper = attach_fused_nadam(params, 3, HP, on_step=on_step, offload=offload)
     x = torch.randn(32, 256, device="cuda", dtype=torch.bfloat16)
     for _ in range(3):
         loss = model(x).float().pow(2).mean()
         loss.backward()
     torch.cuda.synchronize()
+    if offload:
+        OffloadEngine.sync_library_ring()
     assert all(p.grad is None for p in params)
     assert all(len(captured[gi]) == 3 for gi in range(len(stepper.groups)))
     for gi, idx in enumerate(stepper.index):
