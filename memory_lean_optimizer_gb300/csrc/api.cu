@@ -189,6 +189,31 @@ static int validate_grads(const optim_group* g, const void* const* grads) {
 
 static bool finite_nonneg(float x) { return std::isfinite(x) && x >= 0.0f; }
 
+// What the update kernels take for granted about a group's chunk table, checked once when it is
+// built: every entry names a tensor of the group, the u16-state (large) tensors' chunks come
+// first, and each tensor's chunks are 0, 1, ..., ceil(numel / chunk) - 1 in that order, so that
+// every chunk starts inside its tensor and every element lies in exactly one chunk.
+static int check_chunk_table(const optim_tensor_desc_t* t, int32_t n, const std::vector<Chunk>& chunks,
+                             int64_t chunk, int32_t n_large) {
+    std::vector<int64_t> next(n, 0);
+    for (size_t j = 0; j < chunks.size(); ++j) {
+        const Chunk c = chunks[j];
+        if (c.tensor < 0 || c.tensor >= n)
+            return set_error(OPTIM_EINVAL, "internal: chunk table entry %zu names tensor %d of %d", j, c.tensor, n);
+        const int64_t ne = t[c.tensor].numel;
+        if (((int64_t)j < n_large) != (ne > kSmall))
+            return set_error(OPTIM_EINVAL, "internal: chunk table entry %zu outside its tensor's section", j);
+        if (c.index != next[c.tensor] || (int64_t)c.index * chunk >= ne)
+            return set_error(OPTIM_EINVAL, "internal: chunk table entry %zu (tensor %d, chunk %d) out of order or "
+                             "past the tensor's end", j, c.tensor, c.index);
+        ++next[c.tensor];
+    }
+    for (int32_t i = 0; i < n; ++i)
+        if (next[i] != (t[i].numel + chunk - 1) / chunk)
+            return set_error(OPTIM_EINVAL, "internal: tensor %d covered by %lld chunks", i, (long long)next[i]);
+    return OPTIM_OK;
+}
+
 extern "C" {
 
 const char* optim_last_error(void) { return g_err; }
@@ -244,6 +269,7 @@ int optim_group_create(const optim_tensor_desc_t* tensors, int32_t n, int32_t ki
             }
             if (chunks.size() > (size_t)INT32_MAX) rc = set_error(OPTIM_EINVAL, "group too large");
             g->n_chunks_total = (int32_t)chunks.size();
+            if (!rc) rc = check_chunk_table(tensors, n, chunks, g->chunk, g->n_chunks_large);
         }
         if (!rc) rc = dev_upload(&g->d_tensors, recs, "tensor table");
         if (!rc) rc = dev_upload(&g->d_chunks, chunks, "chunk table");
