@@ -16,42 +16,16 @@ struct AdanPrm {
     float lr, b1, omb1, b2, omb2, b3, omb3, eps, inv_decay;
     int32_t sr;
     int64_t step;
-    uint64_t seed;
+    PhiloxKey key;        // stochastic rounding: the generator's key schedule for the seed
 };
 
-// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
-// SC 2011), the same stream as the NAdam kernels: key (seed low, seed high), counter (b low,
-// b high, tensor, step mod 2^32) for the 8-element block b = i / 8; element i takes 16-bit lane
-// i mod 8 (word (i mod 8) / 2, low half for even i).
-__device__ __forceinline__ void philox4x32_10(uint32_t (&c)[4], uint32_t k0, uint32_t k1) {
-    constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u, W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
-#pragma unroll
-    for (int r = 0; r < 10; ++r) {
-        const uint64_t p0 = (uint64_t)M0 * c[0], p1 = (uint64_t)M1 * c[2];
-        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c[1] ^ k0;
-        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c[3] ^ k1;
-        c[0] = n0;
-        c[1] = (uint32_t)p1;
-        c[2] = n2;
-        c[3] = (uint32_t)p0;
-        k0 += W0;
-        k1 += W1;
-    }
-}
+// Stochastic rounding draws from the same stream as the NAdam kernels (key, counter and lanes
+// as described with philox4x32_10).
 __device__ __forceinline__ void sr_block(const AdanPrm& k, uint32_t tensor, int64_t i, uint32_t (&r)[4]) {
-    const uint64_t b = (uint64_t)i >> 3;
-    r[0] = (uint32_t)b;
-    r[1] = (uint32_t)(b >> 32);
-    r[2] = tensor;
-    r[3] = (uint32_t)k.step;
-    philox4x32_10(r, (uint32_t)k.seed, (uint32_t)(k.seed >> 32));
+    sr_block8(k.key, (uint64_t)k.step, tensor, i, r);
 }
 __device__ __forceinline__ uint32_t sr_lane(const AdanPrm& k, uint32_t tensor, int64_t i) {
-    uint32_t r[4];
-    sr_block(k, tensor, i, r);
-    const int lane = (int)(i & 7);
-    const uint32_t wsel = lane < 2 ? r[0] : (lane < 4 ? r[1] : (lane < 6 ? r[2] : r[3]));
-    return (wsel >> (16 * (lane & 1))) & 0xFFFFu;
+    return sr_lane1(k.key, (uint64_t)k.step, tensor, i);
 }
 
 __device__ __forceinline__ float adan_elem(const AdanPrm& k, float w, float g, float gp, float& m, float& v, float& n) {
@@ -79,7 +53,7 @@ __device__ __forceinline__ uint32_t store_bits(float w1, bool has_res, bool sr, 
         return b >> 16;
     }
     lo = 0u;
-    if (sr) return ((b & 0x7F800000u) == 0x7F800000u) ? (b >> 16) : ((b + rnd) >> 16);
+    if (sr) return sr_bf16(w1, rnd);
     return rne_bf16(w1);
 }
 
@@ -253,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_adan_step(NadamLaunch L, AdanPr
 }  // namespace
 
 int launch_adan_step(const NadamLaunch& L, const AdanScalars& s, cudaStream_t stream) {
-    AdanPrm k{s.lr, s.b1, s.omb1, s.b2, s.omb2, s.b3, s.omb3, s.eps, s.inv_decay, s.sr, s.step, s.seed};
+    AdanPrm k{s.lr, s.b1, s.omb1, s.b2, s.omb2, s.b3, s.omb3, s.eps, s.inv_decay, s.sr, s.step, philox_key(s.seed)};
     if (L.n_chunks_total == 0) return OPTIM_OK;
     if (L.f24) {
         if (s.sr) k_adan_step<true, true><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k);

@@ -85,6 +85,63 @@ __device__ __forceinline__ uint32_t rne_bf16(float x) {
     return up & 0xFFFFu;
 }
 
+// ---- stochastic rounding -------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
+// SC 2011): four 32-bit counter words, ten rounds of two 32x32->64 multiplies; round r XORs in
+// the key words k0 + r W0 and k1 + r W1 (Weyl sequence), precomputed here once per launch so
+// that the rounds read them as kernel parameters.  Key (seed low, seed high); counter (b low,
+// b high, tensor, step mod 2^32) for the 8-element block b = i / 8; element i takes 16-bit lane
+// i mod 8 (word (i mod 8) / 2, low half for even i).
+struct PhiloxKey {
+    uint32_t k0[10], k1[10];
+};
+__host__ __device__ inline PhiloxKey philox_key(uint64_t seed) {
+    PhiloxKey key;
+    for (int r = 0; r < 10; ++r) {
+        key.k0[r] = (uint32_t)seed + (uint32_t)r * 0x9E3779B9u;
+        key.k1[r] = (uint32_t)(seed >> 32) + (uint32_t)r * 0xBB67AE85u;
+    }
+    return key;
+}
+__device__ __forceinline__ void philox4x32_10(uint32_t (&c)[4], const PhiloxKey& key) {
+    constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint64_t p0 = (uint64_t)M0 * c[0], p1 = (uint64_t)M1 * c[2];
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c[1] ^ key.k0[r];
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c[3] ^ key.k1[r];
+        c[0] = n0;
+        c[1] = (uint32_t)p1;
+        c[2] = n2;
+        c[3] = (uint32_t)p0;
+    }
+}
+// The random words of the 8-element block holding element i (i need not be a multiple of 8).
+__device__ __forceinline__ void sr_block8(const PhiloxKey& key, uint64_t step, uint32_t tensor, int64_t i,
+                                          uint32_t (&r)[4]) {
+    const uint64_t b = (uint64_t)i >> 3;
+    r[0] = (uint32_t)b;
+    r[1] = (uint32_t)(b >> 32);
+    r[2] = tensor;
+    r[3] = (uint32_t)step;
+    philox4x32_10(r, key);
+}
+// Element i's 16 random bits.
+__device__ __forceinline__ uint32_t sr_lane1(const PhiloxKey& key, uint64_t step, uint32_t tensor, int64_t i) {
+    uint32_t r[4];
+    sr_block8(key, step, tensor, i, r);
+    const int lane = (int)(i & 7);
+    const uint32_t wsel = lane < 2 ? r[0] : (lane < 4 ? r[1] : (lane < 6 ? r[2] : r[3]));
+    return (wsel >> (16 * (lane & 1))) & 0xFFFFu;
+}
+// Stochastic rounding to bf16 bits: the 16 random bits are added below the kept half, which
+// rounds the magnitude up with probability (dropped bits) / 2^16.  Infinities and NaNs are kept
+// as they are (a NaN's all-ones payload would otherwise carry into the sign).
+__device__ __forceinline__ uint32_t sr_bf16(float x, uint32_t r16) {
+    const uint32_t b = __float_as_uint(x);
+    return (b + (fabsf(x) < __int_as_float(0x7F800000) ? r16 : 0u)) >> 16;
+}
+
 // ---- u16 companded codec --------------------------------------------------------------
 // Curve: exp_avg code = 32768 + sgn(m) rint(32767 (|m|/S)^(1/2)); exp_avg_sq code =
 // rint(65535 (v/S)^(1/4)).  Scale and code step are folded into four per-tensor constants:

@@ -31,55 +31,17 @@ struct Prm {
     float lr, b1, omb1, b2, omb2, eps, lr_wd, c_m, c_g, k2;
     int32_t decoupled;
     int32_t sr;           // stochastic rounding of tensors without a residual
-    uint64_t seed;
     uint64_t step;
+    PhiloxKey key;        // stochastic rounding: the generator's key schedule for the seed
 };
 
-// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
-// SC 2011): ten rounds of two 32x32->64 multiplies with Weyl-sequence key bumps.
-__device__ __forceinline__ void philox4x32_10(uint32_t (&c)[4], uint32_t k0, uint32_t k1) {
-    constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u, W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
-#pragma unroll
-    for (int r = 0; r < 10; ++r) {
-        const uint64_t p0 = (uint64_t)M0 * c[0], p1 = (uint64_t)M1 * c[2];
-        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c[1] ^ k0;
-        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c[3] ^ k1;
-        c[0] = n0;
-        c[1] = (uint32_t)p1;
-        c[2] = n2;
-        c[3] = (uint32_t)p0;
-        k0 += W0;
-        k1 += W1;
-    }
-}
-// Random 16-bit lanes for the 8 elements i0 .. i0+7 (i0 % 8 == 0) of tensor `tensor`: key
-// (seed low, seed high), counter (b low, b high, tensor, step mod 2^32) with b = i0 / 8; word j
+// Random 16-bit lanes for the 8 elements i0 .. i0+7 (i0 % 8 == 0) of tensor `tensor`; word j
 // holds lanes 2j (low half) and 2j+1.
 __device__ __forceinline__ void sr_lanes8(const Prm& k, uint32_t tensor, int64_t i0, uint32_t (&r)[4]) {
-    const uint64_t b = (uint64_t)i0 >> 3;
-    r[0] = (uint32_t)b;
-    r[1] = (uint32_t)(b >> 32);
-    r[2] = tensor;
-    r[3] = (uint32_t)k.step;
-    philox4x32_10(r, (uint32_t)k.seed, (uint32_t)(k.seed >> 32));
-}
-__device__ __forceinline__ void sr_lanes16(const Prm& k, uint32_t tensor, int64_t i0, uint32_t (&ra)[4],
-                                           uint32_t (&rb)[4]) {
-    sr_lanes8(k, tensor, i0, ra);
-    sr_lanes8(k, tensor, i0 + 8, rb);
+    sr_block8(k.key, k.step, tensor, i0, r);
 }
 __device__ __forceinline__ uint32_t sr_lane1(const Prm& k, uint32_t tensor, int64_t i) {
-    uint32_t r[4];
-    sr_lanes8(k, tensor, i & ~(int64_t)7, r);
-    const int lane = (int)(i & 7);
-    const uint32_t wsel = lane < 2 ? r[0] : (lane < 4 ? r[1] : (lane < 6 ? r[2] : r[3]));
-    return (wsel >> (16 * (lane & 1))) & 0xFFFFu;
-}
-// Stochastic rounding to bf16 bits: add 16 random bits below the kept half (inf/NaN kept).
-__device__ __forceinline__ uint32_t sr_bf16(float x, uint32_t r16) {
-    const uint32_t b = __float_as_uint(x);
-    if ((b & 0x7F800000u) == 0x7F800000u) return b >> 16;
-    return (b + r16) >> 16;
+    return sr_lane1(k.key, k.step, tensor, i);
 }
 
 // ------------------------------------------------------------------------------------ K1
@@ -665,7 +627,7 @@ int nadam_fused_capacity(bool sr) {
 
 int launch_nadam_fused(const NadamLaunch& L, const NadamScalars& s, cudaStream_t stream, unsigned* bar,
                        unsigned target) {
-    Prm k{s.lr, s.b1, s.omb1, s.b2, s.omb2, s.eps, s.lr_wd, s.c_m, s.c_g, s.k2, s.decoupled, s.sr, s.seed, s.step};
+    Prm k{s.lr, s.b1, s.omb1, s.b2, s.omb2, s.eps, s.lr_wd, s.c_m, s.c_g, s.k2, s.decoupled, s.sr, s.step, philox_key(s.seed)};
     NadamLaunch Lc = L;
     int parity = s.parity;
     void* args[] = {&Lc, &k, &parity, &bar, &target};
@@ -675,7 +637,7 @@ int launch_nadam_fused(const NadamLaunch& L, const NadamScalars& s, cudaStream_t
 }
 
 int launch_nadam_update(const NadamLaunch& L, const NadamScalars& s, cudaStream_t stream, cudaEvent_t mid) {
-    Prm k{s.lr, s.b1, s.omb1, s.b2, s.omb2, s.eps, s.lr_wd, s.c_m, s.c_g, s.k2, s.decoupled, s.sr, s.seed, s.step};
+    Prm k{s.lr, s.b1, s.omb1, s.b2, s.omb2, s.eps, s.lr_wd, s.c_m, s.c_g, s.k2, s.decoupled, s.sr, s.step, philox_key(s.seed)};
     if (mid) {
         int rc = check_cuda(cudaEventRecord(mid, stream), "profile event");
         if (rc) return rc;
