@@ -5,7 +5,7 @@
 // placement of prodigy PR #25 ("more VRAM savings: no first moment and factored second moment"):
 //   q = g*g + eps1 (Adafactor) | g*g (Prodigy)
 //   R = b2t*R + alpha*mean_j(q) (+eps2),  C = b2t*C + alpha*mean_i(q) (+eps2)
-//   u_ij = (rsqrt(R_i / mean(R)) * rsqrt(C_j)) * g_ij        (1-D: u = rsqrt(V) * g)
+//   u_ij = (rsqrt(R_i / mean(R)) * rsqrt(C_j)) * g_ij        (1-D: u = rsqrt(V) * g);  Prodigy: u = u * d
 //   u = (u / max(1, RMS(u)/clip)) * lr_eff;  w = w + w*(-wd*lr_eff);  w = w - u;  Kahan split
 // Factoring is over the last two dims; leading dims are a batch of matrices.
 //
@@ -102,7 +102,7 @@ struct Dev {
 struct K {
     float b2t, alpha, eps1, eps2, clip, lr_eff, nwdlr;
     int32_t mode;
-    float unum, lr_u;
+    float unum;
     const FactoredDevScalars* kdev;
 };
 // The d-dependent scalars from device memory when d is adaptive; called by every kernel right
@@ -114,7 +114,6 @@ __device__ __forceinline__ void load_k(K& k) {
     k.lr_eff = v.lr_eff;
     k.nwdlr = v.nwdlr;
     k.unum = v.unum;
-    k.lr_u = v.lr_u;
 }
 
 __device__ __forceinline__ float qval(float g, const K& k) {
@@ -201,8 +200,14 @@ __device__ __forceinline__ uint32_t max_bf16_mag(uint32_t nf, const uint4& W) {
 // clipped update is then fl(u * fl(lr / den)) rather than fl(fl(u / den) * lr): one multiply per
 // element instead of a division, within about one ulp of the update.
 __device__ __forceinline__ float update_scale(float den, const K& k) {
-    return den == 1.0f ? k.lr_u : __fdiv_rn(k.lr_u, den);
+    return den == 1.0f ? k.lr_eff : __fdiv_rn(k.lr_eff, den);
 }
+// The update's numerator factor: u d in Prodigy mode (the first moment of Prodigy with beta1 = 0
+// is d g), applied to each element before its square is summed and before the clip, as the
+// step is defined; Adafactor mode leaves u as it is.
+template <bool kP>
+__device__ __forceinline__ float numer(float u, const K& k) { return kP ? __fmul_rn(u, k.unum) : u; }
+__device__ __forceinline__ float numer_rt(float u, const K& k) { return k.mode == 1 ? __fmul_rn(u, k.unum) : u; }
 
 __device__ __forceinline__ void apply_elem(uint32_t& hi, uint32_t& lo, bool has_res, float u, float s, const K& k) {
     float w = has_res ? __uint_as_float((hi << 16) | lo) : bf16_to_f32(hi);
@@ -218,11 +223,10 @@ __device__ __forceinline__ void apply_elem(uint32_t& hi, uint32_t& lo, bool has_
     }
 }
 
-// Clip divisor from the tensor's fp32 sum of squares.
-// ss: sum of squares of the update before its numerator factor unum (1, or d in Prodigy mode).
-__device__ __forceinline__ float clip_den(float ss, int64_t n, float clip, float unum) {
+// Clip divisor from the tensor's fp32 sum of squares of the update (numerator factor included).
+__device__ __forceinline__ float clip_den(float ss, int64_t n, float clip) {
     const float ms = __fdiv_rn(ss, (float)n);
-    const float r = __fdiv_rn(__fmul_rn(__fsqrt_rn(ms), unum), clip);
+    const float r = __fdiv_rn(__fsqrt_rn(ms), clip);
     return r < 1.0f ? 1.0f : r;   // a NaN RMS stays NaN (clamp(min=1) semantics), as in the oracle
 }
 
@@ -244,7 +248,7 @@ __device__ void finish_ss(const Dev& D, const FTensor& t, int tensor, int part, 
     for (int i = threadIdx.x; i < t.ss_cnt; i += blockDim.x) acc.add(__ldcg(D.ss + t.ss_off + i));
     const float tot = block_sum(acc.value(), sm);
     if (threadIdx.x == 0) {
-        D.den[tensor] = clip_den(tot, t.numel, k.clip, k.unum);
+        D.den[tensor] = clip_den(tot, t.numel, k.clip);
         D.counter[tensor] = 0u;
     }
 }
@@ -337,7 +341,7 @@ __device__ __noinline__ float tiny_stats_any(const uint16_t* gm, float* Rs, floa
     for (int i = 0; i < r; ++i) {
         const float rr = rsqrt_rn(__fdiv_rn(rsum[i], rbar));
         for (int j = 0; j < c; ++j) {
-            const float u = __fmul_rn(__fmul_rn(rr, csum[j]), bf16_to_f32(gm[i * c + j]));
+            const float u = numer_rt(__fmul_rn(__fmul_rn(rr, csum[j]), bf16_to_f32(gm[i * c + j])), k);
             acc = __fadd_rn(acc, __fmul_rn(u, u));
         }
     }
@@ -391,19 +395,21 @@ __device__ __forceinline__ float stats3(const uint16_t* gm, float* Rs, float* Cs
     float acc = 0.f;
 #pragma unroll
     for (int e = 0; e < 9; ++e) {
-        const float u = __fmul_rn(__fmul_rn(f.rr[e / 3], f.cc[e % 3]), bf16_to_f32(gm[e]));
+        float u = __fmul_rn(__fmul_rn(f.rr[e / 3], f.cc[e % 3]), bf16_to_f32(gm[e]));
+        if (kProdigy) u = __fmul_rn(u, k.unum);
         acc = __fmaf_rn(u, u, acc);
     }
     return acc;
 }
-template <bool kRes, bool kDecay>
+template <bool kRes, bool kDecay, bool kProdigy>
 __device__ __forceinline__ void apply3(uint16_t* wm, uint16_t* rm, const uint16_t* gm, const float* Rs,
-                                       const float* Cs, float us, float nwdlr) {
+                                       const float* Cs, float us, float nwdlr, float unum) {
     const Fac3 f = factors3(Rs[0], Rs[1], Rs[2], Cs);
 #pragma unroll
     for (int e = 0; e < 9; ++e) {
         float w = kRes ? __uint_as_float(((uint32_t)wm[e] << 16) | rm[e]) : bf16_to_f32(wm[e]);
-        const float u = __fmul_rn(__fmul_rn(f.rr[e / 3], f.cc[e % 3]), bf16_to_f32(gm[e]));
+        float u = __fmul_rn(__fmul_rn(f.rr[e / 3], f.cc[e % 3]), bf16_to_f32(gm[e]));
+        if (kProdigy) u = __fmul_rn(u, unum);
         if (kDecay) w = __fadd_rn(w, __fmul_rn(w, nwdlr));
         w = __fsub_rn(w, __fmul_rn(u, us));
         const uint32_t b = __float_as_uint(w);
@@ -469,10 +475,10 @@ __device__ __forceinline__ float conv3_stats(const uint16_t* g, float* row, floa
     return acc;
 }
 
-template <bool kRes, bool kDecay>
+template <bool kRes, bool kDecay, bool kProdigy>
 __device__ __forceinline__ uint32_t conv3_apply(const uint16_t* g, uint16_t* w, uint16_t* res, const float* row,
                                             const float* col, int64_t m_first, int nsub, unsigned char* smem, float us,
-                                            float nwdlr) {
+                                            float nwdlr, float unum) {
     constexpr int kBuf = 3 * kTinyWords * 2 + kTinyStats * 4;
     const int tid = threadIdx.x;
     uint32_t nf = 0u;
@@ -504,9 +510,10 @@ __device__ __forceinline__ uint32_t conv3_apply(const uint16_t* g, uint16_t* w, 
         __syncthreads();
         const int b = kk & 1;
         const float* R = reinterpret_cast<const float*>(plane(b, 3));
-        apply3<kRes, kDecay>(reinterpret_cast<uint16_t*>(plane(b, 1)) + tid * 9, reinterpret_cast<uint16_t*>(plane(b, 2)) + tid * 9,
-                             reinterpret_cast<const uint16_t*>(plane(b, 0)) + tid * 9, R + tid * 3, R + kTinySub * 3 + tid * 3,
-                             us, nwdlr);
+        apply3<kRes, kDecay, kProdigy>(reinterpret_cast<uint16_t*>(plane(b, 1)) + tid * 9,
+                                       reinterpret_cast<uint16_t*>(plane(b, 2)) + tid * 9,
+                                       reinterpret_cast<const uint16_t*>(plane(b, 0)) + tid * 9, R + tid * 3,
+                                       R + kTinySub * 3 + tid * 3, us, nwdlr, unum);
         __syncthreads();
         const int64_t m = m_first + (int64_t)kk * kTinySub;
 #pragma unroll
@@ -534,6 +541,7 @@ __device__ __noinline__ float tiny_stats_call(const uint16_t* gm, float* Rs, flo
 }
 
 // Apply step of any small matrix on staged words (w, res, g and R, C in shared memory).
+template <bool kP>
 __device__ __noinline__ void tiny_apply_any(uint16_t* wm, uint16_t* rm, const uint16_t* gm, const float* Rs, const float* Cs,
                                int r, int c, bool has_res, float us, const K& k) {
     float rtot = 0.f, cfac[16];
@@ -545,7 +553,7 @@ __device__ __noinline__ void tiny_apply_any(uint16_t* wm, uint16_t* rm, const ui
         for (int j = 0; j < c; ++j) {
             const int e = i * c + j;
             uint32_t hi = wm[e], lo = has_res ? rm[e] : 0u;
-            apply_elem(hi, lo, has_res, __fmul_rn(__fmul_rn(rr, cfac[j]), bf16_to_f32(gm[e])), us, k);
+            apply_elem(hi, lo, has_res, numer<kP>(__fmul_rn(__fmul_rn(rr, cfac[j]), bf16_to_f32(gm[e])), k), us, k);
             wm[e] = (uint16_t)hi;
             if (has_res) rm[e] = (uint16_t)lo;
         }
@@ -585,6 +593,7 @@ __device__ __forceinline__ float warp_sum8(const float (&v)[8], int lane) {
 
 
 // ------------------------------------------------------------------------------------ stats
+template <bool kP>
 __global__ void __launch_bounds__(kThreads, 4) k_stats(Dev D, const Item* items, K k) {
     __shared__ float sm[32];
     __shared__ __align__(16) unsigned char smem[kStatsSmem];
@@ -693,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_stats(Dev D, const Item* items,
         const bool pipe = nmat % sub == 0 && aligned16(g) && aligned16(t.row) && aligned16(t.col);
         const int nsub = (int)((nmat + sub - 1) / sub);
         if (pipe && r == 3 && c == 3) {
-            acc = k.mode == 1 ? conv3_stats<true>(g, t.row, t.col, it.x, nsub, smem, k)
+            acc = kP ? conv3_stats<true>(g, t.row, t.col, it.x, nsub, smem, k)
                               : conv3_stats<false>(g, t.row, t.col, it.x, nsub, smem, k);
         } else if (pipe) {
             for (int kk = -1; kk < nsub; ++kk) {
@@ -717,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_stats(Dev D, const Item* items,
                     const uint16_t* gm = words(b) + i * rc;
                     float a;
                     if (r == 3 && c == 3)
-                        a = k.mode == 1 ? stats3<true>(gm, sR + i * r, sC + i * c, k) : stats3<false>(gm, sR + i * r, sC + i * c, k);
+                        a = kP ? stats3<true>(gm, sR + i * r, sC + i * c, k) : stats3<false>(gm, sR + i * r, sC + i * c, k);
                     else
                         a = tiny_stats_any(gm, sR + i * r, sC + i * c, r, c, k);
                     acc = __fadd_rn(acc, a);
@@ -756,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_stats(Dev D, const Item* items,
             const float gg = bf16_to_f32(g[e]);
             const float nv = ema(t.col[e], qval(gg, k), k);
             t.col[e] = nv;
-            const float u = __fmul_rn(rsqrt_rn(nv), gg);
+            const float u = numer<kP>(__fmul_rn(rsqrt_rn(nv), gg), k);
             acc = __fadd_rn(acc, __fmul_rn(u, u));
         }
     }
@@ -842,6 +851,7 @@ __global__ void __launch_bounds__(kThreads) k_final(Dev D, const Item* items, K 
 }
 
 // ------------------------------------------------------------------------------------ rms
+template <bool kP>
 __global__ void __launch_bounds__(kThreads, 4) k_rms(Dev D, const Item* items, K k) {
     __shared__ float sm[32];
     const Item it = items[blockIdx.x];
@@ -878,6 +888,8 @@ __global__ void __launch_bounds__(kThreads, 4) k_rms(Dev D, const Item* items, K
         const float2 cc2[4] = {make_float2(ccv[0], ccv[1]), make_float2(ccv[2], ccv[3]), make_float2(ccv[4], ccv[5]),
                                make_float2(ccv[6], ccv[7])};
         float2 acc2 = f2(0.f);
+        constexpr bool prodigy = kP;
+        const float2 un2 = f2(k.unum);
 #pragma unroll 1
         for (int kb = 0; kb < kTR / 64; ++kb) {
             if (kb > 0) {
@@ -896,7 +908,8 @@ __global__ void __launch_bounds__(kThreads, 4) k_rms(Dev D, const Item* items, K
                     const uint32_t wd[4] = {x[kk].x, x[kk].y, x[kk].z, x[kk].w};
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const float2 u = __fmul2_rn(__fmul2_rn(f2(rr), cc2[q]), bf16x2_to_f2(wd[q]));
+                        float2 u = __fmul2_rn(__fmul2_rn(f2(rr), cc2[q]), bf16x2_to_f2(wd[q]));
+                        if (prodigy) u = __fmul2_rn(u, un2);
                         acc2 = __ffma2_rn(u, u, acc2);
                     }
                 }
@@ -913,7 +926,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_rms(Dev D, const Item* items, K
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 if (j < ncols) {
-                    const float u = __fmul_rn(__fmul_rn(rr, ccv[j]), bf16_to_f32(v[j]));
+                    const float u = numer<kP>(__fmul_rn(__fmul_rn(rr, ccv[j]), bf16_to_f32(v[j])), k);
                     acc = __fadd_rn(acc, __fmul_rn(u, u));
                 }
             }
@@ -925,9 +938,10 @@ __global__ void __launch_bounds__(kThreads, 4) k_rms(Dev D, const Item* items, K
 
 // ------------------------------------------------------------------------------------ apply
 // Applies the update to the eight elements of one row held in (Wv, Rv) with gradients G, in
-// packed pairs: u = (rr * cc_j) * g_j;  w = w + w*nwdlr (when decaying);  w = w + u*(-s);  split.
+// packed pairs: u = (rr * cc_j) * g_j (times d in Prodigy mode);  w = w + w*nwdlr (when decaying);
+// w = w + u*(-s);  split.
 __device__ __forceinline__ void apply8x2(const uint4& G, uint4& Wv, uint4& Rv, float rr, const float2 (&cc2)[4],
-                                         bool has_res, bool decay, float2 nwd2, float2 ns2) {
+                                         bool has_res, bool decay, float2 nwd2, float2 ns2, bool prodigy, float2 un2) {
     const uint32_t g32[4] = {G.x, G.y, G.z, G.w};
     uint32_t* w32 = reinterpret_cast<uint32_t*>(&Wv);
     uint32_t* r32 = reinterpret_cast<uint32_t*>(&Rv);
@@ -936,7 +950,8 @@ __device__ __forceinline__ void apply8x2(const uint4& G, uint4& Wv, uint4& Rv, f
         float2 w2 = has_res ? make_float2(__uint_as_float(__byte_perm(r32[q], w32[q], 0x5410)),
                                           __uint_as_float(__byte_perm(r32[q], w32[q], 0x7632)))
                             : bf16x2_to_f2(w32[q]);
-        const float2 u2 = __fmul2_rn(__fmul2_rn(f2(rr), cc2[q]), bf16x2_to_f2(g32[q]));
+        float2 u2 = __fmul2_rn(__fmul2_rn(f2(rr), cc2[q]), bf16x2_to_f2(g32[q]));
+        if (prodigy) u2 = __fmul2_rn(u2, un2);
         if (decay) w2 = __fadd2_rn(w2, __fmul2_rn(w2, nwd2));
         w2 = __fadd2_rn(w2, __fmul2_rn(u2, ns2));
         const uint32_t b0 = __float_as_uint(w2.x), b1 = __float_as_uint(w2.y);
@@ -949,6 +964,7 @@ __device__ __forceinline__ void apply8x2(const uint4& G, uint4& Wv, uint4& Rv, f
     }
 }
 
+template <bool kP>
 __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items, K k) {
     __shared__ __align__(16) unsigned char smem[kApplySmem];
     const Item it = items[blockIdx.x];
@@ -987,8 +1003,9 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
             pdl_sync();
             load_k(k);
             const float us = update_scale(D.den[it.tensor], k);
-            const float2 ns2 = f2(-us), nwd2 = f2(k.nwdlr);
+            const float2 ns2 = f2(-us), nwd2 = f2(k.nwdlr), un2 = f2(k.unum);
             const bool decay = k.nwdlr != 0.0f;
+            constexpr bool prodigy = kP;
             float2 cc2[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q)
@@ -1008,12 +1025,12 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
                 const bool hasB = rowB < t.R;
                 const int64_t offA = (b * t.R + rowA) * t.C + col0, offB = offA + 8 * t.C;
                 if (kk > 0) load_pair(kk);
-                apply8x2(GA, WA, RA, rrA, cc2, has_res, decay, nwd2, ns2);
+                apply8x2(GA, WA, RA, rrA, cc2, has_res, decay, nwd2, ns2, prodigy, un2);
                 nf = max_bf16_mag(nf, WA);
                 st_stream(reinterpret_cast<uint4*>(t.w + offA), WA);
                 if (has_res) st_stream(reinterpret_cast<uint4*>(t.res + offA), RA);
                 if (hasB) {
-                    apply8x2(GB, WB, RB, rrB, cc2, has_res, decay, nwd2, ns2);
+                    apply8x2(GB, WB, RB, rrB, cc2, has_res, decay, nwd2, ns2, prodigy, un2);
                     nf = max_bf16_mag(nf, WB);
                     st_stream(reinterpret_cast<uint4*>(t.w + offB), WB);
                     if (has_res) st_stream(reinterpret_cast<uint4*>(t.res + offB), RB);
@@ -1034,7 +1051,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
                 const int64_t off = (b * t.R + row) * t.C + col0;
                 for (int j = 0; j < ncols; ++j) {
                     uint32_t hi = t.w[off + j], lo = has_res ? t.res[off + j] : 0u;
-                    const float u = __fmul_rn(__fmul_rn(rr, ccv[j]), bf16_to_f32(g[off + j]));
+                    const float u = numer<kP>(__fmul_rn(__fmul_rn(rr, ccv[j]), bf16_to_f32(g[off + j])), k);
                     apply_elem(hi, lo, has_res, u, us, k);
                     nf = max(nf, hi & 0x7FFFu);
                     t.w[off + j] = (uint16_t)hi;
@@ -1070,12 +1087,13 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
                           aligned16(t.row) && aligned16(t.col);
         const int nsub = (int)((nmat + sub - 1) / sub);
         if (pipe && r == 3 && c == 3) {
+            const float un = k.unum, nw = k.nwdlr;
             if (has_res) {
-                if (k.nwdlr != 0.0f) nf = conv3_apply<true, true>(g, t.w, t.res, t.row, t.col, it.x, nsub, smem, us, k.nwdlr);
-                else nf = conv3_apply<true, false>(g, t.w, t.res, t.row, t.col, it.x, nsub, smem, us, k.nwdlr);
+                if (nw != 0.0f) nf = conv3_apply<true, true, kP>(g, t.w, t.res, t.row, t.col, it.x, nsub, smem, us, nw, un);
+                else nf = conv3_apply<true, false, kP>(g, t.w, t.res, t.row, t.col, it.x, nsub, smem, us, nw, un);
             } else {
-                if (k.nwdlr != 0.0f) nf = conv3_apply<false, true>(g, t.w, t.res, t.row, t.col, it.x, nsub, smem, us, k.nwdlr);
-                else nf = conv3_apply<false, false>(g, t.w, t.res, t.row, t.col, it.x, nsub, smem, us, k.nwdlr);
+                if (nw != 0.0f) nf = conv3_apply<false, true, kP>(g, t.w, t.res, t.row, t.col, it.x, nsub, smem, us, nw, un);
+                else nf = conv3_apply<false, false, kP>(g, t.w, t.res, t.row, t.col, it.x, nsub, smem, us, nw, un);
             }
             count_nonfinite(D, nf);
             return;
@@ -1092,14 +1110,14 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
                 const float* Rs = sR + i * r;
                 const float* Cs = sC + i * c;
                 if (has_res) {
-                    if (k.nwdlr != 0.0f) apply3<true, true>(wm, rm, gm, Rs, Cs, us, k.nwdlr);
-                    else apply3<true, false>(wm, rm, gm, Rs, Cs, us, k.nwdlr);
+                    if (k.nwdlr != 0.0f) apply3<true, true, kP>(wm, rm, gm, Rs, Cs, us, k.nwdlr, k.unum);
+                    else apply3<true, false, kP>(wm, rm, gm, Rs, Cs, us, k.nwdlr, k.unum);
                 } else {
-                    if (k.nwdlr != 0.0f) apply3<false, true>(wm, rm, gm, Rs, Cs, us, k.nwdlr);
-                    else apply3<false, false>(wm, rm, gm, Rs, Cs, us, k.nwdlr);
+                    if (k.nwdlr != 0.0f) apply3<false, true, kP>(wm, rm, gm, Rs, Cs, us, k.nwdlr, k.unum);
+                    else apply3<false, false, kP>(wm, rm, gm, Rs, Cs, us, k.nwdlr, k.unum);
                 }
             } else
-                tiny_apply_any(sw[b] + i * rc, sr[b] + i * rc, sg[b] + i * rc, sR + i * r, sC + i * c, r, c, has_res, us, k);
+                tiny_apply_any<kP>(sw[b] + i * rc, sr[b] + i * rc, sg[b] + i * rc, sR + i * r, sC + i * c, r, c, has_res, us, k);
             for (int e = 0; e < rc; ++e) nf = max(nf, (uint32_t)(sw[b][i * rc + e] & 0x7FFFu));
         };
         if (pipe) {
@@ -1154,7 +1172,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_apply(Dev D, const Item* items,
     const int64_t e1 = (t.numel < e0 + kVecPerCta ? t.numel : e0 + kVecPerCta);
     for (int64_t e = e0 + threadIdx.x; e < e1; e += kThreads) {
         uint32_t hi = t.w[e], lo = has_res ? t.res[e] : 0u;
-        const float u = __fmul_rn(rsqrt_rn(t.col[e]), bf16_to_f32(g[e]));
+        const float u = numer<kP>(__fmul_rn(rsqrt_rn(t.col[e]), bf16_to_f32(g[e])), k);
         apply_elem(hi, lo, has_res, u, us, k);
         nf = max(nf, hi & 0x7FFFu);
         t.w[e] = (uint16_t)hi;
@@ -1407,14 +1425,14 @@ FactoredScalars factored_scalars(const optim_factored_hparams_t* hp, int64_t ste
         k.unum = d;
     }
     k.nwdlr = (float)(-(double)hp->weight_decay * (double)k.lr_eff);
-    k.lr_u = (float)((double)k.lr_eff * (double)k.unum);
     k.kdev = nullptr;
     return k;
 }
 
 int launch_factored_step(const FactoredPlan* p, const uint16_t* const* d_grads, const FactoredScalars& s,
                          cudaStream_t stream, cudaEvent_t mid, unsigned long long* nonfinite, cudaEvent_t apply_wait) {
-    K k{s.b2t, s.alpha, s.eps1, s.eps2, s.clip, s.lr_eff, s.nwdlr, s.mode, s.unum, s.lr_u, s.kdev};
+    K k{s.b2t, s.alpha, s.eps1, s.eps2, s.clip, s.lr_eff, s.nwdlr, s.mode, s.unum, s.kdev};
+    const bool kp = s.mode == 1;   // Prodigy mode: kernels that apply the numerator factor d
     Dev D = p->dev;
     D.grads = d_grads;
     D.nonfinite = nonfinite;
@@ -1430,13 +1448,16 @@ int launch_factored_step(const FactoredPlan* p, const uint16_t* const* d_grads, 
         const cudaStream_t st = (w % ns == 0) ? stream : p->aux[w % ns - 1];
         const Item* items = p->d_items + wv.item_off;
         const Item* fin = p->d_fin + wv.fin_off;
-        if (wv.n_total > 0) rc = check_cuda(launch_pdl(k_stats, wv.n_total, st, D, items, k), "factored stats launch");
+        if (wv.n_total > 0) rc = check_cuda((kp ? launch_pdl(k_stats<true>, wv.n_total, st, D, items, k)
+                                                  : launch_pdl(k_stats<false>, wv.n_total, st, D, items, k)), "factored stats launch");
         if (!rc && wv.n_fin > 0) rc = check_cuda(launch_pdl(k_final, wv.n_fin, st, D, fin, k), "factored finalize launch");
-        if (!rc && wv.n_wide > 0) rc = check_cuda(launch_pdl(k_rms, wv.n_wide, st, D, items, k), "factored rms launch");
+        if (!rc && wv.n_wide > 0) rc = check_cuda((kp ? launch_pdl(k_rms<true>, wv.n_wide, st, D, items, k)
+                                                            : launch_pdl(k_rms<false>, wv.n_wide, st, D, items, k)), "factored rms launch");
         if (!rc && mid && w + 1 == p->waves.size()) rc = check_cuda(cudaEventRecord(mid, st), "profile event");
         // the first update on each stream waits for apply_wait; later ones follow it on the stream
         if (!rc && apply_wait && (int)w < ns) rc = check_cuda(cudaStreamWaitEvent(st, apply_wait, 0), "apply wait");
-        if (!rc && wv.n_total > 0) rc = check_cuda(launch_pdl(k_apply, wv.n_total, st, D, items, k), "factored apply launch");
+        if (!rc && wv.n_total > 0) rc = check_cuda((kp ? launch_pdl(k_apply<true>, wv.n_total, st, D, items, k)
+                                                              : launch_pdl(k_apply<false>, wv.n_total, st, D, items, k)), "factored apply launch");
     }
     // join every internal stream back into the caller's (also after a launch error, so that no
     // internal stream is left ahead of the caller's)

@@ -10,16 +10,17 @@ namespace lmo {
 // The scalars of a Prodigy-mode step that depend on d, when d lives in device memory (written
 // each step by the Prodigy statistics kernel before the factored kernels read it).
 struct FactoredDevScalars {
-    float alpha, lr_eff, nwdlr, unum, lr_u;
+    float alpha, lr_eff, nwdlr, unum;
 };
 
 // Per-step scalars (host-computed: double, then one rounding to fp32).  unum: the update's
-// numerator factor (1 for Adafactor, d for Prodigy); lr_u = fl(lr_eff unum).  kdev (may be
-// null): device copy of the d-dependent scalars, which then replace the host values.
+// numerator factor (1 for Adafactor, d for Prodigy), applied to each element's update before its
+// sum of squares and its clip, as the factored step defines it.  kdev (may be null): device copy
+// of the d-dependent scalars, which then replace the host values.
 struct FactoredScalars {
     float b2t, alpha, eps1, eps2, clip, lr_eff, nwdlr;
     int32_t mode;
-    float unum, lr_u;
+    float unum;
     const FactoredDevScalars* kdev;
 };
 

@@ -121,7 +121,6 @@ __global__ void k_pd_scalars(const PdState* st, PdStep p, FactoredDevScalars* kd
     v.lr_eff = (float)((double)df * (double)p.lr);
     v.nwdlr = (float)(-(double)p.wd * (double)v.lr_eff);
     v.unum = df;
-    v.lr_u = (float)((double)v.lr_eff * (double)df);
     *kdev = v;
 }
 

@@ -7,8 +7,10 @@ Tolerances, derived from that:
   R, C states      : 1e-6 relative  (sums of positive terms: a tree of n terms rounds at most
                      ceil(log2 n) times per term, 14 * 2^-24 = 8.3e-7 for 10240 columns, plus the
                      EMA's two roundings; the cases here reach 2.4e-7)
-  fp32 masters     : |w - w_ref| <= 1e-6 |w_ref| + 1e-6 * lr * steps  (the update is ~lr per step;
-                     a 1e-6-relative difference in it, plus one rounding of w)
+  fp32 masters     : |w - w_ref| <= 1e-6 |w_ref| + 1e-6 (lr d steps + sum_k |update_k|)  (the
+                     kernels' update is within a few ulps of the oracle's -- the statistics above,
+                     and the per-tensor scale fl(u fl(lr/den)) for fl(fl(u/den) lr) -- and single
+                     elements' updates reach several times lr d; plus one rounding of w)
 """
 import numpy as np
 import pytest
@@ -58,7 +60,7 @@ class OracleFactored:
         return self.orc.kahan_merge(t["hi"], t["lo"]).astype(np.float64) if t["lo"] is not None else None
 
 
-def compare(ora, grp, hp, steps, kahan=True, upd_tol=1e-6, moved_tol=0.0):
+def compare(ora, grp, hp, steps, kahan=True, upd_tol=1e-6):
     masters = grp.masters() if kahan else None
     for i, ot in enumerate(ora.t):
         if ot["hi"].size == 0:
@@ -66,7 +68,7 @@ def compare(ora, grp, hp, steps, kahan=True, upd_tol=1e-6, moved_tol=0.0):
         if kahan:
             ref = ora.orc.kahan_merge(ot["hi"], ot["lo"]).astype(np.float64)
             got = masters[i].cpu().numpy().reshape(-1).astype(np.float64)
-            tol = 1e-6 * np.abs(ref) + upd_tol * hp["lr"] * hp.get("d", 1.0) * steps + moved_tol * ot.get("moved", 0.0)
+            tol = 1e-6 * np.abs(ref) + upd_tol * (hp["lr"] * hp.get("d", 1.0) * steps + ot.get("moved", 0.0))
             bad = np.abs(got - ref) > tol
             assert not bad.any(), f"tensor {i} {ot['shape']}: {bad.sum()} masters out of tolerance, " \
                                   f"max excess {np.max(np.abs(got - ref) - tol):.3e}"
@@ -87,8 +89,7 @@ def compare(ora, grp, hp, steps, kahan=True, upd_tol=1e-6, moved_tol=0.0):
             assert np.all(np.abs(gv - r) <= 1e-6 * np.abs(r) + 1e-37), f"tensor {i}: V state differs"
 
 
-def run_parity(orc, eng, shapes, steps, hp, seed=0, g_std=1e-3, kahan=True, scale_rows=False, upd_tol=1e-6,
-               moved_tol=0.0):
+def run_parity(orc, eng, shapes, steps, hp, seed=0, g_std=1e-3, kahan=True, scale_rows=False, upd_tol=1e-6):
     masters = [W.master_weights(s, seed, i) for i, s in enumerate(shapes)]
     ora = OracleFactored(orc, [m.numpy() for m in masters], shapes, kahan=kahan)
     if kahan:
@@ -105,7 +106,7 @@ def run_parity(orc, eng, shapes, steps, hp, seed=0, g_std=1e-3, kahan=True, scal
         ora.step([W.bits16(g).reshape(-1) for g in grads], hp)
         grp.step([g.cuda() for g in grads], hp)
     torch.cuda.synchronize()
-    compare(ora, grp, hp, steps, kahan=kahan, upd_tol=upd_tol, moved_tol=moved_tol)
+    compare(ora, grp, hp, steps, kahan=kahan, upd_tol=upd_tol)
     from memory_lean_optimizer_gb300 import lmopt
     assert lmopt.optim_query_nonfinite(grp.handle) == 0
     return ora, grp
@@ -125,13 +126,12 @@ def test_mixed_shapes(orc, eng, mode):
 
 def test_prodigy_mode_fixed_d(orc, eng):
     """Prodigy mode with a fixed d != 1: the update's numerator d g and the step size d lr on every
-    tensor class (wide, batched, 3x3, small, 1-D), clipped and unclipped.  With d != 1 the kernels
-    carry d through fl(lr d) d and the clip divisor, the oracle through fl(u d): up to four more
-    roundings of each update (2.4e-7 of it), and single elements' updates reach many times lr d,
-    so the allowance adds 1e-6 (16 roundings) of each element's summed |update| over the steps."""
+    tensor class (wide, batched, 3x3, small, 1-D), clipped and unclipped.  The kernels multiply
+    each element's update by d before its square is summed and before the clip, as the oracle
+    does, so the tolerance is the one of Adafactor mode."""
     hp = dict(HP, mode=1, beta2=0.99, d=0.37, weight_decay=0.02)
-    run_parity(orc, eng, SHAPES, 3, hp, seed=8, scale_rows=True, moved_tol=1e-6)
-    run_parity(orc, eng, SHAPES[:6], 2, dict(hp, clip_threshold=1e3), seed=9, moved_tol=1e-6)
+    run_parity(orc, eng, SHAPES, 3, hp, seed=8, scale_rows=True)
+    run_parity(orc, eng, SHAPES[:6], 2, dict(hp, clip_threshold=1e3), seed=9)
 
 
 def test_weight_decay_and_clip_threshold(orc, eng):
