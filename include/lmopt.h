@@ -216,11 +216,10 @@ int optim_step_factored(optim_group_t* group, const void* const* grads_bf16, int
  * counter (>= 1; no sequence check).  A tensor whose scratch would exceed the array (about 3/64
  * byte per element of a matrix: some 7e8 elements) is rejected with OPTIM_EINVAL and a message
  * giving both sizes.
- * The first call on a device looks up the array's device address (once per device); make that
- * first call outside any stream capture.  All calls share the array and it keeps the previous
- * call's contents (the call clears the parts that must start at zero), so calls whose work
- * overlaps on the GPU -- different streams without ordering, or several host threads -- race:
- * order them on one stream.  Calls no cudaMalloc, cudaFree or other allocating routine. */
+ * The first call on a device looks up the array's device address (once per device).  All calls
+ * share the array and it keeps the previous call's contents (the call clears the parts that must
+ * start at zero), so calls whose work overlaps on the GPU -- different streams without ordering,
+ * or several host threads -- race: order them on one stream.  Calls no cudaMalloc, cudaFree or other allocating routine. */
 int optim_step_factored_noalloc(const optim_tensor_desc_t* tensor, const void* grad_bf16, int64_t step,
                                 const optim_factored_hparams_t* hp, void* stream);
 
