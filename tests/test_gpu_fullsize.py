@@ -1,11 +1,12 @@
 """Parity at full workload sizes, in the launch configuration the benchmark times (one library
 group per Flux-like block, the ten SDXL-like factored groups, one group of 20,000 ragged tensors, the
 35-group host-offload pipeline), each for its configuration's own number of steps (5, and 3 for the
-offload pipeline).  Every tensor of every workload is replayed by the oracle: flux19 and ragged20k
-after step 1 and after their last step, sdxl_like and flux35 after their last step.  The oracle
-replays tensor by tensor on a thread pool (one single-threaded oracle call per tensor), each
-tensor's inputs regenerated from their seeds on the device and copied back, so host memory stays
-bounded by the tensors in flight."""
+offload pipeline), and the NEXT rows (f24 moments, stochastic rounding, Adan with fp32 and f24
+states) on the flux19 workload for its 5 steps.  Every tensor of every workload is replayed by
+the oracle: flux19 and ragged20k after step 1 and after their last step, the others after their
+last step.  The oracle replays tensor by tensor on a thread pool (one single-threaded oracle call
+per tensor), each tensor's inputs regenerated from their seeds on the device and copied back, so
+host memory stays bounded by the tensors in flight."""
 import os
 from collections import deque
 from concurrent.futures import ThreadPoolExecutor
@@ -286,4 +287,111 @@ def test_tensor_beyond_2_31_elements(orc, eng):
             assert got[name][j] == want[0], f"element {idx[j]}: {name} {got[name][j]} != {want[0]}"
     grp.close()
     del g, grp
+    torch.cuda.empty_cache()
+
+
+ADAN_HP = dict(lr=3.3e-5, beta1=0.02, beta2=0.08, beta3=0.01, eps=1e-8, weight_decay=0.02)
+SR_SEED = 12345
+NEXT_STEPS = 5          # the flux19 configuration's step count
+
+
+def _replay_next(orc, variant, x, grads, hp, got, tensor, scale, tag):
+    """One tensor's trajectory under a NEXT-row variant, bit for bit against the GPU's bytes."""
+    n = x.size
+    if variant == "sr":
+        o = dict(hi=orc.round_bf16(x), lo=None)
+    else:
+        hi, lo = orc.kahan_split(x)
+        o = dict(hi=hi, lo=lo)
+    if variant in ("f24", "sr"):
+        small = n <= 4096
+        if small:
+            o["m"], o["v"] = np.zeros(n, np.float32), np.zeros(n, np.float32)
+        elif variant == "f24":
+            o["m"], o["v"] = np.zeros(orc.f24_nbytes(n), np.uint8), np.zeros(orc.f24_nbytes(n), np.uint8)
+        else:
+            o["m"], o["v"] = np.full(n, 32768, np.uint16), np.zeros(n, np.uint16)
+        sc, mp = orc.Scale(), 1.0
+        for t, g in enumerate(grads, start=1):
+            k, mp = orc.nadam_scalars(t, hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"],
+                                      hp["wd_mode"] == 1, hp["nesterov"], hp["momentum_decay"], mp)
+            if variant == "f24":
+                orc.nadam_step_tensor_f24(o["hi"], o["lo"], o["m"], o["v"], g, k)
+            else:
+                orc.nadam_step_tensor_sr(o["hi"], o["m"], o["v"], g, sc, k, SR_SEED, tensor, t)
+        keys = ("hi", "m", "v") if variant == "sr" else ("hi", "lo", "m", "v")
+        if variant == "sr" and n > 4096:
+            assert np.array_equal(np.float32(scale), np.float32((sc.s_m, sc.s_v, sc.a_m, sc.a_v))), f"{tag}: scale record"
+    else:
+        k = orc.adan_scalars(hp["lr"], hp["beta1"], hp["beta2"], hp["beta3"], hp["eps"], hp["weight_decay"])
+        o["mnv"] = (np.zeros(orc.adan_f24_nbytes(n), np.uint8) if variant == "adan_f24"
+                    else np.zeros(3 * orc.adan_plane(n), np.float32))
+        o["gp"] = np.zeros(n, np.uint16)
+        step = orc.adan_step_tensor_f24 if variant == "adan_f24" else orc.adan_step_tensor
+        for t, g in enumerate(grads, start=1):
+            step(o["hi"], o["lo"], o["mnv"], o["gp"], g, t, k)
+        keys = ("hi", "lo", "mnv", "gp")
+    for key in keys:
+        want = np.ascontiguousarray(o[key]).view(np.uint8)
+        have = np.ascontiguousarray(got[key]).view(np.uint8)
+        if not np.array_equal(have, want):
+            bad = np.flatnonzero(have != want)
+            raise AssertionError(f"{tag}: {key} differs in {bad.size} bytes, first {bad[:5]}")
+
+
+def _bytes(t):
+    return t.detach().contiguous().cpu().view(torch.uint8).numpy().reshape(-1)
+
+
+@pytest.mark.parametrize("variant", ["f24", "sr", "adan", "adan_f24"])
+def test_flux19_next_rows_full(orc, eng, variant):
+    """The NEXT rows at the headline workload's size, in the benchmark's launch configuration (one
+    group per Flux-like block, 19 groups, 3,227,516,928 params), 5 steps: NAdamW with f24
+    moments; u16 moments with stochastic rounding instead of the residual; Adan with fp32 states;
+    Adan with f24 states.  Every tensor's weights, residuals and every stored state byte equal the
+    oracle's replay of that tensor."""
+    from memory_lean_optimizer_gb300 import lmopt
+    cfg = W.config("flux19")
+    nadam = variant in ("f24", "sr")
+    hp = dict(cfg["hp"], stochastic_rounding=int(variant == "sr"), seed=SR_SEED) if nadam else dict(ADAN_HP)
+    groups, tids, tid = [], [], 0
+    for shapes in cfg["groups"]:
+        ids = list(range(tid, tid + len(shapes)))
+        masters = [W.master_weights(s, cfg["seed"], j, device="cuda") for s, j in zip(shapes, ids)]
+        if variant == "f24":
+            groups.append(eng.NadamGroup.from_masters(masters, states="f24"))
+        elif variant == "sr":
+            groups.append(eng.NadamGroup([x.to(torch.bfloat16) for x in masters], kahan=False))
+        else:
+            groups.append(eng.AdanGroup.from_masters(masters, states="f24" if variant == "adan_f24" else "fp32"))
+        del masters
+        tids.append(ids)
+        tid += len(shapes)
+    for t in range(1, NEXT_STEPS + 1):
+        for grp, shapes, ids in zip(groups, cfg["groups"], tids):
+            grads = [W.grad_bf16(s, cfg["seed"], j, t, cfg["g_std"], device="cuda") for s, j in zip(shapes, ids)]
+            grp.step(grads, hp)
+            del grads
+    torch.cuda.synchronize()
+    rp = Replays()
+    for b, (grp, shapes) in enumerate(zip(groups, cfg["groups"])):
+        scales = lmopt.optim_query_scales(grp.handle, len(shapes)) if variant == "sr" else [None] * len(shapes)
+        for i, s in enumerate(shapes):
+            j = tids[b][i]
+            x = _f32(W.master_weights(s, cfg["seed"], j, device="cuda"))
+            gs = [_bits(W.grad_bf16(s, cfg["seed"], j, t, cfg["g_std"], device="cuda")) for t in range(1, NEXT_STEPS + 1)]
+            got = dict(hi=_bytes(grp.weights[i]))
+            if variant != "sr":
+                got["lo"] = _bytes(grp.res[i])
+            if nadam:
+                got["m"], got["v"] = _bytes(grp.m[i]), _bytes(grp.v[i])
+            else:
+                got["mnv"], got["gp"] = _bytes(grp.mvn[i]), _bytes(grp.gprev[i])
+            rp.submit(_replay_next, orc, variant, x, gs, hp, got, i, scales[i],
+                      f"flux19 {variant} step {NEXT_STEPS} group {b} tensor {i} {tuple(s)}")
+        assert lmopt.optim_query_nonfinite(grp.handle) == 0
+    assert rp.finish() == tid
+    for grp in groups:
+        grp.close()
+    del groups
     torch.cuda.empty_cache()
