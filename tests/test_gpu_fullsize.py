@@ -395,3 +395,66 @@ def test_flux19_next_rows_full(orc, eng, variant):
         grp.close()
     del groups
     torch.cuda.empty_cache()
+
+
+def test_sdxl_like_prodigy_full(orc, eng):
+    """NEXT-4 at full size, in the benchmark's Prodigy configuration: the SDXL-like workload's ten
+    factored groups (2,602,705,920 params) attached to one controller (d0 1e-6, lr 1, beta2
+    0.999, statistics on every 11th 64-element block, one gradient set reused), 5 steps.  The oracle steps every tensor
+    (statistics before the update, the update with the step's d; tensors in parallel, sums in
+    group and tensor order) and ends each step once; d after every step, every tensor's fp32
+    master, p0 and s are checked with the tolerances of test_gpu_prodigy.py."""
+    from test_gpu_prodigy import check, oracle_tensor
+    cfg = W.config("sdxl_like")
+    steps, slice_p, d0 = cfg["steps"], 11, 1e-6
+    hp = dict(cfg["hp"], mode=1, lr=1.0, beta2=0.999, eps2=1e-30)
+    ctrl = eng.ProdigyController(d0=d0, beta2=0.999, slice_p=slice_p)
+    st = orc.ProdigyState(d0, ctrl.beta3, slice_p)
+    groups, ora, tids, tid = [], [], [], 0
+    for shapes in cfg["groups"]:
+        ids = list(range(tid, tid + len(shapes)))
+        masters = [W.master_weights(s, cfg["seed"], j, device="cuda") for s, j in zip(shapes, ids)]
+        grp = eng.FactoredGroup.from_masters(masters)
+        grp.attach_prodigy(ctrl)
+        groups.append(grp)
+        ora.append([oracle_tensor(orc, _f32(m), s, slice_p) for m, s in zip(masters, shapes)])
+        del masters
+        tids.append(ids)
+        tid += len(shapes)
+
+    def ora_tensor_step(tt, g, t, cs, d):
+        dt, lt = orc.prodigy_tensor_stats(tt["hi"], tt["lo"], g, slice_p, tt["p0"], tt["s"], st.beta3, cs)
+        orc.factored_group_step([tt], [g], t, dict(hp, d=d))
+        return dt, lt
+
+    ds, ds_ref, lrd = [], [], 0.0
+    pool = ThreadPoolExecutor(max_workers=os.cpu_count() or 4)
+    for t in range(1, steps + 1):
+        d = st.d32
+        lrd += hp["lr"] * d
+        cdot, l1 = 0.0, 0.0
+        for grp, shapes, ids, og in zip(groups, cfg["groups"], tids, ora):
+            # one gradient set reused every step, as the benchmark does: the displacement then
+            # correlates with the gradients and d grows
+            grads = [W.grad_bf16(s, cfg["seed"], j, 1, cfg["g_std"], device="cuda") for s, j in zip(shapes, ids)]
+            cr = float(np.float32(hp["lr"])) * d * d
+            cs = float(np.float32(cr))
+            futs = [pool.submit(ora_tensor_step, tt, _bits(g), t, cs, d) for tt, g in zip(og, grads)]
+            grp.step(grads, hp)
+            del grads
+            dot_g = 0.0
+            for f in futs:
+                dt, lt = f.result()
+                dot_g += dt
+                l1 += lt
+            cdot += cr * dot_g
+        st.end_step(cdot, l1)
+        ctrl.end_step()
+        ds.append(ctrl.get()[0])
+        ds_ref.append(st.d.value)
+    pool.shutdown()
+    torch.cuda.synchronize()
+    assert ds_ref[-1] > d0                      # d moved during the run
+    check(orc, ora, groups, ds, ds_ref, lrd)
+    ctrl.close()
+    torch.cuda.empty_cache()
