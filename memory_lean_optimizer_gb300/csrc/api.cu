@@ -250,16 +250,18 @@ int optim_group_create(const optim_tensor_desc_t* tensors, int32_t n, int32_t ki
             r.pad = 0;
         }
         if (kind != OPTIM_KIND_FACTORED) {
-            // a group whose kChunk-element chunks would not give every SM a CTA is cut finer
-            // (down to kChunkMin): the launch-bound small case then spreads over the whole GPU
-            // (one CTA per SM measured faster than two: fewer, longer CTAs share the per-CTA
-            // prologue and the instruction fetch of the short launch)
+            // a group whose kChunk-element chunks would not give every SM a CTA (two for the
+            // kinds without the one-launch step) is cut finer, down to kChunkMin: the small case
+            // then spreads over the whole GPU (for the one-launch step one CTA per SM measured
+            // faster than two: fewer, longer CTAs share the per-CTA prologue and the instruction
+            // fetch of the short launch)
             auto count = [&](int64_t ch) {
                 int64_t c = 0;
                 for (int32_t i = 0; i < n; ++i) c += (tensors[i].numel + ch - 1) / ch;
                 return c;
             };
-            while (g->chunk > kChunkMin && count(g->chunk) < (int64_t)sm_count()) g->chunk /= 2;
+            const int64_t per_sm = kind == OPTIM_KIND_NADAM ? 1 : 2;
+            while (g->chunk > kChunkMin && count(g->chunk) < per_sm * (int64_t)sm_count()) g->chunk /= 2;
             for (int pass = 0; pass < 2; ++pass) {   // u16-state tensors first, then fp32-state
                 for (int32_t i = 0; i < n; ++i) {
                     const int64_t ne = tensors[i].numel;
