@@ -46,3 +46,21 @@ def test_byte_counts_and_traffic_record():
         else:
             assert t is None
     assert bench.traffic_per_launch("no_such_kernel", 1000) is None
+
+
+def test_reference_arm_under_torchrun_two_ranks():
+    """Launched as the multi-GPU bench is (torchrun, two ranks): rank 0 alone runs the oracle and
+    prints one line, the other rank exits 0 without work."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl", "reference",
+           "--gpus", "2", "--steps", "1", "--warmup", "1", "--workload", "nadam_1m"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["config"]["workload"] == "nadam_1m"
