@@ -134,3 +134,41 @@ def test_adan_empty_tensors(orc):
     for i, o in enumerate(ora):
         if sizes[i]:
             assert np.array_equal(cuda_bits(grp.weights[i]), o["hi"]) and np.array_equal(cuda_bits(grp.res[i]), o["lo"])
+
+
+@pytest.mark.parametrize("states", ["fp32", "f24"])
+def test_adan_degenerate_inputs_bit_exact(orc, states):
+    """Degenerate gradients against the oracle, every byte after each of 5 steps: all zeros for two
+    steps then normal, bf16 subnormals (squares underflow), magnitudes near 1e18 (c c near the
+    fp32 limit), two scales 27 decades apart in one tensor, a sign flip every step (large
+    differences d = g - g_prev); fp32-plane (<= 4096) and f24 tensors."""
+    from test_gpu_nadam import _degenerate_grad
+    from memory_lean_optimizer_gb300 import build, engine
+    build.build()
+    kinds = ["zero_then_normal", "subnormal", "large", "two_scales", "sign_flip"]
+    sizes = [3001, 20001]
+    seed = 97
+    shapes = [n for n in sizes for _ in kinds]
+    tkinds = [k for _ in sizes for k in kinds]
+    masters = [W.master_weights((n,), seed, i) for i, n in enumerate(shapes)]
+    grp = engine.AdanGroup.from_masters([m.cuda() for m in masters], states=states)
+    ora = [dict(zip(("hi", "lo"), orc.kahan_split(m.numpy()))) for m in masters]
+    for o, n in zip(ora, shapes):
+        o["mnv"] = _ora_state(orc, n, states)
+        o["gp"] = np.zeros(n, np.uint16)
+    k = orc.adan_scalars(HP["lr"], HP["beta1"], HP["beta2"], HP["beta3"], HP["eps"], HP["weight_decay"])
+    for t in range(1, 6):
+        grads = [_degenerate_grad(kd, n, t, seed + i) for i, (kd, n) in enumerate(zip(tkinds, shapes))]
+        for o, g in zip(ora, grads):
+            _ora_step(orc, states, o, W.bits16(g), t, k)
+        grp.step([g.cuda() for g in grads], HP)
+        torch.cuda.synchronize()
+        for i, o in enumerate(ora):
+            tag = (t, i, tkinds[i], shapes[i])
+            assert np.array_equal(cuda_bits(grp.weights[i]), o["hi"]), tag
+            assert np.array_equal(cuda_bits(grp.res[i]), o["lo"]), tag
+            assert np.array_equal(_state_bytes(grp.mvn[i]), o["mnv"].view(np.uint8)), tag
+            assert np.array_equal(cuda_bits(grp.gprev[i]), o["gp"]), tag
+    from memory_lean_optimizer_gb300 import lmopt
+    assert lmopt.optim_query_nonfinite(grp.handle) == 0
+    grp.close()

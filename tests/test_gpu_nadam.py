@@ -65,7 +65,7 @@ def test_empty_tensors_in_a_group(orc, eng, states):
 
 def test_one_1024x1024_ten_steps(orc, eng):
     """The 1024x1024 single-tensor workload, NAdam, lr 3.5e-6, 10 steps, seed 0 (one launch per
-    step: its 512 chunks fit on the GPU at once)."""
+    step: its chunks fit on the GPU at once)."""
     _, grp = run_parity(orc, eng, [(1024, 1024)], 10, HP, g_std=1e-3)
     assert grp.launches(HP) == 1
 
@@ -368,3 +368,61 @@ def test_stochastic_rounding_bit_exact(orc, eng, states):
         torch.cuda.synchronize()
         for i, o in enumerate(ora):
             assert np.array_equal(cuda_bits(grp.weights[i]), o["hi"]), (t, i)
+
+
+def _degenerate_grad(kind, n, t, seed):
+    """bf16 gradients for the degenerate cases (torch CPU, seeded)."""
+    g = torch.Generator().manual_seed(1000 * seed + 10 * t + len(kind))
+    x = torch.randn(n, generator=g)
+    if kind == "zero_then_normal":          # exact zeros for two steps (zero scales), then normal
+        x = x * 1e-3 if t > 2 else torch.zeros(n)
+    elif kind == "subnormal":               # bf16 subnormals and zeros: squares underflow to 0
+        x = x * 1e-39
+        x[::3] = 0.0
+    elif kind == "large":                   # |g| near 1e18: squares near 1e36, still finite
+        x = x * 1e18
+    elif kind == "two_scales":              # codes at both ends of the companding curve
+        x = x * 1e-3
+        x[: n // 2] *= 1e-27
+    elif kind == "sign_flip":               # the same magnitudes, alternating sign per step
+        x = x.abs() * 1e-3 * (1.0 if t % 2 else -1.0)
+    return x.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("variant", ["nadamw", "adam_beta1_0", "lr_0"])
+def test_degenerate_inputs_bit_exact(orc, eng, variant):
+    """Degenerate inputs against the oracle, bit for bit after every step: all-zero gradients (the
+    codec scales start at zero and stay there), bf16 subnormal gradients (squares underflow to
+    zero; no flush to zero on either side), gradients near 1e18 (squares near the fp32 limit),
+    two magnitude scales 27 decades apart in one tensor (codes at both ends of the curve), sign
+    flips every step; u16 (> 4096 elements) and fp32 (<= 4096) tensors, ragged sizes.  Variants:
+    NAdamW, Adam with beta1 = 0, and lr = 0 with decoupled decay (the weights stay bit for bit)."""
+    kinds = ["zero_then_normal", "subnormal", "large", "two_scales", "sign_flip"]
+    sizes = [20001, 3001, 16384, 70007, 4096]
+    hp = dict(HP, lr=1e-3, weight_decay=0.01, wd_mode=1)
+    if variant == "adam_beta1_0":
+        hp = dict(hp, beta1=0.0, nesterov=0, weight_decay=0.0, wd_mode=0)
+    elif variant == "lr_0":
+        hp = dict(hp, lr=0.0)
+    seed = 91
+    shapes = [(n,) for n in sizes for _ in kinds]
+    tkinds = [k for _ in sizes for k in kinds]
+    masters = [W.master_weights(s, seed, i) for i, s in enumerate(shapes)]
+    ora = OracleNadam(orc, [m.numpy() for m in masters])
+    grp = eng.NadamGroup.from_masters([m.cuda() for m in masters])
+    for t in range(1, 6):
+        grads = [_degenerate_grad(k, s[0], t, seed + i) for i, (k, s) in enumerate(zip(tkinds, shapes))]
+        ora.step([W.bits16(g).reshape(-1) for g in grads], hp)
+        grp.step([g.cuda() for g in grads], hp)
+        torch.cuda.synchronize()
+        assert_nadam_equal(ora, grp, f"{variant} step {t}")
+        for i, (a, b) in enumerate(zip(grp.scales(), ora.scales())):
+            if W.numel(shapes[i]) > 4096:
+                assert np.array_equal(np.float32(a), np.float32(b)), (t, i, tkinds[i], a, b)
+    if variant == "lr_0":
+        for i, m in enumerate(masters):
+            hi, lo = orc.kahan_split(m.numpy().reshape(-1))
+            assert np.array_equal(cuda_bits(grp.weights[i]).reshape(-1), hi)
+    from memory_lean_optimizer_gb300 import lmopt
+    assert lmopt.optim_query_nonfinite(grp.handle) == 0
+    grp.close()
