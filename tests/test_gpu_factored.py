@@ -277,3 +277,37 @@ def test_zero_row_with_eps1_zero_is_nan_like_the_oracle(orc, eng):
     # the wide matrix's 1 tile and the small-matrix tensor's 1 block stored non-finite weights
     assert lmopt.optim_query_nonfinite(grp.handle) == 2
     grp.close()
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_degenerate_gradients(orc, eng, mode):
+    """Degenerate gradients on every tensor class, 5 steps, against the oracle with the tolerances
+    above: all zeros for two steps then normal (state EMAs of eps1 or eps2 alone), bf16
+    subnormals (squares underflow), magnitudes near 1e14 (sums of squares near 1e32; the kernels
+    sum in fp32, so magnitudes whose row or column sums pass the fp32 limit are out of their
+    range while the oracle's double sums are not), two scales 27 decades apart, sign flips."""
+    from test_gpu_nadam import _degenerate_grad
+    kinds = ["zero_then_normal", "subnormal", "large", "two_scales", "sign_flip"]
+    shapes = [(64, 80), (3, 40, 72), (8, 8, 3, 3), (300,), (1000, 640)]
+    cases = [(k, s) for k in kinds for s in shapes]
+    hp = dict(HP, mode=mode, weight_decay=0.01)
+    if mode == 1:
+        hp = dict(hp, beta2=0.99, d=0.37)
+    seed = 93
+    masters = [W.master_weights(s, seed, i) for i, (_, s) in enumerate(cases)]
+    ora = OracleFactored(orc, [m.numpy() for m in masters], [s for _, s in cases])
+    grp = eng.FactoredGroup.from_masters([m.cuda() for m in masters])
+    for t in range(1, 6):
+        grads = []
+        for i, (k, s) in enumerate(cases):
+            g = _degenerate_grad(k, W.numel(s), t, seed + i)
+            if k == "large":
+                g = (g.float() * 1e-4).to(torch.bfloat16)     # near 1e14
+            grads.append(g.reshape(s))
+        ora.step([W.bits16(g).reshape(-1) for g in grads], hp)
+        grp.step([g.cuda() for g in grads], hp)
+    torch.cuda.synchronize()
+    compare(ora, grp, hp, 5)
+    from memory_lean_optimizer_gb300 import lmopt
+    assert lmopt.optim_query_nonfinite(grp.handle) == 0
+    grp.close()
