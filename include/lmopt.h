@@ -142,7 +142,10 @@ typedef struct {
 /* Registers `n` tensors as one group (n >= 1) and allocates the group's device tables
  * (tensor table, chunk table, per-tensor scale records).  Synchronises (one upload).
  * All scale records start at zero; the u16 m codes must start at 32768 and v codes at 0 (the
- * zero point), fp32 moments and factored states at 0. */
+ * zero point), fp32 moments and factored states at 0.  With the environment variable
+ * LMOPT_VERBOSE=1 each created group prints one line to stderr (tensors, elements, state kind,
+ * how many tensors keep a Kahan residual, the chunking), as the Kahan change of "Kahan summation
+ * for Adafactor-optimized Flux FFT" reports on the console that it is active. */
 int optim_group_create(const optim_tensor_desc_t* tensors, int32_t n, int32_t kind,
                        optim_group_t** out);
 int optim_group_destroy(optim_group_t* group);

@@ -298,6 +298,21 @@ int optim_group_create(const optim_tensor_desc_t* tensors, int32_t n, int32_t ki
         return rc;
     }
     *out = g;
+    if (const char* vb = std::getenv("LMOPT_VERBOSE"); vb && std::strcmp(vb, "1") == 0) {
+        // one line per group: what was switched on (the Kahan residual, the moment storage)
+        int64_t numel = 0, res = 0;
+        for (int32_t i = 0; i < n; ++i) {
+            numel += tensors[i].numel;
+            res += tensors[i].res_u16 != nullptr && tensors[i].numel > 0;
+        }
+        static const char* const names[] = {"nadam u16", "factored", "nadam f24", "adan fp32", "adan f24"};
+        std::fprintf(stderr, "lmopt: group of %d tensors, %lld elements, %s states, Kahan residual on %lld "
+                     "tensors, device %d", n, (long long)numel, names[kind], (long long)res, g->device);
+        if (kind != OPTIM_KIND_FACTORED)
+            std::fprintf(stderr, ", %d chunks of %lld elements (%d u16-state)", g->n_chunks_total,
+                         (long long)g->chunk, g->n_chunks_large);
+        std::fprintf(stderr, "\n");
+    }
     return OPTIM_OK;
 }
 

@@ -426,3 +426,17 @@ def test_degenerate_inputs_bit_exact(orc, eng, variant):
     from memory_lean_optimizer_gb300 import lmopt
     assert lmopt.optim_query_nonfinite(grp.handle) == 0
     grp.close()
+
+
+def test_verbose_banner(eng, capfd, monkeypatch):
+    """LMOPT_VERBOSE=1: one stderr line per created group saying what is on; silent otherwise."""
+    masters = [W.master_weights((n,), 5, i, device="cuda") for i, n in enumerate([5000, 300])]
+    monkeypatch.setenv("LMOPT_VERBOSE", "1")
+    grp = eng.NadamGroup.from_masters(masters)
+    err = capfd.readouterr().err
+    assert "lmopt: group of 2 tensors, 5300 elements, nadam u16 states, Kahan residual on 2 tensors" in err
+    grp.close()
+    monkeypatch.delenv("LMOPT_VERBOSE")
+    grp = eng.NadamGroup.from_masters(masters)
+    assert "lmopt:" not in capfd.readouterr().err
+    grp.close()
