@@ -162,7 +162,7 @@ int optim_group_destroy(optim_group_t* group);
  *                create (may change from call to call; unchanged pointers cost no upload)
  *   step       : 1 on the first call, then previous + 1; anything else is OPTIM_EINVAL
  * Two enqueued kernels (one if every tensor has 4096 or fewer elements, or if the group is small
- * enough for all of its 2048..16384-element chunks to run on the GPU at once: the pre-pass, a
+ * enough for all of its 2048..32768-element chunks to run on the GPU at once: the pre-pass, a
  * grid-wide barrier and the update then form one cooperative launch, with the same results).
  * The barrier's wait is bounded (about a second); should it run out, the chunk is counted by
  * optim_query_nonfinite and the step's results are not to be trusted. */
@@ -312,7 +312,7 @@ int optim_set_scales(optim_group_t* group, const float* host_in);
 int optim_group_get_step(optim_group_t* group, int64_t* step, double* mu_product);
 int optim_group_set_step(optim_group_t* group, int64_t step, double mu_product);
 /* Non-finite detection: the number of (step, chunk) pairs in which an updated weight came out
- * NaN or infinite, summed over all steps so far (a chunk is up to 16384 elements of one tensor;
+ * NaN or infinite, summed over all steps so far (a chunk is up to 32768 elements of one tensor;
  * in FACTORED groups, one unit of the update kernel: a 128x256 tile, up to 2048 small matrices,
  * or up to 2048 elements of a 1-D tensor). */
 int optim_query_nonfinite(optim_group_t* group, uint64_t* count);

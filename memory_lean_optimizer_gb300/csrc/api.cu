@@ -250,7 +250,8 @@ int optim_group_create(const optim_tensor_desc_t* tensors, int32_t n, int32_t ki
             r.pad = 0;
         }
         if (kind != OPTIM_KIND_FACTORED) {
-            // a group whose kChunk-element chunks would not give every SM a CTA (two for the
+            // chunks of kChunkU16 elements for NAdam u16 groups, kChunk for f24 and Adan groups;
+            // a group whose chunks would not give every SM a CTA (two for the
             // kinds without the one-launch step) is cut finer, down to kChunkMin: the small case
             // then spreads over the whole GPU (for the one-launch step one CTA per SM measured
             // faster than two: fewer, longer CTAs share the per-CTA prologue and the instruction
@@ -261,6 +262,7 @@ int optim_group_create(const optim_tensor_desc_t* tensors, int32_t n, int32_t ki
                 return c;
             };
             const int64_t per_sm = kind == OPTIM_KIND_NADAM ? 1 : 2;
+            g->chunk = kind == OPTIM_KIND_NADAM ? kChunkU16 : kChunk;
             while (g->chunk > kChunkMin && count(g->chunk) < per_sm * (int64_t)sm_count()) g->chunk /= 2;
             for (int pass = 0; pass < 2; ++pass) {   // u16-state tensors first, then fp32-state
                 for (int32_t i = 0; i < n; ++i) {

@@ -16,7 +16,10 @@
 namespace lmo {
 
 constexpr int kThreads = 256;          // threads per CTA of the streaming kernels
-constexpr int64_t kChunk = 16384;      // elements per CTA (u16-state tensors); multiple of 8
+constexpr int64_t kChunk = 16384;      // elements per CTA of the f24 and Adan kernels; multiple of 8
+constexpr int64_t kChunkU16 = 32768;   // elements per CTA of NAdam u16 groups (pre-pass + update):
+                                       // the update's per-chunk prologue (chunk, tensor and scale
+                                       // records, codec constants) is shared by twice the elements
 constexpr int64_t kChunkMin = 2048;    // smallest chunk a small group is cut into
 constexpr int64_t kSmall = OPTIM_SMALL_NUMEL;
 
@@ -51,7 +54,8 @@ struct ScaleRec {
 static_assert(sizeof(ScaleRec) == 64, "ScaleRec layout");
 
 // One CTA's work item: elements [index*chunk, min(numel, (index+1)*chunk)) of a tensor, chunk the
-// group's chunk size (kChunk, or a smaller power of two for groups too small to fill the GPU).
+// group's chunk size (kChunkU16 or kChunk by kind, or a smaller power of two for groups too small
+// to fill the GPU).
 struct Chunk {
     int32_t tensor;
     int32_t index;

@@ -28,7 +28,7 @@ struct optim_group {
     uint8_t* d_zero_chunk = nullptr;   // one flag per u16-state chunk, written by the pre-pass
     int32_t n_chunks_large = 0;
     int32_t n_chunks_total = 0;
-    int64_t chunk = lmo::kChunk;       // elements per chunk of this group
+    int64_t chunk = lmo::kChunk;       // elements per chunk of this group (set by kind at creation)
     lmo::FactoredPlan* fplan = nullptr;
     // gradient pointers: host copy of the last upload, two pinned staging slots
     std::vector<const void*> cur_grads;

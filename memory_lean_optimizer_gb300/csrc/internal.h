@@ -53,7 +53,7 @@ struct NadamLaunch {
     int32_t f24;              // moments stored as f24 planes instead of u16 codes
     uint8_t* zero_chunk;      // per u16 chunk: the gradient pre-pass saw an exact zero (K2 then
                               // takes the zero-guarded arithmetic for that chunk)
-    int64_t chunk;            // elements per chunk (a power of two, kChunkMin..kChunk)
+    int64_t chunk;            // elements per chunk (a power of two, kChunkMin..kChunkU16)
 };
 // K1 (gradient maxima; nothing for f24 moments), then K2 (the update; `mid`, if not null, is
 // recorded on the stream before it).  A step is both, in this order, on one stream.

@@ -51,7 +51,7 @@ __device__ __forceinline__ uint32_t sr_lane1(const Prm& k, uint32_t tensor, int6
 // loads of a chunk at once, and no CTA is launched per chunk, which matters for groups of many
 // small tensors (hundreds of thousands of chunks).
 constexpr int kK1Warps = kThreads / 32;
-constexpr int kK1CtasPerSm = 8;   // 256-thread CTAs resident per SM (<= 32 registers per thread)
+constexpr int kK1CtasPerSm = 4;   // 256-thread CTAs resident per SM (<= 64 registers per thread)
 
 // One chunk of the pre-pass (every thread of the CTA).  red: 2 * kK1Warps words of shared memory.
 __device__ __forceinline__ void k1_chunk(const NadamLaunch& L, int parity, int64_t ci, uint32_t* red) {
@@ -82,14 +82,15 @@ __device__ __forceinline__ void k1_chunk(const NadamLaunch& L, int parity, int64
     };
     int64_t done = start;
     if (aligned16(g)) {
-        const int nv = (int)((end - start) >> 3);   // <= kChunk / 8 = 8 * kThreads vectors
+        const int nv = (int)((end - start) >> 3);   // <= kChunkU16 / 8 = 16 * kThreads vectors
         const uint4* gv = reinterpret_cast<const uint4*>(g + start);
-        if (nv == 8 * kThreads) {                    // a whole chunk: eight loads per thread in flight
-            uint4 x[8];
+        constexpr int kLoads = (int)(kChunkU16 / 8 / kThreads);
+        if (nv == kLoads * kThreads) {               // a whole chunk: all of a thread's loads in flight
+            uint4 x[kLoads];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) x[u] = __ldcg(gv + threadIdx.x + kThreads * u);
+            for (int u = 0; u < kLoads; ++u) x[u] = __ldcg(gv + threadIdx.x + kThreads * u);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) scan4(x[u]);
+            for (int u = 0; u < kLoads; ++u) scan4(x[u]);
         } else {
             for (int i = threadIdx.x; i < nv; i += kThreads) scan4(__ldcg(gv + i));
         }
@@ -250,7 +251,7 @@ template <bool kSR, bool kGuard>
 __device__ __forceinline__ void u16_vectors(const Prm& k, const Codec& cd, bool has_res, uint32_t tensor, int64_t start,
                                             int nv, uint4* wv, uint4* rv, const uint4* gv, uint4* mv, uint4* vv,
                                             float& am, float& av, uint32_t& nf) {
-    // nv <= chunk / 8 <= kChunk / 8: 32-bit vector indices within the chunk
+    // nv <= chunk / 8 <= kChunkU16 / 8: 32-bit vector indices within the chunk
     const bool sr = kSR && !has_res;
     // two independent 8-element groups per iteration, kThreads vectors apart: ten 128-bit
     // loads in flight (one generator call per group under stochastic rounding).
@@ -292,7 +293,7 @@ __device__ __forceinline__ void u16_vectors(const Prm& k, const Codec& cd, bool 
     }
 }
 
-// kFull: the group's chunk is kChunk (every group but small ones), known at compile time.
+// kFull: the group's chunk is kChunkU16 (every group but small ones), known at compile time.
 // One chunk of the update (every thread of the CTA).  red: 3 * 32 words of shared memory.
 template <bool kSR, bool kFull>
 __device__ __forceinline__ void k2_chunk(const NadamLaunch& L, const Prm& k, int parity, int64_t ci, uint32_t* red) {
@@ -302,7 +303,7 @@ __device__ __forceinline__ void k2_chunk(const NadamLaunch& L, const Prm& k, int
     const int p = parity, q = parity ^ 1;
     const bool small = (t.flags & kFlagSmall) != 0;
     const bool has_res = (t.flags & kFlagRes) != 0;
-    const int64_t chunk = kFull ? kChunk : L.chunk;
+    const int64_t chunk = kFull ? kChunkU16 : L.chunk;
     const int64_t start = (int64_t)c.index * chunk;
     const int64_t end = min(t.numel, start + chunk);
 
@@ -648,7 +649,7 @@ int launch_nadam_update(const NadamLaunch& L, const NadamScalars& s, cudaStream_
         else k_nadam_f24<false><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k);
         return check_cuda(cudaGetLastError(), "nadam f24 step launch");
     }
-    const bool full = L.chunk == kChunk;
+    const bool full = L.chunk == kChunkU16;
     if (k.sr) {
         if (full) k_nadam_step<true, true><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k, s.parity);
         else k_nadam_step<true, false><<<L.n_chunks_total, kThreads, 0, stream>>>(L, k, s.parity);

@@ -5,7 +5,7 @@ Each weight, residual, state buffer, gradient and host image of these tests sits
 and every gradient must be unchanged, so a write past either end of a buffer (a ragged head or
 tail, a vector access that runs over, a wrong stride) shows up here even without a memory checker.
 Sizes sit on both sides of the vector widths (8 elements), of the small-tensor limit (4096) and of
-the chunk sizes (2048..16384); buffers start either on a 16-byte boundary or at the smallest
+the chunk sizes (2048..32768); buffers start either on a 16-byte boundary or at the smallest
 offset each buffer accepts (2 bytes, 4 for fp32 states), which takes the element-by-element paths.
 The guarded group's results must also equal those of an ordinary group stepped alongside it.
 """
@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 
 GUARD = 512
 CANARY = 0xA5
-SIZES = [1, 2, 3, 7, 8, 9, 15, 16, 17, 4095, 4096, 4097, 8191, 16383, 16384, 16385, 65537]
+SIZES = [1, 2, 3, 7, 8, 9, 15, 16, 17, 4095, 4096, 4097, 8191, 16383, 16384, 16385, 32767, 32769, 65537]
 FACTORED_SHAPES = [(1,), (3,), (4097,), (1, 1), (3, 5), (17, 33), (64, 4097), (257, 129), (2, 3, 5, 7)]
 ADAN_HP = dict(lr=1e-3, beta1=0.02, beta2=0.08, beta3=0.01, eps=1e-8, weight_decay=0.02)
 FACTORED_HP = dict(lr=1e-3, beta2=0.999, decay_rate=-0.8, eps1=1e-30, eps2=1e-30, d=1.0, clip_threshold=1.0,

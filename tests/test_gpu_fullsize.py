@@ -252,7 +252,7 @@ def test_flux35_offload_full(orc, eng):
 
 
 def test_tensor_beyond_2_31_elements(orc, eng):
-    """One tensor of 2^31 + 13 elements (64-bit element offsets, 131,073 chunks), one NAdamW
+    """One tensor of 2^31 + 13 elements (64-bit element offsets, 65,537 chunks), one NAdamW
     step: sampled elements -- chunk edges, both sides of 2^31, the last one, random ones -- equal
     the oracle's step of the same element, given the tensor's max|g| computed on the host."""
     n = (1 << 31) + 13
@@ -260,7 +260,7 @@ def test_tensor_beyond_2_31_elements(orc, eng):
     master = W.master_weights((n,), 3, 0, device="cuda")
     grp = eng.NadamGroup.from_masters([master])
     rng = np.random.default_rng(0)
-    idx = np.unique(np.concatenate([[0, 1, 7, 8, 16383, 16384, (1 << 31) - 1, 1 << 31, (1 << 31) + 5, n - 1],
+    idx = np.unique(np.concatenate([[0, 1, 7, 8, 16383, 16384, 32767, 32768, (1 << 31) - 1, 1 << 31, (1 << 31) + 5, n - 1],
                                     rng.integers(0, n, 200)]))
     it = torch.from_numpy(idx).cuda()
     x = master[it].cpu().numpy()
