@@ -23,6 +23,11 @@
  *  - All arithmetic is IEEE fp32, each operation rounded once to nearest-even: the update's
  *    a*b+c steps are fused multiply-adds (one rounding), nothing else is contracted.  The
  *    results are deterministic run to run.
+ *  - Environment (read at each call): LMOPT_VERBOSE=1 prints one line per created group (see
+ *    optim_group_create); LMOPT_FAULT_INJECT=h2d|d2h|alloc makes the offload path fail with
+ *    OPTIM_ECUDA / OPTIM_ENOMEM before it enqueues anything, and =timeout makes every bounded
+ *    host wait return OPTIM_ETIMEOUT at once (host-side tests of the error paths; nothing on the
+ *    GPU is disturbed).
  */
 #ifndef LMOPT_H
 #define LMOPT_H
